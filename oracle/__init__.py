@@ -1,0 +1,207 @@
+"""CPU fp64 oracle for context-parallel zigzag causal attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  The product
+path (``context_causal_attention_zigzag_gb300``) never imports it.
+
+The arithmetic lives in ``cpattn_oracle.c`` (plain C, double precision) and,
+for tiny inputs, in the pure-Python ``brute`` module.  This file only moves
+numpy arrays across ctypes.  Sources for each function are given in the C
+file; in short:
+
+* attention definition and gradients -- "Context Parallelism for Long-Context
+  Training", section "Prove attention equivalence";
+* chunk placement (zigzag and contiguous), ring step source and per-step
+  partials -- "Sequence Parallelism IV: Megatron Context Parallel and
+  Load-Balanced Rings", sections 3-5.
+
+Arrays: q [B,S,H,D], k/v [B,S,Hkv,D] float32 (values exactly representable,
+e.g. bf16-rounded), natural token order.  Outputs are float64; LSE is
+[B,H,S] natural log.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+CONTIGUOUS = 0
+ZIGZAG = 1
+
+_libs = {}
+
+_f32p = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS")
+_f64p = np.ctypeslib.ndpointer(dtype=np.float64, flags="C_CONTIGUOUS")
+_i64p = np.ctypeslib.ndpointer(dtype=np.int64, flags="C_CONTIGUOUS")
+_u64p = np.ctypeslib.ndpointer(dtype=np.uint64, flags="C_CONTIGUOUS")
+_L, _I, _D = ctypes.c_long, ctypes.c_int, ctypes.c_double
+
+
+def _lib(mutation: int = 0):
+    if mutation in _libs:
+        return _libs[mutation]
+    lib = ctypes.CDLL(_build.build(mutation))
+    lib.oracle_set_threads.argtypes = [_I]
+    lib.oracle_get_threads.restype = _I
+    lib.oracle_shard_order.argtypes = [_L, _I, _I, _i64p]
+    lib.oracle_shard_order.restype = _I
+    shape = [_L, _I, _I, _L, _I, _I, _D]
+    lib.oracle_attn_fwd.argtypes = [_f32p, _f32p, _f32p] + shape + [_f64p, _f64p]
+    lib.oracle_attn_fwd_rows.argtypes = [_f32p, _f32p, _f32p] + shape + [_i64p, _L, _f64p, _f64p]
+    lib.oracle_lse_merge_arrays.argtypes = [_f64p, _f64p, _f64p, _f64p, _L, _L, _I, _I, _f64p, _f64p]
+    ring = [_L, _I, _I, _L, _I, _I, _I, _I, _D]
+    lib.oracle_ring_step.argtypes = [_f32p, _f32p, _f32p] + ring + [_I, _f64p, _f64p]
+    lib.oracle_ring_step.restype = _I
+    lib.oracle_ring_fwd.argtypes = [_f32p, _f32p, _f32p] + ring + [_I, _f64p, _f64p]
+    lib.oracle_ring_fwd.restype = _I
+    lib.oracle_attn_bwd.argtypes = [_f32p] * 4 + shape + [_f64p] * 3
+    lib.oracle_attn_bwd_dq_rows.argtypes = [_f32p] * 4 + shape + [_i64p, _L, _f64p]
+    lib.oracle_attn_bwd_dkdv_rows_sparse.argtypes = ([_f32p] * 4 + shape
+                                                     + [_i64p, _L, _i64p, _L, _f64p, _f64p])
+    lib.oracle_tile_counts.argtypes = [_L, _I, _I, _I, _L, _u64p, ctypes.c_void_p]
+    lib.oracle_tile_counts.restype = _I
+    _libs[mutation] = lib
+    return lib
+
+
+def set_threads(n: int, mutation: int = 0) -> None:
+    _lib(mutation).oracle_set_threads(int(n))
+
+
+def get_threads(mutation: int = 0) -> int:
+    return int(_lib(mutation).oracle_get_threads())
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _shape(q, k):
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    return B, S, H, Hkv, D
+
+
+def default_scale(D: int) -> float:
+    return 1.0 / float(np.sqrt(D))
+
+
+def shard_order(S: int, cp: int, layout: int, mutation: int = 0) -> np.ndarray:
+    """nat[p] = natural position of sharded position p."""
+    out = np.empty(S, dtype=np.int64)
+    if _lib(mutation).oracle_shard_order(S, cp, layout, out) != 0:
+        raise ValueError(f"S={S} does not split into chunks for cp={cp} layout={layout}")
+    return out
+
+
+def attn_fwd(q, k, v, causal=True, scale=None, mutation: int = 0):
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    _lib(mutation).oracle_attn_fwd(q, k, v, B, H, Hkv, S, D, int(causal), scale, out, lse)
+    return out, lse
+
+
+def attn_fwd_rows(q, k, v, rows, causal=True, scale=None, mutation: int = 0):
+    """rows: int array [n, 3] of natural (b, h, i).  Returns out [n, D], lse [n]."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.empty((n, D), np.float64)
+    lse = np.empty((n,), np.float64)
+    _lib(mutation).oracle_attn_fwd_rows(q, k, v, B, H, Hkv, S, D, int(causal), scale, rows, n,
+                                        out, lse)
+    return out, lse
+
+
+def lse_merge(o_a, l_a, o_b, l_b, mutation: int = 0):
+    """Exact merge of two normalised partials; O [B,S,H,D], LSE [B,H,S]."""
+    o_a, o_b = (np.ascontiguousarray(x, dtype=np.float64) for x in (o_a, o_b))
+    l_a, l_b = (np.ascontiguousarray(x, dtype=np.float64) for x in (l_a, l_b))
+    B, S, H, D = o_a.shape
+    o = np.empty_like(o_a)
+    lo = np.empty_like(l_a)
+    _lib(mutation).oracle_lse_merge_arrays(o_a, l_a, o_b, l_b, B, S, H, D, o, lo)
+    return o, lo
+
+
+def ring_step(q, k, v, cp, layout, t, causal=True, scale=None, mutation: int = 0):
+    """Partial (O_rt, L_rt) of ring step t for every rank, natural order."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    o = np.empty((B, S, H, D), np.float64)
+    l = np.empty((B, H, S), np.float64)
+    rc = _lib(mutation).oracle_ring_step(q, k, v, B, H, Hkv, S, D, cp, layout, int(causal), scale,
+                                         t, o, l)
+    if rc != 0:
+        raise ValueError("bad ring_step arguments")
+    return o, l
+
+
+def ring_fwd(q, k, v, cp, layout, causal=True, scale=None, merge_order=0, mutation: int = 0):
+    """Sequential ring with exact LSE merges; natural order out/lse."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    rc = _lib(mutation).oracle_ring_fwd(q, k, v, B, H, Hkv, S, D, cp, layout, int(causal), scale,
+                                        merge_order, out, lse)
+    if rc != 0:
+        raise ValueError("bad ring_fwd arguments")
+    return out, lse
+
+
+def attn_bwd(q, k, v, dout, causal=True, scale=None, mutation: int = 0):
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    dq = np.empty((B, S, H, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    _lib(mutation).oracle_attn_bwd(q, k, v, dout, B, H, Hkv, S, D, int(causal), scale, dq, dk, dv)
+    return dq, dk, dv
+
+
+def attn_bwd_dq_rows(q, k, v, dout, rows, causal=True, scale=None, mutation: int = 0):
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    dq = np.empty((rows.shape[0], D), np.float64)
+    _lib(mutation).oracle_attn_bwd_dq_rows(q, k, v, dout, B, H, Hkv, S, D, int(causal), scale,
+                                           rows, rows.shape[0], dq)
+    return dq
+
+
+def attn_bwd_dkdv_rows_sparse(q, k, v, dout, qrows, krows, causal=True, scale=None,
+                              mutation: int = 0):
+    """dK/dV rows (b, g, j) for a dout that is zero outside natural rows qrows."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    qrows = np.ascontiguousarray(np.asarray(qrows, dtype=np.int64).reshape(-1))
+    krows = np.ascontiguousarray(np.asarray(krows, dtype=np.int64).reshape(-1, 3))
+    n = krows.shape[0]
+    dk = np.empty((n, D), np.float64)
+    dv = np.empty((n, D), np.float64)
+    _lib(mutation).oracle_attn_bwd_dkdv_rows_sparse(q, k, v, dout, B, H, Hkv, S, D, int(causal),
+                                                    scale, qrows, qrows.shape[0], krows, n, dk, dv)
+    return dk, dv
+
+
+def tile_counts(S, cp, layout, causal, T, pairs=False, mutation: int = 0):
+    """(tiles[cp, cp], pairs[cp, cp] or None) per (rank r, ring step t)."""
+    tiles = np.zeros(cp * cp, np.uint64)
+    pr = np.zeros(cp * cp, np.uint64) if pairs else None
+    ptr = pr.ctypes.data_as(ctypes.c_void_p) if pairs else None
+    rc = _lib(mutation).oracle_tile_counts(S, cp, layout, int(causal), T, tiles, ptr)
+    if rc != 0:
+        raise ValueError("bad tile_counts arguments")
+    return tiles.reshape(cp, cp), (pr.reshape(cp, cp) if pairs else None)

@@ -1,0 +1,628 @@
+/*
+ * cpattn_oracle.c -- plain, slow, fp64 CPU oracle for context-parallel
+ * zigzag causal attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * CPU-baseline leg of bench.py may load this library.  The product path
+ * (libcpattn and its Python binding) never links, loads or calls it, and this
+ * file includes no header and shares no helper with the CUDA path.
+ *
+ * What it computes and where that is defined:
+ *
+ *  - Softmax attention itself (the "unsharded reference"): "Context
+ *    Parallelism for Long-Context Training", section "Prove attention
+ *    equivalence" -- the sharded result must agree with CP=1, outputs and
+ *    gradients, under causal masks.  Written out here from its plain
+ *    definition: s_ij = scale * q_i . k_j over the valid set V(i) (j <= i when
+ *    causal, all j otherwise), LSE_i = ln sum_j exp(s_ij),
+ *    O_i = sum_j exp(s_ij - LSE_i) v_j.
+ *  - The zigzag / load-balanced chunk placement: "Sequence Parallelism IV:
+ *    Megatron Context Parallel and Load-Balanced Rings", section 3 -- the
+ *    sequence is cut into 2*cp chunks and rank r holds chunks r and 2cp-1-r
+ *    (the cp=4 assignment printed there is a golden fixture).  The contiguous
+ *    placement (rank r holds tokens [r*S/cp, (r+1)*S/cp)) is the naive ring of
+ *    the same section and the shard function of the runnable artifact on
+ *    "Context Parallelism for Long-Context Training".
+ *  - The ring: same page, section 4 -- Q stays on its rank, K/V blocks move
+ *    around the group; each arriving block gives a partial output for the
+ *    local query chunks; online-softmax state keeps the result exact.  Here:
+ *    at ring step t rank r holds the K/V of rank (r - t) mod cp, each step
+ *    gives a normalised partial (O_rt, L_rt) over that source's tokens (masked
+ *    on natural positions), and the partials are merged with an exact
+ *    log-add-exp (section 5, "update the online softmax state").
+ *  - Gradients: the plain derivative of the definition above for a loss whose
+ *    gradient with respect to O is dO: with Delta_i = dO_i . O_i and
+ *    P_ij = exp(s_ij - LSE_i), dS_ij = P_ij (dO_i . v_j - Delta_i),
+ *    dQ_i = scale sum_j dS_ij k_j, dK_j = scale sum_i dS_ij q_i,
+ *    dV_j = sum_i P_ij dO_i (sums over i also run over the query heads that
+ *    share kv head j).
+ *
+ * Readings where the pages are silent: tensors are [B, S, H, D] row-major,
+ * LSE is [B, H, S] in natural log; query head h uses kv head h / (H / Hkv);
+ * the ring direction is "rank r receives from r - 1"; inside a rank's shard
+ * the early chunk comes first.
+ *
+ * Inputs are float32 arrays (they hold bf16- or fp32-valued data exactly) and
+ * every sum is taken in double precision.
+ *
+ * Pins (tests/test_oracle.py): pure-Python brute force at S <= 16, the printed
+ * cp=4 zigzag assignment, shard coverage, cp=1 equals the definition, ring
+ * result independent of cp / layout / merge order, constant V gives V, Q = 0
+ * gives the closed-form uniform average, row 0 gives v_0, central finite
+ * differences for every gradient, the sum rules sum_j dV_j = sum_i dO_i and
+ * sum_j dK_j = 0, and closed-form tile / pair counts.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Planted mistakes, compiled in only by the mutation tests (never by the
+ * regular build).  Each one must make at least one pin fail. */
+#ifndef ORACLE_MUTATION
+#define ORACLE_MUTATION 0
+#endif
+
+enum { LAYOUT_CONTIGUOUS = 0, LAYOUT_ZIGZAG = 1 };
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
+int oracle_get_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chunk placement                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* Natural chunk ids held by rank r, in the order they sit in its shard.
+ * Zigzag: chunks r and 2cp-1-r (early one first).  Contiguous: chunk r.
+ * Returns the number of chunks per rank. */
+static int rank_chunks(int r, int cp, int layout, int* out) {
+  if (layout == LAYOUT_ZIGZAG) {
+    out[0] = r;
+    out[1] = 2 * cp - 1 - r;
+#if ORACLE_MUTATION == 1
+    out[1] = 2 * cp - 2 - r + (r == cp - 1 ? cp : 0); /* wrong pairing */
+#endif
+    return 2;
+  }
+  out[0] = r;
+  return 1;
+}
+
+/* Fills nat_of_sharded[p] = natural token position of sharded position p, by
+ * appending each rank's chunks in rank order.  Returns 0, or -1 if S does not
+ * split into whole chunks. */
+int oracle_shard_order(long S, int cp, int layout, long* nat_of_sharded) {
+  if (cp < 1) return -1;
+  int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
+  long nchunk = (long)cp * per_rank;
+  if (S % nchunk != 0) return -1;
+  long c = S / nchunk;
+  long p = 0;
+  for (int r = 0; r < cp; ++r) {
+    int ch[2];
+    int n = rank_chunks(r, cp, layout, ch);
+    for (int a = 0; a < n; ++a)
+      for (long o = 0; o < c; ++o) nat_of_sharded[p++] = (long)ch[a] * c + o;
+  }
+  return 0;
+}
+
+/* Natural positions of every token held by rank s (its K/V, or its Q). */
+static long rank_tokens(long S, int cp, int layout, int s, long* out) {
+  int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
+  long c = S / ((long)cp * per_rank);
+  int ch[2];
+  int n = rank_chunks(s, cp, layout, ch);
+  long m = 0;
+  for (int a = 0; a < n; ++a)
+    for (long o = 0; o < c; ++o) out[m++] = (long)ch[a] * c + o;
+  return m;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Softmax attention over an explicit key set                                */
+/* ------------------------------------------------------------------------ */
+
+static inline long idx4(long b, long s, long h, long d, long S, long H, long D) {
+  return ((b * S + s) * H + h) * D + d;
+}
+
+static inline int kv_head_of(int h, int H, int Hkv) {
+#if ORACLE_MUTATION == 2
+  return h % Hkv; /* interleaved instead of consecutive grouping */
+#else
+  return h / (H / Hkv);
+#endif
+}
+
+static inline int is_valid(long i, long j, int causal) {
+#if ORACLE_MUTATION == 3
+  return !causal || j < i; /* mask seam off by one: diagonal dropped */
+#else
+  return !causal || j <= i;
+#endif
+}
+
+/* Normalised partial of query row (b, h, natural i) against the keys at the
+ * natural positions keys[0..nk): o[0..D) and *l (natural-log LSE).  A row
+ * with no valid key gives o = 0, l = -inf.  s_buf holds nk doubles. */
+static void partial_row(const float* q, const float* k, const float* v, long B, int H,
+                        int Hkv, long S, int D, int causal, double scale, long b, int h,
+                        long i, const long* keys, long nk, double* s_buf, double* o,
+                        double* l) {
+  (void)B;
+  int g = kv_head_of(h, H, Hkv);
+  const float* qi = q + idx4(b, i, h, 0, S, H, D);
+  double mx = -INFINITY;
+  for (long a = 0; a < nk; ++a) {
+    long j = keys[a];
+    if (!is_valid(i, j, causal)) {
+      s_buf[a] = -INFINITY;
+      continue;
+    }
+    const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
+    double dot = 0.0;
+    for (int d = 0; d < D; ++d) dot += (double)qi[d] * (double)kj[d];
+#if ORACLE_MUTATION == 4
+    s_buf[a] = dot; /* softmax scale dropped */
+#else
+    s_buf[a] = scale * dot;
+#endif
+    if (s_buf[a] > mx) mx = s_buf[a];
+  }
+  for (int d = 0; d < D; ++d) o[d] = 0.0;
+  if (mx == -INFINITY) {
+    *l = -INFINITY;
+    return;
+  }
+  double sum = 0.0;
+  for (long a = 0; a < nk; ++a) {
+    if (s_buf[a] == -INFINITY) continue;
+    double w = exp(s_buf[a] - mx);
+    sum += w;
+    const float* vj = v + idx4(b, keys[a], g, 0, S, Hkv, D);
+    for (int d = 0; d < D; ++d) o[d] += w * (double)vj[d];
+  }
+  for (int d = 0; d < D; ++d) o[d] /= sum;
+  *l = mx + log(sum);
+}
+
+/* Full attention (the definition), natural order.  out [B,S,H,D], lse [B,H,S]. */
+void oracle_attn_fwd(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                     long S, int D, int causal, double scale, double* out, double* lse) {
+  long nrows = B * (long)H * S;
+#pragma omp parallel
+  {
+    long* keys = (long*)malloc(sizeof(long) * S);
+    double* sb = (double*)malloc(sizeof(double) * S);
+    for (long j = 0; j < S; ++j) keys[j] = j;
+#pragma omp for schedule(dynamic, 16)
+    for (long row = 0; row < nrows; ++row) {
+      long b = row / ((long)H * S);
+      int h = (int)((row / S) % H);
+      long i = row % S;
+      double l;
+      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, keys, S, sb,
+                  out + idx4(b, i, h, 0, S, H, D), &l);
+      lse[(b * H + h) * S + i] = l;
+    }
+    free(keys);
+    free(sb);
+  }
+}
+
+/* The definition evaluated on a list of rows: rows[3*n + {0,1,2}] = (b, h, i)
+ * natural.  out [n, D], lse [n]. */
+void oracle_attn_fwd_rows(const float* q, const float* k, const float* v, long B, int H,
+                          int Hkv, long S, int D, int causal, double scale, const long* rows,
+                          long n, double* out, double* lse) {
+#pragma omp parallel
+  {
+    long* keys = (long*)malloc(sizeof(long) * S);
+    double* sb = (double*)malloc(sizeof(double) * S);
+    for (long j = 0; j < S; ++j) keys[j] = j;
+#pragma omp for schedule(dynamic, 1)
+    for (long a = 0; a < n; ++a) {
+      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, rows[3 * a], (int)rows[3 * a + 1],
+                  rows[3 * a + 2], keys, S, sb, out + a * D, lse + a);
+    }
+    free(keys);
+    free(sb);
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Exact merge of two normalised partials                                    */
+/* ------------------------------------------------------------------------ */
+
+/* (o_a, l_a) (+) (o_b, l_b): L = log(e^La + e^Lb) taken as Lmax + log1p(e^(Lmin-Lmax)),
+ * O = e^(La-L) O_a + e^(Lb-L) O_b.  An empty side (l = -inf) leaves the other
+ * unchanged.  o may alias o_a or o_b. */
+void oracle_lse_merge(const double* o_a, double l_a, const double* o_b, double l_b, int D,
+                      double* o, double* l) {
+  if (l_b == -INFINITY) {
+    for (int d = 0; d < D; ++d) o[d] = o_a[d];
+    *l = l_a;
+    return;
+  }
+  if (l_a == -INFINITY) {
+    for (int d = 0; d < D; ++d) o[d] = o_b[d];
+    *l = l_b;
+    return;
+  }
+  double hi = l_a > l_b ? l_a : l_b;
+  double lo = l_a > l_b ? l_b : l_a;
+  double L = hi + log1p(exp(lo - hi));
+  double wa = exp(l_a - L), wb = exp(l_b - L);
+#if ORACLE_MUTATION == 5
+  wb = 0.0; /* dropped merge term */
+#endif
+  for (int d = 0; d < D; ++d) o[d] = wa * o_a[d] + wb * o_b[d];
+  *l = L;
+}
+
+/* Array form used by the merge tests: O [B,S,H,D] doubles, LSE [B,H,S]. */
+void oracle_lse_merge_arrays(const double* o_a, const double* l_a, const double* o_b,
+                             const double* l_b, long B, long S, int H, int D, double* o,
+                             double* l) {
+#pragma omp parallel for schedule(static)
+  for (long row = 0; row < B * S * H; ++row) {
+    long b = row / (S * H), s = (row / H) % S;
+    int h = (int)(row % H);
+    long li = (b * H + h) * S + s;
+    double lo;
+    oracle_lse_merge(o_a + row * D, l_a[li], o_b + row * D, l_b[li], D, o + row * D, &lo);
+    l[li] = lo;
+  }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sequential ring                                                           */
+/* ------------------------------------------------------------------------ */
+
+static int ring_source(int r, int t, int cp) {
+#if ORACLE_MUTATION == 6
+  return (r + t) % cp; /* ring turned the other way */
+#else
+  return ((r - t) % cp + cp) % cp;
+#endif
+}
+
+/* Partial of ring step t for every rank: for each natural query row i, owned
+ * by rank r, the normalised partial against the tokens of rank
+ * (r - t) mod cp.  o_part [B,S,H,D], l_part [B,H,S], natural order. */
+int oracle_ring_step(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                     long S, int D, int cp, int layout, int causal, double scale, int t,
+                     double* o_part, double* l_part) {
+  int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
+  if (cp < 1 || S % ((long)cp * per_rank) != 0 || t < 0 || t >= cp) return -1;
+  long L = S / cp;
+  for (int r = 0; r < cp; ++r) {
+    long* qpos = (long*)malloc(sizeof(long) * L);
+    long* kpos = (long*)malloc(sizeof(long) * L);
+    rank_tokens(S, cp, layout, r, qpos);
+    rank_tokens(S, cp, layout, ring_source(r, t, cp), kpos);
+    long n = B * (long)H * L;
+#pragma omp parallel
+    {
+      double* sb = (double*)malloc(sizeof(double) * L);
+#pragma omp for schedule(dynamic, 16)
+      for (long a = 0; a < n; ++a) {
+        long b = a / ((long)H * L);
+        int h = (int)((a / L) % H);
+        long i = qpos[a % L];
+        double l;
+        partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, kpos, L, sb,
+                    o_part + idx4(b, i, h, 0, S, H, D), &l);
+        l_part[(b * H + h) * S + i] = l;
+      }
+      free(sb);
+    }
+    free(qpos);
+    free(kpos);
+  }
+  return 0;
+}
+
+/* The whole ring: cp steps of partials, merged per row.  merge_order 0: t =
+ * 0, 1, ..., cp-1 (left fold); 1: t = cp-1, ..., 0; 2: pairwise tree over t.
+ * out [B,S,H,D], lse [B,H,S], natural order.  Returns 0 or -1 on bad
+ * arguments. */
+int oracle_ring_fwd(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                    long S, int D, int cp, int layout, int causal, double scale,
+                    int merge_order, double* out, double* lse) {
+  int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
+  if (cp < 1 || S % ((long)cp * per_rank) != 0) return -1;
+  long L = S / cp;
+  long* qpos = (long*)malloc(sizeof(long) * L);
+  long* kpos = (long*)malloc(sizeof(long) * L * cp);
+  for (int r = 0; r < cp; ++r) {
+    rank_tokens(S, cp, layout, r, qpos);
+    for (int t = 0; t < cp; ++t) rank_tokens(S, cp, layout, ring_source(r, t, cp), kpos + t * L);
+    long n = B * (long)H * L;
+#pragma omp parallel
+    {
+      double* sb = (double*)malloc(sizeof(double) * L);
+      double* po = (double*)malloc(sizeof(double) * D * cp);
+      double* pl = (double*)malloc(sizeof(double) * cp);
+#pragma omp for schedule(dynamic, 16)
+      for (long a = 0; a < n; ++a) {
+        long b = a / ((long)H * L);
+        int h = (int)((a / L) % H);
+        long i = qpos[a % L];
+        for (int t = 0; t < cp; ++t)
+          partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, kpos + t * L, L, sb,
+                      po + t * D, pl + t);
+        if (merge_order == 2) {
+          for (int w = 1; w < cp; w *= 2)
+            for (int t = 0; t + w < cp; t += 2 * w)
+              oracle_lse_merge(po + t * D, pl[t], po + (t + w) * D, pl[t + w], D, po + t * D,
+                               pl + t);
+        } else if (merge_order == 1) {
+          for (int t = cp - 2; t >= 0; --t)
+            oracle_lse_merge(po + (cp - 1) * D, pl[cp - 1], po + t * D, pl[t], D,
+                             po + (cp - 1) * D, pl + cp - 1);
+          memcpy(po, po + (cp - 1) * D, sizeof(double) * D);
+          pl[0] = pl[cp - 1];
+        } else {
+          for (int t = 1; t < cp; ++t)
+            oracle_lse_merge(po, pl[0], po + t * D, pl[t], D, po, pl);
+        }
+        memcpy(out + idx4(b, i, h, 0, S, H, D), po, sizeof(double) * D);
+        lse[(b * H + h) * S + i] = pl[0];
+      }
+      free(sb);
+      free(po);
+      free(pl);
+    }
+  }
+  free(qpos);
+  free(kpos);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gradients                                                                 */
+/* ------------------------------------------------------------------------ */
+
+static double dot_f(const float* a, const float* b, int D) {
+  double s = 0.0;
+  for (int d = 0; d < D; ++d) s += (double)a[d] * (double)b[d];
+  return s;
+}
+
+/* dQ, dK, dV of the definition for the upstream gradient dout = dL/dO.
+ * All natural order, dq [B,S,H,D], dk/dv [B,S,Hkv,D]. */
+void oracle_attn_bwd(const float* q, const float* k, const float* v, const float* dout,
+                     long B, int H, int Hkv, long S, int D, int causal, double scale,
+                     double* dq, double* dk, double* dv) {
+  double* o = (double*)malloc(sizeof(double) * B * S * H * D);
+  double* lse = (double*)malloc(sizeof(double) * B * H * S);
+  double* delta = (double*)malloc(sizeof(double) * B * H * S);
+  oracle_attn_fwd(q, k, v, B, H, Hkv, S, D, causal, scale, o, lse);
+#pragma omp parallel for schedule(static)
+  for (long row = 0; row < B * S * H; ++row) {
+    long b = row / (S * H), i = (row / H) % S;
+    int h = (int)(row % H);
+    double s = 0.0;
+    for (int d = 0; d < D; ++d) s += (double)dout[row * D + d] * o[row * D + d];
+    delta[(b * H + h) * S + i] = s;
+  }
+  /* dQ: one query row at a time. */
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long row = 0; row < B * S * H; ++row) {
+    long b = row / (S * H), i = (row / H) % S;
+    int h = (int)(row % H);
+    int g = kv_head_of(h, H, Hkv);
+    const float* qi = q + row * D;
+    const float* doi = dout + row * D;
+    double l = lse[(b * H + h) * S + i], dl = delta[(b * H + h) * S + i];
+    double* dqi = dq + row * D;
+    for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+    for (long j = 0; j < S; ++j) {
+      if (!is_valid(i, j, causal)) continue;
+      const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
+      const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
+      double p = exp(scale * dot_f(qi, kj, D) - l);
+      double ds = p * (dot_f(doi, vj, D) - dl);
+      for (int d = 0; d < D; ++d) dqi[d] += scale * ds * (double)kj[d];
+    }
+  }
+  /* dK, dV: one key row at a time, summed over the query heads sharing it. */
+  int grp = H / Hkv;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long krow = 0; krow < B * S * Hkv; ++krow) {
+    long b = krow / (S * Hkv), j = (krow / Hkv) % S;
+    int g = (int)(krow % Hkv);
+    const float* kj = k + krow * D;
+    const float* vj = v + krow * D;
+    double* dkj = dk + krow * D;
+    double* dvj = dv + krow * D;
+    for (int d = 0; d < D; ++d) dkj[d] = dvj[d] = 0.0;
+    for (int h = 0; h < H; ++h) {
+      if (kv_head_of(h, H, Hkv) != g) continue;
+      for (long i = 0; i < S; ++i) {
+        if (!is_valid(i, j, causal)) continue;
+        const float* qi = q + idx4(b, i, h, 0, S, H, D);
+        const float* doi = dout + idx4(b, i, h, 0, S, H, D);
+        double p = exp(scale * dot_f(qi, kj, D) - lse[(b * H + h) * S + i]);
+        double ds = p * (dot_f(doi, vj, D) - delta[(b * H + h) * S + i]);
+        for (int d = 0; d < D; ++d) {
+          dkj[d] += scale * ds * (double)qi[d];
+          dvj[d] += p * (double)doi[d];
+        }
+      }
+    }
+    (void)grp;
+  }
+  free(o);
+  free(lse);
+  free(delta);
+}
+
+/* dQ of the definition on a list of query rows (b, h, i): each row needs only
+ * its own softmax row, so this is exact for any dout.  dq [n, D]. */
+void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, const float* dout,
+                             long B, int H, int Hkv, long S, int D, int causal, double scale,
+                             const long* rows, long n, double* dq) {
+  (void)B;
+#pragma omp parallel
+  {
+    long* keys = (long*)malloc(sizeof(long) * S);
+    double* sb = (double*)malloc(sizeof(double) * S);
+    double* o = (double*)malloc(sizeof(double) * D);
+    for (long j = 0; j < S; ++j) keys[j] = j;
+#pragma omp for schedule(dynamic, 1)
+    for (long a = 0; a < n; ++a) {
+      long b = rows[3 * a], i = rows[3 * a + 2];
+      int h = (int)rows[3 * a + 1];
+      int g = kv_head_of(h, H, Hkv);
+      double l;
+      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, keys, S, sb, o, &l);
+      const float* qi = q + idx4(b, i, h, 0, S, H, D);
+      const float* doi = dout + idx4(b, i, h, 0, S, H, D);
+      double dl = 0.0;
+      for (int d = 0; d < D; ++d) dl += (double)doi[d] * o[d];
+      double* dqi = dq + a * D;
+      for (int d = 0; d < D; ++d) dqi[d] = 0.0;
+      for (long j = 0; j < S; ++j) {
+        if (!is_valid(i, j, causal)) continue;
+        const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
+        const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
+        double p = exp(scale * dot_f(qi, kj, D) - l);
+        double ds = p * (dot_f(doi, vj, D) - dl);
+        for (int d = 0; d < D; ++d) dqi[d] += scale * ds * (double)kj[d];
+      }
+    }
+    free(keys);
+    free(sb);
+    free(o);
+  }
+}
+
+/* dK, dV of the definition on a list of key rows (b, g, j), for an upstream
+ * gradient that is zero on every query row except the natural positions
+ * qrows[0..nq) (all batches, all heads).  Rows with dO_i = 0 have
+ * Delta_i = 0 and hence dS_ij = 0 and P_ij dO_i = 0, so the sums over i may
+ * be restricted to qrows: the result is the exact definition for such a
+ * dout.  dk, dv [n, D]. */
+void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const float* v,
+                                      const float* dout, long B, int H, int Hkv, long S, int D,
+                                      int causal, double scale, const long* qrows, long nq,
+                                      const long* krows, long n, double* dk, double* dv) {
+  /* Softmax state of the needed query rows, every (b, h). */
+  double* lse = (double*)malloc(sizeof(double) * B * H * nq);
+  double* delta = (double*)malloc(sizeof(double) * B * H * nq);
+#pragma omp parallel
+  {
+    long* keys = (long*)malloc(sizeof(long) * S);
+    double* sb = (double*)malloc(sizeof(double) * S);
+    double* o = (double*)malloc(sizeof(double) * D);
+    for (long j = 0; j < S; ++j) keys[j] = j;
+#pragma omp for schedule(dynamic, 1)
+    for (long a = 0; a < B * H * nq; ++a) {
+      long b = a / (H * nq);
+      int h = (int)((a / nq) % H);
+      long i = qrows[a % nq];
+      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, keys, S, sb, o, lse + a);
+      const float* doi = dout + idx4(b, i, h, 0, S, H, D);
+      double dl = 0.0;
+      for (int d = 0; d < D; ++d) dl += (double)doi[d] * o[d];
+      delta[a] = dl;
+    }
+    free(keys);
+    free(sb);
+    free(o);
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long a = 0; a < n; ++a) {
+    long b = krows[3 * a], j = krows[3 * a + 2];
+    int g = (int)krows[3 * a + 1];
+    const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
+    const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
+    double* dkj = dk + a * D;
+    double* dvj = dv + a * D;
+    for (int d = 0; d < D; ++d) dkj[d] = dvj[d] = 0.0;
+    for (int h = 0; h < H; ++h) {
+      if (kv_head_of(h, H, Hkv) != g) continue;
+      for (long x = 0; x < nq; ++x) {
+        long i = qrows[x];
+        if (!is_valid(i, j, causal)) continue;
+        const float* qi = q + idx4(b, i, h, 0, S, H, D);
+        const float* doi = dout + idx4(b, i, h, 0, S, H, D);
+        long si = (b * H + h) * nq + x;
+        double p = exp(scale * dot_f(qi, kj, D) - lse[si]);
+        double ds = p * (dot_f(doi, vj, D) - delta[si]);
+        for (int d = 0; d < D; ++d) {
+          dkj[d] += scale * ds * (double)qi[d];
+          dvj[d] += p * (double)doi[d];
+        }
+      }
+    }
+  }
+  free(lse);
+  free(delta);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Work census of the ring                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* For every rank r and ring step t: the number of T x T tiles that hold at
+ * least one valid (query, key) pair, and (if pairs_rt is not NULL) the number
+ * of valid pairs, per (batch, head).  Tiles are T consecutive tokens of a
+ * rank's shard (query side) and of the source rank's shard (key side), each
+ * inside one chunk; T must divide the chunk length.  Found by enumeration
+ * over tiles (and, for pairs, over every pair of every live tile). */
+int oracle_tile_counts(long S, int cp, int layout, int causal, long T, uint64_t* tiles_rt,
+                       uint64_t* pairs_rt) {
+  int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
+  if (cp < 1 || T < 1 || S % ((long)cp * per_rank) != 0) return -1;
+  long L = S / cp, c = L / per_rank;
+  if (c % T != 0) return -1;
+  long* qpos = (long*)malloc(sizeof(long) * L);
+  long* kpos = (long*)malloc(sizeof(long) * L);
+  for (int r = 0; r < cp; ++r) {
+    rank_tokens(S, cp, layout, r, qpos);
+    for (int t = 0; t < cp; ++t) {
+      rank_tokens(S, cp, layout, ring_source(r, t, cp), kpos);
+      uint64_t tiles = 0, pairs = 0;
+      for (long qa = 0; qa < L; qa += T) {
+        for (long kb = 0; kb < L; kb += T) {
+          /* j <= i is monotone, so some pair of the tile is valid exactly
+           * when the latest query and the earliest key form a valid pair. */
+          long qmax = qpos[qa], kmin = kpos[kb];
+          for (long x = 1; x < T; ++x) qmax = qpos[qa + x] > qmax ? qpos[qa + x] : qmax;
+          for (long y = 1; y < T; ++y) kmin = kpos[kb + y] < kmin ? kpos[kb + y] : kmin;
+          int any = is_valid(qmax, kmin, causal);
+          tiles += (uint64_t)any;
+          if (pairs_rt && any)
+            for (long x = 0; x < T; ++x)
+              for (long y = 0; y < T; ++y)
+                pairs += (uint64_t)is_valid(qpos[qa + x], kpos[kb + y], causal);
+        }
+      }
+      tiles_rt[r * cp + t] = tiles;
+      if (pairs_rt) pairs_rt[r * cp + t] = pairs;
+    }
+  }
+  free(qpos);
+  free(kpos);
+  return 0;
+}

@@ -1,0 +1,301 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each ``pin_*`` function raises AssertionError when the oracle (optionally a
+mutated build of it) disagrees with an independent fact:
+
+* the cp=4 zigzag assignment printed in "Sequence Parallelism IV ...",
+  section 3 (tests/golden/zigzag_cp4.txt);
+* the contiguous shard coverage artifact of "Context Parallelism for
+  Long-Context Training" (tests/golden/contiguous_shards_n8_p4.txt);
+* a pure-Python brute force of the softmax definition at S <= 16;
+* closed forms: constant V gives V, Q = 0 gives the running mean with
+  LSE = ln(#keys), row 0 of a causal mask sees only key 0;
+* "CP=1 equals the unsharded reference" and independence of the ring result
+  from cp, layout and merge order ("Prove attention equivalence");
+* central finite differences of the brute-force forward for dQ, dK, dV,
+  plus the sum rules sum_j dV_j = sum_i dO_i and sum_j dK_j = 0;
+* closed-form per-step tile and pair counts of the two layouts.
+
+``test_mutations_are_caught`` compiles planted mistakes into the oracle and
+checks that some pin fails for each.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import brute
+from context_causal_attention_zigzag_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def small(B, H, Hkv, S, D, seed, dout=False):
+    w = inputs.Workload("tiny", B, H, Hkv, S, D, 1, inputs.ZIGZAG, True,
+                        inputs.torch.float32, seed=seed)
+    q, k, v, do = inputs.generate(w, with_dout=dout)
+    f = inputs.to_f32_numpy
+    return f(q), f(k), f(v), (f(do) if dout else None)
+
+
+def read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return rows
+
+
+# ----------------------------------------------------------------------------
+# pins
+# ----------------------------------------------------------------------------
+
+def pin_zigzag_golden(m=0):
+    rows = read_golden("zigzag_cp4.txt")
+    cp = 4
+    # Chunk length 1: the sharded order lists each rank's chunks in turn.
+    order = oracle.shard_order(2 * cp, cp, oracle.ZIGZAG, mutation=m)
+    expect = [c for r, a, b in rows for c in (a, b)]
+    assert order.tolist() == expect, (order.tolist(), expect)
+    # Chunk length 3: every chunk moves as a block.
+    c = 3
+    order = oracle.shard_order(2 * cp * c, cp, oracle.ZIGZAG, mutation=m)
+    expect = [ch * c + o for r, a, b in rows for ch in (a, b) for o in range(c)]
+    assert order.tolist() == expect
+
+
+def pin_contiguous_golden(m=0):
+    rows = read_golden("contiguous_shards_n8_p4.txt")
+    order = oracle.shard_order(8, 4, oracle.CONTIGUOUS, mutation=m)
+    flat = [t for r in rows for t in r[1:]]
+    assert order.tolist() == flat == list(range(8))
+
+
+def pin_coverage(m=0):
+    for cp in (1, 2, 3, 4, 8, 16):
+        for layout, per in ((oracle.ZIGZAG, 2), (oracle.CONTIGUOUS, 1)):
+            for c in (1, 2, 5):
+                S = cp * per * c
+                order = oracle.shard_order(S, cp, layout, mutation=m)
+                assert sorted(order.tolist()) == list(range(S))
+                if layout == oracle.ZIGZAG and c == 1:
+                    assign = brute.zigzag_assignment(cp)
+                    assert order.tolist() == [x for pair in assign for x in pair]
+
+
+def pin_brute_force(m=0):
+    for causal in (True, False):
+        for (B, H, Hkv, S, D, seed) in ((1, 2, 2, 7, 4, 11), (2, 4, 2, 12, 8, 12),
+                                        (1, 3, 1, 16, 5, 13)):
+            q, k, v, _ = small(B, H, Hkv, S, D, seed)
+            out, lse = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+            bo, bl = brute.attn_fwd(q.tolist(), k.tolist(), v.tolist(), causal=causal)
+            np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
+
+
+def pin_constant_v(m=0):
+    q, k, v, _ = small(2, 4, 2, 32, 8, 21)
+    v[:] = np.random.default_rng(5).standard_normal((2, 1, 2, 8)).astype(np.float32)
+    for causal in (True, False):
+        out, _ = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+        expect = v[:, :, [0, 0, 1, 1], :].astype(np.float64)
+        np.testing.assert_allclose(out, expect, rtol=0, atol=1e-12)
+
+
+def pin_q_zero(m=0):
+    B, H, Hkv, S, D = 1, 2, 1, 24, 8
+    q, k, v, _ = small(B, H, Hkv, S, D, 22)
+    q[:] = 0.0
+    vv = v.astype(np.float64)
+    for causal in (True, False):
+        out, lse = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+        for i in range(S):
+            n = i + 1 if causal else S
+            mean = vv[0, :n, 0, :].mean(axis=0)
+            for h in range(H):
+                np.testing.assert_allclose(out[0, i, h], mean, rtol=0, atol=1e-12)
+                assert abs(lse[0, h, i] - math.log(n)) < 1e-12
+
+
+def pin_row0(m=0):
+    q, k, v, _ = small(1, 2, 2, 16, 8, 23)
+    out, lse = oracle.attn_fwd(q, k, v, causal=True, mutation=m)
+    for h in range(2):
+        np.testing.assert_allclose(out[0, 0, h], v[0, 0, h].astype(np.float64), atol=1e-12)
+        s00 = float(np.dot(q[0, 0, h].astype(np.float64), k[0, 0, h].astype(np.float64)))
+        assert abs(lse[0, h, 0] - s00 / math.sqrt(8)) < 1e-12
+
+
+def pin_ring_invariance(m=0):
+    B, H, Hkv, S, D = 2, 4, 2, 64, 16
+    q, k, v, _ = small(B, H, Hkv, S, D, 31)
+    for causal in (True, False):
+        ref_o, ref_l = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+        for cp in (1, 2, 4, 8, 16):
+            layouts = (oracle.ZIGZAG, oracle.CONTIGUOUS) if S % (2 * cp) == 0 \
+                else (oracle.CONTIGUOUS,)
+            for layout in layouts:
+                for order in (0, 1, 2):
+                    o, l = oracle.ring_fwd(q, k, v, cp, layout, causal=causal,
+                                           merge_order=order, mutation=m)
+                    np.testing.assert_allclose(o, ref_o, rtol=0, atol=1e-12)
+                    np.testing.assert_allclose(l, ref_l, rtol=0, atol=1e-12)
+
+
+def pin_step_partials_merge(m=0):
+    B, H, Hkv, S, D = 1, 2, 1, 48, 8
+    q, k, v, _ = small(B, H, Hkv, S, D, 32)
+    ref_o, ref_l = oracle.attn_fwd(q, k, v, causal=True, mutation=m)
+    for layout in (oracle.ZIGZAG, oracle.CONTIGUOUS):
+        cp = 4
+        acc_o, acc_l = oracle.ring_step(q, k, v, cp, layout, 0, mutation=m)
+        for t in range(1, cp):
+            po, pl = oracle.ring_step(q, k, v, cp, layout, t, mutation=m)
+            acc_o, acc_l = oracle.lse_merge(acc_o, acc_l, po, pl, mutation=m)
+        np.testing.assert_allclose(acc_o, ref_o, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(acc_l, ref_l, rtol=0, atol=1e-12)
+
+
+def pin_finite_differences(m=0):
+    B, H, Hkv, S, D = 1, 2, 1, 5, 3
+    q, k, v, do = small(B, H, Hkv, S, D, 41, dout=True)
+    for causal in (True, False):
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=causal, mutation=m)
+        ql, kl, vl, dol = (x.astype(np.float64).tolist() for x in (q, k, v, do))
+        for name, got in (("q", dq), ("k", dk), ("v", dv)):
+            fd = np.array(brute.finite_diff_grad(name, ql, kl, vl, dol, causal=causal))
+            np.testing.assert_allclose(got, fd, rtol=0, atol=2e-8)
+
+
+def pin_sum_rules(m=0):
+    B, H, Hkv, S, D = 2, 4, 2, 40, 8
+    q, k, v, do = small(B, H, Hkv, S, D, 42, dout=True)
+    for causal in (True, False):
+        dq, dk, dv = oracle.attn_bwd(q, k, v, do, causal=causal, mutation=m)
+        d64 = do.astype(np.float64)
+        for g in range(Hkv):
+            heads = [h for h in range(H) if h * Hkv // H == g]
+            np.testing.assert_allclose(dv[:, :, g].sum(axis=1),
+                                       d64[:, :, heads].sum(axis=(1, 2)), atol=1e-10)
+            np.testing.assert_allclose(dk[:, :, g].sum(axis=1), 0.0, atol=1e-10)
+
+
+def pin_tile_counts(m=0):
+    for cp in (1, 2, 4, 8):
+        for n in (1, 2, 3):
+            T = 4
+            c = n * T
+            # zigzag, causal: 2n^2 + n tiles at t = 0, 2n^2 after; pairs 2c^2 + c, 2c^2.
+            S = 2 * cp * c
+            tiles, pairs = oracle.tile_counts(S, cp, oracle.ZIGZAG, True, T, pairs=True,
+                                              mutation=m)
+            for r in range(cp):
+                for t in range(cp):
+                    assert tiles[r, t] == (2 * n * n + n if t == 0 else 2 * n * n)
+                    assert pairs[r, t] == (2 * c * c + c if t == 0 else 2 * c * c)
+            assert int(pairs.sum()) == S * (S + 1) // 2
+            # contiguous, causal: L(L+1)/2 at t = 0; L^2 when the source is earlier
+            # (t <= r, ring receiving from r - 1), else nothing.
+            Lc = 2 * c
+            mm = Lc // T
+            S = cp * Lc
+            tiles, pairs = oracle.tile_counts(S, cp, oracle.CONTIGUOUS, True, T, pairs=True,
+                                              mutation=m)
+            for r in range(cp):
+                for t in range(cp):
+                    if t == 0:
+                        et, ep = mm * (mm + 1) // 2, Lc * (Lc + 1) // 2
+                    elif t <= r:
+                        et, ep = mm * mm, Lc * Lc
+                    else:
+                        et, ep = 0, 0
+                    assert tiles[r, t] == et and pairs[r, t] == ep, (cp, n, r, t)
+            assert int(pairs.sum()) == S * (S + 1) // 2
+            # non-causal: every tile, every pair.
+            tiles, pairs = oracle.tile_counts(S, cp, oracle.CONTIGUOUS, False, T, pairs=True,
+                                              mutation=m)
+            assert (tiles == mm * mm).all() and (pairs == Lc * Lc).all()
+
+
+PINS = [pin_zigzag_golden, pin_contiguous_golden, pin_coverage, pin_brute_force,
+        pin_constant_v, pin_q_zero, pin_row0, pin_ring_invariance, pin_step_partials_merge,
+        pin_finite_differences, pin_sum_rules, pin_tile_counts]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin(0)
+
+
+# ----------------------------------------------------------------------------
+# consistency of the sampled-row entry points with the full ones
+# ----------------------------------------------------------------------------
+
+def test_rows_match_full():
+    B, H, Hkv, S, D = 2, 4, 2, 40, 8
+    q, k, v, do = small(B, H, Hkv, S, D, 51, dout=True)
+    out, lse = oracle.attn_fwd(q, k, v)
+    rows = np.array([[b, h, i] for b in range(B) for h in range(H) for i in (0, 7, 39)])
+    ro, rl = oracle.attn_fwd_rows(q, k, v, rows)
+    np.testing.assert_array_equal(ro, out[rows[:, 0], rows[:, 2], rows[:, 1]])
+    np.testing.assert_array_equal(rl, lse[rows[:, 0], rows[:, 1], rows[:, 2]])
+    dq, dk, dv = oracle.attn_bwd(q, k, v, do)
+    rdq = oracle.attn_bwd_dq_rows(q, k, v, do, rows)
+    np.testing.assert_allclose(rdq, dq[rows[:, 0], rows[:, 2], rows[:, 1]], atol=1e-12)
+    # dK / dV from a dO that is zero outside a few query rows.
+    qrows = np.array([3, 17, 38])
+    sparse = np.zeros_like(do)
+    sparse[:, qrows] = do[:, qrows]
+    dq2, dk2, dv2 = oracle.attn_bwd(q, k, v, sparse)
+    krows = np.array([[b, g, j] for b in range(B) for g in range(Hkv) for j in (0, 3, 20, 38)])
+    sdk, sdv = oracle.attn_bwd_dkdv_rows_sparse(q, k, v, sparse, qrows, krows)
+    np.testing.assert_allclose(sdk, dk2[krows[:, 0], krows[:, 2], krows[:, 1]], atol=1e-12)
+    np.testing.assert_allclose(sdv, dv2[krows[:, 0], krows[:, 2], krows[:, 1]], atol=1e-12)
+
+
+def test_empty_partial_is_neutral():
+    B, S, H, D = 1, 6, 2, 4
+    rng = np.random.default_rng(3)
+    o = rng.standard_normal((B, S, H, D))
+    l = rng.standard_normal((B, H, S))
+    zo = np.zeros_like(o)
+    zl = np.full_like(l, -np.inf)
+    for a, b in (((o, l), (zo, zl)), ((zo, zl), (o, l))):
+        mo, ml = oracle.lse_merge(a[0], a[1], b[0], b[1])
+        np.testing.assert_array_equal(mo, o)
+        np.testing.assert_array_equal(ml, l)
+    mo, ml = oracle.lse_merge(zo, zl, zo, zl)
+    assert np.isneginf(ml).all() and (mo == 0).all()
+
+
+def test_bad_arguments_rejected():
+    with pytest.raises(ValueError):
+        oracle.shard_order(10, 4, oracle.ZIGZAG)
+    q, k, v, _ = small(1, 1, 1, 10, 4, 1)
+    with pytest.raises(ValueError):
+        oracle.ring_fwd(q, k, v, 4, oracle.ZIGZAG)
+
+
+# ----------------------------------------------------------------------------
+# planted mistakes
+# ----------------------------------------------------------------------------
+
+MUTATIONS = {1: "wrong zigzag pairing", 2: "interleaved GQA head map",
+             3: "causal diagonal dropped", 4: "softmax scale dropped",
+             5: "merge term dropped", 6: "ring turned the other way"}
+
+
+@pytest.mark.parametrize("m", sorted(MUTATIONS), ids=[MUTATIONS[m] for m in sorted(MUTATIONS)])
+def test_mutations_are_caught(m):
+    failed = []
+    for pin in PINS:
+        try:
+            pin(m)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutation {m} ({MUTATIONS[m]})"
