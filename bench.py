@@ -1,0 +1,458 @@
+"""Throughput of the context-parallel zigzag ring attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step is the whole hot path over one batch of synthetic input resident in
+HBM: zigzag-permute Q, K, V, dO into sharded order, ring forward (O, LSE),
+ring backward (dQ, dK, dV from the saved LSE), unpermute O, LSE, dQ, dK, dV
+back to natural order.  The default workload is the S=131072 forward+backward
+one (B=1, H=32, Hkv=8, D=128, cp=16, zigzag, causal, bf16); the S=32768
+forward on which the tensor-roofline target is quoted is timed in the same
+run and reported under "c3_forward".
+
+Metric: useful attention TFLOP/s -- 4*D flops per visible (query, key) pair
+forward, 10*D backward (S(S+1)/2 visible pairs per head when causal).  Inputs
+are far larger than L2 (129 MB), so no flush is needed between steps.
+
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU
+(the path itself runs on one GPU: "replicas only"); the reported value is the
+work of all ranks over the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (rank 0 only).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from context_causal_attention_zigzag_gb300 import inputs  # noqa: E402
+
+METRIC = "useful causal attention TFLOP/s on 1 GB300 (fwd, fwd+bwd) and % of BF16 tensor peak"
+UNIT = "TFLOP/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), \
+            float(d["hbm_gbs"]), "measured"
+    return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import context_causal_attention_zigzag_gb300 as cpa
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = inputs.WORKLOADS[args.workload]
+    peak, peak_sus, hbm, peak_kind = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v, do = inputs.generate(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    dod = do.to(dev) if do is not None else None
+    cp, layout, causal = w.cp, w.layout, w.causal
+    B, S, H, Hkv, D = w.B, w.S, w.H, w.Hkv, w.D
+
+    # Preallocated sharded buffers, outputs and workspace: the step allocates nothing.
+    qs, ks, vs = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, S), device=dev, dtype=torch.float32)
+    o_nat, lse_nat = torch.empty_like(o), torch.empty_like(lse)
+    if w.backward:
+        dos = torch.empty_like(dod)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        dq_nat, dk_nat, dv_nat = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+        wsp = torch.empty(cpa.ring_bwd_workspace_bytes(B, H, Hkv, S, D), device=dev,
+                          dtype=torch.uint8)
+    ev = {}
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        ev.setdefault(name, []).append(e)
+
+    def step(timed=False, src=(qd, kd, vd, dod)):
+        sq, sk, sv, sdo = src
+        cpa.zigzag_permute(sq, cp, layout, out=qs)
+        cpa.zigzag_permute(sk, cp, layout, out=ks)
+        cpa.zigzag_permute(sv, cp, layout, out=vs)
+        if w.backward:
+            cpa.zigzag_permute(sdo, cp, layout, out=dos)
+        if timed:
+            mark("fwd0")
+        cpa.ring_fwd(qs, ks, vs, cp, layout, causal, out=o, lse=lse)
+        if timed:
+            mark("fwd1")
+        if w.backward:
+            cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, dq=dq, dk=dk, dv=dv,
+                         workspace=wsp)
+            if timed:
+                mark("bwd1")
+        cpa.zigzag_unpermute(o, cp, layout, out=o_nat)
+        cpa.zigzag_unpermute(lse, cp, layout, seq_dim=2, out=lse_nat)
+        if w.backward:
+            cpa.zigzag_unpermute(dq, cp, layout, out=dq_nat)
+            cpa.zigzag_unpermute(dk, cp, layout, out=dk_nat)
+            cpa.zigzag_unpermute(dv, cp, layout, out=dv_nat)
+
+    launches_per_step = (4 if w.backward else 3) + 1 + (3 if w.backward else 0) + \
+        (5 if w.backward else 2)
+    fwd_flops = w.useful_flops(False)
+    bwd_flops = w.useful_flops(True) if w.backward else 0.0
+    step_flops = fwd_flops + bwd_flops
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    ev.clear()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(timed=True)
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["fwd0"], ev["fwd1"]))
+    bwd_ms = (statistics.mean(a.elapsed_time(b) for a, b in zip(ev["fwd1"], ev["bwd1"]))
+              if w.backward else None)
+    ms_max = ms
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    value = step_flops * ws / (ms_max * 1e-3) / 1e12
+
+    # End to end through the public API: pinned host inputs in, results out.
+    e2e = None
+    if rank == 0 or ws > 1:
+        hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+        hdo = do.pin_memory() if do is not None else None
+        outs = [o_nat, lse_nat] + ([dq_nat, dk_nat, dv_nat] if w.backward else [])
+        host_outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo) if x is not None)
+        d2h = sum(x.numel() * x.element_size() for x in outs)
+        dq_in = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd), \
+            (torch.empty_like(dod) if dod is not None else None)
+
+        def e2e_step():
+            for dst, src in zip(dq_in, (hq, hk, hv, hdo)):
+                if src is not None:
+                    dst.copy_(src, non_blocking=True)
+            step(src=dq_in)
+            for dst, src in zip(host_outs, outs):
+                dst.copy_(src, non_blocking=True)
+
+        e2e_step()
+        barrier()
+        n_e2e = max(1, min(args.steps, 5))
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = a0.elapsed_time(a1) / n_e2e
+        e2e = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+        del dq_in
+
+    # Roofline of the dominant kernel, from the live event timings.
+    dom_ms, dom_flops, dom_name = (bwd_ms, bwd_flops, "ring_bwd") \
+        if (w.backward and bwd_ms >= fwd_ms) else (fwd_ms, fwd_flops, "ring_fwd")
+    achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_kind": f"{peak_kind} bf16 burst", "ms": dom_ms,
+                "frac_of_sustained": achieved / peak_sus}
+    fwd_info = {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12}
+    fwd_info["frac"] = fwd_info["tflops"] / peak
+    if w.backward:
+        fwd_info["bwd_ms"] = bwd_ms
+        fwd_info["bwd_tflops"] = bwd_flops / (bwd_ms * 1e-3) / 1e12
+
+    # The S=32768 forward (tensor-roofline target workload), timed alone.
+    c3 = None
+    if args.workload != "c3_bf16_s32768_gqa" and not args.no_c3:
+        c3 = time_forward(cpa, inputs.WORKLOADS["c3_bf16_s32768_gqa"], dev, stream,
+                          args.warmup, max(args.steps, 5), peak)
+
+    path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, q, k, v, do, budget_s=args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype_name, "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "S": S, "H": H, "Hkv": Hkv, "D": D, "cp": cp,
+                   "layout": "zigzag" if layout == 1 else "contiguous", "causal": causal,
+                   "backward": w.backward, "seed": w.seed,
+                   "parallelism": "replicas" if ws > 1 else "single_gpu",
+                   "l2": "inputs larger than L2 (no flush)",
+                   "fwd_path": "tcgen05" if path == 1 else "simt", "tile": tile,
+                   "useful_tflop_per_step": step_flops / 1e12},
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+        "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "cpu_baseline": cpu,
+        "status": cpa.device_status(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def time_forward(cpa, w, dev, stream, warmup, steps, peak):
+    q, k, v, _ = inputs.generate(w, with_dout=False)
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    qs, ks, vs = (cpa.zigzag_permute(x, w.cp, w.layout) for x in (qd, kd, vd))
+    o = torch.empty_like(qs)
+    lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    for _ in range(warmup):
+        cpa.ring_fwd(qs, ks, vs, w.cp, w.layout, w.causal, out=o, lse=lse)
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(steps):
+        a.record(stream)
+        cpa.ring_fwd(qs, ks, vs, w.cp, w.layout, w.causal, out=o, lse=lse)
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    tf = w.useful_flops(False) / (ms * 1e-3) / 1e12
+    path, tile = cpa.plan(w.B, w.H, w.Hkv, w.S, w.D, w.cp, w.layout, w.causal, w.dtype)
+    # Kernel census of the same call: per-step max/mean of tiles per rank.
+    counts = torch.zeros((w.cp, w.cp), device=dev, dtype=torch.int64)
+    cpa.ring_fwd(qs, ks, vs, w.cp, w.layout, w.causal, out=o, lse=lse, tiles_rt=counts)
+    c = counts.cpu().numpy().astype(np.float64)
+    imbalance = float(np.max(c.max(axis=0) / np.maximum(c.mean(axis=0), 1)))
+    return {"workload": w.name, "ms_median": ms, "ms_min": min(times), "tflops": tf,
+            "frac": tf / peak, "path": "tcgen05" if path == 1 else "simt", "tile": tile,
+            "zigzag_step_imbalance_max_over_mean": imbalance}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rows(w, n, seed):
+    rng = np.random.default_rng(seed)
+    b = rng.integers(0, w.B, n)
+    h = rng.integers(0, w.H, n)
+    i = rng.integers(0, w.S, n)
+    return np.stack([b, h, i], axis=1).astype(np.int64)
+
+
+def oracle_flops(w, rows, backward):
+    # Visible keys per sampled row; forward 4*D per pair, plus the dQ part of
+    # the backward (recompute S, dP, dQ: 6*D per pair) when timed.
+    keys = (rows[:, 2] + 1) if w.causal else np.full(len(rows), w.S)
+    per = 4 * w.D + (6 * w.D if backward else 0)
+    return float(per) * float(keys.sum())
+
+
+def oracle_step(w, qf, kf, vf, dof, rows):
+    import oracle
+    oracle.attn_fwd_rows(qf, kf, vf, rows, causal=w.causal)
+    if dof is not None:
+        oracle.attn_bwd_dq_rows(qf, kf, vf, dof, rows, causal=w.causal)
+
+
+def cpu_baseline(w, q, k, v, do, budget_s=12.0, seed=0):
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    qf, kf, vf = (inputs.to_f32_numpy(x) for x in (q, k, v))
+    dof = inputs.to_f32_numpy(do) if do is not None else None
+    # Calibrate on a few rows, then size the sample to the budget.
+    n = 2 * cores
+    rows = oracle_sample_rows(w, n, seed)
+    t = time.perf_counter()
+    oracle_step(w, qf, kf, vf, dof, rows)
+    dt = time.perf_counter() - t
+    n = int(max(cores, min(1 << 16, n * max(1.0, budget_s / max(dt, 1e-3)))))
+    rows = oracle_sample_rows(w, n, seed + 1)
+    t = time.perf_counter()
+    oracle_step(w, qf, kf, vf, dof, rows)
+    dt = time.perf_counter() - t
+    fl = oracle_flops(w, rows, dof is not None)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.get_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{n} random query rows (b, h, i) of {w.name}: fp64 forward "
+                      f"definition" + (" + row-local dQ" if dof is not None else "") +
+                      "; useful flops 4*D (+6*D) per visible pair"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = inputs.WORKLOADS[args.workload]
+    q, k, v, do = inputs.generate(w)
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    qf, kf, vf = (inputs.to_f32_numpy(x) for x in (q, k, v))
+    dof = inputs.to_f32_numpy(do) if do is not None else None
+    # Size each step to ~budget seconds of host work.
+    per_step_s = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    rows = oracle_sample_rows(w, 2 * cores, 0)
+    t = time.perf_counter()
+    oracle_step(w, qf, kf, vf, dof, rows)
+    dt = time.perf_counter() - t
+    n = int(max(cores, min(1 << 16, 2 * cores * max(1.0, per_step_s / max(dt, 1e-3)))))
+    for i in range(args.warmup):
+        oracle_step(w, qf, kf, vf, dof, oracle_sample_rows(w, n, 100 + i))
+    total_t, total_f = 0.0, 0.0
+    for i in range(args.steps):
+        rows = oracle_sample_rows(w, n, 1000 + i)
+        t = time.perf_counter()
+        oracle_step(w, qf, kf, vf, dof, rows)
+        total_t += time.perf_counter() - t
+        total_f += oracle_flops(w, rows, dof is not None)
+    value = total_f / total_t / 1e12
+    sample = (f"{n} random query rows (b, h, i) per step of {w.name}: fp64 forward definition"
+              + (" + row-local dQ" if dof is not None else "") +
+              "; useful flops 4*D (+6*D) per visible pair")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "Hkv": w.Hkv,
+                       "D": w.D, "cp": w.cp, "causal": w.causal, "backward": w.backward},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.get_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="c5_bf16_s131072_fwdbwd", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-c3", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

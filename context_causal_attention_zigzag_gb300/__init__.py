@@ -1,1 +1,13 @@
-"""GB300-native context-parallel zigzag causal attention (placeholder, filled below)."""
+"""GB300-native context-parallel zigzag causal attention.
+
+The ring of context-parallel ranks ("Sequence Parallelism IV: Megatron
+Context Parallel and Load-Balanced Rings", sections 3-5) runs on one GPU with
+every virtual rank's shard resident in HBM.  The compute lives in libcpattn
+(C ABI, include/cpattn.h, CUDA kernels for sm_103a); this package is its thin
+Python binding.  ``inputs`` holds the seeded synthetic workloads.
+"""
+from ._binding import (  # noqa: F401
+    BF16, CONTIGUOUS, F32, PATH_SIMT, PATH_TCGEN05, ZIGZAG, CpattnError, attention,
+    attention_fwd_bwd, device_status, lib, lse_merge, plan, ring_bwd,
+    ring_bwd_workspace_bytes, ring_fwd, ring_fwd_census, ring_fwd_step, status_string,
+    tile_counts, zigzag_permute, zigzag_unpermute)

@@ -1,0 +1,308 @@
+"""ctypes binding of libcpattn (include/cpattn.h): argument marshalling only.
+
+Every step of the path runs in the library's CUDA kernels; this module only
+checks tensor dtypes/devices/shapes, allocates outputs with torch (device
+memory plumbing) and passes raw pointers plus the current CUDA stream.  If
+the library has not been built, every call raises: there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcpattn.so")
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_CUDA = -3
+ERR_DEVICE_TIMEOUT = -4
+ERR_WORKSPACE = -5
+
+CONTIGUOUS = 0
+ZIGZAG = 1
+F32 = 0
+BF16 = 1
+PATH_SIMT = 0
+PATH_TCGEN05 = 1
+
+# Every entry point include/cpattn.h declares, with its ctypes signature.
+_vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_ip = ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "cpattn_zigzag_permute": (_i, [_vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
+    "cpattn_zigzag_unpermute": (_i, [_vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
+    "cpattn_ring_fwd": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp]),
+    "cpattn_ring_fwd_census": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp, _vp]),
+    "cpattn_ring_fwd_plan": (_i, [_i] * 9 + [_ip, _ip]),
+    "cpattn_ring_bwd_plan": (_i, [_i] * 9 + [_ip, _ip]),
+    "cpattn_ring_fwd_step": (_i, [_vp, _vp, _vp] + [_i] * 9 + [_f, _i, _vp, _vp, _vp]),
+    "cpattn_lse_merge": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
+    "cpattn_ring_bwd_workspace_bytes": (_sz, [_i] * 6),
+    "cpattn_ring_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _sz, _vp]),
+    "cpattn_tile_counts": (_i, [_i64, _i, _i, _i, _i64, _vp, _vp]),
+    "cpattn_device_status": (_i, [_vp]),
+    "cpattn_status_string": (ctypes.c_char_p, [_i]),
+}
+
+_lib = None
+
+
+class CpattnError(RuntimeError):
+    def __init__(self, fn, code):
+        self.code = code
+        msg = status_string(code) if _lib is not None else str(code)
+        super().__init__(f"{fn} failed: {msg} ({code})")
+
+
+def lib():
+    """Loads libcpattn.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    handle = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = handle
+    return handle
+
+
+def status_string(code: int) -> str:
+    return lib().cpattn_status_string(int(code)).decode()
+
+
+def _check(fn, code):
+    if code != OK:
+        raise CpattnError(fn, code)
+
+
+def _stream(t: torch.Tensor = None):
+    dev = t.device if t is not None else torch.device("cuda", torch.cuda.current_device())
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float32")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensor must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+
+
+def _scale(scale):
+    return 0.0 if scale is None else float(scale)
+
+
+# ---------------------------------------------------------------------------
+# permutation
+# ---------------------------------------------------------------------------
+
+def _perm(name, x, cp, layout, seq_dim, out):
+    _need_cuda(x)
+    if seq_dim < 0:
+        seq_dim += x.dim()
+    outer = 1
+    for s in x.shape[:seq_dim]:
+        outer *= s
+    S = x.shape[seq_dim]
+    inner = x.element_size()
+    for s in x.shape[seq_dim + 1:]:
+        inner *= s
+    if out is None:
+        out = torch.empty_like(x)
+    _need_cuda(out)
+    rc = getattr(lib(), name)(_ptr(x), _ptr(out), outer, S, inner, int(cp), int(layout),
+                              _stream(x))
+    _check(name, rc)
+    return out
+
+
+def zigzag_permute(x, cp, layout=ZIGZAG, seq_dim=1, out=None):
+    """Natural -> sharded order along ``seq_dim`` (see cpattn_zigzag_permute)."""
+    return _perm("cpattn_zigzag_permute", x, cp, layout, seq_dim, out)
+
+
+def zigzag_unpermute(x, cp, layout=ZIGZAG, seq_dim=1, out=None):
+    """Sharded -> natural order along ``seq_dim``."""
+    return _perm("cpattn_zigzag_unpermute", x, cp, layout, seq_dim, out)
+
+
+# ---------------------------------------------------------------------------
+# forward
+# ---------------------------------------------------------------------------
+
+def _shape(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, S, H, D]")
+    B, S, H, D = q.shape
+    if k.shape != v.shape or k.shape[0] != B or k.shape[1] != S or k.shape[3] != D:
+        raise ValueError("k, v must be [B, S, Hkv, D] matching q")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    return B, H, k.shape[2], S, D
+
+
+def ring_fwd(q, k, v, cp, layout=ZIGZAG, causal=True, scale=None, out=None, lse=None,
+             tiles_rt=None):
+    """Ring forward on sharded-order tensors; returns (out, lse)."""
+    _need_cuda(q, k, v)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    _need_cuda(out, lse)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S, D, int(cp),
+            int(layout), int(bool(causal)), _dtype_code(q), _scale(scale)]
+    if tiles_rt is None:
+        rc = lib().cpattn_ring_fwd(*args, _stream(q))
+        _check("cpattn_ring_fwd", rc)
+    else:
+        _need_cuda(tiles_rt)
+        rc = lib().cpattn_ring_fwd_census(*args, _ptr(tiles_rt), _stream(q))
+        _check("cpattn_ring_fwd_census", rc)
+    return out, lse
+
+
+def ring_fwd_census(q, k, v, cp, layout=ZIGZAG, causal=True, scale=None):
+    """Forward plus the kernel's own per-(rank, step) tile counts [cp, cp]."""
+    counts = torch.zeros((cp, cp), device=q.device, dtype=torch.int64)
+    out, lse = ring_fwd(q, k, v, cp, layout, causal, scale, tiles_rt=counts)
+    return out, lse, counts
+
+
+def ring_fwd_step(q, k, v, cp, step, layout=ZIGZAG, causal=True, scale=None, o_part=None,
+                  lse_part=None):
+    """Partial (o_part, lse_part) of one ring step for every rank (float32)."""
+    _need_cuda(q, k, v)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    if o_part is None:
+        o_part = torch.empty((B, S, H, D), device=q.device, dtype=torch.float32)
+    if lse_part is None:
+        lse_part = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    _need_cuda(o_part, lse_part)
+    rc = lib().cpattn_ring_fwd_step(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, S, D, int(cp),
+                                    int(layout), int(bool(causal)), _dtype_code(q),
+                                    _scale(scale), int(step), _ptr(o_part), _ptr(lse_part),
+                                    _stream(q))
+    _check("cpattn_ring_fwd_step", rc)
+    return o_part, lse_part
+
+
+def lse_merge(o_a, lse_a, o_b, lse_b, o_out=None, lse_out=None):
+    """Exact merge of two partials; o_out/lse_out may alias the inputs."""
+    _need_cuda(o_a, lse_a, o_b, lse_b)
+    B, S, H, D = o_a.shape
+    if o_out is None:
+        o_out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    rc = lib().cpattn_lse_merge(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(o_out),
+                                _ptr(lse_out), B, S, H, D, _stream(o_a))
+    _check("cpattn_lse_merge", rc)
+    return o_out, lse_out
+
+
+def plan(B, H, Hkv, S, D, cp, layout, causal, dtype, backward=False):
+    """(path, tile) the library picks for these arguments (host only)."""
+    path, tile = ctypes.c_int(-1), ctypes.c_int(-1)
+    fn = "cpattn_ring_bwd_plan" if backward else "cpattn_ring_fwd_plan"
+    code = dtype if isinstance(dtype, int) else (BF16 if dtype == torch.bfloat16 else F32)
+    rc = getattr(lib(), fn)(B, H, Hkv, S, D, int(cp), int(layout), int(bool(causal)), code,
+                            ctypes.byref(path), ctypes.byref(tile))
+    _check(fn, rc)
+    return path.value, tile.value
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+
+def ring_bwd_workspace_bytes(B, H, Hkv, S, D, dtype=BF16) -> int:
+    return int(lib().cpattn_ring_bwd_workspace_bytes(B, H, Hkv, S, D, int(dtype)))
+
+
+def ring_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
+             dq=None, dk=None, dv=None, workspace=None):
+    """Ring backward on sharded-order tensors; returns (dq, dk, dv)."""
+    _need_cuda(q, k, v, out, dout, lse)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    code = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(dq, dk, dv, workspace)
+    rc = lib().cpattn_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
+                               int(layout), int(bool(causal)), code, _scale(scale),
+                               _ptr(workspace), workspace.numel(), _stream(q))
+    _check("cpattn_ring_bwd", rc)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# census and status
+# ---------------------------------------------------------------------------
+
+def tile_counts(S, cp, layout, causal, tile):
+    """Closed-form (tiles[cp, cp], pairs[cp, cp]) per (batch, head), host only."""
+    import numpy as np
+    tiles = np.zeros(cp * cp, dtype=np.uint64)
+    pairs = np.zeros(cp * cp, dtype=np.uint64)
+    rc = lib().cpattn_tile_counts(int(S), int(cp), int(layout), int(bool(causal)), int(tile),
+                                  tiles.ctypes.data_as(ctypes.c_void_p),
+                                  pairs.ctypes.data_as(ctypes.c_void_p))
+    _check("cpattn_tile_counts", rc)
+    return tiles.reshape(cp, cp), pairs.reshape(cp, cp)
+
+
+def device_status(stream=None):
+    """Synchronises and returns the library status code (0 = OK)."""
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream()
+    return int(lib().cpattn_device_status(s))
+
+
+# ---------------------------------------------------------------------------
+# natural-order conveniences (the whole hot path)
+# ---------------------------------------------------------------------------
+
+def attention(q, k, v, cp, layout=ZIGZAG, causal=True, scale=None):
+    """Natural-order in, natural-order out: permute -> ring forward -> unpermute."""
+    qs = zigzag_permute(q, cp, layout)
+    ks = zigzag_permute(k, cp, layout)
+    vs = zigzag_permute(v, cp, layout)
+    o, lse = ring_fwd(qs, ks, vs, cp, layout, causal, scale)
+    return zigzag_unpermute(o, cp, layout), zigzag_unpermute(lse, cp, layout, seq_dim=2)
+
+
+def attention_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None):
+    """Natural order: forward and backward through the ring.  Returns
+    (out, lse, dq, dk, dv), all natural order."""
+    qs, ks, vs, dos = (zigzag_permute(x, cp, layout) for x in (q, k, v, dout))
+    o, lse = ring_fwd(qs, ks, vs, cp, layout, causal, scale)
+    dq, dk, dv = ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, scale)
+    un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
+    return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dk), un(dv)

@@ -1,0 +1,362 @@
+// C-ABI layer of libcpattn: argument validation, kernel selection, the
+// closed-form work census and the device error word.  Declarations and the
+// meaning of every argument are in include/cpattn.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "cpattn.h"
+#include "cpattn_internal.h"
+
+using namespace cpattn;
+
+namespace {
+
+// One error word per device, written by kernels whose bounded waits give up.
+__device__ int g_device_error;
+
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {nullptr};
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int chunks_per_rank(int layout) { return layout == CPATTN_LAYOUT_ZIGZAG ? 2 : 1; }
+
+// Fills a RingShape; returns CPATTN_OK or CPATTN_ERR_INVALID_ARG.
+int make_shape(int B, int H, int Hkv, int S, int D, int cp, int layout, int causal,
+               float softmax_scale, RingShape* sh) {
+  if (B < 0 || H < 1 || Hkv < 1 || S < 0 || cp < 1) return CPATTN_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return CPATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return CPATTN_ERR_INVALID_ARG;
+  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
+    return CPATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return CPATTN_ERR_INVALID_ARG;
+  const int per = chunks_per_rank(layout);
+  if (S % (cp * per) != 0) return CPATTN_ERR_INVALID_ARG;
+  if (!(softmax_scale <= 0.f) && !isfinite(softmax_scale)) return CPATTN_ERR_INVALID_ARG;
+  sh->B = B;
+  sh->H = H;
+  sh->Hkv = Hkv;
+  sh->S = S;
+  sh->D = D;
+  sh->cp = cp;
+  sh->layout = layout;
+  sh->causal = causal;
+  sh->per_rank = per;
+  sh->L = S / cp;
+  sh->c = sh->L / per;
+  sh->scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
+  sh->scale_log2 = sh->scale * 1.4426950408889634f;
+  return CPATTN_OK;
+}
+
+bool device_is_sm103() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  return major == 10 && minor == 3;
+}
+
+// Tensor-core forward: bf16, D = 128, every chunk a whole number of 256-row
+// query pairs (two 128-row tiles share each K/V tile).
+bool tc_fwd_eligible(const RingShape& sh, int dtype) {
+  return dtype == CPATTN_BF16 && sh.D == 128 && sh.c % (2 * kTcTile) == 0;
+}
+bool tc_bwd_eligible(const RingShape& sh, int dtype) {
+  return dtype == CPATTN_BF16 && sh.D == 128 && sh.c % kTcTile == 0;
+}
+
+int fwd_common(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+               int Hkv, int S, int D, int cp, int layout, int causal, int dtype,
+               float softmax_scale, int t_begin, int t_end, int step_mode,
+               unsigned long long* tiles_rt, cudaStream_t stream) {
+  RingShape sh;
+  int rc = make_shape(B, H, Hkv, S, D, cp, layout, causal, softmax_scale, &sh);
+  if (rc != CPATTN_OK) return rc;
+  if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S == 0) return CPATTN_OK;
+  if (!q || !k || !v || !out || !lse) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return CPATTN_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return CPATTN_ERR_CUDA;
+  FwdArgs a;
+  a.sh = sh;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.t_begin = t_begin;
+  a.t_end = t_end;
+  a.step_mode = step_mode;
+  a.tiles_rt = tiles_rt;
+  a.err = err;
+  cudaError_t e;
+  if (tc_fwd_eligible(sh, dtype) && tc_fwd_available() && device_is_sm103())
+    e = launch_tc_fwd(a, stream);
+  else
+    e = launch_simt_fwd(a, dtype, stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int plan_common(int B, int H, int Hkv, int S, int D, int cp, int layout, int causal, int dtype,
+                bool fwd, int* path, int* tile) {
+  RingShape sh;
+  int rc = make_shape(B, H, Hkv, S, D, cp, layout, causal, 0.f, &sh);
+  if (rc != CPATTN_OK) return rc;
+  if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  bool tc = fwd ? (tc_fwd_eligible(sh, dtype) && tc_fwd_available())
+                : (tc_bwd_eligible(sh, dtype) && tc_bwd_available());
+  if (path) *path = tc ? CPATTN_PATH_TCGEN05 : CPATTN_PATH_SIMT;
+  if (tile) *tile = tc ? kTcTile : kSimtTile;
+  return CPATTN_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" {
+
+int cpattn_zigzag_permute(const void* in, void* out, int64_t outer, int64_t S,
+                          int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream) {
+  if (outer < 0 || S < 0 || inner_bytes < 1 || cp_size < 1) return CPATTN_ERR_INVALID_ARG;
+  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
+    return CPATTN_ERR_INVALID_ARG;
+  const int per = chunks_per_rank(layout);
+  if (S % ((int64_t)cp_size * per) != 0 || S > INT32_MAX) return CPATTN_ERR_INVALID_ARG;
+  if (outer * S == 0) return CPATTN_OK;
+  if (!in || !out) return CPATTN_ERR_INVALID_ARG;
+  const char* a = static_cast<const char*>(in);
+  const char* b = static_cast<const char*>(out);
+  const int64_t bytes = outer * S * inner_bytes;
+  if (a < b + bytes && b < a + bytes) return CPATTN_ERR_INVALID_ARG;
+  RingShape sh;
+  memset(&sh, 0, sizeof(sh));
+  sh.cp = cp_size;
+  sh.per_rank = per;
+  sh.S = (int)S;
+  sh.L = (int)(S / cp_size);
+  sh.c = sh.L / per;
+  cudaError_t e = launch_permute(in, out, outer, S, inner_bytes, sh, false, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int cpattn_zigzag_unpermute(const void* in, void* out, int64_t outer, int64_t S,
+                            int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream) {
+  if (outer < 0 || S < 0 || inner_bytes < 1 || cp_size < 1) return CPATTN_ERR_INVALID_ARG;
+  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
+    return CPATTN_ERR_INVALID_ARG;
+  const int per = chunks_per_rank(layout);
+  if (S % ((int64_t)cp_size * per) != 0 || S > INT32_MAX) return CPATTN_ERR_INVALID_ARG;
+  if (outer * S == 0) return CPATTN_OK;
+  if (!in || !out) return CPATTN_ERR_INVALID_ARG;
+  const char* a = static_cast<const char*>(in);
+  const char* b = static_cast<const char*>(out);
+  const int64_t bytes = outer * S * inner_bytes;
+  if (a < b + bytes && b < a + bytes) return CPATTN_ERR_INVALID_ARG;
+  RingShape sh;
+  memset(&sh, 0, sizeof(sh));
+  sh.cp = cp_size;
+  sh.per_rank = per;
+  sh.S = (int)S;
+  sh.L = (int)(S / cp_size);
+  sh.c = sh.L / per;
+  cudaError_t e = launch_permute(in, out, outer, S, inner_bytes, sh, true, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int cpattn_ring_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                    int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
+                    float softmax_scale, cpattn_stream_t stream) {
+  return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
+                    softmax_scale, 0, cp_size, 0, nullptr, (cudaStream_t)stream);
+}
+
+int cpattn_ring_fwd_census(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                           int causal, int dtype, float softmax_scale,
+                           unsigned long long* tiles_rt, cpattn_stream_t stream) {
+  if (tiles_rt == nullptr) return CPATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
+                    softmax_scale, 0, cp_size, 0, tiles_rt, (cudaStream_t)stream);
+}
+
+int cpattn_ring_fwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                         int causal, int dtype, int* path, int* tile) {
+  return plan_common(B, H, Hkv, S, D, cp_size, layout, causal, dtype, true, path, tile);
+}
+
+int cpattn_ring_bwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                         int causal, int dtype, int* path, int* tile) {
+  return plan_common(B, H, Hkv, S, D, cp_size, layout, causal, dtype, false, path, tile);
+}
+
+int cpattn_ring_fwd_step(const void* q, const void* k, const void* v, int B, int H, int Hkv,
+                         int S, int D, int cp_size, int layout, int causal, int dtype,
+                         float softmax_scale, int step, float* o_part, float* lse_part,
+                         cpattn_stream_t stream) {
+  if (step < 0 || step >= cp_size) return CPATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o_part, lse_part, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
+                    softmax_scale, step, step + 1, 1, nullptr, (cudaStream_t)stream);
+}
+
+int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                     float* o_out, float* lse_out, int B, int S, int H, int D,
+                     cpattn_stream_t stream) {
+  if (B < 0 || S < 0 || H < 0 || (D != 64 && D != 128)) return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S * H == 0) return CPATTN_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !o_out || !lse_out) return CPATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_a) || !aligned16(o_b) || !aligned16(o_out)) return CPATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_lse_merge(o_a, lse_a, o_b, lse_b, o_out, lse_out, B, S, H, D,
+                                   (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, int D, int dtype) {
+  (void)Hkv;
+  (void)dtype;
+  if (B < 0 || H < 0 || S < 0 || D < 0) return 0;
+  size_t dq = (size_t)B * S * H * D * sizeof(float);
+  size_t delta = (size_t)B * H * S * sizeof(float);
+  return align256(dq) + align256(delta);
+}
+
+int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
+                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                    cpattn_stream_t stream) {
+  RingShape sh;
+  int rc = make_shape(B, H, Hkv, S, D, cp_size, layout, causal, softmax_scale, &sh);
+  if (rc != CPATTN_OK) return rc;
+  if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S == 0) return CPATTN_OK;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return CPATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return CPATTN_ERR_INVALID_ARG;
+  const size_t need = cpattn_ring_bwd_workspace_bytes(B, H, Hkv, S, D, dtype);
+  if (workspace == nullptr || workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return CPATTN_ERR_WORKSPACE;
+  int* err = device_error_word();
+  if (err == nullptr) return CPATTN_ERR_CUDA;
+  cudaStream_t st = (cudaStream_t)stream;
+  float* dq_acc = static_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          align256((size_t)B * S * H * D * sizeof(float)));
+  cudaError_t e = launch_bwd_prep(out, dout, delta, dq_acc, B, S, H, D, dtype, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  BwdArgs a;
+  a.sh = sh;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.lse = lse;
+  a.delta = delta;
+  a.dq_acc = dq_acc;
+  a.dk = dk;
+  a.dv = dv;
+  a.err = err;
+  if (tc_bwd_eligible(sh, dtype) && tc_bwd_available() && device_is_sm103())
+    e = launch_tc_bwd(a, st);
+  else
+    e = launch_simt_bwd(a, dtype, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  e = launch_dq_convert(dq_acc, dq, (int64_t)B * S * H * D, dtype, st);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal, int64_t tile,
+                       uint64_t* tiles_rt, uint64_t* pairs_rt) {
+  if (S < 0 || cp_size < 1 || tile < 1) return CPATTN_ERR_INVALID_ARG;
+  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
+    return CPATTN_ERR_INVALID_ARG;
+  const int per = chunks_per_rank(layout);
+  if (S % ((int64_t)cp_size * per) != 0) return CPATTN_ERR_INVALID_ARG;
+  const int64_t c = S / ((int64_t)cp_size * per);
+  if (c % tile != 0) return CPATTN_ERR_INVALID_ARG;
+  const uint64_t n = (uint64_t)(c / tile);
+  const uint64_t cc = (uint64_t)c;
+  // Chunk-pair arithmetic: a key chunk earlier than the query chunk is fully
+  // visible (n^2 tiles, c^2 pairs), the same chunk is a triangle with its
+  // diagonal (n(n+1)/2 tiles, c(c+1)/2 pairs), a later chunk is skipped.
+  for (int r = 0; r < cp_size; ++r) {
+    for (int t = 0; t < cp_size; ++t) {
+      int s = ((r - t) % cp_size + cp_size) % cp_size;
+      uint64_t tiles = 0, pairs = 0;
+      for (int jq = 0; jq < per; ++jq) {
+        int qc = (per == 1 || jq == 0) ? r : 2 * cp_size - 1 - r;
+        for (int jk = 0; jk < per; ++jk) {
+          int kc = (per == 1 || jk == 0) ? s : 2 * cp_size - 1 - s;
+          if (!causal || kc < qc) {
+            tiles += n * n;
+            pairs += cc * cc;
+          } else if (kc == qc) {
+            tiles += n * (n + 1) / 2;
+            pairs += cc * (cc + 1) / 2;
+          }
+        }
+      }
+      if (tiles_rt) tiles_rt[r * cp_size + t] = tiles;
+      if (pairs_rt) pairs_rt[r * cp_size + t] = pairs;
+    }
+  }
+  return CPATTN_OK;
+}
+
+int cpattn_device_status(cpattn_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  int* err = device_error_word();
+  if (err == nullptr) return CPATTN_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  if (host != 0) {
+    int zero = 0;
+    if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return CPATTN_ERR_CUDA;
+    return CPATTN_ERR_DEVICE_TIMEOUT;
+  }
+  return CPATTN_OK;
+}
+
+const char* cpattn_status_string(int status) {
+  switch (status) {
+    case CPATTN_OK:
+      return "ok";
+    case CPATTN_ERR_INVALID_ARG:
+      return "invalid argument";
+    case CPATTN_ERR_UNSUPPORTED:
+      return "unsupported";
+    case CPATTN_ERR_CUDA:
+      return "CUDA error";
+    case CPATTN_ERR_DEVICE_TIMEOUT:
+      return "device-side wait timed out";
+    case CPATTN_ERR_WORKSPACE:
+      return "workspace missing or too small";
+    default:
+      return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+// Internal interfaces between the C-ABI layer (cpattn_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cpattn {
+
+// Shape of one ring problem.  Positions are token indices along S.
+struct RingShape {
+  int B, H, Hkv, S, D;
+  int cp;        // context-parallel size (number of virtual ranks)
+  int layout;    // CPATTN_LAYOUT_*
+  int causal;    // 1: key j visible to query i iff natural(j) <= natural(i)
+  int per_rank;  // chunks per rank: 2 (zigzag) or 1 (contiguous)
+  int L;         // tokens per rank, S / cp
+  int c;         // chunk length, L / per_rank
+  float scale;       // softmax scale
+  float scale_log2;  // softmax scale * log2(e): scores are kept in base 2
+};
+
+// Natural position of sharded position p.  Rank r = p / L owns, in order,
+// chunk r and (zigzag only) chunk 2*cp-1-r ("Sequence Parallelism IV",
+// section 3).
+__host__ __device__ inline int natural_pos(const RingShape& s, int p) {
+  if (s.per_rank == 1) return p;
+  int r = p / s.L, w = p - r * s.L;
+  int j = w / s.c, off = w - j * s.c;
+  int chunk = j == 0 ? r : 2 * s.cp - 1 - r;
+  return chunk * s.c + off;
+}
+
+// Natural chunk id of the j-th chunk of rank r.
+__host__ __device__ inline int rank_chunk(const RingShape& s, int r, int j) {
+  return (s.per_rank == 1 || j == 0) ? r : 2 * s.cp - 1 - r;
+}
+
+// Ring source: at step t rank r holds the K/V of rank (r - t) mod cp.
+__host__ __device__ inline int ring_source(int r, int t, int cp) {
+  int s = (r - t) % cp;
+  return s < 0 ? s + cp : s;
+}
+
+struct FwdArgs {
+  RingShape sh;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;     // dtype [B,S,H,D] (full forward) or float32 partial (step mode)
+  float* lse;    // [B,H,S]
+  int t_begin;   // ring steps processed: [t_begin, t_end)
+  int t_end;
+  int step_mode; // 1: out is a float32 partial, empty rows -> (0, -inf)
+  unsigned long long* tiles_rt;  // optional [cp][cp] census (device)
+  int* err;      // device error word
+};
+
+struct BwdArgs {
+  RingShape sh;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* dout;
+  const float* lse;    // [B,H,S]
+  const float* delta;  // [B,H,S], dout . out
+  float* dq_acc;       // [B,S,H,D] float32, pre-zeroed, scaled by softmax scale
+  void* dk;            // [B,S,Hkv,D] dtype
+  void* dv;            // [B,S,Hkv,D] dtype
+  int* err;
+};
+
+// Kernel launchers; each returns the launch error (cudaSuccess if queued).
+cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t S,
+                           int64_t inner_bytes, const RingShape& sh, bool inverse,
+                           cudaStream_t stream);
+cudaError_t launch_simt_fwd(const FwdArgs& a, int dtype, cudaStream_t stream);
+cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_b,
+                             const float* l_b, float* o, float* l, int B, int S, int H, int D,
+                             cudaStream_t stream);
+cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, float* dq_acc,
+                            int B, int S, int H, int D, int dtype, cudaStream_t stream);
+cudaError_t launch_simt_bwd(const BwdArgs& a, int dtype, cudaStream_t stream);
+cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t n, int dtype,
+                              cudaStream_t stream);
+
+// Whether this build carries the tensor-core kernels.
+bool tc_fwd_available();
+bool tc_bwd_available();
+
+// Tile edges of the kernels (tokens).
+constexpr int kSimtTile = 64;
+constexpr int kTcTile = 128;
+
+}  // namespace cpattn

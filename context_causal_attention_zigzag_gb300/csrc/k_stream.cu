@@ -1,0 +1,293 @@
+// Bandwidth-bound kernels of the ring: zigzag permute / unpermute, the exact
+// LSE merge of two partials, the backward pre-pass (Delta = dO . O and dQ
+// accumulator zeroing) and the dQ float32 -> dtype conversion.
+//
+// All of them move data in 16-byte vectors with consecutive threads on
+// consecutive vectors, and size their grids as a multiple of the SM count.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpattn_internal.h"
+
+namespace cpattn {
+namespace {
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n > 0 ? n : 148;
+}
+
+int grid_for(int64_t work_items, int threads, int per_sm) {
+  int64_t want = (work_items + threads - 1) / threads;
+  int64_t cap = (int64_t)sm_count() * per_sm;
+  if (want > cap) want = cap;
+  return (int)(want < 1 ? 1 : want);
+}
+
+// ---------------------------------------------------------------------------
+// Permute.  A tensor [outer, S, inner] moves as outer * nchunk runs of
+// c * inner contiguous bytes (a chunk keeps its internal order), so the copy
+// is a gather of runs: run (o, sharded chunk ci) <-> (o, natural chunk nc).
+// ---------------------------------------------------------------------------
+template <typename V>
+__global__ void __launch_bounds__(256) permute_runs_kernel(const char* __restrict__ in,
+                                                           char* __restrict__ out,
+                                                           int64_t outer, int64_t S,
+                                                           int64_t inner_bytes, int cp,
+                                                           int per_rank, int64_t c,
+                                                           int64_t run_vecs, bool inverse) {
+  const int64_t nchunk = (int64_t)cp * per_rank;
+  const int64_t total = outer * nchunk * run_vecs;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  constexpr int U = 4;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < total;
+       base += stride * U) {
+    V val[U];
+    int64_t dst[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int64_t idx = base + u * stride;
+      dst[u] = -1;
+      if (idx < total) {
+        int64_t e = idx % run_vecs;
+        int64_t rc = idx / run_vecs;
+        int64_t ci = rc % nchunk;  // sharded chunk index
+        int64_t o = rc / nchunk;
+        int r = (int)(ci / per_rank), j = (int)(ci % per_rank);
+        int64_t nc = (per_rank == 1 || j == 0) ? r : 2 * cp - 1 - r;  // natural chunk
+        int64_t sh_off = (o * S + ci * c) * inner_bytes + e * (int64_t)sizeof(V);
+        int64_t nat_off = (o * S + nc * c) * inner_bytes + e * (int64_t)sizeof(V);
+        int64_t src = inverse ? sh_off : nat_off;
+        dst[u] = inverse ? nat_off : sh_off;
+        val[u] = *reinterpret_cast<const V*>(in + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u] >= 0) *reinterpret_cast<V*>(out + dst[u]) = val[u];
+  }
+}
+
+template <typename V>
+cudaError_t permute_as(const void* in, void* out, int64_t outer, int64_t S, int64_t inner_bytes,
+                       const RingShape& sh, bool inverse, cudaStream_t stream) {
+  int64_t run_bytes = (int64_t)sh.c * inner_bytes;
+  int64_t run_vecs = run_bytes / (int64_t)sizeof(V);
+  int64_t total = outer * (int64_t)sh.cp * sh.per_rank * run_vecs;
+  if (total == 0) return cudaSuccess;
+  int grid = grid_for((total + 3) / 4, 256, 8);
+  permute_runs_kernel<V><<<grid, 256, 0, stream>>>(
+      static_cast<const char*>(in), static_cast<char*>(out), outer, S, inner_bytes, sh.cp,
+      sh.per_rank, (int64_t)sh.c, run_vecs, inverse);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// LSE merge: one warp per row (b, s, h); each lane moves float4s.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const float* o_a, const float* l_a,
+                                                        const float* o_b, const float* l_b,
+                                                        float* o, float* l, int B, int S, int H) {
+  constexpr int VPR = D / 4;  // float4 per row
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)B * S * H;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t row = warp0; row < rows; row += nwarps) {
+    int64_t b = row / ((int64_t)S * H);
+    int64_t s = (row / H) % S;
+    int64_t h = row % H;
+    int64_t li = (b * H + h) * S + s;
+    float la = l_a[li], lb = l_b[li];
+    float hi = fmaxf(la, lb), lo = fminf(la, lb);
+    float L, wa, wb;
+    if (hi == -INFINITY) {
+      L = -INFINITY;
+      wa = 0.f;
+      wb = 0.f;
+    } else {
+      L = hi + log1pf(expf(lo - hi));
+      wa = expf(la - L);
+      wb = expf(lb - L);
+    }
+    float4 va[(VPR + 31) / 32], vb[(VPR + 31) / 32];
+#pragma unroll
+    for (int u = 0; u * 32 < VPR; ++u) {
+      int e = lane + u * 32;
+      if (e < VPR) {
+        va[u] = reinterpret_cast<const float4*>(o_a + row * D)[e];
+        vb[u] = reinterpret_cast<const float4*>(o_b + row * D)[e];
+      }
+    }
+    __syncwarp();  // every lane has read before any lane writes (in-place merge)
+#pragma unroll
+    for (int u = 0; u * 32 < VPR; ++u) {
+      int e = lane + u * 32;
+      if (e < VPR) {
+        float4 r;
+        r.x = wa * va[u].x + wb * vb[u].x;
+        r.y = wa * va[u].y + wb * vb[u].y;
+        r.z = wa * va[u].z + wb * vb[u].z;
+        r.w = wa * va[u].w + wb * vb[u].w;
+        reinterpret_cast<float4*>(o + row * D)[e] = r;
+      }
+    }
+    if (lane == 0) l[li] = L;
+    __syncwarp();
+  }
+}
+
+// Loads N consecutive elements of T (N * sizeof(T) in {4, 8, 16} bytes, aligned)
+// as one vector and widens them to float.
+template <typename T, int N>
+__device__ __forceinline__ void load_vec(const T* p, float* f) {
+  if constexpr (sizeof(T) == 4) {
+    if constexpr (N == 4) {
+      float4 x = *reinterpret_cast<const float4*>(p);
+      f[0] = x.x; f[1] = x.y; f[2] = x.z; f[3] = x.w;
+    } else {
+      float2 x = *reinterpret_cast<const float2*>(p);
+      f[0] = x.x; f[1] = x.y;
+    }
+  } else {
+    if constexpr (N == 4) {
+      uint2 x = *reinterpret_cast<const uint2*>(p);
+      float2 lo = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x.x));
+      float2 hi = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x.y));
+      f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
+    } else {
+      uint32_t x = *reinterpret_cast<const uint32_t*>(p);
+      float2 lo = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&x));
+      f[0] = lo.x; f[1] = lo.y;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Backward pre-pass: delta[b,h,s] = sum_d dout * out (fp32), and zero the
+// float32 dQ accumulator row.  One warp per row.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out,
+                                                       const T* __restrict__ dout,
+                                                       float* __restrict__ delta,
+                                                       float* __restrict__ dq_acc, int B, int S,
+                                                       int H) {
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = (int64_t)B * S * H;
+  const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  constexpr int EPL = D / 32;  // elements per lane: one 4-, 8- or 16-byte vector
+  for (int64_t row = warp0; row < rows; row += nwarps) {
+    float a[EPL], b[EPL];
+    load_vec<T, EPL>(out + row * D + lane * EPL, a);
+    load_vec<T, EPL>(dout + row * D + lane * EPL, b);
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc = fmaf(a[e], b[e], acc);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    float* dq = dq_acc + row * D + lane * EPL;
+    if constexpr (EPL == 4) {
+      *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+    }
+    if (lane == 0) {
+      int64_t bi = row / ((int64_t)S * H), si = (row / H) % S, hi = row % H;
+      delta[(bi * H + hi) * S + si] = acc;
+    }
+  }
+}
+
+// dq[i] = (dtype) dq_acc[i], 4 elements per thread-iteration.
+__global__ void __launch_bounds__(256) dq_convert_bf16_kernel(const float4* __restrict__ in,
+                                                              __nv_bfloat162* __restrict__ out,
+                                                              int64_t n4) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    float4 x = in[i];
+    out[2 * i] = __floats2bfloat162_rn(x.x, x.y);
+    out[2 * i + 1] = __floats2bfloat162_rn(x.z, x.w);
+  }
+}
+
+__global__ void __launch_bounds__(256) dq_convert_f32_kernel(const float4* __restrict__ in,
+                                                             float4* __restrict__ out,
+                                                             int64_t n4) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = in[i];
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t S,
+                           int64_t inner_bytes, const RingShape& sh, bool inverse,
+                           cudaStream_t stream) {
+  int64_t run_bytes = (int64_t)sh.c * inner_bytes;
+  uintptr_t a = reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out);
+  // Every run starts at a multiple of run_bytes from the base pointers.
+  uint64_t align = (uint64_t)a | (uint64_t)run_bytes;
+  if ((align & 15) == 0) return permute_as<uint4>(in, out, outer, S, inner_bytes, sh, inverse, stream);
+  if ((align & 7) == 0) return permute_as<uint2>(in, out, outer, S, inner_bytes, sh, inverse, stream);
+  if ((align & 3) == 0) return permute_as<uint32_t>(in, out, outer, S, inner_bytes, sh, inverse, stream);
+  if ((align & 1) == 0) return permute_as<uint16_t>(in, out, outer, S, inner_bytes, sh, inverse, stream);
+  return permute_as<uint8_t>(in, out, outer, S, inner_bytes, sh, inverse, stream);
+}
+
+cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_b,
+                             const float* l_b, float* o, float* l, int B, int S, int H, int D,
+                             cudaStream_t stream) {
+  int64_t rows = (int64_t)B * S * H;
+  if (rows == 0) return cudaSuccess;
+  int grid = grid_for(rows * 32, 256, 8);
+  if (D == 128)
+    lse_merge_kernel<128><<<grid, 256, 0, stream>>>(o_a, l_a, o_b, l_b, o, l, B, S, H);
+  else
+    lse_merge_kernel<64><<<grid, 256, 0, stream>>>(o_a, l_a, o_b, l_b, o, l, B, S, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, float* dq_acc,
+                            int B, int S, int H, int D, int dtype, cudaStream_t stream) {
+  int64_t rows = (int64_t)B * S * H;
+  if (rows == 0) return cudaSuccess;
+  int grid = grid_for(rows * 32, 256, 8);
+  if (dtype == 1) {
+    auto o = static_cast<const __nv_bfloat16*>(out);
+    auto d = static_cast<const __nv_bfloat16*>(dout);
+    if (D == 128)
+      bwd_prep_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+    else
+      bwd_prep_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+  } else {
+    auto o = static_cast<const float*>(out);
+    auto d = static_cast<const float*>(dout);
+    if (D == 128)
+      bwd_prep_kernel<float, 128><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+    else
+      bwd_prep_kernel<float, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t n, int dtype,
+                              cudaStream_t stream) {
+  int64_t n4 = n / 4;  // n = B*S*H*D with D a multiple of 64
+  if (n4 == 0) return cudaSuccess;
+  int grid = grid_for(n4, 256, 8);
+  if (dtype == 1)
+    dq_convert_bf16_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                     static_cast<__nv_bfloat162*>(dq), n4);
+  else
+    dq_convert_f32_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                    static_cast<float4*>(dq), n4);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

@@ -1,0 +1,206 @@
+/*
+ * cpattn.h -- C ABI of libcpattn: context-parallel blockwise causal attention
+ * with the zigzag (load-balanced) layout, run on ONE GPU with the cp_size
+ * context-parallel ranks held as logical shards of that device's memory.
+ *
+ * What is computed, and where it is defined:
+ *   "Sequence Parallelism IV: Megatron Context Parallel and Load-Balanced
+ *   Rings" (section 3: the sequence is cut into 2*cp_size chunks and rank r
+ *   owns chunks r and 2*cp_size-1-r; section 4: local Q stays, K/V blocks
+ *   move around the ring, each arriving block gives a partial output and the
+ *   online-softmax state keeps the result exact, causal sub-blocks that are
+ *   entirely in the future are skipped; section 5: softmax-state correction
+ *   per ring step), and "Context Parallelism for Long-Context Training"
+ *   (section "Prove attention equivalence": the result, and its gradients,
+ *   equal unsharded attention).
+ *
+ * Conventions shared by every call
+ *   - Tensors are row-major.  Q, O, dQ, dO: [B, S, H, D]; K, V, dK, dV:
+ *     [B, S, Hkv, D]; LSE: [B, H, S] float32, natural log of the softmax
+ *     normaliser including the scale.  Query head h reads kv head
+ *     h / (H / Hkv).
+ *   - Attention calls take tensors in SHARDED order along S: the shards of
+ *     ranks 0..cp_size-1 one after another.  With CPATTN_LAYOUT_ZIGZAG rank r's
+ *     shard is [chunk r, chunk 2*cp_size-1-r] (chunk length S / (2*cp_size));
+ *     with CPATTN_LAYOUT_CONTIGUOUS rank r's shard is chunk r (length
+ *     S / cp_size), i.e. sharded order equals natural order.  The causal mask
+ *     is always taken on natural positions (key j is visible to query i iff
+ *     j <= i).  cpattn_zigzag_permute / _unpermute convert between orders.
+ *   - Ring: at step t = 0..cp_size-1 rank r holds the K/V shard of rank
+ *     (r - t) mod cp_size.
+ *   - Every pointer marked "device" must be device memory of the current
+ *     device; the caller owns every buffer.  The library allocates nothing
+ *     per call; it holds one static device error word per device.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream)
+ *     unless stated.  Arguments are validated before anything is launched; a
+ *     call that returns an error launched nothing.
+ *   - dtype CPATTN_F32: float32 inputs/outputs, computed with fp32 FMA.
+ *     dtype CPATTN_BF16: bf16 inputs/outputs, fp32 accumulation (tensor
+ *     cores on sm_103a when D == 128 and every chunk is a multiple of 256
+ *     tokens; otherwise the fp32 CUDA-core kernels).
+ *   - softmax_scale <= 0 selects 1/sqrt(D).
+ */
+#ifndef CPATTN_H
+#define CPATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define CPATTN_API __attribute__((visibility("default")))
+#else
+#define CPATTN_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* cpattn_stream_t;
+
+enum cpattn_status_code {
+  CPATTN_OK = 0,
+  CPATTN_ERR_INVALID_ARG = -1,    /* shape, pointer, alignment or enum out of range */
+  CPATTN_ERR_UNSUPPORTED = -2,    /* valid request this build cannot run (e.g. no sm_103 device) */
+  CPATTN_ERR_CUDA = -3,           /* a CUDA runtime call or launch failed */
+  CPATTN_ERR_DEVICE_TIMEOUT = -4, /* a bounded device-side wait gave up (reported by cpattn_device_status) */
+  CPATTN_ERR_WORKSPACE = -5       /* workspace missing or smaller than required */
+};
+
+enum cpattn_layout { CPATTN_LAYOUT_CONTIGUOUS = 0, CPATTN_LAYOUT_ZIGZAG = 1 };
+enum cpattn_dtype { CPATTN_F32 = 0, CPATTN_BF16 = 1 };
+enum cpattn_path { CPATTN_PATH_SIMT = 0, CPATTN_PATH_TCGEN05 = 1 };
+
+/*
+ * Reorders a tensor along its sequence axis.  The tensor is viewed as
+ * [outer, S, inner_bytes] bytes (Q: outer = B, inner_bytes = H*D*elt; LSE:
+ * outer = B*H, inner_bytes = 4).
+ *   permute:   out[o, p, :] = in[o, natural(p), :]   (natural -> sharded)
+ *   unpermute: out[o, natural(p), :] = in[o, p, :]   (sharded -> natural)
+ * where natural(p) is the natural position of sharded position p
+ * ("Sequence Parallelism IV ...", section 3).  in, out: device, must not
+ * overlap.  Requires S % (2*cp_size) == 0 (zigzag) or S % cp_size == 0
+ * (contiguous).  Bytes move in 16-byte vectors when alignment allows.
+ */
+CPATTN_API int cpattn_zigzag_permute(const void* in, void* out, int64_t outer, int64_t S,
+                          int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream);
+CPATTN_API int cpattn_zigzag_unpermute(const void* in, void* out, int64_t outer, int64_t S,
+                            int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream);
+
+/*
+ * Ring forward ("Sequence Parallelism IV ...", sections 4-5): for every
+ * virtual rank r, its query shard attends to the K/V shards arriving at ring
+ * steps t = 0..cp_size-1; tiles wholly in the causal future are skipped,
+ * diagonal tiles are masked, and the online-softmax correction merges the
+ * steps exactly.
+ *   q [B,S,H,D], k/v [B,S,Hkv,D] (device, sharded order, dtype);
+ *   out [B,S,H,D] (device, dtype) receives softmax(QK^T*scale) V;
+ *   lse [B,H,S] (device, float32) receives the natural-log normaliser.
+ * Requires H % Hkv == 0, D in {64, 128}, cp_size >= 1, the S divisibility
+ * above, and 16-byte aligned q/k/v/out.
+ */
+CPATTN_API int cpattn_ring_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                    int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
+                    float softmax_scale, cpattn_stream_t stream);
+
+/*
+ * Same computation, and additionally adds to tiles_rt[r * cp_size + t]
+ * (device, uint64, caller zeroes it) the number of (query tile, key tile)
+ * pairs the kernel actually processed for virtual rank r at ring step t,
+ * summed over batch and heads.  The tile edge is the one
+ * cpattn_ring_fwd_plan reports.
+ */
+CPATTN_API int cpattn_ring_fwd_census(const void* q, const void* k, const void* v, void* out, float* lse,
+                           int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                           int causal, int dtype, float softmax_scale,
+                           unsigned long long* tiles_rt, cpattn_stream_t stream);
+
+/*
+ * Which kernel cpattn_ring_fwd / cpattn_ring_bwd would run for these
+ * arguments (host only, no GPU work): *path is a cpattn_path, *tile the tile
+ * edge in tokens.  Either output pointer may be NULL.
+ */
+CPATTN_API int cpattn_ring_fwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                         int causal, int dtype, int* path, int* tile);
+CPATTN_API int cpattn_ring_bwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                         int causal, int dtype, int* path, int* tile);
+
+/*
+ * One ring step as its own partial ("each arriving K/V block gives a partial
+ * output", section 4): for every rank r, the normalised partial attention of
+ * r's queries over the K/V shard of rank (r - step) mod cp_size only.
+ *   o_part [B,S,H,D] float32 (device), lse_part [B,H,S] float32 (device);
+ *   a row with no visible key gets o = 0 and lse = -inf.
+ * Merging the cp_size partials with cpattn_lse_merge gives cpattn_ring_fwd.
+ */
+CPATTN_API int cpattn_ring_fwd_step(const void* q, const void* k, const void* v, int B, int H, int Hkv,
+                         int S, int D, int cp_size, int layout, int causal, int dtype,
+                         float softmax_scale, int step, float* o_part, float* lse_part,
+                         cpattn_stream_t stream);
+
+/*
+ * Exact merge of two normalised partials (the softmax-state correction,
+ * section 5):  L = log(e^La + e^Lb),  O = e^(La-L) O_a + e^(Lb-L) O_b,
+ * with (0, -inf) as the neutral element.
+ *   o_a, o_b, o_out: [B,S,H,D] float32 (device); lse_a, lse_b, lse_out:
+ *   [B,H,S] float32 (device).  o_out may alias o_a or o_b and lse_out may
+ *   alias lse_a or lse_b (in-place merge); other overlaps are not allowed.
+ * Requires D in {64, 128} and 16-byte aligned O pointers.
+ */
+CPATTN_API int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                     float* o_out, float* lse_out, int B, int S, int H, int D,
+                     cpattn_stream_t stream);
+
+/* Device workspace cpattn_ring_bwd needs, in bytes (host only). */
+CPATTN_API size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, int D, int dtype);
+
+/*
+ * Ring backward (gradients through the ring, "Context Parallelism for
+ * Long-Context Training", section "Prove attention equivalence"): from the
+ * saved out and lse of cpattn_ring_fwd and the upstream gradient dout,
+ *   Delta_i = dout_i . out_i,  P_ij = exp(s_ij - lse_i),
+ *   dS_ij = P_ij (dout_i . v_j - Delta_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,
+ *   dv_j = sum_i P_ij dout_i  (dk, dv summed over the heads sharing kv head j).
+ * The K/V tiles of source rank s visit ranks (s + t) mod cp_size, t =
+ * 0..cp_size-1, in the ring's order.
+ *   q, out, dout, dq: [B,S,H,D]; k, v, dk, dv: [B,S,Hkv,D]; lse [B,H,S]
+ *   float32; all device, sharded order, dtype (lse float32).
+ *   workspace: device, at least cpattn_ring_bwd_workspace_bytes, 256-byte
+ *   aligned; its contents are scratch (no state kept between calls).
+ */
+CPATTN_API int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
+                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                    cpattn_stream_t stream);
+
+/*
+ * Closed-form work census of the ring (host only): for every rank r and
+ * step t, the number of tile x tile blocks with at least one visible
+ * (query, key) pair, tiles_rt[r*cp_size + t], and the number of visible
+ * pairs, pairs_rt[r*cp_size + t], per (batch, head).  Either output may be
+ * NULL.  Requires the chunk length to be a multiple of `tile`.
+ * ("Sequence Parallelism IV ...", sections 3-4: the per-iteration balance
+ * the zigzag layout is built for.)
+ */
+CPATTN_API int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal, int64_t tile,
+                       uint64_t* tiles_rt, uint64_t* pairs_rt);
+
+/*
+ * Waits for `stream`, then reads and clears this device's error word.
+ * Returns CPATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since
+ * the last call, CPATTN_ERR_CUDA if the stream reports a CUDA error, else
+ * CPATTN_OK.  Synchronous.
+ */
+CPATTN_API int cpattn_device_status(cpattn_stream_t stream);
+
+/* Static description of a status code (never NULL). */
+CPATTN_API const char* cpattn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CPATTN_H */

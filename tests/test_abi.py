@@ -1,0 +1,127 @@
+"""Host-side checks of libcpattn that need no GPU: the library loads, exports
+every entry point include/cpattn.h declares, validates arguments before any
+launch, and its closed-form work census equals the oracle's enumeration."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import context_causal_attention_zigzag_gb300 as cp_attn
+from context_causal_attention_zigzag_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cpattn.h")
+
+
+def declared_entry_points():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CPATTN_API\s+[\w\s\*]*?\b(cpattn_\w+)\s*\(", text)))
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    names = declared_entry_points()
+    assert len(names) >= 13
+    lib = cp_attn.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _binding.SIGNATURES, f"{n} has no ctypes signature"
+    assert set(_binding.SIGNATURES) == set(names)
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(cp_attn.status_string(code), str)
+    assert cp_attn.status_string(-4) != cp_attn.status_string(-3)
+
+
+@pytest.mark.parametrize("layout", [oracle.ZIGZAG, oracle.CONTIGUOUS])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_census_closed_form_equals_enumeration(layout, causal):
+    for cp in (1, 2, 3, 4, 8, 16):
+        for T in (1, 4, 64):
+            for n in (1, 2, 5):
+                per = 2 if layout == oracle.ZIGZAG else 1
+                S = cp * per * n * T
+                tiles, pairs = cp_attn.tile_counts(S, cp, layout, causal, T)
+                want_pairs = S <= 4096
+                ot, op = oracle.tile_counts(S, cp, layout, causal, T, pairs=want_pairs)
+                np.testing.assert_array_equal(tiles, ot)
+                if want_pairs:
+                    np.testing.assert_array_equal(pairs, op)
+                if causal:
+                    assert int(pairs.sum()) == S * (S + 1) // 2
+                else:
+                    assert int(pairs.sum()) == S * S
+
+
+def test_tile_census_full_size_workloads():
+    # The per-step tile table at T = 128 for the named workloads, closed form
+    # vs enumeration, and the zigzag balance (max/mean per step == 1).
+    cases = [(8192, 4, oracle.ZIGZAG, True), (8192, 4, oracle.CONTIGUOUS, True),
+             (32768, 8, oracle.ZIGZAG, True), (16384, 4, oracle.CONTIGUOUS, False),
+             (131072, 16, oracle.ZIGZAG, True)]
+    for S, cp, layout, causal in cases:
+        tiles, _ = cp_attn.tile_counts(S, cp, layout, causal, 128)
+        ot, _ = oracle.tile_counts(S, cp, layout, causal, 128)
+        np.testing.assert_array_equal(tiles, ot)
+        if layout == oracle.ZIGZAG:
+            per_step = tiles.astype(np.float64)
+            assert np.all(per_step.max(axis=0) == per_step.mean(axis=0))
+
+
+def test_plan():
+    path, tile = cp_attn.plan(1, 2, 2, 256, 64, 2, cp_attn.ZIGZAG, True, cp_attn.F32)
+    assert path == cp_attn.PATH_SIMT and tile == 64
+    for w in [(1, 32, 32, 8192, 128, 4), (2, 32, 8, 32768, 128, 8), (1, 32, 8, 131072, 128, 16)]:
+        path, tile = cp_attn.plan(*w, cp_attn.ZIGZAG, True, cp_attn.BF16)
+        assert path in (cp_attn.PATH_SIMT, cp_attn.PATH_TCGEN05)
+        assert tile == (128 if path == cp_attn.PATH_TCGEN05 else 64)
+
+
+def test_invalid_arguments_rejected_before_launch():
+    lib = cp_attn.lib()
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+    E = _binding.ERR_INVALID_ARG
+    fwd = lib.cpattn_ring_fwd
+    # (B, H, Hkv, S, D, cp, layout, causal, dtype)
+    good = [1, 4, 2, 64, 64, 2, 1, 1, 1]
+    bad_cases = [
+        [1, 4, 3, 64, 64, 2, 1, 1, 1],   # H % Hkv
+        [1, 4, 2, 60, 64, 4, 1, 1, 1],   # S % (2 cp)
+        [1, 4, 2, 64, 96, 2, 1, 1, 1],   # D
+        [1, 4, 2, 64, 64, 0, 1, 1, 1],   # cp
+        [1, 4, 2, 64, 64, 2, 7, 1, 1],   # layout
+        [1, 4, 2, 64, 64, 2, 1, 1, 9],   # dtype
+        [-1, 4, 2, 64, 64, 2, 1, 1, 1],  # B
+    ]
+    for args in bad_cases:
+        assert fwd(fake, fake, fake, fake, fake, *args, 0.0, null) == E, args
+    # null pointers with a valid shape
+    assert fwd(null, fake, fake, fake, fake, *good, 0.0, null) == E
+    # misaligned pointer
+    assert fwd(ctypes.c_void_p(0x1002), fake, fake, fake, fake, *good, 0.0, null) == E
+    # empty problem is a no-op success
+    assert fwd(null, null, null, null, null, 0, 4, 2, 64, 64, 2, 1, 1, 1, 0.0, null) == 0
+    # ring step out of range
+    assert lib.cpattn_ring_fwd_step(fake, fake, fake, *good, 0.0, 2, fake, fake, null) == E
+    # permute: bad S, overlap
+    assert lib.cpattn_zigzag_permute(fake, ctypes.c_void_p(0x9000), 1, 60, 16, 4, 1, null) == E
+    assert lib.cpattn_zigzag_permute(fake, ctypes.c_void_p(0x1010), 1, 64, 16, 4, 1, null) == E
+    # merge: D
+    assert lib.cpattn_lse_merge(fake, fake, fake, fake, fake, fake, 1, 8, 2, 32, null) == E
+    # backward: workspace too small / missing
+    need = lib.cpattn_ring_bwd_workspace_bytes(1, 4, 2, 64, 64, 1)
+    assert need >= 4 * 64 * 4 * 64
+    args9 = [fake] * 9
+    assert lib.cpattn_ring_bwd(*args9, *good, 0.0, null, need, null) == _binding.ERR_WORKSPACE
+    assert lib.cpattn_ring_bwd(*args9, *good, 0.0, fake, need - 1, null) == _binding.ERR_WORKSPACE
+    assert lib.cpattn_ring_bwd(*args9, *[1, 4, 3] + good[3:], 0.0, fake, need, null) == E
+    # census needs its output
+    assert lib.cpattn_ring_fwd_census(fake, fake, fake, fake, fake, *good, 0.0, null, null) == E
+    # closed-form census: chunk length not a multiple of the tile
+    arr = (ctypes.c_uint64 * 16)()
+    assert lib.cpattn_tile_counts(96, 4, 1, 1, 8, arr, None) == E

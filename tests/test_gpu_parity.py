@@ -1,0 +1,402 @@
+"""GPU parity: libcpattn (through its C ABI) against the fp64 CPU oracle.
+
+Bars (element-wise, max abs error, GPU outputs upcast to fp64):
+  * permutation and tile census: bit-exact;
+  * float32 inputs: O <= 1e-4, LSE <= 1e-5 (gradients: 1e-4);
+  * bf16 inputs, fp32 accumulation: O, dQ, dK, dV <= 2e-2, LSE <= 1e-3.
+Small problems are compared in full; the named workloads at full size are
+compared on sampled rows that the oracle evaluates one by one (every chunk's
+first and last row among them), plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import context_causal_attention_zigzag_gb300 as cpa
+from context_causal_attention_zigzag_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: dict(o=1e-4, lse=1e-5, grad=1e-4),
+       torch.bfloat16: dict(o=2e-2, lse=1e-3, grad=2e-2)}
+DEV = "cuda"
+
+
+def make(B, H, Hkv, S, D, cp, layout, causal, dtype, seed, dout=False):
+    w = inputs.Workload("case", B, H, Hkv, S, D, cp, layout, causal, dtype, seed=seed)
+    q, k, v, do = inputs.generate(w, with_dout=dout)
+    return w, q, k, v, do
+
+
+def f32(x):
+    return inputs.to_f32_numpy(x)
+
+
+def maxerr(gpu, ref):
+    g = gpu.detach().to("cpu", torch.float64).numpy() if torch.is_tensor(gpu) else gpu
+    return float(np.max(np.abs(g - ref))) if g.size else 0.0
+
+
+def sharded_pos(S, cp, layout):
+    """pos[i] = sharded position of natural token i (from the oracle's chunker)."""
+    order = oracle.shard_order(S, cp, layout)
+    pos = np.empty_like(order)
+    pos[order] = np.arange(S)
+    return pos
+
+
+# ---------------------------------------------------------------------------
+# permutation
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("layout", [cpa.ZIGZAG, cpa.CONTIGUOUS])
+def test_permute_bit_exact(layout):
+    g = torch.Generator().manual_seed(7)
+    for cp in (1, 2, 3, 4, 8):
+        S = 48
+        if S % (2 * cp if layout == cpa.ZIGZAG else cp):
+            continue
+        order = oracle.shard_order(S, cp, layout)
+        for shape, seq_dim, dtype in [((2, S, 3, 8), 1, torch.float32),
+                                      ((2, S, 3, 8), 1, torch.bfloat16),
+                                      ((2, 3, S), 2, torch.float32),
+                                      ((2, S, 3), 1, torch.uint8),
+                                      ((1, S, 1, 1), 1, torch.bfloat16)]:
+            x = torch.randint(0, 255, shape, generator=g).to(dtype).to(DEV)
+            y = cpa.zigzag_permute(x, cp, layout, seq_dim=seq_dim)
+            idx = torch.as_tensor(order, device=DEV)
+            ref = torch.index_select(x, seq_dim, idx)
+            assert torch.equal(y, ref)
+            z = cpa.zigzag_unpermute(y, cp, layout, seq_dim=seq_dim)
+            assert torch.equal(z, x)
+    assert cpa.device_status() == 0
+
+
+def test_permute_full_size_bit_exact():
+    w = inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"]
+    x = torch.randn((1, w.S, w.Hkv, w.D), device=DEV).to(torch.bfloat16)
+    y = cpa.zigzag_permute(x, w.cp, w.layout)
+    order = torch.as_tensor(oracle.shard_order(w.S, w.cp, w.layout), device=DEV)
+    assert torch.equal(y, x[:, order])
+    lse = torch.randn((1, w.H, w.S), device=DEV)
+    assert torch.equal(cpa.zigzag_unpermute(cpa.zigzag_permute(lse, w.cp, w.layout, seq_dim=2),
+                                            w.cp, w.layout, seq_dim=2), lse)
+
+
+# ---------------------------------------------------------------------------
+# forward, full comparison on problems the oracle finishes in seconds
+# ---------------------------------------------------------------------------
+
+FWD_CASES = [
+    # B, H, Hkv, S, D, cp, layout, causal, dtype
+    (1, 2, 2, 256, 64, 2, cpa.ZIGZAG, True, torch.float32),        # the S=256 fp32 workload
+    (2, 4, 2, 320, 64, 4, cpa.ZIGZAG, True, torch.float32),        # ragged: chunk 40
+    (1, 3, 1, 200, 128, 5, cpa.CONTIGUOUS, True, torch.float32),   # ragged, cp 5
+    (1, 2, 2, 96, 128, 1, cpa.ZIGZAG, False, torch.float32),       # cp 1, non-causal
+    (1, 2, 1, 16, 64, 8, cpa.ZIGZAG, True, torch.float32),         # chunk length 1
+    (2, 4, 2, 384, 64, 3, cpa.ZIGZAG, True, torch.bfloat16),       # bf16, D 64
+    (1, 4, 2, 2048, 128, 4, cpa.ZIGZAG, True, torch.bfloat16),     # chunks of 256
+    (1, 4, 4, 2048, 128, 2, cpa.CONTIGUOUS, True, torch.bfloat16),
+    (1, 2, 1, 2048, 128, 2, cpa.CONTIGUOUS, False, torch.bfloat16),
+    (2, 4, 1, 1536, 128, 3, cpa.ZIGZAG, True, torch.bfloat16),     # cp 3, GQA 4:1
+    (1, 2, 2, 1024, 128, 1, cpa.ZIGZAG, True, torch.bfloat16),     # cp 1
+    (1, 2, 2, 640, 128, 2, cpa.ZIGZAG, True, torch.bfloat16),      # chunk 160 (CUDA cores)
+]
+
+
+@pytest.mark.parametrize("case", FWD_CASES, ids=lambda c: "B{}H{}K{}S{}D{}cp{}L{}c{}{}".format(
+    *c[:8], "f32" if c[8] == torch.float32 else "bf16"))
+def test_forward_matches_oracle(case):
+    B, H, Hkv, S, D, cp, layout, causal, dtype = case
+    w, q, k, v, _ = make(B, H, Hkv, S, D, cp, layout, causal, dtype, seed=2000 + S + cp)
+    out, lse = cpa.attention(q.to(DEV), k.to(DEV), v.to(DEV), cp, layout, causal)
+    ro, rl = oracle.attn_fwd(f32(q), f32(k), f32(v), causal=causal)
+    tol = TOL[dtype]
+    assert maxerr(out, ro) <= tol["o"], maxerr(out, ro)
+    assert maxerr(lse, rl) <= tol["lse"], maxerr(lse, rl)
+    assert cpa.device_status() == 0
+
+
+def test_forward_sharded_order_and_scale():
+    # Direct sharded-order call with a non-default scale and peaky logits.
+    B, H, Hkv, S, D, cp, layout = 1, 2, 1, 1024, 128, 2, cpa.ZIGZAG
+    w, q, k, v, _ = make(B, H, Hkv, S, D, cp, layout, True, torch.bfloat16, seed=77)
+    q = (q.float() * 3).to(torch.bfloat16)
+    scale = 0.2
+    qs, ks, vs = (cpa.zigzag_permute(x.to(DEV), cp, layout) for x in (q, k, v))
+    out, lse = cpa.ring_fwd(qs, ks, vs, cp, layout, True, scale)
+    ro, rl = oracle.attn_fwd(f32(q), f32(k), f32(v), causal=True, scale=scale)
+    pos = sharded_pos(S, cp, layout)
+    assert maxerr(out[:, pos], ro) <= 2e-2
+    assert maxerr(lse[:, :, pos], rl) <= 1e-3
+
+
+def test_empty_problem_is_noop():
+    q = torch.empty((0, 64, 2, 64), device=DEV)
+    out, lse = cpa.ring_fwd(q, q, q, 2)
+    assert out.numel() == 0 and lse.numel() == 0
+    assert cpa.device_status() == 0
+
+
+# ---------------------------------------------------------------------------
+# ring steps as partials, and the merge
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,D,S,cp,layout,causal", [
+    (torch.float32, 64, 256, 4, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 2048, 4, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 2048, 4, cpa.CONTIGUOUS, True),
+    (torch.bfloat16, 128, 1024, 2, cpa.CONTIGUOUS, False),
+])
+def test_step_partials_and_merge(dtype, D, S, cp, layout, causal):
+    B, H, Hkv = 1, 2, 1
+    w, q, k, v, _ = make(B, H, Hkv, S, D, cp, layout, causal, dtype, seed=3000 + S)
+    qs, ks, vs = (cpa.zigzag_permute(x.to(DEV), cp, layout) for x in (q, k, v))
+    pos = sharded_pos(S, cp, layout)
+    tol = TOL[dtype]
+    parts = []
+    for t in range(cp):
+        po, pl = cpa.ring_fwd_step(qs, ks, vs, cp, t, layout, causal)
+        ro, rl = oracle.ring_step(f32(q), f32(k), f32(v), cp, layout, t, causal=causal)
+        po_n, pl_n = po[:, pos].double().cpu().numpy(), pl[:, :, pos].double().cpu().numpy()
+        empty = np.isneginf(rl)
+        assert np.array_equal(np.isneginf(pl_n), empty)
+        assert np.max(np.abs(po_n - ro)) <= tol["o"]
+        assert np.max(np.abs(np.where(empty, 0, pl_n - rl))) <= tol["lse"]
+        parts.append((po, pl))
+    ref_o, ref_l = oracle.attn_fwd(f32(q), f32(k), f32(v), causal=causal)
+    # Left fold, and the reverse order, both in place.
+    for order in (range(cp), reversed(range(cp))):
+        order = list(order)
+        acc_o, acc_l = parts[order[0]][0].clone(), parts[order[0]][1].clone()
+        for t in order[1:]:
+            cpa.lse_merge(acc_o, acc_l, parts[t][0], parts[t][1], acc_o, acc_l)
+        assert maxerr(acc_o[:, pos], ref_o) <= tol["o"]
+        assert maxerr(acc_l[:, :, pos], ref_l) <= tol["lse"]
+    # ... and equal to the one-pass ring forward within the same bar.
+    o1, l1 = cpa.ring_fwd(qs, ks, vs, cp, layout, causal)
+    assert maxerr(o1[:, pos].float(), acc_o[:, pos].double().cpu().numpy()) <= tol["o"]
+
+
+def test_merge_matches_oracle_merge_and_neutral_element():
+    g = torch.Generator().manual_seed(11)
+    B, S, H, D = 2, 33, 3, 128
+    oa, ob = (torch.randn((B, S, H, D), generator=g) for _ in range(2))
+    la, lb = (torch.randn((B, H, S), generator=g) * 4 for _ in range(2))
+    la[0, 0, :5] = -float("inf")
+    lb[0, 0, 3:8] = -float("inf")
+    oa[0, :5, 0] = 0
+    ob[0, 3:8, 0] = 0
+    mo, ml = cpa.lse_merge(oa.to(DEV), la.to(DEV), ob.to(DEV), lb.to(DEV))
+    ro, rl = oracle.lse_merge(oa.double().numpy(), la.double().numpy(), ob.double().numpy(),
+                              lb.double().numpy())
+    assert maxerr(mo, ro) <= 1e-5
+    mln = ml.double().cpu().numpy()
+    assert np.array_equal(np.isneginf(mln), np.isneginf(rl))
+    fin = ~np.isneginf(rl)
+    assert np.max(np.abs(mln[fin] - rl[fin])) <= 1e-5
+
+
+# ---------------------------------------------------------------------------
+# census: the kernel's own tile counts against the closed form and the oracle
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype,D,S,cp,layout,causal", [
+    (torch.float32, 64, 256, 2, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 4096, 4, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 4096, 4, cpa.CONTIGUOUS, True),
+    (torch.bfloat16, 128, 2048, 2, cpa.CONTIGUOUS, False),
+    (torch.bfloat16, 64, 1024, 4, cpa.ZIGZAG, True),
+])
+def test_census_bit_exact(dtype, D, S, cp, layout, causal):
+    B, H, Hkv = 2, 2, 1
+    w, q, k, v, _ = make(B, H, Hkv, S, D, cp, layout, causal, dtype, seed=4000 + S)
+    qs, ks, vs = (cpa.zigzag_permute(x.to(DEV), cp, layout) for x in (q, k, v))
+    _, _, counts = cpa.ring_fwd_census(qs, ks, vs, cp, layout, causal)
+    path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, dtype)
+    closed, _ = cpa.tile_counts(S, cp, layout, causal, tile)
+    enum, _ = oracle.tile_counts(S, cp, layout, causal, tile)
+    got = counts.cpu().numpy().astype(np.uint64)
+    assert np.array_equal(got, closed * (B * H)), (got, closed)
+    assert np.array_equal(closed, enum)
+
+
+# ---------------------------------------------------------------------------
+# backward, full comparison
+# ---------------------------------------------------------------------------
+
+BWD_CASES = [
+    (1, 2, 2, 256, 64, 2, cpa.ZIGZAG, True, torch.float32),
+    (2, 4, 2, 192, 128, 3, cpa.ZIGZAG, True, torch.float32),       # ragged chunk 32
+    (1, 2, 1, 128, 64, 2, cpa.CONTIGUOUS, False, torch.float32),
+    (1, 4, 2, 1024, 128, 4, cpa.ZIGZAG, True, torch.bfloat16),     # chunk 128
+    (1, 4, 1, 2048, 128, 2, cpa.CONTIGUOUS, True, torch.bfloat16),
+    (1, 2, 2, 1024, 128, 2, cpa.ZIGZAG, False, torch.bfloat16),
+    (2, 2, 2, 512, 64, 2, cpa.ZIGZAG, True, torch.bfloat16),       # D 64 (CUDA cores)
+    (1, 2, 1, 768, 128, 3, cpa.ZIGZAG, True, torch.bfloat16),      # chunk 128, cp 3
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "B{}H{}K{}S{}D{}cp{}L{}c{}{}".format(
+    *c[:8], "f32" if c[8] == torch.float32 else "bf16"))
+def test_backward_matches_oracle(case):
+    B, H, Hkv, S, D, cp, layout, causal, dtype = case
+    w, q, k, v, do = make(B, H, Hkv, S, D, cp, layout, causal, dtype, seed=5000 + S, dout=True)
+    out, lse, dq, dk, dv = cpa.attention_fwd_bwd(q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV),
+                                                 cp, layout, causal)
+    rq, rk, rv = oracle.attn_bwd(f32(q), f32(k), f32(v), f32(do), causal=causal)
+    tol = TOL[dtype]["grad"]
+    assert maxerr(dq, rq) <= tol, maxerr(dq, rq)
+    assert maxerr(dk, rk) <= tol, maxerr(dk, rk)
+    assert maxerr(dv, rv) <= tol, maxerr(dv, rv)
+    assert cpa.device_status() == 0
+
+
+def test_backward_workspace_is_scratch():
+    # Two calls with the same workspace (left dirty by the first) agree exactly.
+    B, H, Hkv, S, D, cp = 1, 2, 1, 512, 128, 2
+    w, q, k, v, do = make(B, H, Hkv, S, D, cp, cpa.ZIGZAG, True, torch.bfloat16, 61, dout=True)
+    qs, ks, vs, dos = (cpa.zigzag_permute(x.to(DEV), cp) for x in (q, k, v, do))
+    o, lse = cpa.ring_fwd(qs, ks, vs, cp)
+    ws = torch.full((cpa.ring_bwd_workspace_bytes(B, H, Hkv, S, D),), 255, dtype=torch.uint8,
+                    device=DEV)
+    g1 = cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, workspace=ws)
+    g2 = cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, workspace=ws)
+    for a, b in zip(g1, g2):
+        assert torch.allclose(a.float(), b.float(), atol=2e-2, rtol=0)
+
+
+# ---------------------------------------------------------------------------
+# the named workloads at full size, in the launch configuration of bench.py
+# ---------------------------------------------------------------------------
+
+def sample_rows(w, per_head, seed):
+    """(b, h, i) rows: every chunk's first and last token spread over heads, plus
+    random rows, per_head rows for every (b, h)."""
+    rng = np.random.default_rng(seed)
+    nchunk = w.cp * (2 if w.layout == cpa.ZIGZAG else 1)
+    c = w.S // nchunk
+    edges = sorted({x for ch in range(nchunk) for x in (ch * c, ch * c + c - 1)})
+    rows = []
+    e = 0
+    for b in range(w.B):
+        for h in range(w.H):
+            picks = []
+            for _ in range(per_head // 2):
+                picks.append(edges[e % len(edges)])
+                e += 1
+            picks += rng.integers(0, w.S, per_head - len(picks)).tolist()
+            rows += [(b, h, i) for i in picks]
+    return np.array(rows, dtype=np.int64)
+
+
+def check_rows(w, out, lse, q, k, v, rows):
+    """q, k, v: float32 numpy arrays (natural order)."""
+    ro, rl = oracle.attn_fwd_rows(q, k, v, rows, causal=w.causal)
+    b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
+    go = out[b, i, h].double().cpu().numpy()
+    gl = lse[b, h, i].double().cpu().numpy()
+    tol = TOL[w.dtype]
+    assert np.max(np.abs(go - ro)) <= tol["o"], np.max(np.abs(go - ro))
+    assert np.max(np.abs(gl - rl)) <= tol["lse"], np.max(np.abs(gl - rl))
+
+
+@pytest.mark.parametrize("layout", [cpa.ZIGZAG, cpa.CONTIGUOUS])
+def test_c2_full_size(layout):
+    w = inputs.WORKLOADS["c2_bf16_s8192"].with_(layout=layout)
+    q, k, v, _ = inputs.generate(w)
+    out, lse = cpa.attention(q.to(DEV), k.to(DEV), v.to(DEV), w.cp, w.layout, w.causal)
+    check_rows(w, out, lse, f32(q), f32(k), f32(v), sample_rows(w, 8, 1))
+    assert cpa.device_status() == 0
+
+
+def test_c2_layouts_agree():
+    w = inputs.WORKLOADS["c2_bf16_s8192"]
+    q, k, v, _ = (x.to(DEV) if x is not None else None for x in inputs.generate(w))
+    oz, lz = cpa.attention(q, k, v, w.cp, cpa.ZIGZAG, True)
+    oc, lc = cpa.attention(q, k, v, w.cp, cpa.CONTIGUOUS, True)
+    assert (oz.float() - oc.float()).abs().max().item() <= 2e-2
+    assert (lz - lc).abs().max().item() <= 1e-3
+
+
+def test_c3_full_size():
+    w = inputs.WORKLOADS["c3_bf16_s32768_gqa"]
+    q, k, v, _ = inputs.generate(w)
+    out, lse = cpa.attention(q.to(DEV), k.to(DEV), v.to(DEV), w.cp, w.layout, w.causal)
+    check_rows(w, out, lse, f32(q), f32(k), f32(v), sample_rows(w, 8, 3))
+    assert cpa.device_status() == 0
+
+
+def test_c4_full_size_cp_sweep_and_merge():
+    w = inputs.WORKLOADS["c4_bf16_s16384_bidir"]
+    q, k, v, _ = inputs.generate(w)
+    rows = sample_rows(w, 8, 4)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    q, k, v = f32(q), f32(k), f32(v)
+    ref = None
+    for cp in w.cp_sweep:
+        wc = w.with_(cp=cp)
+        out, lse = cpa.attention(qd, kd, vd, cp, w.layout, w.causal)
+        check_rows(wc, out, lse, q, k, v, rows)
+        if ref is None:
+            ref = (out, lse)
+        else:
+            assert (out.float() - ref[0].float()).abs().max().item() <= 2e-2
+            assert (lse - ref[1]).abs().max().item() <= 1e-3
+        # The literal ring: per-step partials merged with the LSE merge.
+        qs, ks, vs = (cpa.zigzag_permute(x, cp, w.layout) for x in (qd, kd, vd))
+        acc_o, acc_l = cpa.ring_fwd_step(qs, ks, vs, cp, 0, w.layout, w.causal)
+        for t in range(1, cp):
+            po, pl = cpa.ring_fwd_step(qs, ks, vs, cp, t, w.layout, w.causal)
+            cpa.lse_merge(acc_o, acc_l, po, pl, acc_o, acc_l)
+        mo = cpa.zigzag_unpermute(acc_o, cp, w.layout)
+        ml = cpa.zigzag_unpermute(acc_l, cp, w.layout, seq_dim=2)
+        assert (mo - out.float()).abs().max().item() <= 2e-2
+        assert (ml - lse).abs().max().item() <= 1e-3
+        check_rows(wc, mo, ml, q, k, v, rows)
+    assert cpa.device_status() == 0
+
+
+def test_c5_full_size_forward_backward():
+    w = inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"]
+    q, k, v, do = inputs.generate(w)
+    qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
+    out, lse, dq, dk, dv = cpa.attention_fwd_bwd(qd, kd, vd, dod, w.cp, w.layout, w.causal)
+    rows = sample_rows(w, 6, 5)
+    qf, kf, vf = f32(q), f32(k), f32(v)
+    check_rows(w, out, lse, qf, kf, vf, rows)
+    del out, lse
+    # dQ rows are row-local: exact oracle on sampled rows.
+    rdq = oracle.attn_bwd_dq_rows(qf, kf, vf, f32(do), rows, causal=True)
+    gdq = dq[rows[:, 0], rows[:, 2], rows[:, 1]].double().cpu().numpy()
+    assert np.max(np.abs(gdq - rdq)) <= 2e-2, np.max(np.abs(gdq - rdq))
+    # Sum rules at full size: sum_j dV_j = sum over the group's heads of sum_i dO_i,
+    # sum_j dK_j = 0 (per kv head and feature); bf16 rounding of S terms bounds them.
+    grp = w.H // w.Hkv
+    sdv = dv.double().sum(dim=1)[0]                               # [Hkv, D]
+    sdo = dod.double().sum(dim=1)[0].view(w.Hkv, grp, w.D).sum(1)  # [Hkv, D]
+    bound = 4e-3 * np.sqrt(w.S)
+    assert (sdv - sdo).abs().max().item() <= bound
+    assert dk.double().sum(dim=1).abs().max().item() <= bound
+    del dq, dk, dv
+    # dK / dV rows: a second backward with dO zero outside a few query rows, for
+    # which the oracle's sums over queries are exact on those rows alone.
+    nchunk = 2 * w.cp
+    c = w.S // nchunk
+    qrows = np.array(sorted({0, c - 1, c, w.S // 2, w.S // 2 + 1, w.S - c, w.S - 1}
+                            | set(np.random.default_rng(9).integers(0, w.S, 9).tolist())))
+    sparse = torch.zeros_like(do)
+    sparse[:, qrows] = do[:, qrows]
+    sd = sparse.to(DEV)
+    _, _, _, dk2, dv2 = cpa.attention_fwd_bwd(qd, kd, vd, sd, w.cp, w.layout, w.causal)
+    rng = np.random.default_rng(10)
+    kj = sorted(set(qrows.tolist()) | set(rng.integers(0, w.S, 24).tolist()) | {1, c + 1})
+    krows = np.array([(0, g, j) for g in range(w.Hkv) for j in kj], dtype=np.int64)
+    rdk, rdv = oracle.attn_bwd_dkdv_rows_sparse(qf, kf, vf, f32(sparse), qrows, krows,
+                                                causal=True)
+    gdk = dk2[0, krows[:, 2], krows[:, 1]].double().cpu().numpy()
+    gdv = dv2[0, krows[:, 2], krows[:, 1]].double().cpu().numpy()
+    assert np.max(np.abs(gdk - rdk)) <= 2e-2, np.max(np.abs(gdk - rdk))
+    assert np.max(np.abs(gdv - rdv)) <= 2e-2, np.max(np.abs(gdv - rdv))
+    assert cpa.device_status() == 0
