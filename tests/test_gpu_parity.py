@@ -163,7 +163,8 @@ def test_step_partials_and_merge(dtype, D, S, cp, layout, causal):
         empty = np.isneginf(rl)
         assert np.array_equal(np.isneginf(pl_n), empty)
         assert np.max(np.abs(po_n - ro)) <= tol["o"]
-        assert np.max(np.abs(np.where(empty, 0, pl_n - rl))) <= tol["lse"]
+        with np.errstate(invalid="ignore"):
+            assert np.max(np.abs(np.where(empty, 0, pl_n - rl))) <= tol["lse"]
         parts.append((po, pl))
     ref_o, ref_l = oracle.attn_fwd(f32(q), f32(k), f32(v), causal=causal)
     # Left fold, and the reverse order, both in place.
