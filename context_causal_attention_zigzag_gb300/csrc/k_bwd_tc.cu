@@ -1,8 +1,6 @@
-// Placeholder until the tensor-core kernels land.
+// Tensor-core ring backward (not in this build yet: the CUDA-core kernel runs).
 #include "cpattn_internal.h"
 namespace cpattn {
-bool tc_fwd_available() { return false; }
 bool tc_bwd_available() { return false; }
-cudaError_t launch_tc_fwd(const FwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 cudaError_t launch_tc_bwd(const BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 }  // namespace cpattn

@@ -1,0 +1,615 @@
+// Tensor-core ring forward for sm_103a: tcgen05.mma with TMEM accumulators,
+// TMA-staged bf16 tiles, warp-specialised, persistent.
+//
+// The ring ("Sequence Parallelism IV", sections 4-5) on one GPU: every
+// virtual rank's Q/K/V shard sits in HBM; "receiving" the K/V of rank
+// (r - t) mod cp at ring step t is a change of the base row the TMA reads.
+// A work item is 256 query rows of one (batch, head) -- two 128-row tiles of
+// one chunk.  Its CTA streams the K/V tiles of ring steps t = 0..cp-1, skips
+// the tiles wholly in the causal future (never loaded), and keeps the online
+// softmax state; the two tiles on the causal diagonal (the item's own rows)
+// are taken last, masked element-wise.  The rescale of O when the running
+// maximum moves is the softmax-state correction; it is skipped while the
+// maximum grows by less than 2^8, which leaves the result exact because the
+// final normalisation uses the same stale maximum.
+//
+// CTA = 384 threads:
+//   warp 0      TMA producer: Q pair once per item, K and V tiles into a
+//               2-stage ring of 32 KB buffers.
+//   warp 1      TMEM owner and MMA issuer (one thread):
+//               S_i = Q_i K^T  (SS form, 128x128x128, fp32 in TMEM),
+//               O_i += P_i V   (TS form: P read from TMEM, V MN-major).
+//   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1: one thread
+//               per row (TMEM lane), row max / sum in fp32, P -> bf16
+//               written back over S in TMEM, conditional O rescale,
+//               epilogue O / l -> HBM and LSE.
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
+// P_i occupies the first 64 columns of S_i (bf16 pairs).
+// The MMA order per K/V tile j is PV0(j), S0(j+1), PV1(j), S1(j+1): while
+// one softmax warpgroup works on its tile, the tensor core runs the other's.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cpattn_internal.h"
+#include "tc_ptx.cuh"
+
+namespace cpattn {
+namespace {
+
+using namespace tc;
+
+constexpr int kT = 128;                     // tile edge (rows, keys)
+constexpr int kD = 128;                     // head dim
+constexpr int kBoxBytes = kT * 64 * 2;      // [128 rows][64 bf16] = 16 KB
+constexpr int kTileBytes = 2 * kBoxBytes;   // [128 rows][128 bf16] = 32 KB
+constexpr int kStages = 2;
+constexpr int kThreads = 384;
+
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
+constexpr int kOffV = kOffK + kStages * kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kTileBytes;
+// barriers
+constexpr int kBarQFull = 0;
+constexpr int kBarQEmpty = 1;
+constexpr int kBarKFull = 2;
+constexpr int kBarKEmpty = kBarKFull + kStages;
+constexpr int kBarVFull = kBarKEmpty + kStages;
+constexpr int kBarVEmpty = kBarVFull + kStages;
+constexpr int kBarS = kBarVEmpty + kStages;  // [2]
+constexpr int kBarP = kBarS + 2;             // [2]
+constexpr int kBarO = kBarP + 2;             // [2]
+constexpr int kBarDrain = kBarO + 2;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-B alignment
+
+__host__ __device__ constexpr uint32_t col_s(int i) { return 128u * (uint32_t)i; }
+__host__ __device__ constexpr uint32_t col_o(int i) { return 256u + 128u * (uint32_t)i; }
+
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, false, true);
+
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// Flags of one K/V tile for the item's two query tiles.
+constexpr int kUse0 = 1, kUse1 = 2, kDiag0 = 4, kDiag1 = 8;
+
+struct Item {
+  int b, h, g, r, qc, a, qrow;  // qc: natural chunk, a: natural tile of query tile 0
+};
+
+// Work items in order of decreasing cost (natural query position), heads
+// innermost so that the query heads of one kv head run side by side.
+__device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
+  const int BH = sh.B * sh.H;
+  const int npair = sh.S / (2 * kT);
+  const int pr = npair - 1 - idx / BH;
+  const int bh = idx - (idx / BH) * BH;
+  Item it;
+  it.b = bh / sh.H;
+  it.h = bh - it.b * sh.H;
+  it.g = it.h / (sh.H / sh.Hkv);
+  const int nat0 = pr * 2 * kT;
+  it.qc = nat0 / sh.c;
+  const int off = nat0 - it.qc * sh.c;
+  int jq;
+  if (sh.per_rank == 1 || it.qc < sh.cp) {
+    it.r = it.qc;
+    jq = 0;
+  } else {
+    it.r = 2 * sh.cp - 1 - it.qc;
+    jq = 1;
+  }
+  it.qrow = it.r * sh.L + jq * sh.c + off;
+  it.a = nat0 / kT;
+  return it;
+}
+
+// The K/V tiles an item visits, in ring order (step t brings the shard of
+// rank (r - t) mod cp), with the two diagonal tiles deferred to the end.
+struct KvSeq {
+  int cp, per, L, c, ctiles, causal, t_end, r, qc, a, qrow;
+  int t, jj, kt, tail;
+  bool tail_on;
+
+  __device__ __forceinline__ void init(const RingShape& sh, int t_begin, int t_end_,
+                                       const Item& it) {
+    cp = sh.cp;
+    per = sh.per_rank;
+    L = sh.L;
+    c = sh.c;
+    ctiles = sh.c / kT;
+    causal = sh.causal;
+    t_end = t_end_;
+    r = it.r;
+    qc = it.qc;
+    a = it.a;
+    qrow = it.qrow;
+    t = t_begin;
+    jj = 0;
+    kt = 0;
+    tail = 0;
+    tail_on = causal && t_begin == 0;
+  }
+
+  __device__ __forceinline__ bool next(int& kvrow, int& fl, int& step) {
+    while (t < t_end) {
+      const int s = ring_source(r, t, cp);
+      while (jj < per) {
+        const int kc = (per == 1 || jj == 0) ? s : 2 * cp - 1 - s;
+        int lim;
+        if (!causal || kc < qc)
+          lim = ctiles;
+        else if (kc == qc)
+          lim = a - kc * ctiles;  // the tiles before the diagonal
+        else
+          lim = 0;                // wholly in the causal future: skipped
+        if (kt < lim) {
+          kvrow = s * L + jj * c + kt * kT;
+          fl = kUse0 | kUse1;
+          step = t;
+          ++kt;
+          return true;
+        }
+        ++jj;
+        kt = 0;
+      }
+      ++t;
+      jj = 0;
+    }
+    if (tail_on && tail < 2) {
+      kvrow = qrow + tail * kT;  // the diagonal tiles are the item's own rows
+      fl = tail == 0 ? (kUse0 | kUse1 | kDiag0) : (kUse1 | kDiag1);
+      step = 0;
+      ++tail;
+      return true;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ int item_index(int k, int cta, int grid) {
+  // Snake order over the cost-sorted list balances the persistent CTAs.
+  return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs args, int n_items) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
+  const uint32_t bars = base + kOffBar;
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+  const RingShape& sh = args.sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{abort_flag, args.err};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarS + i), 1);
+      mbar_init(bar(kBarP + i), 128);
+      mbar_init(bar(kBarO + i), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t kv_it = 0, q_armed = 0, k_armed[kStages] = {0}, v_armed[kStages] = {0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int idx = item_index(k, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = decode_item(sh, idx);
+        if (!mbar_wait(bar(kBarQEmpty), (k & 1) ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+        ++q_armed;
+        const int row0 = it.b * sh.S + it.qrow;
+        for (int tq = 0; tq < 2; ++tq)
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(sQ + tq * kTileBytes + half * kBoxBytes, &tm_q, bar(kBarQFull), half * 64,
+                        it.h, row0 + tq * kT);
+        KvSeq seq;
+        seq.init(sh, args.t_begin, args.t_end, it);
+        int kvrow, fl, step;
+        while (seq.next(kvrow, fl, step)) {
+          const int st = kv_it % kStages;
+          const uint32_t ph = (kv_it / kStages) & 1;
+          const int krow = it.b * sh.S + kvrow;
+          if (!mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarKFull + st), kTileBytes);
+          ++k_armed[st];
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(sK + st * kTileBytes + half * kBoxBytes, &tm_k, bar(kBarKFull + st),
+                        half * 64, it.g, krow);
+          if (!mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarVFull + st), kTileBytes);
+          ++v_armed[st];
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(sV + st * kTileBytes + half * kBoxBytes, &tm_v, bar(kBarVFull + st),
+                        half * 64, it.g, krow);
+          ++kv_it;
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA exits.
+        if (q_armed) mbar_drain(bar(kBarQFull), (q_armed - 1) & 1);
+        for (int s = 0; s < kStages; ++s) {
+          if (k_armed[s]) mbar_drain(bar(kBarKFull + s), (k_armed[s] - 1) & 1);
+          if (v_armed[s]) mbar_drain(bar(kBarVFull + s), (v_armed[s] - 1) & 1);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      uint32_t kv_it = 0, p_ph[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int idx = item_index(k, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = decode_item(sh, idx);
+        if (!mbar_wait(bar(kBarQFull), k & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        KvSeq seq;
+        seq.init(sh, args.t_begin, args.t_end, it);
+        int kvrow, fl, step;
+        bool have = seq.next(kvrow, fl, step);
+        if (!have) {
+          mma_commit(bar(kBarQEmpty));
+          continue;
+        }
+        unsigned long long census = 0;
+        int census_step = step;
+        // S for the first tile.
+        int st = kv_it % kStages;
+        uint32_t kph = (kv_it / kStages) & 1;
+        if (!mbar_wait(bar(kBarKFull + st), kph, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int i = 0; i < 2; ++i) {
+          if (!(fl & (kUse0 << i))) continue;
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + col_s(i), sdesc_sw128(sQ + i * kTileBytes + off, 16, 1024),
+                   sdesc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
+          }
+          mma_commit(bar(kBarS + i));
+        }
+        mma_commit(bar(kBarKEmpty + st));
+        uint32_t acc[2] = {0, 0};
+        while (true) {
+          int nkvrow, nfl = 0, nstep = 0;
+          const bool have_next = seq.next(nkvrow, nfl, nstep);
+          const int nst = (kv_it + 1) % kStages;
+          const uint32_t nkph = ((kv_it + 1) / kStages) & 1;
+          if (!mbar_wait(bar(kBarVFull + st), kph, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          bool k_ready = false;
+          for (int i = 0; i < 2; ++i) {
+            if (fl & (kUse0 << i)) {
+              if (!mbar_wait(bar(kBarP + i), p_ph[i], wc)) {
+                ok = false;
+                break;
+              }
+              p_ph[i] ^= 1;
+              tc_fence_after();
+              for (int kk = 0; kk < kT / 16; ++kk)
+                mma_ts(tmem + col_o(i), tmem + col_s(i) + kk * 8,
+                       sdesc_sw128(sV + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescPV,
+                       acc[i] | (kk > 0));
+              acc[i] = 1;
+            }
+            if (have_next && (nfl & (kUse0 << i))) {
+              if (!k_ready) {
+                if (!mbar_wait(bar(kBarKFull + nst), nkph, wc)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_ready = true;
+              }
+              for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                mma_ss(tmem + col_s(i), sdesc_sw128(sQ + i * kTileBytes + off, 16, 1024),
+                       sdesc_sw128(sK + nst * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
+              }
+              mma_commit(bar(kBarS + i));
+            }
+          }
+          if (!ok) break;
+          mma_commit(bar(kBarVEmpty + st));
+          if (have_next) mma_commit(bar(kBarKEmpty + nst));
+          if (args.tiles_rt != nullptr) {
+            if (step != census_step) {
+              atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
+              census = 0;
+              census_step = step;
+            }
+            census += (unsigned long long)(((fl & kUse0) ? 1 : 0) + ((fl & kUse1) ? 1 : 0));
+          }
+          ++kv_it;
+          if (!have_next) break;
+          kvrow = nkvrow;
+          fl = nfl;
+          step = nstep;
+          st = nst;
+          kph = nkph;
+        }
+        if (!ok) break;
+        if (args.tiles_rt != nullptr && census)
+          atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
+        mma_commit(bar(kBarO + 0));
+        mma_commit(bar(kBarO + 1));
+        mma_commit(bar(kBarQEmpty));
+      }
+      if (!ok) {
+        // Let every MMA already issued retire before TMEM is released.
+        mma_commit(bar(kBarDrain));
+        mbar_drain(bar(kBarDrain), 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // -------------------------------------------------------------- softmax
+    const int ti = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int wq = warp & 3;         // TMEM sub-partition = rows 32*wq ..
+    const int row = wq * 32 + lane;  // row within the tile
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t colS = col_s(ti), colO = col_o(ti);
+    const float sl2 = sh.scale_log2;
+    uint32_t s_ph = 0, o_ph = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int idx = item_index(k, blockIdx.x, gridDim.x);
+      if (idx >= n_items) break;
+      const Item it = decode_item(sh, idx);
+      KvSeq seq;
+      seq.init(sh, args.t_begin, args.t_end, it);
+      float m = -INFINITY, l = 0.f;
+      int nt = 0;
+      int kvrow, fl, step;
+      while (seq.next(kvrow, fl, step)) {
+        if (!(fl & (kUse0 << ti))) continue;
+        const bool diag = (fl & (kDiag0 << ti)) != 0;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS + ti), s_ph, wc))) {
+          ok = false;
+          break;
+        }
+        s_ph ^= 1;
+        tc_fence_after();
+        uint32_t r[128];
+        tmem_ld32(tl + colS + 0, r + 0);
+        tmem_ld32(tl + colS + 32, r + 32);
+        tmem_ld32(tl + colS + 64, r + 64);
+        tmem_ld32(tl + colS + 96, r + 96);
+        tmem_wait_ld_regs(r);
+        reg_fence32(r + 32);
+        reg_fence32(r + 64);
+        reg_fence32(r + 96);
+        if (diag) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j)
+            if (j > row) r[j] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = __uint_as_float(r[0]), mx1 = __uint_as_float(r[1]);
+        float mx2 = __uint_as_float(r[2]), mx3 = __uint_as_float(r[3]);
+#pragma unroll
+        for (int j = 4; j < 128; j += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(r[j]));
+          mx1 = fmaxf(mx1, __uint_as_float(r[j + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(r[j + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(r[j + 3]));
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+        const float m_new = fmaxf(m, m_tile);
+        const bool need = m_new > m + kRescaleThreshold;
+        const bool rescale = __any_sync(0xffffffffu, need);
+        float alpha = 1.f;
+        if (rescale) {
+          alpha = ex2(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+        const float nm = -m;
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t p[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float a0 = ex2(fmaf(__uint_as_float(r[64 * h + 2 * j]), sl2, nm));
+            const float a1 = ex2(fmaf(__uint_as_float(r[64 * h + 2 * j + 1]), sl2, nm));
+            l0 += a0;
+            l1 += a1;
+            p[j] = pack_bf16(a0, a1);
+          }
+          tmem_st32(tl + colS + 32 * h, p);
+        }
+        l += l0 + l1;
+        if (rescale && nt > 0) {
+          // Softmax-state correction: O <- O * 2^(m_old - m_new).  The S
+          // barrier of this tile also covers the previous P V product, and the
+          // next one is issued only after the P barrier below.
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tl + colO + cc * 32, o);
+            tmem_wait_ld_regs(o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            tmem_st32(tl + colO + cc * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarP + ti));
+        ++nt;
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      const int qrow = it.qrow + ti * kT + row;
+      const int64_t obase = (((int64_t)it.b * sh.S + qrow) * sh.H + it.h) * kD;
+      const int64_t lidx = ((int64_t)it.b * sh.H + it.h) * sh.S + qrow;
+      if (nt == 0) {
+        // Step partial with no visible key: (0, -inf).
+        float4* op = reinterpret_cast<float4*>(static_cast<float*>(args.out) + obase);
+        for (int j = 0; j < kD / 4; ++j) op[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        args.lse[lidx] = -INFINITY;
+        continue;
+      }
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarO + ti), o_ph, wc))) {
+        ok = false;
+        break;
+      }
+      o_ph ^= 1;
+      tc_fence_after();
+      const float inv = 1.f / l;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tl + colO + cc * 32, o);
+        tmem_wait_ld_regs(o);
+        if (args.step_mode) {
+          float4* op = reinterpret_cast<float4*>(static_cast<float*>(args.out) + obase + cc * 32);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            op[j] = make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
+                                __uint_as_float(o[4 * j + 2]) * inv,
+                                __uint_as_float(o[4 * j + 3]) * inv);
+        } else {
+          uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + obase +
+                                               cc * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(o[8 * j + 0]) * inv, __uint_as_float(o[8 * j + 1]) * inv);
+            v.y = pack_bf16(__uint_as_float(o[8 * j + 2]) * inv, __uint_as_float(o[8 * j + 3]) * inv);
+            v.z = pack_bf16(__uint_as_float(o[8 * j + 4]) * inv, __uint_as_float(o[8 * j + 5]) * inv);
+            v.w = pack_bf16(__uint_as_float(o[8 * j + 6]) * inv, __uint_as_float(o[8 * j + 7]) * inv);
+            op[j] = v;
+          }
+        }
+      }
+      args.lse[lidx] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// [rows, heads, 128] bf16 viewed as a 3-D tensor (d, head, row), box
+// (64, 1, 128) with 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* ptr, int heads, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)heads * kD * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kT};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool tc_fwd_available() { return true; }
+
+cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t stream) {
+  const RingShape& sh = a.sh;
+  const int n_items = sh.B * sh.H * (sh.S / (2 * kT));
+  if (n_items == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  const int64_t rows = (int64_t)sh.B * sh.S;
+  if (!make_map(&mq, a.q, sh.H, rows) || !make_map(&mk, a.k, sh.Hkv, rows) ||
+      !make_map(&mv, a.v, sh.Hkv, rows))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = n_items < sms ? n_items : sms;
+  tc_fwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, a, n_items);
+  return cudaGetLastError();
+}
+
+}  // namespace cpattn

@@ -199,8 +199,30 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+#define CPATTN_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), \
+                      "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+
+// tcgen05.ld writes its destination registers asynchronously; they are valid
+// after tcgen05.wait::ld.  Waits, then ties the 32 registers to the wait so
+// that no use of them is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : CPATTN_RW8(0), CPATTN_RW8(8), CPATTN_RW8(16), CPATTN_RW8(24)
+               :
+               : "memory");
+}
+
+// Ties 32 registers to this point without emitting code.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+  asm volatile(""
+               : CPATTN_RW8(0), CPATTN_RW8(8), CPATTN_RW8(16), CPATTN_RW8(24)
+               :
+               : "memory");
+}
+
 #undef CPATTN_R8
 #undef CPATTN_W8
+#undef CPATTN_RW8
 
 // ---------------------------------------------------------------------------
 // Descriptors
