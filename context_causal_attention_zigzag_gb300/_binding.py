@@ -41,6 +41,7 @@ SIGNATURES = {
     "cpattn_lse_merge": (_i, [_vp] * 6 + [_i] * 4 + [_vp]),
     "cpattn_ring_bwd_workspace_bytes": (_sz, [_i] * 6),
     "cpattn_ring_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _sz, _vp]),
+    "cpattn_ring_bwd_noalloc": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp]),
     "cpattn_tile_counts": (_i, [_i64, _i, _i, _i, _i64, _vp, _vp]),
     "cpattn_device_status": (_i, [_vp]),
     "cpattn_status_string": (ctypes.c_char_p, [_i]),
@@ -260,6 +261,25 @@ def ring_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None
                                int(layout), int(bool(causal)), code, _scale(scale),
                                _ptr(workspace), workspace.numel(), _stream(q))
     _check("cpattn_ring_bwd", rc)
+    return dq, dk, dv
+
+
+def ring_bwd_noalloc(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
+                     dq=None, dk=None, dv=None):
+    """cpattn_ring_bwd_noalloc: the ring backward with the library's own fixed
+    64 MiB device scratch instead of a workspace, for callers that cannot
+    allocate device memory.  Calls that overlap on the GPU race on that scratch."""
+    _need_cuda(q, k, v, out, dout, lse)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need_cuda(dq, dk, dv)
+    rc = lib().cpattn_ring_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                       _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D,
+                                       int(cp), int(layout), int(bool(causal)), _dtype_code(q),
+                                       _scale(scale), _stream(q))
+    _check("cpattn_ring_bwd_noalloc", rc)
     return dq, dk, dv
 
 

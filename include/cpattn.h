@@ -177,6 +177,33 @@ CPATTN_API int cpattn_ring_bwd(const void* q, const void* k, const void* v, cons
                     cpattn_stream_t stream);
 
 /*
+ * cpattn_ring_bwd without a workspace argument.  The pages describe no such
+ * call; it exists for callers that cannot allocate device memory -- code
+ * running under a memory manager that owns the whole device (a framework's
+ * caching allocator, a serving runtime that reserves HBM at start-up) or on
+ * a latency-critical loop where cudaMalloc / cudaFree would synchronise the
+ * device.  The caller still passes every input and output exactly as for
+ * cpattn_ring_bwd.
+ *   Scratch: a 64 MiB array inside the library's device image (a static
+ *   __device__ array), held by every GPU that loads the library until the
+ *   process exits.  Problems whose cpattn_ring_bwd_workspace_bytes exceeds
+ *   64 MiB (67108864 bytes) are rejected with CPATTN_ERR_WORKSPACE before
+ *   anything is launched.
+ *   The first call on a device looks the array's device address up
+ *   (cudaGetSymbolAddress with that device current); make that first call
+ *   before any stream capture.  Nothing is allocated, by this call or later.
+ *   Every call on a device shares the one array, which keeps the last call's
+ *   contents (each call re-zeroes what must start at zero): calls whose
+ *   execution overlaps on the GPU -- on different streams, or from different
+ *   host threads -- race on it and give wrong results.  Serialise them.
+ */
+CPATTN_API int cpattn_ring_bwd_noalloc(const void* q, const void* k, const void* v,
+                                       const void* out, const void* dout, const float* lse,
+                                       void* dq, void* dk, void* dv, int B, int H, int Hkv, int S,
+                                       int D, int cp_size, int layout, int causal, int dtype,
+                                       float softmax_scale, cpattn_stream_t stream);
+
+/*
  * Closed-form work census of the ring (host only): for every rank r and
  * step t, the number of tile x tile blocks with at least one visible
  * (query, key) pair, tiles_rt[r*cp_size + t], and the number of visible
