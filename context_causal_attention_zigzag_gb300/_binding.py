@@ -24,6 +24,7 @@ CONTIGUOUS = 0
 ZIGZAG = 1
 F32 = 0
 BF16 = 1
+GRAD_F32 = 0x10  # OR into the backward's dtype: dq, dk, dv written as float32
 PATH_SIMT = 0
 PATH_TCGEN05 = 1
 
@@ -243,15 +244,29 @@ def ring_bwd_workspace_bytes(B, H, Hkv, S, D, dtype=BF16) -> int:
     return int(lib().cpattn_ring_bwd_workspace_bytes(B, H, Hkv, S, D, int(dtype)))
 
 
+def _grad_args(q, k, v, dq, dk, dv, grad_dtype):
+    code = _dtype_code(q)
+    gdt = q.dtype if grad_dtype is None else grad_dtype
+    if gdt == torch.float32 and q.dtype != torch.float32:
+        code |= GRAD_F32
+    elif gdt != q.dtype:
+        raise TypeError("grad_dtype must be the input dtype or torch.float32")
+    dq = torch.empty(q.shape, device=q.device, dtype=gdt) if dq is None else dq
+    dk = torch.empty(k.shape, device=k.device, dtype=gdt) if dk is None else dk
+    dv = torch.empty(v.shape, device=v.device, dtype=gdt) if dv is None else dv
+    for t in (dq, dk, dv):
+        if t.dtype != gdt:
+            raise TypeError("dq, dk, dv must have the gradient dtype")
+    return code, dq, dk, dv
+
+
 def ring_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
-             dq=None, dk=None, dv=None, workspace=None):
-    """Ring backward on sharded-order tensors; returns (dq, dk, dv)."""
+             dq=None, dk=None, dv=None, workspace=None, grad_dtype=None):
+    """Ring backward on sharded-order tensors; returns (dq, dk, dv).
+    grad_dtype=torch.float32 with bf16 inputs writes float32 gradients."""
     _need_cuda(q, k, v, out, dout, lse)
     B, H, Hkv, S, D = _shape(q, k, v)
-    code = _dtype_code(q)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
     need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
@@ -265,19 +280,17 @@ def ring_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None
 
 
 def ring_bwd_noalloc(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
-                     dq=None, dk=None, dv=None):
+                     dq=None, dk=None, dv=None, grad_dtype=None):
     """cpattn_ring_bwd_noalloc: the ring backward with the library's own fixed
     64 MiB device scratch instead of a workspace, for callers that cannot
     allocate device memory.  Calls that overlap on the GPU race on that scratch."""
     _need_cuda(q, k, v, out, dout, lse)
     B, H, Hkv, S, D = _shape(q, k, v)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
     _need_cuda(dq, dk, dv)
     rc = lib().cpattn_ring_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
                                        _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D,
-                                       int(cp), int(layout), int(bool(causal)), _dtype_code(q),
+                                       int(cp), int(layout), int(bool(causal)), code,
                                        _scale(scale), _stream(q))
     _check("cpattn_ring_bwd_noalloc", rc)
     return dq, dk, dv
@@ -318,11 +331,13 @@ def attention(q, k, v, cp, layout=ZIGZAG, causal=True, scale=None):
     return zigzag_unpermute(o, cp, layout), zigzag_unpermute(lse, cp, layout, seq_dim=2)
 
 
-def attention_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None):
+def attention_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None,
+                      grad_dtype=None):
     """Natural order: forward and backward through the ring.  Returns
     (out, lse, dq, dk, dv), all natural order."""
     qs, ks, vs, dos = (zigzag_permute(x, cp, layout) for x in (q, k, v, dout))
     o, lse = ring_fwd(qs, ks, vs, cp, layout, causal, scale)
-    dq, dk, dv = ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, scale)
+    dq, dk, dv = ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, scale,
+                          grad_dtype=grad_dtype)
     un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
     return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dk), un(dv)

@@ -120,6 +120,7 @@ int plan_common(int B, int H, int Hkv, int S, int D, int cp, int layout, int cau
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp, layout, causal, 0.f, &sh);
   if (rc != CPATTN_OK) return rc;
+  dtype &= fwd ? ~0 : ~CPATTN_GRAD_F32;
   if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   bool tc = fwd ? (tc_fwd_eligible(sh, dtype) && tc_fwd_available())
                 : (tc_bwd_eligible(sh, dtype) && tc_bwd_available());
@@ -230,12 +231,12 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
 }
 
 size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, int D, int dtype) {
-  (void)Hkv;
   (void)dtype;
-  if (B < 0 || H < 0 || S < 0 || D < 0) return 0;
-  size_t dq = (size_t)B * S * H * D * sizeof(float);
-  size_t delta = (size_t)B * H * S * sizeof(float);
-  return align256(dq) + align256(delta);
+  if (B < 0 || H < 0 || Hkv < 0 || S < 0 || D < 0) return 0;
+  const size_t dq = (size_t)B * S * H * D * sizeof(float);
+  const size_t dkv = (size_t)B * S * Hkv * D * sizeof(float);
+  const size_t delta = (size_t)B * H * S * sizeof(float);
+  return align256(dq) + 2 * align256(dkv) + align256(delta);
 }
 
 int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -246,7 +247,9 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp_size, layout, causal, softmax_scale, &sh);
   if (rc != CPATTN_OK) return rc;
-  if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  const int out_dtype = (dtype & CPATTN_GRAD_F32) ? CPATTN_F32 : in_dtype;
   if ((long long)B * S == 0) return CPATTN_OK;
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return CPATTN_ERR_INVALID_ARG;
   const void* ptrs[] = {q, k, v, out, dout, lse, dq, dk, dv};
@@ -259,10 +262,17 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   int* err = device_error_word();
   if (err == nullptr) return CPATTN_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
-  float* dq_acc = static_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          align256((size_t)B * S * H * D * sizeof(float)));
-  cudaError_t e = launch_bwd_prep(out, dout, delta, dq_acc, B, S, H, D, dtype, st);
+  const int64_t n_q = (int64_t)B * S * H * D, n_kv = (int64_t)B * S * Hkv * D;
+  char* ws = static_cast<char*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws);
+  ws += align256((size_t)n_q * sizeof(float));
+  float* dk_acc = reinterpret_cast<float*>(ws);
+  ws += align256((size_t)n_kv * sizeof(float));
+  float* dv_acc = reinterpret_cast<float*>(ws);
+  ws += align256((size_t)n_kv * sizeof(float));
+  float* delta = reinterpret_cast<float*>(ws);
+  cudaError_t e = launch_bwd_prep(out, dout, delta, dq_acc, dk_acc, dv_acc, n_kv, B, S, H, D,
+                                  in_dtype, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   BwdArgs a;
   a.sh = sh;
@@ -273,15 +283,15 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   a.lse = lse;
   a.delta = delta;
   a.dq_acc = dq_acc;
-  a.dk = dk;
-  a.dv = dv;
+  a.dk_acc = dk_acc;
+  a.dv_acc = dv_acc;
   a.err = err;
-  if (tc_bwd_eligible(sh, dtype) && tc_bwd_available() && device_is_sm103())
+  if (tc_bwd_eligible(sh, in_dtype) && tc_bwd_available() && device_is_sm103())
     e = launch_tc_bwd(a, st);
   else
-    e = launch_simt_bwd(a, dtype, st);
+    e = launch_simt_bwd(a, in_dtype, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  e = launch_dq_convert(dq_acc, dq, (int64_t)B * S * H * D, dtype, st);
+  e = launch_grad_convert(dq_acc, dk_acc, dv_acc, dq, dk, dv, n_q, n_kv, out_dtype, st);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

@@ -64,9 +64,9 @@ struct BwdArgs {
   const void* dout;
   const float* lse;    // [B,H,S]
   const float* delta;  // [B,H,S], dout . out
-  float* dq_acc;       // [B,S,H,D] float32, pre-zeroed, scaled by softmax scale
-  void* dk;            // [B,S,Hkv,D] dtype
-  void* dv;            // [B,S,Hkv,D] dtype
+  float* dq_acc;       // [B,S,H,D] float32, pre-zeroed; receives scale * dS K
+  float* dk_acc;       // [B,S,Hkv,D] float32, pre-zeroed; receives scale * dS^T Q
+  float* dv_acc;       // [B,S,Hkv,D] float32, pre-zeroed; receives P^T dO
   int* err;
 };
 
@@ -80,11 +80,15 @@ cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_
                              const float* l_b, float* o, float* l, int B, int S, int H, int D,
                              cudaStream_t stream);
 cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, float* dq_acc,
-                            int B, int S, int H, int D, int dtype, cudaStream_t stream);
+                            float* dk_acc, float* dv_acc, int64_t n_kv, int B, int S, int H,
+                            int D, int dtype, cudaStream_t stream);
 cudaError_t launch_simt_bwd(const BwdArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream);
-cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t n, int dtype,
-                              cudaStream_t stream);
+// Converts the three float32 gradient accumulators to the output dtype
+// (CPATTN_F32 or CPATTN_BF16) in one launch; n_q / n_kv elements each.
+cudaError_t launch_grad_convert(const float* dq_acc, const float* dk_acc, const float* dv_acc,
+                                void* dq, void* dk, void* dv, int64_t n_q, int64_t n_kv,
+                                int out_dtype, cudaStream_t stream);
 
 // Whether this build carries the tensor-core kernels.
 bool tc_fwd_available();

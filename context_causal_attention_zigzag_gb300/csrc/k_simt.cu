@@ -14,8 +14,8 @@
 // Backward: one CTA per (64 key rows of one source rank, batch*kv head).  It
 // follows its K/V tile around the ring (step t: receiving rank (s + t) mod
 // cp), over every query head of the group, recomputes P from the saved LSE
-// and accumulates dK, dV in registers; dQ goes to a float32 accumulator with
-// atomic adds.
+// and accumulates dK, dV in registers (written to the float32 accumulators at
+// the end); dQ goes to its float32 accumulator with atomic adds.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <limits.h>
@@ -403,8 +403,8 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
     }
   }
 
-  T* dkp = static_cast<T*>(a.dk);
-  T* dvp = static_cast<T*>(a.dv);
+  // This CTA owns its key rows over every query: plain float32 stores into the
+  // accumulators (the pre-pass zeroed them; the conversion kernel follows).
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int row = ty * 4 + i;
@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
     const int64_t base = (((int64_t)b * sh.S + k0 + row) * sh.Hkv + g) * D;
 #pragma unroll
     for (int dd = 0; dd < DV; ++dd) {
-      from_f(dkp + base + tx + 16 * dd, sh.scale * dk[i][dd]);
-      from_f(dvp + base + tx + 16 * dd, dv[i][dd]);
+      a.dk_acc[base + tx + 16 * dd] = sh.scale * dk[i][dd];
+      a.dv_acc[base + tx + 16 * dd] = dv[i][dd];
     }
   }
 }

@@ -1,6 +1,7 @@
 // Bandwidth-bound kernels of the ring: zigzag permute / unpermute, the exact
-// LSE merge of two partials, the backward pre-pass (Delta = dO . O and dQ
-// accumulator zeroing) and the dQ float32 -> dtype conversion.
+// LSE merge of two partials, the backward pre-pass (Delta = dO . O and zeroing
+// of the gradient accumulators) and the float32 -> output dtype conversion of
+// dQ, dK, dV.
 //
 // All of them move data in 16-byte vectors with consecutive threads on
 // consecutive vectors, and size their grids as a multiple of the SM count.
@@ -168,15 +169,18 @@ __device__ __forceinline__ void load_vec(const T* p, float* f) {
 }
 
 // ---------------------------------------------------------------------------
-// Backward pre-pass: delta[b,h,s] = sum_d dout * out (fp32), and zero the
-// float32 dQ accumulator row.  One warp per row.
+// Backward pre-pass: delta[b,h,s] = sum_d dout * out (fp32), zero the float32
+// dQ accumulator row (one warp per row), and zero the dK / dV accumulators
+// (grid-stride, float4).
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out,
                                                        const T* __restrict__ dout,
                                                        float* __restrict__ delta,
-                                                       float* __restrict__ dq_acc, int B, int S,
-                                                       int H) {
+                                                       float* __restrict__ dq_acc,
+                                                       float4* __restrict__ dk_acc,
+                                                       float4* __restrict__ dv_acc,
+                                                       int64_t n4_kv, int B, int S, int H) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)B * S * H;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -202,26 +206,49 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
       delta[(bi * H + hi) * S + si] = acc;
     }
   }
-}
-
-// dq[i] = (dtype) dq_acc[i], 4 elements per thread-iteration.
-__global__ void __launch_bounds__(256) dq_convert_bf16_kernel(const float4* __restrict__ in,
-                                                              __nv_bfloat162* __restrict__ out,
-                                                              int64_t n4) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4_kv;
        i += (int64_t)gridDim.x * blockDim.x) {
-    float4 x = in[i];
-    out[2 * i] = __floats2bfloat162_rn(x.x, x.y);
-    out[2 * i + 1] = __floats2bfloat162_rn(x.z, x.w);
+    dk_acc[i] = z;
+    dv_acc[i] = z;
   }
 }
 
-__global__ void __launch_bounds__(256) dq_convert_f32_kernel(const float4* __restrict__ in,
-                                                             float4* __restrict__ out,
-                                                             int64_t n4) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
-       i += (int64_t)gridDim.x * blockDim.x)
-    out[i] = in[i];
+// dst[i] = (out dtype) src[i] for the three gradient accumulators, 4
+// elements per thread-iteration; element counts are multiples of 4.
+template <typename O>
+__device__ __forceinline__ void store4(O* dst, int64_t i, float4 x);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, int64_t i, float4 x) {
+  reinterpret_cast<float4*>(dst)[i] = x;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, int64_t i, float4 x) {
+  uint2 v;
+  __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+  v.x = *reinterpret_cast<uint32_t*>(&lo);
+  v.y = *reinterpret_cast<uint32_t*>(&hi);
+  reinterpret_cast<uint2*>(dst)[i] = v;
+}
+
+template <typename O>
+__global__ void __launch_bounds__(256) grad_convert_kernel(const float4* __restrict__ q4,
+                                                           const float4* __restrict__ k4,
+                                                           const float4* __restrict__ v4,
+                                                           O* __restrict__ dq, O* __restrict__ dk,
+                                                           O* __restrict__ dv, int64_t nq4,
+                                                           int64_t nkv4) {
+  const int64_t total = nq4 + 2 * nkv4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < nq4) {
+      store4<O>(dq, i, q4[i]);
+    } else if (i < nq4 + nkv4) {
+      store4<O>(dk, i - nq4, k4[i - nq4]);
+    } else {
+      store4<O>(dv, i - nq4 - nkv4, v4[i - nq4 - nkv4]);
+    }
+  }
 }
 
 }  // namespace
@@ -254,39 +281,54 @@ cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_
 }
 
 cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, float* dq_acc,
-                            int B, int S, int H, int D, int dtype, cudaStream_t stream) {
+                            float* dk_acc, float* dv_acc, int64_t n_kv, int B, int S, int H,
+                            int D, int dtype, cudaStream_t stream) {
   int64_t rows = (int64_t)B * S * H;
   if (rows == 0) return cudaSuccess;
   int grid = grid_for(rows * 32, 256, 8);
+  float4* dk4 = reinterpret_cast<float4*>(dk_acc);
+  float4* dv4 = reinterpret_cast<float4*>(dv_acc);
+  const int64_t n4 = n_kv / 4;
   if (dtype == 1) {
     auto o = static_cast<const __nv_bfloat16*>(out);
     auto d = static_cast<const __nv_bfloat16*>(dout);
     if (D == 128)
-      bwd_prep_kernel<__nv_bfloat16, 128><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+      bwd_prep_kernel<__nv_bfloat16, 128>
+          <<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B, S, H);
     else
-      bwd_prep_kernel<__nv_bfloat16, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+      bwd_prep_kernel<__nv_bfloat16, 64>
+          <<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B, S, H);
   } else {
     auto o = static_cast<const float*>(out);
     auto d = static_cast<const float*>(dout);
     if (D == 128)
-      bwd_prep_kernel<float, 128><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+      bwd_prep_kernel<float, 128><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B,
+                                                            S, H);
     else
-      bwd_prep_kernel<float, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, B, S, H);
+      bwd_prep_kernel<float, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B,
+                                                           S, H);
   }
   return cudaGetLastError();
 }
 
-cudaError_t launch_dq_convert(const float* dq_acc, void* dq, int64_t n, int dtype,
-                              cudaStream_t stream) {
-  int64_t n4 = n / 4;  // n = B*S*H*D with D a multiple of 64
-  if (n4 == 0) return cudaSuccess;
-  int grid = grid_for(n4, 256, 8);
-  if (dtype == 1)
-    dq_convert_bf16_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                     static_cast<__nv_bfloat162*>(dq), n4);
+cudaError_t launch_grad_convert(const float* dq_acc, const float* dk_acc, const float* dv_acc,
+                                void* dq, void* dk, void* dv, int64_t n_q, int64_t n_kv,
+                                int out_dtype, cudaStream_t stream) {
+  const int64_t nq4 = n_q / 4, nkv4 = n_kv / 4;  // D is a multiple of 64
+  const int64_t total = nq4 + 2 * nkv4;
+  if (total == 0) return cudaSuccess;
+  int grid = grid_for(total, 256, 8);
+  auto q4 = reinterpret_cast<const float4*>(dq_acc);
+  auto k4 = reinterpret_cast<const float4*>(dk_acc);
+  auto v4 = reinterpret_cast<const float4*>(dv_acc);
+  if (out_dtype == 1)
+    grad_convert_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        q4, k4, v4, static_cast<__nv_bfloat16*>(dq), static_cast<__nv_bfloat16*>(dk),
+        static_cast<__nv_bfloat16*>(dv), nq4, nkv4);
   else
-    dq_convert_f32_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc),
-                                                    static_cast<float4*>(dq), n4);
+    grad_convert_kernel<float><<<grid, 256, 0, stream>>>(q4, k4, v4, static_cast<float*>(dq),
+                                                         static_cast<float*>(dk),
+                                                         static_cast<float*>(dv), nq4, nkv4);
   return cudaGetLastError();
 }
 

@@ -69,7 +69,15 @@ enum cpattn_status_code {
 };
 
 enum cpattn_layout { CPATTN_LAYOUT_CONTIGUOUS = 0, CPATTN_LAYOUT_ZIGZAG = 1 };
-enum cpattn_dtype { CPATTN_F32 = 0, CPATTN_BF16 = 1 };
+enum cpattn_dtype {
+  CPATTN_F32 = 0,
+  CPATTN_BF16 = 1,
+  /* Flag for the backward calls (OR it into dtype): dq, dk, dv are written
+   * as float32 whatever the input dtype.  A bf16 gradient element of
+   * magnitude >= 8 carries a rounding error of up to 2^-5; float32 output
+   * keeps the gradients at their float32 accumulation accuracy. */
+  CPATTN_GRAD_F32 = 0x10
+};
 enum cpattn_path { CPATTN_PATH_SIMT = 0, CPATTN_PATH_TCGEN05 = 1 };
 
 /*
@@ -166,9 +174,11 @@ CPATTN_API size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, 
  * The K/V tiles of source rank s visit ranks (s + t) mod cp_size, t =
  * 0..cp_size-1, in the ring's order.
  *   q, out, dout, dq: [B,S,H,D]; k, v, dk, dv: [B,S,Hkv,D]; lse [B,H,S]
- *   float32; all device, sharded order, dtype (lse float32).
+ *   float32; all device, sharded order, dtype (lse float32; dq, dk, dv
+ *   float32 when dtype carries CPATTN_GRAD_F32).
  *   workspace: device, at least cpattn_ring_bwd_workspace_bytes, 256-byte
- *   aligned; its contents are scratch (no state kept between calls).
+ *   aligned; its contents are scratch (no state kept between calls): float32
+ *   accumulators for dQ, dK, dV and the Delta rows.
  */
 CPATTN_API int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,

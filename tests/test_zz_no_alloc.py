@@ -26,6 +26,7 @@ DEV = "cuda"
     (1, 4, 2, 1024, 128, 4, cpa.ZIGZAG, True, torch.bfloat16, 2e-2),
     (1, 2, 2, 256, 64, 2, cpa.ZIGZAG, True, torch.float32, 1e-4),
     (2, 2, 1, 512, 128, 2, cpa.CONTIGUOUS, False, torch.bfloat16, 2e-2),
+    (1, 4, 2, 1024, 128, 2, cpa.ZIGZAG, True, torch.float32, 1e-4),
 ])
 def test_noalloc_backward_matches_workspace_backward(case):
     B, H, Hkv, S, D, cp, layout, causal, dtype, tol = case
@@ -50,6 +51,6 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     # B=1, H=32, S=8192, D=128: a 128 MiB float32 dQ accumulator > 64 MiB.
     rc = lib.cpattn_ring_bwd_noalloc(*([fake] * 9), 1, 32, 32, 8192, 128, 4, 1, 1, 1, 0.0, null)
     assert rc == _binding.ERR_WORKSPACE
-    # Within the limit the same shape class is accepted.
-    need = lib.cpattn_ring_bwd_workspace_bytes(1, 32, 32, 2048, 128, 1)
+    # A smaller problem of the same kind fits.
+    need = lib.cpattn_ring_bwd_workspace_bytes(1, 32, 8, 2048, 128, 1)
     assert need <= 64 << 20
