@@ -125,3 +125,17 @@ def test_invalid_arguments_rejected_before_launch():
     # closed-form census: chunk length not a multiple of the tile
     arr = (ctypes.c_uint64 * 16)()
     assert lib.cpattn_tile_counts(96, 4, 1, 1, 8, arr, None) == E
+
+
+def test_balance_report_closed_form():
+    # Zigzag: every ring step perfectly balanced; contiguous: step t has
+    # max/mean = cp/(cp-t) and lockstep efficiency 0.575 / 0.534 / 0.516 for
+    # the S=8192 cp=4, S=32768 cp=8 and S=131072 cp=16 workloads.
+    from context_causal_attention_zigzag_gb300 import balance
+    for S, cp, eff in ((8192, 4, 0.575), (32768, 8, 0.534), (131072, 16, 0.516)):
+        r = balance.report(S=S, cp=cp, run_kernel=False)
+        assert r["zigzag"]["closed_form"]["worst_step_max_over_mean"] == 1.0
+        assert r["zigzag"]["closed_form"]["lockstep_efficiency"] == 1.0
+        ratios = r["contiguous"]["closed_form"]["max_over_mean_per_step"]
+        assert np.allclose(ratios, [cp / (cp - t) for t in range(cp)])
+        assert abs(r["contiguous"]["closed_form"]["lockstep_efficiency"] - eff) < 5e-4

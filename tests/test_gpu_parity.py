@@ -420,3 +420,11 @@ def test_c5_full_size_forward_backward():
     assert np.max(np.abs(gdk - rdk)) <= 2e-2, np.max(np.abs(gdk - rdk))
     assert np.max(np.abs(gdv - rdv)) <= 2e-2, np.max(np.abs(gdv - rdv))
     assert cpa.device_status() == 0
+
+
+def test_balance_report_kernel_census():
+    from context_causal_attention_zigzag_gb300 import balance
+    r = balance.report(B=1, H=4, Hkv=2, S=8192, D=128, cp=4)
+    for name in ("zigzag", "contiguous"):
+        assert r[name]["kernel_equals_closed_form"], name
+    assert r["zigzag"]["kernel"]["worst_step_max_over_mean"] == 1.0
