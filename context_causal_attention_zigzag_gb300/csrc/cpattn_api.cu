@@ -233,10 +233,10 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
 size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, int D, int dtype) {
   (void)dtype;
   if (B < 0 || H < 0 || Hkv < 0 || S < 0 || D < 0) return 0;
-  const size_t dq = (size_t)B * S * H * D * sizeof(float);
-  const size_t dkv = (size_t)B * S * Hkv * D * sizeof(float);
+  const size_t q = (size_t)B * S * H * D * sizeof(float);
+  const size_t kv = (size_t)B * S * Hkv * D * sizeof(float);
   const size_t delta = (size_t)B * H * S * sizeof(float);
-  return align256(dq) + 2 * align256(dkv) + align256(delta);
+  return 2 * align256(q) + 2 * align256(kv) + align256(delta);
 }
 
 int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -263,18 +263,20 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   if (err == nullptr) return CPATTN_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_q = (int64_t)B * S * H * D, n_kv = (int64_t)B * S * Hkv * D;
+  // Workspace: [n_q][n_q][n_kv][n_kv] float32, then Delta [B,H,S].
   char* ws = static_cast<char*>(workspace);
-  float* dq_acc = reinterpret_cast<float*>(ws);
+  float* reg_a = reinterpret_cast<float*>(ws);
   ws += align256((size_t)n_q * sizeof(float));
-  float* dk_acc = reinterpret_cast<float*>(ws);
+  float* reg_b = reinterpret_cast<float*>(ws);
+  ws += align256((size_t)n_q * sizeof(float));
+  float* reg_c = reinterpret_cast<float*>(ws);
   ws += align256((size_t)n_kv * sizeof(float));
-  float* dv_acc = reinterpret_cast<float*>(ws);
+  float* reg_d = reinterpret_cast<float*>(ws);
   ws += align256((size_t)n_kv * sizeof(float));
   float* delta = reinterpret_cast<float*>(ws);
-  cudaError_t e = launch_bwd_prep(out, dout, delta, dq_acc, dk_acc, dv_acc, n_kv, B, S, H, D,
-                                  in_dtype, st);
-  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  const bool tc = tc_bwd_eligible(sh, in_dtype) && tc_bwd_available() && device_is_sm103();
   BwdArgs a;
+  memset(&a, 0, sizeof(a));
   a.sh = sh;
   a.q = q;
   a.k = k;
@@ -282,16 +284,31 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   a.dout = dout;
   a.lse = lse;
   a.delta = delta;
-  a.dq_acc = dq_acc;
-  a.dk_acc = dk_acc;
-  a.dv_acc = dv_acc;
   a.err = err;
-  if (tc_bwd_eligible(sh, in_dtype) && tc_bwd_available() && device_is_sm103())
+  cudaError_t e;
+  if (tc) {
+    // Tensor cores: Delta only, then the dK/dV and dQ kernels (every output
+    // element written exactly once), then the per-group sum of dK / dV.
+    e = launch_bwd_prep(out, dout, delta, nullptr, nullptr, nullptr, 0, B, S, H, D, in_dtype, st);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+    a.dk_part = reg_a;
+    a.dv_part = reg_b;
+    a.dq = dq;
+    a.dq_f32 = out_dtype == CPATTN_F32;
     e = launch_tc_bwd(a, st);
-  else
-    e = launch_simt_bwd(a, in_dtype, st);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+    e = launch_grad_reduce(reg_a, reg_b, dk, dv, B, S, H, Hkv, D, out_dtype, st);
+    return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  }
+  // CUDA cores: Delta and zeroed accumulators, the kernel, the conversion.
+  e = launch_bwd_prep(out, dout, delta, reg_a, reg_c, reg_d, n_kv, B, S, H, D, in_dtype, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  e = launch_grad_convert(dq_acc, dk_acc, dv_acc, dq, dk, dv, n_q, n_kv, out_dtype, st);
+  a.dq_acc = reg_a;
+  a.dk_acc = reg_c;
+  a.dv_acc = reg_d;
+  e = launch_simt_bwd(a, in_dtype, st);
+  if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+  e = launch_grad_convert(reg_a, reg_c, reg_d, dq, dk, dv, n_q, n_kv, out_dtype, st);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 

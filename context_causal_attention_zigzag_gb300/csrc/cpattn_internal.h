@@ -64,9 +64,16 @@ struct BwdArgs {
   const void* dout;
   const float* lse;    // [B,H,S]
   const float* delta;  // [B,H,S], dout . out
-  float* dq_acc;       // [B,S,H,D] float32, pre-zeroed; receives scale * dS K
-  float* dk_acc;       // [B,S,Hkv,D] float32, pre-zeroed; receives scale * dS^T Q
-  float* dv_acc;       // [B,S,Hkv,D] float32, pre-zeroed; receives P^T dO
+  // CUDA-core path: float32 accumulators, pre-zeroed by the pre-pass.
+  float* dq_acc;       // [B,S,H,D]   receives scale * dS K
+  float* dk_acc;       // [B,S,Hkv,D] receives scale * dS^T Q
+  float* dv_acc;       // [B,S,Hkv,D] receives P^T dO
+  // Tensor-core path: per-query-head partials of dK / dV (float32, summed
+  // over each kv head's group afterwards) and dQ written directly.
+  float* dk_part;      // [B,S,H,D]
+  float* dv_part;      // [B,S,H,D]
+  void* dq;            // [B,S,H,D] float32 if dq_f32 else bf16
+  int dq_f32;
   int* err;
 };
 
@@ -84,6 +91,11 @@ cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, flo
                             int D, int dtype, cudaStream_t stream);
 cudaError_t launch_simt_bwd(const BwdArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream);
+// dk[b,s,g,:] = sum of dk_part[b,s,h,:] over the query heads h of kv head g
+// (and the same for dv), written in the output dtype.
+cudaError_t launch_grad_reduce(const float* dk_part, const float* dv_part, void* dk, void* dv,
+                               int B, int S, int H, int Hkv, int D, int out_dtype,
+                               cudaStream_t stream);
 // Converts the three float32 gradient accumulators to the output dtype
 // (CPATTN_F32 or CPATTN_BF16) in one launch; n_q / n_kv elements each.
 cudaError_t launch_grad_convert(const float* dq_acc, const float* dk_acc, const float* dv_acc,

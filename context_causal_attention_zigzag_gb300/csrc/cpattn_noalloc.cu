@@ -16,8 +16,8 @@
 
 namespace {
 
-// 64 MiB: the float32 dQ / dK / dV accumulators and the Delta rows of, e.g.,
-// B=1, S=2048, H=32, Hkv=8, D=128 (48 MiB).
+// 64 MiB: the float32 gradient accumulators and the Delta rows of, e.g.,
+// B=1, S=1024, H=32, Hkv=8, D=128 (40 MiB).
 constexpr size_t kScratchBytes = (size_t)64 << 20;
 
 // Shared by every call on a device; keeps the last call's contents.

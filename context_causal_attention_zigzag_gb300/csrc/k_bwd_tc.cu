@@ -1,38 +1,48 @@
-// Tensor-core ring backward for sm_103a (tcgen05 + TMEM + TMA), persistent,
-// warp-specialised, KV-major.
+// Tensor-core ring backward for sm_103a (tcgen05 + TMEM + TMA): two
+// persistent, warp-specialised kernels that together produce dQ, dK, dV
+// without any atomic reduction.
 //
 // Gradients through the ring ("Context Parallelism for Long-Context
-// Training", section "Prove attention equivalence"): a work item is one
-// 128-row K/V tile of one (batch, query head).  It stays in shared memory
-// while the query tiles that see it stream past, in the order of the ring
-// steps t = 0..cp-1 that carry this K/V to rank (s + t) mod cp ("Sequence
-// Parallelism IV", section 4), tiles wholly in the causal past of the query
-// skipped, the diagonal tile masked.  Per query tile:
+// Training", section "Prove attention equivalence"), from the saved LSE and
+// Delta = rowsum(dO o O):  P = exp(s - LSE),  dS = P (dP - Delta),
+// dP = dO V^T.  The tiles a query tile and a K/V tile share are those of the
+// ring ("Sequence Parallelism IV", section 4): the K/V of source rank s
+// reaches rank (s + t) mod cp at step t; tiles wholly in the causal future
+// are skipped and the diagonal tile is masked.
 //
-//   S^T  = K Q^T                 (SS, 128x128x128)          -> TMEM cols [0,128)
-//   dP^T = V dO^T                (SS)                        -> TMEM cols [128,256)
-//   P^T  = exp2(S^T*scale*log2e - LSE*log2e)   (elementwise warps, bf16 back
-//          over S^T in TMEM)
-//   dV  += P^T dO                (TS: P^T from TMEM, dO MN-major) -> cols [256,384)
-//   dS^T = scale * P^T (dP^T - Delta)          (elementwise warps, bf16 into
-//          shared memory in the 128-byte-swizzled layout)
-//   dK  += dS^T Q                (SS: dS^T K-major, Q MN-major)   -> cols [384,512)
-//   dQ_t = dS K                  (SS: dS^T read MN-major, K MN-major) -> cols [128,256)
-//   dQ  += dQ_t                  (dQ warps: float4 atomic adds into the float32
-//          accumulator in HBM)
-// At the end of the item the dK / dV partials of this query head are added
-// (float4 atomics) into float32 accumulators shared by the heads of the group.
-// One item per query head, rather than per kv head, bounds the number of
-// MMA steps that accumulate into one TMEM sum (the tensor core's float32
-// accumulation drifts toward zero over very long chains).
+// dkdv kernel (K/V-major).  Work item: one 128-row K/V tile and one query
+// head.  The K/V tile stays in shared memory; the query tiles that see it
+// stream past (ring order), Q and dO by TMA, their LSE / Delta rows by bulk
+// copy.  Per query tile, with the tile transposed so that TMEM lanes are K/V
+// rows:
+//   S^T  = K Q^T   -> TMEM [0,128)       dP^T = V dO^T -> TMEM [128,256)
+//   P^T  = exp2(S^T*scale*log2e - LSE*log2e)  -> bf16 over S^T
+//   dS^T = scale * P^T (dP^T - Delta)         -> bf16 over dP^T
+//   dV  += P^T dO  (TS)  -> TMEM [256,384)    dK += dS^T Q (TS) -> TMEM [384,512)
+// MMA order per tile i: dV(i), S(i+1), dK(i), dP(i+1): the elementwise warps
+// of tile i+1 overlap the tensor core's work on tile i.  At the end of the
+// item the head's dK / dV partial (float32) is stored to its own slot; a
+// small kernel sums the slots of the query heads sharing a kv head.  One
+// item per query head keeps each TMEM accumulation chain short (the tensor
+// core's float32 accumulation drifts toward zero over very long chains).
 //
-// CTA = 384 threads: warp 0 TMA (K, V once per item; Q and dO per query tile
-// into a 2-stage ring), warp 1 TMEM owner + MMA issuer, warps 4-7 elementwise
-// (one thread per K/V row = TMEM lane), warps 8-11 dQ reduction and the dK /
-// dV epilogue.  LSE and Delta of the current query tile sit in shared memory,
-// written by the elementwise warps (prefetched one tile ahead in registers);
-// the warps hand that buffer over with two mbarriers, so every wait of the
-// kernel stays bounded.
+// dq kernel (query-major).  Work item: one 128-row query tile of one head.
+// Q, dO stay in shared memory, LSE / Delta in registers (TMEM lane = query
+// row); the K/V tiles of the ring stream past in a 2-stage ring:
+//   S = Q K^T -> TMEM [0,128)     dP = dO V^T -> TMEM [128,256) / [256,384)
+//   dS = scale * exp2(S*scale*log2e - LSE*log2e) (dP - Delta) -> bf16 over dP
+//   dQ += dS K  (TS, K read MN-major) -> TMEM [384,512)
+// MMA order per K/V tile j: S(j+1), dP(j+1), dQ(j); S is released as soon as
+// the elementwise warps have read it, dP alternates between two buffers.
+//
+// Both kernels: CTA = 384 threads; warp 0 TMA, warp 1 TMEM owner + MMA
+// issuer, warps 4-7 and 8-11 the elementwise work on columns [0,64) and
+// [64,128) of each tile (one thread per TMEM lane), and the epilogue.  The
+// packed bf16 result of both halves lands in columns [0,64), part of which
+// the first half still reads as float32: the halves meet at an mbarrier
+// after their reads and before their writes.  Every
+// wait is a bounded mbarrier wait; on expiry the kernel raises the device
+// error word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -51,90 +61,78 @@ constexpr int kD = 128;
 constexpr int kBoxBytes = kT * 64 * 2;     // 16 KB
 constexpr int kTileBytes = 2 * kBoxBytes;  // 32 KB
 constexpr int kThreads = 384;
-
-constexpr int kOffK = 0;
-constexpr int kOffV = kOffK + kTileBytes;
-constexpr int kOffQ = kOffV + kTileBytes;        // 2 stages
-constexpr int kOffDO = kOffQ + 2 * kTileBytes;   // 2 stages
-constexpr int kOffDS = kOffDO + 2 * kTileBytes;  // dS^T, bf16
-constexpr int kOffLse = kOffDS + kTileBytes;     // 128 floats (log2 domain)
-constexpr int kOffDlt = kOffLse + kT * 4;        // 128 floats
-constexpr int kOffBar = kOffDlt + kT * 4;
-constexpr int kBarKVFull = 0;
-constexpr int kBarKVEmpty = 1;
-constexpr int kBarQFull = 2;   // [2]
-constexpr int kBarQEmpty = 4;  // [2]
-constexpr int kBarS = 6;
-constexpr int kBarDP = 7;
-constexpr int kBarP = 8;
-constexpr int kBarDS = 9;
-constexpr int kBarDSFree = 10;
-constexpr int kBarDQ = 11;
-constexpr int kBarDQFree = 12;
-constexpr int kBarAcc = 13;
-constexpr int kBarAccFree = 14;
-constexpr int kBarDrain = 15;
-constexpr int kBarLseReady = 16;  // the elementwise warps staged this tile's LSE / Delta
-constexpr int kBarLseFree = 17;   // ... and are done reading them
-constexpr int kNumBars = 18;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
-
-constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);  // both K-major
-constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);   // A K-major, B MN-major
-constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);    // both MN-major
-
 constexpr float kLog2e = 1.4426950408889634f;
 
-struct Item {
-  int b, h, g, s, kc, kt, kvrow;  // kc: natural chunk of the K/V tile, kt: its tile in the chunk
-};
+constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);  // both K-major
+constexpr uint32_t kIdescKM = idesc_bf16(128, 128, false, true);   // B MN-major
 
-// Items in order of decreasing cost: earliest natural K/V tile first (it is
-// seen by the most query tiles), (batch, query head) innermost so that the
-// heads sharing one K/V tile run side by side.
-__device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
-  const int BH = sh.B * sh.H;
-  const int knat = idx / BH;
-  const int bh = idx - knat * BH;
-  Item it;
-  it.b = bh / sh.H;
-  it.h = bh - it.b * sh.H;
-  it.g = it.h / (sh.H / sh.Hkv);
-  const int nat0 = knat * kT;
-  it.kc = nat0 / sh.c;
-  const int loc = nat0 - it.kc * sh.c;
-  int jj;
-  if (sh.per_rank == 1 || it.kc < sh.cp) {
-    it.s = it.kc;
-    jj = 0;
-  } else {
-    it.s = 2 * sh.cp - 1 - it.kc;
-    jj = 1;
-  }
-  it.kt = loc / kT;
-  it.kvrow = it.s * sh.L + jj * sh.c + loc;
-  return it;
+__device__ __forceinline__ int item_index(int k, int cta, int grid) {
+  return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
 }
 
-// Query tiles of one head that see one K/V tile: ring steps t = 0..cp-1
-// (receiving rank (s + t) mod cp), then that rank's chunks.
+// Bulk (non-tensor) copy global -> shared, completion as transaction bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// The two elementwise warpgroups meet here: every thread arrives, then waits
+// for all 256 arrivals of this phase.  Returns false if the wait gave up.
+__device__ __forceinline__ bool halves_meet(uint32_t bar, uint32_t& phase, const WaitCtl& wc) {
+  tc_fence_before();
+  mbar_arrive(bar);
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase, wc));
+  phase ^= 1;
+  tc_fence_after();
+  return ok;
+}
+
+// Location of a 128-row tile given its natural tile index.
+struct TilePos {
+  int chunk;  // natural chunk
+  int rank;   // owning rank
+  int tile;   // tile index inside the chunk
+  int row;    // sharded row of the tile's first token
+};
+
+__device__ __forceinline__ TilePos tile_pos(const RingShape& sh, int knat) {
+  TilePos p;
+  const int nat0 = knat * kT;
+  p.chunk = nat0 / sh.c;
+  const int loc = nat0 - p.chunk * sh.c;
+  int jj;
+  if (sh.per_rank == 1 || p.chunk < sh.cp) {
+    p.rank = p.chunk;
+    jj = 0;
+  } else {
+    p.rank = 2 * sh.cp - 1 - p.chunk;
+    jj = 1;
+  }
+  p.tile = loc / kT;
+  p.row = p.rank * sh.L + jj * sh.c + loc;
+  return p;
+}
+
+// Query tiles (of one head) that see a K/V tile, in ring order: step t,
+// receiving rank (s + t) mod cp, that rank's chunks.
 struct QSeq {
   int cp, per, L, c, ctiles, causal, s, kc, kt;
   int t, jq, qt;
 
-  __device__ __forceinline__ void init(const RingShape& sh, const Item& it) {
+  __device__ __forceinline__ void init(const RingShape& sh, const TilePos& kv) {
     cp = sh.cp;
     per = sh.per_rank;
     L = sh.L;
     c = sh.c;
     ctiles = sh.c / kT;
     causal = sh.causal;
-    s = it.s;
-    kc = it.kc;
-    kt = it.kt;
+    s = kv.rank;
+    kc = kv.chunk;
+    kt = kv.tile;
     t = 0;
     jq = 0;
     qt = 0;
@@ -149,7 +147,7 @@ struct QSeq {
         if (causal && qc == kc)
           lo = kt;  // from the diagonal tile on
         else if (causal && qc < kc)
-          hi = 0;   // the whole chunk precedes this K/V: skipped
+          hi = 0;   // the whole chunk precedes this K/V: nothing to see
         if (qt < lo) qt = lo;
         if (qt < hi) {
           qrow = r * L + jq * c + qt * kT;
@@ -167,26 +165,126 @@ struct QSeq {
   }
 };
 
-__device__ __forceinline__ int item_index(int k, int cta, int grid) {
-  return k * grid + ((k & 1) ? (grid - 1 - cta) : cta);
-}
+// K/V tiles that a query tile sees, in ring order (step t brings the shard of
+// rank (r - t) mod cp), the diagonal tile last.
+struct KSeq {
+  int cp, per, L, c, ctiles, causal, r, qc, a, qrow;
+  int t, jj, kt;
+  bool tail;
 
-__device__ __forceinline__ void fence_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __device__ __forceinline__ void init(const RingShape& sh, const TilePos& q, int knat) {
+    cp = sh.cp;
+    per = sh.per_rank;
+    L = sh.L;
+    c = sh.c;
+    ctiles = sh.c / kT;
+    causal = sh.causal;
+    r = q.rank;
+    qc = q.chunk;
+    a = knat;
+    qrow = q.row;
+    t = 0;
+    jj = 0;
+    kt = 0;
+    tail = causal;
+  }
+
+  __device__ __forceinline__ bool next(int& kvrow, bool& diag) {
+    while (t < cp) {
+      const int s = ring_source(r, t, cp);
+      while (jj < per) {
+        const int kc = (per == 1 || jj == 0) ? s : 2 * cp - 1 - s;
+        int lim;
+        if (!causal || kc < qc)
+          lim = ctiles;
+        else if (kc == qc)
+          lim = a - kc * ctiles;  // tiles strictly before the diagonal
+        else
+          lim = 0;                // wholly in the causal future: skipped
+        if (kt < lim) {
+          kvrow = s * L + jj * c + kt * kT;
+          diag = false;
+          ++kt;
+          return true;
+        }
+        ++jj;
+        kt = 0;
+      }
+      ++t;
+      jj = 0;
+    }
+    if (tail) {
+      kvrow = qrow;  // the diagonal tile holds the query tile's own tokens
+      diag = true;
+      tail = false;
+      return true;
+    }
+    return false;
+  }
+};
+
+// ===========================================================================
+// dkdv kernel
+// ===========================================================================
+namespace kv {
+
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTileBytes;
+constexpr int kOffQ = kOffV + kTileBytes;         // [2] stages
+constexpr int kOffDO = kOffQ + 2 * kTileBytes;    // [2]
+constexpr int kOffLse = kOffDO + 2 * kTileBytes;  // [2][128] float (natural log)
+constexpr int kOffDlt = kOffLse + 2 * kT * 4;     // [2][128] float
+constexpr int kOffBar = kOffDlt + 2 * kT * 4;
+constexpr int kBarKVFull = 0;
+constexpr int kBarKVEmpty = 1;
+constexpr int kBarQFull = 2;   // [2]
+constexpr int kBarQEmpty = 4;  // [2]
+constexpr int kBarS = 6;
+constexpr int kBarDP = 7;
+constexpr int kBarP = 8;
+constexpr int kBarDS = 9;
+constexpr int kBarAcc = 10;
+constexpr int kBarAccFree = 11;
+constexpr int kBarDrain = 12;
+constexpr int kBarRdS = 13;   // both halves have read S^T
+constexpr int kBarRdDP = 14;  // both halves have read dP^T
+constexpr int kNumBars = 15;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+constexpr uint32_t kQTx = 2 * kTileBytes + 2 * kT * 4;  // Q, dO, LSE, Delta
+
+struct Item {
+  int b, h, g;
+  TilePos kv;
+};
+
+// Earliest natural K/V tile first (seen by the most query tiles), then
+// (batch, query head): the heads sharing one K/V tile run side by side.
+__device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
+  const int BH = sh.B * sh.H;
+  const int knat = idx / BH;
+  const int bh = idx - knat * BH;
+  Item it;
+  it.b = bh / sh.H;
+  it.h = bh - it.b * sh.H;
+  it.g = it.h / (sh.H / sh.Hkv);
+  it.kv = tile_pos(sh, knat);
+  return it;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                  const BwdArgs args, int n_items) {
+    dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const BwdArgs args, int n_items) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sK = base + kOffK, sV = base + kOffV, sQ = base + kOffQ, sDO = base + kOffDO;
-  const uint32_t sDS = base + kOffDS;
-  float* lse_s = reinterpret_cast<float*>(smem + kOffLse);
-  float* dlt_s = reinterpret_cast<float*>(smem + kOffDlt);
+  const uint32_t sLse = base + kOffLse, sDlt = base + kOffDlt;
+  const float* lse_s = reinterpret_cast<const float*>(smem + kOffLse);
+  const float* dlt_s = reinterpret_cast<const float*>(smem + kOffDlt);
   const uint32_t bars = base + kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -205,16 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarS), 1);
     mbar_init(bar(kBarDP), 1);
-    mbar_init(bar(kBarP), 128);
-    mbar_init(bar(kBarDS), 128);
-    mbar_init(bar(kBarDSFree), 1);
-    mbar_init(bar(kBarDQ), 1);
-    mbar_init(bar(kBarDQFree), 128);
+    mbar_init(bar(kBarP), 256);
+    mbar_init(bar(kBarDS), 256);
     mbar_init(bar(kBarAcc), 1);
-    mbar_init(bar(kBarAccFree), 128);
+    mbar_init(bar(kBarAccFree), 256);
     mbar_init(bar(kBarDrain), 1);
-    mbar_init(bar(kBarLseReady), 128);
-    mbar_init(bar(kBarLseFree), 128);
+    mbar_init(bar(kBarRdS), 256);
+    mbar_init(bar(kBarRdDP), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -239,21 +334,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
-        const Item it = decode_item(sh, idx);
+        const Item it = decode(sh, idx);
         if (!mbar_wait(bar(kBarKVEmpty), (k & 1) ^ 1, wc)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(bar(kBarKVFull), 2 * kTileBytes);
         ++kv_armed;
-        const int krow = it.b * sh.S + it.kvrow;
+        const int krow = it.b * sh.S + it.kv.row;
         for (int half = 0; half < 2; ++half) {
           tma_load_3d(sK + half * kBoxBytes, &tm_k, bar(kBarKVFull), half * 64, it.g, krow);
           tma_load_3d(sV + half * kBoxBytes, &tm_v, bar(kBarKVFull), half * 64, it.g, krow);
         }
         QSeq seq;
-        seq.init(sh, it);
-        const int h = it.h;
+        seq.init(sh, it.kv);
         int qrow;
         bool diag;
         while (seq.next(qrow, diag)) {
@@ -263,15 +357,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kBarQFull + st), 2 * kTileBytes);
+          const uint32_t full = bar(kBarQFull + st);
+          mbar_arrive_expect_tx(full, kQTx);
           ++q_armed[st];
           const int row = it.b * sh.S + qrow;
           for (int half = 0; half < 2; ++half) {
-            tma_load_3d(sQ + st * kTileBytes + half * kBoxBytes, &tm_q, bar(kBarQFull + st),
-                        half * 64, h, row);
-            tma_load_3d(sDO + st * kTileBytes + half * kBoxBytes, &tm_do, bar(kBarQFull + st),
-                        half * 64, h, row);
+            tma_load_3d(sQ + st * kTileBytes + half * kBoxBytes, &tm_q, full, half * 64, it.h, row);
+            tma_load_3d(sDO + st * kTileBytes + half * kBoxBytes, &tm_do, full, half * 64, it.h,
+                        row);
           }
+          const int64_t li = ((int64_t)it.b * sh.H + it.h) * sh.S + qrow;
+          bulk_load(sLse + st * kT * 4, args.lse + li, kT * 4, full);
+          bulk_load(sDlt + st * kT * 4, args.delta + li, kT * 4, full);
           ++qi;
         }
       }
@@ -284,51 +381,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
-      uint32_t qi = 0, p_ph = 0, ds_ph = 0, dqf_ph = 1;
+      uint32_t qi = 0, p_ph = 0, ds_ph = 0;
       bool ok = true;
+      auto issue_s = [&](int st) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024),
+                 sdesc_sw128(sQ + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(bar(kBarS));
+      };
+      auto issue_dp = [&](int st) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024),
+                 sdesc_sw128(sDO + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(bar(kBarDP));
+      };
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
-        const Item it = decode_item(sh, idx);
+        const Item it = decode(sh, idx);
         if (!mbar_wait(bar(kBarKVFull), k & 1, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
         QSeq seq;
-        seq.init(sh, it);
+        seq.init(sh, it.kv);
         int qrow;
         bool diag;
-        bool first = true;
-        while (seq.next(qrow, diag)) {
+        bool have = seq.next(qrow, diag);
+        if (have) {
           const int st = qi & 1;
-          const uint32_t ph = (qi >> 1) & 1;
-          const uint32_t q_s = sQ + st * kTileBytes, do_s = sDO + st * kTileBytes;
-          if (!mbar_wait(bar(kBarQFull + st), ph, wc)) {
+          if (!mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // S^T = K Q^T
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(q_s + off, 16, 1024),
-                   kIdescKK, kk > 0);
-          }
-          mma_commit(bar(kBarS));
-          // dP^T = V dO^T, once the previous dQ has left those columns.
-          if (!mbar_wait(bar(kBarDQFree), dqf_ph, wc)) {
-            ok = false;
-            break;
-          }
-          dqf_ph ^= 1;
-          tc_fence_after();
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024),
-                   sdesc_sw128(do_s + off, 16, 1024), kIdescKK, kk > 0);
-          }
-          mma_commit(bar(kBarDP));
+          issue_s(st);
+          issue_dp(st);
+        }
+        bool first = true;
+        while (have) {
+          const int st = qi & 1;
+          int nqrow;
+          bool ndiag;
+          const bool nhave = seq.next(nqrow, ndiag);
+          const int nst = (qi + 1) & 1;
           // dV += P^T dO
           if (!mbar_wait(bar(kBarP), p_ph, wc)) {
             ok = false;
@@ -342,29 +443,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           for (int kk = 0; kk < kT / 16; ++kk)
             mma_ts(tmem + kColDV, tmem + kColS + kk * 8,
-                   sdesc_sw128(do_s + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   sdesc_sw128(sDO + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q ; dQ_t = dS K
+          // S for the next tile (the S^T columns are free once dV has read P^T;
+          // MMAs execute in issue order).
+          if (nhave) {
+            if (!mbar_wait(bar(kBarQFull + nst), ((qi + 1) >> 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(nst);
+          }
+          // dK += dS^T Q
           if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
             ok = false;
             break;
           }
           ds_ph ^= 1;
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
-                   sdesc_sw128(q_s + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                   (!first || kk > 0) ? 1u : 0u);
-          }
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(tmem + kColDP, sdesc_sw128(sDS + kk * 2048, kBoxBytes, 1024),
-                   sdesc_sw128(sK + kk * 2048, kBoxBytes, 1024), kIdescMM, kk > 0);
-          mma_commit(bar(kBarDQ));
+            mma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
+                   sdesc_sw128(sQ + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   (!first || kk > 0) ? 1u : 0u);
           mma_commit(bar(kBarQEmpty + st));
-          mma_commit(bar(kBarDSFree));
+          // dP for the next tile (the dP^T columns are free once dK has read dS^T).
+          if (nhave) issue_dp(nst);
           first = false;
           ++qi;
+          have = nhave;
         }
         if (!ok) break;
         mma_commit(bar(kBarAcc));
@@ -375,194 +482,116 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(bar(kBarDrain), 0);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------------------------------------------------- elementwise
+  } else if (warp >= 4) {
+    // ----------------------------------------- elementwise + dK / dV epilogue
+    const int half = (warp - 4) >> 2;  // columns [64*half, 64*half + 64)
     const int wq = warp & 3;
-    const int row = wq * 32 + lane;  // K/V row of the tile (TMEM lane); also the
-                                     // query column whose LSE / Delta it stages
+    const int row = wq * 32 + lane;    // K/V row of the tile (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = sh.scale_log2, scale = sh.scale;
-    uint32_t s_ph = 0, dp_ph = 0, dsf_ph = 1, lr_ph = 0, lf_ph = 1;
+    uint32_t qi = 0, s_ph = 0, dp_ph = 0, rs_ph = 0, rdp_ph = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int idx = item_index(k, blockIdx.x, gridDim.x);
       if (idx >= n_items) break;
-      const Item it = decode_item(sh, idx);
+      const Item it = decode(sh, idx);
       QSeq seq;
-      seq.init(sh, it);
-      const int h = it.h;
+      seq.init(sh, it.kv);
       int qrow;
       bool diag;
-      bool have = seq.next(qrow, diag);
-      float cur_l = 0.f, cur_d = 0.f;
-      if (have) {
-        const int64_t li = ((int64_t)it.b * sh.H + h) * sh.S + qrow + row;
-        cur_l = args.lse[li] * kLog2e;
-        cur_d = args.delta[li];
-      }
-      while (have) {
-        int nqrow = 0;
-        bool ndiag = false;
-        const bool nhave = seq.next(nqrow, ndiag);
-        // Everyone is done with the previous tile's LSE / Delta ...
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarLseFree), lf_ph, wc))) {
+      while (seq.next(qrow, diag)) {
+        const int st = qi & 1;
+        // LSE / Delta of this tile arrived with its Q / dO.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc))) {
           ok = false;
           break;
         }
-        lf_ph ^= 1;
-        lse_s[row] = cur_l;
-        dlt_s[row] = cur_d;
-        // ... and everyone has staged this tile's.
-        mbar_arrive(bar(kBarLseReady));
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarLseReady), lr_ph, wc))) {
-          ok = false;
-          break;
-        }
-        lr_ph ^= 1;
-        float nl = 0.f, nd = 0.f;
-        if (nhave) {
-          const int64_t li = ((int64_t)it.b * sh.H + h) * sh.S + nqrow + row;
-          nl = args.lse[li] * kLog2e;
-          nd = args.delta[li];
-        }
-        // P^T = exp2(S^T * scale*log2e - LSE*log2e), masked on the diagonal.
+        const float* lse = lse_s + st * kT + 64 * half;
+        const float* dlt = dlt_s + st * kT + 64 * half;
+        // P^T = exp2(S^T * scale*log2e - LSE*log2e), masked on the diagonal
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS), s_ph, wc))) {
           ok = false;
           break;
         }
         s_ph ^= 1;
         tc_fence_after();
-        uint32_t r[128];
-        tmem_ld32(tl + kColS + 0, r + 0);
-        tmem_ld32(tl + kColS + 32, r + 32);
-        tmem_ld32(tl + kColS + 64, r + 64);
-        tmem_ld32(tl + kColS + 96, r + 96);
+        uint32_t r[64];
+        tmem_ld32(tl + kColS + 64 * half, r);
+        tmem_ld32(tl + kColS + 64 * half + 32, r + 32);
         tmem_wait_ld_regs(r);
         reg_fence32(r + 32);
-        reg_fence32(r + 64);
-        reg_fence32(r + 96);
-        uint32_t pk[64];
+        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float2 l2 = *reinterpret_cast<const float2*>(lse_s + 2 * j);
-          float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -l2.x));
-          float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -l2.y));
-          if (diag) {
-            if (2 * j < row) p0 = 0.f;
-            if (2 * j + 1 < row) p1 = 0.f;
+        for (int j = 0; j < 32; ++j) {
+          const float2 l2 = *reinterpret_cast<const float2*>(lse + 2 * j);
+          float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -l2.x * kLog2e));
+          float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -l2.y * kLog2e));
+          if (diag) {  // query column 64*half + c is visible iff c >= row
+            if (64 * half + 2 * j < row) p0 = 0.f;
+            if (64 * half + 2 * j + 1 < row) p1 = 0.f;
           }
           pk[j] = pack_bf16(p0, p1);
         }
-        tmem_st32(tl + kColS + 0, pk);
-        tmem_st32(tl + kColS + 32, pk + 32);
+        if (!halves_meet(bar(kBarRdS), rs_ph, wc)) {
+          ok = false;
+          break;
+        }
+        tmem_st32(tl + kColS + 32 * half, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarP));
-        // dS^T = scale * P^T (dP^T - Delta) -> shared memory (bf16, swizzled)
+        // dS^T = scale * P^T (dP^T - Delta)
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP), dp_ph, wc))) {
           ok = false;
           break;
         }
         dp_ph ^= 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDSFree), dsf_ph, wc))) {
+        tc_fence_after();
+        tmem_ld32(tl + kColDP + 64 * half, r);
+        tmem_ld32(tl + kColDP + 64 * half + 32, r + 32);
+        tmem_wait_ld_regs(r);
+        reg_fence32(r + 32);
+        uint32_t ds[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j]));
+          const float2 dl = *reinterpret_cast<const float2*>(dlt + 2 * j);
+          ds[j] = pack_bf16(scale * p.x * (__uint_as_float(r[2 * j]) - dl.x),
+                            scale * p.y * (__uint_as_float(r[2 * j + 1]) - dl.y));
+        }
+        if (!halves_meet(bar(kBarRdDP), rdp_ph, wc)) {
           ok = false;
           break;
         }
-        dsf_ph ^= 1;
-        tc_fence_after();
-        uint8_t* ds_row = smem + kOffDS + row * 128;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t d[32];
-          tmem_ld32(tl + kColDP + cc * 32, d);
-          tmem_wait_ld_regs(d);
-          uint32_t w[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int col = cc * 32 + 2 * j;
-            const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[col / 2]));
-            const float2 dl = *reinterpret_cast<const float2*>(dlt_s + col);
-            w[j] = pack_bf16(scale * p.x * (__uint_as_float(d[2 * j]) - dl.x),
-                             scale * p.y * (__uint_as_float(d[2 * j + 1]) - dl.y));
-          }
-          const int box = cc >> 1;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int cb = (cc & 1) * 4 + u;  // 16-byte chunk within the 128-byte row
-            uint4 v = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            *reinterpret_cast<uint4*>(ds_row + box * kBoxBytes + ((cb ^ (row & 7)) << 4)) = v;
-          }
-        }
-        fence_async_smem();
+        tmem_st32(tl + kColDP + 32 * half, ds);
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarDS));
-        mbar_arrive(bar(kBarLseFree));
-        cur_l = nl;
-        cur_d = nd;
-        qrow = nqrow;
-        diag = ndiag;
-        have = nhave;
-      }
-    }
-  } else if (warp >= 8) {
-    // ------------------------------------------------ dQ reduction, dK / dV
-    const int wq = warp & 3;
-    const int lrow = wq * 32 + lane;  // TMEM lane: query row of dQ_t, K/V row of dK / dV
-    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
-    uint32_t dq_ph = 0;
-    bool ok = true;
-    for (int k = 0; ok; ++k) {
-      const int idx = item_index(k, blockIdx.x, gridDim.x);
-      if (idx >= n_items) break;
-      const Item it = decode_item(sh, idx);
-      QSeq seq;
-      seq.init(sh, it);
-      const int h = it.h;
-      int qrow;
-      bool diag;
-      while (seq.next(qrow, diag)) {
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDQ), dq_ph, wc))) {
-          ok = false;
-          break;
-        }
-        dq_ph ^= 1;
-        tc_fence_after();
-        float* dst = args.dq_acc + (((int64_t)it.b * sh.S + qrow + lrow) * sh.H + h) * kD;
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t d[32];
-          tmem_ld32(tl + kColDP + cc * 32, d);
-          tmem_wait_ld_regs(d);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            atomicAdd(reinterpret_cast<float4*>(dst + cc * 32 + 4 * u),
-                      make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]),
-                                  __uint_as_float(d[4 * u + 2]), __uint_as_float(d[4 * u + 3])));
-        }
-        tc_fence_before();
-        mbar_arrive(bar(kBarDQFree));
+        ++qi;
       }
       if (!ok) break;
+      // Epilogue: this head's dK / dV partial, columns [64*half, +64).
       if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAcc), k & 1, wc))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const int64_t kbase = (((int64_t)it.b * sh.S + it.kvrow + lrow) * sh.Hkv + it.g) * kD;
+      const int64_t pbase =
+          (((int64_t)it.b * sh.S + it.kv.row + row) * sh.H + it.h) * kD + 64 * half;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        float* dst = (which == 0 ? args.dv_acc : args.dk_acc) + kbase;
-        const uint32_t col = which == 0 ? kColDV : kColDK;
+        float* dst = (which == 0 ? args.dv_part : args.dk_part) + pbase;
+        const uint32_t col = (which == 0 ? kColDV : kColDK) + 64 * half;
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
+        for (int cc = 0; cc < 2; ++cc) {
           uint32_t d[32];
-          tmem_ld32(tl + col + cc * 32, d);
+          tmem_ld32(tl + col + 32 * cc, d);
           tmem_wait_ld_regs(d);
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            atomicAdd(reinterpret_cast<float4*>(dst + cc * 32 + 4 * u),
-                      make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]),
-                                  __uint_as_float(d[4 * u + 2]), __uint_as_float(d[4 * u + 3])));
+            *reinterpret_cast<float4*>(dst + 32 * cc + 4 * u) =
+                make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]),
+                            __uint_as_float(d[4 * u + 2]), __uint_as_float(d[4 * u + 3]));
         }
       }
       tc_fence_before();
@@ -577,6 +606,390 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_dealloc(tmem, 512);
   }
 }
+
+}  // namespace kv
+
+// ===========================================================================
+// dq kernel
+// ===========================================================================
+namespace qm {
+
+constexpr int kOffQ = 0;
+constexpr int kOffDO = kOffQ + kTileBytes;
+constexpr int kOffK = kOffDO + kTileBytes;     // [2] stages
+constexpr int kOffV = kOffK + 2 * kTileBytes;  // [2]
+constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kBarQFull = 0;
+constexpr int kBarQEmpty = 1;
+constexpr int kBarKVFull = 2;   // [2]
+constexpr int kBarKVEmpty = 4;  // [2]
+constexpr int kBarS = 6;
+constexpr int kBarSFree = 7;
+constexpr int kBarDP = 8;       // [2]
+constexpr int kBarDS = 10;
+constexpr int kBarAcc = 11;
+constexpr int kBarAccFree = 12;
+constexpr int kBarDrain = 13;
+constexpr int kBarRdDP = 14;  // both halves have read dP
+constexpr int kNumBars = 15;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr uint32_t kColS = 0, kColDQ = 384;
+__host__ __device__ constexpr uint32_t col_dp(int b) { return 128u + 128u * (uint32_t)b; }
+
+struct Item {
+  int b, h, g, knat;
+  TilePos q;
+};
+
+// Latest natural query tile first (it sees the most K/V tiles), then
+// (batch, query head): the heads sharing one kv head run side by side.
+__device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
+  const int BH = sh.B * sh.H;
+  const int ntiles = sh.S / kT;
+  const int knat = ntiles - 1 - idx / BH;
+  const int bh = idx - (idx / BH) * BH;
+  Item it;
+  it.b = bh / sh.H;
+  it.h = bh - it.b * sh.H;
+  it.g = it.h / (sh.H / sh.Hkv);
+  it.knat = knat;
+  it.q = tile_pos(sh, knat);
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+              const BwdArgs args, int n_items) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + kOffQ, sDO = base + kOffDO, sK = base + kOffK, sV = base + kOffV;
+  const uint32_t bars = base + kOffBar;
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+  const RingShape& sh = args.sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{abort_flag, args.err};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarKVFull + i), 1);
+      mbar_init(bar(kBarKVEmpty + i), 1);
+      mbar_init(bar(kBarDP + i), 1);
+    }
+    mbar_init(bar(kBarS), 1);
+    mbar_init(bar(kBarSFree), 256);
+    mbar_init(bar(kBarDS), 256);
+    mbar_init(bar(kBarAcc), 1);
+    mbar_init(bar(kBarAccFree), 256);
+    mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarRdDP), 256);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      uint32_t kj = 0, q_armed = 0, kv_armed[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int idx = item_index(k, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = decode(sh, idx);
+        if (!mbar_wait(bar(kBarQEmpty), (k & 1) ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+        ++q_armed;
+        const int qrow = it.b * sh.S + it.q.row;
+        for (int half = 0; half < 2; ++half) {
+          tma_load_3d(sQ + half * kBoxBytes, &tm_q, bar(kBarQFull), half * 64, it.h, qrow);
+          tma_load_3d(sDO + half * kBoxBytes, &tm_do, bar(kBarQFull), half * 64, it.h, qrow);
+        }
+        KSeq seq;
+        seq.init(sh, it.q, it.knat);
+        int kvrow;
+        bool diag;
+        while (seq.next(kvrow, diag)) {
+          const int st = kj & 1;
+          const uint32_t ph = (kj >> 1) & 1;
+          if (!mbar_wait(bar(kBarKVEmpty + st), ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarKVFull + st), 2 * kTileBytes);
+          ++kv_armed[st];
+          const int krow = it.b * sh.S + kvrow;
+          for (int half = 0; half < 2; ++half) {
+            tma_load_3d(sK + st * kTileBytes + half * kBoxBytes, &tm_k, bar(kBarKVFull + st),
+                        half * 64, it.g, krow);
+            tma_load_3d(sV + st * kTileBytes + half * kBoxBytes, &tm_v, bar(kBarKVFull + st),
+                        half * 64, it.g, krow);
+          }
+          ++kj;
+        }
+      }
+      if (!ok) {
+        if (q_armed) mbar_drain(bar(kBarQFull), (q_armed - 1) & 1);
+        for (int s = 0; s < 2; ++s)
+          if (kv_armed[s]) mbar_drain(bar(kBarKVFull + s), (kv_armed[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      uint32_t kj = 0, sf_ph = 0, ds_ph = 0;
+      bool ok = true;
+      auto issue_s = [&](int st) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024),
+                 sdesc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(bar(kBarS));
+      };
+      auto issue_dp = [&](int st, int buf) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + col_dp(buf), sdesc_sw128(sDO + off, 16, 1024),
+                 sdesc_sw128(sV + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(bar(kBarDP + buf));
+      };
+      for (int k = 0; ok; ++k) {
+        const int idx = item_index(k, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = decode(sh, idx);
+        if (!mbar_wait(bar(kBarQFull), k & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        KSeq seq;
+        seq.init(sh, it.q, it.knat);
+        int kvrow;
+        bool diag;
+        bool have = seq.next(kvrow, diag);
+        if (have) {
+          const int st = kj & 1;
+          if (!mbar_wait(bar(kBarKVFull + st), (kj >> 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(st);
+          issue_dp(st, kj & 1);
+        }
+        bool first = true;
+        while (have) {
+          const int st = kj & 1;
+          int nkvrow;
+          bool ndiag;
+          const bool nhave = seq.next(nkvrow, ndiag);
+          const int nst = (kj + 1) & 1;
+          if (nhave) {
+            if (!mbar_wait(bar(kBarKVFull + nst), ((kj + 1) >> 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            // S is released as soon as the elementwise warps have read it.
+            if (!mbar_wait(bar(kBarSFree), sf_ph, wc)) {
+              ok = false;
+              break;
+            }
+            sf_ph ^= 1;
+            tc_fence_after();
+            issue_s(nst);
+            // dP into the other buffer: the dQ that read it two tiles ago was
+            // issued earlier, and MMAs execute in issue order.
+            issue_dp(nst, (kj + 1) & 1);
+          }
+          // dQ += dS K
+          if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
+            ok = false;
+            break;
+          }
+          ds_ph ^= 1;
+          if (first && !mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + kk * 8,
+                   sdesc_sw128(sK + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   (!first || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kBarKVEmpty + st));
+          first = false;
+          ++kj;
+          have = nhave;
+        }
+        if (!ok) break;
+        if (first) {
+          // No K/V tile at all (only possible without a causal diagonal): the
+          // epilogue writes zeros; it still waits for the previous epilogue.
+          if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+        } else {
+          // The item's last S was read but not overwritten: take its release
+          // so that the next item's first S waits on a fresh phase.
+          if (!mbar_wait(bar(kBarSFree), sf_ph, wc)) {
+            ok = false;
+            break;
+          }
+          sf_ph ^= 1;
+        }
+        mma_commit(bar(kBarAcc));
+        mma_commit(bar(kBarQEmpty));
+      }
+      if (!ok) {
+        mma_commit(bar(kBarDrain));
+        mbar_drain(bar(kBarDrain), 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ----------------------------------------------- elementwise + dQ epilogue
+    const int half = (warp - 4) >> 2;  // K/V columns [64*half, 64*half + 64)
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;    // query row of the tile (TMEM lane)
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = sh.scale_log2, scale = sh.scale;
+    uint32_t kj = 0, s_ph = 0, dp_ph[2] = {0, 0}, rdp_ph = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int idx = item_index(k, blockIdx.x, gridDim.x);
+      if (idx >= n_items) break;
+      const Item it = decode(sh, idx);
+      const int64_t li = ((int64_t)it.b * sh.H + it.h) * sh.S + it.q.row + row;
+      const float nlse2 = -args.lse[li] * kLog2e;
+      const float dlt = args.delta[li];
+      KSeq seq;
+      seq.init(sh, it.q, it.knat);
+      int kvrow;
+      bool diag;
+      int ntiles = 0;
+      while (seq.next(kvrow, diag)) {
+        const int buf = kj & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS), s_ph, wc))) {
+          ok = false;
+          break;
+        }
+        s_ph ^= 1;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(tl + kColS + 64 * half, r);
+        tmem_ld32(tl + kColS + 64 * half + 32, r + 32);
+        tmem_wait_ld_regs(r);
+        reg_fence32(r + 32);
+        tc_fence_before();
+        mbar_arrive(bar(kBarSFree));
+        float p[64];
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          p[j] = ex2(fmaf(__uint_as_float(r[j]), sl2, nlse2));
+          if (diag && 64 * half + j > row) p[j] = 0.f;  // key after the query
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP + buf), dp_ph[buf], wc))) {
+          ok = false;
+          break;
+        }
+        dp_ph[buf] ^= 1;
+        tc_fence_after();
+        tmem_ld32(tl + col_dp(buf) + 64 * half, r);
+        tmem_ld32(tl + col_dp(buf) + 64 * half + 32, r + 32);
+        tmem_wait_ld_regs(r);
+        reg_fence32(r + 32);
+        uint32_t ds[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          ds[j] = pack_bf16(scale * p[2 * j] * (__uint_as_float(r[2 * j]) - dlt),
+                            scale * p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dlt));
+        if (!halves_meet(bar(kBarRdDP), rdp_ph, wc)) {
+          ok = false;
+          break;
+        }
+        tmem_st32(tl + col_dp(buf) + 32 * half, ds);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarDS));
+        ++kj;
+        ++ntiles;
+      }
+      if (!ok) break;
+      // Epilogue: dQ row, columns [64*half, +64), in the gradient dtype.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAcc), k & 1, wc))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int64_t obase =
+          (((int64_t)it.b * sh.S + it.q.row + row) * sh.H + it.h) * kD + 64 * half;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t d[32];
+        tmem_ld32(tl + kColDQ + 64 * half + 32 * cc, d);
+        tmem_wait_ld_regs(d);
+        if (ntiles == 0) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) d[j] = 0u;
+        }
+        if (args.dq_f32) {
+          float* dst = static_cast<float*>(args.dq) + obase + 32 * cc;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(dst + 4 * u) =
+                make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]),
+                            __uint_as_float(d[4 * u + 2]), __uint_as_float(d[4 * u + 3]));
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.dq) + obase + 32 * cc;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 v;
+            v.x = pack_bf16(__uint_as_float(d[8 * u + 0]), __uint_as_float(d[8 * u + 1]));
+            v.y = pack_bf16(__uint_as_float(d[8 * u + 2]), __uint_as_float(d[8 * u + 3]));
+            v.z = pack_bf16(__uint_as_float(d[8 * u + 4]), __uint_as_float(d[8 * u + 5]));
+            v.w = pack_bf16(__uint_as_float(d[8 * u + 6]), __uint_as_float(d[8 * u + 7]));
+            *reinterpret_cast<uint4*>(dst + 8 * u) = v;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarAccFree));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace qm
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -626,10 +1039,17 @@ cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = cudaFuncSetAttribute(kv::dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kv::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(qm::dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           qm::kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = n_items < sms ? n_items : sms;
-  tc_bwd_kernel<<<grid, kThreads, kSmemBytes, stream>>>(mq, mk, mv, mdo, a, n_items);
+  kv::dkdv_kernel<<<grid, kThreads, kv::kSmemBytes, stream>>>(mq, mk, mv, mdo, a, n_items);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  qm::dq_kernel<<<grid, kThreads, qm::kSmemBytes, stream>>>(mq, mk, mv, mdo, a, n_items);
   return cudaGetLastError();
 }
 

@@ -195,11 +195,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
     for (int e = 0; e < EPL; ++e) acc = fmaf(a[e], b[e], acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    float* dq = dq_acc + row * D + lane * EPL;
-    if constexpr (EPL == 4) {
-      *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
-    } else {
-      *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+    if (dq_acc != nullptr) {
+      float* dq = dq_acc + row * D + lane * EPL;
+      if constexpr (EPL == 4) {
+        *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        *reinterpret_cast<float2*>(dq) = make_float2(0.f, 0.f);
+      }
     }
     if (lane == 0) {
       int64_t bi = row / ((int64_t)S * H), si = (row / H) % S, hi = row % H;
@@ -229,6 +231,33 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, int64_
   v.x = *reinterpret_cast<uint32_t*>(&lo);
   v.y = *reinterpret_cast<uint32_t*>(&hi);
   reinterpret_cast<uint2*>(dst)[i] = v;
+}
+
+// Sum of the per-query-head dK / dV partials over each kv head's group.
+template <typename O>
+__global__ void __launch_bounds__(256) grad_reduce_kernel(const float4* __restrict__ dk_part,
+                                                          const float4* __restrict__ dv_part,
+                                                          O* __restrict__ dk, O* __restrict__ dv,
+                                                          int64_t rows_kv, int H, int Hkv,
+                                                          int D4) {
+  const int grp = H / Hkv;
+  const int64_t total = rows_kv * D4;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / D4;  // (b*S + s)*Hkv + g
+    const int d4 = (int)(i - row * D4);
+    const int64_t bs = row / Hkv;
+    const int g = (int)(row - bs * Hkv);
+    const int64_t p0 = ((bs * H + (int64_t)g * grp) * D4) + d4;
+    float4 a = dk_part[p0], b = dv_part[p0];
+    for (int hh = 1; hh < grp; ++hh) {
+      const float4 x = dk_part[p0 + (int64_t)hh * D4], y = dv_part[p0 + (int64_t)hh * D4];
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      b.x += y.x; b.y += y.y; b.z += y.z; b.w += y.w;
+    }
+    store4<O>(dk, i, a);
+    store4<O>(dv, i, b);
+  }
 }
 
 template <typename O>
@@ -308,6 +337,25 @@ cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, flo
       bwd_prep_kernel<float, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B,
                                                            S, H);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grad_reduce(const float* dk_part, const float* dv_part, void* dk, void* dv,
+                               int B, int S, int H, int Hkv, int D, int out_dtype,
+                               cudaStream_t stream) {
+  const int64_t rows_kv = (int64_t)B * S * Hkv;
+  const int D4 = D / 4;
+  if (rows_kv == 0) return cudaSuccess;
+  int grid = grid_for(rows_kv * D4, 256, 8);
+  auto k4 = reinterpret_cast<const float4*>(dk_part);
+  auto v4 = reinterpret_cast<const float4*>(dv_part);
+  if (out_dtype == 1)
+    grad_reduce_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(
+        k4, v4, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv), rows_kv, H, Hkv,
+        D4);
+  else
+    grad_reduce_kernel<float><<<grid, 256, 0, stream>>>(
+        k4, v4, static_cast<float*>(dk), static_cast<float*>(dv), rows_kv, H, Hkv, D4);
   return cudaGetLastError();
 }
 

@@ -52,5 +52,5 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     rc = lib.cpattn_ring_bwd_noalloc(*([fake] * 9), 1, 32, 32, 8192, 128, 4, 1, 1, 1, 0.0, null)
     assert rc == _binding.ERR_WORKSPACE
     # A smaller problem of the same kind fits.
-    need = lib.cpattn_ring_bwd_workspace_bytes(1, 32, 8, 2048, 128, 1)
+    need = lib.cpattn_ring_bwd_workspace_bytes(1, 32, 8, 1024, 128, 1)
     assert need <= 64 << 20
