@@ -188,8 +188,11 @@ def run_ours(args):
             cpa.zigzag_unpermute(dk, cp, layout, out=dk_nat)
             cpa.zigzag_unpermute(dv, cp, layout, out=dv_nat)
 
-    launches_per_step = (4 if w.backward else 3) + 1 + (3 if w.backward else 0) + \
-        (5 if w.backward else 2)
+    bwd_path = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype, backward=True)[0] \
+        if w.backward else None
+    # permutes + forward + backward (pre-pass, kernel(s), finishing pass) + unpermutes
+    bwd_launches = (4 if bwd_path == cpa.PATH_TCGEN05 else 3) if w.backward else 0
+    launches_per_step = (4 if w.backward else 3) + 1 + bwd_launches + (5 if w.backward else 2)
     fwd_flops = w.useful_flops(False)
     bwd_flops = w.useful_flops(True) if w.backward else 0.0
     step_flops = fwd_flops + bwd_flops

@@ -259,12 +259,14 @@ struct Item {
   TilePos kv;
 };
 
-// Earliest natural K/V tile first (seen by the most query tiles), then
-// (batch, query head): the heads sharing one K/V tile run side by side.
+// (batch, query head) outermost, then the K/V tiles earliest first (an
+// early tile is seen by the most query tiles).  Consecutive items -- the CTAs
+// running at the same time -- share one head, so the Q / dO tiles they all
+// stream stay in L2 (one head's Q and dO: 2 * S * D * 2 bytes).
 __device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
-  const int BH = sh.B * sh.H;
-  const int knat = idx / BH;
-  const int bh = idx - knat * BH;
+  const int ntiles = sh.S / kT;
+  const int bh = idx / ntiles;
+  const int knat = idx - bh * ntiles;
   Item it;
   it.b = bh / sh.H;
   it.h = bh - it.b * sh.H;

@@ -1,0 +1,54 @@
+"""Runs one workload's forward (and backward) a few times: the program that
+profiler captures (ncu) wrap.
+
+    python -m context_causal_attention_zigzag_gb300.profile_case fwd_s32768
+    python -m context_causal_attention_zigzag_gb300.profile_case bwd_s16384
+
+Cases are reduced versions of the named workloads (same heads, head dim and
+layout; fewer tokens or batches) so that a full counter capture of one launch
+stays small: a few hundred MB on the device and a few ms per launch.
+"""
+import argparse
+
+import torch
+
+from . import _binding as cpa
+from . import inputs
+
+CASES = {
+    # half of the S=32768 forward workload (one batch of two)
+    "fwd_s32768": inputs.Workload("fwd_s32768", 1, 32, 8, 32768, 128, 8, cpa.ZIGZAG, True,
+                                  torch.bfloat16, backward=False, seed=5),
+    # the S=131072 forward+backward workload at S=16384 (1/64 of its tile pairs)
+    "bwd_s16384": inputs.Workload("bwd_s16384", 1, 32, 8, 16384, 128, 4, cpa.ZIGZAG, True,
+                                  torch.bfloat16, backward=True, seed=5),
+}
+
+
+def run(case: str, repeats: int = 3) -> int:
+    w = CASES[case]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    q, k, v, do = (x.to(dev) if x is not None else None for x in inputs.generate(w))
+    qs, ks, vs = (cpa.zigzag_permute(x, w.cp, w.layout) for x in (q, k, v))
+    dos = cpa.zigzag_permute(do, w.cp, w.layout) if do is not None else None
+    for _ in range(repeats):
+        o, lse = cpa.ring_fwd(qs, ks, vs, w.cp, w.layout, w.causal)
+        if dos is not None:
+            cpa.ring_bwd(qs, ks, vs, o, dos, lse, w.cp, w.layout, w.causal,
+                         grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    return cpa.device_status()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--repeats", type=int, default=3)
+    a = ap.parse_args()
+    status = run(a.case, a.repeats)
+    print(f"{a.case}: status {status}")
+    raise SystemExit(0 if status == 0 else 1)
+
+
+if __name__ == "__main__":
+    main()
