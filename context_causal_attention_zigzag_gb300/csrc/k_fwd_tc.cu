@@ -15,7 +15,9 @@
 //
 // CTA = 384 threads:
 //   warp 0      TMA producer: Q pair once per item, K and V tiles into a
-//               2-stage ring of 32 KB buffers.
+//               ring of five 32 KB slots (K(j), V(j), K(j+1), ... take
+//               consecutive slots; a slot is freed as soon as the MMAs that
+//               read it retire, so loads run up to two tiles ahead).
 //   warp 1      TMEM owner and MMA issuer (one thread):
 //               S_i = Q_i K^T  (SS form, 128x128x128, fp32 in TMEM),
 //               O_i += P_i V   (TS form: P read from TMEM, V MN-major).
@@ -44,21 +46,18 @@ constexpr int kT = 128;                     // tile edge (rows, keys)
 constexpr int kD = 128;                     // head dim
 constexpr int kBoxBytes = kT * 64 * 2;      // [128 rows][64 bf16] = 16 KB
 constexpr int kTileBytes = 2 * kBoxBytes;   // [128 rows][128 bf16] = 32 KB
-constexpr int kStages = 2;
+constexpr int kSlots = 5;  // K/V ring: K(j), V(j) take consecutive slots
 constexpr int kThreads = 384;
 
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + 2 * kTileBytes;
-constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kOffRing = kOffQ + 2 * kTileBytes;
+constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
 // barriers
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
-constexpr int kBarKFull = 2;
-constexpr int kBarKEmpty = kBarKFull + kStages;
-constexpr int kBarVFull = kBarKEmpty + kStages;
-constexpr int kBarVEmpty = kBarVFull + kStages;
-constexpr int kBarS = kBarVEmpty + kStages;  // [2]
+constexpr int kBarFull = 2;                 // [kSlots]
+constexpr int kBarEmpty = kBarFull + kSlots;  // [kSlots]
+constexpr int kBarS = kBarEmpty + kSlots;     // [2]
 constexpr int kBarP = kBarS + 2;             // [2]
 constexpr int kBarO = kBarP + 2;             // [2]
 constexpr int kBarDrain = kBarO + 2;
@@ -184,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + kOffQ, sK = base + kOffK, sV = base + kOffV;
+  const uint32_t sQ = base + kOffQ, sRing = base + kOffRing;
+  auto slot = [&](uint32_t n) { return sRing + (n % kSlots) * kTileBytes; };
   const uint32_t bars = base + kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -197,11 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 1);
-      mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarVEmpty + s), 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(bar(kBarFull + s), 1);
+      mbar_init(bar(kBarEmpty + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarS + i), 1);
@@ -227,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      uint32_t kv_it = 0, q_armed = 0, k_armed[kStages] = {0}, v_armed[kStages] = {0};
+      uint32_t seq = 0, q_armed = 0, armed[kSlots] = {0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -244,41 +242,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int half = 0; half < 2; ++half)
             tma_load_3d(sQ + tq * kTileBytes + half * kBoxBytes, &tm_q, bar(kBarQFull), half * 64,
                         it.h, row0 + tq * kT);
-        KvSeq seq;
-        seq.init(sh, args.t_begin, args.t_end, it);
+        KvSeq kseq;
+        kseq.init(sh, args.t_begin, args.t_end, it);
         int kvrow, fl, step;
-        while (seq.next(kvrow, fl, step)) {
-          const int st = kv_it % kStages;
-          const uint32_t ph = (kv_it / kStages) & 1;
+        while (ok && kseq.next(kvrow, fl, step)) {
           const int krow = it.b * sh.S + kvrow;
-          if (!mbar_wait(bar(kBarKEmpty + st), ph ^ 1, wc)) {
-            ok = false;
-            break;
+          for (int which = 0; which < 2; ++which) {  // K(j), then V(j)
+            const uint32_t n = seq++;
+            const int sl = n % kSlots;
+            if (!mbar_wait(bar(kBarEmpty + sl), ((n / kSlots) & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kBarFull + sl), kTileBytes);
+            ++armed[sl];
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(slot(n) + half * kBoxBytes, which == 0 ? &tm_k : &tm_v,
+                          bar(kBarFull + sl), half * 64, it.g, krow);
           }
-          mbar_arrive_expect_tx(bar(kBarKFull + st), kTileBytes);
-          ++k_armed[st];
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(sK + st * kTileBytes + half * kBoxBytes, &tm_k, bar(kBarKFull + st),
-                        half * 64, it.g, krow);
-          if (!mbar_wait(bar(kBarVEmpty + st), ph ^ 1, wc)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(kBarVFull + st), kTileBytes);
-          ++v_armed[st];
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(sV + st * kTileBytes + half * kBoxBytes, &tm_v, bar(kBarVFull + st),
-                        half * 64, it.g, krow);
-          ++kv_it;
         }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA exits.
         if (q_armed) mbar_drain(bar(kBarQFull), (q_armed - 1) & 1);
-        for (int s = 0; s < kStages; ++s) {
-          if (k_armed[s]) mbar_drain(bar(kBarKFull + s), (k_armed[s] - 1) & 1);
-          if (v_armed[s]) mbar_drain(bar(kBarVFull + s), (v_armed[s] - 1) & 1);
-        }
+        for (int s = 0; s < kSlots; ++s)
+          if (armed[s]) mbar_drain(bar(kBarFull + s), (armed[s] - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -305,10 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         unsigned long long census = 0;
         int census_step = step;
-        // S for the first tile.
-        int st = kv_it % kStages;
-        uint32_t kph = (kv_it / kStages) & 1;
-        if (!mbar_wait(bar(kBarKFull + st), kph, wc)) {
+        // S for the first tile: K(j) is ring entry 2*kv_it, V(j) entry 2*kv_it + 1.
+        uint32_t kn = 2 * kv_it;
+        if (!mbar_wait(bar(kBarFull + kn % kSlots), (kn / kSlots) & 1, wc)) {
           ok = false;
           break;
         }
@@ -318,18 +305,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
             mma_ss(tmem + col_s(i), sdesc_sw128(sQ + i * kTileBytes + off, 16, 1024),
-                   sdesc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
+                   sdesc_sw128(slot(kn) + off, 16, 1024), kIdescQK, kk > 0);
           }
           mma_commit(bar(kBarS + i));
         }
-        mma_commit(bar(kBarKEmpty + st));
+        mma_commit(bar(kBarEmpty + kn % kSlots));
         uint32_t acc[2] = {0, 0};
         while (true) {
           int nkvrow, nfl = 0, nstep = 0;
           const bool have_next = seq.next(nkvrow, nfl, nstep);
-          const int nst = (kv_it + 1) % kStages;
-          const uint32_t nkph = ((kv_it + 1) / kStages) & 1;
-          if (!mbar_wait(bar(kBarVFull + st), kph, wc)) {
+          const uint32_t vn = 2 * kv_it + 1, nkn = 2 * kv_it + 2;
+          if (!mbar_wait(bar(kBarFull + vn % kSlots), (vn / kSlots) & 1, wc)) {
             ok = false;
             break;
           }
@@ -345,13 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               for (int kk = 0; kk < kT / 16; ++kk)
                 mma_ts(tmem + col_o(i), tmem + col_s(i) + kk * 8,
-                       sdesc_sw128(sV + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescPV,
+                       sdesc_sw128(slot(vn) + kk * 2048, kBoxBytes, 1024), kIdescPV,
                        acc[i] | (kk > 0));
               acc[i] = 1;
             }
             if (have_next && (nfl & (kUse0 << i))) {
               if (!k_ready) {
-                if (!mbar_wait(bar(kBarKFull + nst), nkph, wc)) {
+                if (!mbar_wait(bar(kBarFull + nkn % kSlots), (nkn / kSlots) & 1, wc)) {
                   ok = false;
                   break;
                 }
@@ -361,14 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
                 mma_ss(tmem + col_s(i), sdesc_sw128(sQ + i * kTileBytes + off, 16, 1024),
-                       sdesc_sw128(sK + nst * kTileBytes + off, 16, 1024), kIdescQK, kk > 0);
+                       sdesc_sw128(slot(nkn) + off, 16, 1024), kIdescQK, kk > 0);
               }
               mma_commit(bar(kBarS + i));
             }
           }
           if (!ok) break;
-          mma_commit(bar(kBarVEmpty + st));
-          if (have_next) mma_commit(bar(kBarKEmpty + nst));
+          mma_commit(bar(kBarEmpty + vn % kSlots));
+          if (have_next) mma_commit(bar(kBarEmpty + nkn % kSlots));
           if (args.tiles_rt != nullptr) {
             if (step != census_step) {
               atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
@@ -382,8 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           kvrow = nkvrow;
           fl = nfl;
           step = nstep;
-          st = nst;
-          kph = nkph;
         }
         if (!ok) break;
         if (args.tiles_rt != nullptr && census)
