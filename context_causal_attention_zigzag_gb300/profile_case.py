@@ -22,6 +22,8 @@ CASES = {
     # the S=131072 forward+backward workload at S=16384 (1/64 of its tile pairs)
     "bwd_s16384": inputs.Workload("bwd_s16384", 1, 32, 8, 16384, 128, 4, cpa.ZIGZAG, True,
                                   torch.bfloat16, backward=True, seed=5),
+    # the S=131072 forward+backward workload itself (for single-pass counters only)
+    "c5_full": inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"],
 }
 
 
