@@ -44,6 +44,18 @@ METRIC = "useful causal attention TFLOP/s on 1 GB300 (fwd, fwd+bwd) and % of BF1
 UNIT = "TFLOP/s"
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum), from
+# one single-pass ncu capture of the current kernels on the full workload
+# (profiles/dram_traffic_c5_fwdbwd_b1_h32_hkv8_s131072_cp16.md).  Null for a
+# workload without a capture; must be re-taken whenever a kernel changes.
+CAPTURED_TRAFFIC = {
+    "c5_bf16_s131072_fwdbwd": {
+        "ring_bwd": (2.15e9 + 16.56e6) + (33.48e9 + 4.40e9) + (5.67e9 + 2.12e9) + (4.30e9 + 1.05e9),
+        "ring_fwd": 3.57e9 + 1.07e9,
+    },
+}
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -273,11 +285,13 @@ def run_ours(args):
     dom_ms, dom_flops, dom_name = (bwd_ms, bwd_flops, "ring_bwd") \
         if (w.backward and bwd_ms >= fwd_ms) else (fwd_ms, fwd_flops, "ring_fwd")
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+    traffic = CAPTURED_TRAFFIC.get(w.name, {}).get(dom_name)
     roofline = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_kind": f"{peak_kind} bf16 burst", "ms": dom_ms,
                 "frac_of_sustained": achieved / peak_sus}
-    fwd_info = {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12}
+    fwd_info = {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
+                "traffic": CAPTURED_TRAFFIC.get(w.name, {}).get("ring_fwd")}
     fwd_info["frac"] = fwd_info["tflops"] / peak
     if w.backward:
         fwd_info["bwd_ms"] = bwd_ms

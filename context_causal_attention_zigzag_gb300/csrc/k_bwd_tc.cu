@@ -644,17 +644,20 @@ struct Item {
   TilePos q;
 };
 
-// Latest natural query tile first (it sees the most K/V tiles), then
-// (batch, query head): the heads sharing one kv head run side by side.
+// (batch, kv head) outermost, then the query tiles latest first (a late tile
+// sees the most K/V tiles), then the query heads of the kv head: the CTAs in
+// flight share one kv head's K/V through L2.
 __device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
-  const int BH = sh.B * sh.H;
+  const int grp = sh.H / sh.Hkv;
   const int ntiles = sh.S / kT;
-  const int knat = ntiles - 1 - idx / BH;
-  const int bh = idx - (idx / BH) * BH;
+  const int per_group = ntiles * grp;
+  const int gi = idx / per_group;
+  const int rem = idx - gi * per_group;
+  const int knat = ntiles - 1 - rem / grp;
   Item it;
-  it.b = bh / sh.H;
-  it.h = bh - it.b * sh.H;
-  it.g = it.h / (sh.H / sh.Hkv);
+  it.b = gi / sh.Hkv;
+  it.g = gi - it.b * sh.Hkv;
+  it.h = it.g * grp + (rem - (rem / grp) * grp);
   it.knat = knat;
   it.q = tile_pos(sh, knat);
   return it;

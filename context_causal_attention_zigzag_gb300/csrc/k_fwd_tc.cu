@@ -81,17 +81,22 @@ struct Item {
   int b, h, g, r, qc, a, qrow;  // qc: natural chunk, a: natural tile of query tile 0
 };
 
-// Work items in order of decreasing cost (natural query position), heads
-// innermost so that the query heads of one kv head run side by side.
+// Work items: (batch, kv head) outermost, then query pairs in order of
+// decreasing cost (natural query position), then the query heads of the kv
+// head.  The CTAs running at the same time therefore share one kv head's K/V
+// (2 * S * D * 2 bytes) through L2, and every round of the snake deal holds
+// items of similar cost.
 __device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
-  const int BH = sh.B * sh.H;
+  const int grp = sh.H / sh.Hkv;
   const int npair = sh.S / (2 * kT);
-  const int pr = npair - 1 - idx / BH;
-  const int bh = idx - (idx / BH) * BH;
+  const int per_group = npair * grp;
+  const int gi = idx / per_group;
+  const int rem = idx - gi * per_group;
+  const int pr = npair - 1 - rem / grp;
   Item it;
-  it.b = bh / sh.H;
-  it.h = bh - it.b * sh.H;
-  it.g = it.h / (sh.H / sh.Hkv);
+  it.b = gi / sh.Hkv;
+  it.g = gi - it.b * sh.Hkv;
+  it.h = it.g * grp + (rem - (rem / grp) * grp);
   const int nat0 = pr * 2 * kT;
   it.qc = nat0 / sh.c;
   const int off = nat0 - it.qc * sh.c;
