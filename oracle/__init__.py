@@ -61,6 +61,15 @@ def _lib(mutation: int = 0):
                                                      + [_i64p, _L, _i64p, _L, _f64p, _f64p])
     lib.oracle_tile_counts.argtypes = [_L, _I, _I, _I, _L, _u64p, ctypes.c_void_p]
     lib.oracle_tile_counts.restype = _I
+    docs = [_i64p, _L]
+    lib.oracle_attn_fwd_docs.argtypes = [_f32p, _f32p, _f32p] + shape + docs + [_f64p, _f64p]
+    lib.oracle_ring_fwd_docs.argtypes = ([_f32p, _f32p, _f32p] + ring + docs
+                                         + [_I, _f64p, _f64p])
+    lib.oracle_ring_fwd_docs.restype = _I
+    lib.oracle_attn_bwd_docs.argtypes = [_f32p] * 4 + shape + docs + [_f64p] * 3
+    lib.oracle_tile_counts_docs.argtypes = ([_L, _I, _I, _I] + docs
+                                            + [_L, _u64p, ctypes.c_void_p])
+    lib.oracle_tile_counts_docs.restype = _I
     _libs[mutation] = lib
     return lib
 
@@ -204,4 +213,65 @@ def tile_counts(S, cp, layout, causal, T, pairs=False, mutation: int = 0):
     rc = _lib(mutation).oracle_tile_counts(S, cp, layout, int(causal), T, tiles, ptr)
     if rc != 0:
         raise ValueError("bad tile_counts arguments")
+    return tiles.reshape(cp, cp), (pr.reshape(cp, cp) if pairs else None)
+
+
+def _cu(cu_seqlens, S):
+    """Document offsets as int64; checks cu[0] = 0, cu[-1] = S, increasing."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64).reshape(-1))
+    if cu.size < 2 or cu[0] != 0 or cu[-1] != S or np.any(np.diff(cu) <= 0):
+        raise ValueError(f"cu_seqlens must rise strictly from 0 to S={S}: {cu.tolist()}")
+    return cu, cu.size - 1
+
+
+def attn_fwd_docs(q, k, v, cu_seqlens, causal=True, scale=None, mutation: int = 0):
+    """The definition under the document rule: documents [cu[d], cu[d+1])."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    _lib(mutation).oracle_attn_fwd_docs(q, k, v, B, H, Hkv, S, D, int(causal), scale, cu, nd,
+                                        out, lse)
+    return out, lse
+
+
+def ring_fwd_docs(q, k, v, cp, layout, cu_seqlens, causal=True, scale=None, merge_order=0,
+                  mutation: int = 0):
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    rc = _lib(mutation).oracle_ring_fwd_docs(q, k, v, B, H, Hkv, S, D, cp, layout, int(causal),
+                                             scale, cu, nd, merge_order, out, lse)
+    if rc != 0:
+        raise ValueError("bad ring_fwd_docs arguments")
+    return out, lse
+
+
+def attn_bwd_docs(q, k, v, dout, cu_seqlens, causal=True, scale=None, mutation: int = 0):
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    dq = np.empty((B, S, H, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    _lib(mutation).oracle_attn_bwd_docs(q, k, v, dout, B, H, Hkv, S, D, int(causal), scale, cu,
+                                        nd, dq, dk, dv)
+    return dq, dk, dv
+
+
+def tile_counts_docs(S, cp, layout, causal, cu_seqlens, T, pairs=False, mutation: int = 0):
+    """tile_counts under the document rule (every pair of a tile enumerated)."""
+    cu, nd = _cu(cu_seqlens, S)
+    tiles = np.zeros(cp * cp, np.uint64)
+    pr = np.zeros(cp * cp, np.uint64) if pairs else None
+    ptr = pr.ctypes.data_as(ctypes.c_void_p) if pairs else None
+    rc = _lib(mutation).oracle_tile_counts_docs(S, cp, layout, int(causal), cu, nd, T, tiles, ptr)
+    if rc != 0:
+        raise ValueError("bad tile_counts_docs arguments")
     return tiles.reshape(cp, cp), (pr.reshape(cp, cp) if pairs else None)

@@ -36,6 +36,13 @@
  *    dQ_i = scale sum_j dS_ij k_j, dK_j = scale sum_i dS_ij q_i,
  *    dV_j = sum_i P_ij dO_i (sums over i also run over the query heads that
  *    share kv head j).
+ *  - Document (packed-sequence) masks: "Context Parallelism for Long-Context
+ *    Training", sections "Prove attention equivalence" (causal and document
+ *    masks must agree with CP=1) and "Test sequence divisibility and padding".
+ *    Documents are the ranges [cu[d], cu[d+1]); the valid set V(i) above
+ *    keeps only keys of i's own document.  Padding is read as one more
+ *    document, so no real token sees a padded one.  The *_docs entry points
+ *    take cu; the others use one document (cu = NULL).
  *
  * Readings where the pages are silent: tensors are [B, S, H, D] row-major,
  * LSE is [B, H, S] in natural log; query head h uses kv head h / (H / Hkv);
@@ -50,7 +57,11 @@
  * result independent of cp / layout / merge order, constant V gives V, Q = 0
  * gives the closed-form uniform average, row 0 gives v_0, central finite
  * differences for every gradient, the sum rules sum_j dV_j = sum_i dO_i and
- * sum_j dK_j = 0, and closed-form tile / pair counts.
+ * sum_j dK_j = 0, closed-form tile / pair counts, and for documents: brute
+ * force and finite differences with documents, one token per document in
+ * closed form, packed documents equal to each document alone, one document
+ * equal to the plain mask, the ring under documents equal to the definition,
+ * and per-rank pair counts.
  */
 #include <math.h>
 #include <stdint.h>
@@ -159,11 +170,40 @@ static inline int is_valid(long i, long j, int causal) {
 #endif
 }
 
+/* Which keys a query sees.  The causal rule above, and -- when cu is not NULL
+ * -- the document rule of a packed sequence: documents are the position
+ * ranges [cu[d], cu[d+1]), d = 0..ndocs-1, with cu[0] = 0 and cu[ndocs] = S,
+ * and a token sees only tokens of its own document ("Context Parallelism for
+ * Long-Context Training", "Prove attention equivalence": test causal and
+ * document masks; "Test sequence divisibility and padding": padding is a
+ * document of its own, so real tokens never see it). */
+typedef struct {
+  int causal;
+  const long* cu;
+  long ndocs;
+} Mask;
+
+static long doc_of(const Mask* m, long p) {
+  for (long d = 0; d < m->ndocs; ++d)
+#if ORACLE_MUTATION == 7
+    if (p <= m->cu[d + 1]) return d;
+#else
+    if (p < m->cu[d + 1]) return d;
+#endif
+  return m->ndocs - 1;
+}
+
+static int visible(const Mask* m, long i, long j) {
+  if (!is_valid(i, j, m->causal)) return 0;
+  if (m->cu != NULL && doc_of(m, i) != doc_of(m, j)) return 0;
+  return 1;
+}
+
 /* Normalised partial of query row (b, h, natural i) against the keys at the
  * natural positions keys[0..nk): o[0..D) and *l (natural-log LSE).  A row
  * with no valid key gives o = 0, l = -inf.  s_buf holds nk doubles. */
 static void partial_row(const float* q, const float* k, const float* v, long B, int H,
-                        int Hkv, long S, int D, int causal, double scale, long b, int h,
+                        int Hkv, long S, int D, const Mask* msk, double scale, long b, int h,
                         long i, const long* keys, long nk, double* s_buf, double* o,
                         double* l) {
   (void)B;
@@ -172,7 +212,7 @@ static void partial_row(const float* q, const float* k, const float* v, long B, 
   double mx = -INFINITY;
   for (long a = 0; a < nk; ++a) {
     long j = keys[a];
-    if (!is_valid(i, j, causal)) {
+    if (!visible(msk, i, j)) {
       s_buf[a] = -INFINITY;
       continue;
     }
@@ -204,8 +244,8 @@ static void partial_row(const float* q, const float* k, const float* v, long B, 
 }
 
 /* Full attention (the definition), natural order.  out [B,S,H,D], lse [B,H,S]. */
-void oracle_attn_fwd(const float* q, const float* k, const float* v, long B, int H, int Hkv,
-                     long S, int D, int causal, double scale, double* out, double* lse) {
+static void attn_fwd_m(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                       long S, int D, const Mask* msk, double scale, double* out, double* lse) {
   long nrows = B * (long)H * S;
 #pragma omp parallel
   {
@@ -218,7 +258,7 @@ void oracle_attn_fwd(const float* q, const float* k, const float* v, long B, int
       int h = (int)((row / S) % H);
       long i = row % S;
       double l;
-      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, keys, S, sb,
+      partial_row(q, k, v, B, H, Hkv, S, D, msk, scale, b, h, i, keys, S, sb,
                   out + idx4(b, i, h, 0, S, H, D), &l);
       lse[(b * H + h) * S + i] = l;
     }
@@ -227,11 +267,26 @@ void oracle_attn_fwd(const float* q, const float* k, const float* v, long B, int
   }
 }
 
+void oracle_attn_fwd(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                     long S, int D, int causal, double scale, double* out, double* lse) {
+  const Mask msk = {causal, NULL, 0};
+  attn_fwd_m(q, k, v, B, H, Hkv, S, D, &msk, scale, out, lse);
+}
+
+/* The definition under the document rule (documents cu[0..ndocs]). */
+void oracle_attn_fwd_docs(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                          long S, int D, int causal, double scale, const long* cu, long ndocs,
+                          double* out, double* lse) {
+  const Mask msk = {causal, cu, ndocs};
+  attn_fwd_m(q, k, v, B, H, Hkv, S, D, &msk, scale, out, lse);
+}
+
 /* The definition evaluated on a list of rows: rows[3*n + {0,1,2}] = (b, h, i)
  * natural.  out [n, D], lse [n]. */
 void oracle_attn_fwd_rows(const float* q, const float* k, const float* v, long B, int H,
                           int Hkv, long S, int D, int causal, double scale, const long* rows,
                           long n, double* out, double* lse) {
+  const Mask msk = {causal, NULL, 0};
 #pragma omp parallel
   {
     long* keys = (long*)malloc(sizeof(long) * S);
@@ -239,7 +294,7 @@ void oracle_attn_fwd_rows(const float* q, const float* k, const float* v, long B
     for (long j = 0; j < S; ++j) keys[j] = j;
 #pragma omp for schedule(dynamic, 1)
     for (long a = 0; a < n; ++a) {
-      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, rows[3 * a], (int)rows[3 * a + 1],
+      partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, rows[3 * a], (int)rows[3 * a + 1],
                   rows[3 * a + 2], keys, S, sb, out + a * D, lse + a);
     }
     free(keys);
@@ -312,6 +367,7 @@ int oracle_ring_step(const float* q, const float* k, const float* v, long B, int
                      double* o_part, double* l_part) {
   int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
   if (cp < 1 || S % ((long)cp * per_rank) != 0 || t < 0 || t >= cp) return -1;
+  const Mask msk = {causal, NULL, 0};
   long L = S / cp;
   for (int r = 0; r < cp; ++r) {
     long* qpos = (long*)malloc(sizeof(long) * L);
@@ -328,7 +384,7 @@ int oracle_ring_step(const float* q, const float* k, const float* v, long B, int
         int h = (int)((a / L) % H);
         long i = qpos[a % L];
         double l;
-        partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, kpos, L, sb,
+        partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, b, h, i, kpos, L, sb,
                     o_part + idx4(b, i, h, 0, S, H, D), &l);
         l_part[(b * H + h) * S + i] = l;
       }
@@ -344,9 +400,9 @@ int oracle_ring_step(const float* q, const float* k, const float* v, long B, int
  * 0, 1, ..., cp-1 (left fold); 1: t = cp-1, ..., 0; 2: pairwise tree over t.
  * out [B,S,H,D], lse [B,H,S], natural order.  Returns 0 or -1 on bad
  * arguments. */
-int oracle_ring_fwd(const float* q, const float* k, const float* v, long B, int H, int Hkv,
-                    long S, int D, int cp, int layout, int causal, double scale,
-                    int merge_order, double* out, double* lse) {
+static int ring_fwd_m(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                      long S, int D, int cp, int layout, const Mask* msk, double scale,
+                      int merge_order, double* out, double* lse) {
   int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
   if (cp < 1 || S % ((long)cp * per_rank) != 0) return -1;
   long L = S / cp;
@@ -367,7 +423,7 @@ int oracle_ring_fwd(const float* q, const float* k, const float* v, long B, int 
         int h = (int)((a / L) % H);
         long i = qpos[a % L];
         for (int t = 0; t < cp; ++t)
-          partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, kpos + t * L, L, sb,
+          partial_row(q, k, v, B, H, Hkv, S, D, msk, scale, b, h, i, kpos + t * L, L, sb,
                       po + t * D, pl + t);
         if (merge_order == 2) {
           for (int w = 1; w < cp; w *= 2)
@@ -397,6 +453,22 @@ int oracle_ring_fwd(const float* q, const float* k, const float* v, long B, int 
   return 0;
 }
 
+int oracle_ring_fwd(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                    long S, int D, int cp, int layout, int causal, double scale,
+                    int merge_order, double* out, double* lse) {
+  const Mask msk = {causal, NULL, 0};
+  return ring_fwd_m(q, k, v, B, H, Hkv, S, D, cp, layout, &msk, scale, merge_order, out, lse);
+}
+
+/* The ring under the document rule: a step whose keys hold nothing of a
+ * query's document gives that query the neutral partial (0, -inf). */
+int oracle_ring_fwd_docs(const float* q, const float* k, const float* v, long B, int H, int Hkv,
+                         long S, int D, int cp, int layout, int causal, double scale,
+                         const long* cu, long ndocs, int merge_order, double* out, double* lse) {
+  const Mask msk = {causal, cu, ndocs};
+  return ring_fwd_m(q, k, v, B, H, Hkv, S, D, cp, layout, &msk, scale, merge_order, out, lse);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Gradients                                                                 */
 /* ------------------------------------------------------------------------ */
@@ -409,13 +481,13 @@ static double dot_f(const float* a, const float* b, int D) {
 
 /* dQ, dK, dV of the definition for the upstream gradient dout = dL/dO.
  * All natural order, dq [B,S,H,D], dk/dv [B,S,Hkv,D]. */
-void oracle_attn_bwd(const float* q, const float* k, const float* v, const float* dout,
-                     long B, int H, int Hkv, long S, int D, int causal, double scale,
-                     double* dq, double* dk, double* dv) {
+static void attn_bwd_m(const float* q, const float* k, const float* v, const float* dout,
+                       long B, int H, int Hkv, long S, int D, const Mask* msk, double scale,
+                       double* dq, double* dk, double* dv) {
   double* o = (double*)malloc(sizeof(double) * B * S * H * D);
   double* lse = (double*)malloc(sizeof(double) * B * H * S);
   double* delta = (double*)malloc(sizeof(double) * B * H * S);
-  oracle_attn_fwd(q, k, v, B, H, Hkv, S, D, causal, scale, o, lse);
+  attn_fwd_m(q, k, v, B, H, Hkv, S, D, msk, scale, o, lse);
 #pragma omp parallel for schedule(static)
   for (long row = 0; row < B * S * H; ++row) {
     long b = row / (S * H), i = (row / H) % S;
@@ -436,7 +508,7 @@ void oracle_attn_bwd(const float* q, const float* k, const float* v, const float
     double* dqi = dq + row * D;
     for (int d = 0; d < D; ++d) dqi[d] = 0.0;
     for (long j = 0; j < S; ++j) {
-      if (!is_valid(i, j, causal)) continue;
+      if (!visible(msk, i, j)) continue;
       const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
       const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
       double p = exp(scale * dot_f(qi, kj, D) - l);
@@ -458,7 +530,7 @@ void oracle_attn_bwd(const float* q, const float* k, const float* v, const float
     for (int h = 0; h < H; ++h) {
       if (kv_head_of(h, H, Hkv) != g) continue;
       for (long i = 0; i < S; ++i) {
-        if (!is_valid(i, j, causal)) continue;
+        if (!visible(msk, i, j)) continue;
         const float* qi = q + idx4(b, i, h, 0, S, H, D);
         const float* doi = dout + idx4(b, i, h, 0, S, H, D);
         double p = exp(scale * dot_f(qi, kj, D) - lse[(b * H + h) * S + i]);
@@ -476,12 +548,28 @@ void oracle_attn_bwd(const float* q, const float* k, const float* v, const float
   free(delta);
 }
 
+void oracle_attn_bwd(const float* q, const float* k, const float* v, const float* dout,
+                     long B, int H, int Hkv, long S, int D, int causal, double scale,
+                     double* dq, double* dk, double* dv) {
+  const Mask msk = {causal, NULL, 0};
+  attn_bwd_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, dq, dk, dv);
+}
+
+/* The gradients under the document rule (documents cu[0..ndocs]). */
+void oracle_attn_bwd_docs(const float* q, const float* k, const float* v, const float* dout,
+                          long B, int H, int Hkv, long S, int D, int causal, double scale,
+                          const long* cu, long ndocs, double* dq, double* dk, double* dv) {
+  const Mask msk = {causal, cu, ndocs};
+  attn_bwd_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, dq, dk, dv);
+}
+
 /* dQ of the definition on a list of query rows (b, h, i): each row needs only
  * its own softmax row, so this is exact for any dout.  dq [n, D]. */
 void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, const float* dout,
                              long B, int H, int Hkv, long S, int D, int causal, double scale,
                              const long* rows, long n, double* dq) {
   (void)B;
+  const Mask msk = {causal, NULL, 0};
 #pragma omp parallel
   {
     long* keys = (long*)malloc(sizeof(long) * S);
@@ -494,7 +582,7 @@ void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, con
       int h = (int)rows[3 * a + 1];
       int g = kv_head_of(h, H, Hkv);
       double l;
-      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, keys, S, sb, o, &l);
+      partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, b, h, i, keys, S, sb, o, &l);
       const float* qi = q + idx4(b, i, h, 0, S, H, D);
       const float* doi = dout + idx4(b, i, h, 0, S, H, D);
       double dl = 0.0;
@@ -502,7 +590,7 @@ void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, con
       double* dqi = dq + a * D;
       for (int d = 0; d < D; ++d) dqi[d] = 0.0;
       for (long j = 0; j < S; ++j) {
-        if (!is_valid(i, j, causal)) continue;
+        if (!visible(&msk, i, j)) continue;
         const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
         const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
         double p = exp(scale * dot_f(qi, kj, D) - l);
@@ -526,6 +614,7 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
                                       const float* dout, long B, int H, int Hkv, long S, int D,
                                       int causal, double scale, const long* qrows, long nq,
                                       const long* krows, long n, double* dk, double* dv) {
+  const Mask msk = {causal, NULL, 0};
   /* Softmax state of the needed query rows, every (b, h). */
   double* lse = (double*)malloc(sizeof(double) * B * H * nq);
   double* delta = (double*)malloc(sizeof(double) * B * H * nq);
@@ -540,7 +629,7 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
       long b = a / (H * nq);
       int h = (int)((a / nq) % H);
       long i = qrows[a % nq];
-      partial_row(q, k, v, B, H, Hkv, S, D, causal, scale, b, h, i, keys, S, sb, o, lse + a);
+      partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, b, h, i, keys, S, sb, o, lse + a);
       const float* doi = dout + idx4(b, i, h, 0, S, H, D);
       double dl = 0.0;
       for (int d = 0; d < D; ++d) dl += (double)doi[d] * o[d];
@@ -563,7 +652,7 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
       if (kv_head_of(h, H, Hkv) != g) continue;
       for (long x = 0; x < nq; ++x) {
         long i = qrows[x];
-        if (!is_valid(i, j, causal)) continue;
+        if (!visible(&msk, i, j)) continue;
         const float* qi = q + idx4(b, i, h, 0, S, H, D);
         const float* doi = dout + idx4(b, i, h, 0, S, H, D);
         long si = (b * H + h) * nq + x;
@@ -590,8 +679,8 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
  * rank's shard (query side) and of the source rank's shard (key side), each
  * inside one chunk; T must divide the chunk length.  Found by enumeration
  * over tiles (and, for pairs, over every pair of every live tile). */
-int oracle_tile_counts(long S, int cp, int layout, int causal, long T, uint64_t* tiles_rt,
-                       uint64_t* pairs_rt) {
+static int tile_counts_m(long S, int cp, int layout, const Mask* msk, long T, uint64_t* tiles_rt,
+                         uint64_t* pairs_rt) {
   int per_rank = (layout == LAYOUT_ZIGZAG) ? 2 : 1;
   if (cp < 1 || T < 1 || S % ((long)cp * per_rank) != 0) return -1;
   long L = S / cp, c = L / per_rank;
@@ -605,17 +694,23 @@ int oracle_tile_counts(long S, int cp, int layout, int causal, long T, uint64_t*
       uint64_t tiles = 0, pairs = 0;
       for (long qa = 0; qa < L; qa += T) {
         for (long kb = 0; kb < L; kb += T) {
-          /* j <= i is monotone, so some pair of the tile is valid exactly
-           * when the latest query and the earliest key form a valid pair. */
-          long qmax = qpos[qa], kmin = kpos[kb];
-          for (long x = 1; x < T; ++x) qmax = qpos[qa + x] > qmax ? qpos[qa + x] : qmax;
-          for (long y = 1; y < T; ++y) kmin = kpos[kb + y] < kmin ? kpos[kb + y] : kmin;
-          int any = is_valid(qmax, kmin, causal);
+          int any = 0;
+          if (msk->cu == NULL) {
+            /* j <= i is monotone, so some pair of the tile is valid exactly
+             * when the latest query and the earliest key form a valid pair. */
+            long qmax = qpos[qa], kmin = kpos[kb];
+            for (long x = 1; x < T; ++x) qmax = qpos[qa + x] > qmax ? qpos[qa + x] : qmax;
+            for (long y = 1; y < T; ++y) kmin = kpos[kb + y] < kmin ? kpos[kb + y] : kmin;
+            any = visible(msk, qmax, kmin);
+          } else {
+            for (long x = 0; x < T && !any; ++x)
+              for (long y = 0; y < T && !any; ++y) any = visible(msk, qpos[qa + x], kpos[kb + y]);
+          }
           tiles += (uint64_t)any;
           if (pairs_rt && any)
             for (long x = 0; x < T; ++x)
               for (long y = 0; y < T; ++y)
-                pairs += (uint64_t)is_valid(qpos[qa + x], kpos[kb + y], causal);
+                pairs += (uint64_t)visible(msk, qpos[qa + x], kpos[kb + y]);
         }
       }
       tiles_rt[r * cp + t] = tiles;
@@ -625,4 +720,17 @@ int oracle_tile_counts(long S, int cp, int layout, int causal, long T, uint64_t*
   free(qpos);
   free(kpos);
   return 0;
+}
+
+int oracle_tile_counts(long S, int cp, int layout, int causal, long T, uint64_t* tiles_rt,
+                       uint64_t* pairs_rt) {
+  const Mask msk = {causal, NULL, 0};
+  return tile_counts_m(S, cp, layout, &msk, T, tiles_rt, pairs_rt);
+}
+
+/* The census under the document rule (documents cu[0..ndocs]). */
+int oracle_tile_counts_docs(long S, int cp, int layout, int causal, const long* cu, long ndocs,
+                            long T, uint64_t* tiles_rt, uint64_t* pairs_rt) {
+  const Mask msk = {causal, cu, ndocs};
+  return tile_counts_m(S, cp, layout, &msk, T, tiles_rt, pairs_rt);
 }

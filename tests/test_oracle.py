@@ -14,7 +14,12 @@ mutated build of it) disagrees with an independent fact:
   from cp, layout and merge order ("Prove attention equivalence");
 * central finite differences of the brute-force forward for dQ, dK, dV,
   plus the sum rules sum_j dV_j = sum_i dO_i and sum_j dK_j = 0;
-* closed-form per-step tile and pair counts of the two layouts.
+* closed-form per-step tile and pair counts of the two layouts;
+* document (packed-sequence) masks: brute force and finite differences with
+  documents, one token per document (out = its own V, LSE = its own score),
+  packed documents equal to each document run alone (so padding as a
+  document of its own leaves real tokens untouched), one document equal to
+  the plain mask, and the ring under documents equal to the definition.
 
 ``test_mutations_are_caught`` compiles planted mistakes into the oracle and
 checks that some pin fails for each.
@@ -222,9 +227,143 @@ def pin_tile_counts(m=0):
             assert (tiles == mm * mm).all() and (pairs == Lc * Lc).all()
 
 
+# Document offsets used by the pins: a one-token document, documents that
+# straddle zigzag chunk borders, and one whose end is the sequence end.
+DOCS_S11 = [0, 3, 4, 9, 11]
+DOCS_S32 = [0, 5, 6, 13, 24, 32]
+
+
+def pin_docs_brute_force(m=0):
+    for causal in (True, False):
+        for (B, H, Hkv, S, D, seed, cu) in ((1, 2, 1, 11, 4, 61, DOCS_S11),
+                                            (2, 4, 2, 11, 5, 62, [0, 1, 2, 11]),
+                                            (1, 2, 2, 16, 3, 63, [0, 8, 16])):
+            q, k, v, _ = small(B, H, Hkv, S, D, seed)
+            out, lse = oracle.attn_fwd_docs(q, k, v, cu, causal=causal, mutation=m)
+            bo, bl = brute.attn_fwd(q.tolist(), k.tolist(), v.tolist(), causal=causal, docs=cu)
+            np.testing.assert_allclose(out, np.array(bo), rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse, np.array(bl), rtol=0, atol=1e-12)
+
+
+def pin_docs_finite_differences(m=0):
+    B, H, Hkv, S, D = 1, 2, 1, 6, 3
+    q, k, v, do = small(B, H, Hkv, S, D, 64, dout=True)
+    cu = [0, 2, 3, 6]
+    for causal in (True, False):
+        dq, dk, dv = oracle.attn_bwd_docs(q, k, v, do, cu, causal=causal, mutation=m)
+        ql, kl, vl, dol = (x.astype(np.float64).tolist() for x in (q, k, v, do))
+        for name, got in (("q", dq), ("k", dk), ("v", dv)):
+            fd = np.array(brute.finite_diff_grad(name, ql, kl, vl, dol, causal=causal, docs=cu))
+            np.testing.assert_allclose(got, fd, rtol=0, atol=2e-8)
+
+
+def pin_docs_one_token_each(m=0):
+    # Every token its own document: the softmax has one term, so O_i = V_i of
+    # the query head's group and LSE_i = scale * q_i . k_i; dQ = dK = 0, dV_i
+    # sums dO_i over the group's heads.
+    B, H, Hkv, S, D = 2, 4, 2, 12, 8
+    q, k, v, do = small(B, H, Hkv, S, D, 65, dout=True)
+    cu = list(range(S + 1))
+    scale = oracle.default_scale(D)
+    grp = [h * Hkv // H for h in range(H)]
+    for causal in (True, False):
+        out, lse = oracle.attn_fwd_docs(q, k, v, cu, causal=causal, mutation=m)
+        np.testing.assert_allclose(out, v[:, :, grp, :].astype(np.float64), rtol=0, atol=1e-12)
+        expect = scale * np.einsum("bshd,bshd->bhs", q.astype(np.float64),
+                                   k[:, :, grp, :].astype(np.float64))
+        np.testing.assert_allclose(lse, expect, rtol=0, atol=1e-12)
+        dq, dk, dv = oracle.attn_bwd_docs(q, k, v, do, cu, causal=causal, mutation=m)
+        np.testing.assert_allclose(dq, 0.0, atol=1e-12)
+        np.testing.assert_allclose(dk, 0.0, atol=1e-12)
+        d64 = do.astype(np.float64)
+        for g in range(Hkv):
+            heads = [h for h in range(H) if grp[h] == g]
+            np.testing.assert_allclose(dv[:, :, g], d64[:, :, heads].sum(axis=2), atol=1e-12)
+
+
+def pin_docs_packed_equals_separate(m=0):
+    # Packing documents into one sequence changes nothing for any of them;
+    # with the last document taken as padding (large values, dO = 0 there),
+    # the real tokens' results equal those of the unpadded sequence.
+    B, H, Hkv, S, D = 1, 4, 2, 32, 8
+    q, k, v, do = small(B, H, Hkv, S, D, 66, dout=True)
+    cu = DOCS_S32
+    pad = slice(cu[-2], cu[-1])
+    for x in (q, k, v):
+        x[:, pad] *= 40.0
+    do[:, pad] = 0.0
+    for causal in (True, False):
+        out, lse = oracle.attn_fwd_docs(q, k, v, cu, causal=causal, mutation=m)
+        dq, dk, dv = oracle.attn_bwd_docs(q, k, v, do, cu, causal=causal, mutation=m)
+        for a, b in zip(cu[:-1], cu[1:]):
+            sl = slice(a, b)
+            so, sl_ = oracle.attn_fwd(q[:, sl], k[:, sl], v[:, sl], causal=causal, mutation=m)
+            np.testing.assert_allclose(out[:, sl], so, rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[:, :, sl], sl_, rtol=0, atol=1e-12)
+            sq, sk, sv = oracle.attn_bwd(q[:, sl], k[:, sl], v[:, sl], do[:, sl],
+                                         causal=causal, mutation=m)
+            np.testing.assert_allclose(dq[:, sl], sq, rtol=0, atol=1e-11)
+            np.testing.assert_allclose(dk[:, sl], sk, rtol=0, atol=1e-11)
+            np.testing.assert_allclose(dv[:, sl], sv, rtol=0, atol=1e-11)
+        # The padding document receives no gradient when its dO is zero.
+        assert (dq[:, pad] == 0).all() and (dk[:, pad] == 0).all() and (dv[:, pad] == 0).all()
+
+
+def pin_docs_single_and_ring(m=0):
+    # One document is the plain mask; the ring under documents is independent
+    # of cp, layout and merge order and equals the definition.
+    B, H, Hkv, S, D = 1, 2, 1, 32, 8
+    q, k, v, _ = small(B, H, Hkv, S, D, 67)
+    for causal in (True, False):
+        po, pl = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+        do_, dl = oracle.attn_fwd_docs(q, k, v, [0, S], causal=causal, mutation=m)
+        np.testing.assert_array_equal(do_, po)
+        np.testing.assert_array_equal(dl, pl)
+        ref_o, ref_l = oracle.attn_fwd_docs(q, k, v, DOCS_S32, causal=causal, mutation=m)
+        for cp in (1, 2, 4):
+            for layout in (oracle.CONTIGUOUS, oracle.ZIGZAG):
+                for order in (0, 1, 2):
+                    ro, rl = oracle.ring_fwd_docs(q, k, v, cp, layout, DOCS_S32, causal=causal,
+                                                  merge_order=order, mutation=m)
+                    np.testing.assert_allclose(ro, ref_o, rtol=0, atol=1e-12)
+                    np.testing.assert_allclose(rl, ref_l, rtol=0, atol=1e-12)
+
+
+def pin_docs_tile_counts(m=0):
+    T = 4
+    for cp in (1, 2, 4):
+        for layout in (oracle.CONTIGUOUS, oracle.ZIGZAG):
+            S = 64
+            for causal in (True, False):
+                # One document is the plain census.
+                t1, p1 = oracle.tile_counts_docs(S, cp, layout, causal, [0, S], T, pairs=True,
+                                                 mutation=m)
+                t0, p0 = oracle.tile_counts(S, cp, layout, causal, T, pairs=True, mutation=m)
+                np.testing.assert_array_equal(t1, t0)
+                np.testing.assert_array_equal(p1, p0)
+                # Pairs per rank: each query sees its document's earlier tokens
+                # (causal) or the whole document.
+                cu = [0, 3, 11, 12, 20, 45, S]
+                tiles, pairs = oracle.tile_counts_docs(S, cp, layout, causal, cu, T, pairs=True,
+                                                       mutation=m)
+                nat = oracle.shard_order(S, cp, layout, mutation=m)
+                start = {p: a for a, b in zip(cu[:-1], cu[1:]) for p in range(a, b)}
+                end = {p: b for a, b in zip(cu[:-1], cu[1:]) for p in range(a, b)}
+                L = S // cp
+                for r in range(cp):
+                    mine = nat[r * L:(r + 1) * L]
+                    want = sum((i - start[i] + 1) if causal else (end[i] - start[i])
+                               for i in mine.tolist())
+                    assert int(pairs[r].sum()) == want, (cp, layout, causal, r)
+                assert (tiles <= t0).all()
+                assert ((pairs == 0) == (tiles == 0)).all()
+
+
 PINS = [pin_zigzag_golden, pin_contiguous_golden, pin_coverage, pin_brute_force,
         pin_constant_v, pin_q_zero, pin_row0, pin_ring_invariance, pin_step_partials_merge,
-        pin_finite_differences, pin_sum_rules, pin_tile_counts]
+        pin_finite_differences, pin_sum_rules, pin_tile_counts, pin_docs_brute_force,
+        pin_docs_finite_differences, pin_docs_one_token_each, pin_docs_packed_equals_separate,
+        pin_docs_single_and_ring, pin_docs_tile_counts]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -287,7 +426,8 @@ def test_bad_arguments_rejected():
 
 MUTATIONS = {1: "wrong zigzag pairing", 2: "interleaved GQA head map",
              3: "causal diagonal dropped", 4: "softmax scale dropped",
-             5: "merge term dropped", 6: "ring turned the other way"}
+             5: "merge term dropped", 6: "ring turned the other way",
+             7: "document border off by one"}
 
 
 @pytest.mark.parametrize("m", sorted(MUTATIONS), ids=[MUTATIONS[m] for m in sorted(MUTATIONS)])
