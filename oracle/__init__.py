@@ -70,6 +70,11 @@ def _lib(mutation: int = 0):
     lib.oracle_tile_counts_docs.argtypes = ([_L, _I, _I, _I] + docs
                                             + [_L, _u64p, ctypes.c_void_p])
     lib.oracle_tile_counts_docs.restype = _I
+    lib.oracle_attn_fwd_rows_docs.argtypes = ([_f32p, _f32p, _f32p] + shape + docs
+                                              + [_i64p, _L, _f64p, _f64p])
+    lib.oracle_attn_bwd_dq_rows_docs.argtypes = [_f32p] * 4 + shape + docs + [_i64p, _L, _f64p]
+    lib.oracle_attn_bwd_dkdv_rows_sparse_docs.argtypes = ([_f32p] * 4 + shape + docs
+                                                          + [_i64p, _L, _i64p, _L, _f64p, _f64p])
     _libs[mutation] = lib
     return lib
 
@@ -275,3 +280,48 @@ def tile_counts_docs(S, cp, layout, causal, cu_seqlens, T, pairs=False, mutation
     if rc != 0:
         raise ValueError("bad tile_counts_docs arguments")
     return tiles.reshape(cp, cp), (pr.reshape(cp, cp) if pairs else None)
+
+
+def attn_fwd_rows_docs(q, k, v, rows, cu_seqlens, causal=True, scale=None, mutation: int = 0):
+    """attn_fwd_rows under the document rule."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    n = rows.shape[0]
+    out = np.empty((n, D), np.float64)
+    lse = np.empty((n,), np.float64)
+    _lib(mutation).oracle_attn_fwd_rows_docs(q, k, v, B, H, Hkv, S, D, int(causal), scale, cu, nd,
+                                             rows, n, out, lse)
+    return out, lse
+
+
+def attn_bwd_dq_rows_docs(q, k, v, dout, rows, cu_seqlens, causal=True, scale=None,
+                          mutation: int = 0):
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    dq = np.empty((rows.shape[0], D), np.float64)
+    _lib(mutation).oracle_attn_bwd_dq_rows_docs(q, k, v, dout, B, H, Hkv, S, D, int(causal),
+                                                scale, cu, nd, rows, rows.shape[0], dq)
+    return dq
+
+
+def attn_bwd_dkdv_rows_sparse_docs(q, k, v, dout, qrows, krows, cu_seqlens, causal=True,
+                                   scale=None, mutation: int = 0):
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    qrows = np.ascontiguousarray(np.asarray(qrows, dtype=np.int64).reshape(-1))
+    krows = np.ascontiguousarray(np.asarray(krows, dtype=np.int64).reshape(-1, 3))
+    n = krows.shape[0]
+    dk = np.empty((n, D), np.float64)
+    dv = np.empty((n, D), np.float64)
+    _lib(mutation).oracle_attn_bwd_dkdv_rows_sparse_docs(q, k, v, dout, B, H, Hkv, S, D,
+                                                         int(causal), scale, cu, nd, qrows,
+                                                         qrows.shape[0], krows, n, dk, dv)
+    return dk, dv

@@ -283,10 +283,9 @@ void oracle_attn_fwd_docs(const float* q, const float* k, const float* v, long B
 
 /* The definition evaluated on a list of rows: rows[3*n + {0,1,2}] = (b, h, i)
  * natural.  out [n, D], lse [n]. */
-void oracle_attn_fwd_rows(const float* q, const float* k, const float* v, long B, int H,
-                          int Hkv, long S, int D, int causal, double scale, const long* rows,
-                          long n, double* out, double* lse) {
-  const Mask msk = {causal, NULL, 0};
+static void attn_fwd_rows_m(const float* q, const float* k, const float* v, long B, int H,
+                            int Hkv, long S, int D, const Mask* msk, double scale,
+                            const long* rows, long n, double* out, double* lse) {
 #pragma omp parallel
   {
     long* keys = (long*)malloc(sizeof(long) * S);
@@ -294,12 +293,26 @@ void oracle_attn_fwd_rows(const float* q, const float* k, const float* v, long B
     for (long j = 0; j < S; ++j) keys[j] = j;
 #pragma omp for schedule(dynamic, 1)
     for (long a = 0; a < n; ++a) {
-      partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, rows[3 * a], (int)rows[3 * a + 1],
+      partial_row(q, k, v, B, H, Hkv, S, D, msk, scale, rows[3 * a], (int)rows[3 * a + 1],
                   rows[3 * a + 2], keys, S, sb, out + a * D, lse + a);
     }
     free(keys);
     free(sb);
   }
+}
+
+void oracle_attn_fwd_rows(const float* q, const float* k, const float* v, long B, int H,
+                          int Hkv, long S, int D, int causal, double scale, const long* rows,
+                          long n, double* out, double* lse) {
+  const Mask msk = {causal, NULL, 0};
+  attn_fwd_rows_m(q, k, v, B, H, Hkv, S, D, &msk, scale, rows, n, out, lse);
+}
+
+void oracle_attn_fwd_rows_docs(const float* q, const float* k, const float* v, long B, int H,
+                               int Hkv, long S, int D, int causal, double scale, const long* cu,
+                               long ndocs, const long* rows, long n, double* out, double* lse) {
+  const Mask msk = {causal, cu, ndocs};
+  attn_fwd_rows_m(q, k, v, B, H, Hkv, S, D, &msk, scale, rows, n, out, lse);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -565,11 +578,11 @@ void oracle_attn_bwd_docs(const float* q, const float* k, const float* v, const 
 
 /* dQ of the definition on a list of query rows (b, h, i): each row needs only
  * its own softmax row, so this is exact for any dout.  dq [n, D]. */
-void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, const float* dout,
-                             long B, int H, int Hkv, long S, int D, int causal, double scale,
-                             const long* rows, long n, double* dq) {
+static void attn_bwd_dq_rows_m(const float* q, const float* k, const float* v,
+                               const float* dout, long B, int H, int Hkv, long S, int D,
+                               const Mask* msk, double scale, const long* rows, long n,
+                               double* dq) {
   (void)B;
-  const Mask msk = {causal, NULL, 0};
 #pragma omp parallel
   {
     long* keys = (long*)malloc(sizeof(long) * S);
@@ -582,7 +595,7 @@ void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, con
       int h = (int)rows[3 * a + 1];
       int g = kv_head_of(h, H, Hkv);
       double l;
-      partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, b, h, i, keys, S, sb, o, &l);
+      partial_row(q, k, v, B, H, Hkv, S, D, msk, scale, b, h, i, keys, S, sb, o, &l);
       const float* qi = q + idx4(b, i, h, 0, S, H, D);
       const float* doi = dout + idx4(b, i, h, 0, S, H, D);
       double dl = 0.0;
@@ -590,7 +603,7 @@ void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, con
       double* dqi = dq + a * D;
       for (int d = 0; d < D; ++d) dqi[d] = 0.0;
       for (long j = 0; j < S; ++j) {
-        if (!visible(&msk, i, j)) continue;
+        if (!visible(msk, i, j)) continue;
         const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
         const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
         double p = exp(scale * dot_f(qi, kj, D) - l);
@@ -604,17 +617,32 @@ void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, con
   }
 }
 
+void oracle_attn_bwd_dq_rows(const float* q, const float* k, const float* v, const float* dout,
+                             long B, int H, int Hkv, long S, int D, int causal, double scale,
+                             const long* rows, long n, double* dq) {
+  const Mask msk = {causal, NULL, 0};
+  attn_bwd_dq_rows_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, rows, n, dq);
+}
+
+void oracle_attn_bwd_dq_rows_docs(const float* q, const float* k, const float* v,
+                                  const float* dout, long B, int H, int Hkv, long S, int D,
+                                  int causal, double scale, const long* cu, long ndocs,
+                                  const long* rows, long n, double* dq) {
+  const Mask msk = {causal, cu, ndocs};
+  attn_bwd_dq_rows_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, rows, n, dq);
+}
+
 /* dK, dV of the definition on a list of key rows (b, g, j), for an upstream
  * gradient that is zero on every query row except the natural positions
  * qrows[0..nq) (all batches, all heads).  Rows with dO_i = 0 have
  * Delta_i = 0 and hence dS_ij = 0 and P_ij dO_i = 0, so the sums over i may
  * be restricted to qrows: the result is the exact definition for such a
  * dout.  dk, dv [n, D]. */
-void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const float* v,
-                                      const float* dout, long B, int H, int Hkv, long S, int D,
-                                      int causal, double scale, const long* qrows, long nq,
-                                      const long* krows, long n, double* dk, double* dv) {
-  const Mask msk = {causal, NULL, 0};
+static void attn_bwd_dkdv_rows_sparse_m(const float* q, const float* k, const float* v,
+                                        const float* dout, long B, int H, int Hkv, long S, int D,
+                                        const Mask* msk, double scale, const long* qrows,
+                                        long nq, const long* krows, long n, double* dk,
+                                        double* dv) {
   /* Softmax state of the needed query rows, every (b, h). */
   double* lse = (double*)malloc(sizeof(double) * B * H * nq);
   double* delta = (double*)malloc(sizeof(double) * B * H * nq);
@@ -629,7 +657,7 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
       long b = a / (H * nq);
       int h = (int)((a / nq) % H);
       long i = qrows[a % nq];
-      partial_row(q, k, v, B, H, Hkv, S, D, &msk, scale, b, h, i, keys, S, sb, o, lse + a);
+      partial_row(q, k, v, B, H, Hkv, S, D, msk, scale, b, h, i, keys, S, sb, o, lse + a);
       const float* doi = dout + idx4(b, i, h, 0, S, H, D);
       double dl = 0.0;
       for (int d = 0; d < D; ++d) dl += (double)doi[d] * o[d];
@@ -652,7 +680,7 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
       if (kv_head_of(h, H, Hkv) != g) continue;
       for (long x = 0; x < nq; ++x) {
         long i = qrows[x];
-        if (!visible(&msk, i, j)) continue;
+        if (!visible(msk, i, j)) continue;
         const float* qi = q + idx4(b, i, h, 0, S, H, D);
         const float* doi = dout + idx4(b, i, h, 0, S, H, D);
         long si = (b * H + h) * nq + x;
@@ -667,6 +695,25 @@ void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const floa
   }
   free(lse);
   free(delta);
+}
+
+void oracle_attn_bwd_dkdv_rows_sparse(const float* q, const float* k, const float* v,
+                                      const float* dout, long B, int H, int Hkv, long S, int D,
+                                      int causal, double scale, const long* qrows, long nq,
+                                      const long* krows, long n, double* dk, double* dv) {
+  const Mask msk = {causal, NULL, 0};
+  attn_bwd_dkdv_rows_sparse_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, qrows, nq, krows, n,
+                              dk, dv);
+}
+
+void oracle_attn_bwd_dkdv_rows_sparse_docs(const float* q, const float* k, const float* v,
+                                           const float* dout, long B, int H, int Hkv, long S,
+                                           int D, int causal, double scale, const long* cu,
+                                           long ndocs, const long* qrows, long nq,
+                                           const long* krows, long n, double* dk, double* dv) {
+  const Mask msk = {causal, cu, ndocs};
+  attn_bwd_dkdv_rows_sparse_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, qrows, nq, krows, n,
+                              dk, dv);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -395,6 +395,19 @@ def test_rows_match_full():
     sdk, sdv = oracle.attn_bwd_dkdv_rows_sparse(q, k, v, sparse, qrows, krows)
     np.testing.assert_allclose(sdk, dk2[krows[:, 0], krows[:, 2], krows[:, 1]], atol=1e-12)
     np.testing.assert_allclose(sdv, dv2[krows[:, 0], krows[:, 2], krows[:, 1]], atol=1e-12)
+    # The same under documents.
+    cu = [0, 5, 6, 22, 40]
+    out, lse = oracle.attn_fwd_docs(q, k, v, cu)
+    ro, rl = oracle.attn_fwd_rows_docs(q, k, v, rows, cu)
+    np.testing.assert_array_equal(ro, out[rows[:, 0], rows[:, 2], rows[:, 1]])
+    np.testing.assert_array_equal(rl, lse[rows[:, 0], rows[:, 1], rows[:, 2]])
+    dq, dk, dv = oracle.attn_bwd_docs(q, k, v, do, cu)
+    rdq = oracle.attn_bwd_dq_rows_docs(q, k, v, do, rows, cu)
+    np.testing.assert_allclose(rdq, dq[rows[:, 0], rows[:, 2], rows[:, 1]], atol=1e-12)
+    dq2, dk2, dv2 = oracle.attn_bwd_docs(q, k, v, sparse, cu)
+    sdk, sdv = oracle.attn_bwd_dkdv_rows_sparse_docs(q, k, v, sparse, qrows, krows, cu)
+    np.testing.assert_allclose(sdk, dk2[krows[:, 0], krows[:, 2], krows[:, 1]], atol=1e-12)
+    np.testing.assert_allclose(sdv, dv2[krows[:, 0], krows[:, 2], krows[:, 1]], atol=1e-12)
 
 
 def test_empty_partial_is_neutral():
