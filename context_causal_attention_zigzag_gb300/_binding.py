@@ -34,6 +34,12 @@ _ip = ctypes.POINTER(ctypes.c_int)
 SIGNATURES = {
     "cpattn_zigzag_permute": (_i, [_vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
     "cpattn_zigzag_unpermute": (_i, [_vp, _vp, _i64, _i64, _i64, _i, _i, _vp]),
+    "cpattn_zigzag_permute_pad": (_i, [_vp, _vp, _i64, _i64, _i64, _i64, _i, _i, _vp]),
+    "cpattn_zigzag_unpermute_pad": (_i, [_vp, _vp, _i64, _i64, _i64, _i64, _i, _i, _vp]),
+    "cpattn_doc_bounds": (_i, [_vp, _i, _i, _vp, _vp]),
+    "cpattn_ring_fwd_docs": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _vp]),
+    "cpattn_ring_bwd_docs": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
+    "cpattn_padded_length": (_i64, [_i64, _i, _i]),
     "cpattn_ring_fwd": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp]),
     "cpattn_ring_fwd_census": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp, _vp]),
     "cpattn_ring_fwd_plan": (_i, [_i] * 9 + [_ip, _ip]),
@@ -147,6 +153,59 @@ def zigzag_permute(x, cp, layout=ZIGZAG, seq_dim=1, out=None):
 def zigzag_unpermute(x, cp, layout=ZIGZAG, seq_dim=1, out=None):
     """Sharded -> natural order along ``seq_dim``."""
     return _perm("cpattn_zigzag_unpermute", x, cp, layout, seq_dim, out)
+
+
+def _split(x, seq_dim):
+    if seq_dim < 0:
+        seq_dim += x.dim()
+    outer = 1
+    for s in x.shape[:seq_dim]:
+        outer *= s
+    inner = x.element_size()
+    for s in x.shape[seq_dim + 1:]:
+        inner *= s
+    return seq_dim, outer, inner
+
+
+def zigzag_permute_pad(x, cp, S, layout=ZIGZAG, seq_dim=1, out=None):
+    """Natural [.., S_real, ..] -> sharded [.., S, ..], padding positions
+    S_real..S-1 with zeros (cpattn_zigzag_permute_pad)."""
+    _need_cuda(x)
+    seq_dim, outer, inner = _split(x, seq_dim)
+    S_real = x.shape[seq_dim]
+    if out is None:
+        shape = list(x.shape)
+        shape[seq_dim] = S
+        out = torch.empty(shape, device=x.device, dtype=x.dtype)
+    _need_cuda(out)
+    rc = lib().cpattn_zigzag_permute_pad(_ptr(x), _ptr(out), outer, S_real, int(S), inner,
+                                         int(cp), int(layout), _stream(x))
+    _check("cpattn_zigzag_permute_pad", rc)
+    return out
+
+
+def zigzag_unpermute_pad(x, cp, S_real, layout=ZIGZAG, seq_dim=1, out=None):
+    """Sharded [.., S, ..] -> natural [.., S_real, ..], dropping the padding."""
+    _need_cuda(x)
+    seq_dim, outer, inner = _split(x, seq_dim)
+    S = x.shape[seq_dim]
+    if out is None:
+        shape = list(x.shape)
+        shape[seq_dim] = S_real
+        out = torch.empty(shape, device=x.device, dtype=x.dtype)
+    _need_cuda(out)
+    rc = lib().cpattn_zigzag_unpermute_pad(_ptr(x), _ptr(out), outer, int(S_real), S, inner,
+                                           int(cp), int(layout), _stream(x))
+    _check("cpattn_zigzag_unpermute_pad", rc)
+    return out
+
+
+def padded_length(S, cp, layout=ZIGZAG) -> int:
+    """Length the tensor-core kernels take for S tokens (cpattn_padded_length)."""
+    n = int(lib().cpattn_padded_length(int(S), int(cp), int(layout)))
+    if n < 0:
+        raise ValueError(f"bad arguments to padded_length: S={S} cp={cp} layout={layout}")
+    return n
 
 
 # ---------------------------------------------------------------------------
@@ -297,6 +356,83 @@ def ring_bwd_noalloc(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, sc
 
 
 # ---------------------------------------------------------------------------
+# packed documents
+# ---------------------------------------------------------------------------
+
+def doc_bounds(cu_seqlens, S, device=None):
+    """Per-position document bounds int32 [S, 2] from offsets cu_seqlens
+    (0, strictly increasing, ..., S; a CUDA int32 tensor or anything
+    torch.as_tensor takes)."""
+    dev = device if device is not None else (
+        cu_seqlens.device if torch.is_tensor(cu_seqlens) and cu_seqlens.is_cuda
+        else torch.device("cuda", torch.cuda.current_device()))
+    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev).contiguous()
+    ndocs = cu.numel() - 1
+    bounds = torch.empty((S, 2), device=dev, dtype=torch.int32)
+    rc = lib().cpattn_doc_bounds(_ptr(cu), ndocs, int(S), _ptr(bounds), _stream(cu))
+    _check("cpattn_doc_bounds", rc)
+    return bounds
+
+
+def ring_fwd_docs(q, k, v, cp, bounds, layout=ZIGZAG, causal=True, scale=None, out=None,
+                  lse=None, tiles_rt=None):
+    """Ring forward under the document rule (bounds from doc_bounds)."""
+    _need_cuda(q, k, v, bounds)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    if bounds.dtype != torch.int32 or tuple(bounds.shape) != (S, 2):
+        raise ValueError("bounds must be int32 [S, 2] from doc_bounds")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    _need_cuda(out, lse, tiles_rt)
+    rc = lib().cpattn_ring_fwd_docs(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv,
+                                    S, D, int(cp), int(layout), int(bool(causal)),
+                                    _dtype_code(q), _scale(scale), _ptr(bounds), _ptr(tiles_rt),
+                                    _stream(q))
+    _check("cpattn_ring_fwd_docs", rc)
+    return out, lse
+
+
+def ring_fwd_docs_census(q, k, v, cp, bounds, layout=ZIGZAG, causal=True, scale=None):
+    counts = torch.zeros((cp, cp), device=q.device, dtype=torch.int64)
+    out, lse = ring_fwd_docs(q, k, v, cp, bounds, layout, causal, scale, tiles_rt=counts)
+    return out, lse, counts
+
+
+def ring_bwd_docs(q, k, v, out, dout, lse, cp, bounds, layout=ZIGZAG, causal=True, scale=None,
+                  dq=None, dk=None, dv=None, workspace=None, grad_dtype=None):
+    """Ring backward under the document rule; returns (dq, dk, dv)."""
+    _need_cuda(q, k, v, out, dout, lse, bounds)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    if bounds.dtype != torch.int32 or tuple(bounds.shape) != (S, 2):
+        raise ValueError("bounds must be int32 [S, 2] from doc_bounds")
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
+    need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(dq, dk, dv, workspace)
+    rc = lib().cpattn_ring_bwd_docs(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                    _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
+                                    int(layout), int(bool(causal)), code, _scale(scale),
+                                    _ptr(bounds), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("cpattn_ring_bwd_docs", rc)
+    return dq, dk, dv
+
+
+def _padded_docs(cu_seqlens, S_real, S, device):
+    """Offsets of the real documents plus, when S > S_real, one padding
+    document [S_real, S)."""
+    cu = [int(x) for x in (cu_seqlens.tolist() if torch.is_tensor(cu_seqlens)
+                           else list(cu_seqlens))] if cu_seqlens is not None else [0, S_real]
+    if cu[0] != 0 or cu[-1] != S_real:
+        raise ValueError(f"cu_seqlens must run from 0 to S={S_real}")
+    if S > S_real:
+        cu.append(S)
+    return doc_bounds(cu, S, device)
+
+
+# ---------------------------------------------------------------------------
 # census and status
 # ---------------------------------------------------------------------------
 
@@ -341,3 +477,35 @@ def attention_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None,
                           grad_dtype=grad_dtype)
     un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
     return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dk), un(dv)
+
+
+def attention_docs(q, k, v, cp, cu_seqlens=None, layout=ZIGZAG, causal=True, scale=None):
+    """Natural order, any sequence length, packed documents: pads the sequence
+    to padded_length (the padding is a document of its own), permutes with
+    padding, runs the ring forward under the document rule and drops the
+    padding again.  cu_seqlens: document offsets over the real tokens (None:
+    one document).  Returns (out, lse) for the real tokens."""
+    S_real = q.shape[1]
+    S = padded_length(S_real, cp, layout)
+    bounds = _padded_docs(cu_seqlens, S_real, S, q.device)
+    qs, ks, vs = (zigzag_permute_pad(x, cp, S, layout) for x in (q, k, v))
+    o, lse = ring_fwd_docs(qs, ks, vs, cp, bounds, layout, causal, scale)
+    return (zigzag_unpermute_pad(o, cp, S_real, layout),
+            zigzag_unpermute_pad(lse, cp, S_real, layout, seq_dim=2))
+
+
+def attention_docs_fwd_bwd(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causal=True,
+                           scale=None, grad_dtype=None):
+    """attention_docs with the backward: dout over the real tokens (the
+    padding gets a zero upstream gradient).  Returns (out, lse, dq, dk, dv)
+    for the real tokens, natural order."""
+    S_real = q.shape[1]
+    S = padded_length(S_real, cp, layout)
+    bounds = _padded_docs(cu_seqlens, S_real, S, q.device)
+    qs, ks, vs, dos = (zigzag_permute_pad(x, cp, S, layout) for x in (q, k, v, dout))
+    o, lse = ring_fwd_docs(qs, ks, vs, cp, bounds, layout, causal, scale)
+    dq, dk, dv = ring_bwd_docs(qs, ks, vs, o, dos, lse, cp, bounds, layout, causal, scale,
+                               grad_dtype=grad_dtype)
+    un = lambda x: zigzag_unpermute_pad(x, cp, S_real, layout)  # noqa: E731
+    return (un(o), zigzag_unpermute_pad(lse, cp, S_real, layout, seq_dim=2), un(dq), un(dk),
+            un(dv))

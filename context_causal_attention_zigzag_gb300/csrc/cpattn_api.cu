@@ -59,7 +59,16 @@ int make_shape(int B, int H, int Hkv, int S, int D, int cp, int layout, int caus
   sh->c = sh->L / per;
   sh->scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
   sh->scale_log2 = sh->scale * 1.4426950408889634f;
+  sh->docs = nullptr;
   return CPATTN_OK;
+}
+
+// Document bounds as the kernels read them; NULL passes through, a pointer
+// must be 8-byte aligned.
+bool doc_ptr(const int32_t* bounds, const int2** out) {
+  if (bounds != nullptr && (reinterpret_cast<uintptr_t>(bounds) & 7) != 0) return false;
+  *out = reinterpret_cast<const int2*>(bounds);
+  return true;
 }
 
 bool device_is_sm103() {
@@ -84,10 +93,11 @@ bool tc_bwd_eligible(const RingShape& sh, int dtype) {
 int fwd_common(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
                int Hkv, int S, int D, int cp, int layout, int causal, int dtype,
                float softmax_scale, int t_begin, int t_end, int step_mode,
-               unsigned long long* tiles_rt, cudaStream_t stream) {
+               unsigned long long* tiles_rt, const int2* docs, cudaStream_t stream) {
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp, layout, causal, softmax_scale, &sh);
   if (rc != CPATTN_OK) return rc;
+  sh.docs = docs;
   if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   if ((long long)B * S == 0) return CPATTN_OK;
   if (!q || !k || !v || !out || !lse) return CPATTN_ERR_INVALID_ARG;
@@ -131,63 +141,100 @@ int plan_common(int B, int H, int Hkv, int S, int D, int cp, int layout, int cau
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Sharded tensor [outer, S, inner]; natural tensor [outer, S_nat, inner].
+int permute_common(const void* in, void* out, int64_t outer, int64_t S, int64_t S_nat,
+                   int64_t inner_bytes, int cp_size, int layout, bool inverse,
+                   cudaStream_t stream) {
+  if (outer < 0 || S < 0 || S_nat < 0 || S_nat > S || inner_bytes < 1 || cp_size < 1)
+    return CPATTN_ERR_INVALID_ARG;
+  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
+    return CPATTN_ERR_INVALID_ARG;
+  const int per = chunks_per_rank(layout);
+  if (S % ((int64_t)cp_size * per) != 0 || S > INT32_MAX) return CPATTN_ERR_INVALID_ARG;
+  if (outer * S == 0) return CPATTN_OK;
+  if (!in || !out) return CPATTN_ERR_INVALID_ARG;
+  const char* a = static_cast<const char*>(in);
+  const char* b = static_cast<const char*>(out);
+  const int64_t in_bytes = outer * (inverse ? S : S_nat) * inner_bytes;
+  const int64_t out_bytes = outer * (inverse ? S_nat : S) * inner_bytes;
+  if (a < b + out_bytes && b < a + in_bytes) return CPATTN_ERR_INVALID_ARG;
+  RingShape sh;
+  memset(&sh, 0, sizeof(sh));
+  sh.cp = cp_size;
+  sh.per_rank = per;
+  sh.S = (int)S;
+  sh.L = (int)(S / cp_size);
+  sh.c = sh.L / per;
+  cudaError_t e = launch_permute(in, out, outer, S, S_nat, inner_bytes, sh, inverse, stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
 
 int cpattn_zigzag_permute(const void* in, void* out, int64_t outer, int64_t S,
                           int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream) {
-  if (outer < 0 || S < 0 || inner_bytes < 1 || cp_size < 1) return CPATTN_ERR_INVALID_ARG;
-  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
-    return CPATTN_ERR_INVALID_ARG;
-  const int per = chunks_per_rank(layout);
-  if (S % ((int64_t)cp_size * per) != 0 || S > INT32_MAX) return CPATTN_ERR_INVALID_ARG;
-  if (outer * S == 0) return CPATTN_OK;
-  if (!in || !out) return CPATTN_ERR_INVALID_ARG;
-  const char* a = static_cast<const char*>(in);
-  const char* b = static_cast<const char*>(out);
-  const int64_t bytes = outer * S * inner_bytes;
-  if (a < b + bytes && b < a + bytes) return CPATTN_ERR_INVALID_ARG;
-  RingShape sh;
-  memset(&sh, 0, sizeof(sh));
-  sh.cp = cp_size;
-  sh.per_rank = per;
-  sh.S = (int)S;
-  sh.L = (int)(S / cp_size);
-  sh.c = sh.L / per;
-  cudaError_t e = launch_permute(in, out, outer, S, inner_bytes, sh, false, (cudaStream_t)stream);
-  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return permute_common(in, out, outer, S, S, inner_bytes, cp_size, layout, false,
+                        (cudaStream_t)stream);
 }
 
 int cpattn_zigzag_unpermute(const void* in, void* out, int64_t outer, int64_t S,
                             int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream) {
-  if (outer < 0 || S < 0 || inner_bytes < 1 || cp_size < 1) return CPATTN_ERR_INVALID_ARG;
-  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG)
-    return CPATTN_ERR_INVALID_ARG;
-  const int per = chunks_per_rank(layout);
-  if (S % ((int64_t)cp_size * per) != 0 || S > INT32_MAX) return CPATTN_ERR_INVALID_ARG;
-  if (outer * S == 0) return CPATTN_OK;
-  if (!in || !out) return CPATTN_ERR_INVALID_ARG;
-  const char* a = static_cast<const char*>(in);
-  const char* b = static_cast<const char*>(out);
-  const int64_t bytes = outer * S * inner_bytes;
-  if (a < b + bytes && b < a + bytes) return CPATTN_ERR_INVALID_ARG;
-  RingShape sh;
-  memset(&sh, 0, sizeof(sh));
-  sh.cp = cp_size;
-  sh.per_rank = per;
-  sh.S = (int)S;
-  sh.L = (int)(S / cp_size);
-  sh.c = sh.L / per;
-  cudaError_t e = launch_permute(in, out, outer, S, inner_bytes, sh, true, (cudaStream_t)stream);
-  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  return permute_common(in, out, outer, S, S, inner_bytes, cp_size, layout, true,
+                        (cudaStream_t)stream);
+}
+
+int cpattn_zigzag_permute_pad(const void* in, void* out, int64_t outer, int64_t S_real,
+                              int64_t S, int64_t inner_bytes, int cp_size, int layout,
+                              cpattn_stream_t stream) {
+  return permute_common(in, out, outer, S, S_real, inner_bytes, cp_size, layout, false,
+                        (cudaStream_t)stream);
+}
+
+int cpattn_zigzag_unpermute_pad(const void* in, void* out, int64_t outer, int64_t S_real,
+                                int64_t S, int64_t inner_bytes, int cp_size, int layout,
+                                cpattn_stream_t stream) {
+  return permute_common(in, out, outer, S, S_real, inner_bytes, cp_size, layout, true,
+                        (cudaStream_t)stream);
 }
 
 int cpattn_ring_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
                     float softmax_scale, cpattn_stream_t stream) {
   return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, 0, cp_size, 0, nullptr, (cudaStream_t)stream);
+                    softmax_scale, 0, cp_size, 0, nullptr, nullptr, (cudaStream_t)stream);
+}
+
+int cpattn_doc_bounds(const int32_t* cu_seqlens, int ndocs, int S, int32_t* bounds,
+                      cpattn_stream_t stream) {
+  if (S < 0 || ndocs < 1 || ndocs > (S > 0 ? S : 1)) return CPATTN_ERR_INVALID_ARG;
+  if (S == 0) return CPATTN_OK;
+  if (!cu_seqlens || !bounds || (reinterpret_cast<uintptr_t>(bounds) & 7) != 0 ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens) & 3) != 0)
+    return CPATTN_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return CPATTN_ERR_CUDA;
+  cudaError_t e = launch_doc_bounds(cu_seqlens, ndocs, S, reinterpret_cast<int2*>(bounds), err,
+                                    (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int cpattn_ring_fwd_docs(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
+                         int dtype, float softmax_scale, const int32_t* doc_bounds,
+                         unsigned long long* tiles_rt, cpattn_stream_t stream) {
+  const int2* docs = nullptr;
+  if (doc_bounds == nullptr || !doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
+                    softmax_scale, 0, cp_size, 0, tiles_rt, docs, (cudaStream_t)stream);
+}
+
+int64_t cpattn_padded_length(int64_t S, int cp_size, int layout) {
+  if (S < 0 || cp_size < 1) return -1;
+  if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG) return -1;
+  const int64_t unit = (int64_t)cp_size * chunks_per_rank(layout) * 2 * kTcTile;
+  return (S + unit - 1) / unit * unit;
 }
 
 int cpattn_ring_fwd_census(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -196,7 +243,7 @@ int cpattn_ring_fwd_census(const void* q, const void* k, const void* v, void* ou
                            unsigned long long* tiles_rt, cpattn_stream_t stream) {
   if (tiles_rt == nullptr) return CPATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, 0, cp_size, 0, tiles_rt, (cudaStream_t)stream);
+                    softmax_scale, 0, cp_size, 0, tiles_rt, nullptr, (cudaStream_t)stream);
 }
 
 int cpattn_ring_fwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
@@ -215,7 +262,7 @@ int cpattn_ring_fwd_step(const void* q, const void* k, const void* v, int B, int
                          cpattn_stream_t stream) {
   if (step < 0 || step >= cp_size) return CPATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, o_part, lse_part, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, step, step + 1, 1, nullptr, (cudaStream_t)stream);
+                    softmax_scale, step, step + 1, 1, nullptr, nullptr, (cudaStream_t)stream);
 }
 
 int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
@@ -239,14 +286,18 @@ size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, int D, int 
   return 2 * align256(q) + 2 * align256(kv) + align256(delta);
 }
 
-int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
-                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                    int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
-                    float softmax_scale, void* workspace, size_t workspace_bytes,
-                    cpattn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int bwd_common(const void* q, const void* k, const void* v, const void* out, const void* dout,
+               const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int S,
+               int D, int cp_size, int layout, int causal, int dtype, float softmax_scale,
+               const int2* docs, void* workspace, size_t workspace_bytes, cudaStream_t st) {
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp_size, layout, causal, softmax_scale, &sh);
   if (rc != CPATTN_OK) return rc;
+  sh.docs = docs;
   const int in_dtype = dtype & ~CPATTN_GRAD_F32;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   const int out_dtype = (dtype & CPATTN_GRAD_F32) ? CPATTN_F32 : in_dtype;
@@ -261,7 +312,6 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
     return CPATTN_ERR_WORKSPACE;
   int* err = device_error_word();
   if (err == nullptr) return CPATTN_ERR_CUDA;
-  cudaStream_t st = (cudaStream_t)stream;
   const int64_t n_q = (int64_t)B * S * H * D, n_kv = (int64_t)B * S * Hkv * D;
   // Workspace: [n_q][n_q][n_kv][n_kv] float32, then Delta [B,H,S].
   char* ws = static_cast<char*>(workspace);
@@ -310,6 +360,31 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   e = launch_grad_convert(reg_a, reg_c, reg_d, dq, dk, dv, n_q, n_kv, out_dtype, st);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
+                    float softmax_scale, void* workspace, size_t workspace_bytes,
+                    cpattn_stream_t stream) {
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout, causal,
+                    dtype, softmax_scale, nullptr, workspace, workspace_bytes,
+                    (cudaStream_t)stream);
+}
+
+int cpattn_ring_bwd_docs(const void* q, const void* k, const void* v, const void* out,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                         int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
+                         int dtype, float softmax_scale, const int32_t* doc_bounds,
+                         void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
+  const int2* docs = nullptr;
+  if (doc_bounds == nullptr || !doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout, causal,
+                    dtype, softmax_scale, docs, workspace, workspace_bytes, (cudaStream_t)stream);
 }
 
 int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal, int64_t tile,
@@ -362,7 +437,7 @@ int cpattn_device_status(cpattn_stream_t stream) {
     int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return CPATTN_ERR_CUDA;
-    return CPATTN_ERR_DEVICE_TIMEOUT;
+    return host == kErrBadDocs ? CPATTN_ERR_INVALID_ARG : CPATTN_ERR_DEVICE_TIMEOUT;
   }
   return CPATTN_OK;
 }

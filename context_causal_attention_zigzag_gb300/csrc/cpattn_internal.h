@@ -18,7 +18,53 @@ struct RingShape {
   int c;         // chunk length, L / per_rank
   float scale;       // softmax scale
   float scale_log2;  // softmax scale * log2(e): scores are kept in base 2
+  // Packed documents ("Context Parallelism for Long-Context Training",
+  // "Prove attention equivalence" and "Test sequence divisibility and
+  // padding"): docs[p] = (first position, one past the last position) of the
+  // document holding natural position p; a token sees only its own document.
+  // nullptr: the whole sequence is one document.
+  const int2* docs;
 };
+
+// Keys visible to the query at natural position i: the natural range [lo, hi].
+// Both ends are non-decreasing in i, so the keys that some query of a run of
+// consecutive positions i0..i1 sees form the single range [lo(i0), hi(i1)].
+__host__ __device__ inline void query_window(const RingShape& s, int i, int& lo, int& hi) {
+  if (s.docs != nullptr) {
+    const int2 d = s.docs[i];
+    lo = d.x;
+    hi = s.causal ? i : d.y - 1;
+  } else {
+    lo = 0;
+    hi = s.causal ? i : s.S - 1;
+  }
+}
+
+// Queries that see the key at natural position j: the natural range [lo, hi]
+// (non-decreasing in j, like query_window).
+__host__ __device__ inline void key_window(const RingShape& s, int j, int& lo, int& hi) {
+  if (s.docs != nullptr) {
+    const int2 d = s.docs[j];
+    lo = s.causal ? j : d.x;
+    hi = d.y - 1;
+  } else {
+    lo = s.causal ? j : 0;
+    hi = s.S - 1;
+  }
+}
+
+// Tiles of edge T, counted from the chunk start x0 (chunk length c), that
+// overlap the natural range [lo, hi]: [t_lo, t_hi), empty when t_lo >= t_hi.
+__host__ __device__ inline void tiles_overlapping(int x0, int c, int T, int lo, int hi,
+                                                  int& t_lo, int& t_hi) {
+  if (hi < x0 || lo > x0 + c - 1 || lo > hi) {
+    t_lo = 0;
+    t_hi = 0;
+    return;
+  }
+  t_lo = ((lo > x0 ? lo : x0) - x0) / T;
+  t_hi = ((hi < x0 + c - 1 ? hi : x0 + c - 1) - x0) / T + 1;
+}
 
 // Natural position of sharded position p.  Rank r = p / L owns, in order,
 // chunk r and (zigzag only) chunk 2*cp-1-r ("Sequence Parallelism IV",
@@ -78,7 +124,18 @@ struct BwdArgs {
 };
 
 // Kernel launchers; each returns the launch error (cudaSuccess if queued).
-cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t S,
+// docs[p] for every natural position p from document offsets cu[0..ndocs]
+// (cu[0] = 0, strictly increasing, cu[ndocs] = S).  Offsets that break those
+// rules set the device error word to kErrBadDocs; every entry is still
+// clamped to first <= p < one-past-last, so the kernels stay in bounds.
+cudaError_t launch_doc_bounds(const int* cu, int ndocs, int S, int2* docs, int* err,
+                              cudaStream_t stream);
+constexpr int kErrTimeout = 1;
+constexpr int kErrBadDocs = 2;
+
+// Natural <-> sharded along S; the natural tensor holds S_nat <= S tokens
+// (the rest is padding: zeros when sharding, dropped when unsharding).
+cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t S, int64_t S_nat,
                            int64_t inner_bytes, const RingShape& sh, bool inverse,
                            cudaStream_t stream);
 cudaError_t launch_simt_fwd(const FwdArgs& a, int dtype, cudaStream_t stream);

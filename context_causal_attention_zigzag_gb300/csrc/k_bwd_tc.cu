@@ -7,8 +7,10 @@
 // Delta = rowsum(dO o O):  P = exp(s - LSE),  dS = P (dP - Delta),
 // dP = dO V^T.  The tiles a query tile and a K/V tile share are those of the
 // ring ("Sequence Parallelism IV", section 4): the K/V of source rank s
-// reaches rank (s + t) mod cp at step t; tiles wholly in the causal future
-// are skipped and the diagonal tile is masked.
+// reaches rank (s + t) mod cp at step t; tiles that no pair of the two sees
+// (wholly in the causal future, or in another packed document) are skipped,
+// and a tile that a row's window cuts (the diagonal, a document border) is
+// masked element-wise for that row.
 //
 // dkdv kernel (K/V-major).  Work item: one 128-row K/V tile and one query
 // head.  The K/V tile stays in shared memory; the query tiles that see it
@@ -18,6 +20,7 @@
 //   S^T  = K Q^T   -> TMEM [0,128)       dP^T = V dO^T -> TMEM [128,256)
 //   P^T  = exp2(S^T*scale*log2e - LSE*log2e)  -> bf16 over S^T
 //   dS^T = scale * P^T (dP^T - Delta)         -> bf16 over dP^T
+//   (dS from the float32 P, so that only dS itself is rounded to bf16)
 //   dV  += P^T dO  (TS)  -> TMEM [256,384)    dK += dS^T Q (TS) -> TMEM [384,512)
 // MMA order per tile i: dV(i), S(i+1), dK(i), dP(i+1): the elementwise warps
 // of tile i+1 overlap the tensor core's work on tile i.  At the end of the
@@ -118,45 +121,44 @@ __device__ __forceinline__ TilePos tile_pos(const RingShape& sh, int knat) {
 }
 
 // Query tiles (of one head) that see a K/V tile, in ring order: step t,
-// receiving rank (s + t) mod cp, that rank's chunks.
+// receiving rank (s + t) mod cp, that rank's chunks.  The tile's keys are
+// seen by the queries [lo, hi] (natural positions): under the causal rule
+// from the tile's first key on, within the documents of its keys.
 struct QSeq {
-  int cp, per, L, c, ctiles, causal, s, kc, kt;
-  int t, jq, qt;
+  int cp, per, L, c, s, lo, hi;
+  int t, jq, qt, qt_end;
 
-  __device__ __forceinline__ void init(const RingShape& sh, const TilePos& kv) {
+  __device__ __forceinline__ void init(const RingShape& sh, const TilePos& kv, int knat) {
     cp = sh.cp;
     per = sh.per_rank;
     L = sh.L;
     c = sh.c;
-    ctiles = sh.c / kT;
-    causal = sh.causal;
     s = kv.rank;
-    kc = kv.chunk;
-    kt = kv.tile;
+    int x;
+    key_window(sh, knat * kT, lo, x);
+    key_window(sh, knat * kT + kT - 1, x, hi);
     t = 0;
     jq = 0;
     qt = 0;
+    qt_end = -1;
   }
 
-  __device__ __forceinline__ bool next(int& qrow, bool& diag) {
+  // qrow: sharded row of the query tile; qnat: natural position of its first row.
+  __device__ __forceinline__ bool next(int& qrow, int& qnat) {
     while (t < cp) {
       const int r = (s + t) % cp;
       while (jq < per) {
         const int qc = (per == 1 || jq == 0) ? r : 2 * cp - 1 - r;
-        int lo = 0, hi = ctiles;
-        if (causal && qc == kc)
-          lo = kt;  // from the diagonal tile on
-        else if (causal && qc < kc)
-          hi = 0;   // the whole chunk precedes this K/V: nothing to see
-        if (qt < lo) qt = lo;
-        if (qt < hi) {
+        if (qt_end < 0) tiles_overlapping(qc * c, c, kT, lo, hi, qt, qt_end);
+        if (qt < qt_end) {
           qrow = r * L + jq * c + qt * kT;
-          diag = causal && qc == kc && qt == kt;
+          qnat = qc * c + qt * kT;
           ++qt;
           return true;
         }
         ++jq;
         qt = 0;
+        qt_end = -1;
       }
       ++t;
       jq = 0;
@@ -166,10 +168,12 @@ struct QSeq {
 };
 
 // K/V tiles that a query tile sees, in ring order (step t brings the shard of
-// rank (r - t) mod cp), the diagonal tile last.
+// rank (r - t) mod cp), the diagonal tile last.  The query tile sees the keys
+// [lo(first row), hi(last row)]; under the causal rule the ring walk stops
+// before the tile's own first key and the diagonal tile comes at the end.
 struct KSeq {
-  int cp, per, L, c, ctiles, causal, r, qc, a, qrow;
-  int t, jj, kt;
+  int cp, per, L, c, r, qrow, q0, wlo, whi;
+  int t, jj, kt, kt_end;
   bool tail;
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& q, int knat) {
@@ -177,45 +181,43 @@ struct KSeq {
     per = sh.per_rank;
     L = sh.L;
     c = sh.c;
-    ctiles = sh.c / kT;
-    causal = sh.causal;
     r = q.rank;
-    qc = q.chunk;
-    a = knat;
     qrow = q.row;
+    q0 = knat * kT;
+    int x, hi;
+    query_window(sh, q0, wlo, x);
+    query_window(sh, q0 + kT - 1, x, hi);
+    whi = sh.causal ? q0 - 1 : hi;
     t = 0;
     jj = 0;
     kt = 0;
-    tail = causal;
+    kt_end = -1;
+    tail = sh.causal;
   }
 
-  __device__ __forceinline__ bool next(int& kvrow, bool& diag) {
+  // kvrow: sharded row of the K/V tile; knat: natural position of its first key.
+  __device__ __forceinline__ bool next(int& kvrow, int& knat) {
     while (t < cp) {
       const int s = ring_source(r, t, cp);
       while (jj < per) {
         const int kc = (per == 1 || jj == 0) ? s : 2 * cp - 1 - s;
-        int lim;
-        if (!causal || kc < qc)
-          lim = ctiles;
-        else if (kc == qc)
-          lim = a - kc * ctiles;  // tiles strictly before the diagonal
-        else
-          lim = 0;                // wholly in the causal future: skipped
-        if (kt < lim) {
+        if (kt_end < 0) tiles_overlapping(kc * c, c, kT, wlo, whi, kt, kt_end);
+        if (kt < kt_end) {
           kvrow = s * L + jj * c + kt * kT;
-          diag = false;
+          knat = kc * c + kt * kT;
           ++kt;
           return true;
         }
         ++jj;
         kt = 0;
+        kt_end = -1;
       }
       ++t;
       jj = 0;
     }
     if (tail) {
       kvrow = qrow;  // the diagonal tile holds the query tile's own tokens
-      diag = true;
+      knat = q0;
       tail = false;
       return true;
     }
@@ -255,7 +257,7 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
 constexpr uint32_t kQTx = 2 * kTileBytes + 2 * kT * 4;  // Q, dO, LSE, Delta
 
 struct Item {
-  int b, h, g;
+  int b, h, g, knat;
   TilePos kv;
 };
 
@@ -271,6 +273,7 @@ __device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
   it.b = bh / sh.H;
   it.h = bh - it.b * sh.H;
   it.g = it.h / (sh.H / sh.Hkv);
+  it.knat = knat;
   it.kv = tile_pos(sh, knat);
   return it;
 }
@@ -349,10 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sV + half * kBoxBytes, &tm_v, bar(kBarKVFull), half * 64, it.g, krow);
         }
         QSeq seq;
-        seq.init(sh, it.kv);
-        int qrow;
-        bool diag;
-        while (seq.next(qrow, diag)) {
+        seq.init(sh, it.kv, it.knat);
+        int qrow, qnat;
+        while (seq.next(qrow, qnat)) {
           const int st = qi & 1;
           const uint32_t ph = (qi >> 1) & 1;
           if (!mbar_wait(bar(kBarQEmpty + st), ph ^ 1, wc)) {
@@ -411,10 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         QSeq seq;
-        seq.init(sh, it.kv);
-        int qrow;
-        bool diag;
-        bool have = seq.next(qrow, diag);
+        seq.init(sh, it.kv, it.knat);
+        int qrow, qnat;
+        bool have = seq.next(qrow, qnat);
         if (have) {
           const int st = qi & 1;
           if (!mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc)) {
@@ -428,9 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first = true;
         while (have) {
           const int st = qi & 1;
-          int nqrow;
-          bool ndiag;
-          const bool nhave = seq.next(nqrow, ndiag);
+          int nqrow, nqnat;
+          const bool nhave = seq.next(nqrow, nqnat);
           const int nst = (qi + 1) & 1;
           // dV += P^T dO
           if (!mbar_wait(bar(kBarP), p_ph, wc)) {
@@ -476,6 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           have = nhave;
         }
         if (!ok) break;
+        if (first) {
+          // No query tile at all (cannot happen for well-formed windows: every
+          // key sees its own query): the epilogue writes zeros once the
+          // previous one has been read out.
+          if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+        }
         mma_commit(bar(kBarAcc));
         mma_commit(bar(kBarKVEmpty));
       }
@@ -498,11 +507,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx >= n_items) break;
       const Item it = decode(sh, idx);
       QSeq seq;
-      seq.init(sh, it.kv);
-      int qrow;
-      bool diag;
-      while (seq.next(qrow, diag)) {
+      seq.init(sh, it.kv, it.knat);
+      // Queries that see this thread's key (natural positions).
+      int w_lo, w_hi;
+      key_window(sh, it.knat * kT + row, w_lo, w_hi);
+      int qrow, qnat, nq = 0;
+      while (seq.next(qrow, qnat)) {
         const int st = qi & 1;
+        const int c_lo = w_lo - qnat, c_hi = w_hi - qnat;  // visible query columns
+        const bool cut = c_lo > 0 || c_hi < kT - 1;
         // LSE / Delta of this tile arrived with its Q / dO.
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc))) {
           ok = false;
@@ -510,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float* lse = lse_s + st * kT + 64 * half;
         const float* dlt = dlt_s + st * kT + 64 * half;
-        // P^T = exp2(S^T * scale*log2e - LSE*log2e), masked on the diagonal
+        // P^T = exp2(S^T * scale*log2e - LSE*log2e), masked outside the window
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS), s_ph, wc))) {
           ok = false;
           break;
@@ -522,16 +535,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tl + kColS + 64 * half + 32, r + 32);
         tmem_wait_ld_regs(r);
         reg_fence32(r + 32);
+        // P^T stays in float32 in r for dS below (the bf16 copy feeds dV only).
         uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float2 l2 = *reinterpret_cast<const float2*>(lse + 2 * j);
           float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -l2.x * kLog2e));
           float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -l2.y * kLog2e));
-          if (diag) {  // query column 64*half + c is visible iff c >= row
-            if (64 * half + 2 * j < row) p0 = 0.f;
-            if (64 * half + 2 * j + 1 < row) p1 = 0.f;
+          if (cut) {
+            const int c0 = 64 * half + 2 * j;
+            if (c0 < c_lo || c0 > c_hi) p0 = 0.f;
+            if (c0 + 1 < c_lo || c0 + 1 > c_hi) p1 = 0.f;
           }
+          r[2 * j] = __float_as_uint(p0);
+          r[2 * j + 1] = __float_as_uint(p1);
           pk[j] = pack_bf16(p0, p1);
         }
         if (!halves_meet(bar(kBarRdS), rs_ph, wc)) {
@@ -542,24 +559,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarP));
-        // dS^T = scale * P^T (dP^T - Delta)
+        // dS^T = scale * P^T (dP^T - Delta), dP^T read 32 columns at a time
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP), dp_ph, wc))) {
           ok = false;
           break;
         }
         dp_ph ^= 1;
         tc_fence_after();
-        tmem_ld32(tl + kColDP + 64 * half, r);
-        tmem_ld32(tl + kColDP + 64 * half + 32, r + 32);
-        tmem_wait_ld_regs(r);
-        reg_fence32(r + 32);
         uint32_t ds[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 p = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[j]));
-          const float2 dl = *reinterpret_cast<const float2*>(dlt + 2 * j);
-          ds[j] = pack_bf16(scale * p.x * (__uint_as_float(r[2 * j]) - dl.x),
-                            scale * p.y * (__uint_as_float(r[2 * j + 1]) - dl.y));
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t d[32];
+          tmem_ld32(tl + kColDP + 64 * half + 32 * cc, d);
+          tmem_wait_ld_regs(d);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = 32 * cc + 2 * j;
+            const float2 dl = *reinterpret_cast<const float2*>(dlt + c);
+            ds[16 * cc + j] = pack_bf16(scale * __uint_as_float(r[c]) * (__uint_as_float(d[2 * j]) - dl.x),
+                                        scale * __uint_as_float(r[c + 1]) *
+                                            (__uint_as_float(d[2 * j + 1]) - dl.y));
+          }
         }
         if (!halves_meet(bar(kBarRdDP), rdp_ph, wc)) {
           ok = false;
@@ -570,6 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(kBarDS));
         ++qi;
+        ++nq;
       }
       if (!ok) break;
       // Epilogue: this head's dK / dV partial, columns [64*half, +64).
@@ -589,6 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t d[32];
           tmem_ld32(tl + col + 32 * cc, d);
           tmem_wait_ld_regs(d);
+          if (nq == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d[j] = 0u;
+          }
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<float4*>(dst + 32 * cc + 4 * u) =
@@ -734,9 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         KSeq seq;
         seq.init(sh, it.q, it.knat);
-        int kvrow;
-        bool diag;
-        while (seq.next(kvrow, diag)) {
+        int kvrow, knat;
+        while (seq.next(kvrow, knat)) {
           const int st = kj & 1;
           const uint32_t ph = (kj >> 1) & 1;
           if (!mbar_wait(bar(kBarKVEmpty + st), ph ^ 1, wc)) {
@@ -793,9 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         KSeq seq;
         seq.init(sh, it.q, it.knat);
-        int kvrow;
-        bool diag;
-        bool have = seq.next(kvrow, diag);
+        int kvrow, knat;
+        bool have = seq.next(kvrow, knat);
         if (have) {
           const int st = kj & 1;
           if (!mbar_wait(bar(kBarKVFull + st), (kj >> 1) & 1, wc)) {
@@ -809,9 +832,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool first = true;
         while (have) {
           const int st = kj & 1;
-          int nkvrow;
-          bool ndiag;
-          const bool nhave = seq.next(nkvrow, ndiag);
+          int nkvrow, nknat;
+          const bool nhave = seq.next(nkvrow, nknat);
           const int nst = (kj + 1) & 1;
           if (nhave) {
             if (!mbar_wait(bar(kBarKVFull + nst), ((kj + 1) >> 1) & 1, wc)) {
@@ -852,8 +874,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         if (first) {
-          // No K/V tile at all (only possible without a causal diagonal): the
-          // epilogue writes zeros; it still waits for the previous epilogue.
+          // No K/V tile at all (cannot happen for well-formed windows: every
+          // query sees its own key): the epilogue writes zeros; it still
+          // waits for the previous epilogue.
           if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
             ok = false;
             break;
@@ -893,11 +916,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float dlt = args.delta[li];
       KSeq seq;
       seq.init(sh, it.q, it.knat);
-      int kvrow;
-      bool diag;
+      // Keys that this thread's query sees (natural positions).
+      int w_lo, w_hi;
+      query_window(sh, it.knat * kT + row, w_lo, w_hi);
+      int kvrow, knat;
       int ntiles = 0;
-      while (seq.next(kvrow, diag)) {
+      while (seq.next(kvrow, knat)) {
         const int buf = kj & 1;
+        const int j_lo = w_lo - knat, j_hi = w_hi - knat;  // visible key columns
+        const bool cut = j_lo > 0 || j_hi < kT - 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS), s_ph, wc))) {
           ok = false;
           break;
@@ -915,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           p[j] = ex2(fmaf(__uint_as_float(r[j]), sl2, nlse2));
-          if (diag && 64 * half + j > row) p[j] = 0.f;  // key after the query
+          if (cut && (64 * half + j < j_lo || 64 * half + j > j_hi)) p[j] = 0.f;
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP + buf), dp_ph[buf], wc))) {
           ok = false;

@@ -6,9 +6,12 @@
 // (r - t) mod cp at ring step t is a change of the base row the TMA reads.
 // A work item is 256 query rows of one (batch, head) -- two 128-row tiles of
 // one chunk.  Its CTA streams the K/V tiles of ring steps t = 0..cp-1, skips
-// the tiles wholly in the causal future (never loaded), and keeps the online
-// softmax state; the two tiles on the causal diagonal (the item's own rows)
-// are taken last, masked element-wise.  The rescale of O when the running
+// the tiles that no query of the item sees (wholly in the causal future, or,
+// for packed documents, outside the documents of the item's rows: never
+// loaded), and keeps the online softmax state; the two tiles on the causal
+// diagonal (the item's own rows) are taken last.  Each softmax thread masks
+// its row element-wise against the row's key window only on tiles that
+// window cuts (the diagonal, document borders).  The rescale of O when the running
 // maximum moves is the softmax-state correction; it is skipped while the
 // maximum grows by less than 2^8, which leaves the result exact because the
 // final normalisation uses the same stale maximum.
@@ -75,7 +78,12 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // Flags of one K/V tile for the item's two query tiles.
-constexpr int kUse0 = 1, kUse1 = 2, kDiag0 = 4, kDiag1 = 8;
+constexpr int kUse0 = 1, kUse1 = 2;
+
+// Whether the 128 keys from natural position k0 meet the range [lo, hi].
+__device__ __forceinline__ bool tile_meets(int k0, int lo, int hi) {
+  return k0 <= hi && k0 + kT - 1 >= lo;
+}
 
 struct Item {
   int b, h, g, r, qc, a, qrow;  // qc: natural chunk, a: natural tile of query tile 0
@@ -115,9 +123,14 @@ __device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
 
 // The K/V tiles an item visits, in ring order (step t brings the shard of
 // rank (r - t) mod cp), with the two diagonal tiles deferred to the end.
+// Query tile i sees the keys [lo[i], hi[i]] (natural positions); a tile is
+// visited when either window meets it.  Under the causal rule the ring walk
+// stops before the item's first row: keys from there on are the diagonal
+// tiles (step 0 only) or the causal future.
 struct KvSeq {
-  int cp, per, L, c, ctiles, causal, t_end, r, qc, a, qrow;
-  int t, jj, kt, tail;
+  int cp, per, L, c, t_end, r, a, qrow;
+  int lo[2], hi[2], wlo, whi;
+  int t, jj, kt, kt_end, tail;
   bool tail_on;
 
   __device__ __forceinline__ void init(const RingShape& sh, int t_begin, int t_end_,
@@ -126,50 +139,64 @@ struct KvSeq {
     per = sh.per_rank;
     L = sh.L;
     c = sh.c;
-    ctiles = sh.c / kT;
-    causal = sh.causal;
     t_end = t_end_;
     r = it.r;
-    qc = it.qc;
     a = it.a;
     qrow = it.qrow;
+    int x;
+    for (int i = 0; i < 2; ++i) {
+      query_window(sh, (a + i) * kT, lo[i], x);
+      query_window(sh, (a + i) * kT + kT - 1, x, hi[i]);
+    }
+    wlo = lo[0];
+    whi = sh.causal ? a * kT - 1 : hi[1];
     t = t_begin;
     jj = 0;
     kt = 0;
+    kt_end = -1;
     tail = 0;
-    tail_on = causal && t_begin == 0;
+    tail_on = sh.causal && t_begin == 0;
   }
 
-  __device__ __forceinline__ bool next(int& kvrow, int& fl, int& step) {
+  __device__ __forceinline__ int flags(int k0) const {
+    return (tile_meets(k0, lo[0], hi[0]) ? kUse0 : 0) | (tile_meets(k0, lo[1], hi[1]) ? kUse1 : 0);
+  }
+
+  // kvrow: sharded row of the tile; fl: kUse* flags; step: ring step;
+  // knat: natural position of the tile's first key.
+  __device__ __forceinline__ bool next(int& kvrow, int& fl, int& step, int& knat) {
     while (t < t_end) {
       const int s = ring_source(r, t, cp);
       while (jj < per) {
         const int kc = (per == 1 || jj == 0) ? s : 2 * cp - 1 - s;
-        int lim;
-        if (!causal || kc < qc)
-          lim = ctiles;
-        else if (kc == qc)
-          lim = a - kc * ctiles;  // the tiles before the diagonal
-        else
-          lim = 0;                // wholly in the causal future: skipped
-        if (kt < lim) {
+        if (kt_end < 0) tiles_overlapping(kc * c, c, kT, wlo, whi, kt, kt_end);
+        while (kt < kt_end) {
+          const int k0 = kc * c + kt * kT;
           kvrow = s * L + jj * c + kt * kT;
-          fl = kUse0 | kUse1;
-          step = t;
           ++kt;
+          fl = flags(k0);
+          if (fl == 0) continue;
+          step = t;
+          knat = k0;
           return true;
         }
         ++jj;
         kt = 0;
+        kt_end = -1;
       }
       ++t;
       jj = 0;
     }
-    if (tail_on && tail < 2) {
-      kvrow = qrow + tail * kT;  // the diagonal tiles are the item's own rows
-      fl = tail == 0 ? (kUse0 | kUse1 | kDiag0) : (kUse1 | kDiag1);
-      step = 0;
+    while (tail_on && tail < 2) {
+      // The diagonal tiles are the item's own rows; tile a + 1 is in the
+      // future of query tile 0.
+      const int k0 = (a + tail) * kT;
+      kvrow = qrow + tail * kT;
+      fl = flags(k0) & (tail == 0 ? (kUse0 | kUse1) : kUse1);
       ++tail;
+      if (fl == 0) continue;
+      step = 0;
+      knat = k0;
       return true;
     }
     return false;
@@ -249,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         it.h, row0 + tq * kT);
         KvSeq kseq;
         kseq.init(sh, args.t_begin, args.t_end, it);
-        int kvrow, fl, step;
-        while (ok && kseq.next(kvrow, fl, step)) {
+        int kvrow, fl, step, knat;
+        while (ok && kseq.next(kvrow, fl, step, knat)) {
           const int krow = it.b * sh.S + kvrow;
           for (int which = 0; which < 2; ++which) {  // K(j), then V(j)
             const uint32_t n = seq++;
@@ -290,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         KvSeq seq;
         seq.init(sh, args.t_begin, args.t_end, it);
-        int kvrow, fl, step;
-        bool have = seq.next(kvrow, fl, step);
+        int kvrow, fl, step, knat;
+        bool have = seq.next(kvrow, fl, step, knat);
         if (!have) {
           mma_commit(bar(kBarQEmpty));
           continue;
@@ -317,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarEmpty + kn % kSlots));
         uint32_t acc[2] = {0, 0};
         while (true) {
-          int nkvrow, nfl = 0, nstep = 0;
-          const bool have_next = seq.next(nkvrow, nfl, nstep);
+          int nkvrow, nfl = 0, nstep = 0, nknat;
+          const bool have_next = seq.next(nkvrow, nfl, nstep, nknat);
           const uint32_t vn = 2 * kv_it + 1, nkn = 2 * kv_it + 2;
           if (!mbar_wait(bar(kBarFull + vn % kSlots), (vn / kSlots) & 1, wc)) {
             ok = false;
@@ -403,12 +430,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = decode_item(sh, idx);
       KvSeq seq;
       seq.init(sh, args.t_begin, args.t_end, it);
+      // This row's key window (natural positions).
+      int w_lo, w_hi;
+      query_window(sh, (it.a + ti) * kT + row, w_lo, w_hi);
       float m = -INFINITY, l = 0.f;
       int nt = 0;
-      int kvrow, fl, step;
-      while (seq.next(kvrow, fl, step)) {
+      int kvrow, fl, step, knat;
+      while (seq.next(kvrow, fl, step, knat)) {
         if (!(fl & (kUse0 << ti))) continue;
-        const bool diag = (fl & (kDiag0 << ti)) != 0;
+        const int j_lo = w_lo - knat, j_hi = w_hi - knat;  // visible columns
+        const bool cut = j_lo > 0 || j_hi < kT - 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS + ti), s_ph, wc))) {
           ok = false;
           break;
@@ -424,10 +455,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence32(r + 32);
         reg_fence32(r + 64);
         reg_fence32(r + 96);
-        if (diag) {
+        if (cut) {
 #pragma unroll
           for (int j = 0; j < 128; ++j)
-            if (j > row) r[j] = __float_as_uint(-INFINITY);
+            if (j < j_lo || j > j_hi) r[j] = __float_as_uint(-INFINITY);
         }
         float mx0 = __uint_as_float(r[0]), mx1 = __uint_as_float(r[1]);
         float mx2 = __uint_as_float(r[2]), mx3 = __uint_as_float(r[3]);
@@ -444,11 +475,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool rescale = __any_sync(0xffffffffu, need);
         float alpha = 1.f;
         if (rescale) {
-          alpha = ex2(m - m_new);
+          // A row that has seen no key yet keeps m = -inf and alpha = 1.
+          alpha = m_new == -INFINITY ? 1.f : ex2(m - m_new);
           l *= alpha;
           m = m_new;
         }
-        const float nm = -m;
+        const float nm = m == -INFINITY ? 0.f : -m;
         float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -501,7 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       o_ph ^= 1;
       tc_fence_after();
-      const float inv = 1.f / l;
+      // A row with no visible key (possible only in a step partial) gets
+      // (0, -inf).
+      const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t o[32];
@@ -528,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      args.lse[lidx] = (m + log2f(l)) * kLn2;
+      args.lse[lidx] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
     }
   }
 

@@ -4,8 +4,9 @@
 //
 // Forward: one CTA per (64 query rows of one rank, batch*head).  The CTA walks
 // the ring -- step t brings the K/V shard of rank (r - t) mod cp -- in 64-key
-// tiles, skips tiles that lie wholly in the causal future of every query of
-// the block, masks the rest element-wise on natural positions, and keeps the
+// tiles, skips tiles that no query of the block sees (wholly in the causal
+// future, or outside the packed documents of its rows), masks the rest
+// element-wise against each row's key window (natural positions), and keeps the
 // online-softmax state (running max m, running sum l, unnormalised O) in
 // registers ("Sequence Parallelism IV", sections 4-5).  A 64 x 64 score tile
 // is spread over 256 threads as 4 x 4 blocks; row max and row sum are reduced
@@ -79,9 +80,9 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const FwdArgs a) {
   float* Ks = Qs + BM * DP;
   float* Vs = Ks + BN * DP;
   float* Ps = Vs + BN * DP;
-  __shared__ int q_nat[BM];
+  __shared__ int q_lo[BM], q_hi[BM];  // key window of each query row
   __shared__ int k_nat[BN];
-  __shared__ int s_qmax;
+  __shared__ int s_lo, s_hi;
 
   const RingShape& sh = a.sh;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -96,16 +97,27 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const FwdArgs a) {
   const T* vp = static_cast<const T*>(a.v);
 
   load_tile<T, D>(Qs, qp, b, q0, qn, h, sh.H, sh.S);
-  if (tid < BM) q_nat[tid] = tid < qn ? natural_pos(sh, q0 + tid) : -1;
-  __syncthreads();
-  if (tid < 32) {
-    int mx = max(q_nat[tid], q_nat[tid + 32]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (tid == 0) s_qmax = mx;
+  if (tid < BM) {
+    int lo = INT_MAX, hi = -1;  // padding rows see nothing
+    if (tid < qn) query_window(sh, natural_pos(sh, q0 + tid), lo, hi);
+    q_lo[tid] = lo;
+    q_hi[tid] = hi;
   }
   __syncthreads();
-  const int qmax = s_qmax;
+  if (tid < 32) {
+    int lo = min(q_lo[tid], q_lo[tid + 32]), hi = max(q_hi[tid], q_hi[tid + 32]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    }
+    if (tid == 0) {
+      s_lo = lo;
+      s_hi = hi;
+    }
+  }
+  __syncthreads();
+  const int blk_lo = s_lo, blk_hi = s_hi;  // keys some row of the block sees
 
   float m[4], l[4], o[4][DV];
 #pragma unroll
@@ -126,9 +138,9 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const FwdArgs a) {
       if (tid < BN) {
         int kpos = tid < kn ? natural_pos(sh, k0 + tid) : INT_MAX;
         k_nat[tid] = kpos;
-        live = tid < kn && (!sh.causal || kpos <= qmax);
+        live = tid < kn && kpos >= blk_lo && kpos <= blk_hi;
       }
-      if (!__syncthreads_or(live)) continue;  // tile wholly in the causal future
+      if (!__syncthreads_or(live)) continue;  // no row of the block sees the tile
       ++tiles;
       load_tile<T, D>(Ks, kp, b, k0, kn, g, sh.Hkv, sh.S);
       load_tile<T, D>(Vs, vp, b, k0, kn, g, sh.Hkv, sh.S);
@@ -155,12 +167,12 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const FwdArgs a) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = ty * 4 + i;
-        const int qpos = q_nat[row];
+        const int lo = q_lo[row], hi = q_hi[row];
         float mx = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int col = tx + 16 * j;
-          const bool ok = qpos >= 0 && col < kn && (!sh.causal || k_nat[col] <= qpos);
+          const bool ok = col < kn && k_nat[col] >= lo && k_nat[col] <= hi;
           sc[i][j] = ok ? sc[i][j] * sh.scale_log2 : -INFINITY;
           mx = fmaxf(mx, sc[i][j]);
         }
@@ -236,11 +248,11 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
   float* Qs = Vs + BN * DP;
   float* Os = Qs + BM * DP;  // dO tile
   float* Ps = Os + BM * DP;  // P, then dS
-  __shared__ int q_nat[BM];
+  __shared__ int q_lo[BM], q_hi[BM];  // key window of each query row
   __shared__ int k_nat[BN];
   __shared__ float lse2[BM];  // LSE in base 2
   __shared__ float dlt[BM];
-  __shared__ int s_kmin;
+  __shared__ int s_kmin, s_kmax;
 
   const RingShape& sh = a.sh;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
@@ -260,12 +272,19 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
   __syncthreads();
   if (tid < 32) {
     int mn = min(k_nat[tid], k_nat[tid + 32]);
+    int mx = max(tid < kn ? k_nat[tid] : -1, tid + 32 < kn ? k_nat[tid + 32] : -1);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
-    if (tid == 0) s_kmin = mn;
+    for (int off = 16; off > 0; off >>= 1) {
+      mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    }
+    if (tid == 0) {
+      s_kmin = mn;
+      s_kmax = mx;
+    }
   }
   __syncthreads();
-  const int kmin = s_kmin;
+  const int kmin = s_kmin, kmax = s_kmax;
 
   float dk[4][DV], dv[4][DV];
 #pragma unroll
@@ -282,9 +301,11 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
         __syncthreads();
         int live = 0;
         if (tid < BM) {
-          int qpos = tid < qn ? natural_pos(sh, q0 + tid) : -1;
-          q_nat[tid] = qpos;
-          live = tid < qn && (!sh.causal || qpos >= kmin);
+          int lo = INT_MAX, hi = -1;  // padding rows see nothing
+          if (tid < qn) query_window(sh, natural_pos(sh, q0 + tid), lo, hi);
+          q_lo[tid] = lo;
+          q_hi[tid] = hi;
+          live = lo <= kmax && hi >= kmin;
           if (tid < qn) {
             int64_t li = ((int64_t)b * sh.H + h) * sh.S + q0 + tid;
             lse2[tid] = a.lse[li] * kLog2e;
@@ -329,11 +350,11 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int row = ty * 4 + i;
-          const int qpos = q_nat[row];
+          const int lo = q_lo[row], hi = q_hi[row];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int col = tx + 16 * j;
-            const bool ok = qpos >= 0 && col < kn && (!sh.causal || k_nat[col] <= qpos);
+            const bool ok = col < kn && k_nat[col] >= lo && k_nat[col] <= hi;
             const float p = ok ? exp2f(sc[i][j] * sh.scale_log2 - lse2[row]) : 0.f;
             sc[i][j] = p;
             dp[i][j] = p * (dp[i][j] - dlt[row]);

@@ -1,7 +1,7 @@
 // Bandwidth-bound kernels of the ring: zigzag permute / unpermute, the exact
 // LSE merge of two partials, the backward pre-pass (Delta = dO . O and zeroing
 // of the gradient accumulators) and the float32 -> output dtype conversion of
-// dQ, dK, dV.
+// dQ, dK, dV; and the per-position document bounds of a packed sequence.
 //
 // All of them move data in 16-byte vectors with consecutive threads on
 // consecutive vectors, and size their grids as a multiple of the SM count.
@@ -32,13 +32,16 @@ int grid_for(int64_t work_items, int threads, int per_sm) {
 // Permute.  A tensor [outer, S, inner] moves as outer * nchunk runs of
 // c * inner contiguous bytes (a chunk keeps its internal order), so the copy
 // is a gather of runs: run (o, sharded chunk ci) <-> (o, natural chunk nc).
+// The natural side may be shorter (S_nat <= S tokens): natural positions from
+// S_nat on are padding, written as zeros into the sharded tensor and dropped
+// on the way back.
 // ---------------------------------------------------------------------------
 template <typename V>
 __global__ void __launch_bounds__(256) permute_runs_kernel(const char* __restrict__ in,
                                                            char* __restrict__ out,
                                                            int64_t outer, int64_t S,
-                                                           int64_t inner_bytes, int cp,
-                                                           int per_rank, int64_t c,
+                                                           int64_t S_nat, int64_t inner_bytes,
+                                                           int cp, int per_rank, int64_t c,
                                                            int64_t run_vecs, bool inverse) {
   const int64_t nchunk = (int64_t)cp * per_rank;
   const int64_t total = outer * nchunk * run_vecs;
@@ -60,10 +63,21 @@ __global__ void __launch_bounds__(256) permute_runs_kernel(const char* __restric
         int r = (int)(ci / per_rank), j = (int)(ci % per_rank);
         int64_t nc = (per_rank == 1 || j == 0) ? r : 2 * cp - 1 - r;  // natural chunk
         int64_t sh_off = (o * S + ci * c) * inner_bytes + e * (int64_t)sizeof(V);
-        int64_t nat_off = (o * S + nc * c) * inner_bytes + e * (int64_t)sizeof(V);
-        int64_t src = inverse ? sh_off : nat_off;
-        dst[u] = inverse ? nat_off : sh_off;
-        val[u] = *reinterpret_cast<const V*>(in + src);
+        int64_t nat_off = (o * S_nat + nc * c) * inner_bytes + e * (int64_t)sizeof(V);
+        // Bytes of this run that hold real (non-padding) tokens.
+        int64_t real = S_nat - nc * c;
+        real = real < 0 ? 0 : (real > c ? c : real);
+        const bool is_real = e * (int64_t)sizeof(V) < real * inner_bytes;
+        if (inverse) {
+          dst[u] = is_real ? nat_off : -1;
+          if (is_real) val[u] = *reinterpret_cast<const V*>(in + sh_off);
+        } else {
+          dst[u] = sh_off;
+          if (is_real)
+            val[u] = *reinterpret_cast<const V*>(in + nat_off);
+          else
+            val[u] = V{};
+        }
       }
     }
 #pragma unroll
@@ -73,15 +87,16 @@ __global__ void __launch_bounds__(256) permute_runs_kernel(const char* __restric
 }
 
 template <typename V>
-cudaError_t permute_as(const void* in, void* out, int64_t outer, int64_t S, int64_t inner_bytes,
-                       const RingShape& sh, bool inverse, cudaStream_t stream) {
+cudaError_t permute_as(const void* in, void* out, int64_t outer, int64_t S, int64_t S_nat,
+                       int64_t inner_bytes, const RingShape& sh, bool inverse,
+                       cudaStream_t stream) {
   int64_t run_bytes = (int64_t)sh.c * inner_bytes;
   int64_t run_vecs = run_bytes / (int64_t)sizeof(V);
   int64_t total = outer * (int64_t)sh.cp * sh.per_rank * run_vecs;
   if (total == 0) return cudaSuccess;
   int grid = grid_for((total + 3) / 4, 256, 8);
   permute_runs_kernel<V><<<grid, 256, 0, stream>>>(
-      static_cast<const char*>(in), static_cast<char*>(out), outer, S, inner_bytes, sh.cp,
+      static_cast<const char*>(in), static_cast<char*>(out), outer, S, S_nat, inner_bytes, sh.cp,
       sh.per_rank, (int64_t)sh.c, run_vecs, inverse);
   return cudaGetLastError();
 }
@@ -280,20 +295,63 @@ __global__ void __launch_bounds__(256) grad_convert_kernel(const float4* __restr
   }
 }
 
+// ---------------------------------------------------------------------------
+// Document bounds.  Position p belongs to the document d with
+// cu[d] <= p < cu[d+1] (binary search over the offsets); threads d < ndocs
+// also check the offsets themselves (the caller guarantees 1 <= ndocs <= S,
+// so every offset is checked).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) doc_bounds_kernel(const int* __restrict__ cu, int ndocs,
+                                                         int S, int2* __restrict__ docs,
+                                                         int* err) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < S; x += stride) {
+    const int p = (int)x;
+    if (x < ndocs) {
+      bool bad = cu[x] >= cu[x + 1];
+      if (x == 0) bad = bad || cu[0] != 0 || cu[ndocs] != S;
+      if (bad) atomicExch(err, kErrBadDocs);
+    }
+    int lo = 0, hi = ndocs;  // invariant: cu[lo] <= p < cu[hi] for valid offsets
+    while (hi - lo > 1) {
+      const int mid = lo + (hi - lo) / 2;
+      if (cu[mid] <= p)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    int first = cu[lo], end = cu[lo + 1];
+    if (first < 0 || first > p) first = p;  // only for broken offsets
+    if (end <= p || end > S) end = p + 1;
+    docs[p] = make_int2(first, end);
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t S,
+cudaError_t launch_doc_bounds(const int* cu, int ndocs, int S, int2* docs, int* err,
+                              cudaStream_t stream) {
+  if (S == 0) return cudaSuccess;
+  doc_bounds_kernel<<<grid_for(S, 256, 4), 256, 0, stream>>>(cu, ndocs, S, docs, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const void* in, void* out, int64_t outer, int64_t S, int64_t S_nat,
                            int64_t inner_bytes, const RingShape& sh, bool inverse,
                            cudaStream_t stream) {
   int64_t run_bytes = (int64_t)sh.c * inner_bytes;
   uintptr_t a = reinterpret_cast<uintptr_t>(in) | reinterpret_cast<uintptr_t>(out);
-  // Every run starts at a multiple of run_bytes from the base pointers.
-  uint64_t align = (uint64_t)a | (uint64_t)run_bytes;
-  if ((align & 15) == 0) return permute_as<uint4>(in, out, outer, S, inner_bytes, sh, inverse, stream);
-  if ((align & 7) == 0) return permute_as<uint2>(in, out, outer, S, inner_bytes, sh, inverse, stream);
-  if ((align & 3) == 0) return permute_as<uint32_t>(in, out, outer, S, inner_bytes, sh, inverse, stream);
-  if ((align & 1) == 0) return permute_as<uint16_t>(in, out, outer, S, inner_bytes, sh, inverse, stream);
-  return permute_as<uint8_t>(in, out, outer, S, inner_bytes, sh, inverse, stream);
+  // Every run starts at a multiple of run_bytes (plus whole rows of S_nat
+  // tokens on the natural side) from the base pointers.
+  uint64_t align = (uint64_t)a | (uint64_t)run_bytes | (uint64_t)(S_nat * inner_bytes);
+#define CPATTN_PERMUTE_AS(V) \
+  permute_as<V>(in, out, outer, S, S_nat, inner_bytes, sh, inverse, stream)
+  if ((align & 15) == 0) return CPATTN_PERMUTE_AS(uint4);
+  if ((align & 7) == 0) return CPATTN_PERMUTE_AS(uint2);
+  if ((align & 3) == 0) return CPATTN_PERMUTE_AS(uint32_t);
+  if ((align & 1) == 0) return CPATTN_PERMUTE_AS(uint16_t);
+  return CPATTN_PERMUTE_AS(uint8_t);
+#undef CPATTN_PERMUTE_AS
 }
 
 cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_b,

@@ -10,7 +10,14 @@ the workload's dtype (round to nearest even for bf16).  Tensors are
 [B, S, H, D] (K, V, dO: [B, S, Hkv, D] / [B, S, H, D]) in natural token order.
 The pages publish no data set; these standard-normal draws are the
 distribution every workload below names.
+
+Packed documents: the pages test document masks but give no length
+distribution.  ``packed_doc_offsets`` draws document lengths from an
+exponential distribution with a stated mean (many short documents, a few
+long ones), from its own generator seeded with ``doc_seed``; the last
+document is cut at S.
 """
+import math
 from dataclasses import dataclass, field, replace
 from typing import Optional, Tuple
 
@@ -35,6 +42,8 @@ class Workload:
     backward: bool = False
     seed: int = 0
     cp_sweep: Tuple[int, ...] = field(default_factory=tuple)
+    doc_mean: int = 0   # > 0: packed documents of this mean length
+    doc_seed: int = 0
 
     def with_(self, **kw) -> "Workload":
         return replace(self, **kw)
@@ -43,8 +52,16 @@ class Workload:
     def dtype_name(self) -> str:
         return {torch.float32: "f32", torch.bfloat16: "bf16"}[self.dtype]
 
+    def doc_offsets(self):
+        """Document offsets [0, ..., S], or None for one document."""
+        if self.doc_mean <= 0:
+            return None
+        return packed_doc_offsets(self.S, self.doc_mean, self.doc_seed)
+
     def valid_pairs_per_head(self) -> int:
-        return self.S * (self.S + 1) // 2 if self.causal else self.S * self.S
+        cu = self.doc_offsets()
+        lens = [self.S] if cu is None else [b - a for a, b in zip(cu[:-1], cu[1:])]
+        return sum(n * (n + 1) // 2 if self.causal else n * n for n in lens)
 
     def useful_flops(self, backward: bool = False) -> float:
         """4*D flops per valid (q, k) pair forward, 10*D backward."""
@@ -67,6 +84,28 @@ WORKLOADS = {
     "c5_bf16_s131072_fwdbwd": Workload("c5_bf16_s131072_fwdbwd", 1, 32, 8, 131072, 128, 16,
                                        ZIGZAG, True, torch.bfloat16, backward=True, seed=1005),
 }
+
+# The S=131072 shape with packed documents (mean length 8192 tokens): the
+# document-mask workload.
+DOC_WORKLOADS = {
+    "docs_bf16_s131072_fwdbwd": Workload("docs_bf16_s131072_fwdbwd", 1, 32, 8, 131072, 128, 16,
+                                         ZIGZAG, True, torch.bfloat16, backward=True, seed=1006,
+                                         doc_mean=8192, doc_seed=2006),
+}
+
+
+def packed_doc_offsets(S: int, mean_len: float, seed: int, min_len: int = 1):
+    """Offsets [0, c1, ..., S] of documents packed into S tokens: lengths
+    exponential with mean ``mean_len`` (at least ``min_len``), the last
+    document cut at S."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    cu = [0]
+    while cu[-1] < S:
+        u = float(torch.rand((), generator=g, dtype=torch.float64))
+        n = max(min_len, int(round(-mean_len * math.log1p(-u))))
+        cu.append(min(S, cu[-1] + n))
+    return cu
 
 
 def generate(w: Workload, with_dout: Optional[bool] = None, pin: bool = False):

@@ -97,6 +97,27 @@ CPATTN_API int cpattn_zigzag_unpermute(const void* in, void* out, int64_t outer,
                             int64_t inner_bytes, int cp_size, int layout, cpattn_stream_t stream);
 
 /*
+ * The same reorderings with padding ("Context Parallelism for Long-Context
+ * Training", section "Test sequence divisibility and padding"): a sequence of
+ * S_real tokens that does not split into the ring's chunks is padded at its
+ * end to S tokens (S_real <= S, S as the permute above requires, e.g. from
+ * cpattn_padded_length).  The padding belongs to whichever ranks own the last
+ * natural positions (with zigzag: rank 0's second chunk first).
+ *   permute_pad:   in [outer, S_real, inner] natural -> out [outer, S, inner]
+ *                  sharded; natural positions >= S_real are written as zeros.
+ *   unpermute_pad: in [outer, S, inner] sharded -> out [outer, S_real, inner]
+ *                  natural; the padded positions are dropped.
+ * Pair the padded tensors with a document whose range is [S_real, S) (see
+ * cpattn_doc_bounds) so that no real token sees the padding.
+ */
+CPATTN_API int cpattn_zigzag_permute_pad(const void* in, void* out, int64_t outer, int64_t S_real,
+                                         int64_t S, int64_t inner_bytes, int cp_size, int layout,
+                                         cpattn_stream_t stream);
+CPATTN_API int cpattn_zigzag_unpermute_pad(const void* in, void* out, int64_t outer,
+                                           int64_t S_real, int64_t S, int64_t inner_bytes,
+                                           int cp_size, int layout, cpattn_stream_t stream);
+
+/*
  * Ring forward ("Sequence Parallelism IV ...", sections 4-5): for every
  * virtual rank r, its query shard attends to the K/V shards arriving at ring
  * steps t = 0..cp_size-1; tiles wholly in the causal future are skipped,
@@ -214,6 +235,68 @@ CPATTN_API int cpattn_ring_bwd_noalloc(const void* q, const void* k, const void*
                                        float softmax_scale, cpattn_stream_t stream);
 
 /*
+ * Packed documents and padding ("Context Parallelism for Long-Context
+ * Training", section "Prove attention equivalence": document masks, like the
+ * causal mask, must give the unsharded result; section "Test sequence
+ * divisibility and padding": padded tokens must not change any real token's
+ * output).  The sequence holds ndocs documents back to back: document d
+ * covers the natural positions [cu_seqlens[d], cu_seqlens[d+1]), and a token
+ * sees only tokens of its own document (with causal = 1, only the earlier
+ * ones and itself).  The same documents apply to every batch row.  Padding is
+ * one more document at the end: no real token sees it, and a zero dout on it
+ * gives it no gradient and makes it contribute none.
+ *
+ * cpattn_doc_bounds turns the offsets into per-position bounds, computed once
+ * and passed to the *_docs calls: bounds[2p] = first position and
+ * bounds[2p+1] = one past the last position of the document holding natural
+ * position p.
+ *   cu_seqlens: device int32 [ndocs + 1]: 0, strictly increasing, ending at S.
+ *   bounds: device int32 [S][2], 8-byte aligned.
+ * Requires 1 <= ndocs <= S.  Offsets that break the rule above are reported
+ * as CPATTN_ERR_INVALID_ARG by the next cpattn_device_status; the bounds are
+ * still written (each position's range contains the position), so the calls
+ * that read them stay within their buffers, but their results are undefined.
+ */
+CPATTN_API int cpattn_doc_bounds(const int32_t* cu_seqlens, int ndocs, int S, int32_t* bounds,
+                                 cpattn_stream_t stream);
+
+/*
+ * cpattn_ring_fwd under the document rule.  doc_bounds: from
+ * cpattn_doc_bounds for this S (device, natural positions).  Tiles that hold
+ * no visible pair -- causal future or other documents -- are skipped, so a
+ * packed sequence costs about the sum of its documents' own costs.
+ * tiles_rt: NULL, or the census of cpattn_ring_fwd_census (tiles with at
+ * least one visible pair under the document rule).
+ */
+CPATTN_API int cpattn_ring_fwd_docs(const void* q, const void* k, const void* v, void* out,
+                                    float* lse, int B, int H, int Hkv, int S, int D, int cp_size,
+                                    int layout, int causal, int dtype, float softmax_scale,
+                                    const int32_t* doc_bounds, unsigned long long* tiles_rt,
+                                    cpattn_stream_t stream);
+
+/*
+ * cpattn_ring_bwd under the document rule; out and lse from
+ * cpattn_ring_fwd_docs with the same doc_bounds.  Workspace as
+ * cpattn_ring_bwd (cpattn_ring_bwd_workspace_bytes).
+ */
+CPATTN_API int cpattn_ring_bwd_docs(const void* q, const void* k, const void* v, const void* out,
+                                    const void* dout, const float* lse, void* dq, void* dk,
+                                    void* dv, int B, int H, int Hkv, int S, int D, int cp_size,
+                                    int layout, int causal, int dtype, float softmax_scale,
+                                    const int32_t* doc_bounds, void* workspace,
+                                    size_t workspace_bytes, cpattn_stream_t stream);
+
+/*
+ * Sequence length to pad a sequence of S tokens to (host only): the smallest
+ * multiple of cp_size * 256 (contiguous) or 2 * cp_size * 256 (zigzag) that
+ * is >= S, so that every chunk is a whole number of 256-token query pairs
+ * and the tensor-core kernels take the problem.  With zigzag the padding
+ * lands in the last chunks (rank 0's second chunk first).  Returns -1 for
+ * S < 0, cp_size < 1 or an unknown layout.
+ */
+CPATTN_API int64_t cpattn_padded_length(int64_t S, int cp_size, int layout);
+
+/*
  * Closed-form work census of the ring (host only): for every rank r and
  * step t, the number of tile x tile blocks with at least one visible
  * (query, key) pair, tiles_rt[r*cp_size + t], and the number of visible
@@ -228,8 +311,9 @@ CPATTN_API int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal
 /*
  * Waits for `stream`, then reads and clears this device's error word.
  * Returns CPATTN_ERR_DEVICE_TIMEOUT if a kernel's bounded wait gave up since
- * the last call, CPATTN_ERR_CUDA if the stream reports a CUDA error, else
- * CPATTN_OK.  Synchronous.
+ * the last call, CPATTN_ERR_INVALID_ARG if cpattn_doc_bounds found broken
+ * document offsets since the last call, CPATTN_ERR_CUDA if the stream
+ * reports a CUDA error, else CPATTN_OK.  Synchronous.
  */
 CPATTN_API int cpattn_device_status(cpattn_stream_t stream);
 

@@ -125,6 +125,33 @@ def test_invalid_arguments_rejected_before_launch():
     # closed-form census: chunk length not a multiple of the tile
     arr = (ctypes.c_uint64 * 16)()
     assert lib.cpattn_tile_counts(96, 4, 1, 1, 8, arr, None) == E
+    # documents: bounds missing or misaligned, document count out of range
+    assert lib.cpattn_ring_fwd_docs(fake, fake, fake, fake, fake, *good, 0.0, null, null,
+                                    null) == E
+    assert lib.cpattn_ring_fwd_docs(fake, fake, fake, fake, fake, *good, 0.0,
+                                    ctypes.c_void_p(0x1004), null, null) == E
+    assert lib.cpattn_ring_bwd_docs(*args9, *good, 0.0, null, fake, need, null) == E
+    assert lib.cpattn_doc_bounds(fake, 0, 64, fake, null) == E
+    assert lib.cpattn_doc_bounds(fake, 65, 64, fake, null) == E
+    assert lib.cpattn_doc_bounds(null, 2, 64, fake, null) == E
+    assert lib.cpattn_doc_bounds(fake, 2, 64, ctypes.c_void_p(0x1004), null) == E
+    # padded permute: real length above the padded one
+    assert lib.cpattn_zigzag_permute_pad(fake, ctypes.c_void_p(0x90000), 1, 65, 64, 16, 4, 1,
+                                         null) == E
+
+
+@pytest.mark.parametrize("layout", [_binding.CONTIGUOUS, _binding.ZIGZAG])
+def test_padded_length(layout):
+    # The smallest length >= S whose chunks are whole 256-token query pairs.
+    per = 2 if layout == _binding.ZIGZAG else 1
+    for cp in (1, 2, 3, 4, 8, 16):
+        unit = cp * per * 256
+        for S in (0, 1, 255, unit - 1, unit, unit + 1, 5 * unit + 7, 131072):
+            got = cp_attn.padded_length(S, cp, layout)
+            assert got >= S and got % unit == 0 and got - S < unit, (S, cp, got)
+    assert cp_attn.lib().cpattn_padded_length(-1, 2, layout) == -1
+    assert cp_attn.lib().cpattn_padded_length(10, 0, layout) == -1
+    assert cp_attn.lib().cpattn_padded_length(10, 2, 5) == -1
 
 
 def test_balance_report_closed_form():
