@@ -12,8 +12,14 @@ forward on which the tensor-roofline target is quoted is timed in the same
 run and reported under "c3_forward".
 
 Metric: useful attention TFLOP/s -- 4*D flops per visible (query, key) pair
-forward, 10*D backward (S(S+1)/2 visible pairs per head when causal).  Inputs
-are far larger than L2 (129 MB), so no flush is needed between steps.
+forward, 10*D backward (S(S+1)/2 visible pairs per head when causal; under
+packed documents, the sum over documents).  Inputs are far larger than L2
+(129 MB), so no flush is needed between steps.
+
+The same run times the packed-document workload (S=131072, documents of mean
+length 8192) forward and backward and reports it under "docs";
+``--workload docs_bf16_s131072_fwdbwd`` makes it the main line (its step adds
+the document-bounds kernel and uses the document-rule forward/backward).
 
 Under torchrun (N > 1) each rank runs an independent replica on its own GPU
 (the path itself runs on one GPU: "replicas only"); the reported value is the
@@ -42,6 +48,7 @@ from context_causal_attention_zigzag_gb300 import inputs  # noqa: E402
 
 METRIC = "useful causal attention TFLOP/s on 1 GB300 (fwd, fwd+bwd) and % of BF16 tensor peak"
 UNIT = "TFLOP/s"
+ALL_WORKLOADS = {**inputs.WORKLOADS, **inputs.DOC_WORKLOADS}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum), from
@@ -50,8 +57,14 @@ UNIT = "TFLOP/s"
 # workload without a capture; must be re-taken whenever a kernel changes.
 CAPTURED_TRAFFIC = {
     "c5_bf16_s131072_fwdbwd": {
-        "ring_bwd": (2.15e9 + 16.56e6) + (33.48e9 + 4.40e9) + (5.67e9 + 2.12e9) + (4.30e9 + 1.05e9),
-        "ring_fwd": 3.57e9 + 1.07e9,
+        "ring_bwd": (2.149e9 + 16.82e6) + (55.861e9 + 4.291e9) + (5.646e9 + 2.121e9)
+        + (4.295e9 + 1.054e9),
+        "ring_fwd": 4.350e9 + 1.069e9,
+    },
+    "docs_bf16_s131072_fwdbwd": {
+        "ring_bwd": (2.149e9 + 16.65e6) + (12.209e9 + 4.272e9) + (2.946e9 + 2.109e9)
+        + (4.295e9 + 1.054e9),
+        "ring_fwd": 1.776e9 + 1.058e9,
     },
 }
 
@@ -143,7 +156,7 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = inputs.WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     peak, peak_sus, hbm, peak_kind = peaks()
     stream = torch.cuda.current_stream(dev)
 
@@ -169,6 +182,10 @@ def run_ours(args):
         dq_nat, dk_nat, dv_nat = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
         wsp = torch.empty(cpa.ring_bwd_workspace_bytes(B, H, Hkv, S, D, cpa.BF16 | cpa.GRAD_F32),
                           device=dev, dtype=torch.uint8)
+    docs = w.doc_offsets()
+    if docs is not None:
+        cu_dev = torch.tensor(docs, dtype=torch.int32, device=dev)
+        bounds = torch.empty((S, 2), dtype=torch.int32, device=dev)
     ev = {}
 
     def mark(name):
@@ -183,14 +200,23 @@ def run_ours(args):
         cpa.zigzag_permute(sv, cp, layout, out=vs)
         if w.backward:
             cpa.zigzag_permute(sdo, cp, layout, out=dos)
+        if docs is not None:
+            cpa.doc_bounds(cu_dev, S, out=bounds)
         if timed:
             mark("fwd0")
-        cpa.ring_fwd(qs, ks, vs, cp, layout, causal, out=o, lse=lse)
+        if docs is None:
+            cpa.ring_fwd(qs, ks, vs, cp, layout, causal, out=o, lse=lse)
+        else:
+            cpa.ring_fwd_docs(qs, ks, vs, cp, bounds, layout, causal, out=o, lse=lse)
         if timed:
             mark("fwd1")
         if w.backward:
-            cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, dq=dq, dk=dk, dv=dv,
-                         workspace=wsp, grad_dtype=gdt)
+            if docs is None:
+                cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, dq=dq, dk=dk, dv=dv,
+                             workspace=wsp, grad_dtype=gdt)
+            else:
+                cpa.ring_bwd_docs(qs, ks, vs, o, dos, lse, cp, bounds, layout, causal, dq=dq,
+                                  dk=dk, dv=dv, workspace=wsp, grad_dtype=gdt)
             if timed:
                 mark("bwd1")
         cpa.zigzag_unpermute(o, cp, layout, out=o_nat)
@@ -204,7 +230,8 @@ def run_ours(args):
         if w.backward else None
     # permutes + forward + backward (pre-pass, kernel(s), finishing pass) + unpermutes
     bwd_launches = (4 if bwd_path == cpa.PATH_TCGEN05 else 3) if w.backward else 0
-    launches_per_step = (4 if w.backward else 3) + 1 + bwd_launches + (5 if w.backward else 2)
+    launches_per_step = ((4 if w.backward else 3) + 1 + bwd_launches + (5 if w.backward else 2)
+                         + (1 if docs is not None else 0))
     fwd_flops = w.useful_flops(False)
     bwd_flops = w.useful_flops(True) if w.backward else 0.0
     step_flops = fwd_flops + bwd_flops
@@ -302,6 +329,12 @@ def run_ours(args):
     if args.workload != "c3_bf16_s32768_gqa" and not args.no_c3:
         c3 = time_forward(cpa, inputs.WORKLOADS["c3_bf16_s32768_gqa"], dev, stream,
                           args.warmup, max(args.steps, 5), peak)
+    # The packed-document workload, forward and backward timed alone.
+    docs_info = None
+    if docs is None and not args.no_docs:
+        wd = inputs.DOC_WORKLOADS["docs_bf16_s131072_fwdbwd"]
+        docs_info = time_docs(cpa, wd, dev, stream, args.warmup, max(args.steps, 5), peak)
+        docs_info["traffic"] = CAPTURED_TRAFFIC.get(wd.name)
 
     path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype)
     cpu = None
@@ -319,9 +352,11 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (no flush)",
                    "fwd_path": "tcgen05" if path == 1 else "simt", "tile": tile,
                    "grad_dtype": "f32" if w.backward else None,
+                   "documents": None if docs is None else len(docs) - 1,
                    "useful_tflop_per_step": step_flops / 1e12},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
-        "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "cpu_baseline": cpu,
+        "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "docs": docs_info,
+        "cpu_baseline": cpu,
         "status": cpa.device_status(),
     }
     if rank == 0:
@@ -362,6 +397,52 @@ def time_forward(cpa, w, dev, stream, warmup, steps, peak):
             "zigzag_step_imbalance_max_over_mean": imbalance}
 
 
+def time_docs(cpa, w, dev, stream, warmup, steps, peak):
+    """Forward and backward of a packed-document workload, each timed alone
+    (median of `steps`), in sharded order with the bounds precomputed."""
+    q, k, v, do = inputs.generate(w)
+    cu = w.doc_offsets()
+    qs, ks, vs, dos = (cpa.zigzag_permute(x.to(dev), w.cp, w.layout) for x in (q, k, v, do))
+    del q, k, v, do
+    bounds = cpa.doc_bounds(cu, w.S, dev)
+    o = torch.empty_like(qs)
+    lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    g = [torch.empty(x.shape, device=dev, dtype=torch.float32) for x in (qs, ks, vs)]
+    wsp = torch.empty(cpa.ring_bwd_workspace_bytes(w.B, w.H, w.Hkv, w.S, w.D,
+                                                   cpa.BF16 | cpa.GRAD_F32),
+                      device=dev, dtype=torch.uint8)
+
+    def fwd():
+        cpa.ring_fwd_docs(qs, ks, vs, w.cp, bounds, w.layout, w.causal, out=o, lse=lse)
+
+    def bwd():
+        cpa.ring_bwd_docs(qs, ks, vs, o, dos, lse, w.cp, bounds, w.layout, w.causal, dq=g[0],
+                          dk=g[1], dv=g[2], workspace=wsp, grad_dtype=torch.float32)
+
+    res = {}
+    for name, fn in (("fwd", fwd), ("bwd", bwd)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        tf = w.useful_flops(name == "bwd") / (ms * 1e-3) / 1e12
+        res[name] = {"ms_median": ms, "ms_min": min(times), "tflops": tf, "frac": tf / peak}
+    full = w.S * (w.S + 1) // 2
+    return {"workload": w.name, "documents": len(cu) - 1, "doc_mean": w.doc_mean,
+            "useful_pairs_vs_one_document": w.valid_pairs_per_head() / full,
+            "forward": res["fwd"], "backward": res["bwd"], "grad_dtype": "f32",
+            "status": cpa.device_status()}
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -377,16 +458,28 @@ def oracle_sample_rows(w, n, seed):
 def oracle_flops(w, rows, backward):
     # Visible keys per sampled row; forward 4*D per pair, plus the dQ part of
     # the backward (recompute S, dP, dQ: 6*D per pair) when timed.
-    keys = (rows[:, 2] + 1) if w.causal else np.full(len(rows), w.S)
+    cu = w.doc_offsets()
+    if cu is None:
+        keys = (rows[:, 2] + 1) if w.causal else np.full(len(rows), w.S)
+    else:
+        cu = np.asarray(cu)
+        d = np.searchsorted(cu, rows[:, 2], side="right") - 1
+        keys = (rows[:, 2] - cu[d] + 1) if w.causal else (cu[d + 1] - cu[d])
     per = 4 * w.D + (6 * w.D if backward else 0)
     return float(per) * float(keys.sum())
 
 
 def oracle_step(w, qf, kf, vf, dof, rows):
     import oracle
-    oracle.attn_fwd_rows(qf, kf, vf, rows, causal=w.causal)
-    if dof is not None:
-        oracle.attn_bwd_dq_rows(qf, kf, vf, dof, rows, causal=w.causal)
+    cu = w.doc_offsets()
+    if cu is None:
+        oracle.attn_fwd_rows(qf, kf, vf, rows, causal=w.causal)
+        if dof is not None:
+            oracle.attn_bwd_dq_rows(qf, kf, vf, dof, rows, causal=w.causal)
+    else:
+        oracle.attn_fwd_rows_docs(qf, kf, vf, rows, cu, causal=w.causal)
+        if dof is not None:
+            oracle.attn_bwd_dq_rows_docs(qf, kf, vf, dof, rows, cu, causal=w.causal)
 
 
 def cpu_baseline(w, q, k, v, do, budget_s=12.0, seed=0):
@@ -419,7 +512,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    w = inputs.WORKLOADS[args.workload]
+    w = ALL_WORKLOADS[args.workload]
     q, k, v, do = inputs.generate(w)
     cores = len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
@@ -450,7 +543,9 @@ def run_reference(args):
             "ms_per_step": total_t / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "Hkv": w.Hkv,
-                       "D": w.D, "cp": w.cp, "causal": w.causal, "backward": w.backward},
+                       "D": w.D, "cp": w.cp, "causal": w.causal, "backward": w.backward,
+                       "documents": (None if w.doc_offsets() is None
+                                     else len(w.doc_offsets()) - 1)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.get_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -463,11 +558,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c5_bf16_s131072_fwdbwd", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="c5_bf16_s131072_fwdbwd", choices=sorted(ALL_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-c3", action="store_true")
+    ap.add_argument("--no-docs", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

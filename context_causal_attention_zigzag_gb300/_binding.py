@@ -359,16 +359,19 @@ def ring_bwd_noalloc(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, sc
 # packed documents
 # ---------------------------------------------------------------------------
 
-def doc_bounds(cu_seqlens, S, device=None):
+def doc_bounds(cu_seqlens, S, device=None, out=None):
     """Per-position document bounds int32 [S, 2] from offsets cu_seqlens
     (0, strictly increasing, ..., S; a CUDA int32 tensor or anything
     torch.as_tensor takes)."""
     dev = device if device is not None else (
         cu_seqlens.device if torch.is_tensor(cu_seqlens) and cu_seqlens.is_cuda
         else torch.device("cuda", torch.cuda.current_device()))
-    cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev).contiguous()
+    cu = cu_seqlens if (torch.is_tensor(cu_seqlens) and cu_seqlens.is_cuda
+                        and cu_seqlens.dtype == torch.int32 and cu_seqlens.is_contiguous()) \
+        else torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev).contiguous()
     ndocs = cu.numel() - 1
-    bounds = torch.empty((S, 2), device=dev, dtype=torch.int32)
+    bounds = torch.empty((S, 2), device=dev, dtype=torch.int32) if out is None else out
+    _need_cuda(bounds)
     rc = lib().cpattn_doc_bounds(_ptr(cu), ndocs, int(S), _ptr(bounds), _stream(cu))
     _check("cpattn_doc_bounds", rc)
     return bounds

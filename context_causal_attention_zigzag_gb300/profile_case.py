@@ -3,6 +3,7 @@ profiler captures (ncu) wrap.
 
     python -m context_causal_attention_zigzag_gb300.profile_case fwd_s32768
     python -m context_causal_attention_zigzag_gb300.profile_case bwd_s16384
+    python -m context_causal_attention_zigzag_gb300.profile_case docs_full
 
 Cases are reduced versions of the named workloads (same heads, head dim and
 layout; fewer tokens or batches) so that a full counter capture of one launch
@@ -24,6 +25,8 @@ CASES = {
                                   torch.bfloat16, backward=True, seed=5),
     # the S=131072 forward+backward workload itself (for single-pass counters only)
     "c5_full": inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"],
+    # the same shape with packed documents (single-pass counters only)
+    "docs_full": inputs.DOC_WORKLOADS["docs_bf16_s131072_fwdbwd"],
 }
 
 
@@ -33,11 +36,19 @@ def run(case: str, repeats: int = 3) -> int:
     q, k, v, do = (x.to(dev) if x is not None else None for x in inputs.generate(w))
     qs, ks, vs = (cpa.zigzag_permute(x, w.cp, w.layout) for x in (q, k, v))
     dos = cpa.zigzag_permute(do, w.cp, w.layout) if do is not None else None
+    cu = w.doc_offsets()
+    bounds = cpa.doc_bounds(cu, w.S) if cu is not None else None
     for _ in range(repeats):
-        o, lse = cpa.ring_fwd(qs, ks, vs, w.cp, w.layout, w.causal)
-        if dos is not None:
+        if bounds is None:
+            o, lse = cpa.ring_fwd(qs, ks, vs, w.cp, w.layout, w.causal)
+        else:
+            o, lse = cpa.ring_fwd_docs(qs, ks, vs, w.cp, bounds, w.layout, w.causal)
+        if dos is not None and bounds is None:
             cpa.ring_bwd(qs, ks, vs, o, dos, lse, w.cp, w.layout, w.causal,
                          grad_dtype=torch.float32)
+        elif dos is not None:
+            cpa.ring_bwd_docs(qs, ks, vs, o, dos, lse, w.cp, bounds, w.layout, w.causal,
+                              grad_dtype=torch.float32)
     torch.cuda.synchronize()
     return cpa.device_status()
 
