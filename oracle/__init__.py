@@ -75,6 +75,11 @@ def _lib(mutation: int = 0):
     lib.oracle_attn_bwd_dq_rows_docs.argtypes = [_f32p] * 4 + shape + docs + [_i64p, _L, _f64p]
     lib.oracle_attn_bwd_dkdv_rows_sparse_docs.argtypes = ([_f32p] * 4 + shape + docs
                                                           + [_i64p, _L, _i64p, _L, _f64p, _f64p])
+    lib.oracle_allgather_fwd.argtypes = ([_f32p, _f32p, _f32p] + ring + docs
+                                         + [_f64p, _f64p])
+    lib.oracle_allgather_fwd.restype = _I
+    lib.oracle_allgather_bwd.argtypes = [_f32p] * 4 + ring + docs + [_f64p] * 3
+    lib.oracle_allgather_bwd.restype = _I
     _libs[mutation] = lib
     return lib
 
@@ -325,3 +330,43 @@ def attn_bwd_dkdv_rows_sparse_docs(q, k, v, dout, qrows, krows, cu_seqlens, caus
                                                          int(causal), scale, cu, nd, qrows,
                                                          qrows.shape[0], krows, n, dk, dv)
     return dk, dv
+
+
+def _cu_or_one(cu_seqlens, S):
+    return _cu(cu_seqlens if cu_seqlens is not None else [0, S], S)
+
+
+def allgather_fwd(q_sh, k_sh, v_sh, cp, layout, causal=True, scale=None, cu_seqlens=None,
+                  mutation: int = 0):
+    """The all-gather schedule on SHARDED-order inputs: every rank gathers the
+    whole K/V, then attends its own queries to it in one pass.  Returns
+    (out, lse) in sharded order."""
+    q, k, v = _f32(q_sh), _f32(k_sh), _f32(v_sh)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu_or_one(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    rc = _lib(mutation).oracle_allgather_fwd(q, k, v, B, H, Hkv, S, D, cp, layout, int(causal),
+                                             scale, cu, nd, out, lse)
+    if rc != 0:
+        raise ValueError("bad allgather_fwd arguments")
+    return out, lse
+
+
+def allgather_bwd(q_sh, k_sh, v_sh, do_sh, cp, layout, causal=True, scale=None, cu_seqlens=None,
+                  mutation: int = 0):
+    """Backward of the all-gather schedule, sharded order in and out: per-rank
+    dK/dV contributions summed over ranks, each rank keeping its shard."""
+    q, k, v, do = _f32(q_sh), _f32(k_sh), _f32(v_sh), _f32(do_sh)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu_or_one(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    dq = np.empty((B, S, H, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    rc = _lib(mutation).oracle_allgather_bwd(q, k, v, do, B, H, Hkv, S, D, cp, layout,
+                                             int(causal), scale, cu, nd, dq, dk, dv)
+    if rc != 0:
+        raise ValueError("bad allgather_bwd arguments")
+    return dq, dk, dv

@@ -483,6 +483,77 @@ int oracle_ring_fwd_docs(const float* q, const float* k, const float* v, long B,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The all-gather schedule                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Sharded <-> natural copies of a [B, S, X, D] float tensor with the chunker
+ * above: natural[b, nat[p]] = sharded[b, p]. */
+static void unshard_f(const float* sh, float* nat, const long* nat_of, long B, long S, long X,
+                      int D) {
+  for (long b = 0; b < B; ++b)
+    for (long p = 0; p < S; ++p)
+      memcpy(nat + idx4(b, nat_of[p], 0, 0, S, X, D), sh + idx4(b, p, 0, 0, S, X, D),
+             sizeof(float) * X * D);
+}
+
+/* The all-gather variant of context parallelism ("Context Parallelism in
+ * MegaDLMs", key-value communication patterns: the ranks exchange K/V before
+ * attention so that each holds the whole context).  Inputs are in sharded
+ * order, as the ranks hold them.  Step 1, all-gather: every rank r builds the
+ * whole K/V in natural order from all ranks' shards (shard s lands on the
+ * natural positions of s's chunks).  Step 2: r's own query tokens attend to
+ * the gathered K/V in one pass -- no ring steps, no partials to merge.  Out
+ * and LSE are written at r's own (sharded) positions.  Returns 0, or -1 if S
+ * does not split into chunks. */
+static int allgather_fwd_m(const float* q_sh, const float* k_sh, const float* v_sh, long B, int H,
+                           int Hkv, long S, int D, int cp, int layout, const Mask* msk,
+                           double scale, double* out_sh, double* lse_sh) {
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  if (oracle_shard_order(S, cp, layout, nat_of) != 0) {
+    free(nat_of);
+    return -1;
+  }
+  float* qn = (float*)malloc(sizeof(float) * B * S * H * D + 1);
+  float* kn = (float*)malloc(sizeof(float) * B * S * Hkv * D + 1);
+  float* vn = (float*)malloc(sizeof(float) * B * S * Hkv * D + 1);
+  unshard_f(q_sh, qn, nat_of, B, S, H, D);  /* only to index r's own queries */
+  unshard_f(k_sh, kn, nat_of, B, S, Hkv, D); /* the all-gather of K */
+  unshard_f(v_sh, vn, nat_of, B, S, Hkv, D); /* and of V */
+  const long L = S / cp;
+  for (int r = 0; r < cp; ++r) {
+#pragma omp parallel
+    {
+      long* keys = (long*)malloc(sizeof(long) * S);
+      double* sb = (double*)malloc(sizeof(double) * S);
+      for (long j = 0; j < S; ++j) keys[j] = j;
+#pragma omp for schedule(dynamic, 16)
+      for (long a = 0; a < B * H * L; ++a) {
+        long b = a / (H * L);
+        int h = (int)((a / L) % H);
+        long p = r * L + a % L; /* r's sharded position */
+        partial_row(qn, kn, vn, B, H, Hkv, S, D, msk, scale, b, h, nat_of[p], keys, S, sb,
+                    out_sh + idx4(b, p, h, 0, S, H, D), lse_sh + (b * H + h) * S + p);
+      }
+      free(keys);
+      free(sb);
+    }
+  }
+  free(qn);
+  free(kn);
+  free(vn);
+  free(nat_of);
+  return 0;
+}
+
+int oracle_allgather_fwd(const float* q_sh, const float* k_sh, const float* v_sh, long B, int H,
+                         int Hkv, long S, int D, int cp, int layout, int causal, double scale,
+                         const long* cu, long ndocs, double* out_sh, double* lse_sh) {
+  const Mask msk = {causal, cu, ndocs};
+  return allgather_fwd_m(q_sh, k_sh, v_sh, B, H, Hkv, S, D, cp, layout, &msk, scale, out_sh,
+                         lse_sh);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gradients                                                                 */
 /* ------------------------------------------------------------------------ */
 
@@ -559,6 +630,120 @@ static void attn_bwd_m(const float* q, const float* k, const float* v, const flo
   free(o);
   free(lse);
   free(delta);
+}
+
+/* Backward of the all-gather schedule, inputs and outputs in sharded order.
+ * Each rank r, from its own query tokens only: dQ of those tokens, and a
+ * contribution to dK / dV of every gathered key.  The contributions of all
+ * ranks are then summed and each rank keeps its own shard (the
+ * reduce-scatter that returns gathered gradients to their owners). */
+static int allgather_bwd_m(const float* q_sh, const float* k_sh, const float* v_sh,
+                           const float* do_sh, long B, int H, int Hkv, long S, int D, int cp,
+                           int layout, const Mask* msk, double scale, double* dq_sh,
+                           double* dk_sh, double* dv_sh) {
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  if (oracle_shard_order(S, cp, layout, nat_of) != 0) {
+    free(nat_of);
+    return -1;
+  }
+  const long nq = B * S * H * D, nkv = B * S * Hkv * D;
+  float* qn = (float*)malloc(sizeof(float) * nq + 1);
+  float* kn = (float*)malloc(sizeof(float) * nkv + 1);
+  float* vn = (float*)malloc(sizeof(float) * nkv + 1);
+  float* don = (float*)malloc(sizeof(float) * nq + 1);
+  unshard_f(q_sh, qn, nat_of, B, S, H, D);
+  unshard_f(k_sh, kn, nat_of, B, S, Hkv, D);
+  unshard_f(v_sh, vn, nat_of, B, S, Hkv, D);
+  unshard_f(do_sh, don, nat_of, B, S, H, D);
+  long* rank_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  const long L = S / cp;
+  for (long p = 0; p < S; ++p) rank_of[nat_of[p]] = p / L;
+  /* Forward state of every query row, natural order. */
+  double* o = (double*)malloc(sizeof(double) * nq + 1);
+  double* lse = (double*)malloc(sizeof(double) * B * H * S + 1);
+  double* delta = (double*)malloc(sizeof(double) * B * H * S + 1);
+  attn_fwd_m(qn, kn, vn, B, H, Hkv, S, D, msk, scale, o, lse);
+  for (long row = 0; row < B * S * H; ++row) {
+    long b = row / (S * H), i = (row / H) % S;
+    int h = (int)(row % H);
+    double t = 0.0;
+    for (int d = 0; d < D; ++d) t += (double)don[row * D + d] * o[row * D + d];
+    delta[(b * H + h) * S + i] = t;
+  }
+  /* Per-rank contributions to the gathered dK / dV, natural order. */
+  double* part_k = (double*)calloc((size_t)cp * nkv + 1, sizeof(double));
+  double* part_v = (double*)calloc((size_t)cp * nkv + 1, sizeof(double));
+  double* dqn = (double*)calloc((size_t)nq + 1, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 4)
+  for (long bg = 0; bg < B * Hkv; ++bg) {
+    long b = bg / Hkv;
+    int g = (int)(bg % Hkv);
+    for (int h = 0; h < H; ++h) {
+      if (kv_head_of(h, H, Hkv) != g) continue;
+      for (long i = 0; i < S; ++i) {
+        const long r = rank_of[i];
+        const float* qi = qn + idx4(b, i, h, 0, S, H, D);
+        const float* doi = don + idx4(b, i, h, 0, S, H, D);
+        const double l = lse[(b * H + h) * S + i], dl = delta[(b * H + h) * S + i];
+        double* dqi = dqn + idx4(b, i, h, 0, S, H, D);
+        for (long j = 0; j < S; ++j) {
+          if (!visible(msk, i, j)) continue;
+          const float* kj = kn + idx4(b, j, g, 0, S, Hkv, D);
+          const float* vj = vn + idx4(b, j, g, 0, S, Hkv, D);
+          double pr = exp(scale * dot_f(qi, kj, D) - l);
+          double ds = pr * (dot_f(doi, vj, D) - dl);
+          double* pk = part_k + r * nkv + idx4(b, j, g, 0, S, Hkv, D);
+          double* pv = part_v + r * nkv + idx4(b, j, g, 0, S, Hkv, D);
+          for (int d = 0; d < D; ++d) {
+            dqi[d] += scale * ds * (double)kj[d];
+            pk[d] += scale * ds * (double)qi[d];
+            pv[d] += pr * (double)doi[d];
+          }
+        }
+      }
+    }
+  }
+  /* Reduce over ranks, scatter to the owners (sharded order). */
+  for (long b = 0; b < B; ++b)
+    for (long p = 0; p < S; ++p) {
+      const long j = nat_of[p];
+      for (long x = 0; x < (long)Hkv * D; ++x) {
+        double sk = 0.0, sv = 0.0;
+        for (int r = 0; r < cp; ++r) {
+#if ORACLE_MUTATION == 8
+          if (r == cp - 1 && cp > 1) continue; /* one rank's contribution dropped */
+#endif
+          sk += part_k[r * nkv + idx4(b, j, 0, 0, S, Hkv, D) + x];
+          sv += part_v[r * nkv + idx4(b, j, 0, 0, S, Hkv, D) + x];
+        }
+        dk_sh[idx4(b, p, 0, 0, S, Hkv, D) + x] = sk;
+        dv_sh[idx4(b, p, 0, 0, S, Hkv, D) + x] = sv;
+      }
+      memcpy(dq_sh + idx4(b, p, 0, 0, S, H, D), dqn + idx4(b, j, 0, 0, S, H, D),
+             sizeof(double) * H * D);
+    }
+  free(qn);
+  free(kn);
+  free(vn);
+  free(don);
+  free(rank_of);
+  free(o);
+  free(lse);
+  free(delta);
+  free(part_k);
+  free(part_v);
+  free(dqn);
+  free(nat_of);
+  return 0;
+}
+
+int oracle_allgather_bwd(const float* q_sh, const float* k_sh, const float* v_sh,
+                         const float* do_sh, long B, int H, int Hkv, long S, int D, int cp,
+                         int layout, int causal, double scale, const long* cu, long ndocs,
+                         double* dq_sh, double* dk_sh, double* dv_sh) {
+  const Mask msk = {causal, cu, ndocs};
+  return allgather_bwd_m(q_sh, k_sh, v_sh, do_sh, B, H, Hkv, S, D, cp, layout, &msk, scale,
+                         dq_sh, dk_sh, dv_sh);
 }
 
 void oracle_attn_bwd(const float* q, const float* k, const float* v, const float* dout,

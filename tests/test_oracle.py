@@ -19,7 +19,12 @@ mutated build of it) disagrees with an independent fact:
   documents, one token per document (out = its own V, LSE = its own score),
   packed documents equal to each document run alone (so padding as a
   document of its own leaves real tokens untouched), one document equal to
-  the plain mask, and the ring under documents equal to the definition.
+  the plain mask, and the ring under documents equal to the definition;
+* the all-gather schedule ("Context Parallelism in MegaDLMs", key-value
+  communication patterns: each rank gathers all K/V, then attends in one
+  pass; gradients summed over ranks and returned to the owners) equal to
+  the definition, forward and backward, for every cp and layout, with and
+  without documents.
 
 ``test_mutations_are_caught`` compiles planted mistakes into the oracle and
 checks that some pin fails for each.
@@ -359,11 +364,38 @@ def pin_docs_tile_counts(m=0):
                 assert ((pairs == 0) == (tiles == 0)).all()
 
 
+def _shard(x, order):
+    return np.ascontiguousarray(x[:, order])
+
+
+def pin_allgather(m=0):
+    B, H, Hkv, S, D = 1, 2, 1, 32, 4
+    q, k, v, do = small(B, H, Hkv, S, D, 68, dout=True)
+    for causal in (True, False):
+        for cu in (None, DOCS_S32):
+            cuo = cu if cu is not None else [0, S]
+            ro, rl = oracle.attn_fwd_docs(q, k, v, cuo, causal=causal, mutation=m)
+            rq, rk, rv = oracle.attn_bwd_docs(q, k, v, do, cuo, causal=causal, mutation=m)
+            for cp in (1, 2, 4):
+                for layout in (oracle.CONTIGUOUS, oracle.ZIGZAG):
+                    order = oracle.shard_order(S, cp, layout, mutation=m)
+                    qs, ks, vs, ds = (_shard(x, order) for x in (q, k, v, do))
+                    o, l = oracle.allgather_fwd(qs, ks, vs, cp, layout, causal, cu_seqlens=cu,
+                                                mutation=m)
+                    np.testing.assert_allclose(o, ro[:, order], rtol=0, atol=1e-12)
+                    np.testing.assert_allclose(l, rl[:, :, order], rtol=0, atol=1e-12)
+                    gq, gk, gv = oracle.allgather_bwd(qs, ks, vs, ds, cp, layout, causal,
+                                                      cu_seqlens=cu, mutation=m)
+                    np.testing.assert_allclose(gq, rq[:, order], rtol=0, atol=1e-11)
+                    np.testing.assert_allclose(gk, rk[:, order], rtol=0, atol=1e-11)
+                    np.testing.assert_allclose(gv, rv[:, order], rtol=0, atol=1e-11)
+
+
 PINS = [pin_zigzag_golden, pin_contiguous_golden, pin_coverage, pin_brute_force,
         pin_constant_v, pin_q_zero, pin_row0, pin_ring_invariance, pin_step_partials_merge,
         pin_finite_differences, pin_sum_rules, pin_tile_counts, pin_docs_brute_force,
         pin_docs_finite_differences, pin_docs_one_token_each, pin_docs_packed_equals_separate,
-        pin_docs_single_and_ring, pin_docs_tile_counts]
+        pin_docs_single_and_ring, pin_docs_tile_counts, pin_allgather]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -440,7 +472,7 @@ def test_bad_arguments_rejected():
 MUTATIONS = {1: "wrong zigzag pairing", 2: "interleaved GQA head map",
              3: "causal diagonal dropped", 4: "softmax scale dropped",
              5: "merge term dropped", 6: "ring turned the other way",
-             7: "document border off by one"}
+             7: "document border off by one", 8: "all-gather reduce drops a rank"}
 
 
 @pytest.mark.parametrize("m", sorted(MUTATIONS), ids=[MUTATIONS[m] for m in sorted(MUTATIONS)])
