@@ -40,6 +40,8 @@ SIGNATURES = {
     "cpattn_ring_fwd_docs": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _vp]),
     "cpattn_ring_bwd_docs": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_padded_length": (_i64, [_i64, _i, _i]),
+    "cpattn_allgather_fwd": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _vp]),
+    "cpattn_allgather_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_ring_fwd": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp]),
     "cpattn_ring_fwd_census": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp, _vp]),
     "cpattn_ring_fwd_plan": (_i, [_i] * 9 + [_ip, _ip]),
@@ -436,6 +438,65 @@ def _padded_docs(cu_seqlens, S_real, S, device):
 
 
 # ---------------------------------------------------------------------------
+# all-gather K/V schedule
+# ---------------------------------------------------------------------------
+
+def _kv_full_shape(q, k_full, v_full):
+    B, S, H, D = q.shape
+    if k_full.shape != v_full.shape or k_full.shape[0] != B or k_full.shape[1] != S \
+            or k_full.shape[3] != D or k_full.dtype != q.dtype or v_full.dtype != q.dtype:
+        raise ValueError("k_full, v_full must be [B, S, Hkv, D] of q's dtype")
+    return B, H, k_full.shape[2], S, D
+
+
+def kv_allgather(k, v, cp, layout=ZIGZAG, k_full=None, v_full=None):
+    """The all-gather of the sharded K and V on one GPU: every rank's shard
+    placed at its natural positions (cpattn_zigzag_unpermute)."""
+    return (zigzag_unpermute(k, cp, layout, out=k_full),
+            zigzag_unpermute(v, cp, layout, out=v_full))
+
+
+def allgather_fwd(q, k_full, v_full, cp, layout=ZIGZAG, causal=True, scale=None, bounds=None,
+                  out=None, lse=None, tiles_rt=None):
+    """Each rank's sharded queries against the whole natural-order K/V in one
+    pass (cpattn_allgather_fwd); returns (out, lse) in sharded order."""
+    _need_cuda(q, k_full, v_full, bounds)
+    B, H, Hkv, S, D = _kv_full_shape(q, k_full, v_full)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    _need_cuda(out, lse, tiles_rt)
+    rc = lib().cpattn_allgather_fwd(_ptr(q), _ptr(k_full), _ptr(v_full), _ptr(out), _ptr(lse), B,
+                                    H, Hkv, S, D, int(cp), int(layout), int(bool(causal)),
+                                    _dtype_code(q), _scale(scale), _ptr(bounds), _ptr(tiles_rt),
+                                    _stream(q))
+    _check("cpattn_allgather_fwd", rc)
+    return out, lse
+
+
+def allgather_bwd(q, k_full, v_full, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
+                  bounds=None, dq=None, dk_full=None, dv_full=None, workspace=None,
+                  grad_dtype=None):
+    """Backward of the all-gather schedule: dq sharded, dk_full / dv_full in
+    natural order summed over every rank's queries."""
+    _need_cuda(q, k_full, v_full, out, dout, lse, bounds)
+    B, H, Hkv, S, D = _kv_full_shape(q, k_full, v_full)
+    code, dq, dk_full, dv_full = _grad_args(q, k_full, v_full, dq, dk_full, dv_full, grad_dtype)
+    need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(dq, dk_full, dv_full, workspace)
+    rc = lib().cpattn_allgather_bwd(_ptr(q), _ptr(k_full), _ptr(v_full), _ptr(out), _ptr(dout),
+                                    _ptr(lse), _ptr(dq), _ptr(dk_full), _ptr(dv_full), B, H, Hkv,
+                                    S, D, int(cp), int(layout), int(bool(causal)), code,
+                                    _scale(scale), _ptr(bounds), _ptr(workspace),
+                                    workspace.numel(), _stream(q))
+    _check("cpattn_allgather_bwd", rc)
+    return dq, dk_full, dv_full
+
+
+# ---------------------------------------------------------------------------
 # census and status
 # ---------------------------------------------------------------------------
 
@@ -512,3 +573,19 @@ def attention_docs_fwd_bwd(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, ca
     un = lambda x: zigzag_unpermute_pad(x, cp, S_real, layout)  # noqa: E731
     return (un(o), zigzag_unpermute_pad(lse, cp, S_real, layout, seq_dim=2), un(dq), un(dk),
             un(dv))
+
+
+def attention_allgather_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None,
+                                grad_dtype=None):
+    """Natural order in and out, through the all-gather schedule: shard Q,
+    dO (and K, V as the ranks hold them), all-gather K/V, attend, backward,
+    reduce-scatter dK/dV to their owners, unshard.  Returns (out, lse, dq,
+    dk, dv) in natural order."""
+    qs, ks, vs, dos = (zigzag_permute(x, cp, layout) for x in (q, k, v, dout))
+    kf, vf = kv_allgather(ks, vs, cp, layout)
+    o, lse = allgather_fwd(qs, kf, vf, cp, layout, causal, scale)
+    dq, dkf, dvf = allgather_bwd(qs, kf, vf, o, dos, lse, cp, layout, causal, scale,
+                                 grad_dtype=grad_dtype)
+    dks, dvs = zigzag_permute(dkf, cp, layout), zigzag_permute(dvf, cp, layout)
+    un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
+    return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dks), un(dvs)

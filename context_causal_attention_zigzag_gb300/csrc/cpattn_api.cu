@@ -60,6 +60,7 @@ int make_shape(int B, int H, int Hkv, int S, int D, int cp, int layout, int caus
   sh->scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)D);
   sh->scale_log2 = sh->scale * 1.4426950408889634f;
   sh->docs = nullptr;
+  sh->kv_natural = 0;
   return CPATTN_OK;
 }
 
@@ -93,11 +94,13 @@ bool tc_bwd_eligible(const RingShape& sh, int dtype) {
 int fwd_common(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
                int Hkv, int S, int D, int cp, int layout, int causal, int dtype,
                float softmax_scale, int t_begin, int t_end, int step_mode,
-               unsigned long long* tiles_rt, const int2* docs, cudaStream_t stream) {
+               unsigned long long* tiles_rt, const int2* docs, int kv_natural,
+               cudaStream_t stream) {
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp, layout, causal, softmax_scale, &sh);
   if (rc != CPATTN_OK) return rc;
   sh.docs = docs;
+  sh.kv_natural = kv_natural;
   if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   if ((long long)B * S == 0) return CPATTN_OK;
   if (!q || !k || !v || !out || !lse) return CPATTN_ERR_INVALID_ARG;
@@ -203,7 +206,7 @@ int cpattn_ring_fwd(const void* q, const void* k, const void* v, void* out, floa
                     int H, int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
                     float softmax_scale, cpattn_stream_t stream) {
   return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, 0, cp_size, 0, nullptr, nullptr, (cudaStream_t)stream);
+                    softmax_scale, 0, cp_size, 0, nullptr, nullptr, 0, (cudaStream_t)stream);
 }
 
 int cpattn_doc_bounds(const int32_t* cu_seqlens, int ndocs, int S, int32_t* bounds,
@@ -227,7 +230,7 @@ int cpattn_ring_fwd_docs(const void* q, const void* k, const void* v, void* out,
   const int2* docs = nullptr;
   if (doc_bounds == nullptr || !doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, 0, cp_size, 0, tiles_rt, docs, (cudaStream_t)stream);
+                    softmax_scale, 0, cp_size, 0, tiles_rt, docs, 0, (cudaStream_t)stream);
 }
 
 int64_t cpattn_padded_length(int64_t S, int cp_size, int layout) {
@@ -243,7 +246,7 @@ int cpattn_ring_fwd_census(const void* q, const void* k, const void* v, void* ou
                            unsigned long long* tiles_rt, cpattn_stream_t stream) {
   if (tiles_rt == nullptr) return CPATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, 0, cp_size, 0, tiles_rt, nullptr, (cudaStream_t)stream);
+                    softmax_scale, 0, cp_size, 0, tiles_rt, nullptr, 0, (cudaStream_t)stream);
 }
 
 int cpattn_ring_fwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
@@ -262,7 +265,7 @@ int cpattn_ring_fwd_step(const void* q, const void* k, const void* v, int B, int
                          cpattn_stream_t stream) {
   if (step < 0 || step >= cp_size) return CPATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, o_part, lse_part, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
-                    softmax_scale, step, step + 1, 1, nullptr, nullptr, (cudaStream_t)stream);
+                    softmax_scale, step, step + 1, 1, nullptr, nullptr, 0, (cudaStream_t)stream);
 }
 
 int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
@@ -293,11 +296,13 @@ namespace {
 int bwd_common(const void* q, const void* k, const void* v, const void* out, const void* dout,
                const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int S,
                int D, int cp_size, int layout, int causal, int dtype, float softmax_scale,
-               const int2* docs, void* workspace, size_t workspace_bytes, cudaStream_t st) {
+               const int2* docs, int kv_natural, void* workspace, size_t workspace_bytes,
+               cudaStream_t st) {
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp_size, layout, causal, softmax_scale, &sh);
   if (rc != CPATTN_OK) return rc;
   sh.docs = docs;
+  sh.kv_natural = kv_natural;
   const int in_dtype = dtype & ~CPATTN_GRAD_F32;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   const int out_dtype = (dtype & CPATTN_GRAD_F32) ? CPATTN_F32 : in_dtype;
@@ -372,7 +377,7 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
                     float softmax_scale, void* workspace, size_t workspace_bytes,
                     cpattn_stream_t stream) {
   return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout, causal,
-                    dtype, softmax_scale, nullptr, workspace, workspace_bytes,
+                    dtype, softmax_scale, nullptr, 0, workspace, workspace_bytes,
                     (cudaStream_t)stream);
 }
 
@@ -384,7 +389,31 @@ int cpattn_ring_bwd_docs(const void* q, const void* k, const void* v, const void
   const int2* docs = nullptr;
   if (doc_bounds == nullptr || !doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
   return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout, causal,
-                    dtype, softmax_scale, docs, workspace, workspace_bytes, (cudaStream_t)stream);
+                    dtype, softmax_scale, docs, 0, workspace, workspace_bytes,
+                    (cudaStream_t)stream);
+}
+
+int cpattn_allgather_fwd(const void* q, const void* k_full, const void* v_full, void* out,
+                         float* lse, int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                         int causal, int dtype, float softmax_scale, const int32_t* doc_bounds,
+                         unsigned long long* tiles_rt, cpattn_stream_t stream) {
+  const int2* docs = nullptr;
+  if (!doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k_full, v_full, out, lse, B, H, Hkv, S, D, cp_size, layout, causal, dtype,
+                    softmax_scale, 0, cp_size, 0, tiles_rt, docs, 1, (cudaStream_t)stream);
+}
+
+int cpattn_allgather_bwd(const void* q, const void* k_full, const void* v_full, const void* out,
+                         const void* dout, const float* lse, void* dq, void* dk_full,
+                         void* dv_full, int B, int H, int Hkv, int S, int D, int cp_size,
+                         int layout, int causal, int dtype, float softmax_scale,
+                         const int32_t* doc_bounds, void* workspace, size_t workspace_bytes,
+                         cpattn_stream_t stream) {
+  const int2* docs = nullptr;
+  if (!doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
+  return bwd_common(q, k_full, v_full, out, dout, lse, dq, dk_full, dv_full, B, H, Hkv, S, D,
+                    cp_size, layout, causal, dtype, softmax_scale, docs, 1, workspace,
+                    workspace_bytes, (cudaStream_t)stream);
 }
 
 int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal, int64_t tile,

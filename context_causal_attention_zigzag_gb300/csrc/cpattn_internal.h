@@ -24,7 +24,26 @@ struct RingShape {
   // document holding natural position p; a token sees only its own document.
   // nullptr: the whole sequence is one document.
   const int2* docs;
+  // K/V schedule.  0, ring: K, V (dK, dV) are in sharded order like Q and
+  // the tiles of rank (r - t) mod cp arrive at step t ("Sequence Parallelism
+  // IV", section 4).  1, all-gather: every rank holds the whole K, V (dK,
+  // dV) in natural order and walks it chunk by chunk in natural order
+  // ("Context Parallelism in MegaDLMs", key-value communication patterns).
+  int kv_natural;
 };
+
+// Rank owning natural chunk kc, and the chunk's slot in that rank's shard.
+__host__ __device__ inline int chunk_owner(const RingShape& s, int kc) {
+  return (s.per_rank == 1 || kc < s.cp) ? kc : 2 * s.cp - 1 - kc;
+}
+__host__ __device__ inline int chunk_slot(const RingShape& s, int kc) {
+  return (s.per_rank == 1 || kc < s.cp) ? 0 : 1;
+}
+// Ring step at which rank r holds the K/V of rank src.
+__host__ __device__ inline int ring_step_of(int r, int src, int cp) {
+  int t = (r - src) % cp;
+  return t < 0 ? t + cp : t;
+}
 
 // Keys visible to the query at natural position i: the natural range [lo, hi].
 // Both ends are non-decreasing in i, so the keys that some query of a run of

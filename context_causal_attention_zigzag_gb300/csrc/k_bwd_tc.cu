@@ -123,10 +123,13 @@ __device__ __forceinline__ TilePos tile_pos(const RingShape& sh, int knat) {
 // Query tiles (of one head) that see a K/V tile, in ring order: step t,
 // receiving rank (s + t) mod cp, that rank's chunks.  The tile's keys are
 // seen by the queries [lo, hi] (natural positions): under the causal rule
-// from the tile's first key on, within the documents of its keys.
+// from the tile's first key on, within the documents of its keys.  In the
+// all-gather schedule (sh.kv_natural) the query chunks are taken in natural
+// order instead (t is then the chunk index); query rows stay sharded.
 struct QSeq {
-  int cp, per, L, c, s, lo, hi;
+  int cp, per, L, c, s, lo, hi, t_end;
   int t, jq, qt, qt_end;
+  bool natural;
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& kv, int knat) {
     cp = sh.cp;
@@ -134,6 +137,8 @@ struct QSeq {
     L = sh.L;
     c = sh.c;
     s = kv.rank;
+    natural = sh.kv_natural != 0;
+    t_end = natural ? cp * per : cp;
     int x;
     key_window(sh, knat * kT, lo, x);
     key_window(sh, knat * kT + kT - 1, x, hi);
@@ -145,13 +150,14 @@ struct QSeq {
 
   // qrow: sharded row of the query tile; qnat: natural position of its first row.
   __device__ __forceinline__ bool next(int& qrow, int& qnat) {
-    while (t < cp) {
-      const int r = (s + t) % cp;
-      while (jq < per) {
-        const int qc = (per == 1 || jq == 0) ? r : 2 * cp - 1 - r;
+    while (t < t_end) {
+      const int r = natural ? ((per == 1 || t < cp) ? t : 2 * cp - 1 - t) : (s + t) % cp;
+      while (jq < (natural ? 1 : per)) {
+        const int qc = natural ? t : ((per == 1 || jq == 0) ? r : 2 * cp - 1 - r);
+        const int slot = natural ? ((per == 1 || t < cp) ? 0 : 1) : jq;
         if (qt_end < 0) tiles_overlapping(qc * c, c, kT, lo, hi, qt, qt_end);
         if (qt < qt_end) {
-          qrow = r * L + jq * c + qt * kT;
+          qrow = r * L + slot * c + qt * kT;
           qnat = qc * c + qt * kT;
           ++qt;
           return true;
@@ -171,10 +177,11 @@ struct QSeq {
 // rank (r - t) mod cp), the diagonal tile last.  The query tile sees the keys
 // [lo(first row), hi(last row)]; under the causal rule the ring walk stops
 // before the tile's own first key and the diagonal tile comes at the end.
+// All-gather schedule: natural chunk order, natural K/V rows.
 struct KSeq {
-  int cp, per, L, c, r, qrow, q0, wlo, whi;
+  int cp, per, L, c, r, qrow, q0, wlo, whi, t_end;
   int t, jj, kt, kt_end;
-  bool tail;
+  bool tail, natural;
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& q, int knat) {
     cp = sh.cp;
@@ -188,6 +195,8 @@ struct KSeq {
     query_window(sh, q0, wlo, x);
     query_window(sh, q0 + kT - 1, x, hi);
     whi = sh.causal ? q0 - 1 : hi;
+    natural = sh.kv_natural != 0;
+    t_end = natural ? cp * per : cp;
     t = 0;
     jj = 0;
     kt = 0;
@@ -197,14 +206,14 @@ struct KSeq {
 
   // kvrow: sharded row of the K/V tile; knat: natural position of its first key.
   __device__ __forceinline__ bool next(int& kvrow, int& knat) {
-    while (t < cp) {
-      const int s = ring_source(r, t, cp);
-      while (jj < per) {
-        const int kc = (per == 1 || jj == 0) ? s : 2 * cp - 1 - s;
+    while (t < t_end) {
+      const int s = natural ? 0 : ring_source(r, t, cp);
+      while (jj < (natural ? 1 : per)) {
+        const int kc = natural ? t : ((per == 1 || jj == 0) ? s : 2 * cp - 1 - s);
         if (kt_end < 0) tiles_overlapping(kc * c, c, kT, wlo, whi, kt, kt_end);
         if (kt < kt_end) {
-          kvrow = s * L + jj * c + kt * kT;
           knat = kc * c + kt * kT;
+          kvrow = natural ? knat : s * L + jj * c + kt * kT;
           ++kt;
           return true;
         }
@@ -216,7 +225,7 @@ struct KSeq {
       jj = 0;
     }
     if (tail) {
-      kvrow = qrow;  // the diagonal tile holds the query tile's own tokens
+      kvrow = natural ? q0 : qrow;  // the diagonal tile: the query tile's own tokens
       knat = q0;
       tail = false;
       return true;
@@ -346,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(bar(kBarKVFull), 2 * kTileBytes);
         ++kv_armed;
-        const int krow = it.b * sh.S + it.kv.row;
+        const int krow = it.b * sh.S + (sh.kv_natural ? it.knat * kT : it.kv.row);
         for (int half = 0; half < 2; ++half) {
           tma_load_3d(sK + half * kBoxBytes, &tm_k, bar(kBarKVFull), half * 64, it.g, krow);
           tma_load_3d(sV + half * kBoxBytes, &tm_v, bar(kBarKVFull), half * 64, it.g, krow);
@@ -599,8 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
+      const int kv_row0 = sh.kv_natural ? it.knat * kT : it.kv.row;
       const int64_t pbase =
-          (((int64_t)it.b * sh.S + it.kv.row + row) * sh.H + it.h) * kD + 64 * half;
+          (((int64_t)it.b * sh.S + kv_row0 + row) * sh.H + it.h) * kD + 64 * half;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         float* dst = (which == 0 ? args.dv_part : args.dk_part) + pbase;

@@ -127,11 +127,16 @@ __device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
 // visited when either window meets it.  Under the causal rule the ring walk
 // stops before the item's first row: keys from there on are the diagonal
 // tiles (step 0 only) or the causal future.
+//
+// All-gather schedule (sh.kv_natural): K/V rows are natural positions and
+// the walk takes the natural chunks in order (t is then the chunk index);
+// `step` still reports the ring step at which the chunk's owner would have
+// delivered it, so the census is the same.
 struct KvSeq {
   int cp, per, L, c, t_end, r, a, qrow;
   int lo[2], hi[2], wlo, whi;
   int t, jj, kt, kt_end, tail;
-  bool tail_on;
+  bool tail_on, natural;
 
   __device__ __forceinline__ void init(const RingShape& sh, int t_begin, int t_end_,
                                        const Item& it) {
@@ -150,7 +155,9 @@ struct KvSeq {
     }
     wlo = lo[0];
     whi = sh.causal ? a * kT - 1 : hi[1];
+    natural = sh.kv_natural != 0;
     t = t_begin;
+    if (natural) t_end = cp * per;  // whole ring only
     jj = 0;
     kt = 0;
     kt_end = -1;
@@ -166,17 +173,18 @@ struct KvSeq {
   // knat: natural position of the tile's first key.
   __device__ __forceinline__ bool next(int& kvrow, int& fl, int& step, int& knat) {
     while (t < t_end) {
-      const int s = ring_source(r, t, cp);
-      while (jj < per) {
-        const int kc = (per == 1 || jj == 0) ? s : 2 * cp - 1 - s;
+      // ring: source rank of step t; all-gather: owner of natural chunk t
+      const int s = natural ? ((per == 1 || t < cp) ? t : 2 * cp - 1 - t) : ring_source(r, t, cp);
+      while (jj < (natural ? 1 : per)) {
+        const int kc = natural ? t : ((per == 1 || jj == 0) ? s : 2 * cp - 1 - s);
         if (kt_end < 0) tiles_overlapping(kc * c, c, kT, wlo, whi, kt, kt_end);
         while (kt < kt_end) {
           const int k0 = kc * c + kt * kT;
-          kvrow = s * L + jj * c + kt * kT;
+          kvrow = natural ? k0 : s * L + jj * c + kt * kT;
           ++kt;
           fl = flags(k0);
           if (fl == 0) continue;
-          step = t;
+          step = natural ? ring_step_of(r, s, cp) : t;
           knat = k0;
           return true;
         }
@@ -191,7 +199,7 @@ struct KvSeq {
       // The diagonal tiles are the item's own rows; tile a + 1 is in the
       // future of query tile 0.
       const int k0 = (a + tail) * kT;
-      kvrow = qrow + tail * kT;
+      kvrow = natural ? k0 : qrow + tail * kT;
       fl = flags(k0) & (tail == 0 ? (kUse0 | kUse1) : kUse1);
       ++tail;
       if (fl == 0) continue;

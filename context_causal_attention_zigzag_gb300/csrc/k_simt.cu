@@ -128,20 +128,34 @@ __global__ void __launch_bounds__(NT) simt_fwd_kernel(const FwdArgs a) {
     for (int dd = 0; dd < DV; ++dd) o[i][dd] = 0.f;
   }
 
-  for (int t = a.t_begin; t < a.t_end; ++t) {
+  // Ring: steps t_begin..t_end-1, the shard of rank (r - t) mod cp each.
+  // All-gather (kv_natural): one pass over the whole K/V in natural order.
+  const bool nat_kv = sh.kv_natural != 0;
+  const int n_pass = nat_kv ? 1 : a.t_end - a.t_begin;
+  for (int pass = 0; pass < n_pass; ++pass) {
+    const int t = a.t_begin + pass;
     const int s = ring_source(r, t, sh.cp);
+    const int kbase = nat_kv ? 0 : s * sh.L, klen = nat_kv ? sh.S : sh.L;
     unsigned long long tiles = 0;
-    for (int kb = 0; kb < sh.L; kb += BN) {
-      const int k0 = s * sh.L + kb, kn = min(BN, sh.L - kb);
+    for (int kb = 0; kb < klen; kb += BN) {
+      const int k0 = kbase + kb, kn = min(BN, klen - kb);
       __syncthreads();  // the previous tile is fully consumed
       int live = 0;
       if (tid < BN) {
-        int kpos = tid < kn ? natural_pos(sh, k0 + tid) : INT_MAX;
+        int kpos = tid < kn ? (nat_kv ? k0 + tid : natural_pos(sh, k0 + tid)) : INT_MAX;
         k_nat[tid] = kpos;
         live = tid < kn && kpos >= blk_lo && kpos <= blk_hi;
       }
       if (!__syncthreads_or(live)) continue;  // no row of the block sees the tile
-      ++tiles;
+      if (nat_kv) {
+        // Census: the ring step at which the tile's first key would arrive.
+        if (a.tiles_rt != nullptr && tid == 0)
+          atomicAdd(&a.tiles_rt[r * sh.cp +
+                                ring_step_of(r, chunk_owner(sh, k_nat[0] / sh.c), sh.cp)],
+                    1ull);
+      } else {
+        ++tiles;
+      }
       load_tile<T, D>(Ks, kp, b, k0, kn, g, sh.Hkv, sh.S);
       load_tile<T, D>(Vs, vp, b, k0, kn, g, sh.Hkv, sh.S);
       __syncthreads();
@@ -256,11 +270,15 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
 
   const RingShape& sh = a.sh;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  // Ring: the CTA's 64 key rows lie in source rank s's shard.  All-gather
+  // (kv_natural): 64 rows of the natural-order K/V.
+  const bool nat_kv = sh.kv_natural != 0;
   const int nblk = (sh.L + BN - 1) / BN;
-  const int s = blockIdx.x / nblk, kb = blockIdx.x - s * nblk;
+  const int s = nat_kv ? 0 : blockIdx.x / nblk, kb = blockIdx.x - s * nblk;
   const int b = blockIdx.y / sh.Hkv, g = blockIdx.y - b * sh.Hkv;
   const int grp = sh.H / sh.Hkv;
-  const int k0 = s * sh.L + kb * BN, kn = min(BN, sh.L - kb * BN);
+  const int k0 = nat_kv ? blockIdx.x * BN : s * sh.L + kb * BN;
+  const int kn = nat_kv ? min(BN, sh.S - k0) : min(BN, sh.L - kb * BN);
   const T* qp = static_cast<const T*>(a.q);
   const T* kp = static_cast<const T*>(a.k);
   const T* vp = static_cast<const T*>(a.v);
@@ -268,7 +286,8 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
 
   load_tile<T, D>(Ks, kp, b, k0, kn, g, sh.Hkv, sh.S);
   load_tile<T, D>(Vs, vp, b, k0, kn, g, sh.Hkv, sh.S);
-  if (tid < BN) k_nat[tid] = tid < kn ? natural_pos(sh, k0 + tid) : INT_MAX;
+  if (tid < BN)
+    k_nat[tid] = tid < kn ? (nat_kv ? k0 + tid : natural_pos(sh, k0 + tid)) : INT_MAX;
   __syncthreads();
   if (tid < 32) {
     int mn = min(k_nat[tid], k_nat[tid + 32]);
@@ -295,7 +314,8 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
   for (int hh = 0; hh < grp; ++hh) {
     const int h = g * grp + hh;
     for (int t = 0; t < sh.cp; ++t) {
-      const int r = (s + t) % sh.cp;  // the rank holding this K/V at step t
+      // the rank holding this K/V at step t (all-gather: every rank, in order)
+      const int r = nat_kv ? t : (s + t) % sh.cp;
       for (int qb = 0; qb < sh.L; qb += BM) {
         const int q0 = r * sh.L + qb, qn = min(BM, sh.L - qb);
         __syncthreads();
@@ -458,7 +478,7 @@ cudaError_t bwd_as(const BwdArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nblk = (a.sh.L + BN - 1) / BN;
-  dim3 grid(nblk * a.sh.cp, a.sh.B * a.sh.Hkv);
+  dim3 grid(a.sh.kv_natural ? (a.sh.S + BN - 1) / BN : nblk * a.sh.cp, a.sh.B * a.sh.Hkv);
   kern<<<grid, NT, smem, stream>>>(a);
   return cudaGetLastError();
 }

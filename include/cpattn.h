@@ -287,6 +287,37 @@ CPATTN_API int cpattn_ring_bwd_docs(const void* q, const void* k, const void* v,
                                     size_t workspace_bytes, cpattn_stream_t stream);
 
 /*
+ * The all-gather K/V schedule ("Context Parallelism in MegaDLMs", key-value
+ * communication patterns: the ranks exchange K/V before attention so that
+ * each holds the whole context).  Every virtual rank attends its own query
+ * shard to the WHOLE K/V in one pass, walking it chunk by chunk in natural
+ * order; there are no ring steps and no partials to merge.  On one GPU the
+ * all-gather itself is cpattn_zigzag_unpermute of the sharded K and V into
+ * k_full / v_full (one copy serves every rank), and the reduce-scatter that
+ * returns gathered gradients to their owners is cpattn_zigzag_permute of
+ * dk_full / dv_full (the sum over ranks happens inside the backward).
+ *   q, out, lse, dout, dq: SHARDED order, as for cpattn_ring_fwd / _bwd;
+ *   k_full, v_full, dk_full, dv_full: [B,S,Hkv,D] in NATURAL order.
+ *   doc_bounds: NULL (one document) or from cpattn_doc_bounds.
+ *   tiles_rt: NULL or the census of cpattn_ring_fwd_census, each tile
+ *   attributed to the ring step at which its chunk's owner would deliver it
+ *   (so the counts equal the ring's).
+ * Shapes, dtypes, workspace and errors as cpattn_ring_fwd / cpattn_ring_bwd.
+ */
+CPATTN_API int cpattn_allgather_fwd(const void* q, const void* k_full, const void* v_full,
+                                    void* out, float* lse, int B, int H, int Hkv, int S, int D,
+                                    int cp_size, int layout, int causal, int dtype,
+                                    float softmax_scale, const int32_t* doc_bounds,
+                                    unsigned long long* tiles_rt, cpattn_stream_t stream);
+CPATTN_API int cpattn_allgather_bwd(const void* q, const void* k_full, const void* v_full,
+                                    const void* out, const void* dout, const float* lse, void* dq,
+                                    void* dk_full, void* dv_full, int B, int H, int Hkv, int S,
+                                    int D, int cp_size, int layout, int causal, int dtype,
+                                    float softmax_scale, const int32_t* doc_bounds,
+                                    void* workspace, size_t workspace_bytes,
+                                    cpattn_stream_t stream);
+
+/*
  * Sequence length to pad a sequence of S tokens to (host only): the smallest
  * multiple of cp_size * 256 (contiguous) or 2 * cp_size * 256 (zigzag) that
  * is >= S, so that every chunk is a whole number of 256-token query pairs

@@ -670,35 +670,49 @@ static int allgather_bwd_m(const float* q_sh, const float* k_sh, const float* v_
     for (int d = 0; d < D; ++d) t += (double)don[row * D + d] * o[row * D + d];
     delta[(b * H + h) * S + i] = t;
   }
-  /* Per-rank contributions to the gathered dK / dV, natural order. */
+  /* dQ of every query token (each rank computes its own). */
+  double* dqn = (double*)calloc((size_t)nq + 1, sizeof(double));
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long row = 0; row < B * S * H; ++row) {
+    long b = row / (S * H), i = (row / H) % S;
+    int h = (int)(row % H);
+    int g = kv_head_of(h, H, Hkv);
+    const float* qi = qn + row * D;
+    const float* doi = don + row * D;
+    const double l = lse[(b * H + h) * S + i], dl = delta[(b * H + h) * S + i];
+    for (long j = 0; j < S; ++j) {
+      if (!visible(msk, i, j)) continue;
+      const float* kj = kn + idx4(b, j, g, 0, S, Hkv, D);
+      const float* vj = vn + idx4(b, j, g, 0, S, Hkv, D);
+      double pr = exp(scale * dot_f(qi, kj, D) - l);
+      double ds = pr * (dot_f(doi, vj, D) - dl);
+      for (int d = 0; d < D; ++d) dqn[row * D + d] += scale * ds * (double)kj[d];
+    }
+  }
+  /* Per-rank contributions to the gathered dK / dV: rank r's queries only,
+   * for every key, natural order. */
   double* part_k = (double*)calloc((size_t)cp * nkv + 1, sizeof(double));
   double* part_v = (double*)calloc((size_t)cp * nkv + 1, sizeof(double));
-  double* dqn = (double*)calloc((size_t)nq + 1, sizeof(double));
-#pragma omp parallel for schedule(dynamic, 4)
-  for (long bg = 0; bg < B * Hkv; ++bg) {
-    long b = bg / Hkv;
-    int g = (int)(bg % Hkv);
+#pragma omp parallel for schedule(dynamic, 16)
+  for (long krow = 0; krow < B * S * Hkv; ++krow) {
+    long b = krow / (S * Hkv), j = (krow / Hkv) % S;
+    int g = (int)(krow % Hkv);
+    const float* kj = kn + krow * D;
+    const float* vj = vn + krow * D;
     for (int h = 0; h < H; ++h) {
       if (kv_head_of(h, H, Hkv) != g) continue;
       for (long i = 0; i < S; ++i) {
+        if (!visible(msk, i, j)) continue;
         const long r = rank_of[i];
         const float* qi = qn + idx4(b, i, h, 0, S, H, D);
         const float* doi = don + idx4(b, i, h, 0, S, H, D);
-        const double l = lse[(b * H + h) * S + i], dl = delta[(b * H + h) * S + i];
-        double* dqi = dqn + idx4(b, i, h, 0, S, H, D);
-        for (long j = 0; j < S; ++j) {
-          if (!visible(msk, i, j)) continue;
-          const float* kj = kn + idx4(b, j, g, 0, S, Hkv, D);
-          const float* vj = vn + idx4(b, j, g, 0, S, Hkv, D);
-          double pr = exp(scale * dot_f(qi, kj, D) - l);
-          double ds = pr * (dot_f(doi, vj, D) - dl);
-          double* pk = part_k + r * nkv + idx4(b, j, g, 0, S, Hkv, D);
-          double* pv = part_v + r * nkv + idx4(b, j, g, 0, S, Hkv, D);
-          for (int d = 0; d < D; ++d) {
-            dqi[d] += scale * ds * (double)kj[d];
-            pk[d] += scale * ds * (double)qi[d];
-            pv[d] += pr * (double)doi[d];
-          }
+        double pr = exp(scale * dot_f(qi, kj, D) - lse[(b * H + h) * S + i]);
+        double ds = pr * (dot_f(doi, vj, D) - delta[(b * H + h) * S + i]);
+        double* pk = part_k + r * nkv + krow * D;
+        double* pv = part_v + r * nkv + krow * D;
+        for (int d = 0; d < D; ++d) {
+          pk[d] += scale * ds * (double)qi[d];
+          pv[d] += pr * (double)doi[d];
         }
       }
     }
