@@ -80,6 +80,13 @@ def _lib(mutation: int = 0):
     lib.oracle_allgather_fwd.restype = _I
     lib.oracle_allgather_bwd.argtypes = [_f32p] * 4 + ring + docs + [_f64p] * 3
     lib.oracle_allgather_bwd.restype = _I
+    _f32o = np.ctypeslib.ndpointer(dtype=np.float32, flags="C_CONTIGUOUS,WRITEABLE")
+    lib.oracle_ulysses_a2a.argtypes = [_f32p, _L, _L, _I, _I, _I, _I, _I, _I, _f32o]
+    lib.oracle_ulysses_a2a.restype = _I
+    lib.oracle_ulysses_fwd.argtypes = [_f32p, _f32p, _f32p] + ring + docs + [_f64p, _f64p]
+    lib.oracle_ulysses_fwd.restype = _I
+    lib.oracle_ulysses_bwd.argtypes = [_f32p] * 4 + ring + docs + [_f64p] * 3
+    lib.oracle_ulysses_bwd.restype = _I
     _libs[mutation] = lib
     return lib
 
@@ -369,4 +376,57 @@ def allgather_bwd(q_sh, k_sh, v_sh, do_sh, cp, layout, causal=True, scale=None, 
                                              int(causal), scale, cu, nd, dq, dk, dv)
     if rc != 0:
         raise ValueError("bad allgather_bwd arguments")
+    return dq, dk, dv
+
+
+def ulysses_heads(r, cp, H, Hkv):
+    """(first query head, count, first kv head, count) of rank r after the
+    sequence-to-head all-to-all (as the C oracle assigns them)."""
+    hc, grp = H // cp, H // Hkv
+    return r * hc, hc, (r * hc) // grp, (hc // grp if hc >= grp else 1)
+
+
+def ulysses_a2a(x_sh, H, Hkv, cp, layout, kv=False, mutation: int = 0):
+    """Sequence-to-head all-to-all of a sharded [B,S,X,D] tensor: returns
+    [cp, B, S, nx, D], rank r's head slice of every token in natural order."""
+    x = _f32(x_sh)
+    B, S, X, D = x.shape
+    nx = ulysses_heads(0, cp, H, Hkv)[3 if kv else 1]
+    out = np.empty((cp, B, S, nx, D), np.float32)
+    rc = _lib(mutation).oracle_ulysses_a2a(x, B, S, H, Hkv, D, cp, layout, int(kv), out)
+    if rc != 0:
+        raise ValueError("bad ulysses_a2a arguments")
+    return out
+
+
+def ulysses_fwd(q_sh, k_sh, v_sh, cp, layout, causal=True, scale=None, cu_seqlens=None,
+                mutation: int = 0):
+    """Ulysses attention on sharded-order inputs: all-to-all to head owners,
+    full attention per head slice, all-to-all back.  Sharded (out, lse)."""
+    q, k, v = _f32(q_sh), _f32(k_sh), _f32(v_sh)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu_or_one(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    rc = _lib(mutation).oracle_ulysses_fwd(q, k, v, B, H, Hkv, S, D, cp, layout, int(causal),
+                                           scale, cu, nd, out, lse)
+    if rc != 0:
+        raise ValueError("bad ulysses_fwd arguments")
+    return out, lse
+
+
+def ulysses_bwd(q_sh, k_sh, v_sh, do_sh, cp, layout, causal=True, scale=None, cu_seqlens=None,
+                mutation: int = 0):
+    q, k, v, do = _f32(q_sh), _f32(k_sh), _f32(v_sh), _f32(do_sh)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu_or_one(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    dq = np.empty((B, S, H, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    rc = _lib(mutation).oracle_ulysses_bwd(q, k, v, do, B, H, Hkv, S, D, cp, layout, int(causal),
+                                           scale, cu, nd, dq, dk, dv)
+    if rc != 0:
+        raise ValueError("bad ulysses_bwd arguments")
     return dq, dk, dv

@@ -554,6 +554,183 @@ int oracle_allgather_fwd(const float* q_sh, const float* k_sh, const float* v_sh
 }
 
 /* ------------------------------------------------------------------------ */
+/* The Ulysses (all-to-all) variant                                          */
+/* ------------------------------------------------------------------------ */
+
+/* Heads of rank r after the sequence-to-head all-to-all ("Sequence
+ * Parallelism IV", section 7: after the transpose a rank has all tokens for
+ * a head slice).  Query heads: the r-th of cp equal slices, H/cp heads.  KV
+ * heads: those the slice's query heads read (query head h reads kv head
+ * h / (H/Hkv)); when a slice holds fewer query heads than a kv group, one kv
+ * head, shared with the other ranks of the group. */
+static void ulysses_heads(int r, int cp, int H, int Hkv, int* q0, int* nq, int* g0, int* ng) {
+  const int hc = H / cp, grp = H / Hkv;
+  *q0 = r * hc;
+  *nq = hc;
+  *g0 = (r * hc) / grp;
+#if ORACLE_MUTATION == 9
+  *g0 = (((r + 1) % cp) * hc) / grp; /* kv slice of the wrong rank */
+#endif
+  *ng = hc >= grp ? hc / grp : 1;
+}
+
+/* The sequence-to-head all-to-all for one rank: from sharded [B,S,X,D]
+ * (rank s holds sharded rows [s*L, (s+1)*L)) to rank r's [B,S,nx,D] holding
+ * heads x0..x0+nx-1 of every token in natural order. */
+static void a2a_to_rank(const float* sh, float* out, const long* nat_of, long B, long S, int X,
+                        int x0, int nx, int D) {
+  for (long b = 0; b < B; ++b)
+    for (long p = 0; p < S; ++p)
+      memcpy(out + idx4(b, nat_of[p], 0, 0, S, nx, D), sh + idx4(b, p, x0, 0, S, X, D),
+             sizeof(float) * nx * D);
+}
+
+/* The all-to-all itself, as an entry point: out is [cp][B,S,nx,D], rank r's
+ * head slice (query heads when kv = 0, its kv heads when kv = 1). */
+int oracle_ulysses_a2a(const float* sh, long B, long S, int H, int Hkv, int D, int cp, int layout,
+                       int kv, float* out) {
+  if (cp < 1 || H % cp != 0 || H % Hkv != 0) return -1;
+  const int hc = H / cp, grp = H / Hkv;
+  if (hc % grp != 0 && grp % hc != 0) return -1;
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  if (oracle_shard_order(S, cp, layout, nat_of) != 0) {
+    free(nat_of);
+    return -1;
+  }
+  for (int r = 0; r < cp; ++r) {
+    int q0, nq, g0, ng;
+    ulysses_heads(r, cp, H, Hkv, &q0, &nq, &g0, &ng);
+    const int X = kv ? Hkv : H, x0 = kv ? g0 : q0, nx = kv ? ng : nq;
+    a2a_to_rank(sh, out + (long)r * B * S * nx * D, nat_of, B, S, X, x0, nx, D);
+  }
+  free(nat_of);
+  return 0;
+}
+
+/* Ulysses attention ("Sequence Parallelism IV", section 7), sharded order in
+ * and out: the all-to-all gives each rank all tokens of its head slice; each
+ * rank computes full attention (the definition) over the whole sequence for
+ * those heads; the inverse all-to-all returns out and LSE to the sequence
+ * owners. */
+static int ulysses_fwd_m(const float* q_sh, const float* k_sh, const float* v_sh, long B, int H,
+                         int Hkv, long S, int D, int cp, int layout, const Mask* msk,
+                         double scale, double* out_sh, double* lse_sh) {
+  if (cp < 1 || H % cp != 0 || H % Hkv != 0) return -1;
+  const int hc = H / cp, grp = H / Hkv;
+  if (hc % grp != 0 && grp % hc != 0) return -1;
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  if (oracle_shard_order(S, cp, layout, nat_of) != 0) {
+    free(nat_of);
+    return -1;
+  }
+  for (int r = 0; r < cp; ++r) {
+    int q0, nq, g0, ng;
+    ulysses_heads(r, cp, H, Hkv, &q0, &nq, &g0, &ng);
+    float* qr = (float*)malloc(sizeof(float) * B * S * nq * D + 1);
+    float* kr = (float*)malloc(sizeof(float) * B * S * ng * D + 1);
+    float* vr = (float*)malloc(sizeof(float) * B * S * ng * D + 1);
+    double* orr = (double*)malloc(sizeof(double) * B * S * nq * D + 1);
+    double* lr = (double*)malloc(sizeof(double) * B * nq * S + 1);
+    a2a_to_rank(q_sh, qr, nat_of, B, S, H, q0, nq, D);
+    a2a_to_rank(k_sh, kr, nat_of, B, S, Hkv, g0, ng, D);
+    a2a_to_rank(v_sh, vr, nat_of, B, S, Hkv, g0, ng, D);
+    attn_fwd_m(qr, kr, vr, B, nq, ng, S, D, msk, scale, orr, lr);
+    /* Inverse all-to-all: rank r's heads go back to the token owners. */
+    for (long b = 0; b < B; ++b)
+      for (long p = 0; p < S; ++p) {
+        const long n = nat_of[p];
+        memcpy(out_sh + idx4(b, p, q0, 0, S, H, D), orr + idx4(b, n, 0, 0, S, nq, D),
+               sizeof(double) * nq * D);
+        for (int h = 0; h < nq; ++h)
+          lse_sh[(b * H + q0 + h) * S + p] = lr[(b * nq + h) * S + n];
+      }
+    free(qr);
+    free(kr);
+    free(vr);
+    free(orr);
+    free(lr);
+  }
+  free(nat_of);
+  return 0;
+}
+
+int oracle_ulysses_fwd(const float* q_sh, const float* k_sh, const float* v_sh, long B, int H,
+                       int Hkv, long S, int D, int cp, int layout, int causal, double scale,
+                       const long* cu, long ndocs, double* out_sh, double* lse_sh) {
+  const Mask msk = {causal, cu, ndocs};
+  return ulysses_fwd_m(q_sh, k_sh, v_sh, B, H, Hkv, S, D, cp, layout, &msk, scale, out_sh,
+                       lse_sh);
+}
+
+static void attn_bwd_m(const float* q, const float* k, const float* v, const float* dout,
+                       long B, int H, int Hkv, long S, int D, const Mask* msk, double scale,
+                       double* dq, double* dk, double* dv);
+
+/* Ulysses backward, sharded order in and out: dO follows the all-to-all to
+ * the head owners, each rank takes the gradients of full attention for its
+ * heads, and the inverse all-to-all returns dQ, dK, dV to the token owners;
+ * a kv head held by several ranks receives the sum of their dK / dV. */
+static int ulysses_bwd_m(const float* q_sh, const float* k_sh, const float* v_sh,
+                         const float* do_sh, long B, int H, int Hkv, long S, int D, int cp,
+                         int layout, const Mask* msk, double scale, double* dq_sh, double* dk_sh,
+                         double* dv_sh) {
+  if (cp < 1 || H % cp != 0 || H % Hkv != 0) return -1;
+  const int hc = H / cp, grp = H / Hkv;
+  if (hc % grp != 0 && grp % hc != 0) return -1;
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  if (oracle_shard_order(S, cp, layout, nat_of) != 0) {
+    free(nat_of);
+    return -1;
+  }
+  memset(dk_sh, 0, sizeof(double) * B * S * Hkv * D);
+  memset(dv_sh, 0, sizeof(double) * B * S * Hkv * D);
+  for (int r = 0; r < cp; ++r) {
+    int q0, nq, g0, ng;
+    ulysses_heads(r, cp, H, Hkv, &q0, &nq, &g0, &ng);
+    float* qr = (float*)malloc(sizeof(float) * B * S * nq * D + 1);
+    float* dor = (float*)malloc(sizeof(float) * B * S * nq * D + 1);
+    float* kr = (float*)malloc(sizeof(float) * B * S * ng * D + 1);
+    float* vr = (float*)malloc(sizeof(float) * B * S * ng * D + 1);
+    double* dqr = (double*)malloc(sizeof(double) * B * S * nq * D + 1);
+    double* dkr = (double*)malloc(sizeof(double) * B * S * ng * D + 1);
+    double* dvr = (double*)malloc(sizeof(double) * B * S * ng * D + 1);
+    a2a_to_rank(q_sh, qr, nat_of, B, S, H, q0, nq, D);
+    a2a_to_rank(do_sh, dor, nat_of, B, S, H, q0, nq, D);
+    a2a_to_rank(k_sh, kr, nat_of, B, S, Hkv, g0, ng, D);
+    a2a_to_rank(v_sh, vr, nat_of, B, S, Hkv, g0, ng, D);
+    attn_bwd_m(qr, kr, vr, dor, B, nq, ng, S, D, msk, scale, dqr, dkr, dvr);
+    for (long b = 0; b < B; ++b)
+      for (long p = 0; p < S; ++p) {
+        const long n = nat_of[p];
+        memcpy(dq_sh + idx4(b, p, q0, 0, S, H, D), dqr + idx4(b, n, 0, 0, S, nq, D),
+               sizeof(double) * nq * D);
+        for (long x = 0; x < (long)ng * D; ++x) {
+          dk_sh[idx4(b, p, g0, 0, S, Hkv, D) + x] += dkr[idx4(b, n, 0, 0, S, ng, D) + x];
+          dv_sh[idx4(b, p, g0, 0, S, Hkv, D) + x] += dvr[idx4(b, n, 0, 0, S, ng, D) + x];
+        }
+      }
+    free(qr);
+    free(dor);
+    free(kr);
+    free(vr);
+    free(dqr);
+    free(dkr);
+    free(dvr);
+  }
+  free(nat_of);
+  return 0;
+}
+
+int oracle_ulysses_bwd(const float* q_sh, const float* k_sh, const float* v_sh,
+                       const float* do_sh, long B, int H, int Hkv, long S, int D, int cp,
+                       int layout, int causal, double scale, const long* cu, long ndocs,
+                       double* dq_sh, double* dk_sh, double* dv_sh) {
+  const Mask msk = {causal, cu, ndocs};
+  return ulysses_bwd_m(q_sh, k_sh, v_sh, do_sh, B, H, Hkv, S, D, cp, layout, &msk, scale, dq_sh,
+                       dk_sh, dv_sh);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gradients                                                                 */
 /* ------------------------------------------------------------------------ */
 

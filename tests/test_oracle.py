@@ -24,7 +24,12 @@ mutated build of it) disagrees with an independent fact:
   communication patterns: each rank gathers all K/V, then attends in one
   pass; gradients summed over ranks and returned to the owners) equal to
   the definition, forward and backward, for every cp and layout, with and
-  without documents.
+  without documents;
+* the Ulysses variant ("Sequence Parallelism IV", section 7: an all-to-all
+  from sequence to head ownership, after which a rank has all tokens of a
+  head slice): the all-to-all places rank r's head slice of every token in
+  natural order, and the variant equals the definition, forward and
+  backward, also when kv heads are fewer than ranks (shared kv heads).
 
 ``test_mutations_are_caught`` compiles planted mistakes into the oracle and
 checks that some pin fails for each.
@@ -391,11 +396,53 @@ def pin_allgather(m=0):
                     np.testing.assert_allclose(gv, rv[:, order], rtol=0, atol=1e-11)
 
 
+def pin_ulysses_a2a(m=0):
+    B, S, D = 2, 16, 3
+    rng = np.random.default_rng(69)
+    for H, Hkv, cp in ((8, 2, 4), (8, 4, 2), (8, 8, 8), (4, 1, 1), (8, 2, 8)):
+        for layout in (oracle.CONTIGUOUS, oracle.ZIGZAG):
+            order = oracle.shard_order(S, cp, layout, mutation=m)
+            for kv in (False, True):
+                X = Hkv if kv else H
+                x = rng.standard_normal((B, S, X, D)).astype(np.float32)
+                out = oracle.ulysses_a2a(_shard(x, order), H, Hkv, cp, layout, kv, mutation=m)
+                for r in range(cp):
+                    # rank r's query heads are the r-th of cp equal slices; its
+                    # kv heads are those these query heads read
+                    qh = list(range(r * H // cp, (r + 1) * H // cp))
+                    heads = sorted({h * Hkv // H for h in qh}) if kv else qh
+                    np.testing.assert_array_equal(out[r], x[:, :, heads])
+
+
+def pin_ulysses(m=0):
+    B, H, Hkv, S, D = 1, 8, 2, 32, 4
+    q, k, v, do = small(B, H, Hkv, S, D, 70, dout=True)
+    for causal in (True, False):
+        for cu in (None, DOCS_S32):
+            cuo = cu if cu is not None else [0, S]
+            ro, rl = oracle.attn_fwd_docs(q, k, v, cuo, causal=causal, mutation=m)
+            rq, rk, rv = oracle.attn_bwd_docs(q, k, v, do, cuo, causal=causal, mutation=m)
+            for cp in (1, 2, 4, 8):
+                for layout in (oracle.CONTIGUOUS, oracle.ZIGZAG):
+                    order = oracle.shard_order(S, cp, layout, mutation=m)
+                    qs, ks, vs, ds = (_shard(x, order) for x in (q, k, v, do))
+                    o, l = oracle.ulysses_fwd(qs, ks, vs, cp, layout, causal, cu_seqlens=cu,
+                                              mutation=m)
+                    np.testing.assert_allclose(o, ro[:, order], rtol=0, atol=1e-12)
+                    np.testing.assert_allclose(l, rl[:, :, order], rtol=0, atol=1e-12)
+                    gq, gk, gv = oracle.ulysses_bwd(qs, ks, vs, ds, cp, layout, causal,
+                                                    cu_seqlens=cu, mutation=m)
+                    np.testing.assert_allclose(gq, rq[:, order], rtol=0, atol=1e-11)
+                    np.testing.assert_allclose(gk, rk[:, order], rtol=0, atol=1e-11)
+                    np.testing.assert_allclose(gv, rv[:, order], rtol=0, atol=1e-11)
+
+
 PINS = [pin_zigzag_golden, pin_contiguous_golden, pin_coverage, pin_brute_force,
         pin_constant_v, pin_q_zero, pin_row0, pin_ring_invariance, pin_step_partials_merge,
         pin_finite_differences, pin_sum_rules, pin_tile_counts, pin_docs_brute_force,
         pin_docs_finite_differences, pin_docs_one_token_each, pin_docs_packed_equals_separate,
-        pin_docs_single_and_ring, pin_docs_tile_counts, pin_allgather]
+        pin_docs_single_and_ring, pin_docs_tile_counts, pin_allgather, pin_ulysses_a2a,
+        pin_ulysses]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -472,7 +519,8 @@ def test_bad_arguments_rejected():
 MUTATIONS = {1: "wrong zigzag pairing", 2: "interleaved GQA head map",
              3: "causal diagonal dropped", 4: "softmax scale dropped",
              5: "merge term dropped", 6: "ring turned the other way",
-             7: "document border off by one", 8: "all-gather reduce drops a rank"}
+             7: "document border off by one", 8: "all-gather reduce drops a rank",
+             9: "Ulysses kv heads of the wrong rank"}
 
 
 @pytest.mark.parametrize("m", sorted(MUTATIONS), ids=[MUTATIONS[m] for m in sorted(MUTATIONS)])
