@@ -17,7 +17,10 @@ packed documents, the sum over documents).  Inputs are far larger than L2
 (129 MB), so no flush is needed between steps.
 
 The same run times the packed-document workload (S=131072, documents of mean
-length 8192) forward and backward and reports it under "docs";
+length 8192) forward and backward and reports it under "docs", and the
+S=131072 workload through the all-gather K/V schedule (K/V gathered into
+natural order, one pass per rank, gathered dK/dV returned to their owners)
+under "allgather";
 ``--workload docs_bf16_s131072_fwdbwd`` makes it the main line (its step adds
 the document-bounds kernel and uses the document-rule forward/backward).
 
@@ -335,6 +338,10 @@ def run_ours(args):
         wd = inputs.DOC_WORKLOADS["docs_bf16_s131072_fwdbwd"]
         docs_info = time_docs(cpa, wd, dev, stream, args.warmup, max(args.steps, 5), peak)
         docs_info["traffic"] = CAPTURED_TRAFFIC.get(wd.name)
+    ag_info = None
+    if docs is None and not args.no_allgather and w.backward:
+        ag_info = time_allgather(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
+                                 (qs, ks, vs, dos))
 
     path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype)
     cpu = None
@@ -356,6 +363,7 @@ def run_ours(args):
                    "useful_tflop_per_step": step_flops / 1e12},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
         "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "docs": docs_info,
+        "allgather": ag_info,
         "cpu_baseline": cpu,
         "status": cpa.device_status(),
     }
@@ -441,6 +449,54 @@ def time_docs(cpa, w, dev, stream, warmup, steps, peak):
             "useful_pairs_vs_one_document": w.valid_pairs_per_head() / full,
             "forward": res["fwd"], "backward": res["bwd"], "grad_dtype": "f32",
             "status": cpa.device_status()}
+
+
+def time_allgather(cpa, w, dev, stream, warmup, steps, peak, sharded):
+    """The all-gather schedule on sharded inputs: gather K/V (natural order),
+    forward, backward, reduce-scatter dK/dV to sharded order; each part timed
+    with CUDA events (median of `steps`)."""
+    qs, ks, vs, dos = sharded
+    kf, vf = torch.empty_like(ks), torch.empty_like(vs)
+    o = torch.empty_like(qs)
+    lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    g = [torch.empty(x.shape, device=dev, dtype=torch.float32) for x in (qs, ks, vs)]
+    gs = [torch.empty_like(g[1]), torch.empty_like(g[2])]
+    wsp = torch.empty(cpa.ring_bwd_workspace_bytes(w.B, w.H, w.Hkv, w.S, w.D,
+                                                   cpa.BF16 | cpa.GRAD_F32),
+                      device=dev, dtype=torch.uint8)
+    parts = {
+        "gather": lambda: cpa.kv_allgather(ks, vs, w.cp, w.layout, k_full=kf, v_full=vf),
+        "fwd": lambda: cpa.allgather_fwd(qs, kf, vf, w.cp, w.layout, w.causal, out=o, lse=lse),
+        "bwd": lambda: cpa.allgather_bwd(qs, kf, vf, o, dos, lse, w.cp, w.layout, w.causal,
+                                         dq=g[0], dk_full=g[1], dv_full=g[2], workspace=wsp,
+                                         grad_dtype=torch.float32),
+        "scatter": lambda: (cpa.zigzag_permute(g[1], w.cp, w.layout, out=gs[0]),
+                            cpa.zigzag_permute(g[2], w.cp, w.layout, out=gs[1])),
+    }
+    res = {}
+    for name, fn in parts.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+    fwd_tf = w.useful_flops(False) / (res["fwd"] * 1e-3) / 1e12
+    bwd_tf = w.useful_flops(True) / (res["bwd"] * 1e-3) / 1e12
+    total = sum(res.values())
+    return {"workload": w.name, "schedule": "all-gather K/V", "ms": res,
+            "forward": {"tflops": fwd_tf, "frac": fwd_tf / peak},
+            "backward": {"tflops": bwd_tf, "frac": bwd_tf / peak},
+            "fwd_bwd_with_gather_scatter_tflops":
+                (w.useful_flops(False) + w.useful_flops(True)) / (total * 1e-3) / 1e12,
+            "grad_dtype": "f32", "status": cpa.device_status()}
 
 
 # ---------------------------------------------------------------------------
@@ -564,6 +620,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-c3", action="store_true")
     ap.add_argument("--no-docs", action="store_true")
+    ap.add_argument("--no-allgather", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
