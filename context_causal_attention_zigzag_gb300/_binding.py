@@ -42,6 +42,11 @@ SIGNATURES = {
     "cpattn_padded_length": (_i64, [_i64, _i, _i]),
     "cpattn_allgather_fwd": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _vp]),
     "cpattn_allgather_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
+    "cpattn_ulysses_a2a": (_i, [_vp, _vp] + [_i] * 10 + [_vp]),
+    "cpattn_ulysses_lse_a2a": (_i, [_vp, _vp] + [_i] * 6 + [_vp]),
+    "cpattn_ulysses_workspace_bytes": (_sz, [_i] * 9),
+    "cpattn_ulysses_fwd": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
+    "cpattn_ulysses_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_ring_fwd": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp]),
     "cpattn_ring_fwd_census": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp, _vp]),
     "cpattn_ring_fwd_plan": (_i, [_i] * 9 + [_ip, _ip]),
@@ -497,6 +502,83 @@ def allgather_bwd(q, k_full, v_full, out, dout, lse, cp, layout=ZIGZAG, causal=T
 
 
 # ---------------------------------------------------------------------------
+# Ulysses (all-to-all to head ownership)
+# ---------------------------------------------------------------------------
+
+def ulysses_heads(H, Hkv, cp):
+    """(query heads, kv heads) per rank after the sequence-to-head all-to-all."""
+    hc, grp = H // cp, H // Hkv
+    return hc, (hc // grp if hc >= grp else 1)
+
+
+def ulysses_a2a(x, cp, H, Hkv, layout=ZIGZAG, kv_heads=False, to_seq=False, out=None):
+    """One Ulysses all-to-all (cpattn_ulysses_a2a).  Sequence -> head: x
+    [B,S,X,D] sharded -> [cp, B, S, nx, D]; head -> sequence: the inverse
+    (shared kv heads summed)."""
+    _need_cuda(x)
+    hc, nkv = ulysses_heads(H, Hkv, cp)
+    nx = nkv if kv_heads else hc
+    if to_seq:
+        _, B, S, _, D = x.shape
+        shape = (B, S, Hkv if kv_heads else H, D)
+    else:
+        B, S, _, D = x.shape
+        shape = (cp, B, S, nx, D)
+    if out is None:
+        out = torch.empty(shape, device=x.device, dtype=x.dtype)
+    _need_cuda(out)
+    rc = lib().cpattn_ulysses_a2a(_ptr(x), _ptr(out), B, S, H, Hkv, D, int(cp), int(layout),
+                                  int(bool(kv_heads)), int(bool(to_seq)), _dtype_code(x),
+                                  _stream(x))
+    _check("cpattn_ulysses_a2a", rc)
+    return out
+
+
+def ulysses_workspace_bytes(B, H, Hkv, S, D, cp, layout=ZIGZAG, dtype=BF16, backward=False):
+    return int(lib().cpattn_ulysses_workspace_bytes(B, H, Hkv, S, D, int(cp), int(layout),
+                                                    int(dtype), int(bool(backward))))
+
+
+def ulysses_fwd(q, k, v, cp, layout=ZIGZAG, causal=True, scale=None, bounds=None, out=None,
+                lse=None, workspace=None):
+    """The Ulysses variant on sharded-order tensors; returns (out, lse)."""
+    _need_cuda(q, k, v, bounds)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    need = ulysses_workspace_bytes(B, H, Hkv, S, D, cp, layout, _dtype_code(q), False)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(out, lse, workspace)
+    rc = lib().cpattn_ulysses_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S,
+                                  D, int(cp), int(layout), int(bool(causal)), _dtype_code(q),
+                                  _scale(scale), _ptr(bounds), _ptr(workspace), workspace.numel(),
+                                  _stream(q))
+    _check("cpattn_ulysses_fwd", rc)
+    return out, lse
+
+
+def ulysses_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None, bounds=None,
+                dq=None, dk=None, dv=None, workspace=None, grad_dtype=None):
+    """Backward of the Ulysses variant on sharded-order tensors."""
+    _need_cuda(q, k, v, out, dout, lse, bounds)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
+    need = ulysses_workspace_bytes(B, H, Hkv, S, D, cp, layout, code, True)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(dq, dk, dv, workspace)
+    rc = lib().cpattn_ulysses_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
+                                  int(layout), int(bool(causal)), code, _scale(scale),
+                                  _ptr(bounds), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("cpattn_ulysses_bwd", rc)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
 # census and status
 # ---------------------------------------------------------------------------
 
@@ -589,3 +671,16 @@ def attention_allgather_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, s
     dks, dvs = zigzag_permute(dkf, cp, layout), zigzag_permute(dvf, cp, layout)
     un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
     return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dks), un(dvs)
+
+
+def attention_ulysses_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None,
+                              grad_dtype=None):
+    """Natural order in and out through the Ulysses variant: shard, all-to-all
+    to head owners, attend, backward, all-to-all back, unshard.  Returns
+    (out, lse, dq, dk, dv) in natural order."""
+    qs, ks, vs, dos = (zigzag_permute(x, cp, layout) for x in (q, k, v, dout))
+    o, lse = ulysses_fwd(qs, ks, vs, cp, layout, causal, scale)
+    dq, dk, dv = ulysses_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, scale,
+                             grad_dtype=grad_dtype)
+    un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
+    return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dk), un(dv)

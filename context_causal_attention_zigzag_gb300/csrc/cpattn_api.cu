@@ -367,9 +367,208 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
+// Ulysses: the sharded sequence layout, heads per rank and kv heads per rank.
+int ulysses_shape(int B, int H, int Hkv, int S, int D, int cp, int layout, int* hc, int* nkv,
+                  RingShape* sh) {
+  int rc = make_shape(B, H, Hkv, S, D, cp, layout, 1, 0.f, sh);
+  if (rc != CPATTN_OK) return rc;
+  if (H % cp != 0) return CPATTN_ERR_INVALID_ARG;
+  const int h = H / cp, grp = H / Hkv;
+  if (h % grp != 0 && grp % h != 0) return CPATTN_ERR_INVALID_ARG;
+  *hc = h;
+  *nkv = h >= grp ? h / grp : 1;
+  return CPATTN_OK;
+}
+
+A2aShape a2a_shape(const RingShape& sh, int B, int H, int Hkv, int hc, int nkv, bool kv) {
+  A2aShape a;
+  a.sh = sh;
+  a.B = B;
+  a.D = sh.D;
+  a.X = kv ? Hkv : H;
+  a.nx = kv ? nkv : hc;
+  a.x_num = hc;
+  a.x_den = kv ? H / Hkv : 1;
+  return a;
+}
+
+struct UlyssesWs {
+  size_t q, kv, lse, grad_q, grad_kv, inner, total;
+};
+
+UlyssesWs ulysses_ws(int B, int H, int Hkv, int S, int D, int dtype, bool backward, int cp,
+                     int hc, int nkv) {
+  UlyssesWs w;
+  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  const size_t elt = in_dtype == CPATTN_BF16 ? 2 : 4;
+  const size_t gelt = (dtype & CPATTN_GRAD_F32) ? 4 : elt;
+  const size_t rows = (size_t)cp * B * S;
+  w.q = align256(rows * hc * D * elt);
+  w.kv = align256(rows * nkv * D * elt);
+  w.lse = align256((size_t)B * H * S * sizeof(float));
+  w.grad_q = backward ? align256(rows * hc * D * gelt) : 0;
+  w.grad_kv = backward ? align256(rows * nkv * D * gelt) : 0;
+  w.inner = backward ? align256(cpattn_ring_bwd_workspace_bytes(cp * B, hc, nkv, S, D, dtype))
+                     : 0;
+  // q-like: q, o (+ dO, dQ); kv-like: k, v (+ dK, dV)
+  w.total = (backward ? 3 : 2) * w.q + 2 * w.kv + w.lse + w.grad_q + 2 * w.grad_kv + w.inner;
+  return w;
+}
+
 }  // namespace
 
 extern "C" {
+
+int cpattn_ulysses_a2a(const void* in, void* out, int B, int S, int H, int Hkv, int D,
+                       int cp_size, int layout, int kv_heads, int to_seq, int dtype,
+                       cpattn_stream_t stream) {
+  RingShape sh;
+  int hc = 0, nkv = 0;
+  int rc = ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh);
+  if (rc != CPATTN_OK) return rc;
+  if ((dtype != CPATTN_F32 && dtype != CPATTN_BF16) || (kv_heads != 0 && kv_heads != 1) ||
+      (to_seq != 0 && to_seq != 1))
+    return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S == 0) return CPATTN_OK;
+  if (!in || !out || !aligned16(in) || !aligned16(out)) return CPATTN_ERR_INVALID_ARG;
+  const A2aShape a = a2a_shape(sh, B, H, Hkv, hc, nkv, kv_heads != 0);
+  const size_t elt = dtype == CPATTN_BF16 ? 2 : 4;
+  const size_t big = (size_t)cp_size * B * S * a.nx * D * elt;
+  const size_t small = (size_t)B * S * a.X * D * elt;
+  const char* x = static_cast<const char*>(in);
+  const char* y = static_cast<const char*>(out);
+  const size_t in_b = to_seq ? big : small, out_b = to_seq ? small : big;
+  if (x < y + out_b && y < x + in_b) return CPATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_a2a(in, out, a, to_seq != 0, dtype, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+int cpattn_ulysses_lse_a2a(const float* in, float* out, int B, int S, int H, int cp_size,
+                           int layout, int to_seq, cpattn_stream_t stream) {
+  RingShape sh;
+  int hc = 0, nkv = 0;
+  int rc = ulysses_shape(B, H, H, S, 64, cp_size, layout, &hc, &nkv, &sh);
+  if (rc != CPATTN_OK) return rc;
+  if (to_seq != 0 && to_seq != 1) return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S == 0) return CPATTN_OK;
+  if (!in || !out) return CPATTN_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)B * H * S * sizeof(float);
+  const char* x = reinterpret_cast<const char*>(in);
+  const char* y = reinterpret_cast<const char*>(out);
+  if (x < y + bytes && y < x + bytes) return CPATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_lse_a2a(in, out, sh, B, H, to_seq != 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
+size_t cpattn_ulysses_workspace_bytes(int B, int H, int Hkv, int S, int D, int cp_size,
+                                      int layout, int dtype, int backward) {
+  RingShape sh;
+  int hc = 0, nkv = 0;
+  if (ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh) != CPATTN_OK) return 0;
+  return ulysses_ws(B, H, Hkv, S, D, dtype, backward != 0, cp_size, hc, nkv).total;
+}
+
+int cpattn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int B, int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
+                       int dtype, float softmax_scale, const int32_t* doc_bounds,
+                       void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
+  RingShape sh;
+  int hc = 0, nkv = 0;
+  int rc = ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh);
+  if (rc != CPATTN_OK) return rc;
+  if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S == 0) return CPATTN_OK;
+  if (!q || !k || !v || !out || !lse) return CPATTN_ERR_INVALID_ARG;
+  const int2* docs = nullptr;
+  if (!doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
+  const UlyssesWs w = ulysses_ws(B, H, Hkv, S, D, dtype, false, cp_size, hc, nkv);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return CPATTN_ERR_WORKSPACE;
+  char* p = static_cast<char*>(workspace);
+  void* wq = p;
+  void* wo = p + w.q;
+  void* wk = p + 2 * w.q;
+  void* wv = p + 2 * w.q + w.kv;
+  float* wl = reinterpret_cast<float*>(p + 2 * w.q + 2 * w.kv);
+  cudaStream_t st = (cudaStream_t)stream;
+  // All-to-all: sequence owners -> head owners.
+  rc = cpattn_ulysses_a2a(q, wq, B, S, H, Hkv, D, cp_size, layout, 0, 0, dtype, stream);
+  if (rc == CPATTN_OK)
+    rc = cpattn_ulysses_a2a(k, wk, B, S, H, Hkv, D, cp_size, layout, 1, 0, dtype, stream);
+  if (rc == CPATTN_OK)
+    rc = cpattn_ulysses_a2a(v, wv, B, S, H, Hkv, D, cp_size, layout, 1, 0, dtype, stream);
+  if (rc != CPATTN_OK) return rc;
+  // Each rank: full attention over the whole sequence for its heads (the
+  // ranks stacked along the batch axis, one launch).
+  rc = fwd_common(wq, wk, wv, wo, wl, cp_size * B, hc, nkv, S, D, 1, CPATTN_LAYOUT_CONTIGUOUS,
+                  causal, dtype, softmax_scale, 0, 1, 0, nullptr, docs, 0, st);
+  if (rc != CPATTN_OK) return rc;
+  // Back to the sequence owners.
+  rc = cpattn_ulysses_a2a(wo, out, B, S, H, Hkv, D, cp_size, layout, 0, 1, dtype, stream);
+  if (rc != CPATTN_OK) return rc;
+  return cpattn_ulysses_lse_a2a(wl, lse, B, S, H, cp_size, layout, 1, stream);
+}
+
+int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
+                       int dtype, float softmax_scale, const int32_t* doc_bounds,
+                       void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
+  RingShape sh;
+  int hc = 0, nkv = 0;
+  int rc = ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh);
+  if (rc != CPATTN_OK) return rc;
+  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
+  const int out_dtype = (dtype & CPATTN_GRAD_F32) ? CPATTN_F32 : in_dtype;
+  if (causal != 0 && causal != 1) return CPATTN_ERR_INVALID_ARG;
+  if ((long long)B * S == 0) return CPATTN_OK;
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return CPATTN_ERR_INVALID_ARG;
+  const int2* docs = nullptr;
+  if (!doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
+  const UlyssesWs w = ulysses_ws(B, H, Hkv, S, D, dtype, true, cp_size, hc, nkv);
+  if (workspace == nullptr || workspace_bytes < w.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
+    return CPATTN_ERR_WORKSPACE;
+  char* p = static_cast<char*>(workspace);
+  void* wq = p;
+  void* wo = p + w.q;
+  void* wdo = p + 2 * w.q;
+  void* wk = p + 3 * w.q;
+  void* wv = p + 3 * w.q + w.kv;
+  float* wl = reinterpret_cast<float*>(p + 3 * w.q + 2 * w.kv);
+  char* g = p + 3 * w.q + 2 * w.kv + w.lse;
+  void* wdq = g;
+  void* wdk = g + w.grad_q;
+  void* wdv = g + w.grad_q + w.grad_kv;
+  void* inner = g + w.grad_q + 2 * w.grad_kv;
+  cudaStream_t st = (cudaStream_t)stream;
+  const void* src_q[3] = {q, out, dout};
+  void* dst_q[3] = {wq, wo, wdo};
+  for (int i = 0; i < 3 && rc == CPATTN_OK; ++i)
+    rc = cpattn_ulysses_a2a(src_q[i], dst_q[i], B, S, H, Hkv, D, cp_size, layout, 0, 0, in_dtype,
+                            stream);
+  if (rc == CPATTN_OK)
+    rc = cpattn_ulysses_a2a(k, wk, B, S, H, Hkv, D, cp_size, layout, 1, 0, in_dtype, stream);
+  if (rc == CPATTN_OK)
+    rc = cpattn_ulysses_a2a(v, wv, B, S, H, Hkv, D, cp_size, layout, 1, 0, in_dtype, stream);
+  if (rc == CPATTN_OK) rc = cpattn_ulysses_lse_a2a(lse, wl, B, S, H, cp_size, layout, 0, stream);
+  if (rc != CPATTN_OK) return rc;
+  rc = bwd_common(wq, wk, wv, wo, wdo, wl, wdq, wdk, wdv, cp_size * B, hc, nkv, S, D, 1,
+                  CPATTN_LAYOUT_CONTIGUOUS, causal, dtype, softmax_scale, docs, 0, inner,
+                  w.inner, st);
+  if (rc != CPATTN_OK) return rc;
+  // Back to the sequence owners; a kv head held by several ranks gets the
+  // sum of their dK / dV.
+  rc = cpattn_ulysses_a2a(wdq, dq, B, S, H, Hkv, D, cp_size, layout, 0, 1, out_dtype, stream);
+  if (rc == CPATTN_OK)
+    rc = cpattn_ulysses_a2a(wdk, dk, B, S, H, Hkv, D, cp_size, layout, 1, 1, out_dtype, stream);
+  if (rc == CPATTN_OK)
+    rc = cpattn_ulysses_a2a(wdv, dv, B, S, H, Hkv, D, cp_size, layout, 1, 1, out_dtype, stream);
+  return rc;
+}
 
 int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,
                     const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,

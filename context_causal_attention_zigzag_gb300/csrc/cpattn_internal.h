@@ -39,6 +39,13 @@ __host__ __device__ inline int chunk_owner(const RingShape& s, int kc) {
 __host__ __device__ inline int chunk_slot(const RingShape& s, int kc) {
   return (s.per_rank == 1 || kc < s.cp) ? 0 : 1;
 }
+// Sharded position of natural position n (inverse of natural_pos).
+__host__ __device__ inline int sharded_pos(const RingShape& s, int n) {
+  if (s.per_rank == 1) return n;
+  const int kc = n / s.c, off = n - kc * s.c;
+  return chunk_owner(s, kc) * s.L + chunk_slot(s, kc) * s.c + off;
+}
+
 // Ring step at which rank r holds the K/V of rank src.
 __host__ __device__ inline int ring_step_of(int r, int src, int cp) {
   int t = (r - src) % cp;
@@ -143,6 +150,22 @@ struct BwdArgs {
 };
 
 // Kernel launchers; each returns the launch error (cudaSuccess if queued).
+// Ulysses all-to-all ("Sequence Parallelism IV", section 7).  A tensor
+// [B, S, X, D] in sharded order (rank r owns sharded rows [r*L, (r+1)*L))
+// <-> [cp][B, S, nx, D] in natural order, rank r holding heads
+// x0(r) .. x0(r)+nx-1 with x0(r) = (r * x_num) / x_den.  Seq -> head copies;
+// head -> seq sums the ranks that hold a head (kv heads shared by ranks).
+// dtype: CPATTN_F32 / CPATTN_BF16 (the element type; sums in float32).
+struct A2aShape {
+  RingShape sh;  // only cp, per_rank, S, L, c are used
+  int B, X, nx, x_num, x_den, D;
+};
+cudaError_t launch_a2a(const void* in, void* out, const A2aShape& a, bool to_seq, int dtype,
+                       cudaStream_t stream);
+// LSE [B, H, S] sharded <-> [cp][B, H/cp, S] natural (query heads only).
+cudaError_t launch_lse_a2a(const float* in, float* out, const RingShape& sh, int B, int H,
+                           bool to_seq, cudaStream_t stream);
+
 // docs[p] for every natural position p from document offsets cu[0..ndocs]
 // (cu[0] = 0, strictly increasing, cu[ndocs] = S).  Offsets that break those
 // rules set the device error word to kErrBadDocs; every entry is still

@@ -1,7 +1,8 @@
 // Bandwidth-bound kernels of the ring: zigzag permute / unpermute, the exact
 // LSE merge of two partials, the backward pre-pass (Delta = dO . O and zeroing
 // of the gradient accumulators) and the float32 -> output dtype conversion of
-// dQ, dK, dV; and the per-position document bounds of a packed sequence.
+// dQ, dK, dV; the per-position document bounds of a packed sequence; and the
+// all-to-all transposes of the Ulysses variant.
 //
 // All of them move data in 16-byte vectors with consecutive threads on
 // consecutive vectors, and size their grids as a multiple of the SM count.
@@ -327,7 +328,140 @@ __global__ void __launch_bounds__(256) doc_bounds_kernel(const int* __restrict__
   }
 }
 
+// ---------------------------------------------------------------------------
+// Ulysses all-to-all.  Sequence -> head: each (rank r, b, natural n) row of
+// the output is nx*D contiguous elements read from one sharded row of the
+// input, so the copy moves 16-byte vectors of those runs.  Head -> sequence:
+// each (b, sharded p, head x) row of D elements sums the ranks holding x.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int a2a_x0(const A2aShape& a, int r) {
+  return (int)(((long long)r * a.x_num) / a.x_den);
+}
+
+template <typename V>
+__global__ void __launch_bounds__(256) a2a_to_head_kernel(const char* __restrict__ in,
+                                                          char* __restrict__ out,
+                                                          const A2aShape a, int elt) {
+  const int64_t row_vecs = (int64_t)a.nx * a.D * elt / (int64_t)sizeof(V);
+  const int64_t total = (int64_t)a.sh.cp * a.B * a.sh.S * row_vecs;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t row = i / row_vecs, e = i - row * row_vecs;
+    const int n = (int)(row % a.sh.S);
+    const int64_t rb = row / a.sh.S;
+    const int b = (int)(rb % a.B), r = (int)(rb / a.B);
+    const int p = sharded_pos(a.sh, n);
+    const int64_t src = ((((int64_t)b * a.sh.S + p) * a.X + a2a_x0(a, r)) * a.D) * elt +
+                        e * (int64_t)sizeof(V);
+    reinterpret_cast<V*>(out)[i] = *reinterpret_cast<const V*>(in + src);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float a2a_ld(const T* p);
+template <>
+__device__ __forceinline__ float a2a_ld<float>(const float* p) { return *p; }
+template <>
+__device__ __forceinline__ float a2a_ld<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+template <typename T>
+__device__ __forceinline__ void a2a_st(T* p, float x);
+template <>
+__device__ __forceinline__ void a2a_st<float>(float* p, float x) { *p = x; }
+template <>
+__device__ __forceinline__ void a2a_st<__nv_bfloat16>(__nv_bfloat16* p, float x) {
+  *p = __float2bfloat16_rn(x);
+}
+
+// One thread per 4 elements of an output row (D is a multiple of 4).
+template <typename T>
+__global__ void __launch_bounds__(256) a2a_to_seq_kernel(const T* __restrict__ in,
+                                                         T* __restrict__ out, const A2aShape a) {
+  const int q4 = a.D / 4;
+  const int64_t total = (int64_t)a.B * a.sh.S * a.X * q4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int d = (int)(i % q4) * 4;
+    const int64_t row = i / q4;  // (b, p, x)
+    const int x = (int)(row % a.X);
+    const int64_t bp = row / a.X;
+    const int p = (int)(bp % a.sh.S), b = (int)(bp / a.sh.S);
+    const int n = natural_pos(a.sh, p);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = 0; r < a.sh.cp; ++r) {
+      const int x0 = a2a_x0(a, r);
+      if (x < x0 || x >= x0 + a.nx) continue;
+      const T* src = in + ((((int64_t)r * a.B + b) * a.sh.S + n) * a.nx + (x - x0)) * a.D + d;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[u] += a2a_ld<T>(src + u);
+    }
+    T* dst = out + row * a.D + d;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a2a_st<T>(dst + u, acc[u]);
+  }
+}
+
+// LSE: out[r, b, h', n] = in[b, r*hc + h', p(n)] (to heads) and back.
+__global__ void __launch_bounds__(256) lse_a2a_kernel(const float* __restrict__ in,
+                                                      float* __restrict__ out,
+                                                      const RingShape sh, int B, int H,
+                                                      bool to_seq) {
+  const int hc = H / sh.cp;
+  const int64_t total = (int64_t)B * H * sh.S;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    // i indexes the sharded [B, H, S] tensor: (b, h, p)
+    const int p = (int)(i % sh.S);
+    const int64_t bh = i / sh.S;
+    const int h = (int)(bh % H), b = (int)(bh / H);
+    const int r = h / hc, hh = h - r * hc;
+    const int64_t j = (((int64_t)r * B + b) * hc + hh) * sh.S + natural_pos(sh, p);
+    if (to_seq)
+      out[i] = in[j];
+    else
+      out[j] = in[i];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_a2a(const void* in, void* out, const A2aShape& a, bool to_seq, int dtype,
+                       cudaStream_t stream) {
+  const int elt = dtype == 1 ? 2 : 4;
+  const int64_t rows = (int64_t)a.sh.cp * a.B * a.sh.S;
+  if (rows == 0 || a.nx == 0) return cudaSuccess;
+  if (!to_seq) {
+    const int64_t row_bytes = (int64_t)a.nx * a.D * elt;
+    const uint64_t align = (uint64_t)(reinterpret_cast<uintptr_t>(in) |
+                                      reinterpret_cast<uintptr_t>(out)) |
+                           (uint64_t)row_bytes | (uint64_t)((int64_t)a.X * a.D * elt);
+    if ((align & 15) == 0) {
+      a2a_to_head_kernel<uint4><<<grid_for(rows * row_bytes / 16, 256, 8), 256, 0, stream>>>(
+          static_cast<const char*>(in), static_cast<char*>(out), a, elt);
+    } else {
+      a2a_to_head_kernel<uint32_t><<<grid_for(rows * row_bytes / 4, 256, 8), 256, 0, stream>>>(
+          static_cast<const char*>(in), static_cast<char*>(out), a, elt);
+    }
+    return cudaGetLastError();
+  }
+  const int64_t n = (int64_t)a.B * a.sh.S * a.X * (a.D / 4);
+  if (dtype == 1)
+    a2a_to_seq_kernel<__nv_bfloat16><<<grid_for(n, 256, 8), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(in), static_cast<__nv_bfloat16*>(out), a);
+  else
+    a2a_to_seq_kernel<float><<<grid_for(n, 256, 8), 256, 0, stream>>>(
+        static_cast<const float*>(in), static_cast<float*>(out), a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_a2a(const float* in, float* out, const RingShape& sh, int B, int H,
+                           bool to_seq, cudaStream_t stream) {
+  const int64_t n = (int64_t)B * H * sh.S;
+  if (n == 0) return cudaSuccess;
+  lse_a2a_kernel<<<grid_for(n, 256, 8), 256, 0, stream>>>(in, out, sh, B, H, to_seq);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_doc_bounds(const int* cu, int ndocs, int S, int2* docs, int* err,
                               cudaStream_t stream) {

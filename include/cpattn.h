@@ -318,6 +318,56 @@ CPATTN_API int cpattn_allgather_bwd(const void* q, const void* k_full, const voi
                                     cpattn_stream_t stream);
 
 /*
+ * The Ulysses variant ("Sequence Parallelism IV", section 7): an all-to-all
+ * moves sequence ownership to head ownership, so that rank r holds ALL
+ * tokens of a head slice and computes full attention for it; the inverse
+ * all-to-all returns the results to the token owners.  Rank r's query heads
+ * are the r-th of cp_size equal slices (H % cp_size == 0); its kv heads are
+ * the ones those query heads read, h / (H / Hkv): whole kv groups when a
+ * slice holds them, else one kv head shared with the other ranks of its
+ * group (so H/cp_size and H/Hkv must divide one another).  No zigzag is
+ * needed for balance (every rank does the same work); `layout` only says how
+ * the sequence is sharded in the inputs and outputs.
+ *
+ * cpattn_ulysses_a2a: one all-to-all on one GPU.
+ *   to_seq = 0 (sequence -> head): in [B,S,X,D] sharded order ->
+ *     out [cp][B,S,nx,D], rank r's heads of every token in natural order;
+ *   to_seq = 1 (head -> sequence): the inverse; a kv head held by several
+ *     ranks receives the sum of their rows (the gradient reduction).
+ *   kv_heads = 0: query-head tensors (X = H, nx = H/cp_size); 1: kv-head
+ *   tensors (X = Hkv, nx = kv heads per rank).  dtype CPATTN_F32 or
+ *   CPATTN_BF16 (the element type).  16-byte aligned, non-overlapping.
+ * cpattn_ulysses_lse_a2a: the same for LSE, [B,H,S] sharded <->
+ *   [cp][B,H/cp,S] natural (float32).
+ * cpattn_ulysses_fwd / _bwd: the whole variant on sharded-order tensors
+ *   (shapes, dtypes and outputs as cpattn_ring_fwd / cpattn_ring_bwd):
+ *   all-to-all of the inputs into the workspace, attention for every rank
+ *   in one launch (ranks stacked along the batch), all-to-all back.
+ *   doc_bounds: NULL or from cpattn_doc_bounds.  workspace: device, at least
+ *   cpattn_ulysses_workspace_bytes(..., backward), 256-byte aligned, scratch.
+ */
+CPATTN_API int cpattn_ulysses_a2a(const void* in, void* out, int B, int S, int H, int Hkv, int D,
+                                  int cp_size, int layout, int kv_heads, int to_seq, int dtype,
+                                  cpattn_stream_t stream);
+CPATTN_API int cpattn_ulysses_lse_a2a(const float* in, float* out, int B, int S, int H,
+                                      int cp_size, int layout, int to_seq,
+                                      cpattn_stream_t stream);
+CPATTN_API size_t cpattn_ulysses_workspace_bytes(int B, int H, int Hkv, int S, int D,
+                                                 int cp_size, int layout, int dtype,
+                                                 int backward);
+CPATTN_API int cpattn_ulysses_fwd(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int H, int Hkv, int S, int D, int cp_size,
+                                  int layout, int causal, int dtype, float softmax_scale,
+                                  const int32_t* doc_bounds, void* workspace,
+                                  size_t workspace_bytes, cpattn_stream_t stream);
+CPATTN_API int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, const void* out,
+                                  const void* dout, const float* lse, void* dq, void* dk,
+                                  void* dv, int B, int H, int Hkv, int S, int D, int cp_size,
+                                  int layout, int causal, int dtype, float softmax_scale,
+                                  const int32_t* doc_bounds, void* workspace,
+                                  size_t workspace_bytes, cpattn_stream_t stream);
+
+/*
  * Sequence length to pad a sequence of S tokens to (host only): the smallest
  * multiple of cp_size * 256 (contiguous) or 2 * cp_size * 256 (zigzag) that
  * is >= S, so that every chunk is a whole number of 256-token query pairs

@@ -31,6 +31,24 @@ def test_library_loads_and_exports_every_declared_symbol():
     assert set(_binding.SIGNATURES) == set(names)
 
 
+def declared_parameter_counts():
+    """name -> number of parameters, read from the CPATTN_API declarations."""
+    text = open(HEADER).read()
+    out = {}
+    for m in re.finditer(r"CPATTN_API\s+[\w\s\*]*?\b(cpattn_\w+)\s*\(([^;]*?)\)\s*;", text,
+                         re.S):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_ctypes_signatures_match_header_parameter_counts():
+    counts = declared_parameter_counts()
+    assert set(counts) == set(_binding.SIGNATURES)
+    for name, (_, args) in _binding.SIGNATURES.items():
+        assert len(args) == counts[name], (name, len(args), counts[name])
+
+
 def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5, 7):
         assert isinstance(cp_attn.status_string(code), str)
