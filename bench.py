@@ -20,7 +20,8 @@ The same run times the packed-document workload (S=131072, documents of mean
 length 8192) forward and backward and reports it under "docs", and the
 S=131072 workload through the all-gather K/V schedule (K/V gathered into
 natural order, one pass per rank, gathered dK/dV returned to their owners)
-under "allgather";
+under "allgather", and through the Ulysses variant (all-to-all to head
+ownership, full attention per head slice, all-to-all back) under "ulysses";
 ``--workload docs_bf16_s131072_fwdbwd`` makes it the main line (its step adds
 the document-bounds kernel and uses the document-rule forward/backward).
 
@@ -342,6 +343,10 @@ def run_ours(args):
     if docs is None and not args.no_allgather and w.backward:
         ag_info = time_allgather(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
                                  (qs, ks, vs, dos))
+    ul_info = None
+    if docs is None and not args.no_ulysses and w.backward:
+        ul_info = time_ulysses(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
+                               (qs, ks, vs, dos))
 
     path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype)
     cpu = None
@@ -363,7 +368,7 @@ def run_ours(args):
                    "useful_tflop_per_step": step_flops / 1e12},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
         "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "docs": docs_info,
-        "allgather": ag_info,
+        "allgather": ag_info, "ulysses": ul_info,
         "cpu_baseline": cpu,
         "status": cpa.device_status(),
     }
@@ -499,6 +504,53 @@ def time_allgather(cpa, w, dev, stream, warmup, steps, peak, sharded):
             "grad_dtype": "f32", "status": cpa.device_status()}
 
 
+def time_ulysses(cpa, w, dev, stream, warmup, steps, peak, sharded):
+    """The Ulysses variant on sharded inputs, forward and backward calls (each
+    includes its all-to-alls), timed with CUDA events (median of `steps`)."""
+    qs, ks, vs, dos = sharded
+    o = torch.empty_like(qs)
+    lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    g = [torch.empty(x.shape, device=dev, dtype=torch.float32) for x in (qs, ks, vs)]
+    code = cpa.BF16 if w.dtype == torch.bfloat16 else cpa.F32
+    wf = torch.empty(cpa.ulysses_workspace_bytes(w.B, w.H, w.Hkv, w.S, w.D, w.cp, w.layout, code,
+                                                 False), device=dev, dtype=torch.uint8)
+    wb = torch.empty(cpa.ulysses_workspace_bytes(w.B, w.H, w.Hkv, w.S, w.D, w.cp, w.layout,
+                                                 code | cpa.GRAD_F32, True),
+                     device=dev, dtype=torch.uint8)
+    parts = {
+        "fwd": lambda: cpa.ulysses_fwd(qs, ks, vs, w.cp, w.layout, w.causal, out=o, lse=lse,
+                                       workspace=wf),
+        "bwd": lambda: cpa.ulysses_bwd(qs, ks, vs, o, dos, lse, w.cp, w.layout, w.causal,
+                                       dq=g[0], dk=g[1], dv=g[2], workspace=wb,
+                                       grad_dtype=torch.float32),
+    }
+    res = {}
+    for name, fn in parts.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+    fwd_tf = w.useful_flops(False) / (res["fwd"] * 1e-3) / 1e12
+    bwd_tf = w.useful_flops(True) / (res["bwd"] * 1e-3) / 1e12
+    hc, nkv = cpa._binding.ulysses_heads(w.H, w.Hkv, w.cp)
+    return {"workload": w.name, "schedule": "Ulysses all-to-all", "ms": res,
+            "heads_per_rank": hc, "kv_heads_per_rank": nkv,
+            "forward": {"tflops": fwd_tf, "frac": fwd_tf / peak},
+            "backward": {"tflops": bwd_tf, "frac": bwd_tf / peak},
+            "fwd_bwd_tflops": (w.useful_flops(False) + w.useful_flops(True))
+            / ((res["fwd"] + res["bwd"]) * 1e-3) / 1e12,
+            "grad_dtype": "f32", "status": cpa.device_status()}
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -621,6 +673,7 @@ def main():
     ap.add_argument("--no-c3", action="store_true")
     ap.add_argument("--no-docs", action="store_true")
     ap.add_argument("--no-allgather", action="store_true")
+    ap.add_argument("--no-ulysses", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
