@@ -40,10 +40,11 @@
 //
 // Both kernels: CTA = 384 threads; warp 0 TMA, warp 1 TMEM owner + MMA
 // issuer, warps 4-7 and 8-11 the elementwise work on columns [0,64) and
-// [64,128) of each tile (one thread per TMEM lane), and the epilogue.  The
-// packed bf16 result of both halves lands in columns [0,64), part of which
-// the first half still reads as float32: the halves meet at an mbarrier
-// after their reads and before their writes.  Every
+// [64,128) of each tile (one thread per TMEM lane), and the epilogue.  Each
+// half writes its packed bf16 result over the first 32 of the 64 columns it
+// read itself ([0,32) and [64,96)), so the halves never wait for each other;
+// the MMA that consumes the packed tile takes its K = 16 slices from those
+// two column ranges (a_col).  Every
 // wait is a bounded mbarrier wait; on expiry the kernel raises the device
 // error word, drains its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
@@ -83,15 +84,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// The two elementwise warpgroups meet here: every thread arrives, then waits
-// for all 256 arrivals of this phase.  Returns false if the wait gave up.
-__device__ __forceinline__ bool halves_meet(uint32_t bar, uint32_t& phase, const WaitCtl& wc) {
-  tc_fence_before();
-  mbar_arrive(bar);
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, phase, wc));
-  phase ^= 1;
-  tc_fence_after();
-  return ok;
+// TMEM column of the kk-th K = 16 slice of a packed bf16 128 x 128 tile
+// written by the two elementwise halves: half h packs its 64 columns into
+// [64h, 64h + 32).
+__device__ __forceinline__ uint32_t a_col(int kk) {
+  return (uint32_t)((kk >> 2) * 64 + (kk & 3) * 8);
 }
 
 // Location of a 128-row tile given its natural tile index.
@@ -257,9 +254,7 @@ constexpr int kBarDS = 9;
 constexpr int kBarAcc = 10;
 constexpr int kBarAccFree = 11;
 constexpr int kBarDrain = 12;
-constexpr int kBarRdS = 13;   // both halves have read S^T
-constexpr int kBarRdDP = 14;  // both halves have read dP^T
-constexpr int kNumBars = 15;
+constexpr int kNumBars = 13;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -322,8 +317,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarAcc), 1);
     mbar_init(bar(kBarAccFree), 256);
     mbar_init(bar(kBarDrain), 1);
-    mbar_init(bar(kBarRdS), 256);
-    mbar_init(bar(kBarRdDP), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -453,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDV, tmem + kColS + kk * 8,
+            mma_ts(tmem + kColDV, tmem + kColS + a_col(kk),
                    sdesc_sw128(sDO + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
           // S for the next tile (the S^T columns are free once dV has read P^T;
@@ -474,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ds_ph ^= 1;
           tc_fence_after();
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDK, tmem + kColDP + kk * 8,
+            mma_ts(tmem + kColDK, tmem + kColDP + a_col(kk),
                    sdesc_sw128(sQ + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
           mma_commit(bar(kBarQEmpty + st));
@@ -509,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;    // K/V row of the tile (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = sh.scale_log2, scale = sh.scale;
-    uint32_t qi = 0, s_ph = 0, dp_ph = 0, rs_ph = 0, rdp_ph = 0;
+    uint32_t qi = 0, s_ph = 0, dp_ph = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -560,11 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           r[2 * j + 1] = __float_as_uint(p1);
           pk[j] = pack_bf16(p0, p1);
         }
-        if (!halves_meet(bar(kBarRdS), rs_ph, wc)) {
-          ok = false;
-          break;
-        }
-        tmem_st32(tl + kColS + 32 * half, pk);
+        tmem_st32(tl + kColS + 64 * half, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarP));
@@ -590,11 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             (__uint_as_float(d[2 * j + 1]) - dl.y));
           }
         }
-        if (!halves_meet(bar(kBarRdDP), rdp_ph, wc)) {
-          ok = false;
-          break;
-        }
-        tmem_st32(tl + kColDP + 32 * half, ds);
+        tmem_st32(tl + kColDP + 64 * half, ds);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarDS));
@@ -667,8 +652,7 @@ constexpr int kBarDS = 10;
 constexpr int kBarAcc = 11;
 constexpr int kBarAccFree = 12;
 constexpr int kBarDrain = 13;
-constexpr int kBarRdDP = 14;  // both halves have read dP
-constexpr int kNumBars = 15;
+constexpr int kNumBars = 14;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDQ = 384;
@@ -730,7 +714,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarAcc), 1);
     mbar_init(bar(kBarAccFree), 256);
     mbar_init(bar(kBarDrain), 1);
-    mbar_init(bar(kBarRdDP), 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -874,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + kk * 8,
+            mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
                    sdesc_sw128(sK + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
           mma_commit(bar(kBarKVEmpty + st));
@@ -915,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;    // query row of the tile (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = sh.scale_log2, scale = sh.scale;
-    uint32_t kj = 0, s_ph = 0, dp_ph[2] = {0, 0}, rdp_ph = 0;
+    uint32_t kj = 0, s_ph = 0, dp_ph[2] = {0, 0};
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -969,11 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j)
           ds[j] = pack_bf16(scale * p[2 * j] * (__uint_as_float(r[2 * j]) - dlt),
                             scale * p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dlt));
-        if (!halves_meet(bar(kBarRdDP), rdp_ph, wc)) {
-          ok = false;
-          break;
-        }
-        tmem_st32(tl + col_dp(buf) + 32 * half, ds);
+        tmem_st32(tl + col_dp(buf) + 64 * half, ds);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarDS));
