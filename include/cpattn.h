@@ -378,6 +378,34 @@ CPATTN_API int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, c
 CPATTN_API int64_t cpattn_padded_length(int64_t S, int cp_size, int layout);
 
 /*
+ * The whole path from HOST memory to HOST memory: natural-order q, k, v (and
+ * dout) in host buffers, natural-order out, lse (and dq, dk, dv) written back
+ * to host buffers; in between, on the device, the sharded layout, the ring
+ * forward (cpattn_ring_fwd) and, when dout is not NULL, the ring backward
+ * (cpattn_ring_bwd).  The zigzag permutation happens in the copies (one
+ * cudaMemcpyAsync per chunk and batch row).  dout uploads while the forward
+ * runs and out / lse download while the backward runs, on a side stream the
+ * library creates once per device (its first use with dout); the caller's
+ * stream waits for it, so the call has finished when `stream` reaches it.
+ *   Host buffers: pinned memory for asynchronous copies (pageable memory
+ *   works, synchronously); they must stay valid until `stream` gets there.
+ *   dtype: as cpattn_ring_bwd (CPATTN_GRAD_F32 for float32 gradients).
+ *   workspace: device, at least cpattn_attention_host_workspace_bytes (with
+ *   backward = dout != NULL), 256-byte aligned, scratch.  Calls that share a
+ *   workspace, or that run on one device from several host threads at once
+ *   (they share the side stream), must be serialised by the caller.
+ */
+CPATTN_API size_t cpattn_attention_host_workspace_bytes(int B, int H, int Hkv, int S, int D,
+                                                        int cp_size, int layout, int dtype,
+                                                        int backward);
+CPATTN_API int cpattn_attention_host(const void* q, const void* k, const void* v,
+                                     const void* dout, void* out, float* lse, void* dq, void* dk,
+                                     void* dv, int B, int H, int Hkv, int S, int D, int cp_size,
+                                     int layout, int causal, int dtype, float softmax_scale,
+                                     void* workspace, size_t workspace_bytes,
+                                     cpattn_stream_t stream);
+
+/*
  * Closed-form work census of the ring (host only): for every rank r and
  * step t, the number of tile x tile blocks with at least one visible
  * (query, key) pair, tiles_rt[r*cp_size + t], and the number of visible

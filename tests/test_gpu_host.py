@@ -1,0 +1,63 @@
+"""The host-buffer entry point (cpattn_attention_host): natural-order host
+tensors in and out, with the permutation done by the chunked copies and the
+dO upload / O download overlapped on a side stream.  It runs the same
+kernels as the device path, so its results must equal, bit for bit, the
+device path's (cpattn_zigzag_permute -> ring forward -> ring backward ->
+cpattn_zigzag_unpermute); the device path itself is checked against the
+oracle in the other test files.
+"""
+import pytest
+import torch
+
+import context_causal_attention_zigzag_gb300 as cpa
+from context_causal_attention_zigzag_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # B, H, Hkv, S, D, cp, layout, causal, dtype, grad_dtype
+    (1, 4, 2, 2048, 128, 4, cpa.ZIGZAG, True, torch.bfloat16, torch.float32),
+    (2, 4, 1, 1536, 128, 3, cpa.ZIGZAG, True, torch.bfloat16, None),
+    (1, 2, 2, 2048, 128, 2, cpa.CONTIGUOUS, False, torch.bfloat16, torch.float32),
+    (2, 2, 2, 256, 64, 2, cpa.ZIGZAG, True, torch.float32, None),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}H{}K{}S{}D{}cp{}L{}c{}".format(*c[:8]))
+@pytest.mark.parametrize("backward", [True, False])
+def test_host_path_equals_device_path(case, backward):
+    B, H, Hkv, S, D, cp, layout, causal, dtype, gdt = case
+    w = inputs.Workload("host", B, H, Hkv, S, D, cp, layout, causal, dtype, seed=9000 + S)
+    q, k, v, do = inputs.generate(w, with_dout=True, pin=True)
+    res = cpa.attention_host(q, k, v, do if backward else None, cp, layout, causal,
+                             grad_dtype=gdt)
+    torch.cuda.synchronize()
+    dev = [x.cuda() for x in (q, k, v, do)]
+    if backward:
+        ref = cpa.attention_fwd_bwd(*dev, cp, layout, causal, grad_dtype=gdt)
+    else:
+        ref = cpa.attention(*dev[:3], cp, layout, causal)
+    assert len(res) == len(ref)
+    for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), res, ref):
+        assert not a.is_cuda and a.dtype == b.dtype and a.shape == b.shape, name
+        assert torch.equal(a, b.cpu()), name
+    assert cpa.device_status() == 0
+
+
+def test_host_path_repeated_calls_reuse_workspace():
+    # Two calls in a row with one workspace and the same output buffers: the
+    # second call's results equal the first's (nothing left over matters).
+    B, H, Hkv, S, D, cp = 1, 4, 2, 2048, 128, 4
+    w = inputs.Workload("host2", B, H, Hkv, S, D, cp, cpa.ZIGZAG, True, torch.bfloat16, seed=91)
+    q, k, v, do = inputs.generate(w, with_dout=True, pin=True)
+    need = cpa.attention_host_workspace_bytes(B, H, Hkv, S, D, cp, cpa.ZIGZAG,
+                                              cpa.BF16 | cpa.GRAD_F32, True)
+    ws = torch.empty(need, device="cuda", dtype=torch.uint8)
+    outs = cpa.attention_host(q, k, v, do, cp, grad_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    first = [x.clone() for x in outs]
+    outs = cpa.attention_host(q, k, v, do, cp, grad_dtype=torch.float32, workspace=ws)
+    torch.cuda.synchronize()
+    for a, b in zip(outs, first):
+        assert torch.equal(a, b)
+    assert cpa.device_status() == 0
