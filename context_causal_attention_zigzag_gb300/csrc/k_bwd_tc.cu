@@ -31,7 +31,10 @@
 //
 // dq kernel (query-major).  Work item: one 128-row query tile of one head.
 // Q, dO stay in shared memory, LSE / Delta in registers (TMEM lane = query
-// row); the K/V tiles of the ring stream past in a 2-stage ring:
+// row); the K/V tiles of the ring stream past through a ring of five 32 KB
+// slots (K(j), V(j), K(j+1), ... in consecutive slots; V(j)'s slot is free
+// once dP(j) has read it, K(j)'s once dQ(j) has, so loads run up to two
+// tiles ahead):
 //   S = Q K^T -> TMEM [0,128)     dP = dO V^T -> TMEM [128,256) / [256,384)
 //   dS = scale * exp2(S*scale*log2e - LSE*log2e) (dP - Delta) -> bf16 over dP
 //   dQ += dS K  (TS, K read MN-major) -> TMEM [384,512)
@@ -636,23 +639,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 namespace qm {
 
+constexpr int kSlots = 5;  // K/V ring: K(j), V(j) take consecutive slots
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kOffQ + kTileBytes;
-constexpr int kOffK = kOffDO + kTileBytes;     // [2] stages
-constexpr int kOffV = kOffK + 2 * kTileBytes;  // [2]
-constexpr int kOffBar = kOffV + 2 * kTileBytes;
+constexpr int kOffRing = kOffDO + kTileBytes;  // [kSlots]
+constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
-constexpr int kBarKVFull = 2;   // [2]
-constexpr int kBarKVEmpty = 4;  // [2]
-constexpr int kBarS = 6;
-constexpr int kBarSFree = 7;
-constexpr int kBarDP = 8;       // [2]
-constexpr int kBarDS = 10;
-constexpr int kBarAcc = 11;
-constexpr int kBarAccFree = 12;
-constexpr int kBarDrain = 13;
-constexpr int kNumBars = 14;
+constexpr int kBarFull = 2;                    // [kSlots]
+constexpr int kBarEmpty = kBarFull + kSlots;   // [kSlots]
+constexpr int kBarS = kBarEmpty + kSlots;
+constexpr int kBarSFree = kBarS + 1;
+constexpr int kBarDP = kBarSFree + 1;          // [2]
+constexpr int kBarDS = kBarDP + 2;
+constexpr int kBarAcc = kBarDS + 1;
+constexpr int kBarAccFree = kBarAcc + 1;
+constexpr int kBarDrain = kBarAccFree + 1;
+constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kColS = 0, kColDQ = 384;
@@ -690,7 +693,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
-  const uint32_t sQ = base + kOffQ, sDO = base + kOffDO, sK = base + kOffK, sV = base + kOffV;
+  const uint32_t sQ = base + kOffQ, sDO = base + kOffDO, sRing = base + kOffRing;
+  auto slot = [&](uint32_t n) { return sRing + (n % kSlots) * kTileBytes; };
   const uint32_t bars = base + kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -703,11 +707,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarKVFull + i), 1);
-      mbar_init(bar(kBarKVEmpty + i), 1);
-      mbar_init(bar(kBarDP + i), 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar(kBarFull + i), 1);
+      mbar_init(bar(kBarEmpty + i), 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(bar(kBarDP + i), 1);
     mbar_init(bar(kBarS), 1);
     mbar_init(bar(kBarSFree), 256);
     mbar_init(bar(kBarDS), 256);
@@ -733,7 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      uint32_t kj = 0, q_armed = 0, kv_armed[2] = {0, 0};
+      uint32_t seq_n = 0, q_armed = 0, armed[kSlots] = {0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -753,51 +757,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         KSeq seq;
         seq.init(sh, it.q, it.knat);
         int kvrow, knat;
-        while (seq.next(kvrow, knat)) {
-          const int st = kj & 1;
-          const uint32_t ph = (kj >> 1) & 1;
-          if (!mbar_wait(bar(kBarKVEmpty + st), ph ^ 1, wc)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(kBarKVFull + st), 2 * kTileBytes);
-          ++kv_armed[st];
+        while (ok && seq.next(kvrow, knat)) {
           const int krow = it.b * sh.S + kvrow;
-          for (int half = 0; half < 2; ++half) {
-            tma_load_3d(sK + st * kTileBytes + half * kBoxBytes, &tm_k, bar(kBarKVFull + st),
-                        half * 64, it.g, krow);
-            tma_load_3d(sV + st * kTileBytes + half * kBoxBytes, &tm_v, bar(kBarKVFull + st),
-                        half * 64, it.g, krow);
+          for (int which = 0; which < 2; ++which) {  // K(j), then V(j)
+            const uint32_t n = seq_n++;
+            const int sl = n % kSlots;
+            if (!mbar_wait(bar(kBarEmpty + sl), ((n / kSlots) & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar(kBarFull + sl), kTileBytes);
+            ++armed[sl];
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(slot(n) + half * kBoxBytes, which == 0 ? &tm_k : &tm_v,
+                          bar(kBarFull + sl), half * 64, it.g, krow);
           }
-          ++kj;
         }
       }
       if (!ok) {
         if (q_armed) mbar_drain(bar(kBarQFull), (q_armed - 1) & 1);
-        for (int s = 0; s < 2; ++s)
-          if (kv_armed[s]) mbar_drain(bar(kBarKVFull + s), (kv_armed[s] - 1) & 1);
+        for (int s = 0; s < kSlots; ++s)
+          if (armed[s]) mbar_drain(bar(kBarFull + s), (armed[s] - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
+      // Tile j's K is ring entry 2j, its V entry 2j + 1.
       uint32_t kj = 0, sf_ph = 0, ds_ph = 0;
       bool ok = true;
-      auto issue_s = [&](int st) {
+      auto wait_full = [&](uint32_t n) {
+        return mbar_wait(bar(kBarFull + n % kSlots), (n / kSlots) & 1, wc);
+      };
+      auto issue_s = [&](uint32_t kn) {
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
           mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024),
-                 sdesc_sw128(sK + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+                 sdesc_sw128(slot(kn) + off, 16, 1024), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarS));
       };
-      auto issue_dp = [&](int st, int buf) {
+      auto issue_dp = [&](uint32_t vn, int buf) {
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
           mma_ss(tmem + col_dp(buf), sdesc_sw128(sDO + off, 16, 1024),
-                 sdesc_sw128(sV + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+                 sdesc_sw128(slot(vn) + off, 16, 1024), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarDP + buf));
+        mma_commit(bar(kBarEmpty + vn % kSlots));  // V is read only by dP
       };
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -813,23 +820,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kvrow, knat;
         bool have = seq.next(kvrow, knat);
         if (have) {
-          const int st = kj & 1;
-          if (!mbar_wait(bar(kBarKVFull + st), (kj >> 1) & 1, wc)) {
+          if (!wait_full(2 * kj)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(st);
-          issue_dp(st, kj & 1);
+          issue_s(2 * kj);
+          if (!wait_full(2 * kj + 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_dp(2 * kj + 1, kj & 1);
         }
         bool first = true;
         while (have) {
-          const int st = kj & 1;
           int nkvrow, nknat;
           const bool nhave = seq.next(nkvrow, nknat);
-          const int nst = (kj + 1) & 1;
           if (nhave) {
-            if (!mbar_wait(bar(kBarKVFull + nst), ((kj + 1) >> 1) & 1, wc)) {
+            if (!wait_full(2 * kj + 2)) {
               ok = false;
               break;
             }
@@ -840,10 +849,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             sf_ph ^= 1;
             tc_fence_after();
-            issue_s(nst);
+            issue_s(2 * kj + 2);
             // dP into the other buffer: the dQ that read it two tiles ago was
             // issued earlier, and MMAs execute in issue order.
-            issue_dp(nst, (kj + 1) & 1);
+            if (!wait_full(2 * kj + 3)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_dp(2 * kj + 3, (kj + 1) & 1);
           }
           // dQ += dS K
           if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
@@ -858,9 +872,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           for (int kk = 0; kk < kT / 16; ++kk)
             mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
-                   sdesc_sw128(sK + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   sdesc_sw128(slot(2 * kj) + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
-          mma_commit(bar(kBarKVEmpty + st));
+          mma_commit(bar(kBarEmpty + (2 * kj) % kSlots));  // K is free after dQ
           first = false;
           ++kj;
           have = nhave;
