@@ -344,7 +344,8 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   if (tc) {
     // Tensor cores: Delta only, then the dK/dV and dQ kernels (every output
     // element written exactly once), then the per-group sum of dK / dV.
-    e = launch_bwd_prep(out, dout, delta, nullptr, nullptr, nullptr, 0, B, S, H, D, in_dtype, st);
+    e = launch_bwd_prep(out, dout, delta, nullptr, nullptr, nullptr, 0, B, S, H, D, in_dtype,
+                        sh.scale, st);
     if (e != cudaSuccess) return CPATTN_ERR_CUDA;
     a.dk_part = reg_a;
     a.dv_part = reg_b;
@@ -356,7 +357,8 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
     return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
   }
   // CUDA cores: Delta and zeroed accumulators, the kernel, the conversion.
-  e = launch_bwd_prep(out, dout, delta, reg_a, reg_c, reg_d, n_kv, B, S, H, D, in_dtype, st);
+  e = launch_bwd_prep(out, dout, delta, reg_a, reg_c, reg_d, n_kv, B, S, H, D, in_dtype, 1.f,
+                      st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   a.dq_acc = reg_a;
   a.dk_acc = reg_c;

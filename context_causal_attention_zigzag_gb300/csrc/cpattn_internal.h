@@ -135,7 +135,7 @@ struct BwdArgs {
   const void* v;
   const void* dout;
   const float* lse;    // [B,H,S]
-  const float* delta;  // [B,H,S], dout . out
+  const float* delta;  // [B,H,S], dout . out (times the softmax scale on the tensor-core path)
   // CUDA-core path: float32 accumulators, pre-zeroed by the pre-pass.
   float* dq_acc;       // [B,S,H,D]   receives scale * dS K
   float* dk_acc;       // [B,S,Hkv,D] receives scale * dS^T Q
@@ -185,9 +185,11 @@ cudaError_t launch_tc_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_b,
                              const float* l_b, float* o, float* l, int B, int S, int H, int D,
                              cudaStream_t stream);
+// delta[b,h,s] = delta_scale * (dout . out) of the row (the tensor-core
+// backward takes it pre-multiplied by the softmax scale).
 cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, float* dq_acc,
                             float* dk_acc, float* dv_acc, int64_t n_kv, int B, int S, int H,
-                            int D, int dtype, cudaStream_t stream);
+                            int D, int dtype, float delta_scale, cudaStream_t stream);
 cudaError_t launch_simt_bwd(const BwdArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream);
 // dk[b,s,g,:] = sum of dk_part[b,s,h,:] over the query heads h of kv head g

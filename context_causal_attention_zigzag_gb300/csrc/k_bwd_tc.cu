@@ -20,7 +20,9 @@
 //   S^T  = K Q^T   -> TMEM [0,128)       dP^T = V dO^T -> TMEM [128,256)
 //   P^T  = exp2(S^T*scale*log2e - LSE*log2e)  -> bf16 over S^T
 //   dS^T = scale * P^T (dP^T - Delta)         -> bf16 over dP^T
-//   (dS from the float32 P, so that only dS itself is rounded to bf16)
+//   (dS from the float32 P, so that only dS itself is rounded to bf16; Delta
+//   arrives multiplied by the scale, so dS = P (scale dP - scale Delta) is an
+//   FMA and a multiply per element)
 //   dV  += P^T dO  (TS)  -> TMEM [256,384)    dK += dS^T Q (TS) -> TMEM [384,512)
 // MMA order per tile i: dV(i), S(i+1), dK(i), dP(i+1): the elementwise warps
 // of tile i+1 overlap the tensor core's work on tile i.  At the end of the
@@ -576,10 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = 32 * cc + 2 * j;
-            const float2 dl = *reinterpret_cast<const float2*>(dlt + c);
-            ds[16 * cc + j] = pack_bf16(scale * __uint_as_float(r[c]) * (__uint_as_float(d[2 * j]) - dl.x),
-                                        scale * __uint_as_float(r[c + 1]) *
-                                            (__uint_as_float(d[2 * j + 1]) - dl.y));
+            const float2 dl = *reinterpret_cast<const float2*>(dlt + c);  // scale * Delta
+            ds[16 * cc + j] =
+                pack_bf16(__uint_as_float(r[c]) * fmaf(__uint_as_float(d[2 * j]), scale, -dl.x),
+                          __uint_as_float(r[c + 1]) *
+                              fmaf(__uint_as_float(d[2 * j + 1]), scale, -dl.y));
           }
         }
         tmem_st32(tl + kColDP + 64 * half, ds);
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = decode(sh, idx);
       const int64_t li = ((int64_t)it.b * sh.H + it.h) * sh.S + it.q.row + row;
       const float nlse2 = -args.lse[li] * kLog2e;
-      const float dlt = args.delta[li];
+      const float dlt = args.delta[li];  // scale * Delta
       KSeq seq;
       seq.init(sh, it.q, it.knat);
       // Keys that this thread's query sees (natural positions).
@@ -964,8 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ds[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          ds[j] = pack_bf16(scale * p[2 * j] * (__uint_as_float(r[2 * j]) - dlt),
-                            scale * p[2 * j + 1] * (__uint_as_float(r[2 * j + 1]) - dlt));
+          ds[j] = pack_bf16(p[2 * j] * fmaf(__uint_as_float(r[2 * j]), scale, -dlt),
+                            p[2 * j + 1] * fmaf(__uint_as_float(r[2 * j + 1]), scale, -dlt));
         tmem_st32(tl + col_dp(buf) + 64 * half, ds);
         tmem_wait_st();
         tc_fence_before();

@@ -196,7 +196,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
                                                        float* __restrict__ dq_acc,
                                                        float4* __restrict__ dk_acc,
                                                        float4* __restrict__ dv_acc,
-                                                       int64_t n4_kv, int B, int S, int H) {
+                                                       int64_t n4_kv, int B, int S, int H,
+                                                       float delta_scale) {
   const int lane = threadIdx.x & 31;
   const int64_t rows = (int64_t)B * S * H;
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -221,7 +222,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
     }
     if (lane == 0) {
       int64_t bi = row / ((int64_t)S * H), si = (row / H) % S, hi = row % H;
-      delta[(bi * H + hi) * S + si] = acc;
+      delta[(bi * H + hi) * S + si] = acc * delta_scale;
     }
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -503,7 +504,7 @@ cudaError_t launch_lse_merge(const float* o_a, const float* l_a, const float* o_
 
 cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, float* dq_acc,
                             float* dk_acc, float* dv_acc, int64_t n_kv, int B, int S, int H,
-                            int D, int dtype, cudaStream_t stream) {
+                            int D, int dtype, float delta_scale, cudaStream_t stream) {
   int64_t rows = (int64_t)B * S * H;
   if (rows == 0) return cudaSuccess;
   int grid = grid_for(rows * 32, 256, 8);
@@ -515,19 +516,19 @@ cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, flo
     auto d = static_cast<const __nv_bfloat16*>(dout);
     if (D == 128)
       bwd_prep_kernel<__nv_bfloat16, 128>
-          <<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B, S, H);
+          <<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B, S, H, delta_scale);
     else
       bwd_prep_kernel<__nv_bfloat16, 64>
-          <<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B, S, H);
+          <<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B, S, H, delta_scale);
   } else {
     auto o = static_cast<const float*>(out);
     auto d = static_cast<const float*>(dout);
     if (D == 128)
       bwd_prep_kernel<float, 128><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B,
-                                                            S, H);
+                                                            S, H, delta_scale);
     else
       bwd_prep_kernel<float, 64><<<grid, 256, 0, stream>>>(o, d, delta, dq_acc, dk4, dv4, n4, B,
-                                                           S, H);
+                                                           S, H, delta_scale);
   }
   return cudaGetLastError();
 }
