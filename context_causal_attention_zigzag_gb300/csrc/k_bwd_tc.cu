@@ -543,21 +543,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld_regs(r);
         reg_fence32(r + 32);
         // P^T stays in float32 in r for dS below (the bf16 copy feeds dV only).
-        uint32_t pk[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float2 l2 = *reinterpret_cast<const float2*>(lse + 2 * j);
-          float p0 = ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -l2.x * kLog2e));
-          float p1 = ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -l2.y * kLog2e));
-          if (cut) {
-            const int c0 = 64 * half + 2 * j;
-            if (c0 < c_lo || c0 > c_hi) p0 = 0.f;
-            if (c0 + 1 < c_lo || c0 + 1 > c_hi) p1 = 0.f;
-          }
-          r[2 * j] = __float_as_uint(p0);
-          r[2 * j + 1] = __float_as_uint(p1);
-          pk[j] = pack_bf16(p0, p1);
+          r[2 * j] = __float_as_uint(ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -l2.x * kLog2e)));
+          r[2 * j + 1] =
+              __float_as_uint(ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -l2.y * kLog2e)));
         }
+        if (cut) {  // only on tiles the key's window cuts (diagonal, document borders)
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (64 * half + j < c_lo || 64 * half + j > c_hi) r[j] = 0u;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          pk[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
         tmem_st32(tl + kColS + 64 * half, pk);
         tmem_wait_st();
         tc_fence_before();
@@ -950,9 +951,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kBarSFree));
         float p[64];
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          p[j] = ex2(fmaf(__uint_as_float(r[j]), sl2, nlse2));
-          if (cut && (64 * half + j < j_lo || 64 * half + j > j_hi)) p[j] = 0.f;
+        for (int j = 0; j < 64; ++j) p[j] = ex2(fmaf(__uint_as_float(r[j]), sl2, nlse2));
+        if (cut) {  // only on tiles the query's window cuts (diagonal, document borders)
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (64 * half + j < j_lo || 64 * half + j > j_hi) p[j] = 0.f;
         }
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP + buf), dp_ph[buf], wc))) {
           ok = false;
