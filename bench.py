@@ -61,14 +61,14 @@ ALL_WORKLOADS = {**inputs.WORKLOADS, **inputs.DOC_WORKLOADS}
 # workload without a capture; must be re-taken whenever a kernel changes.
 CAPTURED_TRAFFIC = {
     "c5_bf16_s131072_fwdbwd": {
-        "ring_bwd": (2.149e9 + 16.82e6) + (55.861e9 + 4.291e9) + (5.646e9 + 2.121e9)
+        "ring_bwd": (2.149e9 + 0.017e9) + (33.521e9 + 4.277e9) + (5.521e9 + 2.117e9)
         + (4.295e9 + 1.054e9),
-        "ring_fwd": 4.350e9 + 1.069e9,
+        "ring_fwd": 5.355e9 + 1.069e9,
     },
     "docs_bf16_s131072_fwdbwd": {
-        "ring_bwd": (2.149e9 + 16.65e6) + (12.209e9 + 4.272e9) + (2.946e9 + 2.109e9)
-        + (4.295e9 + 1.054e9),
-        "ring_fwd": 1.776e9 + 1.058e9,
+        "ring_bwd": (2.148e9 + 0.016e9) + (7.692e9 + 4.257e9) + (2.934e9 + 2.110e9)
+        + (4.296e9 + 1.054e9),
+        "ring_fwd": 1.795e9 + 1.059e9,
     },
 }
 
