@@ -83,6 +83,22 @@ def peaks():
     return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+def max_over_ranks(x, ws, device):
+    """The largest of x over all ranks (x itself for one rank); `device` is
+    where the process group's backend wants the tensor (CUDA for NCCL)."""
+    if ws == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(step_flops, ws, ms_max):
+    """TFLOP/s of the whole job: every rank's step over the slowest rank's time."""
+    return step_flops * ws / (ms_max * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -268,13 +284,8 @@ def run_ours(args):
     fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(ev["fwd0"], ev["fwd1"]))
     bwd_ms = (statistics.mean(a.elapsed_time(b) for a, b in zip(ev["fwd1"], ev["bwd1"]))
               if w.backward else None)
-    ms_max = ms
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
-    value = step_flops * ws / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms, ws, dev)
+    value = whole_job_value(step_flops, ws, ms_max)
 
     # End to end through the C ABI on host buffers (cpattn_attention_host):
     # pinned natural-order host inputs in, every result back in host memory.
