@@ -60,6 +60,7 @@ SIGNATURES = {
     "cpattn_ring_bwd_noalloc": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp]),
     "cpattn_tile_counts": (_i, [_i64, _i, _i, _i, _i64, _vp, _vp]),
     "cpattn_device_status": (_i, [_vp]),
+    "cpattn_wait_probe": (_i, [_i64, _vp]),
     "cpattn_status_string": (ctypes.c_char_p, [_i]),
 }
 
@@ -594,6 +595,12 @@ def tile_counts(S, cp, layout, causal, tile):
                                   pairs.ctypes.data_as(ctypes.c_void_p))
     _check("cpattn_tile_counts", rc)
     return tiles.reshape(cp, cp), pairs.reshape(cp, cp)
+
+
+def wait_probe(limit_ns, stream=None):
+    """cpattn_wait_probe: a bounded device wait that is made to give up."""
+    s = ctypes.c_void_p(stream.cuda_stream) if stream is not None else _stream()
+    _check("cpattn_wait_probe", lib().cpattn_wait_probe(int(limit_ns), s))
 
 
 def device_status(stream=None):

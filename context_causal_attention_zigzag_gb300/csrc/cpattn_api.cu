@@ -655,6 +655,14 @@ int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal, int64_t t
   return CPATTN_OK;
 }
 
+int cpattn_wait_probe(int64_t limit_ns, cpattn_stream_t stream) {
+  if (limit_ns < 1 || limit_ns > 2000000000LL) return CPATTN_ERR_INVALID_ARG;
+  int* err = device_error_word();
+  if (err == nullptr) return CPATTN_ERR_CUDA;
+  cudaError_t e = launch_wait_probe(err, (uint64_t)limit_ns, (cudaStream_t)stream);
+  return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+}
+
 int cpattn_device_status(cpattn_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;

@@ -203,6 +203,9 @@ cudaError_t launch_grad_convert(const float* dq_acc, const float* dk_acc, const 
                                 void* dq, void* dk, void* dv, int64_t n_q, int64_t n_kv,
                                 int out_dtype, cudaStream_t stream);
 
+// One CTA whose bounded mbarrier wait gives up after limit_ns (raising *err).
+cudaError_t launch_wait_probe(int* err, uint64_t limit_ns, cudaStream_t stream);
+
 // Whether this build carries the tensor-core kernels.
 bool tc_fwd_available();
 bool tc_bwd_available();

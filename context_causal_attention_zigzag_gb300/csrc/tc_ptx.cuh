@@ -66,20 +66,21 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // Shared state of the bounded waits of one CTA.
 struct WaitCtl {
-  volatile int* abort;  // shared flag: some wait of this CTA gave up
-  int* err;             // device error word (global)
+  volatile int* abort;              // shared flag: some wait of this CTA gave up
+  int* err;                         // device error word (global)
+  uint64_t limit_ns = kWaitLimitNs;  // how long a wait may spin
 };
 
 // Waits for the phase of `bar` with the given parity to complete.  Returns
 // false (after raising the CTA's abort flag and the device error word) if it
-// does not within kWaitLimitNs, or if another wait of the CTA already gave up.
+// does not within w.limit_ns, or if another wait of the CTA already gave up.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   if (mbar_test(bar, parity)) return true;
   const uint64_t t0 = global_timer();
   while (true) {
     if (mbar_test(bar, parity)) return true;
     if (*w.abort) return false;
-    if (global_timer() - t0 > kWaitLimitNs) {
+    if (global_timer() - t0 > w.limit_ns) {
       *w.abort = 1;
       atomicExch(w.err, 1);
       return false;

@@ -426,6 +426,17 @@ CPATTN_API int cpattn_tile_counts(int64_t S, int cp_size, int layout, int causal
  */
 CPATTN_API int cpattn_device_status(cpattn_stream_t stream);
 
+/*
+ * Checks the device-side failure path without faulting the GPU: launches one
+ * CTA that waits, with the same bounded wait the attention kernels use, on an
+ * mbarrier phase that never completes.  After limit_ns nanoseconds (1 ..
+ * 2e9) the wait gives up, raises the device error word and the kernel
+ * returns; the next cpattn_device_status reports CPATTN_ERR_DEVICE_TIMEOUT
+ * (and clears it), and the context stays usable.  (The attention kernels'
+ * waits give up after 2 s.)  The pages describe no such call.
+ */
+CPATTN_API int cpattn_wait_probe(int64_t limit_ns, cpattn_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 CPATTN_API const char* cpattn_status_string(int status);
 
