@@ -326,17 +326,20 @@ def run_ours(args):
         e2e_step()
         barrier()
         n_e2e = max(1, min(args.steps, 5))
-        a0 = torch.cuda.Event(enable_timing=True)
-        a1 = torch.cuda.Event(enable_timing=True)
-        a0.record(stream)
-        for _ in range(n_e2e):
+        e2e_clocks = ClockSampler(gpu_id)
+        e2e_clocks.start()
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e + 1)]
+        marks[0].record(stream)
+        for i in range(n_e2e):
             e2e_step()
-        a1.record(stream)
+            marks[i + 1].record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = a0.elapsed_time(a1) / n_e2e
+        e2e_clk = e2e_clocks.stop()
+        per_call = [marks[i].elapsed_time(marks[i + 1]) for i in range(n_e2e)]
+        e2e_ms = sum(per_call) / n_e2e
         e2e = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "api": e2e_api}
+               "ms_per_step": e2e_ms, "ms_per_call": per_call, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "api": e2e_api, "clocks": e2e_clk}
 
     # Roofline of the dominant kernel, from the live event timings.
     dom_ms, dom_flops, dom_name = (bwd_ms, bwd_flops, "ring_bwd") \
