@@ -1,7 +1,9 @@
 // Microbenchmark: cycles per tcgen05.mma (kind::f16, bf16, cta_group::1) for
 // the SS and TS forms at M=128, N in {128, 256}, K=16, issued back to back by
 // one thread, optionally while eight other warps load / store TMEM the way the
-// attention kernels' softmax warps do.  One CTA of 384 threads per SM on every
+// attention kernels' softmax warps do.  Modes 4 and 5 issue N=128 MMAs that
+// alternate between two independent accumulators (two chains interleaved
+// instruction by instruction) instead of one accumulation chain.  One CTA of 384 threads per SM on every
 // SM; every wait is bounded.  It measures the per-instruction ceiling the
 // attention kernels run against; it is not part of the library.
 //
@@ -56,17 +58,20 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsign
   }
   if (threadIdx.x == 0) {
     const int N = (mode == 1 || mode == 3) ? 256 : 128;
-    const bool ts = mode >= 2;
+    const bool ts = mode == 2 || mode == 3 || mode == 5;
+    const bool two = mode >= 4;
     const uint32_t idesc = idesc_bf16(128, N, false, ts);
     unsigned long long t0 = clock64();
     for (int r = 0; r < reps; ++r) {
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+        // two chains: D at columns 128 and 256 (the noise warps use 384-511)
+        const uint32_t d = two ? 128u + 128u * (uint32_t)(kk & 1) : (ts ? 256u : 0u);
         if (!ts)
-          mma_ss(tmem + 0, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024), idesc,
+          mma_ss(tmem + d, sdesc_sw128(sA + off, 16, 1024), sdesc_sw128(sB + off, 16, 1024), idesc,
                  1);
         else
-          mma_ts(tmem + 256, tmem + 0 + kk * 8, sdesc_sw128(sB + kk * 2048, 16384, 1024), idesc, 1);
+          mma_ts(tmem + d, tmem + 0 + kk * 8, sdesc_sw128(sB + kk * 2048, 16384, 1024), idesc, 1);
       }
     }
     mma_commit(bar0);
@@ -92,8 +97,9 @@ int main() {
   cudaMemset(err, 0, 4);
   int smem = 98304 + 1024 + 128;
   cudaFuncSetAttribute(rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  const char* names[] = {"SS N=128", "SS N=256", "TS N=128", "TS N=256"};
-  for (int mode = 0; mode < 4; ++mode) {
+  const char* names[] = {"SS N=128", "SS N=256", "TS N=128", "TS N=256",
+                         "SS N=128 two chains", "TS N=128 two chains"};
+  for (int mode = 0; mode < 6; ++mode) {
     for (int noise : {0, 1}) {
       const int grid = sms;
       const int reps = 200;
