@@ -4,7 +4,9 @@ dO upload / O download overlapped on a side stream.  It runs the same
 kernels as the device path, so its results must equal, bit for bit, the
 device path's (cpattn_zigzag_permute -> ring forward -> ring backward ->
 cpattn_zigzag_unpermute); the device path itself is checked against the
-oracle in the other test files.
+oracle in the other test files.  One exception: the CUDA-core backward (used
+for float32 inputs) adds dQ partials with float atomics, whose order varies
+from run to run, so there dQ is held to float32 reordering error instead.
 """
 import pytest
 import torch
@@ -38,9 +40,15 @@ def test_host_path_equals_device_path(case, backward):
     else:
         ref = cpa.attention(*dev[:3], cp, layout, causal)
     assert len(res) == len(ref)
+    path, _ = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, dtype, backward=True)
     for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), res, ref):
         assert not a.is_cuda and a.dtype == b.dtype and a.shape == b.shape, name
-        assert torch.equal(a, b.cpu()), name
+        if name == "dq" and path != cpa.PATH_TCGEN05:
+            # float32 sums of at most S / 64 atomic partials per element
+            bound = 1e-6 * (b.abs().max().item() + 1e-30) * S / 64
+            assert (a - b.cpu()).abs().max().item() <= bound, name
+        else:
+            assert torch.equal(a, b.cpu()), name
     assert cpa.device_status() == 0
 
 
