@@ -340,6 +340,8 @@ def run_ours(args):
         e2e = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e2e_ms, "ms_per_call": per_call, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "api": e2e_api, "clocks": e2e_clk}
+        if docs is None:
+            e2e["head_parts"] = cpa.attention_host_parts(B, H, Hkv, S, D)
 
     # Roofline of the dominant kernel, from the live event timings.
     dom_ms, dom_flops, dom_name = (bwd_ms, bwd_flops, "ring_bwd") \

@@ -48,7 +48,8 @@ SIGNATURES = {
     "cpattn_ulysses_fwd": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_ulysses_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_attention_host_workspace_bytes": (_sz, [_i] * 9),
-    "cpattn_attention_host": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _sz, _vp]),
+    "cpattn_attention_host_parts": (_i, [_i] * 5),
+    "cpattn_attention_host": (_i, [_vp] * 9 + [_i] * 9 + [_f, _i, _vp, _sz, _vp]),
     "cpattn_ring_fwd": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp]),
     "cpattn_ring_fwd_census": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp, _vp]),
     "cpattn_ring_fwd_plan": (_i, [_i] * 9 + [_ip, _ip]),
@@ -701,11 +702,17 @@ def attention_host_workspace_bytes(B, H, Hkv, S, D, cp, layout=ZIGZAG, dtype=BF1
                                                            int(dtype), int(bool(backward))))
 
 
+def attention_host_parts(B, H, Hkv, S, D) -> int:
+    """The number of head parts attention_host takes when parts=0."""
+    return int(lib().cpattn_attention_host_parts(B, H, Hkv, S, D))
+
+
 def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, out=None,
                    lse=None, dq=None, dk=None, dv=None, grad_dtype=None, workspace=None,
-                   device=None, stream=None):
+                   device=None, stream=None, parts=0):
     """cpattn_attention_host: natural-order CPU tensors (pinned for
-    asynchronous copies) in and out, the whole path on the GPU in between.
+    asynchronous copies) in and out, the whole path on the GPU in between,
+    the heads in `parts` pipelined groups (0: the library's choice).
     dout None: forward only.  Returns (out, lse) or (out, lse, dq, dk, dv) as
     CPU tensors; they are complete once the stream has been synchronised."""
     if q.is_cuda or k.is_cuda or v.is_cuda:
@@ -738,6 +745,6 @@ def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, ou
     rc = lib().cpattn_attention_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out), _ptr(lse),
                                      _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
                                      int(layout), int(bool(causal)), code, _scale(scale),
-                                     _ptr(workspace), workspace.numel(), st)
+                                     int(parts), _ptr(workspace), workspace.numel(), st)
     _check("cpattn_attention_host", rc)
     return (out, lse, dq, dk, dv) if backward else (out, lse)

@@ -2,18 +2,27 @@
 // memory, natural-order results back to host memory, the whole path on the
 // device in between.
 //
-// The zigzag permutation is folded into the copies: natural chunk nc of
-// batch row b is one contiguous run on both sides (host: natural position
-// nc*c; device: the sharded position of that chunk), so each tensor moves as
-// B * 2*cp (zigzag) or B * cp (contiguous) cudaMemcpyAsync calls.  LSE, whose
-// sequence axis is innermost, is unpermuted by the device kernel and copied
-// back in one piece.
+// Parts: the heads are split into `parts` groups of whole kv-head groups
+// (part p: query heads [p*Hp, (p+1)*Hp), kv heads [p*Hkvp, (p+1)*Hkvp)).
+// Each part has contiguous device tensors [B, S, Hp, D] of its own, filled
+// by copies that gather the part's heads out of the natural host rows and
+// fold the zigzag permutation in (natural chunk nc of batch row b is one
+// run of rows on both sides: one 2-D copy per chunk and batch row).  The
+// attention of a head does not depend on the other heads, so each part runs
+// the ring forward and backward unchanged on its own tensors and the
+// results are, bit for bit, those of one call over all heads.
 //
-// Overlap: dO goes up on a side stream while the forward runs, and O / LSE
-// come down on the side stream while the backward runs.  The side stream
-// and its events are created once per device on first use; the caller's
-// stream waits for the side stream before the call's last operation, so the
-// call is complete when the caller's stream reaches that point.
+// Overlap, three streams:
+//   up stream       Q_p, K_p, V_p of every part in turn, then dO_p;
+//   caller stream   forward(p) once part p is up, then backward(p) once dO_p
+//                   is up;
+//   down stream     O_p and LSE_p once forward(p) is done, dQ_p, dK_p, dV_p
+//                   once backward(p) is done.
+// Only the first part's upload and the last part's download are not hidden
+// behind computation.  The two side streams and their events are created
+// once per device on first use; the caller's stream waits for both before
+// the call's last operation, so the call is complete when the caller's
+// stream reaches that point.
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -29,66 +38,125 @@ using namespace cpattn;
 namespace {
 
 constexpr int kMaxDevices = 64;
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t ev_a = nullptr, ev_b = nullptr, ev_c = nullptr;
+constexpr int kMaxParts = 8;
+
+struct SideStreams {
+  bool ready = false;
+  cudaStream_t up = nullptr, down = nullptr;
+  cudaEvent_t start = nullptr, up_end = nullptr, down_end = nullptr;
+  cudaEvent_t qkv[kMaxParts], dout[kMaxParts], fwd[kMaxParts], bwd[kMaxParts];
 };
-SideStream g_side[kMaxDevices];
+SideStreams g_side[kMaxDevices];
 std::mutex g_side_mutex;
 
-// The side stream of the current device (created on first use).
-SideStream* side_stream() {
+// The side streams of the current device (created on first use).
+SideStreams* side_streams() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_side_mutex);
-  SideStream& s = g_side[dev];
-  if (s.stream == nullptr) {
-    cudaStream_t st = nullptr;
-    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    cudaEvent_t e[3] = {nullptr, nullptr, nullptr};
-    for (auto& ev : e)
-      if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return nullptr;
-    s.ev_a = e[0];
-    s.ev_b = e[1];
-    s.ev_c = e[2];
-    s.stream = st;
+  SideStreams& s = g_side[dev];
+  if (s.ready) return &s;
+  SideStreams n;
+  bool ok = cudaStreamCreateWithFlags(&n.up, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&n.down, cudaStreamNonBlocking) == cudaSuccess;
+  cudaEvent_t* evs[3 + 4 * kMaxParts];
+  int ne = 0;
+  evs[ne++] = &n.start;
+  evs[ne++] = &n.up_end;
+  evs[ne++] = &n.down_end;
+  for (int p = 0; p < kMaxParts; ++p) {
+    evs[ne++] = &n.qkv[p];
+    evs[ne++] = &n.dout[p];
+    evs[ne++] = &n.fwd[p];
+    evs[ne++] = &n.bwd[p];
   }
+  for (int i = 0; i < ne; ++i) *evs[i] = nullptr;
+  for (int i = 0; i < ne && ok; ++i)
+    ok = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    for (int i = 0; i < ne; ++i)
+      if (*evs[i]) cudaEventDestroy(*evs[i]);
+    if (n.up) cudaStreamDestroy(n.up);
+    if (n.down) cudaStreamDestroy(n.down);
+    return nullptr;
+  }
+  n.ready = true;
+  s = n;
   return &s;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Device bytes reserved for a tensor of `full` bytes split into up to
+// kMaxParts 256-byte-aligned parts.
+size_t reserve(size_t full) { return align256(full) + (size_t)kMaxParts * 256; }
+
 struct HostPlan {
-  int B, S, cp, per, c, L;
+  int B, S, H, Hkv, D, cp, per, c, L;
+  int n, Hp, Hkvp;  // parts, query / kv heads per part
   size_t elt, gelt;
-  size_t q, kv, lse, gq, gkv, bwd, total;
+  // bytes of one part's tensor (slot = 256-aligned stride between parts)
+  size_t q, kv, lse, gq, gkv;
+  size_t q_slot, kv_slot, lse_slot, gq_slot, gkv_slot;
+  size_t bwd;    // backward workspace of one part
+  size_t total;  // workspace bound, independent of the number of parts
 };
 
+// Parts chosen when the caller passes 0: four (else two) when the kv heads
+// split evenly and one query tensor is at least 64 MiB, else one.
+int auto_parts(int B, int S, int H, int Hkv, int D) {
+  if ((double)B * S * H * D * 2.0 < 64.0 * 1024 * 1024) return 1;
+  if (Hkv % 4 == 0) return 4;
+  if (Hkv % 2 == 0) return 2;
+  return 1;
+}
+
 bool plan_host(int B, int H, int Hkv, int S, int D, int cp, int layout, int dtype, bool backward,
-               HostPlan* p) {
+               int parts, HostPlan* p) {
   if (B < 0 || H < 1 || Hkv < 1 || S < 0 || cp < 1 || (D != 64 && D != 128)) return false;
+  if (H % Hkv != 0) return false;
   if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG) return false;
   const int in_dtype = dtype & ~CPATTN_GRAD_F32;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return false;
   const int per = layout == CPATTN_LAYOUT_ZIGZAG ? 2 : 1;
   if (S % (cp * per) != 0) return false;
+  if (parts == 0) parts = auto_parts(B, S, H, Hkv, D);
+  if (parts < 1 || parts > kMaxParts || Hkv % parts != 0) return false;
   p->B = B;
   p->S = S;
+  p->H = H;
+  p->Hkv = Hkv;
+  p->D = D;
   p->cp = cp;
   p->per = per;
   p->L = S / cp;
   p->c = p->L / per;
+  p->n = parts;
+  p->Hp = H / parts;
+  p->Hkvp = Hkv / parts;
   p->elt = in_dtype == CPATTN_BF16 ? 2 : 4;
   p->gelt = (dtype & CPATTN_GRAD_F32) ? 4 : p->elt;
   const size_t rows = (size_t)B * S;
-  p->q = align256(rows * H * D * p->elt);
-  p->kv = align256(rows * Hkv * D * p->elt);
-  p->lse = align256((size_t)B * H * S * sizeof(float));
-  p->gq = backward ? align256(rows * H * D * p->gelt) : 0;
-  p->gkv = backward ? align256(rows * Hkv * D * p->gelt) : 0;
-  p->bwd = backward ? align256(cpattn_ring_bwd_workspace_bytes(B, H, Hkv, S, D, dtype)) : 0;
-  // q, k, v, (dO), out, lse sharded, lse natural, (dq, dk, dv), backward workspace
-  p->total = (backward ? 3 : 2) * p->q + 2 * p->kv + 2 * p->lse + p->gq + 2 * p->gkv + p->bwd;
+  p->q = rows * p->Hp * D * p->elt;
+  p->kv = rows * p->Hkvp * D * p->elt;
+  p->lse = (size_t)B * p->Hp * S * sizeof(float);
+  p->gq = rows * p->Hp * D * p->gelt;
+  p->gkv = rows * p->Hkvp * D * p->gelt;
+  p->q_slot = align256(p->q);
+  p->kv_slot = align256(p->kv);
+  p->lse_slot = align256(p->lse);
+  p->gq_slot = align256(p->gq);
+  p->gkv_slot = align256(p->gkv);
+  p->bwd = backward ? cpattn_ring_bwd_workspace_bytes(B, p->Hp, p->Hkvp, S, D, dtype) : 0;
+  // q, out, (dO); k, v; lse sharded, lse natural; (dq, dk, dv); backward
+  // workspace -- each reserved for any number of parts up to kMaxParts.
+  const size_t fq = rows * H * D * p->elt, fkv = rows * Hkv * D * p->elt;
+  const size_t flse = (size_t)B * H * S * sizeof(float);
+  const size_t fgq = rows * H * D * p->gelt, fgkv = rows * Hkv * D * p->gelt;
+  p->total = (backward ? 3 : 2) * reserve(fq) + 2 * reserve(fkv) + 2 * reserve(flse);
+  if (backward)
+    p->total += reserve(fgq) + 2 * reserve(fgkv) +
+                align256(cpattn_ring_bwd_workspace_bytes(B, H, Hkv, S, D, dtype));
   return true;
 }
 
@@ -99,24 +167,47 @@ int64_t chunk_row(const HostPlan& p, int nc) {
   return (int64_t)r * p.L + (nc < p.cp ? 0 : p.c);
 }
 
-// Copies a [B, S, row_bytes] tensor between natural-order host memory and
-// sharded-order device memory, one contiguous chunk per cudaMemcpyAsync.
-cudaError_t copy_chunks(const HostPlan& p, const void* src, void* dst, size_t row_bytes,
-                        bool to_device, cudaStream_t st) {
+// Copies the heads of part `part` of a [B, S, X, D] tensor (X heads, elt
+// bytes each) from src to dst: natural-order host memory to the part's
+// sharded device tensor [B, S, X / n, D] (to_device), or back.  One copy per
+// natural chunk and batch row, 2-D (a run of rows, each the part's slice of
+// a host row) when the part is not the whole row.
+cudaError_t copy_part(const HostPlan& p, const void* src, void* dst, int X, size_t elt, int part,
+                      bool to_device, cudaStream_t st) {
+  const size_t hpitch = (size_t)X * p.D * elt;  // a natural host row
+  const size_t dpitch = hpitch / p.n;            // a row of the part's device tensor
+  const size_t hoff = (size_t)part * dpitch;     // the part's heads within a host row
   const int nchunk = p.cp * p.per;
-  const size_t chunk_bytes = (size_t)p.c * row_bytes;
+  char* host = static_cast<char*>(to_device ? const_cast<void*>(src) : dst);
+  char* dev = static_cast<char*>(to_device ? dst : const_cast<void*>(src));
   for (int b = 0; b < p.B; ++b)
     for (int nc = 0; nc < nchunk; ++nc) {
-      const size_t nat = ((size_t)b * p.S + (size_t)nc * p.c) * row_bytes;
-      const size_t shd = ((size_t)b * p.S + (size_t)chunk_row(p, nc)) * row_bytes;
-      const char* s = static_cast<const char*>(src) + (to_device ? nat : shd);
-      char* d = static_cast<char*>(dst) + (to_device ? shd : nat);
-      cudaError_t e = cudaMemcpyAsync(d, s, chunk_bytes,
-                                      to_device ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToHost,
-                                      st);
+      const size_t nat = (size_t)b * p.S + (size_t)nc * p.c;
+      const size_t shd = (size_t)b * p.S + (size_t)chunk_row(p, nc);
+      char* h = host + nat * hpitch + hoff;
+      char* d = dev + shd * dpitch;
+      cudaError_t e;
+      if (p.n == 1)
+        e = to_device ? cudaMemcpyAsync(d, h, (size_t)p.c * dpitch, cudaMemcpyHostToDevice, st)
+                      : cudaMemcpyAsync(h, d, (size_t)p.c * dpitch, cudaMemcpyDeviceToHost, st);
+      else
+        e = to_device
+                ? cudaMemcpy2DAsync(d, dpitch, h, hpitch, dpitch, p.c, cudaMemcpyHostToDevice, st)
+                : cudaMemcpy2DAsync(h, hpitch, d, dpitch, dpitch, p.c, cudaMemcpyDeviceToHost, st);
       if (e != cudaSuccess) return e;
     }
   return cudaSuccess;
+}
+
+// LSE of part `part` ([B, Hp, S], natural order on the device) into the
+// host's [B, H, S].
+cudaError_t copy_lse_part(const HostPlan& p, const float* dev, float* host, int part,
+                          cudaStream_t st) {
+  const size_t width = (size_t)p.Hp * p.S * sizeof(float);
+  const size_t hpitch = (size_t)p.H * p.S * sizeof(float);
+  char* h = reinterpret_cast<char*>(host) + (size_t)part * width;
+  if (p.n == 1) return cudaMemcpyAsync(h, dev, (size_t)p.B * width, cudaMemcpyDeviceToHost, st);
+  return cudaMemcpy2DAsync(h, hpitch, dev, width, width, p.B, cudaMemcpyDeviceToHost, st);
 }
 
 }  // namespace
@@ -126,18 +217,23 @@ extern "C" {
 size_t cpattn_attention_host_workspace_bytes(int B, int H, int Hkv, int S, int D, int cp_size,
                                              int layout, int dtype, int backward) {
   HostPlan p;
-  if (!plan_host(B, H, Hkv, S, D, cp_size, layout, dtype, backward != 0, &p)) return 0;
+  if (!plan_host(B, H, Hkv, S, D, cp_size, layout, dtype, backward != 0, 1, &p)) return 0;
   return p.total;
+}
+
+int cpattn_attention_host_parts(int B, int H, int Hkv, int S, int D) {
+  if (B < 0 || H < 1 || Hkv < 1 || S < 0 || H % Hkv != 0) return 1;
+  return auto_parts(B, S, H, Hkv, D);
 }
 
 int cpattn_attention_host(const void* q, const void* k, const void* v, const void* dout,
                           void* out, float* lse, void* dq, void* dk, void* dv, int B, int H,
                           int Hkv, int S, int D, int cp_size, int layout, int causal, int dtype,
-                          float softmax_scale, void* workspace, size_t workspace_bytes,
+                          float softmax_scale, int parts, void* workspace, size_t workspace_bytes,
                           cpattn_stream_t stream) {
   const bool backward = dout != nullptr;
   HostPlan p;
-  if (!plan_host(B, H, Hkv, S, D, cp_size, layout, dtype, backward, &p))
+  if (!plan_host(B, H, Hkv, S, D, cp_size, layout, dtype, backward, parts, &p))
     return CPATTN_ERR_INVALID_ARG;
   if ((long long)B * S == 0) return CPATTN_OK;
   if (!q || !k || !v || !out || !lse) return CPATTN_ERR_INVALID_ARG;
@@ -147,80 +243,108 @@ int cpattn_attention_host(const void* q, const void* k, const void* v, const voi
     return CPATTN_ERR_WORKSPACE;
   const int in_dtype = dtype & ~CPATTN_GRAD_F32;
   cudaStream_t st = (cudaStream_t)stream;
+  SideStreams* ss = side_streams();
+  if (ss == nullptr) return CPATTN_ERR_CUDA;
+
+  // Workspace regions, one 256-byte-aligned slot per part in each.
   char* w = static_cast<char*>(workspace);
-  void* qs = w;
-  w += p.q;
-  void* os = w;
-  w += p.q;
-  void* dos = nullptr;
+  const size_t fq = (size_t)B * S * H * D * p.elt, fkv = (size_t)B * S * Hkv * D * p.elt;
+  const size_t flse = (size_t)B * H * S * sizeof(float);
+  char* qs = w;
+  w += reserve(fq);
+  char* os = w;
+  w += reserve(fq);
+  char* dos = nullptr;
   if (backward) {
     dos = w;
-    w += p.q;
+    w += reserve(fq);
   }
-  void* ks = w;
-  w += p.kv;
-  void* vs = w;
-  w += p.kv;
-  float* lse_s = reinterpret_cast<float*>(w);
-  w += p.lse;
-  float* lse_n = reinterpret_cast<float*>(w);
-  w += p.lse;
-  void* dqs = w;
-  w += p.gq;
-  void* dks = w;
-  w += p.gkv;
-  void* dvs = w;
-  w += p.gkv;
-  void* bws = w;
-
-  const size_t qrow = (size_t)H * D * p.elt, kvrow = (size_t)Hkv * D * p.elt;
-  const size_t gqrow = (size_t)H * D * p.gelt, gkvrow = (size_t)Hkv * D * p.gelt;
-  SideStream* side = backward ? side_stream() : nullptr;
-  if (backward && side == nullptr) return CPATTN_ERR_CUDA;
-  int rc = CPATTN_OK;
-#define CPATTN_TRY(x)                                 \
-  do {                                                \
-    if ((x) != cudaSuccess) return CPATTN_ERR_CUDA;   \
-  } while (0)
+  char* ks = w;
+  w += reserve(fkv);
+  char* vs = w;
+  w += reserve(fkv);
+  char* lse_s = w;
+  w += reserve(flse);
+  char* lse_n = w;
+  w += reserve(flse);
+  char *dqs = nullptr, *dks = nullptr, *dvs = nullptr, *bws = nullptr;
   if (backward) {
-    // dO goes up on the side stream, once the caller's stream is here.
-    CPATTN_TRY(cudaEventRecord(side->ev_a, st));
-    CPATTN_TRY(cudaStreamWaitEvent(side->stream, side->ev_a, 0));
-    CPATTN_TRY(copy_chunks(p, dout, dos, qrow, true, side->stream));
-    CPATTN_TRY(cudaEventRecord(side->ev_b, side->stream));
+    dqs = w;
+    w += reserve((size_t)B * S * H * D * p.gelt);
+    dks = w;
+    w += reserve((size_t)B * S * Hkv * D * p.gelt);
+    dvs = w;
+    w += reserve((size_t)B * S * Hkv * D * p.gelt);
+    bws = w;
   }
-  CPATTN_TRY(copy_chunks(p, q, qs, qrow, true, st));
-  CPATTN_TRY(copy_chunks(p, k, ks, kvrow, true, st));
-  CPATTN_TRY(copy_chunks(p, v, vs, kvrow, true, st));
-  rc = cpattn_ring_fwd(qs, ks, vs, os, lse_s, B, H, Hkv, S, D, cp_size, layout, causal, in_dtype,
-                       softmax_scale, stream);
-  if (rc != CPATTN_OK) return rc;
-  rc = cpattn_zigzag_unpermute(lse_s, lse_n, (int64_t)B * H, S, sizeof(float), cp_size, layout,
-                               stream);
-  if (rc != CPATTN_OK) return rc;
-  if (!backward) {
-    CPATTN_TRY(copy_chunks(p, os, out, qrow, false, st));
-    CPATTN_TRY(cudaMemcpyAsync(lse, lse_n, (size_t)B * H * S * sizeof(float),
-                               cudaMemcpyDeviceToHost, st));
-    return CPATTN_OK;
+
+  // From here on every exit makes the caller's stream wait for both side
+  // streams, so nothing the call enqueued outlives it unseen.
+  if (cudaEventRecord(ss->start, st) != cudaSuccess ||
+      cudaStreamWaitEvent(ss->up, ss->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(ss->down, ss->start, 0) != cudaSuccess)
+    return CPATTN_ERR_CUDA;
+  int rc = CPATTN_OK;
+  auto cuda = [&](cudaError_t e) {
+    if (e != cudaSuccess && rc == CPATTN_OK) rc = CPATTN_ERR_CUDA;
+    return rc == CPATTN_OK;
+  };
+  auto lib = [&](int r) {
+    if (r != CPATTN_OK && rc == CPATTN_OK) rc = r;
+    return rc == CPATTN_OK;
+  };
+  const int n = p.n;
+  // Uploads: Q, K, V part by part, then dO part by part.
+  for (int i = 0; i < n && rc == CPATTN_OK; ++i) {
+    cuda(copy_part(p, q, qs + i * p.q_slot, H, p.elt, i, true, ss->up)) &&
+        cuda(copy_part(p, k, ks + i * p.kv_slot, Hkv, p.elt, i, true, ss->up)) &&
+        cuda(copy_part(p, v, vs + i * p.kv_slot, Hkv, p.elt, i, true, ss->up)) &&
+        cuda(cudaEventRecord(ss->qkv[i], ss->up));
   }
-  // O and LSE come down on the side stream while the backward runs.
-  CPATTN_TRY(cudaEventRecord(side->ev_c, st));
-  CPATTN_TRY(cudaStreamWaitEvent(side->stream, side->ev_c, 0));
-  CPATTN_TRY(copy_chunks(p, os, out, qrow, false, side->stream));
-  CPATTN_TRY(cudaMemcpyAsync(lse, lse_n, (size_t)B * H * S * sizeof(float),
-                             cudaMemcpyDeviceToHost, side->stream));
-  CPATTN_TRY(cudaEventRecord(side->ev_a, side->stream));
-  CPATTN_TRY(cudaStreamWaitEvent(st, side->ev_b, 0));  // dO is on the device
-  rc = cpattn_ring_bwd(qs, ks, vs, os, dos, lse_s, dqs, dks, dvs, B, H, Hkv, S, D, cp_size, layout,
-                       causal, dtype, softmax_scale, bws, p.bwd, stream);
-  if (rc != CPATTN_OK) return rc;
-  CPATTN_TRY(copy_chunks(p, dqs, dq, gqrow, false, st));
-  CPATTN_TRY(copy_chunks(p, dks, dk, gkvrow, false, st));
-  CPATTN_TRY(copy_chunks(p, dvs, dv, gkvrow, false, st));
-  CPATTN_TRY(cudaStreamWaitEvent(st, side->ev_a, 0));  // O and LSE are on the host
-#undef CPATTN_TRY
-  return CPATTN_OK;
+  for (int i = 0; backward && i < n && rc == CPATTN_OK; ++i) {
+    cuda(copy_part(p, dout, dos + i * p.q_slot, H, p.elt, i, true, ss->up)) &&
+        cuda(cudaEventRecord(ss->dout[i], ss->up));
+  }
+  // Forward part by part; each part's O and LSE go down behind it.
+  for (int i = 0; i < n && rc == CPATTN_OK; ++i) {
+    void* o_i = os + i * p.q_slot;
+    float* ls_i = reinterpret_cast<float*>(lse_s + i * p.lse_slot);
+    float* ln_i = reinterpret_cast<float*>(lse_n + i * p.lse_slot);
+    cuda(cudaStreamWaitEvent(st, ss->qkv[i], 0)) &&
+        lib(cpattn_ring_fwd(qs + i * p.q_slot, ks + i * p.kv_slot, vs + i * p.kv_slot, o_i, ls_i,
+                            B, p.Hp, p.Hkvp, S, D, cp_size, layout, causal, in_dtype,
+                            softmax_scale, stream)) &&
+        lib(cpattn_zigzag_unpermute(ls_i, ln_i, (int64_t)B * p.Hp, S, sizeof(float), cp_size,
+                                    layout, stream)) &&
+        cuda(cudaEventRecord(ss->fwd[i], st)) &&
+        cuda(cudaStreamWaitEvent(ss->down, ss->fwd[i], 0)) &&
+        cuda(copy_part(p, o_i, out, H, p.elt, i, false, ss->down)) &&
+        cuda(copy_lse_part(p, ln_i, lse, i, ss->down));
+  }
+  // Backward part by part; each part's gradients go down behind it.
+  for (int i = 0; backward && i < n && rc == CPATTN_OK; ++i) {
+    void* dq_i = dqs + i * p.gq_slot;
+    void* dk_i = dks + i * p.gkv_slot;
+    void* dv_i = dvs + i * p.gkv_slot;
+    cuda(cudaStreamWaitEvent(st, ss->dout[i], 0)) &&
+        lib(cpattn_ring_bwd(qs + i * p.q_slot, ks + i * p.kv_slot, vs + i * p.kv_slot,
+                            os + i * p.q_slot, dos + i * p.q_slot,
+                            reinterpret_cast<float*>(lse_s + i * p.lse_slot), dq_i, dk_i, dv_i, B,
+                            p.Hp, p.Hkvp, S, D, cp_size, layout, causal, dtype, softmax_scale,
+                            bws, p.bwd, stream)) &&
+        cuda(cudaEventRecord(ss->bwd[i], st)) &&
+        cuda(cudaStreamWaitEvent(ss->down, ss->bwd[i], 0)) &&
+        cuda(copy_part(p, dq_i, dq, H, p.gelt, i, false, ss->down)) &&
+        cuda(copy_part(p, dk_i, dk, Hkv, p.gelt, i, false, ss->down)) &&
+        cuda(copy_part(p, dv_i, dv, Hkv, p.gelt, i, false, ss->down));
+  }
+  // The caller's stream waits for both side streams.
+  const bool joined = cudaEventRecord(ss->up_end, ss->up) == cudaSuccess &&
+                      cudaEventRecord(ss->down_end, ss->down) == cudaSuccess &&
+                      cudaStreamWaitEvent(st, ss->up_end, 0) == cudaSuccess &&
+                      cudaStreamWaitEvent(st, ss->down_end, 0) == cudaSuccess;
+  if (!joined && rc == CPATTN_OK) rc = CPATTN_ERR_CUDA;
+  return rc;
 }
 
 }  // extern "C"

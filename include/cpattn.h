@@ -382,27 +382,42 @@ CPATTN_API int64_t cpattn_padded_length(int64_t S, int cp_size, int layout);
  * dout) in host buffers, natural-order out, lse (and dq, dk, dv) written back
  * to host buffers; in between, on the device, the sharded layout, the ring
  * forward (cpattn_ring_fwd) and, when dout is not NULL, the ring backward
- * (cpattn_ring_bwd).  The zigzag permutation happens in the copies (one
- * cudaMemcpyAsync per chunk and batch row).  dout uploads while the forward
- * runs and out / lse download while the backward runs, on a side stream the
- * library creates once per device (its first use with dout); the caller's
- * stream waits for it, so the call has finished when `stream` reaches it.
+ * (cpattn_ring_bwd).  The zigzag permutation happens in the copies (one copy
+ * per chunk and batch row).
+ *   parts: the heads are processed in `parts` groups of whole kv-head groups
+ *   (parts must divide Hkv; 1..8; 0 = the library's choice: 4 or 2 when Hkv
+ *   allows and one query tensor is at least 64 MiB, else 1).  A part's
+ *   inputs upload while the previous part computes and its results download
+ *   while the next one computes, on two side streams (upload, download) the
+ *   library creates once per device; only the first part's upload and the
+ *   last part's download are exposed.  Results are bit for bit those of
+ *   parts = 1 (heads are independent).
+ *   The caller's stream waits for both side streams, so the call has
+ *   finished when `stream` reaches that point.
  *   Host buffers: pinned memory for asynchronous copies (pageable memory
  *   works, synchronously); they must stay valid until `stream` gets there.
  *   dtype: as cpattn_ring_bwd (CPATTN_GRAD_F32 for float32 gradients).
  *   workspace: device, at least cpattn_attention_host_workspace_bytes (with
- *   backward = dout != NULL), 256-byte aligned, scratch.  Calls that share a
- *   workspace, or that run on one device from several host threads at once
- *   (they share the side stream), must be serialised by the caller.
+ *   backward = dout != NULL; the size covers every value of parts),
+ *   256-byte aligned, scratch.  Calls that share a workspace, or that run on
+ *   one device from several host threads at once (they share the side
+ *   streams), must be serialised by the caller.
+ *   Errors: CPATTN_ERR_INVALID_ARG for shapes as cpattn_ring_fwd, a parts
+ *   value that does not divide Hkv or is outside 0..8, or a NULL buffer;
+ *   CPATTN_ERR_WORKSPACE; CPATTN_ERR_CUDA when a copy or launch fails (the
+ *   caller's stream still waits for what was enqueued).
  */
 CPATTN_API size_t cpattn_attention_host_workspace_bytes(int B, int H, int Hkv, int S, int D,
                                                         int cp_size, int layout, int dtype,
                                                         int backward);
+/* The number of parts cpattn_attention_host takes for parts = 0 (host only;
+ * 1 for shapes it would reject). */
+CPATTN_API int cpattn_attention_host_parts(int B, int H, int Hkv, int S, int D);
 CPATTN_API int cpattn_attention_host(const void* q, const void* k, const void* v,
                                      const void* dout, void* out, float* lse, void* dq, void* dk,
                                      void* dv, int B, int H, int Hkv, int S, int D, int cp_size,
                                      int layout, int causal, int dtype, float softmax_scale,
-                                     void* workspace, size_t workspace_bytes,
+                                     int parts, void* workspace, size_t workspace_bytes,
                                      cpattn_stream_t stream);
 
 /*

@@ -156,6 +156,24 @@ def test_invalid_arguments_rejected_before_launch():
     # padded permute: real length above the padded one
     assert lib.cpattn_zigzag_permute_pad(fake, ctypes.c_void_p(0x90000), 1, 65, 64, 16, 4, 1,
                                          null) == E
+    # host path: parts must divide Hkv and lie in 0..8; workspace checked next
+    host = lib.cpattn_attention_host
+    hneed = lib.cpattn_attention_host_workspace_bytes(*good, 1)
+    assert hneed > 0
+    for parts in (3, -1, 9):
+        assert host(*args9, *good, 0.0, parts, fake, hneed, null) == E, parts
+    assert host(*args9, *good, 0.0, 2, null, hneed, null) == _binding.ERR_WORKSPACE
+    assert host(*args9, *good, 0.0, 2, ctypes.c_void_p(0x1010), hneed, null) == \
+        _binding.ERR_WORKSPACE  # not 256-byte aligned
+
+
+def test_host_parts_choice():
+    lib = cp_attn.lib()
+    assert lib.cpattn_attention_host_parts(1, 32, 8, 131072, 128) == 4   # 1 GiB of Q, Hkv 8
+    assert lib.cpattn_attention_host_parts(1, 32, 2, 131072, 128) == 2   # Hkv 2
+    assert lib.cpattn_attention_host_parts(1, 32, 1, 131072, 128) == 1   # one kv head
+    assert lib.cpattn_attention_host_parts(1, 4, 2, 2048, 128) == 1      # small
+    assert lib.cpattn_attention_host_parts(1, 4, 3, 2048, 128) == 1      # invalid shape
 
 
 @pytest.mark.parametrize("layout", [_binding.CONTIGUOUS, _binding.ZIGZAG])

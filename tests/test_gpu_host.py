@@ -22,17 +22,22 @@ CASES = [
     (2, 4, 1, 1536, 128, 3, cpa.ZIGZAG, True, torch.bfloat16, None),
     (1, 2, 2, 2048, 128, 2, cpa.CONTIGUOUS, False, torch.bfloat16, torch.float32),
     (2, 2, 2, 256, 64, 2, cpa.ZIGZAG, True, torch.float32, None),
+    (1, 8, 4, 2048, 128, 4, cpa.ZIGZAG, True, torch.bfloat16, torch.float32),
 ]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "B{}H{}K{}S{}D{}cp{}L{}c{}".format(*c[:8]))
 @pytest.mark.parametrize("backward", [True, False])
-def test_host_path_equals_device_path(case, backward):
+@pytest.mark.parametrize("split", ["one", "most"])
+def test_host_path_equals_device_path(case, backward, split):
+    # "most": as many head parts as the kv heads allow (each part one kv
+    # head), so the pipelined per-part copies and launches are exercised.
     B, H, Hkv, S, D, cp, layout, causal, dtype, gdt = case
+    parts = 1 if split == "one" else Hkv
     w = inputs.Workload("host", B, H, Hkv, S, D, cp, layout, causal, dtype, seed=9000 + S)
     q, k, v, do = inputs.generate(w, with_dout=True, pin=True)
     res = cpa.attention_host(q, k, v, do if backward else None, cp, layout, causal,
-                             grad_dtype=gdt)
+                             grad_dtype=gdt, parts=parts)
     torch.cuda.synchronize()
     dev = [x.cuda() for x in (q, k, v, do)]
     if backward:
@@ -68,4 +73,18 @@ def test_host_path_repeated_calls_reuse_workspace():
     torch.cuda.synchronize()
     for a, b in zip(outs, first):
         assert torch.equal(a, b)
+    assert cpa.device_status() == 0
+
+
+def test_host_parts_choice_and_rejects():
+    # The automatic choice: 4 parts for the S=131072 problem (8 kv heads),
+    # one for small tensors; a parts value that does not divide Hkv is an
+    # argument error.
+    assert cpa.attention_host_parts(1, 32, 8, 131072, 128) == 4
+    assert cpa.attention_host_parts(1, 4, 2, 2048, 128) == 1
+    q = torch.zeros((1, 512, 4, 64), dtype=torch.bfloat16).pin_memory()
+    k = torch.zeros((1, 512, 2, 64), dtype=torch.bfloat16).pin_memory()
+    for bad in (3, 9, -1):
+        with pytest.raises(cpa.CpattnError):
+            cpa.attention_host(q, k, k, None, 2, parts=bad)
     assert cpa.device_status() == 0
