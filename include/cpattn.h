@@ -385,8 +385,9 @@ CPATTN_API int64_t cpattn_padded_length(int64_t S, int cp_size, int layout);
  * (cpattn_ring_bwd).  The zigzag permutation happens in the copies (one copy
  * per chunk and batch row).
  *   parts: the heads are processed in `parts` groups of whole kv-head groups
- *   (parts must divide Hkv; 1..8; 0 = the library's choice: 4 or 2 when Hkv
- *   allows and one query tensor is at least 64 MiB, else 1).  A part's
+ *   (parts must divide Hkv; 1..8; 0 = the library's choice: the largest of
+ *   8, 4, 2 that divides Hkv and leaves each part at least 64 MiB of bf16
+ *   queries, else 1).  A part's
  *   inputs upload while the previous part computes and its results download
  *   while the next one computes, on two side streams (upload, download) the
  *   library creates once per device; only the first part's upload and the

@@ -169,7 +169,8 @@ def test_invalid_arguments_rejected_before_launch():
 
 def test_host_parts_choice():
     lib = cp_attn.lib()
-    assert lib.cpattn_attention_host_parts(1, 32, 8, 131072, 128) == 4   # 1 GiB of Q, Hkv 8
+    assert lib.cpattn_attention_host_parts(1, 32, 8, 131072, 128) == 8   # 1 GiB of Q, Hkv 8
+    assert lib.cpattn_attention_host_parts(1, 32, 8, 16384, 128) == 2    # 128 MiB of Q
     assert lib.cpattn_attention_host_parts(1, 32, 2, 131072, 128) == 2   # Hkv 2
     assert lib.cpattn_attention_host_parts(1, 32, 1, 131072, 128) == 1   # one kv head
     assert lib.cpattn_attention_host_parts(1, 4, 2, 2048, 128) == 1      # small

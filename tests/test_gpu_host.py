@@ -77,10 +77,10 @@ def test_host_path_repeated_calls_reuse_workspace():
 
 
 def test_host_parts_choice_and_rejects():
-    # The automatic choice: 4 parts for the S=131072 problem (8 kv heads),
+    # The automatic choice: 8 parts for the S=131072 problem (8 kv heads),
     # one for small tensors; a parts value that does not divide Hkv is an
     # argument error.
-    assert cpa.attention_host_parts(1, 32, 8, 131072, 128) == 4
+    assert cpa.attention_host_parts(1, 32, 8, 131072, 128) == 8
     assert cpa.attention_host_parts(1, 4, 2, 2048, 128) == 1
     q = torch.zeros((1, 512, 4, 64), dtype=torch.bfloat16).pin_memory()
     k = torch.zeros((1, 512, 2, 64), dtype=torch.bfloat16).pin_memory()
