@@ -88,3 +88,20 @@ def test_host_parts_choice_and_rejects():
         with pytest.raises(cpa.CpattnError):
             cpa.attention_host(q, k, k, None, 2, parts=bad)
     assert cpa.device_status() == 0
+
+
+def test_host_path_full_size_equals_device_path():
+    # The S=131072 step that the end-to-end bench line times, through the
+    # host path with the automatic number of head parts (8): bit for bit the
+    # device path's results.
+    w = inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"]
+    q, k, v, do = inputs.generate(w, pin=True)
+    B, S, H, D = q.shape
+    assert cpa.attention_host_parts(B, H, k.shape[2], S, D) == 8
+    res = cpa.attention_host(q, k, v, do, w.cp, w.layout, w.causal, grad_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = cpa.attention_fwd_bwd(*(x.cuda() for x in (q, k, v, do)), w.cp, w.layout, w.causal,
+                                grad_dtype=torch.float32)
+    for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), res, ref):
+        assert torch.equal(a, b.cpu()), name
+    assert cpa.device_status() == 0
