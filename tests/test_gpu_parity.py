@@ -5,8 +5,12 @@ Bars (element-wise, max abs error, GPU outputs upcast to fp64):
   * float32 inputs: O <= 1e-4, LSE <= 1e-5 (gradients: 1e-4);
   * bf16 inputs, fp32 accumulation: O, dQ, dK, dV <= 2e-2, LSE <= 1e-3.
 Small problems are compared in full; the named workloads at full size are
-compared on sampled rows that the oracle evaluates one by one (every chunk's
-first and last row among them), plus properties that hold at any size.
+compared on rows that the oracle evaluates one by one: whole heads where the
+oracle's cost allows (S=8192: two heads; S=32768: one kv group, i.e. its
+four query heads; S=16384 full attention: one head at every ring size),
+32-256 rows of every head, every chunk's first and last rows, and for
+S=131072 the first and last 32 rows of every chunk of one head; plus
+properties that hold at any size.
 """
 import numpy as np
 import pytest
@@ -307,9 +311,25 @@ def sample_rows(w, per_head, seed):
     return np.array(rows, dtype=np.int64)
 
 
-def check_rows(w, out, lse, q, k, v, rows):
-    """q, k, v: float32 numpy arrays (natural order)."""
-    ro, rl = oracle.attn_fwd_rows(q, k, v, rows, causal=w.causal)
+def full_rows(w, heads):
+    """Every query row of the given (b, h) heads."""
+    return np.array([(b, h, i) for b, h in heads for i in range(w.S)], dtype=np.int64)
+
+
+def band_rows(w, b, h, width):
+    """The first and last `width` rows of every chunk of head (b, h)."""
+    nchunk = w.cp * (2 if w.layout == cpa.ZIGZAG else 1)
+    c = w.S // nchunk
+    idx = sorted({x for ch in range(nchunk)
+                  for x in list(range(ch * c, ch * c + width)) +
+                  list(range(ch * c + c - width, ch * c + c))})
+    return np.array([(b, h, i) for i in idx], dtype=np.int64)
+
+
+def check_rows(w, out, lse, q, k, v, rows, ref=None):
+    """q, k, v: float32 numpy arrays (natural order); ref: the oracle's
+    (O, LSE) on these rows, if already computed."""
+    ro, rl = oracle.attn_fwd_rows(q, k, v, rows, causal=w.causal) if ref is None else ref
     b, h, i = rows[:, 0], rows[:, 1], rows[:, 2]
     go = out[b, i, h].double().cpu().numpy()
     gl = lse[b, h, i].double().cpu().numpy()
@@ -323,7 +343,9 @@ def test_c2_full_size(layout):
     w = inputs.WORKLOADS["c2_bf16_s8192"].with_(layout=layout)
     q, k, v, _ = inputs.generate(w)
     out, lse = cpa.attention(q.to(DEV), k.to(DEV), v.to(DEV), w.cp, w.layout, w.causal)
-    check_rows(w, out, lse, f32(q), f32(k), f32(v), sample_rows(w, 8, 1))
+    # Two heads in full, 64 rows of every head.
+    rows = np.concatenate([full_rows(w, [(0, 0), (0, 17)]), sample_rows(w, 64, 1)])
+    check_rows(w, out, lse, f32(q), f32(k), f32(v), rows)
     assert cpa.device_status() == 0
 
 
@@ -340,21 +362,28 @@ def test_c3_full_size():
     w = inputs.WORKLOADS["c3_bf16_s32768_gqa"]
     q, k, v, _ = inputs.generate(w)
     out, lse = cpa.attention(q.to(DEV), k.to(DEV), v.to(DEV), w.cp, w.layout, w.causal)
-    check_rows(w, out, lse, f32(q), f32(k), f32(v), sample_rows(w, 8, 3))
+    # One kv group of the second batch row in full (its four query heads),
+    # 64 rows of every (b, h).
+    grp = w.H // w.Hkv
+    rows = np.concatenate([full_rows(w, [(1, 3 * grp + j) for j in range(grp)]),
+                           sample_rows(w, 64, 3)])
+    check_rows(w, out, lse, f32(q), f32(k), f32(v), rows)
     assert cpa.device_status() == 0
 
 
 def test_c4_full_size_cp_sweep_and_merge():
     w = inputs.WORKLOADS["c4_bf16_s16384_bidir"]
     q, k, v, _ = inputs.generate(w)
-    rows = sample_rows(w, 8, 4)
+    # One head in full, 32 rows of every head, at every ring size.
+    rows = np.concatenate([full_rows(w, [(0, 5)]), sample_rows(w, 32, 4)])
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     q, k, v = f32(q), f32(k), f32(v)
+    oref = oracle.attn_fwd_rows(q, k, v, rows, causal=w.causal)
     ref = None
     for cp in w.cp_sweep:
         wc = w.with_(cp=cp)
         out, lse = cpa.attention(qd, kd, vd, cp, w.layout, w.causal)
-        check_rows(wc, out, lse, q, k, v, rows)
+        check_rows(wc, out, lse, q, k, v, rows, oref)
         if ref is None:
             ref = (out, lse)
         else:
@@ -370,7 +399,7 @@ def test_c4_full_size_cp_sweep_and_merge():
         ml = cpa.zigzag_unpermute(acc_l, cp, w.layout, seq_dim=2)
         assert (mo - out.float()).abs().max().item() <= 2e-2
         assert (ml - lse).abs().max().item() <= 1e-3
-        check_rows(wc, mo, ml, q, k, v, rows)
+        check_rows(wc, mo, ml, q, k, v, rows, oref)
     assert cpa.device_status() == 0
 
 
@@ -382,13 +411,16 @@ def test_c5_full_size_forward_backward():
     # where one bf16 rounding alone exceeds the 2e-2 bar.
     out, lse, dq, dk, dv = cpa.attention_fwd_bwd(qd, kd, vd, dod, w.cp, w.layout, w.causal,
                                                  grad_dtype=torch.float32)
-    rows = sample_rows(w, 6, 5)
+    # 256 rows of every head, and the first and last 32 rows of every chunk
+    # of one head (the rows next to the ring's chunk borders).
+    rows = np.concatenate([sample_rows(w, 256, 5), band_rows(w, 0, 21, 32)])
     qf, kf, vf = f32(q), f32(k), f32(v)
     check_rows(w, out, lse, qf, kf, vf, rows)
     del out, lse
-    # dQ rows are row-local: exact oracle on sampled rows.
-    rdq = oracle.attn_bwd_dq_rows(qf, kf, vf, f32(do), rows, causal=True)
-    gdq = dq[rows[:, 0], rows[:, 2], rows[:, 1]].double().cpu().numpy()
+    # dQ rows are row-local: exact oracle on 512 of the sampled rows.
+    sub = rows[np.random.default_rng(6).choice(len(rows), 512, replace=False)]
+    rdq = oracle.attn_bwd_dq_rows(qf, kf, vf, f32(do), sub, causal=True)
+    gdq = dq[sub[:, 0], sub[:, 2], sub[:, 1]].double().cpu().numpy()
     assert np.max(np.abs(gdq - rdq)) <= 2e-2, np.max(np.abs(gdq - rdq))
     # Sum rules at full size: sum_j dV_j = sum over the group's heads of sum_i dO_i,
     # sum_j dK_j = 0 (per kv head and feature); bf16 rounding of S terms bounds them.
