@@ -1,6 +1,7 @@
 """The host-buffer entry point (cpattn_attention_host): natural-order host
 tensors in and out, with the permutation done by the chunked copies and the
-dO upload / O download overlapped on a side stream.  It runs the same
+heads in pipelined parts (uploads and downloads on two side streams,
+overlapping the neighbouring parts' kernels).  It runs the same
 kernels as the device path, so its results must equal, bit for bit, the
 device path's (cpattn_zigzag_permute -> ring forward -> ring backward ->
 cpattn_zigzag_unpermute); the device path itself is checked against the
