@@ -343,18 +343,22 @@ def run_ours(args):
         if docs is None:
             e2e["head_parts"] = cpa.attention_host_parts(B, H, Hkv, S, D)
 
-    # Roofline of the dominant kernel, from the live event timings.
+    # Roofline of the dominant kernel, from the live event timings.  The
+    # kernels of the step are timed inside the multi-second loop of back-to-back
+    # steps, so the denominator is the sustained bf16 figure; the burst one is
+    # reported beside it.
     dom_ms, dom_flops, dom_name = (bwd_ms, bwd_flops, "ring_bwd") \
         if (w.backward and bwd_ms >= fwd_ms) else (fwd_ms, fwd_flops, "ring_fwd")
     achieved = dom_flops / (dom_ms * 1e-3) / 1e12
     traffic = CAPTURED_TRAFFIC.get(w.name, {}).get(dom_name)
-    roofline = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                "peak_kind": f"{peak_kind} bf16 burst", "ms": dom_ms,
-                "frac_of_sustained": achieved / peak_sus}
+    roofline = {"kernel": dom_name, "bound": "tensor", "achieved": achieved, "peak": peak_sus,
+                "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
+                "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside the step loop)",
+                "ms": dom_ms, "peak_burst": peak, "frac_of_burst": achieved / peak}
     fwd_info = {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
                 "traffic": CAPTURED_TRAFFIC.get(w.name, {}).get("ring_fwd")}
-    fwd_info["frac"] = fwd_info["tflops"] / peak
+    fwd_info["frac"] = fwd_info["tflops"] / peak_sus
+    fwd_info["frac_of_burst"] = fwd_info["tflops"] / peak
     if w.backward:
         fwd_info["bwd_ms"] = bwd_ms
         fwd_info["bwd_tflops"] = bwd_flops / (bwd_ms * 1e-3) / 1e12
