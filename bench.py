@@ -298,30 +298,27 @@ def run_ours(args):
         host_outs = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
         h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo) if x is not None)
         d2h = sum(x.numel() * x.element_size() for x in outs)
+        hcode = (cpa.BF16 if w.dtype == torch.bfloat16 else cpa.F32) | \
+            (cpa.GRAD_F32 if w.backward else 0)
+        hres = dict(zip(("out", "lse", "dq", "dk", "dv"), host_outs))
         if docs is None:
             e2e_api = "cpattn_attention_host"
-            hcode = (cpa.BF16 if w.dtype == torch.bfloat16 else cpa.F32) | \
-                (cpa.GRAD_F32 if w.backward else 0)
             hws = torch.empty(cpa.attention_host_workspace_bytes(B, H, Hkv, S, D, cp, layout, hcode,
                                                                  w.backward),
                               device=dev, dtype=torch.uint8)
-            hres = dict(zip(("out", "lse", "dq", "dk", "dv"), host_outs))
 
             def e2e_step():
                 cpa.attention_host(hq, hk, hv, hdo, cp, layout, causal, workspace=hws,
                                    grad_dtype=gdt if w.backward else None, **hres)
         else:
-            e2e_api = "torch copies around the document-rule step"
-            dq_in = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd), \
-                (torch.empty_like(dod) if dod is not None else None)
+            e2e_api = "cpattn_attention_host_docs"
+            hws = torch.empty(cpa.attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout,
+                                                                      hcode, w.backward),
+                              device=dev, dtype=torch.uint8)
 
             def e2e_step():
-                for dst, src in zip(dq_in, (hq, hk, hv, hdo)):
-                    if src is not None:
-                        dst.copy_(src, non_blocking=True)
-                step(src=dq_in)
-                for dst, src in zip(host_outs, outs):
-                    dst.copy_(src, non_blocking=True)
+                cpa.attention_host_docs(hq, hk, hv, hdo, cp, docs, layout, causal, workspace=hws,
+                                        grad_dtype=gdt if w.backward else None, **hres)
 
         e2e_step()
         barrier()
@@ -340,8 +337,7 @@ def run_ours(args):
         e2e = {"value": step_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "ms_per_step": e2e_ms, "ms_per_call": per_call, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "api": e2e_api, "clocks": e2e_clk}
-        if docs is None:
-            e2e["head_parts"] = cpa.attention_host_parts(B, H, Hkv, S, D)
+        e2e["head_parts"] = cpa.attention_host_parts(B, H, Hkv, S, D)
 
     # Roofline of the dominant kernel, from the live event timings.  The
     # kernels of the step are timed inside the multi-second loop of back-to-back

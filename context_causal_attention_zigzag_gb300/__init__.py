@@ -14,4 +14,5 @@ from ._binding import (  # noqa: F401
     ring_fwd_step, status_string, tile_counts, zigzag_permute, zigzag_permute_pad,
     zigzag_unpermute, zigzag_unpermute_pad, kv_allgather, ulysses_a2a, ulysses_fwd, ulysses_bwd,
     ulysses_workspace_bytes, attention_ulysses_fwd_bwd, attention_host,
-    attention_host_workspace_bytes, attention_host_parts, wait_probe)
+    attention_host_workspace_bytes, attention_host_parts, attention_host_docs,
+    attention_host_docs_workspace_bytes, wait_probe)

@@ -49,6 +49,8 @@ SIGNATURES = {
     "cpattn_ulysses_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_attention_host_workspace_bytes": (_sz, [_i] * 9),
     "cpattn_attention_host_parts": (_i, [_i] * 5),
+    "cpattn_attention_host_docs_workspace_bytes": (_sz, [_i] * 9),
+    "cpattn_attention_host_docs": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _i, _i, _vp, _sz, _vp]),
     "cpattn_attention_host": (_i, [_vp] * 9 + [_i] * 9 + [_f, _i, _vp, _sz, _vp]),
     "cpattn_ring_fwd": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp]),
     "cpattn_ring_fwd_census": (_i, [_vp, _vp, _vp, _vp, _vp] + [_i] * 9 + [_f, _vp, _vp]),
@@ -747,4 +749,58 @@ def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, ou
                                      int(layout), int(bool(causal)), code, _scale(scale),
                                      int(parts), _ptr(workspace), workspace.numel(), st)
     _check("cpattn_attention_host", rc)
+    return (out, lse, dq, dk, dv) if backward else (out, lse)
+
+
+def attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout=ZIGZAG, dtype=BF16,
+                                        backward=True) -> int:
+    return int(lib().cpattn_attention_host_docs_workspace_bytes(B, H, Hkv, S, D, int(cp),
+                                                                int(layout), int(dtype),
+                                                                int(bool(backward))))
+
+
+def attention_host_docs(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causal=True,
+                        scale=None, out=None, lse=None, dq=None, dk=None, dv=None,
+                        grad_dtype=None, workspace=None, device=None, stream=None, parts=0):
+    """cpattn_attention_host_docs: attention_host for packed documents and any
+    sequence length.  cu_seqlens: document offsets over the S tokens (a
+    sequence of ints, 0 ... S), None for one document.  Returns (out, lse) or
+    (out, lse, dq, dk, dv) as CPU tensors over the S real tokens."""
+    if q.is_cuda or k.is_cuda or v.is_cuda:
+        raise ValueError("attention_host_docs takes host (CPU) tensors")
+    for t in (q, k, v, dout):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensor must be contiguous")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
+    code = _dtype_code(q)
+    backward = dout is not None
+    gdt = q.dtype if grad_dtype is None else grad_dtype
+    if backward and gdt == torch.float32 and q.dtype != torch.float32:
+        code |= GRAD_F32
+    pin = q.is_pinned()
+
+    def host(shape, dtype, t):
+        return torch.empty(shape, dtype=dtype, pin_memory=pin) if t is None else t
+    out = host(q.shape, q.dtype, out)
+    lse = host((B, H, S), torch.float32, lse)
+    if backward:
+        dq = host(q.shape, gdt, dq)
+        dk = host(k.shape, gdt, dk)
+        dv = host(v.shape, gdt, dv)
+    need = attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout, code, backward)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
+    cu_arr, ndocs = None, 0
+    if cu_seqlens is not None:
+        cu_list = [int(x) for x in cu_seqlens]
+        cu_arr, ndocs = (ctypes.c_int32 * len(cu_list))(*cu_list), len(cu_list) - 1
+    st = ctypes.c_void_p((stream or torch.cuda.current_stream(dev)).cuda_stream)
+    rc = lib().cpattn_attention_host_docs(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk),
+        _ptr(dv), B, H, Hkv, S, D, int(cp), int(layout), int(bool(causal)), code, _scale(scale),
+        ctypes.cast(cu_arr, ctypes.c_void_p) if cu_arr is not None else None, ndocs, int(parts),
+        _ptr(workspace), workspace.numel(), st)
+    _check("cpattn_attention_host_docs", rc)
     return (out, lse, dq, dk, dv) if backward else (out, lse)

@@ -422,6 +422,31 @@ CPATTN_API int cpattn_attention_host(const void* q, const void* k, const void* v
                                      cpattn_stream_t stream);
 
 /*
+ * cpattn_attention_host for packed documents and any sequence length: q, k,
+ * v (and dout), out, lse (and dq, dk, dv) hold S real tokens in natural
+ * order on the host ([B, S, H, D], lse [B, H, S]); on the device the
+ * sequence is padded to cpattn_padded_length(S, cp_size, layout) (the
+ * padding is one more document, zero on the device and never copied back)
+ * and the ring runs under the document rule (cpattn_ring_fwd_docs /
+ * cpattn_ring_bwd_docs).
+ *   cu_seqlens: HOST int32 [ndocs + 1], 0 = cu[0] < ... < cu[ndocs] = S
+ *   (checked here: CPATTN_ERR_INVALID_ARG otherwise), or NULL for one
+ *   document.  Read before the call returns.
+ *   workspace: at least cpattn_attention_host_docs_workspace_bytes.
+ *   Everything else as cpattn_attention_host.
+ */
+CPATTN_API size_t cpattn_attention_host_docs_workspace_bytes(int B, int H, int Hkv, int S, int D,
+                                                             int cp_size, int layout, int dtype,
+                                                             int backward);
+CPATTN_API int cpattn_attention_host_docs(const void* q, const void* k, const void* v,
+                                          const void* dout, void* out, float* lse, void* dq,
+                                          void* dk, void* dv, int B, int H, int Hkv, int S,
+                                          int D, int cp_size, int layout, int causal, int dtype,
+                                          float softmax_scale, const int32_t* cu_seqlens,
+                                          int ndocs, int parts, void* workspace,
+                                          size_t workspace_bytes, cpattn_stream_t stream);
+
+/*
  * Closed-form work census of the ring (host only): for every rank r and
  * step t, the number of tile x tile blocks with at least one visible
  * (query, key) pair, tiles_rt[r*cp_size + t], and the number of visible

@@ -167,6 +167,23 @@ def test_invalid_arguments_rejected_before_launch():
         _binding.ERR_WORKSPACE  # not 256-byte aligned
 
 
+def test_host_docs_rejects_bad_offsets_before_any_copy():
+    lib = cp_attn.lib()
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(0x1000)
+    E = _binding.ERR_INVALID_ARG
+    args9 = [fake] * 9
+    shape = [1, 4, 2, 100, 64, 2, 1, 1, 1]  # S = 100 real tokens, padded on the device
+    need = lib.cpattn_attention_host_docs_workspace_bytes(*shape, 1)
+    assert need > 0
+    for cu in ([0, 50, 40, 100], [0, 50, 99], [1, 50, 100], [0, 100, 100]):
+        arr = (ctypes.c_int32 * len(cu))(*cu)
+        rc = lib.cpattn_attention_host_docs(*args9, *shape, 0.0, ctypes.cast(arr, ctypes.c_void_p),
+                                            len(cu) - 1, 0, fake, need, null)
+        assert rc == E, cu
+    assert lib.cpattn_attention_host_docs(*args9, *shape, 0.0, null, 0, 3, fake, need, null) == E
+
+
 def test_host_parts_choice():
     lib = cp_attn.lib()
     assert lib.cpattn_attention_host_parts(1, 32, 8, 131072, 128) == 8   # 1 GiB of Q, Hkv 8

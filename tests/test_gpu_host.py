@@ -106,3 +106,44 @@ def test_host_path_full_size_equals_device_path():
     for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), res, ref):
         assert torch.equal(a, b.cpu()), name
     assert cpa.device_status() == 0
+
+
+DOC_CASES = [
+    # B, H, Hkv, S (real), D, cp, layout, causal, dtype, grad_dtype, cu_seqlens
+    (1, 4, 2, 1000, 128, 2, cpa.ZIGZAG, True, torch.bfloat16, torch.float32, [0, 300, 1000]),
+    (2, 4, 2, 777, 128, 3, cpa.CONTIGUOUS, True, torch.bfloat16, None, None),
+    (1, 2, 2, 333, 64, 3, cpa.ZIGZAG, False, torch.float32, None, [0, 1, 200, 333]),
+]
+
+
+@pytest.mark.parametrize("case", DOC_CASES, ids=lambda c: "B{}H{}K{}S{}D{}cp{}L{}c{}".format(*c[:8]))
+@pytest.mark.parametrize("backward", [True, False])
+@pytest.mark.parametrize("split", ["one", "most"])
+def test_host_docs_path_equals_device_docs_path(case, backward, split):
+    # Any length and packed documents from host buffers: the padded device
+    # sequence, the document rule, the real tokens back; the same results as
+    # the device path (attention_docs / attention_docs_fwd_bwd), bit for bit
+    # apart from the CUDA-core backward's atomic dQ.
+    B, H, Hkv, S, D, cp, layout, causal, dtype, gdt, cu = case
+    parts = 1 if split == "one" else Hkv
+    w = inputs.Workload("hostdocs", B, H, Hkv, S, D, cp, layout, causal, dtype, seed=9500 + S)
+    q, k, v, do = inputs.generate(w, with_dout=True, pin=True)
+    res = cpa.attention_host_docs(q, k, v, do if backward else None, cp, cu, layout, causal,
+                                  grad_dtype=gdt, parts=parts)
+    torch.cuda.synchronize()
+    dev = [x.cuda() for x in (q, k, v, do)]
+    if backward:
+        ref = cpa.attention_docs_fwd_bwd(*dev, cp, cu, layout, causal, grad_dtype=gdt)
+    else:
+        ref = cpa.attention_docs(*dev[:3], cp, cu, layout, causal)
+    Sp = cpa.padded_length(S, cp, layout)
+    path, _ = cpa.plan(B, H, Hkv, Sp, D, cp, layout, causal, dtype, backward=True)
+    assert len(res) == len(ref)
+    for name, a, b in zip(("out", "lse", "dq", "dk", "dv"), res, ref):
+        assert not a.is_cuda and a.dtype == b.dtype and a.shape == b.shape, name
+        if name == "dq" and path != cpa.PATH_TCGEN05:
+            bound = 1e-6 * (b.abs().max().item() + 1e-30) * Sp / 64
+            assert (a - b.cpu()).abs().max().item() <= bound, name
+        else:
+            assert torch.equal(a, b.cpu()), name
+    assert cpa.device_status() == 0
