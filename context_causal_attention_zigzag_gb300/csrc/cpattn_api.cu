@@ -356,8 +356,9 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
     e = launch_grad_reduce(reg_a, reg_b, dk, dv, B, S, H, Hkv, D, out_dtype, st);
     return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
   }
-  // CUDA cores: Delta and zeroed accumulators, the kernel, the conversion.
-  e = launch_bwd_prep(out, dout, delta, reg_a, reg_c, reg_d, n_kv, B, S, H, D, in_dtype, 1.f,
+  // CUDA cores: Delta, the dK/dV and dQ kernels (every accumulator element
+  // written once), the conversion.
+  e = launch_bwd_prep(out, dout, delta, nullptr, nullptr, nullptr, 0, B, S, H, D, in_dtype, 1.f,
                       st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   a.dq_acc = reg_a;

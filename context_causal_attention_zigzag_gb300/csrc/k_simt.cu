@@ -12,11 +12,16 @@
 // is spread over 256 threads as 4 x 4 blocks; row max and row sum are reduced
 // across the 16 threads of a row with warp shuffles.
 //
-// Backward: one CTA per (64 key rows of one source rank, batch*kv head).  It
-// follows its K/V tile around the ring (step t: receiving rank (s + t) mod
-// cp), over every query head of the group, recomputes P from the saved LSE
-// and accumulates dK, dV in registers (written to the float32 accumulators at
-// the end); dQ goes to its float32 accumulator with atomic adds.
+// Backward, two kernels, no atomics (every gradient element is written once,
+// so the result does not depend on scheduling):
+//   dK/dV: one CTA per (64 key rows of one source rank, batch*kv head).  It
+//   follows its K/V tile around the ring (step t: receiving rank (s + t) mod
+//   cp), over every query head of the group, recomputes P from the saved LSE
+//   and accumulates dK, dV in registers, written to the float32 accumulators
+//   at the end.
+//   dQ: one CTA per (64 query rows of one rank, batch*head), the forward's
+//   tile walk over the K/V of every ring step; P, dP and dS recomputed per
+//   tile, dQ in registers, written at the end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <limits.h>
@@ -414,38 +419,12 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
 #pragma unroll
             for (int dd = 0; dd < DV; ++dd) dk[i][dd] = fmaf(sv[i], qv[dd], dk[i][dd]);
         }
-        // dQ[q][d] += scale * sum_key dS[q][key] K[key][d]   (rows ty*4+i, d = tx+16dd)
-        float dq[4][DV];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int dd = 0; dd < DV; ++dd) dq[i][dd] = 0.f;
-#pragma unroll 4
-        for (int c = 0; c < BN; ++c) {
-          float sv[4], kv[DV];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) sv[i] = Ps[(ty * 4 + i) * PP + c];
-#pragma unroll
-          for (int dd = 0; dd < DV; ++dd) kv[dd] = Ks[c * DP + tx + 16 * dd];
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int dd = 0; dd < DV; ++dd) dq[i][dd] = fmaf(sv[i], kv[dd], dq[i][dd]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = ty * 4 + i;
-          if (row >= qn) continue;
-          float* dst = a.dq_acc + (((int64_t)b * sh.S + q0 + row) * sh.H + h) * D;
-#pragma unroll
-          for (int dd = 0; dd < DV; ++dd) atomicAdd(dst + tx + 16 * dd, sh.scale * dq[i][dd]);
-        }
       }
     }
   }
 
   // This CTA owns its key rows over every query: plain float32 stores into the
-  // accumulators (the pre-pass zeroed them; the conversion kernel follows).
+  // accumulators (the conversion kernel follows).
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int row = ty * 4 + i;
@@ -456,6 +435,161 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
       a.dk_acc[base + tx + 16 * dd] = sh.scale * dk[i][dd];
       a.dv_acc[base + tx + 16 * dd] = dv[i][dd];
     }
+  }
+}
+
+// dQ, query-major (see the file header).
+template <typename T, int D>
+__global__ void __launch_bounds__(NT) simt_dq_kernel(const BwdArgs a) {
+  constexpr int DP = D + 1, PP = BN + 1, DV = D / 16;
+  extern __shared__ float smem[];
+  float* Qs = smem;
+  float* Os = Qs + BM * DP;  // dO tile
+  float* Ks = Os + BM * DP;
+  float* Vs = Ks + BN * DP;
+  float* Ps = Vs + BN * DP;  // dS
+  __shared__ int q_lo[BM], q_hi[BM];  // key window of each query row
+  __shared__ int k_nat[BN];
+  __shared__ float lse2[BM];  // LSE in base 2
+  __shared__ float dlt[BM];
+  __shared__ int s_lo, s_hi;
+
+  const RingShape& sh = a.sh;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int nblk = (sh.L + BM - 1) / BM;
+  const int r = blockIdx.x / nblk, qb = blockIdx.x - r * nblk;
+  const int b = blockIdx.y / sh.H, h = blockIdx.y - b * sh.H;
+  const int g = h / (sh.H / sh.Hkv);
+  const int q0 = r * sh.L + qb * BM;
+  const int qn = min(BM, sh.L - qb * BM);
+  const T* qp = static_cast<const T*>(a.q);
+  const T* kp = static_cast<const T*>(a.k);
+  const T* vp = static_cast<const T*>(a.v);
+  const T* dop = static_cast<const T*>(a.dout);
+
+  load_tile<T, D>(Qs, qp, b, q0, qn, h, sh.H, sh.S);
+  load_tile<T, D>(Os, dop, b, q0, qn, h, sh.H, sh.S);
+  if (tid < BM) {
+    int lo = INT_MAX, hi = -1;  // padding rows see nothing
+    float l2 = 0.f, dl = 0.f;
+    if (tid < qn) {
+      query_window(sh, natural_pos(sh, q0 + tid), lo, hi);
+      const int64_t li = ((int64_t)b * sh.H + h) * sh.S + q0 + tid;
+      l2 = a.lse[li] * kLog2e;
+      dl = a.delta[li];
+    }
+    q_lo[tid] = lo;
+    q_hi[tid] = hi;
+    lse2[tid] = l2;
+    dlt[tid] = dl;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    int lo = min(q_lo[tid], q_lo[tid + 32]), hi = max(q_hi[tid], q_hi[tid + 32]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
+      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, off));
+    }
+    if (tid == 0) {
+      s_lo = lo;
+      s_hi = hi;
+    }
+  }
+  __syncthreads();
+  const int blk_lo = s_lo, blk_hi = s_hi;  // keys some row of the block sees
+
+  float dq[4][DV];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int dd = 0; dd < DV; ++dd) dq[i][dd] = 0.f;
+
+  // Ring: every step t, the shard of rank (r - t) mod cp.  All-gather
+  // (kv_natural): one pass over the whole K/V in natural order.
+  const bool nat_kv = sh.kv_natural != 0;
+  const int n_pass = nat_kv ? 1 : sh.cp;
+  for (int t = 0; t < n_pass; ++t) {
+    const int s = ring_source(r, t, sh.cp);
+    const int kbase = nat_kv ? 0 : s * sh.L, klen = nat_kv ? sh.S : sh.L;
+    for (int kb = 0; kb < klen; kb += BN) {
+      const int k0 = kbase + kb, kn = min(BN, klen - kb);
+      __syncthreads();  // the previous tile is fully consumed
+      int live = 0;
+      if (tid < BN) {
+        int kpos = tid < kn ? (nat_kv ? k0 + tid : natural_pos(sh, k0 + tid)) : INT_MAX;
+        k_nat[tid] = kpos;
+        live = tid < kn && kpos >= blk_lo && kpos <= blk_hi;
+      }
+      if (!__syncthreads_or(live)) continue;  // no row of the block sees the tile
+      load_tile<T, D>(Ks, kp, b, k0, kn, g, sh.Hkv, sh.S);
+      load_tile<T, D>(Vs, vp, b, k0, kn, g, sh.Hkv, sh.S);
+      __syncthreads();
+
+      float sc[4][4], dp[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[i][j] = dp[i][j] = 0.f;
+#pragma unroll 4
+      for (int d = 0; d < D; ++d) {
+        float qv[4], ov[4], kv[4], vv[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qv[i] = Qs[(ty * 4 + i) * DP + d];
+          ov[i] = Os[(ty * 4 + i) * DP + d];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          kv[j] = Ks[(tx + 16 * j) * DP + d];
+          vv[j] = Vs[(tx + 16 * j) * DP + d];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            sc[i][j] = fmaf(qv[i], kv[j], sc[i][j]);
+            dp[i][j] = fmaf(ov[i], vv[j], dp[i][j]);
+          }
+      }
+      // dS = P (dP - Delta) for this thread's 4 x 4 block (query rows
+      // ty*4+i, keys tx+16j), P from the saved LSE.
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = ty * 4 + i;
+        const int lo = q_lo[row], hi = q_hi[row];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int col = tx + 16 * j;
+          const bool ok = col < kn && k_nat[col] >= lo && k_nat[col] <= hi;
+          const float p = ok ? exp2f(sc[i][j] * sh.scale_log2 - lse2[row]) : 0.f;
+          Ps[row * PP + col] = p * (dp[i][j] - dlt[row]);
+        }
+      }
+      __syncthreads();
+      // dQ[q][d] += sum_key dS[q][key] K[key][d]   (rows ty*4+i, d = tx+16dd)
+#pragma unroll 4
+      for (int c = 0; c < BN; ++c) {
+        float sv[4], kv[DV];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sv[i] = Ps[(ty * 4 + i) * PP + c];
+#pragma unroll
+        for (int dd = 0; dd < DV; ++dd) kv[dd] = Ks[c * DP + tx + 16 * dd];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int dd = 0; dd < DV; ++dd) dq[i][dd] = fmaf(sv[i], kv[dd], dq[i][dd]);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = ty * 4 + i;
+    if (row >= qn) continue;
+    float* dst = a.dq_acc + (((int64_t)b * sh.S + q0 + row) * sh.H + h) * D;
+#pragma unroll
+    for (int dd = 0; dd < DV; ++dd) dst[tx + 16 * dd] = sh.scale * dq[i][dd];
   }
 }
 
@@ -475,11 +609,19 @@ template <typename T, int D>
 cudaError_t bwd_as(const BwdArgs& a, cudaStream_t stream) {
   constexpr int smem = bwd_smem_bytes<D>();
   auto kern = simt_bwd_kernel<T, D>;
+  auto kern_dq = simt_dq_kernel<T, D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern_dq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nblk = (a.sh.L + BN - 1) / BN;
   dim3 grid(a.sh.kv_natural ? (a.sh.S + BN - 1) / BN : nblk * a.sh.cp, a.sh.B * a.sh.Hkv);
   kern<<<grid, NT, smem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int qblk = (a.sh.L + BM - 1) / BM;
+  dim3 grid_dq(qblk * a.sh.cp, a.sh.B * a.sh.H);
+  kern_dq<<<grid_dq, NT, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -124,9 +124,9 @@ def test_backward_docs_matches_oracle(case):
     tol = TOL[dtype]["grad"]
     for name, got, ref in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
         assert maxerr(got, ref) <= tol, (name, maxerr(got, ref))
-    Sp = cpa.padded_length(S, cp, layout)
-    path, _ = cpa.plan(B, H, Hkv, Sp, D, cp, layout, causal, dtype, backward=True)
-    if path == cpa.PATH_TCGEN05:  # deterministic kernels (no atomics)
+    if dtype == torch.bfloat16:
+        # Both backward paths write every gradient element once (no atomics),
+        # so bf16 gradients are the float32 ones rounded, bit for bit.
         _, _, bq, bk, bv = cpa.attention_docs_fwd_bwd(q, k, v, do, cp, cu, layout, causal)
         for a, b in ((bq, dq), (bk, dk), (bv, dv)):
             assert a.dtype == torch.bfloat16 and torch.equal(a, b.to(torch.bfloat16))
