@@ -281,3 +281,37 @@ def test_docs_full_size_forward_backward():
     assert maxerr(dk2[0, krows[:, 2], krows[:, 1]], rdk) <= 2e-2
     assert maxerr(dv2[0, krows[:, 2], krows[:, 1]], rdv) <= 2e-2
     assert cpa.device_status() == 0
+
+
+def test_many_short_documents_s32768():
+    # 32768 tokens packed with 320 documents of mean length 100: most tiles
+    # hold no visible pair and most visited tiles are cut by a border.
+    # Forward rows and dQ rows against the oracle (every document's first
+    # and last row of one head, random rows of every head), and dK / dV of
+    # whole documents against the oracle run on each document alone
+    # (documents are independent, so that is exact).
+    B, H, Hkv, S, D, cp = 1, 8, 2, 32768, 128, 8
+    cu = inputs.packed_doc_offsets(S, 100, seed=77)
+    q, k, v, do = make(B, H, Hkv, S, D, torch.bfloat16, seed=7700, dout=True)
+    qd, kd, vd, dod = (x.to(DEV) for x in (q, k, v, do))
+    o, lse, dq, dk, dv = cpa.attention_docs_fwd_bwd(qd, kd, vd, dod, cp, cu, cpa.ZIGZAG, True,
+                                                    grad_dtype=torch.float32)
+    assert cpa.device_status() == 0
+    rng = np.random.default_rng(78)
+    rows = [(0, 3, i) for i in sorted(set(cu[:-1]) | {x - 1 for x in cu[1:]})]
+    rows += [(0, h, int(i)) for h in range(H) for i in rng.integers(0, S, 128)]
+    rows = np.array(rows, dtype=np.int64)
+    fq, fk, fv, fdo = f32(q), f32(k), f32(v), f32(do)
+    ro, rl = oracle.attn_fwd_rows_docs(fq, fk, fv, rows, cu)
+    assert maxerr(o[0, rows[:, 2], rows[:, 1]], ro) <= 2e-2
+    assert maxerr(lse[0, rows[:, 1], rows[:, 2]], rl) <= 1e-3
+    rdq = oracle.attn_bwd_dq_rows_docs(fq, fk, fv, fdo, rows, cu)
+    assert maxerr(dq[0, rows[:, 2], rows[:, 1]], rdq) <= 2e-2
+    ndoc = len(cu) - 1
+    picks = sorted({0, ndoc - 1} | set(rng.choice(ndoc, 24, replace=False).tolist()))
+    for d in picks:
+        a, b = cu[d], cu[d + 1]
+        _, rk, rv = oracle.attn_bwd(fq[:, a:b], fk[:, a:b], fv[:, a:b], fdo[:, a:b], causal=True)
+        assert maxerr(dk[:, a:b], rk) <= 2e-2, ("dk", d, maxerr(dk[:, a:b], rk))
+        assert maxerr(dv[:, a:b], rv) <= 2e-2, ("dv", d, maxerr(dv[:, a:b], rv))
+    assert cpa.device_status() == 0

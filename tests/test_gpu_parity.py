@@ -469,3 +469,28 @@ def test_balance_report_kernel_census():
     for name in ("zigzag", "contiguous"):
         assert r[name]["kernel_equals_closed_form"], name
     assert r["zigzag"]["kernel"]["worst_step_max_over_mean"] == 1.0
+
+
+def test_gqa_32_query_heads_on_one_kv_head():
+    # The widest grouping: 32 query heads share one kv head (the dK / dV
+    # kernel's per-head partials summed over 32 slots).  Whole-tensor
+    # comparison with the oracle at S=2048.  O, LSE and dQ are per query head
+    # and keep the plain bars.  dK / dV add 32 per-head partials, each
+    # carrying the bf16 rounding of dS / P before its MMA: their magnitude
+    # and their error grow like sqrt(group), so their bar is 2e-2 scaled by
+    # sqrt(group / 4) (the five named workloads have groups of at most 4),
+    # and they must also stay within 1 % of the largest |dK| / |dV|.
+    B, H, Hkv, S, D, cp = 1, 32, 1, 2048, 128, 4
+    w, q, k, v, do = make(B, H, Hkv, S, D, cp, cpa.ZIGZAG, True, torch.bfloat16, 88, dout=True)
+    out, lse, dq, dk, dv = cpa.attention_fwd_bwd(q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV), cp,
+                                                 cpa.ZIGZAG, True, grad_dtype=torch.float32)
+    ro, rl = oracle.attn_fwd(f32(q), f32(k), f32(v), causal=True)
+    rq, rk, rv = oracle.attn_bwd(f32(q), f32(k), f32(v), f32(do), causal=True)
+    assert maxerr(out, ro) <= 2e-2 and maxerr(lse, rl) <= 1e-3
+    assert maxerr(dq, rq) <= 2e-2, maxerr(dq, rq)
+    group_bar = 2e-2 * np.sqrt((H // Hkv) / 4)
+    for name, got, ref in (("dk", dk, rk), ("dv", dv, rv)):
+        err = maxerr(got, ref)
+        assert err <= group_bar, (name, err)
+        assert err <= 1e-2 * np.max(np.abs(ref)), (name, err, np.max(np.abs(ref)))
+    assert cpa.device_status() == 0
