@@ -374,6 +374,9 @@ def run_ours(args):
     if docs is None and not args.no_allgather and w.backward:
         ag_info = time_allgather(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
                                  (qs, ks, vs, dos))
+    hbm_info = None
+    if not args.no_hbm:
+        hbm_info = time_hbm_kernels(cpa, w, dev, stream, args.warmup, max(args.steps, 5), hbm)
     ul_info = None
     if docs is None and not args.no_ulysses and w.backward:
         ul_info = time_ulysses(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
@@ -399,7 +402,7 @@ def run_ours(args):
                    "useful_tflop_per_step": step_flops / 1e12},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
         "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "docs": docs_info,
-        "allgather": ag_info, "ulysses": ul_info,
+        "allgather": ag_info, "ulysses": ul_info, "hbm_kernels": hbm_info,
         "cpu_baseline": cpu,
         "status": cpa.device_status(),
     }
@@ -408,6 +411,52 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def time_hbm_kernels(cpa, w, dev, stream, warmup, steps, hbm):
+    """The HBM-bound kernels alone, on tensors larger than L2: the zigzag
+    permute and unpermute of a query-sized tensor of the workload, and the
+    LSE merge of two float32 step partials of it.  Algorithmic bytes: one
+    read and one write of the tensor (permute); two partials and two LSE
+    read, one of each written (merge).  Median of `steps` launches, CUDA
+    events on the launching stream."""
+    x = torch.randn((w.B, w.S, w.H, w.D), device=dev, dtype=torch.float32).to(w.dtype)
+    y = torch.empty_like(x)
+    o_a = torch.randn((w.B, w.S, w.H, w.D), device=dev, dtype=torch.float32)
+    o_b = torch.randn_like(o_a)
+    l_a = torch.randn((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    l_b = torch.randn_like(l_a)
+    o_out, l_out = torch.empty_like(o_a), torch.empty_like(l_a)
+    calls = {
+        "zigzag_permute": (lambda: cpa.zigzag_permute(x, w.cp, w.layout, out=y),
+                           2 * x.numel() * x.element_size()),
+        "zigzag_unpermute": (lambda: cpa.zigzag_unpermute(y, w.cp, w.layout, out=x),
+                             2 * x.numel() * x.element_size()),
+        "lse_merge": (lambda: cpa.lse_merge(o_a, l_a, o_b, l_b, o_out, l_out),
+                      3 * (o_a.numel() + l_a.numel()) * 4),
+    }
+    res = {}
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    for name, (fn, nbytes) in calls.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[name] = {"ms_median": ms, "bytes": nbytes, "GB/s": gbs, "peak": hbm,
+                     "frac": gbs / hbm}
+    res["status"] = cpa.device_status()
+    del x, y, o_a, o_b, l_a, l_b, o_out, l_out
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_forward(cpa, w, dev, stream, warmup, steps, peak):
@@ -705,6 +754,7 @@ def main():
     ap.add_argument("--no-docs", action="store_true")
     ap.add_argument("--no-allgather", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true")
+    ap.add_argument("--no-hbm", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -8,6 +8,7 @@
 // consecutive vectors, and size their grids as a multiple of the SM count.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <limits.h>
 #include <stdint.h>
 
 #include "cpattn_internal.h"
@@ -39,51 +40,46 @@ int grid_for(int64_t work_items, int threads, int per_sm) {
 // ---------------------------------------------------------------------------
 template <typename V>
 __global__ void __launch_bounds__(256) permute_runs_kernel(const char* __restrict__ in,
-                                                           char* __restrict__ out,
-                                                           int64_t outer, int64_t S,
+                                                           char* __restrict__ out, int64_t S,
                                                            int64_t S_nat, int64_t inner_bytes,
                                                            int cp, int per_rank, int64_t c,
-                                                           int64_t run_vecs, bool inverse) {
-  const int64_t nchunk = (int64_t)cp * per_rank;
-  const int64_t total = outer * nchunk * run_vecs;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+                                                           int64_t run_vecs, int64_t blocks_per_run,
+                                                           bool inverse) {
+  // Block -> (run, part of the run); the run's offsets once per block, then
+  // a plain strided copy of its vectors.
   constexpr int U = 4;
-  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < total;
-       base += stride * U) {
+  const int64_t nchunk = (int64_t)cp * per_rank;
+  const int64_t run = blockIdx.x / blocks_per_run;  // (outer index, sharded chunk)
+  const int64_t part = blockIdx.x - run * blocks_per_run;
+  const int64_t ci = run % nchunk, o = run / nchunk;
+  const int r = (int)(ci / per_rank), j = (int)(ci % per_rank);
+  const int64_t nc = (per_rank == 1 || j == 0) ? r : 2 * cp - 1 - r;  // natural chunk
+  // Tokens of this run that are real (not padding); a whole number of
+  // vectors (the launcher picks V so that S_nat * inner_bytes and the run
+  // length are multiples of it).
+  int64_t real = S_nat - nc * c;
+  real = real < 0 ? 0 : (real > c ? c : real);
+  const int64_t real_vecs = real * inner_bytes / (int64_t)sizeof(V);
+  const int64_t sh_off = (o * S + ci * c) * inner_bytes;
+  const int64_t nat_off = (o * S_nat + nc * c) * inner_bytes;
+  const V* src = reinterpret_cast<const V*>(in + (inverse ? sh_off : nat_off));
+  V* dst = reinterpret_cast<V*>(out + (inverse ? nat_off : sh_off));
+  // Sharding writes the whole run (zeros for padding); unsharding writes
+  // only the real tokens.
+  const int64_t nwrite = inverse ? real_vecs : run_vecs;
+  const int64_t step = blocks_per_run * (int64_t)blockDim.x;
+  for (int64_t e0 = part * blockDim.x + threadIdx.x; e0 < nwrite; e0 += step * U) {
     V val[U];
-    int64_t dst[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      int64_t idx = base + u * stride;
-      dst[u] = -1;
-      if (idx < total) {
-        int64_t e = idx % run_vecs;
-        int64_t rc = idx / run_vecs;
-        int64_t ci = rc % nchunk;  // sharded chunk index
-        int64_t o = rc / nchunk;
-        int r = (int)(ci / per_rank), j = (int)(ci % per_rank);
-        int64_t nc = (per_rank == 1 || j == 0) ? r : 2 * cp - 1 - r;  // natural chunk
-        int64_t sh_off = (o * S + ci * c) * inner_bytes + e * (int64_t)sizeof(V);
-        int64_t nat_off = (o * S_nat + nc * c) * inner_bytes + e * (int64_t)sizeof(V);
-        // Bytes of this run that hold real (non-padding) tokens.
-        int64_t real = S_nat - nc * c;
-        real = real < 0 ? 0 : (real > c ? c : real);
-        const bool is_real = e * (int64_t)sizeof(V) < real * inner_bytes;
-        if (inverse) {
-          dst[u] = is_real ? nat_off : -1;
-          if (is_real) val[u] = *reinterpret_cast<const V*>(in + sh_off);
-        } else {
-          dst[u] = sh_off;
-          if (is_real)
-            val[u] = *reinterpret_cast<const V*>(in + nat_off);
-          else
-            val[u] = V{};
-        }
-      }
+      const int64_t e = e0 + u * step;
+      val[u] = e < real_vecs ? src[e] : V{};
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (dst[u] >= 0) *reinterpret_cast<V*>(out + dst[u]) = val[u];
+    for (int u = 0; u < U; ++u) {
+      const int64_t e = e0 + u * step;
+      if (e < nwrite) dst[e] = val[u];
+    }
   }
 }
 
@@ -91,14 +87,22 @@ template <typename V>
 cudaError_t permute_as(const void* in, void* out, int64_t outer, int64_t S, int64_t S_nat,
                        int64_t inner_bytes, const RingShape& sh, bool inverse,
                        cudaStream_t stream) {
-  int64_t run_bytes = (int64_t)sh.c * inner_bytes;
-  int64_t run_vecs = run_bytes / (int64_t)sizeof(V);
-  int64_t total = outer * (int64_t)sh.cp * sh.per_rank * run_vecs;
-  if (total == 0) return cudaSuccess;
-  int grid = grid_for((total + 3) / 4, 256, 8);
-  permute_runs_kernel<V><<<grid, 256, 0, stream>>>(
-      static_cast<const char*>(in), static_cast<char*>(out), outer, S, S_nat, inner_bytes, sh.cp,
-      sh.per_rank, (int64_t)sh.c, run_vecs, inverse);
+  const int64_t run_bytes = (int64_t)sh.c * inner_bytes;
+  const int64_t run_vecs = run_bytes / (int64_t)sizeof(V);
+  const int64_t nruns = outer * (int64_t)sh.cp * sh.per_rank;
+  if (nruns == 0 || run_vecs == 0) return cudaSuccess;
+  // About eight resident blocks per SM in total, no more per run than its
+  // vectors can keep busy.
+  const int64_t target = (int64_t)sm_count() * 8;
+  int64_t bpr = (target + nruns - 1) / nruns;
+  const int64_t useful = (run_vecs + 256 * 4 - 1) / (256 * 4);
+  if (bpr > useful) bpr = useful;
+  if (bpr < 1) bpr = 1;
+  const int64_t grid = nruns * bpr;
+  if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
+  permute_runs_kernel<V><<<(unsigned)grid, 256, 0, stream>>>(
+      static_cast<const char*>(in), static_cast<char*>(out), S, S_nat, inner_bytes, sh.cp,
+      sh.per_rank, (int64_t)sh.c, run_vecs, bpr, inverse);
   return cudaGetLastError();
 }
 

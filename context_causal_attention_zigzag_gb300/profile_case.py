@@ -4,6 +4,8 @@ profiler captures (ncu) wrap.
     python -m context_causal_attention_zigzag_gb300.profile_case fwd_s32768
     python -m context_causal_attention_zigzag_gb300.profile_case bwd_s16384
     python -m context_causal_attention_zigzag_gb300.profile_case docs_full
+    python -m context_causal_attention_zigzag_gb300.profile_case permute_s32768
+    python -m context_causal_attention_zigzag_gb300.profile_case merge_s32768
 
 Cases are reduced versions of the named workloads (same heads, head dim and
 layout; fewer tokens or batches) so that a full counter capture of one launch
@@ -30,7 +32,36 @@ CASES = {
 }
 
 
+# The HBM-bound kernels on a query-sized tensor of the S=32768 shape (larger
+# than L2): zigzag permute of a bf16 [1, 32768, 32, 128] tensor (256 MiB),
+# LSE merge of two float32 partials of that shape (512 MiB each).
+HBM_CASES = {"permute_s32768": (1, 32768, 32, 128, 8), "merge_s32768": (1, 32768, 32, 128, 8)}
+
+
+def run_hbm(case: str, repeats: int) -> int:
+    B, S, H, D, cp = HBM_CASES[case]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    g = torch.Generator(device="cpu").manual_seed(6)
+    if case.startswith("permute"):
+        x = torch.randn((B, S, H, D), generator=g).to(torch.bfloat16).to(dev)
+        y = torch.empty_like(x)
+        for _ in range(repeats):
+            cpa.zigzag_permute(x, cp, cpa.ZIGZAG, out=y)
+    else:
+        o_a = torch.randn((B, S, H, D), generator=g).to(dev)
+        o_b = torch.randn((B, S, H, D), generator=g).to(dev)
+        l_a = torch.randn((B, H, S), generator=g).to(dev)
+        l_b = torch.randn((B, H, S), generator=g).to(dev)
+        o_out, l_out = torch.empty_like(o_a), torch.empty_like(l_a)
+        for _ in range(repeats):
+            cpa.lse_merge(o_a, l_a, o_b, l_b, o_out, l_out)
+    torch.cuda.synchronize()
+    return cpa.device_status()
+
+
 def run(case: str, repeats: int = 3) -> int:
+    if case in HBM_CASES:
+        return run_hbm(case, repeats)
     w = CASES[case]
     dev = torch.device("cuda", torch.cuda.current_device())
     q, k, v, do = (x.to(dev) if x is not None else None for x in inputs.generate(w))
@@ -55,7 +86,7 @@ def run(case: str, repeats: int = 3) -> int:
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("case", choices=sorted(CASES) + sorted(HBM_CASES))
     ap.add_argument("--repeats", type=int, default=3)
     a = ap.parse_args()
     status = run(a.case, a.repeats)
