@@ -206,24 +206,17 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
   const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   constexpr int EPL = D / 32;  // elements per lane: one 4-, 8- or 16-byte vector
-  // A warp takes R consecutive positions of one (batch, head) per iteration:
-  // R rows' loads in flight at once, and their Delta values adjacent (two
-  // rows when a lane's share of a row is already a 16-byte float4).
+  // A warp takes R consecutive rows (b, s, h) of the [B, S, H, D] tensors per
+  // iteration: R * D contiguous elements of each, all loads in flight at once.
   constexpr int R = (sizeof(T) == 4 && D == 128) ? 2 : 4;
-  const int64_t sg = ((int64_t)S + R - 1) / R;  // position groups per (batch, head)
-  const int64_t groups = (int64_t)B * H * sg;
-  for (int64_t gi = warp0; gi < groups; gi += nwarps) {
-    const int64_t bh = gi / sg;
-    const int64_t s0 = (gi - bh * sg) * R;
-    const int64_t bi = bh / H;
-    const int64_t hi = bh - bi * H;
+  const int64_t rows = (int64_t)B * S * H;
+  for (int64_t row0 = warp0 * R; row0 < rows; row0 += nwarps * R) {
     float a[R][EPL], b[R][EPL];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      if (s0 + r < S) {
-        const int64_t row = (bi * S + s0 + r) * H + hi;
-        load_vec<T, EPL>(out + row * D + lane * EPL, a[r]);
-        load_vec<T, EPL>(dout + row * D + lane * EPL, b[r]);
+      if (row0 + r < rows) {
+        load_vec<T, EPL>(out + (row0 + r) * D + lane * EPL, a[r]);
+        load_vec<T, EPL>(dout + (row0 + r) * D + lane * EPL, b[r]);
       } else {
 #pragma unroll
         for (int e = 0; e < EPL; ++e) a[r][e] = b[r][e] = 0.f;
@@ -242,8 +235,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
     if (dq_acc != nullptr) {
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        if (s0 + r >= S) continue;
-        float* dq = dq_acc + ((bi * S + s0 + r) * H + hi) * D + lane * EPL;
+        if (row0 + r >= rows) continue;
+        float* dq = dq_acc + (row0 + r) * D + lane * EPL;
         if constexpr (EPL == 4) {
           *reinterpret_cast<float4*>(dq) = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
@@ -251,7 +244,11 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const T* __restrict__ out
         }
       }
     }
-    if (lane < R && s0 + lane < S) delta[bh * S + s0 + lane] = mine * delta_scale;
+    if (lane < R && row0 + lane < rows) {
+      const int64_t row = row0 + lane;
+      const int64_t bi = row / ((int64_t)S * H), si = (row / H) % S, hi = row % H;
+      delta[(bi * H + hi) * S + si] = mine * delta_scale;
+    }
   }
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4_kv;
