@@ -354,19 +354,15 @@ int host_common(const HostPlan& p, const void* q, const void* k, const void* v, 
         lib(cpattn_doc_bounds(cu_dev, (int)ncu - 1, S, bounds, stream));
     ss->cu_pending = true;
   }
-  // Uploads: Q, K, V part by part, then dO part by part.
+  // Part by part: Q, K, V up, then the forward (which waits for them) and
+  // the part's O and LSE down behind it.  The host enqueues in this order so
+  // that the first forward is queued before the later parts' copies.
   for (int i = 0; i < n && rc == CPATTN_OK; ++i) {
     cuda(copy_part(p, q, qs + i * p.q_slot, H, p.elt, i, true, ss->up)) &&
         cuda(copy_part(p, k, ks + i * p.kv_slot, Hkv, p.elt, i, true, ss->up)) &&
         cuda(copy_part(p, v, vs + i * p.kv_slot, Hkv, p.elt, i, true, ss->up)) &&
         cuda(cudaEventRecord(ss->qkv[i], ss->up));
-  }
-  for (int i = 0; backward && i < n && rc == CPATTN_OK; ++i) {
-    cuda(copy_part(p, dout, dos + i * p.q_slot, H, p.elt, i, true, ss->up)) &&
-        cuda(cudaEventRecord(ss->dout[i], ss->up));
-  }
-  // Forward part by part; each part's O and LSE go down behind it.
-  for (int i = 0; i < n && rc == CPATTN_OK; ++i) {
+    if (rc != CPATTN_OK) break;
     void* o_i = os + i * p.q_slot;
     float* ls_i = reinterpret_cast<float*>(lse_s + i * p.lse_slot);
     float* ln_i = reinterpret_cast<float*>(lse_n + i * p.lse_slot);
@@ -385,6 +381,11 @@ int host_common(const HostPlan& p, const void* q, const void* k, const void* v, 
         cuda(cudaStreamWaitEvent(ss->down, ss->fwd[i], 0)) &&
         cuda(copy_part(p, o_i, out, H, p.elt, i, false, ss->down)) &&
         cuda(copy_lse_part(p, ln_i, lse, i, ss->down));
+  }
+  // dO up part by part (behind the last Q, K, V, while the forwards run).
+  for (int i = 0; backward && i < n && rc == CPATTN_OK; ++i) {
+    cuda(copy_part(p, dout, dos + i * p.q_slot, H, p.elt, i, true, ss->up)) &&
+        cuda(cudaEventRecord(ss->dout[i], ss->up));
   }
   // Backward part by part; each part's gradients go down behind it.
   for (int i = 0; backward && i < n && rc == CPATTN_OK; ++i) {
