@@ -61,14 +61,14 @@ ALL_WORKLOADS = {**inputs.WORKLOADS, **inputs.DOC_WORKLOADS}
 # workload without a capture; must be re-taken whenever a kernel changes.
 CAPTURED_TRAFFIC = {
     "c5_bf16_s131072_fwdbwd": {
-        "ring_bwd": (2.149e9 + 0.017e9) + (33.521e9 + 4.277e9) + (5.521e9 + 2.117e9)
+        "ring_bwd": (2.148e9 + 0.016e9) + (33.108e9 + 4.277e9) + (5.553e9 + 2.119e9)
         + (4.295e9 + 1.054e9),
-        "ring_fwd": 5.355e9 + 1.069e9,
+        "ring_fwd": 5.064e9 + 1.070e9,
     },
     "docs_bf16_s131072_fwdbwd": {
-        "ring_bwd": (2.148e9 + 0.016e9) + (7.692e9 + 4.257e9) + (2.934e9 + 2.110e9)
-        + (4.296e9 + 1.054e9),
-        "ring_fwd": 1.795e9 + 1.059e9,
+        "ring_bwd": (2.148e9 + 0.016e9) + (6.831e9 + 4.256e9) + (2.927e9 + 2.110e9)
+        + (4.295e9 + 1.054e9),
+        "ring_fwd": 1.766e9 + 1.059e9,
     },
 }
 
