@@ -338,6 +338,7 @@ def run_ours(args):
                "ms_per_step": e2e_ms, "ms_per_call": per_call, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "api": e2e_api, "clocks": e2e_clk}
         e2e["head_parts"] = cpa.attention_host_parts(B, H, Hkv, S, D)
+        e2e["host_link_gbs"] = host_link_gbs(dev, stream)
 
     # Roofline of the dominant kernel, from the live event timings.  The
     # kernels of the step are timed inside the multi-second loop of back-to-back
@@ -411,6 +412,28 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def host_link_gbs(dev, stream, mib=256, reps=3):
+    """The machine's host link as the end-to-end run sees it: a pinned 256 MiB
+    copy up and one down, best of `reps`, CUDA events (context for the e2e
+    figure, which depends on it)."""
+    h = torch.empty(mib << 20, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(mib << 20, dtype=torch.uint8, device=dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    res = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = None
+        for _ in range(reps):
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        res[name] = (mib << 20) / (best * 1e-3) / 1e9
+    return res
 
 
 def time_hbm_kernels(cpa, w, dev, stream, warmup, steps, hbm):
