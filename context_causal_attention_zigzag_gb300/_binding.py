@@ -709,22 +709,16 @@ def attention_host_parts(B, H, Hkv, S, D) -> int:
     return int(lib().cpattn_attention_host_parts(B, H, Hkv, S, D))
 
 
-def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, out=None,
-                   lse=None, dq=None, dk=None, dv=None, grad_dtype=None, workspace=None,
-                   device=None, stream=None, parts=0):
-    """cpattn_attention_host: natural-order CPU tensors (pinned for
-    asynchronous copies) in and out, the whole path on the GPU in between,
-    the heads in `parts` pipelined groups (0: the library's choice).
-    dout None: forward only.  Returns (out, lse) or (out, lse, dq, dk, dv) as
-    CPU tensors; they are complete once the stream has been synchronised."""
+def _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype, device, name):
+    """Shared marshalling of the host-to-host calls: checks, dtype code,
+    output tensors (pinned when the inputs are)."""
     if q.is_cuda or k.is_cuda or v.is_cuda:
-        raise ValueError("attention_host takes host (CPU) tensors")
+        raise ValueError(f"{name} takes host (CPU) tensors")
     for t in (q, k, v, dout):
         if t is not None and not t.is_contiguous():
             raise ValueError("tensor must be contiguous")
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     B, S, H, D = q.shape
-    Hkv = k.shape[2]
     code = _dtype_code(q)
     backward = dout is not None
     gdt = q.dtype if grad_dtype is None else grad_dtype
@@ -740,16 +734,31 @@ def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, ou
         dq = host(q.shape, gdt, dq)
         dk = host(k.shape, gdt, dk)
         dv = host(v.shape, gdt, dv)
+    return dev, code, backward, (out, lse, dq, dk, dv)
+
+
+def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, out=None,
+                   lse=None, dq=None, dk=None, dv=None, grad_dtype=None, workspace=None,
+                   device=None, stream=None, parts=0):
+    """cpattn_attention_host: natural-order CPU tensors (pinned for
+    asynchronous copies) in and out, the whole path on the GPU in between,
+    the heads in `parts` pipelined groups (0: the library's choice).
+    dout None: forward only.  Returns (out, lse) or (out, lse, dq, dk, dv) as
+    CPU tensors; they are complete once the stream has been synchronised."""
+    dev, code, backward, res = _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype,
+                                             device, "attention_host")
+    B, S, H, D = q.shape
+    Hkv = k.shape[2]
     need = attention_host_workspace_bytes(B, H, Hkv, S, D, cp, layout, code, backward)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
     st = ctypes.c_void_p((stream or torch.cuda.current_stream(dev)).cuda_stream)
-    rc = lib().cpattn_attention_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out), _ptr(lse),
-                                     _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
-                                     int(layout), int(bool(causal)), code, _scale(scale),
-                                     int(parts), _ptr(workspace), workspace.numel(), st)
+    rc = lib().cpattn_attention_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), *map(_ptr, res), B, H,
+                                     Hkv, S, D, int(cp), int(layout), int(bool(causal)), code,
+                                     _scale(scale), int(parts), _ptr(workspace), workspace.numel(),
+                                     st)
     _check("cpattn_attention_host", rc)
-    return (out, lse, dq, dk, dv) if backward else (out, lse)
+    return res if backward else res[:2]
 
 
 def attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout=ZIGZAG, dtype=BF16,
@@ -766,29 +775,10 @@ def attention_host_docs(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causa
     sequence length.  cu_seqlens: document offsets over the S tokens (a
     sequence of ints, 0 ... S), None for one document.  Returns (out, lse) or
     (out, lse, dq, dk, dv) as CPU tensors over the S real tokens."""
-    if q.is_cuda or k.is_cuda or v.is_cuda:
-        raise ValueError("attention_host_docs takes host (CPU) tensors")
-    for t in (q, k, v, dout):
-        if t is not None and not t.is_contiguous():
-            raise ValueError("tensor must be contiguous")
-    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    dev, code, backward, res = _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype,
+                                             device, "attention_host_docs")
     B, S, H, D = q.shape
     Hkv = k.shape[2]
-    code = _dtype_code(q)
-    backward = dout is not None
-    gdt = q.dtype if grad_dtype is None else grad_dtype
-    if backward and gdt == torch.float32 and q.dtype != torch.float32:
-        code |= GRAD_F32
-    pin = q.is_pinned()
-
-    def host(shape, dtype, t):
-        return torch.empty(shape, dtype=dtype, pin_memory=pin) if t is None else t
-    out = host(q.shape, q.dtype, out)
-    lse = host((B, H, S), torch.float32, lse)
-    if backward:
-        dq = host(q.shape, gdt, dq)
-        dk = host(k.shape, gdt, dk)
-        dv = host(v.shape, gdt, dv)
     need = attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout, code, backward)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
@@ -798,9 +788,9 @@ def attention_host_docs(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causa
         cu_arr, ndocs = (ctypes.c_int32 * len(cu_list))(*cu_list), len(cu_list) - 1
     st = ctypes.c_void_p((stream or torch.cuda.current_stream(dev)).cuda_stream)
     rc = lib().cpattn_attention_host_docs(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk),
-        _ptr(dv), B, H, Hkv, S, D, int(cp), int(layout), int(bool(causal)), code, _scale(scale),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(dout), *map(_ptr, res), B, H, Hkv, S, D, int(cp),
+        int(layout), int(bool(causal)), code, _scale(scale),
         ctypes.cast(cu_arr, ctypes.c_void_p) if cu_arr is not None else None, ndocs, int(parts),
         _ptr(workspace), workspace.numel(), st)
     _check("cpattn_attention_host_docs", rc)
-    return (out, lse, dq, dk, dv) if backward else (out, lse)
+    return res if backward else res[:2]
