@@ -18,9 +18,11 @@ long ones), from its own generator seeded with ``doc_seed``; the last
 document is cut at S.
 """
 import math
+import os
 from dataclasses import dataclass, field, replace
 from typing import Optional, Tuple
 
+import numpy as np
 import torch
 
 CONTIGUOUS = 0
@@ -129,3 +131,120 @@ def generate(w: Workload, with_dout: Optional[bool] = None, pin: bool = False):
 def to_f32_numpy(x: torch.Tensor):
     """Exact float32 copy (bf16 and fp32 values are representable) as numpy."""
     return x.detach().to("cpu", torch.float32).contiguous().numpy()
+
+
+# ---------------------------------------------------------------------------
+# Counter-based draws that every machine reproduces bit for bit
+# ---------------------------------------------------------------------------
+#
+# ``torch.randn`` on the CPU takes a vectorised path on some x86 builds and a
+# scalar one elsewhere, so its float32 draws can differ in the last bit from
+# one machine to the next; after rounding to bf16 a few values out of a
+# hundred million then differ.  Expected values computed on one machine and
+# checked on another need draws that do not depend on the machine.  Here
+# element n of a tensor gets two 64-bit words from SplitMix64 (Steele, Lea
+# and Flood, "Fast splittable pseudorandom number generators", 2014: the
+# state advances by the odd constant 0x9E3779B97F4A7C15 and each output is
+# the state passed through two xor-shift-multiply rounds and a final
+# xor-shift) used as a counter-based generator: the state for counter c is
+# key + (c + 1) * 0x9E3779B97F4A7C15, so any element can be drawn on its own.
+# The two words become uniforms u1 in (0, 1] and u2 in [0, 1) from their top
+# 53 bits, and the Box-Muller transform sqrt(-2 ln u1) cos(2 pi u2) gives a
+# standard normal in float64 (integer steps are exact everywhere; the
+# float64 log / cos differ between math libraries by an ulp at most, which
+# moves a bf16 rounding once in about 2^43 draws).  The value is then rounded
+# to float32 and to the workload dtype (round to nearest even).
+
+_GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+
+def _splitmix_out(z):
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def counter_key(seed: int, stream: int) -> int:
+    """The generator key of one tensor (``stream``) of a seeded draw."""
+    with np.errstate(over="ignore"):
+        z = np.array([(int(seed) * 16 + int(stream)) & (2**64 - 1)], np.uint64) * _GAMMA
+        return int(_splitmix_out(z)[0])
+
+
+def counter_normal(key: int, index: np.ndarray) -> np.ndarray:
+    """Standard normals (float64) for the counters ``index`` (natural flat
+    element indices) of the tensor with generator key ``key``."""
+    c = np.asarray(index, dtype=np.uint64) * np.uint64(2)
+    k = np.uint64(key)
+    with np.errstate(over="ignore"):
+        w1 = _splitmix_out(k + (c + np.uint64(1)) * _GAMMA)
+        w2 = _splitmix_out(k + (c + np.uint64(2)) * _GAMMA)
+    u1 = ((w1 >> np.uint64(11)) + np.uint64(1)).astype(np.float64) * (2.0 ** -53)
+    u2 = (w2 >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
+
+
+def counter_slice(key: int, full_shape, x0: int, nx: int, threads: int = 0) -> np.ndarray:
+    """float32 draws of the heads [x0, x0 + nx) of a [B, S, X, D] tensor:
+    element (b, s, x, d) takes counter ((b*S + s)*X + x)*D + d of the full
+    tensor, so a slice holds the same values as the whole tensor would."""
+    import concurrent.futures as cf
+    B, S, X, D = (int(a) for a in full_shape)
+    out = np.empty((B * S, nx, D), np.float32)
+    rows = B * S
+    step = 4096
+    hx = np.arange(x0, x0 + nx, dtype=np.uint64)[:, None] * np.uint64(D)
+    dd = np.arange(D, dtype=np.uint64)[None, :]
+    inner = (hx + dd)[None]                       # [1, nx, D]
+
+    def fill(r0):
+        r1 = min(rows, r0 + step)
+        base = np.arange(r0, r1, dtype=np.uint64)[:, None, None] * np.uint64(X * D)
+        out[r0:r1] = counter_normal(key, base + inner).astype(np.float32)
+
+    n = threads or min(16, os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(fill, range(0, rows, step)))
+    return out.reshape(B, S, nx, D)
+
+
+def group_inputs(w: Workload, g: int):
+    """Counter-based inputs of kv group ``g`` of workload ``w``: Q and dO of
+    its query heads [g*H/Hkv, (g+1)*H/Hkv), K and V of kv head g, each value
+    drawn for its natural index in the full tensor and rounded to w.dtype.
+    Returns CPU tensors q [B,S,H/Hkv,D], k, v [B,S,1,D], dout [B,S,H/Hkv,D]."""
+    grp = w.H // w.Hkv
+    full_q = (w.B, w.S, w.H, w.D)
+    full_k = (w.B, w.S, w.Hkv, w.D)
+    parts = []
+    for stream, (shape, x0, nx) in enumerate(((full_q, g * grp, grp), (full_k, g, 1),
+                                              (full_k, g, 1), (full_q, g * grp, grp))):
+        a = counter_slice(counter_key(w.seed, stream), shape, x0, nx)
+        parts.append(torch.from_numpy(a).to(w.dtype))
+    return tuple(parts)
+
+
+def embed_group(w: Workload, g: int, full, group):
+    """Writes the kv-group tensors ``group`` (from ``group_inputs``) into the
+    full tensors ``full`` = (q, k, v, dout) in place."""
+    grp = w.H // w.Hkv
+    q, k, v, do = full
+    gq, gk, gv, gdo = group
+    q[:, :, g * grp:(g + 1) * grp] = gq
+    k[:, :, g:g + 1] = gk
+    v[:, :, g:g + 1] = gv
+    do[:, :, g * grp:(g + 1) * grp] = gdo
+
+
+def digest(*tensors) -> str:
+    """sha256 over the raw bytes of the tensors, in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for t in tensors:
+        t = t.detach().contiguous().cpu()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        h.update(t.numpy().tobytes())
+    return h.hexdigest()

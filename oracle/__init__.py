@@ -13,7 +13,11 @@ file; in short:
   Training", section "Prove attention equivalence";
 * chunk placement (zigzag and contiguous), ring step source and per-step
   partials -- "Sequence Parallelism IV: Megatron Context Parallel and
-  Load-Balanced Rings", sections 3-5.
+  Load-Balanced Rings", sections 3-5;
+* the all-gather schedule, the a2a (Ulysses) variant and hierarchical
+  a2a+p2p context parallelism -- "Context Parallelism in MegaDLMs",
+  sections "Key-Value Communication Patterns" and "Hierarchical Context
+  Parallelism", and "Sequence Parallelism IV", section 7.
 
 Arrays: q [B,S,H,D], k/v [B,S,Hkv,D] float32 (values exactly representable,
 e.g. bf16-rounded), natural token order.  Outputs are float64; LSE is
@@ -59,6 +63,8 @@ def _lib(mutation: int = 0):
     lib.oracle_attn_bwd_dq_rows.argtypes = [_f32p] * 4 + shape + [_i64p, _L, _f64p]
     lib.oracle_attn_bwd_dkdv_rows_sparse.argtypes = ([_f32p] * 4 + shape
                                                      + [_i64p, _L, _i64p, _L, _f64p, _f64p])
+    lib.oracle_attn_bwd_dkdv_rows.argtypes = ([_f32p] * 4 + shape
+                                              + [_f64p, _f64p, _i64p, _L, _f64p, _f64p])
     lib.oracle_tile_counts.argtypes = [_L, _I, _I, _I, _L, _u64p, ctypes.c_void_p]
     lib.oracle_tile_counts.restype = _I
     docs = [_i64p, _L]
@@ -87,6 +93,13 @@ def _lib(mutation: int = 0):
     lib.oracle_ulysses_fwd.restype = _I
     lib.oracle_ulysses_bwd.argtypes = [_f32p] * 4 + ring + docs + [_f64p] * 3
     lib.oracle_ulysses_bwd.restype = _I
+    lib.oracle_hier_a2a.argtypes = [_f32p, _L, _L, _I, _I, _I, _I, _I, _I, _I, _f32o]
+    lib.oracle_hier_a2a.restype = _I
+    hier = [_L, _I, _I, _L, _I, _I, _I, _I, _I, _D]
+    lib.oracle_hier_fwd.argtypes = [_f32p, _f32p, _f32p] + hier + docs + [_f64p, _f64p]
+    lib.oracle_hier_fwd.restype = _I
+    lib.oracle_hier_bwd.argtypes = [_f32p] * 4 + hier + docs + [_f64p] * 3
+    lib.oracle_hier_bwd.restype = _I
     _libs[mutation] = lib
     return lib
 
@@ -219,6 +232,26 @@ def attn_bwd_dkdv_rows_sparse(q, k, v, dout, qrows, krows, causal=True, scale=No
     dv = np.empty((n, D), np.float64)
     _lib(mutation).oracle_attn_bwd_dkdv_rows_sparse(q, k, v, dout, B, H, Hkv, S, D, int(causal),
                                                     scale, qrows, qrows.shape[0], krows, n, dk, dv)
+    return dk, dv
+
+
+def attn_bwd_dkdv_rows(q, k, v, dout, out, lse, krows, causal=True, scale=None,
+                       mutation: int = 0):
+    """dK/dV rows (b, g, j) for any dout, from the definition's out [B,S,H,D]
+    and lse [B,H,S] of every query row (as ``attn_fwd`` returns them)."""
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, S, H, Hkv, D = _shape(q, k)
+    scale = default_scale(D) if scale is None else scale
+    out = np.ascontiguousarray(out, dtype=np.float64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    if out.shape != (B, S, H, D) or lse.shape != (B, H, S):
+        raise ValueError("out / lse do not match the problem's shape")
+    krows = np.ascontiguousarray(np.asarray(krows, dtype=np.int64).reshape(-1, 3))
+    n = krows.shape[0]
+    dk = np.empty((n, D), np.float64)
+    dv = np.empty((n, D), np.float64)
+    _lib(mutation).oracle_attn_bwd_dkdv_rows(q, k, v, dout, B, H, Hkv, S, D, int(causal), scale,
+                                             out, lse, krows, n, dk, dv)
     return dk, dv
 
 
@@ -429,4 +462,54 @@ def ulysses_bwd(q_sh, k_sh, v_sh, do_sh, cp, layout, causal=True, scale=None, cu
                                            scale, cu, nd, dq, dk, dv)
     if rc != 0:
         raise ValueError("bad ulysses_bwd arguments")
+    return dq, dk, dv
+
+
+def hier_a2a(x_sh, H, Hkv, A, P, layout, kv=False, mutation: int = 0):
+    """First-level all-to-all of hierarchical context parallelism (level sizes
+    [A, P], cp = A*P) on a [B,S,X,D] tensor sharded over cp ranks: returns
+    [A, B, S, nx, D]; block a holds member a's head slice, rows
+    [p*S/P, (p+1)*S/P) being what member a of group p holds, in the order of
+    level-two shard p."""
+    x = _f32(x_sh)
+    B, S, X, D = x.shape
+    nx = ulysses_heads(0, A, H, Hkv)[3 if kv else 1]
+    out = np.empty((A, B, S, nx, D), np.float32)
+    rc = _lib(mutation).oracle_hier_a2a(x, B, S, H, Hkv, D, A, P, layout, int(kv), out)
+    if rc != 0:
+        raise ValueError("bad hier_a2a arguments")
+    return out
+
+
+def hier_fwd(q_sh, k_sh, v_sh, A, P, layout, causal=True, scale=None, cu_seqlens=None,
+             mutation: int = 0):
+    """Hierarchical (a2a+p2p) attention on inputs sharded over cp = A*P
+    ranks: all-to-all inside groups of A, ring over the P groups on each
+    head slice, all-to-all back.  Sharded (out, lse)."""
+    q, k, v = _f32(q_sh), _f32(k_sh), _f32(v_sh)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu_or_one(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    out = np.empty((B, S, H, D), np.float64)
+    lse = np.empty((B, H, S), np.float64)
+    rc = _lib(mutation).oracle_hier_fwd(q, k, v, B, H, Hkv, S, D, A, P, layout, int(causal),
+                                        scale, cu, nd, out, lse)
+    if rc != 0:
+        raise ValueError("bad hier_fwd arguments")
+    return out, lse
+
+
+def hier_bwd(q_sh, k_sh, v_sh, do_sh, A, P, layout, causal=True, scale=None, cu_seqlens=None,
+             mutation: int = 0):
+    q, k, v, do = _f32(q_sh), _f32(k_sh), _f32(v_sh), _f32(do_sh)
+    B, S, H, Hkv, D = _shape(q, k)
+    cu, nd = _cu_or_one(cu_seqlens, S)
+    scale = default_scale(D) if scale is None else scale
+    dq = np.empty((B, S, H, D), np.float64)
+    dk = np.empty((B, S, Hkv, D), np.float64)
+    dv = np.empty((B, S, Hkv, D), np.float64)
+    rc = _lib(mutation).oracle_hier_bwd(q, k, v, do, B, H, Hkv, S, D, A, P, layout, int(causal),
+                                        scale, cu, nd, dq, dk, dv)
+    if rc != 0:
+        raise ValueError("bad hier_bwd arguments")
     return dq, dk, dv

@@ -43,6 +43,11 @@
  *    keeps only keys of i's own document.  Padding is read as one more
  *    document, so no real token sees a padded one.  The *_docs entry points
  *    take cu; the others use one document (cu = NULL).
+ *  - Hierarchical context parallelism (a2a+p2p): "Context Parallelism in
+ *    MegaDLMs", sections "Hierarchical Context Parallelism" and "Key-Value
+ *    Communication Patterns" -- an all-to-all inside groups of A consecutive
+ *    ranks, then the ring of the second level over the P groups (cp = A*P);
+ *    see oracle_hier_a2a below for the reading.
  *
  * Readings where the pages are silent: tensors are [B, S, H, D] row-major,
  * LSE is [B, H, S] in natural log; query head h uses kv head h / (H / Hkv);
@@ -61,7 +66,9 @@
  * force and finite differences with documents, one token per document in
  * closed form, packed documents equal to each document alone, one document
  * equal to the plain mask, the ring under documents equal to the definition,
- * and per-rank pair counts.
+ * and per-rank pair counts; the hierarchical all-to-all against the two
+ * levels' token lists and the hierarchical schedule against the definition;
+ * dK / dV on listed key rows against finite differences and the sum rules.
  */
 #include <math.h>
 #include <stdint.h>
@@ -731,6 +738,228 @@ int oracle_ulysses_bwd(const float* q_sh, const float* k_sh, const float* v_sh,
 }
 
 /* ------------------------------------------------------------------------ */
+/* Hierarchical context parallelism: all-to-all inside groups, ring across   */
+/* ------------------------------------------------------------------------ */
+
+/* "Context Parallelism in MegaDLMs", sections "Hierarchical Context
+ * Parallelism" (a list of level sizes such as [2, 2] splits the context
+ * group over two levels) and "Key-Value Communication Patterns" (the
+ * a2a+p2p type combines the all-to-all and the point-to-point ring).
+ * Reading: the sizes are [A, P] with cp = A * P; the first level is an
+ * all-to-all among A consecutive ranks (a group), the second a ring among
+ * the P groups.  Global rank r = p * A + a is member a of group p.  The
+ * sequence is sharded over all cp ranks with the chosen layout (zigzag:
+ * 2*cp chunks).  The all-to-all gives member a of group p head slice a
+ * (ulysses_heads with A slices) of every token its group holds, ordered as
+ * shard p of the second level (zigzag: level-two chunks p and 2P-1-p of
+ * 2P); the members a of all P groups then run the ring of the second level
+ * on that head slice, and the inverse all-to-all returns out, LSE and the
+ * gradients to the token owners. */
+static int hier_rank(int p, int a, int A, int P) {
+#if ORACLE_MUTATION == 11
+  (void)A;
+  return a * P + p; /* groups of strided ranks: the wrong level */
+#else
+  (void)P;
+  return p * A + a;
+#endif
+}
+
+/* The first-level all-to-all, as an entry point: sh [B,S,X,D] sharded over
+ * cp = A*P ranks -> out [A][B][S][nx][D]; block a holds member a's head
+ * slice, rows [p*S/P, (p+1)*S/P) being what member a of group p holds, in
+ * the order of level-two shard p.  Returns -1 on bad arguments or when a
+ * group does not hold exactly the tokens of its level-two shard. */
+int oracle_hier_a2a(const float* sh, long B, long S, int H, int Hkv, int D, int A, int P,
+                    int layout, int kv, float* out) {
+  if (A < 1 || P < 1 || H % A != 0 || H % Hkv != 0) return -1;
+  const int hc = H / A, grp = H / Hkv;
+  if (hc % grp != 0 && grp % hc != 0) return -1;
+  const int cp = A * P;
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  long* slot = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  long* tok = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  int rc = 0;
+  if (oracle_shard_order(S, cp, layout, nat_of) != 0 || oracle_shard_order(S, P, layout, tok))
+    rc = -1;
+  const long L = S / cp, LP = S / P;
+  for (int p = 0; p < P && rc == 0; ++p) {
+    /* Where each token of the group sits in the cp-level sharded tensor. */
+    for (long n = 0; n < S; ++n) slot[n] = -1;
+    for (int a = 0; a < A; ++a) {
+      const long r = hier_rank(p, a, A, P);
+      for (long o = 0; o < L; ++o) slot[nat_of[r * L + o]] = r * L + o;
+    }
+    rank_tokens(S, P, layout, p, tok); /* level-two shard p, in its order */
+    for (long m = 0; m < LP; ++m)
+      if (slot[tok[m]] < 0) rc = -1;
+    for (int a = 0; a < A && rc == 0; ++a) {
+      int q0, nq, g0, ng;
+      ulysses_heads(a, A, H, Hkv, &q0, &nq, &g0, &ng);
+      const int X = kv ? Hkv : H, x0 = kv ? g0 : q0, nx = kv ? ng : nq;
+      for (long b = 0; b < B; ++b)
+        for (long m = 0; m < LP; ++m)
+          memcpy(out + (((long)a * B + b) * S + p * LP + m) * nx * D,
+                 sh + idx4(b, slot[tok[m]], x0, 0, S, X, D), sizeof(float) * nx * D);
+    }
+  }
+  free(nat_of);
+  free(slot);
+  free(tok);
+  return rc;
+}
+
+/* Member a's head slice of every token in natural order, from the
+ * all-to-all's block a (level-two sharded order). */
+static void hier_block_natural(const float* blk, float* nat, long B, long S, int nx, int D, int P,
+                               int layout, long* tmp) {
+  oracle_shard_order(S, P, layout, tmp);
+  for (long b = 0; b < B; ++b)
+    for (long m = 0; m < S; ++m)
+      memcpy(nat + idx4(b, tmp[m], 0, 0, S, nx, D), blk + ((b * S + m) * nx) * D,
+             sizeof(float) * nx * D);
+}
+
+/* Hierarchical forward, sharded order in and out: the all-to-all, the ring
+ * of the second level (P ranks) on each member's head slice, the inverse
+ * all-to-all. */
+static int hier_fwd_m(const float* q_sh, const float* k_sh, const float* v_sh, long B, int H,
+                      int Hkv, long S, int D, int A, int P, int layout, const Mask* msk,
+                      double scale, double* out_sh, double* lse_sh) {
+  if (A < 1 || P < 1 || H % A != 0 || H % Hkv != 0) return -1;
+  const int hc = H / A, grp = H / Hkv;
+  if (hc % grp != 0 && grp % hc != 0) return -1;
+  const int nkv = hc >= grp ? hc / grp : 1;
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  long* tmp = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  float* qa = (float*)malloc(sizeof(float) * A * B * S * hc * D + 1);
+  float* ka = (float*)malloc(sizeof(float) * A * B * S * nkv * D + 1);
+  float* va = (float*)malloc(sizeof(float) * A * B * S * nkv * D + 1);
+  float* qn = (float*)malloc(sizeof(float) * B * S * hc * D + 1);
+  float* kn = (float*)malloc(sizeof(float) * B * S * nkv * D + 1);
+  float* vn = (float*)malloc(sizeof(float) * B * S * nkv * D + 1);
+  double* on = (double*)malloc(sizeof(double) * B * S * hc * D + 1);
+  double* ln = (double*)malloc(sizeof(double) * B * hc * S + 1);
+  int rc = oracle_shard_order(S, A * P, layout, nat_of);
+  if (rc == 0) rc = oracle_hier_a2a(q_sh, B, S, H, Hkv, D, A, P, layout, 0, qa);
+  if (rc == 0) rc = oracle_hier_a2a(k_sh, B, S, H, Hkv, D, A, P, layout, 1, ka);
+  if (rc == 0) rc = oracle_hier_a2a(v_sh, B, S, H, Hkv, D, A, P, layout, 1, va);
+  for (int a = 0; a < A && rc == 0; ++a) {
+    int q0, nq, g0, ng;
+    ulysses_heads(a, A, H, Hkv, &q0, &nq, &g0, &ng);
+    hier_block_natural(qa + (long)a * B * S * hc * D, qn, B, S, hc, D, P, layout, tmp);
+    hier_block_natural(ka + (long)a * B * S * nkv * D, kn, B, S, nkv, D, P, layout, tmp);
+    hier_block_natural(va + (long)a * B * S * nkv * D, vn, B, S, nkv, D, P, layout, tmp);
+    rc = ring_fwd_m(qn, kn, vn, B, nq, ng, S, D, P, layout, msk, scale, 0, on, ln);
+    for (long b = 0; b < B && rc == 0; ++b)
+      for (long p = 0; p < S; ++p) {
+        const long n = nat_of[p];
+        memcpy(out_sh + idx4(b, p, q0, 0, S, H, D), on + idx4(b, n, 0, 0, S, nq, D),
+               sizeof(double) * nq * D);
+        for (int h = 0; h < nq; ++h) lse_sh[(b * H + q0 + h) * S + p] = ln[(b * nq + h) * S + n];
+      }
+  }
+  free(nat_of);
+  free(tmp);
+  free(qa);
+  free(ka);
+  free(va);
+  free(qn);
+  free(kn);
+  free(vn);
+  free(on);
+  free(ln);
+  return rc;
+}
+
+int oracle_hier_fwd(const float* q_sh, const float* k_sh, const float* v_sh, long B, int H,
+                    int Hkv, long S, int D, int A, int P, int layout, int causal, double scale,
+                    const long* cu, long ndocs, double* out_sh, double* lse_sh) {
+  const Mask msk = {causal, cu, ndocs};
+  return hier_fwd_m(q_sh, k_sh, v_sh, B, H, Hkv, S, D, A, P, layout, &msk, scale, out_sh,
+                    lse_sh);
+}
+
+/* Hierarchical backward, sharded order in and out: dO follows the
+ * all-to-all; each member takes the gradients of attention on its head
+ * slice (the ring of the second level reaches the same sums); the inverse
+ * all-to-all returns dQ, dK, dV to the token owners, a kv head held by
+ * several members receiving the sum of their dK / dV. */
+static int hier_bwd_m(const float* q_sh, const float* k_sh, const float* v_sh,
+                      const float* do_sh, long B, int H, int Hkv, long S, int D, int A, int P,
+                      int layout, const Mask* msk, double scale, double* dq_sh, double* dk_sh,
+                      double* dv_sh) {
+  if (A < 1 || P < 1 || H % A != 0 || H % Hkv != 0) return -1;
+  const int hc = H / A, grp = H / Hkv;
+  if (hc % grp != 0 && grp % hc != 0) return -1;
+  const int nkv = hc >= grp ? hc / grp : 1;
+  long* nat_of = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  long* tmp = (long*)malloc(sizeof(long) * (S > 0 ? S : 1));
+  float* qa = (float*)malloc(sizeof(float) * A * B * S * hc * D + 1);
+  float* da = (float*)malloc(sizeof(float) * A * B * S * hc * D + 1);
+  float* ka = (float*)malloc(sizeof(float) * A * B * S * nkv * D + 1);
+  float* va = (float*)malloc(sizeof(float) * A * B * S * nkv * D + 1);
+  float* qn = (float*)malloc(sizeof(float) * B * S * hc * D + 1);
+  float* dn = (float*)malloc(sizeof(float) * B * S * hc * D + 1);
+  float* kn = (float*)malloc(sizeof(float) * B * S * nkv * D + 1);
+  float* vn = (float*)malloc(sizeof(float) * B * S * nkv * D + 1);
+  double* dqn = (double*)malloc(sizeof(double) * B * S * hc * D + 1);
+  double* dkn = (double*)malloc(sizeof(double) * B * S * nkv * D + 1);
+  double* dvn = (double*)malloc(sizeof(double) * B * S * nkv * D + 1);
+  int rc = oracle_shard_order(S, A * P, layout, nat_of);
+  if (rc == 0) rc = oracle_hier_a2a(q_sh, B, S, H, Hkv, D, A, P, layout, 0, qa);
+  if (rc == 0) rc = oracle_hier_a2a(do_sh, B, S, H, Hkv, D, A, P, layout, 0, da);
+  if (rc == 0) rc = oracle_hier_a2a(k_sh, B, S, H, Hkv, D, A, P, layout, 1, ka);
+  if (rc == 0) rc = oracle_hier_a2a(v_sh, B, S, H, Hkv, D, A, P, layout, 1, va);
+  if (rc == 0) {
+    memset(dk_sh, 0, sizeof(double) * B * S * Hkv * D);
+    memset(dv_sh, 0, sizeof(double) * B * S * Hkv * D);
+  }
+  for (int a = 0; a < A && rc == 0; ++a) {
+    int q0, nq, g0, ng;
+    ulysses_heads(a, A, H, Hkv, &q0, &nq, &g0, &ng);
+    hier_block_natural(qa + (long)a * B * S * hc * D, qn, B, S, hc, D, P, layout, tmp);
+    hier_block_natural(da + (long)a * B * S * hc * D, dn, B, S, hc, D, P, layout, tmp);
+    hier_block_natural(ka + (long)a * B * S * nkv * D, kn, B, S, nkv, D, P, layout, tmp);
+    hier_block_natural(va + (long)a * B * S * nkv * D, vn, B, S, nkv, D, P, layout, tmp);
+    attn_bwd_m(qn, kn, vn, dn, B, nq, ng, S, D, msk, scale, dqn, dkn, dvn);
+    for (long b = 0; b < B; ++b)
+      for (long p = 0; p < S; ++p) {
+        const long n = nat_of[p];
+        memcpy(dq_sh + idx4(b, p, q0, 0, S, H, D), dqn + idx4(b, n, 0, 0, S, nq, D),
+               sizeof(double) * nq * D);
+        for (long x = 0; x < (long)ng * D; ++x) {
+          dk_sh[idx4(b, p, g0, 0, S, Hkv, D) + x] += dkn[idx4(b, n, 0, 0, S, ng, D) + x];
+          dv_sh[idx4(b, p, g0, 0, S, Hkv, D) + x] += dvn[idx4(b, n, 0, 0, S, ng, D) + x];
+        }
+      }
+  }
+  free(nat_of);
+  free(tmp);
+  free(qa);
+  free(da);
+  free(ka);
+  free(va);
+  free(qn);
+  free(dn);
+  free(kn);
+  free(vn);
+  free(dqn);
+  free(dkn);
+  free(dvn);
+  return rc;
+}
+
+int oracle_hier_bwd(const float* q_sh, const float* k_sh, const float* v_sh, const float* do_sh,
+                    long B, int H, int Hkv, long S, int D, int A, int P, int layout, int causal,
+                    double scale, const long* cu, long ndocs, double* dq_sh, double* dk_sh,
+                    double* dv_sh) {
+  const Mask msk = {causal, cu, ndocs};
+  return hier_bwd_m(q_sh, k_sh, v_sh, do_sh, B, H, Hkv, S, D, A, P, layout, &msk, scale, dq_sh,
+                    dk_sh, dv_sh);
+}
+
+/* ------------------------------------------------------------------------ */
 /* Gradients                                                                 */
 /* ------------------------------------------------------------------------ */
 
@@ -1090,6 +1319,61 @@ void oracle_attn_bwd_dkdv_rows_sparse_docs(const float* q, const float* k, const
   const Mask msk = {causal, cu, ndocs};
   attn_bwd_dkdv_rows_sparse_m(q, k, v, dout, B, H, Hkv, S, D, &msk, scale, qrows, nq, krows, n,
                               dk, dv);
+}
+
+/* dK, dV of the definition on a list of key rows (b, g, j) for ANY upstream
+ * gradient dout, given the definition's output and LSE of every query row
+ * (out [B,S,H,D] and lse [B,H,S] as oracle_attn_fwd returns them):
+ * Delta_i = dout_i . out_i, P_ij = exp(s_ij - lse_i),
+ * dS_ij = P_ij (dout_i . v_j - Delta_i), dK_j = scale sum_h sum_i dS_ij q_i,
+ * dV_j = sum_h sum_i P_ij dout_i, the sums running over the query heads h
+ * that read kv head g and over every query row i that sees key j.  This is
+ * the key-row half of the gradients above with the forward state handed in,
+ * so that a long sequence's forward is computed once for many key rows.
+ * dk, dv [n, D]. */
+void oracle_attn_bwd_dkdv_rows(const float* q, const float* k, const float* v,
+                               const float* dout, long B, int H, int Hkv, long S, int D,
+                               int causal, double scale, const double* out, const double* lse,
+                               const long* krows, long n, double* dk, double* dv) {
+  const Mask msk = {causal, NULL, 0};
+  double* delta = (double*)malloc(sizeof(double) * B * H * S);
+#pragma omp parallel for schedule(static)
+  for (long row = 0; row < B * S * H; ++row) {
+    long b = row / (S * H), i = (row / H) % S;
+    int h = (int)(row % H);
+    double s = 0.0;
+    for (int d = 0; d < D; ++d) s += (double)dout[row * D + d] * out[row * D + d];
+    delta[(b * H + h) * S + i] = s;
+  }
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long a = 0; a < n; ++a) {
+    long b = krows[3 * a], j = krows[3 * a + 2];
+    int g = (int)krows[3 * a + 1];
+    const float* kj = k + idx4(b, j, g, 0, S, Hkv, D);
+    const float* vj = v + idx4(b, j, g, 0, S, Hkv, D);
+    double* dkj = dk + a * D;
+    double* dvj = dv + a * D;
+    for (int d = 0; d < D; ++d) dkj[d] = dvj[d] = 0.0;
+    for (int h = 0; h < H; ++h) {
+      if (kv_head_of(h, H, Hkv) != g) continue;
+#if ORACLE_MUTATION == 10
+      if (h != g * (H / Hkv)) continue; /* only the first query head of the group */
+#endif
+      for (long i = 0; i < S; ++i) {
+        if (!visible(&msk, i, j)) continue;
+        const float* qi = q + idx4(b, i, h, 0, S, H, D);
+        const float* doi = dout + idx4(b, i, h, 0, S, H, D);
+        long si = (b * H + h) * S + i;
+        double p = exp(scale * dot_f(qi, kj, D) - lse[si]);
+        double ds = p * (dot_f(doi, vj, D) - delta[si]);
+        for (int d = 0; d < D; ++d) {
+          dkj[d] += scale * ds * (double)qi[d];
+          dvj[d] += p * (double)doi[d];
+        }
+      }
+    }
+  }
+  free(delta);
 }
 
 /* ------------------------------------------------------------------------ */

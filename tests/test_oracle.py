@@ -29,7 +29,16 @@ mutated build of it) disagrees with an independent fact:
   from sequence to head ownership, after which a rank has all tokens of a
   head slice): the all-to-all places rank r's head slice of every token in
   natural order, and the variant equals the definition, forward and
-  backward, also when kv heads are fewer than ranks (shared kv heads).
+  backward, also when kv heads are fewer than ranks (shared kv heads);
+* hierarchical context parallelism ("Context Parallelism in MegaDLMs",
+  "Hierarchical Context Parallelism" and the a2a+p2p type of "Key-Value
+  Communication Patterns"): the first-level all-to-all puts head slice a of
+  level-two shard p on member a of group p, checked against the two levels'
+  token lists written out independently, and the whole a2a+p2p schedule
+  equals the definition, forward and backward, for level sizes [2, 2],
+  [2, 4] and [4, 2];
+* dK / dV on listed key rows from the definition's O and LSE: finite
+  differences and the sum rules.
 
 ``test_mutations_are_caught`` compiles planted mistakes into the oracle and
 checks that some pin fails for each.
@@ -198,6 +207,39 @@ def pin_sum_rules(m=0):
             np.testing.assert_allclose(dv[:, :, g].sum(axis=1),
                                        d64[:, :, heads].sum(axis=(1, 2)), atol=1e-10)
             np.testing.assert_allclose(dk[:, :, g].sum(axis=1), 0.0, atol=1e-10)
+
+
+def pin_key_rows_given_forward(m=0):
+    # dK / dV on listed key rows for a dense dO, from the definition's O and
+    # LSE: central finite differences of the brute force (two query heads on
+    # one kv head, so the sum over the group is exercised) and the sum rules
+    # over every key row of a longer problem.
+    B, H, Hkv, S, D = 1, 2, 1, 5, 3
+    q, k, v, do = small(B, H, Hkv, S, D, 43, dout=True)
+    krows = np.array([[0, 0, j] for j in range(S)])
+    for causal in (True, False):
+        out, lse = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+        dk, dv = oracle.attn_bwd_dkdv_rows(q, k, v, do, out, lse, krows, causal=causal,
+                                           mutation=m)
+        ql, kl, vl, dol = (x.astype(np.float64).tolist() for x in (q, k, v, do))
+        for name, got in (("k", dk), ("v", dv)):
+            fd = np.array(brute.finite_diff_grad(name, ql, kl, vl, dol, causal=causal))
+            np.testing.assert_allclose(got, fd[0, :, 0], rtol=0, atol=2e-8)
+    B, H, Hkv, S, D = 2, 4, 2, 40, 8
+    q, k, v, do = small(B, H, Hkv, S, D, 44, dout=True)
+    krows = np.array([[b, g, j] for b in range(B) for g in range(Hkv) for j in range(S)])
+    for causal in (True, False):
+        out, lse = oracle.attn_fwd(q, k, v, causal=causal, mutation=m)
+        dk, dv = oracle.attn_bwd_dkdv_rows(q, k, v, do, out, lse, krows, causal=causal,
+                                           mutation=m)
+        dk = dk.reshape(B, Hkv, S, D)
+        dv = dv.reshape(B, Hkv, S, D)
+        d64 = do.astype(np.float64)
+        for g in range(Hkv):
+            heads = [h for h in range(H) if h * Hkv // H == g]
+            np.testing.assert_allclose(dv[:, g].sum(axis=1), d64[:, :, heads].sum(axis=(1, 2)),
+                                       atol=1e-10)
+            np.testing.assert_allclose(dk[:, g].sum(axis=1), 0.0, atol=1e-10)
 
 
 def pin_tile_counts(m=0):
@@ -437,12 +479,83 @@ def pin_ulysses(m=0):
                     np.testing.assert_allclose(gv, rv[:, order], rtol=0, atol=1e-11)
 
 
+def _level_tokens(S, n_ranks, layout):
+    """Natural tokens of each rank, in shard order, for one level of ranks:
+    zigzag pairs chunk r with chunk 2n-1-r (the printed assignment's rule,
+    restated in the brute-force module), contiguous gives chunk r."""
+    if layout == oracle.ZIGZAG:
+        chunks = brute.zigzag_assignment(n_ranks)
+        c = S // (2 * n_ranks)
+    else:
+        chunks = [[r] for r in range(n_ranks)]
+        c = S // n_ranks
+    return [[ch * c + o for ch in rank for o in range(c)] for rank in chunks]
+
+
+HIER_SIZES = [(2, 2), (2, 4), (4, 2)]
+
+
+def pin_hier_a2a(m=0):
+    # Hierarchical context parallelism, level sizes [A, P] ("Context
+    # Parallelism in MegaDLMs", "Hierarchical Context Parallelism"): member a
+    # of group p (global rank p*A + a) holds, after the first-level
+    # all-to-all, head slice a of the tokens of level-two shard p in that
+    # shard's order.  Expected values from the two levels' token lists.
+    B, H, D = 2, 8, 4
+    for A, P in HIER_SIZES:
+        cp = A * P
+        S = 4 * cp
+        for layout in (oracle.ZIGZAG, oracle.CONTIGUOUS):
+            order = np.concatenate(_level_tokens(S, cp, layout))
+            inner = _level_tokens(S, P, layout)
+            for Hkv in (2, 4, 8):
+                for kv in (False, True):
+                    X = Hkv if kv else H
+                    x = np.arange(B * S * X * D, dtype=np.float32).reshape(B, S, X, D)
+                    try:
+                        got = oracle.hier_a2a(x[:, order], H, Hkv, A, P, layout, kv, mutation=m)
+                    except ValueError as e:
+                        raise AssertionError(f"hier_a2a refused [A={A}, P={P}]: {e}")
+                    for a in range(A):
+                        q0, nq, g0, ng = oracle.ulysses_heads(a, A, H, Hkv)
+                        x0, nx = (g0, ng) if kv else (q0, nq)
+                        want = np.concatenate([x[:, inner[p], x0:x0 + nx] for p in range(P)],
+                                              axis=1)
+                        np.testing.assert_array_equal(got[a], want)
+
+
+def pin_hier(m=0):
+    # Hierarchical (a2a+p2p) attention equals the definition, forward and
+    # backward, for every level split, layout and mask.
+    B, H, S, D = 1, 8, 32, 8
+    for A, P in HIER_SIZES:
+        for layout in (oracle.ZIGZAG, oracle.CONTIGUOUS):
+            for Hkv, causal, cu in ((2, True, None), (4, False, None), (2, True, [0, 5, 19, 32])):
+                q, k, v, do = small(B, H, Hkv, S, D, 70 + A * 10 + P, dout=True)
+                cuo = [0, S] if cu is None else cu
+                ro, rl = oracle.attn_fwd_docs(q, k, v, cuo, causal=causal, mutation=m)
+                rq, rk, rv = oracle.attn_bwd_docs(q, k, v, do, cuo, causal=causal, mutation=m)
+                order = oracle.shard_order(S, A * P, layout, mutation=m)
+                sh = lambda x: np.ascontiguousarray(x[:, order])  # noqa: E731
+                try:
+                    go, gl = oracle.hier_fwd(sh(q), sh(k), sh(v), A, P, layout, causal,
+                                             cu_seqlens=cu, mutation=m)
+                    gq, gk, gv = oracle.hier_bwd(sh(q), sh(k), sh(v), sh(do), A, P, layout,
+                                                 causal, cu_seqlens=cu, mutation=m)
+                except ValueError as e:
+                    raise AssertionError(f"hier refused [A={A}, P={P}]: {e}")
+                np.testing.assert_allclose(go, ro[:, order], rtol=0, atol=1e-12)
+                np.testing.assert_allclose(gl, rl[:, :, order], rtol=0, atol=1e-12)
+                for got, ref in ((gq, rq), (gk, rk), (gv, rv)):
+                    np.testing.assert_allclose(got, ref[:, order], rtol=0, atol=1e-11)
+
+
 PINS = [pin_zigzag_golden, pin_contiguous_golden, pin_coverage, pin_brute_force,
         pin_constant_v, pin_q_zero, pin_row0, pin_ring_invariance, pin_step_partials_merge,
-        pin_finite_differences, pin_sum_rules, pin_tile_counts, pin_docs_brute_force,
-        pin_docs_finite_differences, pin_docs_one_token_each, pin_docs_packed_equals_separate,
-        pin_docs_single_and_ring, pin_docs_tile_counts, pin_allgather, pin_ulysses_a2a,
-        pin_ulysses]
+        pin_finite_differences, pin_sum_rules, pin_key_rows_given_forward, pin_tile_counts,
+        pin_docs_brute_force, pin_docs_finite_differences, pin_docs_one_token_each,
+        pin_docs_packed_equals_separate, pin_docs_single_and_ring, pin_docs_tile_counts,
+        pin_allgather, pin_ulysses_a2a, pin_ulysses, pin_hier_a2a, pin_hier]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -520,7 +633,9 @@ MUTATIONS = {1: "wrong zigzag pairing", 2: "interleaved GQA head map",
              3: "causal diagonal dropped", 4: "softmax scale dropped",
              5: "merge term dropped", 6: "ring turned the other way",
              7: "document border off by one", 8: "all-gather reduce drops a rank",
-             9: "Ulysses kv heads of the wrong rank"}
+             9: "Ulysses kv heads of the wrong rank",
+             10: "key-row gradients drop a query head of the group",
+             11: "hierarchical groups of strided ranks (wrong level)"}
 
 
 @pytest.mark.parametrize("m", sorted(MUTATIONS), ids=[MUTATIONS[m] for m in sorted(MUTATIONS)])
