@@ -20,8 +20,12 @@ The same run times the packed-document workload (S=131072, documents of mean
 length 8192) forward and backward and reports it under "docs", and the
 S=131072 workload through the all-gather K/V schedule (K/V gathered into
 natural order, one pass per rank, gathered dK/dV returned to their owners)
-under "allgather", and through the Ulysses variant (all-to-all to head
-ownership, full attention per head slice, all-to-all back) under "ulysses";
+under "allgather", through the Ulysses variant (all-to-all to head
+ownership, full attention per head slice, all-to-all back) under "ulysses",
+and through the hierarchical a2a+p2p schedule with level sizes [4, 4] under
+"hierarchical"; the forwards of the other named workloads (S=256 float32,
+S=8192 zigzag and contiguous with their kernel censuses, S=16384 full
+attention at cp 1, 2, 4, 8) are timed alone under "named_forwards";
 ``--workload docs_bf16_s131072_fwdbwd`` makes it the main line (its step adds
 the document-bounds kernel and uses the document-rule forward/backward).
 
@@ -56,9 +60,9 @@ ALL_WORKLOADS = {**inputs.WORKLOADS, **inputs.DOC_WORKLOADS}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum), from
-# one single-pass ncu capture of the current kernels on the full workload
-# (profiles/dram_traffic_c5_fwdbwd_b1_h32_hkv8_s131072_cp16.md).  Null for a
-# workload without a capture; must be re-taken whenever a kernel changes.
+# one single-pass ncu capture of the current kernels on the full workload.
+# Null for a workload without a capture; must be re-taken whenever a kernel
+# changes.
 CAPTURED_TRAFFIC = {
     "c5_bf16_s131072_fwdbwd": {
         "ring_bwd": (2.148e9 + 0.016e9) + (33.108e9 + 4.277e9) + (5.553e9 + 2.119e9)
@@ -383,6 +387,14 @@ def run_ours(args):
         ul_info = time_ulysses(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
                                (qs, ks, vs, dos))
 
+    hier_info = None
+    if docs is None and not args.no_hier and w.backward and cp == 16:
+        hier_info = time_hier(cpa, w, dev, stream, args.warmup, max(args.steps, 5), peak,
+                              (qs, ks, vs, dos), (4, 4))
+    named = None
+    if not args.no_named:
+        named = time_named_forwards(cpa, dev, stream, args.warmup, max(args.steps, 10), peak)
+
     path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype)
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -403,7 +415,8 @@ def run_ours(args):
                    "useful_tflop_per_step": step_flops / 1e12},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
         "roofline": roofline, "kernels": fwd_info, "c3_forward": c3, "docs": docs_info,
-        "allgather": ag_info, "ulysses": ul_info, "hbm_kernels": hbm_info,
+        "allgather": ag_info, "ulysses": ul_info, "hierarchical": hier_info,
+        "named_forwards": named, "hbm_kernels": hbm_info,
         "cpu_baseline": cpu,
         "status": cpa.device_status(),
     }
@@ -511,6 +524,73 @@ def time_forward(cpa, w, dev, stream, warmup, steps, peak):
     return {"workload": w.name, "ms_median": ms, "ms_min": min(times), "tflops": tf,
             "frac": tf / peak, "path": "tcgen05" if path == 1 else "simt", "tile": tile,
             "zigzag_step_imbalance_max_over_mean": imbalance}
+
+
+def census_balance(counts):
+    """Per-step balance of a kernel census tiles[r, t]: the worst step's
+    max/mean over ranks, and the lockstep efficiency sum_t mean_t / sum_t
+    max_t (the share of rank-steps doing work when every step waits for its
+    slowest rank)."""
+    c = np.asarray(counts, dtype=np.float64)
+    mx, mean = c.max(axis=0), c.mean(axis=0)
+    worst = float(np.max(np.where(mean > 0, mx / np.maximum(mean, 1e-30), 1.0)))
+    return {"worst_step_max_over_mean": worst, "lockstep_efficiency": float(mean.sum() / mx.sum())}
+
+
+def time_named_forwards(cpa, dev, stream, warmup, steps, peak):
+    """The forward of every named workload that the main line does not time:
+    the S=256 float32 one, the S=8192 one in both layouts (with the kernel's
+    own census of each), and the S=16384 full-attention one at every ring
+    size of its sweep.  Median of `steps` calls, CUDA events on the
+    launching stream, clocks sampled over the whole section."""
+    gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    clk = ClockSampler(gpu_id)
+    clk.start()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        return statistics.median(times), min(times)
+
+    def one(w, cp, layout):
+        q, k, v, _ = inputs.generate(w, with_dout=False)
+        qs, ks, vs = (cpa.zigzag_permute(x.to(dev), cp, layout) for x in (q, k, v))
+        o = torch.empty_like(qs)
+        lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+        ms, ms_min = timed(lambda: cpa.ring_fwd(qs, ks, vs, cp, layout, w.causal, out=o, lse=lse))
+        tf = w.useful_flops(False) / (ms * 1e-3) / 1e12
+        path, tile = cpa.plan(w.B, w.H, w.Hkv, w.S, w.D, cp, layout, w.causal, w.dtype)
+        res = {"cp": cp, "layout": "zigzag" if layout == cpa.ZIGZAG else "contiguous",
+               "ms_median": ms, "ms_min": ms_min, "tflops": tf, "frac": tf / peak,
+               "path": "tcgen05" if path == cpa.PATH_TCGEN05 else "simt", "tile": tile}
+        if w.causal:
+            counts = torch.zeros((cp, cp), device=dev, dtype=torch.int64)
+            cpa.ring_fwd(qs, ks, vs, cp, layout, w.causal, out=o, lse=lse, tiles_rt=counts)
+            res["census"] = census_balance(counts.cpu().numpy())
+        return res
+
+    out = {}
+    w1 = inputs.WORKLOADS["c1_fp32_s256"]
+    out[w1.name] = one(w1, w1.cp, w1.layout)
+    w2 = inputs.WORKLOADS["c2_bf16_s8192"]
+    out[w2.name] = {"zigzag": one(w2, w2.cp, cpa.ZIGZAG),
+                    "contiguous": one(w2, w2.cp, cpa.CONTIGUOUS)}
+    w4 = inputs.WORKLOADS["c4_bf16_s16384_bidir"]
+    out[w4.name] = {f"cp{cp}": one(w4, cp, w4.layout) for cp in w4.cp_sweep}
+    out["clocks"] = clk.stop()
+    out["status"] = cpa.device_status()
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_docs(cpa, w, dev, stream, warmup, steps, peak):
@@ -654,6 +734,57 @@ def time_ulysses(cpa, w, dev, stream, warmup, steps, peak, sharded):
             "grad_dtype": "f32", "status": cpa.device_status()}
 
 
+def time_hier(cpa, w, dev, stream, warmup, steps, peak, sharded, split):
+    """The hierarchical (a2a+p2p) schedule on sharded inputs with level sizes
+    `split` = (cp_a2a, cp_p2p), forward and backward calls (each includes its
+    all-to-alls), timed with CUDA events (median of `steps`)."""
+    A, P = split
+    qs, ks, vs, dos = sharded
+    o = torch.empty_like(qs)
+    lse = torch.empty((w.B, w.H, w.S), device=dev, dtype=torch.float32)
+    g = [torch.empty(x.shape, device=dev, dtype=torch.float32) for x in (qs, ks, vs)]
+    code = cpa.BF16 if w.dtype == torch.bfloat16 else cpa.F32
+    wf = torch.empty(cpa.hier_workspace_bytes(w.B, w.H, w.Hkv, w.S, w.D, A, P, w.layout, code,
+                                              False), device=dev, dtype=torch.uint8)
+    wb = torch.empty(cpa.hier_workspace_bytes(w.B, w.H, w.Hkv, w.S, w.D, A, P, w.layout,
+                                              code | cpa.GRAD_F32, True),
+                     device=dev, dtype=torch.uint8)
+    parts = {
+        "fwd": lambda: cpa.hier_fwd(qs, ks, vs, A, P, w.layout, w.causal, out=o, lse=lse,
+                                    workspace=wf),
+        "bwd": lambda: cpa.hier_bwd(qs, ks, vs, o, dos, lse, A, P, w.layout, w.causal,
+                                    dq=g[0], dk=g[1], dv=g[2], workspace=wb,
+                                    grad_dtype=torch.float32),
+    }
+    res = {}
+    for name, fn in parts.items():
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        times = []
+        for _ in range(steps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.median(times)
+    fwd_tf = w.useful_flops(False) / (res["fwd"] * 1e-3) / 1e12
+    bwd_tf = w.useful_flops(True) / (res["bwd"] * 1e-3) / 1e12
+    hc, nkv = cpa._binding.ulysses_heads(w.H, w.Hkv, A)
+    del wf, wb, g
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "schedule": f"hierarchical a2a+p2p [{A}, {P}]", "ms": res,
+            "heads_per_member": hc, "kv_heads_per_member": nkv,
+            "forward": {"tflops": fwd_tf, "frac": fwd_tf / peak},
+            "backward": {"tflops": bwd_tf, "frac": bwd_tf / peak},
+            "fwd_bwd_tflops": (w.useful_flops(False) + w.useful_flops(True))
+            / ((res["fwd"] + res["bwd"]) * 1e-3) / 1e12,
+            "grad_dtype": "f32", "status": cpa.device_status()}
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores
 # ---------------------------------------------------------------------------
@@ -778,6 +909,8 @@ def main():
     ap.add_argument("--no-allgather", action="store_true")
     ap.add_argument("--no-ulysses", action="store_true")
     ap.add_argument("--no-hbm", action="store_true")
+    ap.add_argument("--no-hier", action="store_true")
+    ap.add_argument("--no-named", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

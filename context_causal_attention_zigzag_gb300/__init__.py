@@ -8,7 +8,9 @@ Python binding.  ``inputs`` holds the seeded synthetic workloads.
 """
 from ._binding import (  # noqa: F401
     BF16, CONTIGUOUS, F32, GRAD_F32, PATH_SIMT, PATH_TCGEN05, ZIGZAG, CpattnError,
-    allgather_bwd, allgather_fwd, attention, attention_allgather_fwd_bwd, attention_docs, attention_docs_fwd_bwd, attention_fwd_bwd, device_status, doc_bounds, lib,
+    allgather_bwd, allgather_fwd, attention, attention_allgather_fwd_bwd, attention_docs,
+    attention_docs_fwd_bwd, attention_fwd_bwd, device_status, doc_bounds, lib,
+    hier_a2a, hier_fwd, hier_bwd, hier_workspace_bytes, attention_hier_fwd_bwd,
     lse_merge, padded_length, plan, ring_bwd, ring_bwd_docs, ring_bwd_noalloc,
     ring_bwd_workspace_bytes, ring_fwd, ring_fwd_census, ring_fwd_docs, ring_fwd_docs_census,
     ring_fwd_step, status_string, tile_counts, zigzag_permute, zigzag_permute_pad,

@@ -47,6 +47,11 @@ SIGNATURES = {
     "cpattn_ulysses_workspace_bytes": (_sz, [_i] * 9),
     "cpattn_ulysses_fwd": (_i, [_vp] * 5 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_ulysses_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _vp, _sz, _vp]),
+    "cpattn_hier_a2a": (_i, [_vp, _vp] + [_i] * 11 + [_vp]),
+    "cpattn_hier_lse_a2a": (_i, [_vp, _vp] + [_i] * 7 + [_vp]),
+    "cpattn_hier_workspace_bytes": (_sz, [_i] * 10),
+    "cpattn_hier_fwd": (_i, [_vp] * 5 + [_i] * 10 + [_f, _vp, _vp, _sz, _vp]),
+    "cpattn_hier_bwd": (_i, [_vp] * 9 + [_i] * 10 + [_f, _vp, _vp, _sz, _vp]),
     "cpattn_attention_host_workspace_bytes": (_sz, [_i] * 9),
     "cpattn_attention_host_parts": (_i, [_i] * 5),
     "cpattn_attention_host_docs_workspace_bytes": (_sz, [_i] * 9),
@@ -585,6 +590,80 @@ def ulysses_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=N
 
 
 # ---------------------------------------------------------------------------
+# Hierarchical a2a+p2p (all-to-all inside groups, ring across them)
+# ---------------------------------------------------------------------------
+
+def hier_a2a(x, cp_a2a, cp_p2p, H, Hkv, layout=ZIGZAG, kv_heads=False, to_seq=False, out=None):
+    """The first-level all-to-all (cpattn_hier_a2a).  Sequence -> head: x
+    [B,S,X,D] sharded over cp_a2a*cp_p2p ranks -> [cp_a2a, B, S, nx, D], the
+    sequence axis in the second level's sharded order; head -> sequence: the
+    inverse (shared kv heads summed)."""
+    _need_cuda(x)
+    hc, nkv = ulysses_heads(H, Hkv, cp_a2a)
+    nx = nkv if kv_heads else hc
+    if to_seq:
+        _, B, S, _, D = x.shape
+        shape = (B, S, Hkv if kv_heads else H, D)
+    else:
+        B, S, _, D = x.shape
+        shape = (cp_a2a, B, S, nx, D)
+    if out is None:
+        out = torch.empty(shape, device=x.device, dtype=x.dtype)
+    _need_cuda(out)
+    rc = lib().cpattn_hier_a2a(_ptr(x), _ptr(out), B, S, H, Hkv, D, int(cp_a2a), int(cp_p2p),
+                               int(layout), int(bool(kv_heads)), int(bool(to_seq)),
+                               _dtype_code(x), _stream(x))
+    _check("cpattn_hier_a2a", rc)
+    return out
+
+
+def hier_workspace_bytes(B, H, Hkv, S, D, cp_a2a, cp_p2p, layout=ZIGZAG, dtype=BF16,
+                         backward=False):
+    return int(lib().cpattn_hier_workspace_bytes(B, H, Hkv, S, D, int(cp_a2a), int(cp_p2p),
+                                                 int(layout), int(dtype), int(bool(backward))))
+
+
+def hier_fwd(q, k, v, cp_a2a, cp_p2p, layout=ZIGZAG, causal=True, scale=None, bounds=None,
+             out=None, lse=None, workspace=None):
+    """The hierarchical schedule on tensors sharded over cp_a2a*cp_p2p ranks;
+    returns (out, lse) in the same order."""
+    _need_cuda(q, k, v, bounds)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), device=q.device, dtype=torch.float32)
+    need = hier_workspace_bytes(B, H, Hkv, S, D, cp_a2a, cp_p2p, layout, _dtype_code(q), False)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(out, lse, workspace)
+    rc = lib().cpattn_hier_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Hkv, S, D,
+                               int(cp_a2a), int(cp_p2p), int(layout), int(bool(causal)),
+                               _dtype_code(q), _scale(scale), _ptr(bounds), _ptr(workspace),
+                               workspace.numel(), _stream(q))
+    _check("cpattn_hier_fwd", rc)
+    return out, lse
+
+
+def hier_bwd(q, k, v, out, dout, lse, cp_a2a, cp_p2p, layout=ZIGZAG, causal=True, scale=None,
+             bounds=None, dq=None, dk=None, dv=None, workspace=None, grad_dtype=None):
+    """Backward of the hierarchical schedule on sharded-order tensors."""
+    _need_cuda(q, k, v, out, dout, lse, bounds)
+    B, H, Hkv, S, D = _shape(q, k, v)
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
+    need = hier_workspace_bytes(B, H, Hkv, S, D, cp_a2a, cp_p2p, layout, code, True)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
+    _need_cuda(dq, dk, dv, workspace)
+    rc = lib().cpattn_hier_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp_a2a),
+                               int(cp_p2p), int(layout), int(bool(causal)), code, _scale(scale),
+                               _ptr(bounds), _ptr(workspace), workspace.numel(), _stream(q))
+    _check("cpattn_hier_bwd", rc)
+    return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
 # census and status
 # ---------------------------------------------------------------------------
 
@@ -794,3 +873,17 @@ def attention_host_docs(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causa
         _ptr(workspace), workspace.numel(), st)
     _check("cpattn_attention_host_docs", rc)
     return res if backward else res[:2]
+
+
+def attention_hier_fwd_bwd(q, k, v, dout, cp_a2a, cp_p2p, layout=ZIGZAG, causal=True,
+                           scale=None, grad_dtype=None):
+    """Natural order in and out through the hierarchical schedule: shard over
+    cp_a2a*cp_p2p ranks, all-to-all inside groups, second-level ring,
+    backward, all-to-all back, unshard.  Returns (out, lse, dq, dk, dv)."""
+    cp = cp_a2a * cp_p2p
+    qs, ks, vs, dos = (zigzag_permute(x, cp, layout) for x in (q, k, v, dout))
+    o, lse = hier_fwd(qs, ks, vs, cp_a2a, cp_p2p, layout, causal, scale)
+    dq, dk, dv = hier_bwd(qs, ks, vs, o, dos, lse, cp_a2a, cp_p2p, layout, causal, scale,
+                          grad_dtype=grad_dtype)
+    un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
+    return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dk), un(dv)

@@ -370,87 +370,101 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-// Ulysses: the sharded sequence layout, heads per rank and kv heads per rank.
-int ulysses_shape(int B, int H, int Hkv, int S, int D, int cp, int layout, int* hc, int* nkv,
-                  RingShape* sh) {
-  int rc = make_shape(B, H, Hkv, S, D, cp, layout, 1, 0.f, sh);
+// Sequence <-> head all-to-all schedules.  The hierarchical (a2a+p2p)
+// schedule has level sizes [A, P], cp = A * P: an all-to-all inside groups
+// of A consecutive ranks, then the ring of the second level over the P
+// groups.  The Ulysses variant is its one-level case [cp, 1] (the ring is
+// then a single rank attending to the whole sequence).
+struct A2aPlan {
+  RingShape sh;     // the sequence owners: cp = A * P ranks, the caller's layout
+  RingShape inner;  // the second level's order on the head owners' side
+  int A, P;
+  int hc, nkv;      // query heads and kv heads per head owner
+  int inner_layout;
+};
+
+int a2a_plan(int B, int H, int Hkv, int S, int D, int A, int P, int layout, A2aPlan* pl) {
+  if (A < 1 || P < 1 || (long long)A * P > (1 << 20)) return CPATTN_ERR_INVALID_ARG;
+  int rc = make_shape(B, H, Hkv, S, D, A * P, layout, 1, 0.f, &pl->sh);
   if (rc != CPATTN_OK) return rc;
-  if (H % cp != 0) return CPATTN_ERR_INVALID_ARG;
-  const int h = H / cp, grp = H / Hkv;
+  if (H % A != 0) return CPATTN_ERR_INVALID_ARG;
+  const int h = H / A, grp = H / Hkv;
   if (h % grp != 0 && grp % h != 0) return CPATTN_ERR_INVALID_ARG;
-  *hc = h;
-  *nkv = h >= grp ? h / grp : 1;
+  // With one group of the second level the ring is one rank: keep the
+  // sequence in natural order.
+  pl->inner_layout = P == 1 ? CPATTN_LAYOUT_CONTIGUOUS : layout;
+  rc = make_shape(B, H, Hkv, S, D, P, pl->inner_layout, 1, 0.f, &pl->inner);
+  if (rc != CPATTN_OK) return rc;
+  pl->A = A;
+  pl->P = P;
+  pl->hc = h;
+  pl->nkv = h >= grp ? h / grp : 1;
   return CPATTN_OK;
 }
 
-A2aShape a2a_shape(const RingShape& sh, int B, int H, int Hkv, int hc, int nkv, bool kv) {
+A2aShape a2a_shape(const A2aPlan& pl, int B, int H, int Hkv, bool kv) {
   A2aShape a;
-  a.sh = sh;
+  a.sh = pl.sh;
+  a.inner = pl.inner;
+  a.ranks = pl.A;
   a.B = B;
-  a.D = sh.D;
+  a.D = pl.sh.D;
   a.X = kv ? Hkv : H;
-  a.nx = kv ? nkv : hc;
-  a.x_num = hc;
+  a.nx = kv ? pl.nkv : pl.hc;
+  a.x_num = pl.hc;
   a.x_den = kv ? H / Hkv : 1;
   return a;
 }
 
-struct UlyssesWs {
+struct A2aWs {
   size_t q, kv, lse, grad_q, grad_kv, inner, total;
 };
 
-UlyssesWs ulysses_ws(int B, int H, int Hkv, int S, int D, int dtype, bool backward, int cp,
-                     int hc, int nkv) {
-  UlyssesWs w;
+A2aWs a2a_ws(const A2aPlan& pl, int B, int H, int S, int D, int dtype, bool backward) {
+  A2aWs w;
   const int in_dtype = dtype & ~CPATTN_GRAD_F32;
   const size_t elt = in_dtype == CPATTN_BF16 ? 2 : 4;
   const size_t gelt = (dtype & CPATTN_GRAD_F32) ? 4 : elt;
-  const size_t rows = (size_t)cp * B * S;
-  w.q = align256(rows * hc * D * elt);
-  w.kv = align256(rows * nkv * D * elt);
+  const size_t rows = (size_t)pl.A * B * S;
+  w.q = align256(rows * pl.hc * D * elt);
+  w.kv = align256(rows * pl.nkv * D * elt);
   w.lse = align256((size_t)B * H * S * sizeof(float));
-  w.grad_q = backward ? align256(rows * hc * D * gelt) : 0;
-  w.grad_kv = backward ? align256(rows * nkv * D * gelt) : 0;
-  w.inner = backward ? align256(cpattn_ring_bwd_workspace_bytes(cp * B, hc, nkv, S, D, dtype))
+  w.grad_q = backward ? align256(rows * pl.hc * D * gelt) : 0;
+  w.grad_kv = backward ? align256(rows * pl.nkv * D * gelt) : 0;
+  w.inner = backward ? align256(cpattn_ring_bwd_workspace_bytes(pl.A * B, pl.hc, pl.nkv, S, D,
+                                                                dtype))
                      : 0;
   // q-like: q, o (+ dO, dQ); kv-like: k, v (+ dK, dV)
   w.total = (backward ? 3 : 2) * w.q + 2 * w.kv + w.lse + w.grad_q + 2 * w.grad_kv + w.inner;
   return w;
 }
 
-}  // namespace
-
-extern "C" {
-
-int cpattn_ulysses_a2a(const void* in, void* out, int B, int S, int H, int Hkv, int D,
-                       int cp_size, int layout, int kv_heads, int to_seq, int dtype,
-                       cpattn_stream_t stream) {
-  RingShape sh;
-  int hc = 0, nkv = 0;
-  int rc = ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh);
+int a2a_copy(const void* in, void* out, int B, int S, int H, int Hkv, int D, int A, int P,
+             int layout, int kv_heads, int to_seq, int dtype, cudaStream_t stream) {
+  A2aPlan pl;
+  int rc = a2a_plan(B, H, Hkv, S, D, A, P, layout, &pl);
   if (rc != CPATTN_OK) return rc;
   if ((dtype != CPATTN_F32 && dtype != CPATTN_BF16) || (kv_heads != 0 && kv_heads != 1) ||
       (to_seq != 0 && to_seq != 1))
     return CPATTN_ERR_INVALID_ARG;
   if ((long long)B * S == 0) return CPATTN_OK;
   if (!in || !out || !aligned16(in) || !aligned16(out)) return CPATTN_ERR_INVALID_ARG;
-  const A2aShape a = a2a_shape(sh, B, H, Hkv, hc, nkv, kv_heads != 0);
+  const A2aShape a = a2a_shape(pl, B, H, Hkv, kv_heads != 0);
   const size_t elt = dtype == CPATTN_BF16 ? 2 : 4;
-  const size_t big = (size_t)cp_size * B * S * a.nx * D * elt;
+  const size_t big = (size_t)A * B * S * a.nx * D * elt;
   const size_t small = (size_t)B * S * a.X * D * elt;
   const char* x = static_cast<const char*>(in);
   const char* y = static_cast<const char*>(out);
   const size_t in_b = to_seq ? big : small, out_b = to_seq ? small : big;
   if (x < y + out_b && y < x + in_b) return CPATTN_ERR_INVALID_ARG;
-  cudaError_t e = launch_a2a(in, out, a, to_seq != 0, dtype, (cudaStream_t)stream);
+  cudaError_t e = launch_a2a(in, out, a, to_seq != 0, dtype, stream);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-int cpattn_ulysses_lse_a2a(const float* in, float* out, int B, int S, int H, int cp_size,
-                           int layout, int to_seq, cpattn_stream_t stream) {
-  RingShape sh;
-  int hc = 0, nkv = 0;
-  int rc = ulysses_shape(B, H, H, S, 64, cp_size, layout, &hc, &nkv, &sh);
+int a2a_lse_copy(const float* in, float* out, int B, int S, int H, int A, int P, int layout,
+                 int to_seq, cudaStream_t stream) {
+  A2aPlan pl;
+  int rc = a2a_plan(B, H, H, S, 64, A, P, layout, &pl);
   if (rc != CPATTN_OK) return rc;
   if (to_seq != 0 && to_seq != 1) return CPATTN_ERR_INVALID_ARG;
   if ((long long)B * S == 0) return CPATTN_OK;
@@ -459,25 +473,26 @@ int cpattn_ulysses_lse_a2a(const float* in, float* out, int B, int S, int H, int
   const char* x = reinterpret_cast<const char*>(in);
   const char* y = reinterpret_cast<const char*>(out);
   if (x < y + bytes && y < x + bytes) return CPATTN_ERR_INVALID_ARG;
-  cudaError_t e = launch_lse_a2a(in, out, sh, B, H, to_seq != 0, (cudaStream_t)stream);
+  cudaError_t e = launch_lse_a2a(in, out, pl.sh, pl.inner, A, B, H, to_seq != 0, stream);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
-size_t cpattn_ulysses_workspace_bytes(int B, int H, int Hkv, int S, int D, int cp_size,
-                                      int layout, int dtype, int backward) {
-  RingShape sh;
-  int hc = 0, nkv = 0;
-  if (ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh) != CPATTN_OK) return 0;
-  return ulysses_ws(B, H, Hkv, S, D, dtype, backward != 0, cp_size, hc, nkv).total;
+size_t a2a_workspace_bytes(int B, int H, int Hkv, int S, int D, int A, int P, int layout,
+                           int dtype, int backward) {
+  A2aPlan pl;
+  if (a2a_plan(B, H, Hkv, S, D, A, P, layout, &pl) != CPATTN_OK) return 0;
+  return a2a_ws(pl, B, H, S, D, dtype, backward != 0).total;
 }
 
-int cpattn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
-                       int B, int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
-                       int dtype, float softmax_scale, const int32_t* doc_bounds,
-                       void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
-  RingShape sh;
-  int hc = 0, nkv = 0;
-  int rc = ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh);
+// All-to-all to the head owners, the ring of the second level on every head
+// owner's slice in ONE launch of the ring kernels (the head owners stacked
+// along the batch axis, cp = P), all-to-all back.
+int a2a_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+            int Hkv, int S, int D, int A, int P, int layout, int causal, int dtype,
+            float softmax_scale, const int32_t* doc_bounds, void* workspace,
+            size_t workspace_bytes, cudaStream_t st) {
+  A2aPlan pl;
+  int rc = a2a_plan(B, H, Hkv, S, D, A, P, layout, &pl);
   if (rc != CPATTN_OK) return rc;
   if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return CPATTN_ERR_INVALID_ARG;
@@ -485,7 +500,7 @@ int cpattn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, f
   if (!q || !k || !v || !out || !lse) return CPATTN_ERR_INVALID_ARG;
   const int2* docs = nullptr;
   if (!doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
-  const UlyssesWs w = ulysses_ws(B, H, Hkv, S, D, dtype, false, cp_size, hc, nkv);
+  const A2aWs w = a2a_ws(pl, B, H, S, D, dtype, false);
   if (workspace == nullptr || workspace_bytes < w.total ||
       (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return CPATTN_ERR_WORKSPACE;
@@ -495,33 +510,25 @@ int cpattn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, f
   void* wk = p + 2 * w.q;
   void* wv = p + 2 * w.q + w.kv;
   float* wl = reinterpret_cast<float*>(p + 2 * w.q + 2 * w.kv);
-  cudaStream_t st = (cudaStream_t)stream;
-  // All-to-all: sequence owners -> head owners.
-  rc = cpattn_ulysses_a2a(q, wq, B, S, H, Hkv, D, cp_size, layout, 0, 0, dtype, stream);
-  if (rc == CPATTN_OK)
-    rc = cpattn_ulysses_a2a(k, wk, B, S, H, Hkv, D, cp_size, layout, 1, 0, dtype, stream);
-  if (rc == CPATTN_OK)
-    rc = cpattn_ulysses_a2a(v, wv, B, S, H, Hkv, D, cp_size, layout, 1, 0, dtype, stream);
+  rc = a2a_copy(q, wq, B, S, H, Hkv, D, A, P, layout, 0, 0, dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_copy(k, wk, B, S, H, Hkv, D, A, P, layout, 1, 0, dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_copy(v, wv, B, S, H, Hkv, D, A, P, layout, 1, 0, dtype, st);
   if (rc != CPATTN_OK) return rc;
-  // Each rank: full attention over the whole sequence for its heads (the
-  // ranks stacked along the batch axis, one launch).
-  rc = fwd_common(wq, wk, wv, wo, wl, cp_size * B, hc, nkv, S, D, 1, CPATTN_LAYOUT_CONTIGUOUS,
-                  causal, dtype, softmax_scale, 0, 1, 0, nullptr, docs, 0, st);
+  rc = fwd_common(wq, wk, wv, wo, wl, A * B, pl.hc, pl.nkv, S, D, P, pl.inner_layout, causal,
+                  dtype, softmax_scale, 0, 1, 0, nullptr, docs, 0, st);
   if (rc != CPATTN_OK) return rc;
-  // Back to the sequence owners.
-  rc = cpattn_ulysses_a2a(wo, out, B, S, H, Hkv, D, cp_size, layout, 0, 1, dtype, stream);
+  rc = a2a_copy(wo, out, B, S, H, Hkv, D, A, P, layout, 0, 1, dtype, st);
   if (rc != CPATTN_OK) return rc;
-  return cpattn_ulysses_lse_a2a(wl, lse, B, S, H, cp_size, layout, 1, stream);
+  return a2a_lse_copy(wl, lse, B, S, H, A, P, layout, 1, st);
 }
 
-int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, const void* out,
-                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
-                       int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
-                       int dtype, float softmax_scale, const int32_t* doc_bounds,
-                       void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
-  RingShape sh;
-  int hc = 0, nkv = 0;
-  int rc = ulysses_shape(B, H, Hkv, S, D, cp_size, layout, &hc, &nkv, &sh);
+int a2a_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+            const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int S, int D,
+            int A, int P, int layout, int causal, int dtype, float softmax_scale,
+            const int32_t* doc_bounds, void* workspace, size_t workspace_bytes,
+            cudaStream_t st) {
+  A2aPlan pl;
+  int rc = a2a_plan(B, H, Hkv, S, D, A, P, layout, &pl);
   if (rc != CPATTN_OK) return rc;
   const int in_dtype = dtype & ~CPATTN_GRAD_F32;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
@@ -531,7 +538,7 @@ int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, const void* 
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) return CPATTN_ERR_INVALID_ARG;
   const int2* docs = nullptr;
   if (!doc_ptr(doc_bounds, &docs)) return CPATTN_ERR_INVALID_ARG;
-  const UlyssesWs w = ulysses_ws(B, H, Hkv, S, D, dtype, true, cp_size, hc, nkv);
+  const A2aWs w = a2a_ws(pl, B, H, S, D, dtype, true);
   if (workspace == nullptr || workspace_bytes < w.total ||
       (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return CPATTN_ERR_WORKSPACE;
@@ -547,30 +554,97 @@ int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, const void* 
   void* wdk = g + w.grad_q;
   void* wdv = g + w.grad_q + w.grad_kv;
   void* inner = g + w.grad_q + 2 * w.grad_kv;
-  cudaStream_t st = (cudaStream_t)stream;
   const void* src_q[3] = {q, out, dout};
   void* dst_q[3] = {wq, wo, wdo};
   for (int i = 0; i < 3 && rc == CPATTN_OK; ++i)
-    rc = cpattn_ulysses_a2a(src_q[i], dst_q[i], B, S, H, Hkv, D, cp_size, layout, 0, 0, in_dtype,
-                            stream);
-  if (rc == CPATTN_OK)
-    rc = cpattn_ulysses_a2a(k, wk, B, S, H, Hkv, D, cp_size, layout, 1, 0, in_dtype, stream);
-  if (rc == CPATTN_OK)
-    rc = cpattn_ulysses_a2a(v, wv, B, S, H, Hkv, D, cp_size, layout, 1, 0, in_dtype, stream);
-  if (rc == CPATTN_OK) rc = cpattn_ulysses_lse_a2a(lse, wl, B, S, H, cp_size, layout, 0, stream);
+    rc = a2a_copy(src_q[i], dst_q[i], B, S, H, Hkv, D, A, P, layout, 0, 0, in_dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_copy(k, wk, B, S, H, Hkv, D, A, P, layout, 1, 0, in_dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_copy(v, wv, B, S, H, Hkv, D, A, P, layout, 1, 0, in_dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_lse_copy(lse, wl, B, S, H, A, P, layout, 0, st);
   if (rc != CPATTN_OK) return rc;
-  rc = bwd_common(wq, wk, wv, wo, wdo, wl, wdq, wdk, wdv, cp_size * B, hc, nkv, S, D, 1,
-                  CPATTN_LAYOUT_CONTIGUOUS, causal, dtype, softmax_scale, docs, 0, inner,
-                  w.inner, st);
+  rc = bwd_common(wq, wk, wv, wo, wdo, wl, wdq, wdk, wdv, A * B, pl.hc, pl.nkv, S, D, P,
+                  pl.inner_layout, causal, dtype, softmax_scale, docs, 0, inner, w.inner, st);
   if (rc != CPATTN_OK) return rc;
-  // Back to the sequence owners; a kv head held by several ranks gets the
-  // sum of their dK / dV.
-  rc = cpattn_ulysses_a2a(wdq, dq, B, S, H, Hkv, D, cp_size, layout, 0, 1, out_dtype, stream);
-  if (rc == CPATTN_OK)
-    rc = cpattn_ulysses_a2a(wdk, dk, B, S, H, Hkv, D, cp_size, layout, 1, 1, out_dtype, stream);
-  if (rc == CPATTN_OK)
-    rc = cpattn_ulysses_a2a(wdv, dv, B, S, H, Hkv, D, cp_size, layout, 1, 1, out_dtype, stream);
+  // Back to the sequence owners; a kv head held by several head owners gets
+  // the sum of their dK / dV.
+  rc = a2a_copy(wdq, dq, B, S, H, Hkv, D, A, P, layout, 0, 1, out_dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_copy(wdk, dk, B, S, H, Hkv, D, A, P, layout, 1, 1, out_dtype, st);
+  if (rc == CPATTN_OK) rc = a2a_copy(wdv, dv, B, S, H, Hkv, D, A, P, layout, 1, 1, out_dtype, st);
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cpattn_ulysses_a2a(const void* in, void* out, int B, int S, int H, int Hkv, int D,
+                       int cp_size, int layout, int kv_heads, int to_seq, int dtype,
+                       cpattn_stream_t stream) {
+  return a2a_copy(in, out, B, S, H, Hkv, D, cp_size, 1, layout, kv_heads, to_seq, dtype,
+                  (cudaStream_t)stream);
+}
+
+int cpattn_ulysses_lse_a2a(const float* in, float* out, int B, int S, int H, int cp_size,
+                           int layout, int to_seq, cpattn_stream_t stream) {
+  return a2a_lse_copy(in, out, B, S, H, cp_size, 1, layout, to_seq, (cudaStream_t)stream);
+}
+
+size_t cpattn_ulysses_workspace_bytes(int B, int H, int Hkv, int S, int D, int cp_size,
+                                      int layout, int dtype, int backward) {
+  return a2a_workspace_bytes(B, H, Hkv, S, D, cp_size, 1, layout, dtype, backward);
+}
+
+int cpattn_ulysses_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int B, int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
+                       int dtype, float softmax_scale, const int32_t* doc_bounds,
+                       void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
+  return a2a_fwd(q, k, v, out, lse, B, H, Hkv, S, D, cp_size, 1, layout, causal, dtype,
+                 softmax_scale, doc_bounds, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                       int H, int Hkv, int S, int D, int cp_size, int layout, int causal,
+                       int dtype, float softmax_scale, const int32_t* doc_bounds,
+                       void* workspace, size_t workspace_bytes, cpattn_stream_t stream) {
+  return a2a_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, 1, layout,
+                 causal, dtype, softmax_scale, doc_bounds, workspace, workspace_bytes,
+                 (cudaStream_t)stream);
+}
+
+int cpattn_hier_a2a(const void* in, void* out, int B, int S, int H, int Hkv, int D, int cp_a2a,
+                    int cp_p2p, int layout, int kv_heads, int to_seq, int dtype,
+                    cpattn_stream_t stream) {
+  return a2a_copy(in, out, B, S, H, Hkv, D, cp_a2a, cp_p2p, layout, kv_heads, to_seq, dtype,
+                  (cudaStream_t)stream);
+}
+
+int cpattn_hier_lse_a2a(const float* in, float* out, int B, int S, int H, int cp_a2a,
+                        int cp_p2p, int layout, int to_seq, cpattn_stream_t stream) {
+  return a2a_lse_copy(in, out, B, S, H, cp_a2a, cp_p2p, layout, to_seq, (cudaStream_t)stream);
+}
+
+size_t cpattn_hier_workspace_bytes(int B, int H, int Hkv, int S, int D, int cp_a2a, int cp_p2p,
+                                   int layout, int dtype, int backward) {
+  return a2a_workspace_bytes(B, H, Hkv, S, D, cp_a2a, cp_p2p, layout, dtype, backward);
+}
+
+int cpattn_hier_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                    int H, int Hkv, int S, int D, int cp_a2a, int cp_p2p, int layout, int causal,
+                    int dtype, float softmax_scale, const int32_t* doc_bounds, void* workspace,
+                    size_t workspace_bytes, cpattn_stream_t stream) {
+  return a2a_fwd(q, k, v, out, lse, B, H, Hkv, S, D, cp_a2a, cp_p2p, layout, causal, dtype,
+                 softmax_scale, doc_bounds, workspace, workspace_bytes, (cudaStream_t)stream);
+}
+
+int cpattn_hier_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                    int H, int Hkv, int S, int D, int cp_a2a, int cp_p2p, int layout, int causal,
+                    int dtype, float softmax_scale, const int32_t* doc_bounds, void* workspace,
+                    size_t workspace_bytes, cpattn_stream_t stream) {
+  return a2a_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_a2a, cp_p2p, layout,
+                 causal, dtype, softmax_scale, doc_bounds, workspace, workspace_bytes,
+                 (cudaStream_t)stream);
 }
 
 int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out,

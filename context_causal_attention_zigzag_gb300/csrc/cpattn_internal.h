@@ -156,15 +156,25 @@ struct BwdArgs {
 // x0(r) .. x0(r)+nx-1 with x0(r) = (r * x_num) / x_den.  Seq -> head copies;
 // head -> seq sums the ranks that hold a head (kv heads shared by ranks).
 // dtype: CPATTN_F32 / CPATTN_BF16 (the element type; sums in float32).
+// Sequence <-> head all-to-all.  The sequence owners hold [B, S, X, D] in
+// the sharded order of `sh` (cp ranks); the `ranks` head owners each hold
+// [B, S, nx, D] with the sequence axis in the sharded order of `inner`:
+// natural order (cp = 1) for the Ulysses variant, the second level's shard
+// order for the hierarchical (a2a+p2p) schedule.  Of each shape only cp,
+// per_rank, S, L and c are used.
 struct A2aShape {
-  RingShape sh;  // only cp, per_rank, S, L, c are used
+  RingShape sh;
+  RingShape inner;
+  int ranks;
   int B, X, nx, x_num, x_den, D;
 };
 cudaError_t launch_a2a(const void* in, void* out, const A2aShape& a, bool to_seq, int dtype,
                        cudaStream_t stream);
-// LSE [B, H, S] sharded <-> [cp][B, H/cp, S] natural (query heads only).
-cudaError_t launch_lse_a2a(const float* in, float* out, const RingShape& sh, int B, int H,
-                           bool to_seq, cudaStream_t stream);
+// LSE [B, H, S] in `sh` order <-> [ranks][B, H/ranks, S] in `inner` order
+// (query heads only).
+cudaError_t launch_lse_a2a(const float* in, float* out, const RingShape& sh,
+                           const RingShape& inner, int ranks, int B, int H, bool to_seq,
+                           cudaStream_t stream);
 
 // docs[p] for every natural position p from document offsets cu[0..ndocs]
 // (cu[0] = 0, strictly increasing, cu[ndocs] = S).  Offsets that break those

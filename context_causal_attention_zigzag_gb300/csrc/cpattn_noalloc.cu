@@ -1,11 +1,13 @@
 // Allocation-free ring backward.
 //
-// cpattn_ring_bwd needs a caller-provided device workspace (the float32 dQ
-// accumulator and the Delta rows).  Some callers cannot provide one: code
-// that runs under a memory manager owning all of the device memory (a
-// framework's caching allocator, a serving runtime that reserves HBM at
-// start-up) and forbids allocations behind its back, or code on a latency-
-// critical loop where a cudaMalloc / cudaFree would synchronise the device.
+// cpattn_ring_bwd needs a caller-provided device workspace: the float32
+// per-query-head dK / dV partials of the tensor-core kernels (the CUDA-core
+// kernels keep their float32 dQ, dK and dV there instead) and the Delta rows.
+// Some callers cannot provide one: code that runs under a memory manager
+// owning all of the device memory (a framework's caching allocator, a
+// serving runtime that reserves HBM at start-up) and forbids allocations
+// behind its back, or code on a latency-critical loop where a cudaMalloc /
+// cudaFree would synchronise the device.
 // For them the scratch lives in a fixed-size array in this library's own
 // device image: every GPU that loads the library holds it until the process
 // exits, and no call allocates anything.
@@ -16,8 +18,7 @@
 
 namespace {
 
-// 64 MiB: the float32 gradient accumulators and the Delta rows of, e.g.,
-// B=1, S=1024, H=32, Hkv=8, D=128 (40 MiB).
+// 64 MiB: the workspace of, e.g., B=1, S=1024, H=32, Hkv=8, D=128 (40 MiB).
 constexpr size_t kScratchBytes = (size_t)64 << 20;
 
 // Shared by every call on a device; keeps the last call's contents.
@@ -53,8 +54,10 @@ extern "C" int cpattn_ring_bwd_noalloc(const void* q, const void* k, const void*
   if (need > kScratchBytes) return CPATTN_ERR_WORKSPACE;
   void* scratch = scratch_on_current_device();
   if (scratch == nullptr) return CPATTN_ERR_CUDA;
-  // The backward zeroes the dQ accumulator and overwrites Delta itself, so
-  // whatever an earlier call left in the array does not leak into this one.
+  // The backward writes every workspace element before it reads it (Delta
+  // by its pre-pass, each partial or accumulator slot once by the kernel that
+  // owns it), so whatever an earlier call left in the array does not leak
+  // into this one.
   return cpattn_ring_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout,
                          causal, dtype, softmax_scale, scratch, kScratchBytes, stream);
 }

@@ -355,10 +355,12 @@ __global__ void __launch_bounds__(256) doc_bounds_kernel(const int* __restrict__
 }
 
 // ---------------------------------------------------------------------------
-// Ulysses all-to-all.  Sequence -> head: each (rank r, b, natural n) row of
-// the output is nx*D contiguous elements read from one sharded row of the
-// input, so the copy moves 16-byte vectors of those runs.  Head -> sequence:
-// each (b, sharded p, head x) row of D elements sums the ranks holding x.
+// Sequence <-> head all-to-all (Ulysses, and the first level of the
+// hierarchical schedule).  Sequence -> head: each (head owner r, b, row m)
+// row of the output is nx*D contiguous elements read from one sharded row of
+// the input (the token at natural position natural_pos(inner, m)), so the
+// copy moves 16-byte vectors of those runs.  Head -> sequence: each
+// (b, sharded p, head x) row of D elements sums the head owners holding x.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int a2a_x0(const A2aShape& a, int r) {
   return (int)(((long long)r * a.x_num) / a.x_den);
@@ -369,14 +371,14 @@ __global__ void __launch_bounds__(256) a2a_to_head_kernel(const char* __restrict
                                                           char* __restrict__ out,
                                                           const A2aShape a, int elt) {
   const int64_t row_vecs = (int64_t)a.nx * a.D * elt / (int64_t)sizeof(V);
-  const int64_t total = (int64_t)a.sh.cp * a.B * a.sh.S * row_vecs;
+  const int64_t total = (int64_t)a.ranks * a.B * a.sh.S * row_vecs;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int64_t row = i / row_vecs, e = i - row * row_vecs;
-    const int n = (int)(row % a.sh.S);
+    const int m = (int)(row % a.sh.S);
     const int64_t rb = row / a.sh.S;
     const int b = (int)(rb % a.B), r = (int)(rb / a.B);
-    const int p = sharded_pos(a.sh, n);
+    const int p = sharded_pos(a.sh, natural_pos(a.inner, m));
     const int64_t src = ((((int64_t)b * a.sh.S + p) * a.X + a2a_x0(a, r)) * a.D) * elt +
                         e * (int64_t)sizeof(V);
     reinterpret_cast<V*>(out)[i] = *reinterpret_cast<const V*>(in + src);
@@ -413,12 +415,12 @@ __global__ void __launch_bounds__(256) a2a_to_seq_kernel(const T* __restrict__ i
     const int x = (int)(row % a.X);
     const int64_t bp = row / a.X;
     const int p = (int)(bp % a.sh.S), b = (int)(bp / a.sh.S);
-    const int n = natural_pos(a.sh, p);
+    const int m = sharded_pos(a.inner, natural_pos(a.sh, p));
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < a.sh.cp; ++r) {
+    for (int r = 0; r < a.ranks; ++r) {
       const int x0 = a2a_x0(a, r);
       if (x < x0 || x >= x0 + a.nx) continue;
-      const T* src = in + ((((int64_t)r * a.B + b) * a.sh.S + n) * a.nx + (x - x0)) * a.D + d;
+      const T* src = in + ((((int64_t)r * a.B + b) * a.sh.S + m) * a.nx + (x - x0)) * a.D + d;
 #pragma unroll
       for (int u = 0; u < 4; ++u) acc[u] += a2a_ld<T>(src + u);
     }
@@ -428,12 +430,13 @@ __global__ void __launch_bounds__(256) a2a_to_seq_kernel(const T* __restrict__ i
   }
 }
 
-// LSE: out[r, b, h', n] = in[b, r*hc + h', p(n)] (to heads) and back.
+// LSE: out[r, b, h', m] = in[b, r*hc + h', p(m)] (to heads) and back, p(m)
+// the sharded position of the token at row m of the head owners' order.
 __global__ void __launch_bounds__(256) lse_a2a_kernel(const float* __restrict__ in,
                                                       float* __restrict__ out,
-                                                      const RingShape sh, int B, int H,
-                                                      bool to_seq) {
-  const int hc = H / sh.cp;
+                                                      const RingShape sh, const RingShape inner,
+                                                      int ranks, int B, int H, bool to_seq) {
+  const int hc = H / ranks;
   const int64_t total = (int64_t)B * H * sh.S;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -442,7 +445,8 @@ __global__ void __launch_bounds__(256) lse_a2a_kernel(const float* __restrict__ 
     const int64_t bh = i / sh.S;
     const int h = (int)(bh % H), b = (int)(bh / H);
     const int r = h / hc, hh = h - r * hc;
-    const int64_t j = (((int64_t)r * B + b) * hc + hh) * sh.S + natural_pos(sh, p);
+    const int64_t j =
+        (((int64_t)r * B + b) * hc + hh) * sh.S + sharded_pos(inner, natural_pos(sh, p));
     if (to_seq)
       out[i] = in[j];
     else
@@ -455,7 +459,7 @@ __global__ void __launch_bounds__(256) lse_a2a_kernel(const float* __restrict__ 
 cudaError_t launch_a2a(const void* in, void* out, const A2aShape& a, bool to_seq, int dtype,
                        cudaStream_t stream) {
   const int elt = dtype == 1 ? 2 : 4;
-  const int64_t rows = (int64_t)a.sh.cp * a.B * a.sh.S;
+  const int64_t rows = (int64_t)a.ranks * a.B * a.sh.S;
   if (rows == 0 || a.nx == 0) return cudaSuccess;
   if (!to_seq) {
     const int64_t row_bytes = (int64_t)a.nx * a.D * elt;
@@ -481,11 +485,13 @@ cudaError_t launch_a2a(const void* in, void* out, const A2aShape& a, bool to_seq
   return cudaGetLastError();
 }
 
-cudaError_t launch_lse_a2a(const float* in, float* out, const RingShape& sh, int B, int H,
-                           bool to_seq, cudaStream_t stream) {
+cudaError_t launch_lse_a2a(const float* in, float* out, const RingShape& sh,
+                           const RingShape& inner, int ranks, int B, int H, bool to_seq,
+                           cudaStream_t stream) {
   const int64_t n = (int64_t)B * H * sh.S;
   if (n == 0) return cudaSuccess;
-  lse_a2a_kernel<<<grid_for(n, 256, 8), 256, 0, stream>>>(in, out, sh, B, H, to_seq);
+  lse_a2a_kernel<<<grid_for(n, 256, 8), 256, 0, stream>>>(in, out, sh, inner, ranks, B, H,
+                                                          to_seq);
   return cudaGetLastError();
 }
 

@@ -368,6 +368,62 @@ CPATTN_API int cpattn_ulysses_bwd(const void* q, const void* k, const void* v, c
                                   size_t workspace_bytes, cpattn_stream_t stream);
 
 /*
+ * Hierarchical context parallelism, the a2a+p2p type ("Context Parallelism
+ * in MegaDLMs", sections "Hierarchical Context Parallelism": a list of level
+ * sizes such as [2, 2] splits the context group over two levels, and
+ * "Key-Value Communication Patterns": a2a+p2p combines the all-to-all and
+ * the point-to-point ring).  Level sizes [cp_a2a, cp_p2p], cp = cp_a2a *
+ * cp_p2p virtual ranks; global rank r = p * cp_a2a + a is member a of group
+ * p (groups are cp_a2a consecutive ranks).  The sequence is sharded over
+ * all cp ranks with `layout` (zigzag: 2*cp chunks, rank r holding chunks r
+ * and 2cp-1-r), so group p holds exactly shard p of the second level (for
+ * zigzag: chunks p and 2*cp_p2p-1-p of 2*cp_p2p).  The first-level
+ * all-to-all gives member a head slice a of its group's tokens (heads as
+ * for the Ulysses variant with cp_a2a ranks), ordered as that second-level
+ * shard; the members a of all groups then run the ring of cpattn_ring_fwd /
+ * _bwd with cp_size = cp_p2p and the same layout on their head slice; the
+ * inverse all-to-all returns the results to the token owners.
+ * [cp, 1] is the Ulysses variant, [1, cp] the plain ring (through the copy).
+ *
+ * cpattn_hier_a2a: the first-level all-to-all on one GPU.
+ *   to_seq = 0: in [B,S,X,D] sharded over cp ranks -> out
+ *     [cp_a2a][B,S,nx,D]; block a holds member a's head slice, rows
+ *     [p*S/cp_p2p, (p+1)*S/cp_p2p) being what member a of group p holds, in
+ *     the second level's sharded order;
+ *   to_seq = 1: the inverse; a kv head held by several members receives the
+ *     sum of their rows.  kv_heads, dtype, alignment as cpattn_ulysses_a2a.
+ * cpattn_hier_lse_a2a: the same for LSE, [B,H,S] <-> [cp_a2a][B,H/cp_a2a,S].
+ * cpattn_hier_fwd / _bwd: the whole schedule on sharded-order tensors
+ *   (shapes, dtypes and outputs as cpattn_ring_fwd / cpattn_ring_bwd): the
+ *   all-to-all into the workspace, the second-level ring for every member in
+ *   one launch (members stacked along the batch), the all-to-all back.
+ *   doc_bounds: NULL or from cpattn_doc_bounds.  workspace: device, at least
+ *   cpattn_hier_workspace_bytes(..., backward), 256-byte aligned, scratch.
+ * Errors: CPATTN_ERR_INVALID_ARG for level sizes < 1, H % cp_a2a != 0, head
+ * slices that do not divide the kv groups (or the reverse), S not split into
+ * whole chunks at cp = cp_a2a * cp_p2p; CPATTN_ERR_WORKSPACE for a short or
+ * misaligned workspace; otherwise as cpattn_ring_fwd / _bwd.
+ */
+CPATTN_API int cpattn_hier_a2a(const void* in, void* out, int B, int S, int H, int Hkv, int D,
+                               int cp_a2a, int cp_p2p, int layout, int kv_heads, int to_seq,
+                               int dtype, cpattn_stream_t stream);
+CPATTN_API int cpattn_hier_lse_a2a(const float* in, float* out, int B, int S, int H, int cp_a2a,
+                                   int cp_p2p, int layout, int to_seq, cpattn_stream_t stream);
+CPATTN_API size_t cpattn_hier_workspace_bytes(int B, int H, int Hkv, int S, int D, int cp_a2a,
+                                              int cp_p2p, int layout, int dtype, int backward);
+CPATTN_API int cpattn_hier_fwd(const void* q, const void* k, const void* v, void* out,
+                               float* lse, int B, int H, int Hkv, int S, int D, int cp_a2a,
+                               int cp_p2p, int layout, int causal, int dtype,
+                               float softmax_scale, const int32_t* doc_bounds, void* workspace,
+                               size_t workspace_bytes, cpattn_stream_t stream);
+CPATTN_API int cpattn_hier_bwd(const void* q, const void* k, const void* v, const void* out,
+                               const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                               int B, int H, int Hkv, int S, int D, int cp_a2a, int cp_p2p,
+                               int layout, int causal, int dtype, float softmax_scale,
+                               const int32_t* doc_bounds, void* workspace,
+                               size_t workspace_bytes, cpattn_stream_t stream);
+
+/*
  * Sequence length to pad a sequence of S tokens to (host only): the smallest
  * multiple of cp_size * 256 (contiguous) or 2 * cp_size * 256 (zigzag) that
  * is >= S, so that every chunk is a whole number of 256-token query pairs

@@ -10,8 +10,14 @@ oracle's cost allows (S=8192: two heads; S=32768: one kv group, i.e. its
 four query heads; S=16384 full attention: one head at every ring size),
 32-256 rows of every head, every chunk's first and last rows, and for
 S=131072 the first and last 32 rows of every chunk of one head; plus
-properties that hold at any size.
+properties that hold at any size.  At S=131072 one kv group with the real
+dO is compared with fp64 values stored by tests/golden/make_c5_group_golden.py
+(the oracle alone): LSE of every row of its four heads, O and dQ on sampled
+rows, dK / dV at the first keys and at every chunk border.
 """
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -412,16 +418,50 @@ def test_c4_full_size_cp_sweep_and_merge():
     assert cpa.device_status() == 0
 
 
+GOLDEN_C5 = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                         "c5_kvgroup5_s131072.npz")
+
+
 def test_c5_full_size_forward_backward():
     w = inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"]
     q, k, v, do = inputs.generate(w)
+    # Kv group 5 (query heads 20-23, kv head 5) carries counter-based draws
+    # that every machine reproduces; the fp64 oracle's values for it, with
+    # this dense dO, are stored (tests/golden/make_c5_group_golden.py, which
+    # calls only the oracle).  The digest proves the draw is the one stored.
+    gold = np.load(GOLDEN_C5)
+    meta = json.loads(str(gold["meta"]))
+    g = meta["group"]
+    group = inputs.group_inputs(w, g)
+    assert inputs.digest(*group) == meta["input_sha256"], "kv group draw differs from the stored"
+    inputs.embed_group(w, g, (q, k, v, do), group)
     qd, kd, vd, dod = q.to(DEV), k.to(DEV), v.to(DEV), do.to(DEV)
     # Gradients in float32: a bf16 dV element near the first key reaches ~9,
     # where one bf16 rounding alone exceeds the 2e-2 bar.
     out, lse, dq, dk, dv = cpa.attention_fwd_bwd(qd, kd, vd, dod, w.cp, w.layout, w.causal,
                                                  grad_dtype=torch.float32)
-    # 256 rows of every head, and the first and last 32 rows of every chunk
-    # of one head (the rows next to the ring's chunk borders).
+    assert cpa.device_status() == 0
+    heads = meta["query_heads"]
+    # The stored kv group: LSE of every row of its four heads, O on the first
+    # and last 8 rows of every chunk and 64 more, dQ on 128 of those rows, and
+    # dK / dV of its kv head at the first 32 keys (the longest sums over
+    # queries), the keys on both sides of every chunk border and the last key,
+    # all with the real dO.
+    glse = lse[0, heads].double().cpu().numpy()
+    assert np.max(np.abs(glse - gold["lse"])) <= 1e-3, np.max(np.abs(glse - gold["lse"]))
+    orows = torch.as_tensor(gold["o_rows"])
+    go = out[0, orows.to(DEV)][:, heads].double().cpu().numpy().transpose(1, 0, 2)
+    assert np.max(np.abs(go - gold["o"])) <= 2e-2, np.max(np.abs(go - gold["o"]))
+    qrows = torch.as_tensor(gold["dq_rows"])
+    gdq = dq[0, qrows.to(DEV)][:, heads].double().cpu().numpy().transpose(1, 0, 2)
+    assert np.max(np.abs(gdq - gold["dq"])) <= 2e-2, np.max(np.abs(gdq - gold["dq"]))
+    krows = torch.as_tensor(gold["k_rows"]).to(DEV)
+    gdk = dk[0, krows, g].double().cpu().numpy()
+    gdv = dv[0, krows, g].double().cpu().numpy()
+    assert np.max(np.abs(gdk - gold["dk"])) <= 2e-2, np.max(np.abs(gdk - gold["dk"]))
+    assert np.max(np.abs(gdv - gold["dv"])) <= 2e-2, np.max(np.abs(gdv - gold["dv"]))
+    # The other groups: 256 rows of every head and the first and last 32 rows
+    # of every chunk of one head, against the oracle evaluated here.
     rows = np.concatenate([sample_rows(w, 256, 5), band_rows(w, 0, 21, 32)])
     qf, kf, vf = f32(q), f32(k), f32(v)
     check_rows(w, out, lse, qf, kf, vf, rows)
@@ -440,8 +480,9 @@ def test_c5_full_size_forward_backward():
     assert (sdv - sdo).abs().max().item() <= bound
     assert dk.double().sum(dim=1).abs().max().item() <= bound
     del dq, dk, dv
-    # dK / dV rows: a second backward with dO zero outside a few query rows, for
-    # which the oracle's sums over queries are exact on those rows alone.
+    # dK / dV rows of every kv head: a second backward with dO zero outside a
+    # few query rows, for which the oracle's sums over queries are exact on
+    # those rows alone.
     nchunk = 2 * w.cp
     c = w.S // nchunk
     qrows = np.array(sorted({0, c - 1, c, w.S // 2, w.S // 2 + 1, w.S - c, w.S - 1}
