@@ -66,6 +66,7 @@ SIGNATURES = {
     "cpattn_ring_bwd_workspace_bytes": (_sz, [_i] * 6),
     "cpattn_ring_bwd": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _sz, _vp]),
     "cpattn_ring_bwd_noalloc": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp]),
+    "cpattn_ring_bwd_census": (_i, [_vp] * 9 + [_i] * 9 + [_f, _vp, _sz, _vp, _vp, _vp]),
     "cpattn_tile_counts": (_i, [_i64, _i, _i, _i, _i64, _vp, _vp]),
     "cpattn_device_status": (_i, [_vp]),
     "cpattn_wait_probe": (_i, [_i64, _vp]),
@@ -338,21 +339,35 @@ def _grad_args(q, k, v, dq, dk, dv, grad_dtype):
 
 
 def ring_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
-             dq=None, dk=None, dv=None, workspace=None, grad_dtype=None):
+             dq=None, dk=None, dv=None, workspace=None, grad_dtype=None, tiles_kv_rt=None,
+             tiles_q_rt=None):
     """Ring backward on sharded-order tensors; returns (dq, dk, dv).
-    grad_dtype=torch.float32 with bf16 inputs writes float32 gradients."""
-    _need_cuda(q, k, v, out, dout, lse)
+    grad_dtype=torch.float32 with bf16 inputs writes float32 gradients.
+    tiles_kv_rt / tiles_q_rt (int64 [cp, cp] device tensors, zeroed): the
+    census of the K/V-major and query-major walks (cpattn_ring_bwd_census)."""
+    _need_cuda(q, k, v, out, dout, lse, tiles_kv_rt, tiles_q_rt)
     B, H, Hkv, S, D = _shape(q, k, v)
     code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
     need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
     _need_cuda(dq, dk, dv, workspace)
-    rc = lib().cpattn_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
-                               _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
-                               int(layout), int(bool(causal)), code, _scale(scale),
-                               _ptr(workspace), workspace.numel(), _stream(q))
-    _check("cpattn_ring_bwd", rc)
+    if tiles_kv_rt is None and tiles_q_rt is None:
+        rc = lib().cpattn_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S, D, int(cp),
+                                   int(layout), int(bool(causal)), code, _scale(scale),
+                                   _ptr(workspace), workspace.numel(), _stream(q))
+        _check("cpattn_ring_bwd", rc)
+    else:
+        for t in (tiles_kv_rt, tiles_q_rt):
+            if t is None or t.dtype != torch.int64 or t.numel() < cp * cp:
+                raise ValueError("tiles_kv_rt and tiles_q_rt must both be int64 [cp, cp]")
+        rc = lib().cpattn_ring_bwd_census(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout),
+                                          _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), B, H, Hkv, S,
+                                          D, int(cp), int(layout), int(bool(causal)), code,
+                                          _scale(scale), _ptr(workspace), workspace.numel(),
+                                          _ptr(tiles_kv_rt), _ptr(tiles_q_rt), _stream(q))
+        _check("cpattn_ring_bwd_census", rc)
     return dq, dk, dv
 
 

@@ -14,8 +14,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-BUILD = os.path.join(PKG, "_build")
-LIB = os.path.join(PKG, "libcpattn.so")
+BUILD = _BUILD = os.path.join(PKG, "_build")
+LIB = _LIB = os.path.join(PKG, "libcpattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall", "-Xcompiler", "-fvisibility=hidden",
@@ -45,7 +45,20 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def mutant_lib_path(mutation: int) -> str:
+    """Where the build with planted mistake ``mutation`` puts its library."""
+    return os.path.join(PKG, f"_build_mut{int(mutation)}", "libcpattn.so")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), mutation: int = 0) -> str:
+    """Compiles every translation unit under csrc/ and links libcpattn.so.
+    ``mutation`` > 0 compiles planted mistake number ``mutation`` (see
+    CPATTN_MUTATION in csrc/cpattn_internal.h) into a library of its own
+    folder, for the mutation tests; the regular build is 0."""
+    BUILD = _BUILD if mutation == 0 else os.path.dirname(mutant_lib_path(mutation))
+    LIB = _LIB if mutation == 0 else mutant_lib_path(mutation)
+    if mutation:
+        extra_flags = tuple(extra_flags) + (f"-DCPATTN_MUTATION={int(mutation)}",)
     os.makedirs(BUILD, exist_ok=True)
     srcs = _sources()
     hdrs = _headers()

@@ -297,7 +297,8 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
                const float* lse, void* dq, void* dk, void* dv, int B, int H, int Hkv, int S,
                int D, int cp_size, int layout, int causal, int dtype, float softmax_scale,
                const int2* docs, int kv_natural, void* workspace, size_t workspace_bytes,
-               cudaStream_t st) {
+               cudaStream_t st, unsigned long long* tiles_kv_rt = nullptr,
+               unsigned long long* tiles_q_rt = nullptr) {
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp_size, layout, causal, softmax_scale, &sh);
   if (rc != CPATTN_OK) return rc;
@@ -340,6 +341,8 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   a.lse = lse;
   a.delta = delta;
   a.err = err;
+  a.tiles_kv_rt = tiles_kv_rt;
+  a.tiles_q_rt = tiles_q_rt;
   cudaError_t e;
   if (tc) {
     // Tensor cores: Delta only, then the dK/dV and dQ kernels (every output
@@ -515,7 +518,7 @@ int a2a_fwd(const void* q, const void* k, const void* v, void* out, float* lse, 
   if (rc == CPATTN_OK) rc = a2a_copy(v, wv, B, S, H, Hkv, D, A, P, layout, 1, 0, dtype, st);
   if (rc != CPATTN_OK) return rc;
   rc = fwd_common(wq, wk, wv, wo, wl, A * B, pl.hc, pl.nkv, S, D, P, pl.inner_layout, causal,
-                  dtype, softmax_scale, 0, 1, 0, nullptr, docs, 0, st);
+                  dtype, softmax_scale, 0, P, 0, nullptr, docs, 0, st);
   if (rc != CPATTN_OK) return rc;
   rc = a2a_copy(wo, out, B, S, H, Hkv, D, A, P, layout, 0, 1, dtype, st);
   if (rc != CPATTN_OK) return rc;
@@ -655,6 +658,18 @@ int cpattn_ring_bwd(const void* q, const void* k, const void* v, const void* out
   return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout, causal,
                     dtype, softmax_scale, nullptr, 0, workspace, workspace_bytes,
                     (cudaStream_t)stream);
+}
+
+int cpattn_ring_bwd_census(const void* q, const void* k, const void* v, const void* out,
+                           const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                           int B, int H, int Hkv, int S, int D, int cp_size, int layout,
+                           int causal, int dtype, float softmax_scale, void* workspace,
+                           size_t workspace_bytes, unsigned long long* tiles_kv_rt,
+                           unsigned long long* tiles_q_rt, cpattn_stream_t stream) {
+  if (tiles_kv_rt == nullptr || tiles_q_rt == nullptr) return CPATTN_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, out, dout, lse, dq, dk, dv, B, H, Hkv, S, D, cp_size, layout, causal,
+                    dtype, softmax_scale, nullptr, 0, workspace, workspace_bytes,
+                    (cudaStream_t)stream, tiles_kv_rt, tiles_q_rt);
 }
 
 int cpattn_ring_bwd_docs(const void* q, const void* k, const void* v, const void* out,

@@ -108,10 +108,22 @@ __host__ __device__ inline int rank_chunk(const RingShape& s, int r, int j) {
   return (s.per_rank == 1 || j == 0) ? r : 2 * s.cp - 1 - r;
 }
 
+// Planted mistakes for the mutation tests: a build with -DCPATTN_MUTATION=n
+// (n > 0, into a build folder of its own) compiles mistake n into the
+// library, so that the tests can show that the GPU parity checks catch it.
+// The regular build is always 0.
+#ifndef CPATTN_MUTATION
+#define CPATTN_MUTATION 0
+#endif
+
 // Ring source: at step t rank r holds the K/V of rank (r - t) mod cp.
 __host__ __device__ inline int ring_source(int r, int t, int cp) {
+#if CPATTN_MUTATION == 2
+  return (r + t) % cp;  // planted: the ring turned the other way
+#else
   int s = (r - t) % cp;
   return s < 0 ? s + cp : s;
+#endif
 }
 
 struct FwdArgs {
@@ -147,6 +159,11 @@ struct BwdArgs {
   void* dq;            // [B,S,H,D] float32 if dq_f32 else bf16
   int dq_f32;
   int* err;
+  // Optional [cp][cp] census of the tiles each walk visits, per receiving
+  // rank r and ring step t: the K/V-major walk (dK / dV) and the query-major
+  // walk (dQ).  Ring schedule only (not filled when kv_natural).
+  unsigned long long* tiles_kv_rt;
+  unsigned long long* tiles_q_rt;
 };
 
 // Kernel launchers; each returns the launch error (cudaSuccess if queued).

@@ -361,7 +361,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         QSeq seq;
         seq.init(sh, it.kv, it.knat);
         int qrow, qnat;
+        // Census: query tiles per (receiving rank, ring step), flushed at
+        // each change of step.
+        unsigned long long* census = sh.kv_natural ? nullptr : args.tiles_kv_rt;
+        int c_step = -1;
+        unsigned long long c_n = 0;
         while (seq.next(qrow, qnat)) {
+          if (census != nullptr) {
+            if (seq.t != c_step) {
+              if (c_n) atomicAdd(&census[((it.kv.rank + c_step) % sh.cp) * sh.cp + c_step], c_n);
+              c_step = seq.t;
+              c_n = 0;
+            }
+            ++c_n;
+          }
           const int st = qi & 1;
           const uint32_t ph = (qi >> 1) & 1;
           if (!mbar_wait(bar(kBarQEmpty + st), ph ^ 1, wc)) {
@@ -382,6 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           bulk_load(sDlt + st * kT * 4, args.delta + li, kT * 4, full);
           ++qi;
         }
+        if (census != nullptr && c_n)
+          atomicAdd(&census[((it.kv.rank + c_step) % sh.cp) * sh.cp + c_step], c_n);
       }
       if (!ok) {
         if (kv_armed) mbar_drain(bar(kBarKVFull), (kv_armed - 1) & 1);
@@ -579,7 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int c = 32 * cc + 2 * j;
+#if CPATTN_MUTATION == 4
+            const float2 dl = make_float2(0.f, 0.f);  // planted: Delta dropped from dS
+#else
             const float2 dl = *reinterpret_cast<const float2*>(dlt + c);  // scale * Delta
+#endif
             ds[16 * cc + j] =
                 pack_bf16(__uint_as_float(r[c]) * fmaf(__uint_as_float(d[2 * j]), scale, -dl.x),
                           __uint_as_float(r[c + 1]) *
@@ -761,7 +780,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         KSeq seq;
         seq.init(sh, it.q, it.knat);
         int kvrow, knat;
+        // Census: K/V tiles per ring step (the diagonal tile, last in the
+        // walk, arrives at step 0), flushed at each change of step.
+        unsigned long long* census = sh.kv_natural ? nullptr : args.tiles_q_rt;
+        int c_step = -1;
+        unsigned long long c_n = 0;
         while (ok && seq.next(kvrow, knat)) {
+          if (census != nullptr) {
+            const int step = seq.t < seq.t_end ? seq.t : 0;
+            if (step != c_step) {
+              if (c_n) atomicAdd(&census[it.q.rank * sh.cp + c_step], c_n);
+              c_step = step;
+              c_n = 0;
+            }
+            ++c_n;
+          }
           const int krow = it.b * sh.S + kvrow;
           for (int which = 0; which < 2; ++which) {  // K(j), then V(j)
             const uint32_t n = seq_n++;
@@ -777,6 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           bar(kBarFull + sl), half * 64, it.g, krow);
           }
         }
+        if (census != nullptr && c_n) atomicAdd(&census[it.q.rank * sh.cp + c_step], c_n);
       }
       if (!ok) {
         if (q_armed) mbar_drain(bar(kBarQFull), (q_armed - 1) & 1);

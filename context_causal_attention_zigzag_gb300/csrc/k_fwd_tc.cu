@@ -466,7 +466,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cut) {
 #pragma unroll
           for (int j = 0; j < 128; ++j)
+#if CPATTN_MUTATION == 1
+            if (j < j_lo || j >= j_hi) r[j] = __float_as_uint(-INFINITY);  // planted: seam
+#else
             if (j < j_lo || j > j_hi) r[j] = __float_as_uint(-INFINITY);
+#endif
         }
         float mx0 = __uint_as_float(r[0]), mx1 = __uint_as_float(r[1]);
         float mx2 = __uint_as_float(r[2]), mx3 = __uint_as_float(r[3]);

@@ -341,6 +341,8 @@ __global__ void __launch_bounds__(NT) simt_bwd_kernel(const BwdArgs a) {
           }
         }
         if (!__syncthreads_or(live)) continue;
+        if (a.tiles_kv_rt != nullptr && !nat_kv && tid == 0)
+          atomicAdd(&a.tiles_kv_rt[r * sh.cp + t], 1ull);
         load_tile<T, D>(Qs, qp, b, q0, qn, h, sh.H, sh.S);
         load_tile<T, D>(Os, dop, b, q0, qn, h, sh.H, sh.S);
         __syncthreads();
@@ -522,6 +524,8 @@ __global__ void __launch_bounds__(NT) simt_dq_kernel(const BwdArgs a) {
         live = tid < kn && kpos >= blk_lo && kpos <= blk_hi;
       }
       if (!__syncthreads_or(live)) continue;  // no row of the block sees the tile
+      if (a.tiles_q_rt != nullptr && !nat_kv && tid == 0)
+        atomicAdd(&a.tiles_q_rt[r * sh.cp + t], 1ull);
       load_tile<T, D>(Ks, kp, b, k0, kn, g, sh.Hkv, sh.S);
       load_tile<T, D>(Vs, vp, b, k0, kn, g, sh.Hkv, sh.S);
       __syncthreads();

@@ -150,10 +150,15 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const float* o_a, const 
       int e = lane + u * 32;
       if (e < VPR) {
         float4 r;
+#if CPATTN_MUTATION == 3
+        r = make_float4(wa * va[u].x, wa * va[u].y, wa * va[u].z, wa * va[u].w);  // planted
+        (void)wb;
+#else
         r.x = wa * va[u].x + wb * vb[u].x;
         r.y = wa * va[u].y + wb * vb[u].y;
         r.z = wa * va[u].z + wb * vb[u].z;
         r.w = wa * va[u].w + wb * vb[u].w;
+#endif
         reinterpret_cast<float4*>(o + row * D)[e] = r;
       }
     }

@@ -11,6 +11,10 @@ the workload's dtype (round to nearest even for bf16).  Tensors are
 The pages publish no data set; these standard-normal draws are the
 distribution every workload below names.
 
+Expected values stored in tests/golden/ for a kv group of the S=131072
+workload use the counter-based draws at the end of this module instead,
+which every machine reproduces bit for bit.
+
 Packed documents: the pages test document masks but give no length
 distribution.  ``packed_doc_offsets`` draws document lengths from an
 exponential distribution with a stated mean (many short documents, a few
@@ -137,11 +141,11 @@ def to_f32_numpy(x: torch.Tensor):
 # Counter-based draws that every machine reproduces bit for bit
 # ---------------------------------------------------------------------------
 #
-# ``torch.randn`` on the CPU takes a vectorised path on some x86 builds and a
-# scalar one elsewhere, so its float32 draws can differ in the last bit from
-# one machine to the next; after rounding to bf16 a few values out of a
-# hundred million then differ.  Expected values computed on one machine and
-# checked on another need draws that do not depend on the machine.  Here
+# ``torch.randn`` on the CPU is not reproducible across machines: the same
+# seeded workload drawn on an x86_64 host and on an aarch64 host gives
+# tensors with different digests (its float32 normal sampler is vectorised
+# differently per architecture).  Expected values computed on one machine
+# and checked on another need draws that do not depend on the machine.  Here
 # element n of a tensor gets two 64-bit words from SplitMix64 (Steele, Lea
 # and Flood, "Fast splittable pseudorandom number generators", 2014: the
 # state advances by the odd constant 0x9E3779B97F4A7C15 and each output is

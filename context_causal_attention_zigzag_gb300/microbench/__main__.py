@@ -1,4 +1,7 @@
-"""Builds and runs the tcgen05.mma rate microbenchmark (mma_rate.cu) on GPU 0."""
+"""Builds and runs the tcgen05.mma rate microbenchmarks on GPU 0: one CTA
+per SM with cta_group::1 (mma_rate.cu), and CTA pairs with cta_group::2
+(mma_rate_pair.cu).  ``--pair`` runs only the second, ``--single`` only the
+first."""
 import os
 import subprocess
 import sys
@@ -9,15 +12,26 @@ from .. import build as _build
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def main():
-    exe = os.path.join(tempfile.gettempdir(), f"cpattn_mma_rate_{os.getpid()}")
+def run(src):
+    exe = os.path.join(tempfile.gettempdir(), f"cpattn_{os.path.splitext(src)[0]}_{os.getpid()}")
     cmd = [_build.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
-           "-I", _build.CSRC, "-o", exe, os.path.join(HERE, "mma_rate.cu")]
+           "-I", _build.CSRC, "-o", exe, os.path.join(HERE, src)]
     subprocess.run(cmd, check=True)
     try:
-        rc = subprocess.run([exe]).returncode
+        return subprocess.run([exe]).returncode
     finally:
         os.unlink(exe)
+
+
+def main():
+    srcs = ["mma_rate.cu", "mma_rate_pair.cu"]
+    if "--pair" in sys.argv:
+        srcs = ["mma_rate_pair.cu"]
+    elif "--single" in sys.argv:
+        srcs = ["mma_rate.cu"]
+    rc = 0
+    for s in srcs:
+        rc |= run(s)
     sys.exit(rc)
 
 

@@ -208,6 +208,25 @@ CPATTN_API int cpattn_ring_bwd(const void* q, const void* k, const void* v, cons
                     cpattn_stream_t stream);
 
 /*
+ * The same backward, and additionally the device census of the tiles its
+ * kernels visit ("Sequence Parallelism IV ...", sections 3-4: per-iteration
+ * work of each rank, future sub-blocks skipped): tiles_kv_rt[r * cp_size +
+ * t] += the (query tile, key tile) pairs the K/V-major walk (dK, dV) handled
+ * for receiving rank r at ring step t, tiles_q_rt likewise for the
+ * query-major walk (dQ); summed over batch and heads, tile edge as
+ * cpattn_ring_bwd_plan reports.  Both device, uint64 [cp_size * cp_size],
+ * zeroed by the caller, non-NULL (else CPATTN_ERR_INVALID_ARG).  Each must
+ * equal the forward's census and the closed form of cpattn_tile_counts.
+ */
+CPATTN_API int cpattn_ring_bwd_census(const void* q, const void* k, const void* v,
+                                      const void* out, const void* dout, const float* lse,
+                                      void* dq, void* dk, void* dv, int B, int H, int Hkv, int S,
+                                      int D, int cp_size, int layout, int causal, int dtype,
+                                      float softmax_scale, void* workspace,
+                                      size_t workspace_bytes, unsigned long long* tiles_kv_rt,
+                                      unsigned long long* tiles_q_rt, cpattn_stream_t stream);
+
+/*
  * cpattn_ring_bwd without a workspace argument.  The pages describe no such
  * call; it exists for callers that cannot allocate device memory -- code
  * running under a memory manager that owns the whole device (a framework's

@@ -233,6 +233,36 @@ def test_census_bit_exact(dtype, D, S, cp, layout, causal):
     assert np.array_equal(closed, enum)
 
 
+@pytest.mark.parametrize("dtype,D,S,cp,layout,causal", [
+    (torch.float32, 64, 256, 2, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 4096, 4, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 4096, 4, cpa.CONTIGUOUS, True),
+    (torch.bfloat16, 128, 2048, 2, cpa.CONTIGUOUS, False),
+    (torch.bfloat16, 128, 8192, 8, cpa.ZIGZAG, True),
+    (torch.bfloat16, 128, 8192, 8, cpa.CONTIGUOUS, True),
+])
+def test_backward_census_bit_exact(dtype, D, S, cp, layout, causal):
+    # Both walks of the backward (K/V-major for dK / dV, query-major for dQ)
+    # visit exactly the tiles of the closed form at every (rank, step), the
+    # same tiles as the forward: future sub-blocks skipped, nothing twice.
+    B, H, Hkv = 2, 4, 2
+    w, q, k, v, do = make(B, H, Hkv, S, D, cp, layout, causal, dtype, seed=4100 + S, dout=True)
+    qs, ks, vs, dos = (cpa.zigzag_permute(x.to(DEV), cp, layout) for x in (q, k, v, do))
+    o, lse, fwd_counts = cpa.ring_fwd_census(qs, ks, vs, cp, layout, causal)
+    kv_rt = torch.zeros((cp, cp), device=DEV, dtype=torch.int64)
+    q_rt = torch.zeros((cp, cp), device=DEV, dtype=torch.int64)
+    cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, tiles_kv_rt=kv_rt, tiles_q_rt=q_rt)
+    path, tile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, dtype, backward=True)
+    closed, _ = cpa.tile_counts(S, cp, layout, causal, tile)
+    for name, got in (("kv walk", kv_rt), ("q walk", q_rt)):
+        g = got.cpu().numpy().astype(np.uint64)
+        assert np.array_equal(g, closed * (B * H)), (name, g, closed)
+    fpath, ftile = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, dtype)
+    if ftile == tile:
+        assert torch.equal(fwd_counts, kv_rt)
+    assert cpa.device_status() == 0
+
+
 # ---------------------------------------------------------------------------
 # backward, full comparison
 # ---------------------------------------------------------------------------
