@@ -25,7 +25,6 @@ using namespace cpattn::tc;
 namespace {
 
 constexpr uint32_t kCols = 256;          // TMEM columns per SM
-constexpr int kSmemUse = 98304 + 1024;   // A 32 KB, B 64 KB, barriers
 constexpr int kSmemReq = 160 * 1024;     // one CTA per SM
 
 __device__ __forceinline__ uint32_t cluster_rank() {

@@ -1,0 +1,111 @@
+// Microbenchmark: aggregate throughput of bulk asynchronous reductions
+// (cp.reduce.async.bulk .add.f32, shared -> global) from every SM into a
+// float32 buffer, the primitive a K/V-major attention backward would use to
+// add each tile's dQ partial (128 query rows x 128 features, 64 KB) into a
+// float32 accumulator.  One CTA per SM issues `chunk`-byte reductions of a
+// shared-memory tile to tile-sized slots of the buffer, walking the slots so
+// that the CTAs in flight touch `live` distinct tiles (the accumulator's
+// working set), with up to four tiles in flight per SM.  Reported: bytes
+// reduced per second over all SMs, for a working set inside L2 and one
+// larger than L2.  The kernel has no spin-waits (only the bulk-group waits,
+// which end when the copies do); not part of the library.
+//
+//   python -m context_causal_attention_zigzag_gb300.microbench --reduce
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdio.h>
+
+namespace {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
+                   dst),
+               "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+constexpr int kTileBytes = 65536;
+
+// Each CTA reduces its shared tile `reps` times; rep i of CTA c goes to tile
+// slot (i * grid + c) % live of the buffer (live tiles of 64 KB).
+__global__ void __launch_bounds__(128, 1)
+    reduce_kernel(float* buf, int live, int reps, int chunk, unsigned long long* ns) {
+  extern __shared__ __align__(1024) uint8_t sm[];
+  for (int i = threadIdx.x; i < kTileBytes / 4; i += blockDim.x)
+    reinterpret_cast<float*>(sm)[i] = 1.0f;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t src = smem_u32(sm);
+    const uint64_t t0 = gtimer();
+    for (int i = 0; i < reps; ++i) {
+      const int64_t slot = ((int64_t)i * gridDim.x + blockIdx.x) % live;
+      char* dst = reinterpret_cast<char*>(buf) + slot * kTileBytes;
+      for (int off = 0; off < kTileBytes; off += chunk)
+        bulk_reduce_add_f32(reinterpret_cast<float*>(dst + off), src + off, (uint32_t)chunk);
+      bulk_commit();
+      bulk_wait_read<3>();  // at most four tiles' reductions still reading shared memory
+    }
+    bulk_wait<0>();
+    ns[blockIdx.x] = gtimer() - t0;
+  }
+}
+
+}  // namespace
+
+int main() {
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, 0);
+  const int64_t big_tiles = (int64_t)8192;  // 512 MB of float32 accumulator
+  float* buf = nullptr;
+  unsigned long long* ns = nullptr;
+  if (cudaMalloc(&buf, big_tiles * kTileBytes) != cudaSuccess) return 1;
+  cudaMalloc(&ns, sizeof(unsigned long long) * sms);
+  cudaMemset(buf, 0, big_tiles * kTileBytes);
+  cudaFuncSetAttribute(reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTileBytes);
+  const int reps = 400;
+  struct Case {
+    int live;
+    int chunk;
+  } cases[] = {{16, 65536}, {1024, 65536}, {1024, 16384}, {1024, 4096},
+               {8192, 65536}, {8192, 16384}};
+  for (const Case& c : cases) {
+    reduce_kernel<<<sms, 128, kTileBytes>>>(buf, c.live, 20, c.chunk, ns);  // warm-up
+    cudaEvent_t a, b;
+    cudaEventCreate(&a);
+    cudaEventCreate(&b);
+    cudaEventRecord(a);
+    reduce_kernel<<<sms, 128, kTileBytes>>>(buf, c.live, reps, c.chunk, ns);
+    cudaEventRecord(b);
+    cudaError_t e = cudaEventSynchronize(b);
+    if (e != cudaSuccess) {
+      printf("error %s\n", cudaGetErrorString(e));
+      return 1;
+    }
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, a, b);
+    const double bytes = (double)sms * reps * kTileBytes;
+    printf("live %5d tiles (%6.1f MB) chunk %6d B: %.3f ms, %.2f TB/s reduced\n", c.live,
+           c.live * (double)kTileBytes / 1e6, c.chunk, ms, bytes / (ms * 1e-3) / 1e12);
+  }
+  return 0;
+}
