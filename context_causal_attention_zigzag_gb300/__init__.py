@@ -7,7 +7,7 @@ every virtual rank's shard resident in HBM.  The compute lives in libcpattn
 Python binding.  ``inputs`` holds the seeded synthetic workloads.
 """
 from ._binding import (  # noqa: F401
-    BF16, CONTIGUOUS, F32, GRAD_F32, PATH_SIMT, PATH_TCGEN05, ZIGZAG, CpattnError,
+    BF16, CONTIGUOUS, F32, GRAD_F32, ONEPASS, PATH_SIMT, PATH_TCGEN05, ZIGZAG, CpattnError,
     allgather_bwd, allgather_fwd, attention, attention_allgather_fwd_bwd, attention_docs,
     attention_docs_fwd_bwd, attention_fwd_bwd, device_status, doc_bounds, lib,
     hier_a2a, hier_fwd, hier_bwd, hier_workspace_bytes, attention_hier_fwd_bwd,

@@ -25,6 +25,7 @@ ZIGZAG = 1
 F32 = 0
 BF16 = 1
 GRAD_F32 = 0x10  # OR into the backward's dtype: dq, dk, dv written as float32
+ONEPASS = 0x20   # OR into the backward's dtype: one-pass tensor-core backward (dQ by reductions)
 PATH_SIMT = 0
 PATH_TCGEN05 = 1
 
@@ -322,8 +323,8 @@ def ring_bwd_workspace_bytes(B, H, Hkv, S, D, dtype=BF16) -> int:
     return int(lib().cpattn_ring_bwd_workspace_bytes(B, H, Hkv, S, D, int(dtype)))
 
 
-def _grad_args(q, k, v, dq, dk, dv, grad_dtype):
-    code = _dtype_code(q)
+def _grad_args(q, k, v, dq, dk, dv, grad_dtype, onepass=False):
+    code = _dtype_code(q) | (ONEPASS if onepass else 0)
     gdt = q.dtype if grad_dtype is None else grad_dtype
     if gdt == torch.float32 and q.dtype != torch.float32:
         code |= GRAD_F32
@@ -340,14 +341,16 @@ def _grad_args(q, k, v, dq, dk, dv, grad_dtype):
 
 def ring_bwd(q, k, v, out, dout, lse, cp, layout=ZIGZAG, causal=True, scale=None,
              dq=None, dk=None, dv=None, workspace=None, grad_dtype=None, tiles_kv_rt=None,
-             tiles_q_rt=None):
+             tiles_q_rt=None, onepass=False):
     """Ring backward on sharded-order tensors; returns (dq, dk, dv).
     grad_dtype=torch.float32 with bf16 inputs writes float32 gradients.
+    onepass=True selects the one-pass tensor-core backward (CPATTN_BWD_ONEPASS:
+    dQ added by bulk reductions, not bitwise reproducible).
     tiles_kv_rt / tiles_q_rt (int64 [cp, cp] device tensors, zeroed): the
     census of the K/V-major and query-major walks (cpattn_ring_bwd_census)."""
     _need_cuda(q, k, v, out, dout, lse, tiles_kv_rt, tiles_q_rt)
     B, H, Hkv, S, D = _shape(q, k, v)
-    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype, onepass)
     need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
@@ -437,13 +440,13 @@ def ring_fwd_docs_census(q, k, v, cp, bounds, layout=ZIGZAG, causal=True, scale=
 
 
 def ring_bwd_docs(q, k, v, out, dout, lse, cp, bounds, layout=ZIGZAG, causal=True, scale=None,
-                  dq=None, dk=None, dv=None, workspace=None, grad_dtype=None):
+                  dq=None, dk=None, dv=None, workspace=None, grad_dtype=None, onepass=False):
     """Ring backward under the document rule; returns (dq, dk, dv)."""
     _need_cuda(q, k, v, out, dout, lse, bounds)
     B, H, Hkv, S, D = _shape(q, k, v)
     if bounds.dtype != torch.int32 or tuple(bounds.shape) != (S, 2):
         raise ValueError("bounds must be int32 [S, 2] from doc_bounds")
-    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype)
+    code, dq, dk, dv = _grad_args(q, k, v, dq, dk, dv, grad_dtype, onepass)
     need = ring_bwd_workspace_bytes(B, H, Hkv, S, D, code)
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=q.device, dtype=torch.uint8)
@@ -720,13 +723,13 @@ def attention(q, k, v, cp, layout=ZIGZAG, causal=True, scale=None):
 
 
 def attention_fwd_bwd(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None,
-                      grad_dtype=None):
+                      grad_dtype=None, onepass=False):
     """Natural order: forward and backward through the ring.  Returns
     (out, lse, dq, dk, dv), all natural order."""
     qs, ks, vs, dos = (zigzag_permute(x, cp, layout) for x in (q, k, v, dout))
     o, lse = ring_fwd(qs, ks, vs, cp, layout, causal, scale)
     dq, dk, dv = ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, scale,
-                          grad_dtype=grad_dtype)
+                          grad_dtype=grad_dtype, onepass=onepass)
     un = lambda x: zigzag_unpermute(x, cp, layout)  # noqa: E731
     return un(o), zigzag_unpermute(lse, cp, layout, seq_dim=2), un(dq), un(dk), un(dv)
 
@@ -747,7 +750,7 @@ def attention_docs(q, k, v, cp, cu_seqlens=None, layout=ZIGZAG, causal=True, sca
 
 
 def attention_docs_fwd_bwd(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causal=True,
-                           scale=None, grad_dtype=None):
+                           scale=None, grad_dtype=None, onepass=False):
     """attention_docs with the backward: dout over the real tokens (the
     padding gets a zero upstream gradient).  Returns (out, lse, dq, dk, dv)
     for the real tokens, natural order."""
@@ -757,7 +760,7 @@ def attention_docs_fwd_bwd(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, ca
     qs, ks, vs, dos = (zigzag_permute_pad(x, cp, S, layout) for x in (q, k, v, dout))
     o, lse = ring_fwd_docs(qs, ks, vs, cp, bounds, layout, causal, scale)
     dq, dk, dv = ring_bwd_docs(qs, ks, vs, o, dos, lse, cp, bounds, layout, causal, scale,
-                               grad_dtype=grad_dtype)
+                               grad_dtype=grad_dtype, onepass=onepass)
     un = lambda x: zigzag_unpermute_pad(x, cp, S_real, layout)  # noqa: E731
     return (un(o), zigzag_unpermute_pad(lse, cp, S_real, layout, seq_dim=2), un(dq), un(dk),
             un(dv))

@@ -133,7 +133,7 @@ int plan_common(int B, int H, int Hkv, int S, int D, int cp, int layout, int cau
   RingShape sh;
   int rc = make_shape(B, H, Hkv, S, D, cp, layout, causal, 0.f, &sh);
   if (rc != CPATTN_OK) return rc;
-  dtype &= fwd ? ~0 : ~CPATTN_GRAD_F32;
+  dtype &= fwd ? ~0 : ~kDtypeFlags;
   if (dtype != CPATTN_F32 && dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   bool tc = fwd ? (tc_fwd_eligible(sh, dtype) && tc_fwd_available())
                 : (tc_bwd_eligible(sh, dtype) && tc_bwd_available());
@@ -283,10 +283,10 @@ int cpattn_lse_merge(const float* o_a, const float* lse_a, const float* o_b, con
 size_t cpattn_ring_bwd_workspace_bytes(int B, int H, int Hkv, int S, int D, int dtype) {
   (void)dtype;
   if (B < 0 || H < 0 || Hkv < 0 || S < 0 || D < 0) return 0;
+  (void)Hkv;
   const size_t q = (size_t)B * S * H * D * sizeof(float);
-  const size_t kv = (size_t)B * S * Hkv * D * sizeof(float);
   const size_t delta = (size_t)B * H * S * sizeof(float);
-  return 2 * align256(q) + 2 * align256(kv) + align256(delta);
+  return 3 * align256(q) + align256(delta);
 }
 
 }  // extern "C"
@@ -304,7 +304,7 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   if (rc != CPATTN_OK) return rc;
   sh.docs = docs;
   sh.kv_natural = kv_natural;
-  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  const int in_dtype = dtype & ~kDtypeFlags;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   const int out_dtype = (dtype & CPATTN_GRAD_F32) ? CPATTN_F32 : in_dtype;
   if ((long long)B * S == 0) return CPATTN_OK;
@@ -319,16 +319,17 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   int* err = device_error_word();
   if (err == nullptr) return CPATTN_ERR_CUDA;
   const int64_t n_q = (int64_t)B * S * H * D, n_kv = (int64_t)B * S * Hkv * D;
-  // Workspace: [n_q][n_q][n_kv][n_kv] float32, then Delta [B,H,S].
+  // Workspace: three float32 regions of n_q elements, then Delta [B,H,S].
+  // Tensor cores: the per-query-head dK / dV partials, and the one-pass
+  // kernel's dQ accumulator for non-float32 outputs.  CUDA cores: the dQ,
+  // dK, dV accumulators.
   char* ws = static_cast<char*>(workspace);
   float* reg_a = reinterpret_cast<float*>(ws);
   ws += align256((size_t)n_q * sizeof(float));
   float* reg_b = reinterpret_cast<float*>(ws);
   ws += align256((size_t)n_q * sizeof(float));
   float* reg_c = reinterpret_cast<float*>(ws);
-  ws += align256((size_t)n_kv * sizeof(float));
-  float* reg_d = reinterpret_cast<float*>(ws);
-  ws += align256((size_t)n_kv * sizeof(float));
+  ws += align256((size_t)n_q * sizeof(float));
   float* delta = reinterpret_cast<float*>(ws);
   const bool tc = tc_bwd_eligible(sh, in_dtype) && tc_bwd_available() && device_is_sm103();
   BwdArgs a;
@@ -344,6 +345,26 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
   a.tiles_kv_rt = tiles_kv_rt;
   a.tiles_q_rt = tiles_q_rt;
   cudaError_t e;
+  if (tc && (dtype & CPATTN_BWD_ONEPASS)) {
+    // One pass: Delta and a zeroed float32 dQ accumulator (the output itself
+    // for float32 gradients), the one-pass kernel, the per-group sum of
+    // dK / dV, and for bf16 gradients the conversion of dQ.
+    float* dq_acc = out_dtype == CPATTN_F32 ? static_cast<float*>(dq) : reg_c;
+    e = launch_bwd_prep(out, dout, delta, dq_acc, nullptr, nullptr, 0, B, S, H, D, in_dtype,
+                        sh.scale, st);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+    a.dk_part = reg_a;
+    a.dv_part = reg_b;
+    a.dq_acc = dq_acc;
+    e = launch_tc_bwd_onepass(a, st);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+    e = launch_grad_reduce(reg_a, reg_b, dk, dv, B, S, H, Hkv, D, out_dtype, st);
+    if (e != cudaSuccess) return CPATTN_ERR_CUDA;
+    if (out_dtype != CPATTN_F32)
+      e = launch_grad_convert(dq_acc, nullptr, nullptr, dq, nullptr, nullptr, n_q, 0, out_dtype,
+                              st);
+    return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
+  }
   if (tc) {
     // Tensor cores: Delta only, then the dK/dV and dQ kernels (every output
     // element written exactly once), then the per-group sum of dK / dV.
@@ -365,11 +386,11 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
                       st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
   a.dq_acc = reg_a;
-  a.dk_acc = reg_c;
-  a.dv_acc = reg_d;
+  a.dk_acc = reg_b;
+  a.dv_acc = reg_c;
   e = launch_simt_bwd(a, in_dtype, st);
   if (e != cudaSuccess) return CPATTN_ERR_CUDA;
-  e = launch_grad_convert(reg_a, reg_c, reg_d, dq, dk, dv, n_q, n_kv, out_dtype, st);
+  e = launch_grad_convert(reg_a, reg_b, reg_c, dq, dk, dv, n_q, n_kv, out_dtype, st);
   return e == cudaSuccess ? CPATTN_OK : CPATTN_ERR_CUDA;
 }
 
@@ -425,7 +446,7 @@ struct A2aWs {
 
 A2aWs a2a_ws(const A2aPlan& pl, int B, int H, int S, int D, int dtype, bool backward) {
   A2aWs w;
-  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  const int in_dtype = dtype & ~kDtypeFlags;
   const size_t elt = in_dtype == CPATTN_BF16 ? 2 : 4;
   const size_t gelt = (dtype & CPATTN_GRAD_F32) ? 4 : elt;
   const size_t rows = (size_t)pl.A * B * S;
@@ -533,7 +554,7 @@ int a2a_bwd(const void* q, const void* k, const void* v, const void* out, const 
   A2aPlan pl;
   int rc = a2a_plan(B, H, Hkv, S, D, A, P, layout, &pl);
   if (rc != CPATTN_OK) return rc;
-  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  const int in_dtype = dtype & ~kDtypeFlags;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return CPATTN_ERR_INVALID_ARG;
   const int out_dtype = (dtype & CPATTN_GRAD_F32) ? CPATTN_F32 : in_dtype;
   if (causal != 0 && causal != 1) return CPATTN_ERR_INVALID_ARG;
@@ -765,7 +786,9 @@ int cpattn_device_status(cpattn_stream_t stream) {
     int zero = 0;
     if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
       return CPATTN_ERR_CUDA;
-    return host == kErrBadDocs ? CPATTN_ERR_INVALID_ARG : CPATTN_ERR_DEVICE_TIMEOUT;
+    if (host == kErrBadDocs) return CPATTN_ERR_INVALID_ARG;
+    if (host == kErrLaunch) return CPATTN_ERR_UNSUPPORTED;
+    return CPATTN_ERR_DEVICE_TIMEOUT;
   }
   return CPATTN_OK;
 }

@@ -131,7 +131,7 @@ bool plan_host(int B, int H, int Hkv, int S_real, int S, int D, int cp, int layo
     return false;
   if (H % Hkv != 0) return false;
   if (layout != CPATTN_LAYOUT_CONTIGUOUS && layout != CPATTN_LAYOUT_ZIGZAG) return false;
-  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  const int in_dtype = dtype & ~kDtypeFlags;
   if (in_dtype != CPATTN_F32 && in_dtype != CPATTN_BF16) return false;
   const int per = layout == CPATTN_LAYOUT_ZIGZAG ? 2 : 1;
   if (S % (cp * per) != 0) return false;
@@ -261,7 +261,7 @@ int host_common(const HostPlan& p, const void* q, const void* k, const void* v, 
   if (workspace == nullptr || workspace_bytes < p.total ||
       (reinterpret_cast<uintptr_t>(workspace) & 255) != 0)
     return CPATTN_ERR_WORKSPACE;
-  const int in_dtype = dtype & ~CPATTN_GRAD_F32;
+  const int in_dtype = dtype & ~kDtypeFlags;
   cudaStream_t st = (cudaStream_t)stream;
   SideStreams* ss = side_streams();
   if (ss == nullptr) return CPATTN_ERR_CUDA;

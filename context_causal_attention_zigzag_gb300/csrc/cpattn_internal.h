@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "cpattn.h"
+
 namespace cpattn {
 
 // Shape of one ring problem.  Positions are token indices along S.
@@ -201,6 +203,10 @@ cudaError_t launch_doc_bounds(const int* cu, int ndocs, int S, int2* docs, int* 
                               cudaStream_t stream);
 constexpr int kErrTimeout = 1;
 constexpr int kErrBadDocs = 2;
+constexpr int kErrLaunch = 3;  // a kernel found its launch unusable (shared-memory alignment)
+
+// Flags callers OR into the dtype argument (include/cpattn.h).
+constexpr int kDtypeFlags = CPATTN_GRAD_F32 | CPATTN_BWD_ONEPASS;
 
 // Natural <-> sharded along S; the natural tensor holds S_nat <= S tokens
 // (the rest is padding: zeros when sharding, dropped when unsharding).
@@ -219,6 +225,9 @@ cudaError_t launch_bwd_prep(const void* out, const void* dout, float* delta, flo
                             int D, int dtype, float delta_scale, cudaStream_t stream);
 cudaError_t launch_simt_bwd(const BwdArgs& a, int dtype, cudaStream_t stream);
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream);
+// One-pass tensor-core backward: dK / dV partials as launch_tc_bwd, dQ added
+// into a.dq_acc (float32 [B,S,H,D], zeroed by the caller).
+cudaError_t launch_tc_bwd_onepass(const BwdArgs& a, cudaStream_t stream);
 // dk[b,s,g,:] = sum of dk_part[b,s,h,:] over the query heads h of kv head g
 // (and the same for dv), written in the output dtype.
 cudaError_t launch_grad_reduce(const float* dk_part, const float* dv_part, void* dk, void* dv,

@@ -1066,6 +1066,622 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace qm
 
+// ===========================================================================
+// One-pass kernel: dK, dV and dQ from one K/V-major walk
+// ===========================================================================
+//
+// Work item and walk as the dkdv kernel (one 128-row K/V tile x one query
+// head, the query tiles that see it in ring order).  Per query tile j, with
+// TMEM lanes = K/V rows for S^T, dP^T, dV, dK and lanes = features for dQ^T:
+//   S^T  = K Q^T  -> X             dP^T = V dO^T -> Y
+//   P^T  -> bf16 over X (TMEM)     dS^T = scale P^T (dP^T - Delta) -> bf16
+//                                  into shared memory (128-byte swizzle)
+//   dV  += P^T dO  (TS, A = X)     dK  += dS^T Q  (SS, A = dS^T K-major)
+//   dQ^T = K^T dS^T (SS, A = K MN-major, B = dS^T MN-major) -> Y
+// and the dQ^T tile (this K/V tile's share of the query tile's dQ) is read
+// out of TMEM by the drain warpgroup, staged in shared memory (over dS^T,
+// which the two MMAs have finished reading) and added to the float32 dQ
+// accumulator [B,S,H,D] with tensor bulk reductions (cp.reduce.async.bulk
+// .add), 32 query rows (16 KB) at a time through two slots.  Every K/V tile
+// that a query tile sees adds its share once: 5 GEMMs per tile pair instead
+// of the two-kernel path's 7, at the price of dQ's summation order, which
+// follows the order the reductions reach L2 (the result is not bitwise
+// reproducible from run to run; the two-kernel path is).
+//
+// CTA = 512 threads: warp 0 TMA, warp 1 TMEM owner + MMA issuer (warps 0-3:
+// 88 registers), warps 4-11 the elementwise halves ([0,64) and [64,128) of
+// the query columns) and the dK / dV epilogue (152 registers), warps 12-15
+// the dQ drain (120 registers; thread = feature lane).  The split uses the
+// whole 512 x 128 registers of the launch and leaves ptxas nothing to spill.  Shared memory: K, V,
+// two Q / dO stages, dS^T (= the dQ staging), LSE / Delta rows: 226 KB.
+namespace fz {
+
+constexpr int kThreadsF = 512;
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + kTileBytes;
+constexpr int kOffQ = kOffV + kTileBytes;         // [2] stages
+constexpr int kOffDO = kOffQ + 2 * kTileBytes;    // [2]
+constexpr int kOffDS = kOffDO + 2 * kTileBytes;   // dS^T, then the two dQ staging slots
+constexpr int kOffLse = kOffDS + kTileBytes;      // [2][128] float (natural log)
+constexpr int kOffDlt = kOffLse + 2 * kT * 4;     // [2][128] float
+constexpr int kOffBar = kOffDlt + 2 * kT * 4;
+constexpr int kBarKVFull = 0;
+constexpr int kBarKVEmpty = 1;
+constexpr int kBarQFull = 2;       // [2]
+constexpr int kBarQEmpty = 4;      // [2]
+constexpr int kBarS = 6;
+constexpr int kBarDP = 7;
+constexpr int kBarP = 8;
+constexpr int kBarDS = 9;
+constexpr int kBarDQ = 10;
+constexpr int kBarYFree = 11;
+constexpr int kBarDSFree = 12;
+constexpr int kBarStageFull = 13;  // [2]
+constexpr int kBarStageFree = 15;  // [2]
+constexpr int kBarAcc = 17;
+constexpr int kBarAccFree = 18;
+constexpr int kBarDrain = 19;
+constexpr int kNumBars = 20;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;
+// The dynamic shared memory starts on a 1024-byte boundary (checked at run
+// time; the kernel refuses to run otherwise), so no alignment slack.
+constexpr int kSmemBytes = kOffMisc + 16;
+constexpr uint32_t kColX = 0, kColY = 128, kColDV = 256, kColDK = 384;
+constexpr uint32_t kQTx = 2 * kTileBytes + 2 * kT * 4;  // Q, dO, LSE, Delta
+constexpr uint32_t kIdescMM = idesc_bf16(128, 128, true, true);  // A and B MN-major
+constexpr int kStageRows = 32;                       // query rows per reduction
+constexpr int kStageBytes = kStageRows * kD * 4;     // 16 KB of float32
+// Registers per thread for the three roles (setmaxnreg); the launch gives
+// 512 threads x 128.
+constexpr int kRegCtl = 88, kRegEw = 152, kRegDrain = 120;
+static_assert(128 * (kRegCtl + 2 * kRegEw + kRegDrain) <= 512 * 128, "register split");
+static_assert(kSmemBytes <= 232448, "shared memory");
+
+template <int N>
+__device__ __forceinline__ void reg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Adds a [32 rows][128] float32 box of shared memory into the accumulator at
+// (feature 0, head h, row); completion tracked as a bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int h,
+                                                  int row) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group "
+      "[%0, {%1, %2, %3}], [%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(0), "r"(h), "r"(row), "r"(src)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+using kv::Item;
+using kv::decode;
+
+__global__ void __launch_bounds__(kThreadsF, 1)
+    dkdvq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_do,
+                 const __grid_constant__ CUtensorMap tm_dq, const BwdArgs args, int n_items) {
+  extern __shared__ __align__(1024) uint8_t smem_fz[];
+  const uint32_t base = smem_u32(smem_fz);
+  if ((base & 1023u) != 0) {  // uniform: every thread leaves before any wait
+    if (threadIdx.x == 0) atomicExch(args.err, kErrLaunch);
+    return;
+  }
+  uint8_t* smem = smem_fz;
+  const uint32_t sK = base + kOffK, sV = base + kOffV, sQ = base + kOffQ, sDO = base + kOffDO;
+  const uint32_t sDS = base + kOffDS, sLse = base + kOffLse, sDlt = base + kOffDlt;
+  const float* lse_s = reinterpret_cast<const float*>(smem + kOffLse);
+  const float* dlt_s = reinterpret_cast<const float*>(smem + kOffDlt);
+  const uint32_t bars = base + kOffBar;
+  auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+
+  const RingShape& sh = args.sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{abort_flag, args.err};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarKVFull), 1);
+    mbar_init(bar(kBarKVEmpty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarQFull + i), 1);
+      mbar_init(bar(kBarQEmpty + i), 1);
+      mbar_init(bar(kBarStageFull + i), 128);
+      mbar_init(bar(kBarStageFree + i), 1);
+    }
+    mbar_init(bar(kBarS), 1);
+    mbar_init(bar(kBarDP), 1);
+    mbar_init(bar(kBarP), 256);
+    mbar_init(bar(kBarDS), 256);
+    mbar_init(bar(kBarDQ), 1);
+    mbar_init(bar(kBarYFree), 128);
+    mbar_init(bar(kBarDSFree), 1);
+    mbar_init(bar(kBarAcc), 1);
+    mbar_init(bar(kBarAccFree), 256);
+    mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    reg_dec<kRegCtl>();
+  }
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      uint32_t qi = 0, kv_armed = 0, q_armed[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        const int idx = item_index(k, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = decode(sh, idx);
+        if (!mbar_wait(bar(kBarKVEmpty), (k & 1) ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kBarKVFull), 2 * kTileBytes);
+        ++kv_armed;
+        const int krow = it.b * sh.S + (sh.kv_natural ? it.knat * kT : it.kv.row);
+        for (int half = 0; half < 2; ++half) {
+          tma_load_3d(sK + half * kBoxBytes, &tm_k, bar(kBarKVFull), half * 64, it.g, krow);
+          tma_load_3d(sV + half * kBoxBytes, &tm_v, bar(kBarKVFull), half * 64, it.g, krow);
+        }
+        QSeq seq;
+        seq.init(sh, it.kv, it.knat);
+        int qrow, qnat;
+        unsigned long long* census = sh.kv_natural ? nullptr : args.tiles_kv_rt;
+        unsigned long long* census_q = sh.kv_natural ? nullptr : args.tiles_q_rt;
+        int c_step = -1;
+        unsigned long long c_n = 0;
+        while (seq.next(qrow, qnat)) {
+          if (census != nullptr) {
+            if (seq.t != c_step) {
+              if (c_n) {
+                const int cell = ((it.kv.rank + c_step) % sh.cp) * sh.cp + c_step;
+                atomicAdd(&census[cell], c_n);
+                if (census_q != nullptr) atomicAdd(&census_q[cell], c_n);
+              }
+              c_step = seq.t;
+              c_n = 0;
+            }
+            ++c_n;
+          }
+          const int st = qi & 1;
+          const uint32_t ph = (qi >> 1) & 1;
+          if (!mbar_wait(bar(kBarQEmpty + st), ph ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar(kBarQFull + st);
+          mbar_arrive_expect_tx(full, kQTx);
+          ++q_armed[st];
+          const int row = it.b * sh.S + qrow;
+          for (int half = 0; half < 2; ++half) {
+            tma_load_3d(sQ + st * kTileBytes + half * kBoxBytes, &tm_q, full, half * 64, it.h, row);
+            tma_load_3d(sDO + st * kTileBytes + half * kBoxBytes, &tm_do, full, half * 64, it.h,
+                        row);
+          }
+          const int64_t li = ((int64_t)it.b * sh.H + it.h) * sh.S + qrow;
+          bulk_load(sLse + st * kT * 4, args.lse + li, kT * 4, full);
+          bulk_load(sDlt + st * kT * 4, args.delta + li, kT * 4, full);
+          ++qi;
+        }
+        if (census != nullptr && c_n) {
+          const int cell = ((it.kv.rank + c_step) % sh.cp) * sh.cp + c_step;
+          atomicAdd(&census[cell], c_n);
+          if (census_q != nullptr) atomicAdd(&census_q[cell], c_n);
+        }
+      }
+      if (!ok) {
+        if (kv_armed) mbar_drain(bar(kBarKVFull), (kv_armed - 1) & 1);
+        for (int s = 0; s < 2; ++s)
+          if (q_armed[s]) mbar_drain(bar(kBarQFull + s), (q_armed[s] - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      uint32_t qi = 0, p_ph = 0, ds_ph = 0;
+      bool ok = true;
+      auto issue_s = [&](int st) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColX, sdesc_sw128(sK + off, 16, 1024),
+                 sdesc_sw128(sQ + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(bar(kBarS));
+      };
+      auto issue_dp = [&](int st) {
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          mma_ss(tmem + kColY, sdesc_sw128(sV + off, 16, 1024),
+                 sdesc_sw128(sDO + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+        }
+        mma_commit(bar(kBarDP));
+      };
+      for (int k = 0; ok; ++k) {
+        const int idx = item_index(k, blockIdx.x, gridDim.x);
+        if (idx >= n_items) break;
+        const Item it = decode(sh, idx);
+        if (!mbar_wait(bar(kBarKVFull), k & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        QSeq seq;
+        seq.init(sh, it.kv, it.knat);
+        int qrow, qnat;
+        bool have = seq.next(qrow, qnat);
+        if (have) {
+          const int st = qi & 1;
+          if (!mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(st);
+          // Y holds the previous tile's dQ^T until the drain has read it.
+          if (!mbar_wait(bar(kBarYFree), (qi & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_dp(st);
+        }
+        bool first = true;
+        while (have) {
+          const int st = qi & 1;
+          int nqrow, nqnat;
+          const bool nhave = seq.next(nqrow, nqnat);
+          const int nst = (qi + 1) & 1;
+          // dV += P^T dO
+          if (!mbar_wait(bar(kBarP), p_ph, wc)) {
+            ok = false;
+            break;
+          }
+          p_ph ^= 1;
+          if (first && !mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + kColDV, tmem + kColX + a_col(kk),
+                   sdesc_sw128(sDO + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   (!first || kk > 0) ? 1u : 0u);
+          // dK += dS^T Q, then dQ^T = K^T dS^T into Y (the elementwise warps
+          // have read dP^T there before signalling dS^T).
+          if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
+            ok = false;
+            break;
+          }
+          ds_ph ^= 1;
+          tc_fence_after();
+          for (int kk = 0; kk < kT / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
+                   sdesc_sw128(sQ + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   (!first || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(kBarQEmpty + st));  // Q, dO of this tile read for the last time
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ss(tmem + kColY, sdesc_sw128(sK + kk * 2048, kBoxBytes, 1024),
+                   sdesc_sw128(sDS + kk * 2048, kBoxBytes, 1024), kIdescMM, kk > 0 ? 1u : 0u);
+          mma_commit(bar(kBarDQ));
+          if (nhave) {
+            // S of the next tile over X (dV has read P^T; MMAs run in order).
+            if (!mbar_wait(bar(kBarQFull + nst), ((qi + 1) >> 1) & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(nst);
+            // dP of the next tile once the drain has read this tile's dQ^T.
+            if (!mbar_wait(bar(kBarYFree), ((qi + 1) & 1) ^ 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_dp(nst);
+          }
+          first = false;
+          ++qi;
+          have = nhave;
+        }
+        if (!ok) break;
+        if (first) {
+          if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+        }
+        mma_commit(bar(kBarAcc));
+        mma_commit(bar(kBarKVEmpty));
+      }
+      if (!ok) {
+        mma_commit(bar(kBarDrain));
+        mbar_drain(bar(kBarDrain), 0);
+      }
+    }
+  } else if (warp < 4) {
+    // warps 2-3: no role
+  } else if (warp < 12) {
+    // ------------------------------------------------ elementwise + dK / dV
+    reg_inc<kRegEw>();
+    const int half = (warp - 4) >> 2;  // query columns [64*half, 64*half + 64)
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;    // K/V row of the tile (TMEM lane)
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = sh.scale_log2, scale = sh.scale;
+    // This thread's 128-byte row of its half's dS^T box (128-byte swizzle).
+    const uint32_t ds_row = sDS + half * kBoxBytes + row * 128;
+    uint32_t qi = 0, s_ph = 0, dp_ph = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int idx = item_index(k, blockIdx.x, gridDim.x);
+      if (idx >= n_items) break;
+      const Item it = decode(sh, idx);
+      QSeq seq;
+      seq.init(sh, it.kv, it.knat);
+      int w_lo, w_hi;
+      key_window(sh, it.knat * kT + row, w_lo, w_hi);
+      int qrow, qnat, nq = 0;
+      while (seq.next(qrow, qnat)) {
+        const int st = qi & 1;
+        const int c_lo = w_lo - qnat, c_hi = w_hi - qnat;  // visible query columns
+        const bool cut = c_lo > 0 || c_hi < kT - 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc))) {
+          ok = false;
+          break;
+        }
+        const float* lse = lse_s + st * kT + 64 * half;
+        const float* dlt = dlt_s + st * kT + 64 * half;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS), s_ph, wc))) {
+          ok = false;
+          break;
+        }
+        s_ph ^= 1;
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(tl + kColX + 64 * half, r);
+        tmem_ld32(tl + kColX + 64 * half + 32, r + 32);
+        tmem_wait_ld_regs(r);
+        reg_fence32(r + 32);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float2 l2 = *reinterpret_cast<const float2*>(lse + 2 * j);
+          r[2 * j] = __float_as_uint(ex2(fmaf(__uint_as_float(r[2 * j]), sl2, -l2.x * kLog2e)));
+          r[2 * j + 1] =
+              __float_as_uint(ex2(fmaf(__uint_as_float(r[2 * j + 1]), sl2, -l2.y * kLog2e)));
+        }
+        if (cut) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (64 * half + j < c_lo || 64 * half + j > c_hi) r[j] = 0u;
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          pk[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+        tmem_st32(tl + kColX + 64 * half, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarP));
+        // dS^T = scale * P^T (dP^T - Delta), dP^T read 32 columns at a time
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP), dp_ph, wc))) {
+          ok = false;
+          break;
+        }
+        dp_ph ^= 1;
+        tc_fence_after();
+        uint32_t ds[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t d[32];
+          tmem_ld32(tl + kColY + 64 * half + 32 * cc, d);
+          tmem_wait_ld_regs(d);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int c = 32 * cc + 2 * j;
+            const float2 dl = *reinterpret_cast<const float2*>(dlt + c);  // scale * Delta
+            ds[16 * cc + j] =
+                pack_bf16(__uint_as_float(r[c]) * fmaf(__uint_as_float(d[2 * j]), scale, -dl.x),
+                          __uint_as_float(r[c + 1]) *
+                              fmaf(__uint_as_float(d[2 * j + 1]), scale, -dl.y));
+          }
+        }
+        // The dS^T buffer doubles as the previous tile's dQ staging: wait
+        // until the drain's last reduction of that tile has read it.
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDSFree), (qi & 1) ^ 1, wc))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = ds_row + ((uint32_t)(c ^ (row & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(ds[4 * c]),
+                       "r"(ds[4 * c + 1]), "r"(ds[4 * c + 2]), "r"(ds[4 * c + 3])
+                       : "memory");
+        }
+        fence_async_smem();  // generic-proxy writes -> the tensor core's reads
+        tc_fence_before();
+        mbar_arrive(bar(kBarDS));
+        ++qi;
+        ++nq;
+      }
+      if (!ok) break;
+      // Epilogue: this head's dK / dV partial, columns [64*half, +64).
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarAcc), k & 1, wc))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kv_row0 = sh.kv_natural ? it.knat * kT : it.kv.row;
+      const int64_t pbase =
+          (((int64_t)it.b * sh.S + kv_row0 + row) * sh.H + it.h) * kD + 64 * half;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        float* dst = (which == 0 ? args.dv_part : args.dk_part) + pbase;
+        const uint32_t col = (which == 0 ? kColDV : kColDK) + 64 * half;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t d[32];
+          tmem_ld32(tl + col + 32 * cc, d);
+          tmem_wait_ld_regs(d);
+          if (nq == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) d[j] = 0u;
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<float4*>(dst + 32 * cc + 4 * u) =
+                make_float4(__uint_as_float(d[4 * u]), __uint_as_float(d[4 * u + 1]),
+                            __uint_as_float(d[4 * u + 2]), __uint_as_float(d[4 * u + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(bar(kBarAccFree));
+    }
+  } else {
+    // -------------------------------------------------------------- dQ drain
+    // Thread = feature lane d of dQ^T (TMEM lane); four rounds of 32 query
+    // columns per tile, staged as [32 rows][128] float32 in two 16 KB slots
+    // over the dS^T buffer, each added to the accumulator by one bulk
+    // reduction issued by the leader thread.
+    reg_dec<kRegDrain>();
+    const int wq = warp & 3;
+    const int dl = wq * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
+    const bool leader = warp == 12 && lane == 0;
+    uint32_t qi = 0;
+    bool ok = true;
+    auto stage = [&](int slot, const uint32_t* v) {
+      const uint32_t dst = sDS + slot * kStageBytes + dl * 4;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst + i * (kD * 4)), "r"(v[i]) : "memory");
+      fence_async_smem();
+      mbar_arrive(bar(kBarStageFull + slot));
+    };
+    for (int k = 0; ok; ++k) {
+      const int idx = item_index(k, blockIdx.x, gridDim.x);
+      if (idx >= n_items) break;
+      const Item it = decode(sh, idx);
+      QSeq seq;
+      seq.init(sh, it.kv, it.knat);
+      int qrow, qnat;
+      while (seq.next(qrow, qnat)) {
+        const int row0 = it.b * sh.S + qrow;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDQ), qi & 1, wc))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t v[64];
+        tmem_ld32(tl + kColY, v);
+        tmem_ld32(tl + kColY + 32, v + 32);
+        tmem_wait_ld_regs(v);
+        reg_fence32(v + 32);
+        stage(0, v);
+        stage(1, v + 32);
+        tmem_ld32(tl + kColY + 64, v);
+        tmem_ld32(tl + kColY + 96, v + 32);
+        tmem_wait_ld_regs(v);
+        reg_fence32(v + 32);
+        tc_fence_before();
+        mbar_arrive(bar(kBarYFree));  // Y is free for the next tile's dP^T
+        if (leader) {
+          for (int s = 0; s < 2 && ok; ++s) {
+            if (!mbar_wait(bar(kBarStageFull + s), 0u, wc)) {
+              ok = false;
+              break;
+            }
+            tma_reduce_add_3d(&tm_dq, sDS + s * kStageBytes, it.h, row0 + s * kStageRows);
+            bulk_commit();
+          }
+          if (ok) {
+            bulk_wait_read<1>();
+            mbar_arrive(bar(kBarStageFree + 0));
+            bulk_wait_read<0>();
+            mbar_arrive(bar(kBarStageFree + 1));
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        for (int s = 0; s < 2; ++s) {
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarStageFree + s), qi & 1, wc))) {
+            ok = false;
+            break;
+          }
+          stage(s, v + 32 * s);
+        }
+        if (!ok) break;
+        if (leader) {
+          for (int s = 0; s < 2 && ok; ++s) {
+            if (!mbar_wait(bar(kBarStageFull + s), 1u, wc)) {
+              ok = false;
+              break;
+            }
+            tma_reduce_add_3d(&tm_dq, sDS + s * kStageBytes, it.h,
+                              row0 + (2 + s) * kStageRows);
+            bulk_commit();
+          }
+          if (ok) {
+            bulk_wait_read<0>();
+            mbar_arrive(bar(kBarDSFree));  // dS^T of the next tile may overwrite the slots
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        ++qi;
+      }
+    }
+    if (leader) bulk_wait_all();  // every reduction complete before the CTA ends
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fz
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -1096,9 +1712,48 @@ bool make_map(CUtensorMap* m, const void* ptr, int heads, int64_t rows) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The float32 dQ accumulator [rows][heads][128] as a 3-D tensor, box of 32
+// rows x 1 head x 128 features (16 KB, no swizzle): the bulk reductions'
+// destination.
+bool make_map_dq(CUtensorMap* m, const float* ptr, int heads, int64_t rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)kD * 4, (cuuint64_t)heads * kD * 4};
+  cuuint32_t box[3] = {(cuuint32_t)kD, 1, (cuuint32_t)fz::kStageRows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool tc_bwd_available() { return true; }
+
+cudaError_t launch_tc_bwd_onepass(const BwdArgs& a, cudaStream_t stream) {
+  const RingShape& sh = a.sh;
+  const int n_items = sh.B * sh.H * (sh.S / kT);
+  if (n_items == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  const int64_t rows = (int64_t)sh.B * sh.S;
+  if (!make_map(&mq, a.q, sh.H, rows) || !make_map(&mk, a.k, sh.Hkv, rows) ||
+      !make_map(&mv, a.v, sh.Hkv, rows) || !make_map(&mdo, a.dout, sh.H, rows) ||
+      !make_map_dq(&mdq, a.dq_acc, sh.H, rows))
+    return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fz::dkdvq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           fz::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = n_items < sms ? n_items : sms;
+  fz::dkdvq_kernel<<<grid, fz::kThreadsF, fz::kSmemBytes, stream>>>(mq, mk, mv, mdo, mdq, a,
+                                                                    n_items);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_tc_bwd(const BwdArgs& a, cudaStream_t stream) {
   const RingShape& sh = a.sh;

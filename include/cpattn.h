@@ -76,7 +76,15 @@ enum cpattn_dtype {
    * as float32 whatever the input dtype.  A bf16 gradient element of
    * magnitude >= 8 carries a rounding error of up to 2^-5; float32 output
    * keeps the gradients at their float32 accumulation accuracy. */
-  CPATTN_GRAD_F32 = 0x10
+  CPATTN_GRAD_F32 = 0x10,
+  /* Flag for the ring backward (OR it into dtype): on the tensor-core path,
+   * compute dK, dV and dQ in one pass over the K/V tiles (five tile
+   * products per tile pair instead of seven), each K/V tile adding its share
+   * of dQ to a float32 accumulator with bulk reductions.  The order of
+   * those additions varies from run to run, so dQ is not bitwise
+   * reproducible (it stays within the same tolerance); without the flag the
+   * backward is deterministic.  Ignored on the CUDA-core path. */
+  CPATTN_BWD_ONEPASS = 0x20
 };
 enum cpattn_path { CPATTN_PATH_SIMT = 0, CPATTN_PATH_TCGEN05 = 1 };
 
