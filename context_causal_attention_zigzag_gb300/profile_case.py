@@ -2,8 +2,8 @@
 profiler captures (ncu) wrap.
 
     python -m context_causal_attention_zigzag_gb300.profile_case fwd_s32768
-    python -m context_causal_attention_zigzag_gb300.profile_case bwd_s16384
-    python -m context_causal_attention_zigzag_gb300.profile_case docs_full
+    python -m context_causal_attention_zigzag_gb300.profile_case bwd_s16384 [--onepass]
+    python -m context_causal_attention_zigzag_gb300.profile_case docs_s16384 [--onepass]
     python -m context_causal_attention_zigzag_gb300.profile_case permute_s32768
     python -m context_causal_attention_zigzag_gb300.profile_case merge_s32768
 
@@ -25,10 +25,11 @@ CASES = {
     # the S=131072 forward+backward workload at S=16384 (1/64 of its tile pairs)
     "bwd_s16384": inputs.Workload("bwd_s16384", 1, 32, 8, 16384, 128, 4, cpa.ZIGZAG, True,
                                   torch.bfloat16, backward=True, seed=5),
-    # the S=131072 forward+backward workload itself (for single-pass counters only)
-    "c5_full": inputs.WORKLOADS["c5_bf16_s131072_fwdbwd"],
-    # the same shape with packed documents (single-pass counters only)
-    "docs_full": inputs.DOC_WORKLOADS["docs_bf16_s131072_fwdbwd"],
+    # the packed-document workload reduced the same way (documents of mean
+    # length 1024 instead of 8192)
+    "docs_s16384": inputs.Workload("docs_s16384", 1, 32, 8, 16384, 128, 4, cpa.ZIGZAG, True,
+                                   torch.bfloat16, backward=True, seed=5, doc_mean=1024,
+                                   doc_seed=2006),
 }
 
 
@@ -59,7 +60,7 @@ def run_hbm(case: str, repeats: int) -> int:
     return cpa.device_status()
 
 
-def run(case: str, repeats: int = 3) -> int:
+def run(case: str, repeats: int = 3, onepass: bool = False) -> int:
     if case in HBM_CASES:
         return run_hbm(case, repeats)
     w = CASES[case]
@@ -76,10 +77,10 @@ def run(case: str, repeats: int = 3) -> int:
             o, lse = cpa.ring_fwd_docs(qs, ks, vs, w.cp, bounds, w.layout, w.causal)
         if dos is not None and bounds is None:
             cpa.ring_bwd(qs, ks, vs, o, dos, lse, w.cp, w.layout, w.causal,
-                         grad_dtype=torch.float32)
+                         grad_dtype=torch.float32, onepass=onepass)
         elif dos is not None:
             cpa.ring_bwd_docs(qs, ks, vs, o, dos, lse, w.cp, bounds, w.layout, w.causal,
-                              grad_dtype=torch.float32)
+                              grad_dtype=torch.float32, onepass=onepass)
     torch.cuda.synchronize()
     return cpa.device_status()
 
@@ -88,8 +89,10 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=sorted(CASES) + sorted(HBM_CASES))
     ap.add_argument("--repeats", type=int, default=3)
+    ap.add_argument("--onepass", action="store_true",
+                    help="the one-pass backward (CPATTN_BWD_ONEPASS) instead of the two kernels")
     a = ap.parse_args()
-    status = run(a.case, a.repeats)
+    status = run(a.case, a.repeats, a.onepass)
     print(f"{a.case}: status {status}")
     raise SystemExit(0 if status == 0 else 1)
 
