@@ -183,6 +183,7 @@ def run_ours(args):
     w = ALL_WORKLOADS[args.workload]
     peak, peak_sus, hbm, peak_kind = peaks()
     stream = torch.cuda.current_stream(dev)
+    onepass = args.bwd == "onepass"
 
     q, k, v, do = inputs.generate(w)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
@@ -237,10 +238,10 @@ def run_ours(args):
         if w.backward:
             if docs is None:
                 cpa.ring_bwd(qs, ks, vs, o, dos, lse, cp, layout, causal, dq=dq, dk=dk, dv=dv,
-                             workspace=wsp, grad_dtype=gdt)
+                             workspace=wsp, grad_dtype=gdt, onepass=onepass)
             else:
                 cpa.ring_bwd_docs(qs, ks, vs, o, dos, lse, cp, bounds, layout, causal, dq=dq,
-                                  dk=dk, dv=dv, workspace=wsp, grad_dtype=gdt)
+                                  dk=dk, dv=dv, workspace=wsp, grad_dtype=gdt, onepass=onepass)
             if timed:
                 mark("bwd1")
         cpa.zigzag_unpermute(o, cp, layout, out=o_nat)
@@ -252,8 +253,13 @@ def run_ours(args):
 
     bwd_path = cpa.plan(B, H, Hkv, S, D, cp, layout, causal, w.dtype, backward=True)[0] \
         if w.backward else None
-    # permutes + forward + backward (pre-pass, kernel(s), finishing pass) + unpermutes
-    bwd_launches = (4 if bwd_path == cpa.PATH_TCGEN05 else 3) if w.backward else 0
+    # permutes + forward + backward (pre-pass, kernel(s), finishing pass(es)) + unpermutes
+    if not w.backward:
+        bwd_launches = 0
+    elif bwd_path != cpa.PATH_TCGEN05:
+        bwd_launches = 3
+    else:
+        bwd_launches = 3 if onepass else 4   # one-pass: float32 dQ needs no conversion
     launches_per_step = ((4 if w.backward else 3) + 1 + bwd_launches + (5 if w.backward else 2)
                          + (1 if docs is not None else 0))
     fwd_flops = w.useful_flops(False)
@@ -313,7 +319,8 @@ def run_ours(args):
 
             def e2e_step():
                 cpa.attention_host(hq, hk, hv, hdo, cp, layout, causal, workspace=hws,
-                                   grad_dtype=gdt if w.backward else None, **hres)
+                                   grad_dtype=gdt if w.backward else None, onepass=onepass,
+                                   **hres)
         else:
             e2e_api = "cpattn_attention_host_docs"
             hws = torch.empty(cpa.attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout,
@@ -322,7 +329,8 @@ def run_ours(args):
 
             def e2e_step():
                 cpa.attention_host_docs(hq, hk, hv, hdo, cp, docs, layout, causal, workspace=hws,
-                                        grad_dtype=gdt if w.backward else None, **hres)
+                                        grad_dtype=gdt if w.backward else None,
+                                        onepass=onepass, **hres)
 
         e2e_step()
         barrier()
@@ -411,6 +419,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (no flush)",
                    "fwd_path": "tcgen05" if path == 1 else "simt", "tile": tile,
                    "grad_dtype": "f32" if w.backward else None,
+                   "bwd_path": (args.bwd if w.backward else None),
                    "documents": None if docs is None else len(docs) - 1,
                    "useful_tflop_per_step": step_flops / 1e12},
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps, "clocks": clk,
@@ -910,6 +919,9 @@ def main():
     ap.add_argument("--no-ulysses", action="store_true")
     ap.add_argument("--no-hbm", action="store_true")
     ap.add_argument("--no-hier", action="store_true")
+    ap.add_argument("--bwd", default="two", choices=["two", "onepass"],
+                    help="tensor-core backward of the main step: the deterministic two-kernel "
+                         "path or the one-pass kernel (CPATTN_BWD_ONEPASS)")
     ap.add_argument("--no-named", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

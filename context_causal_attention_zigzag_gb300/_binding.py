@@ -806,7 +806,7 @@ def attention_host_parts(B, H, Hkv, S, D) -> int:
     return int(lib().cpattn_attention_host_parts(B, H, Hkv, S, D))
 
 
-def _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype, device, name):
+def _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype, device, name, onepass=False):
     """Shared marshalling of the host-to-host calls: checks, dtype code,
     output tensors (pinned when the inputs are)."""
     if q.is_cuda or k.is_cuda or v.is_cuda:
@@ -821,6 +821,8 @@ def _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype, device, name)
     gdt = q.dtype if grad_dtype is None else grad_dtype
     if backward and gdt == torch.float32 and q.dtype != torch.float32:
         code |= GRAD_F32
+    if backward and onepass:
+        code |= ONEPASS
     pin = q.is_pinned()
 
     def host(shape, dtype, t):
@@ -836,14 +838,14 @@ def _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype, device, name)
 
 def attention_host(q, k, v, dout, cp, layout=ZIGZAG, causal=True, scale=None, out=None,
                    lse=None, dq=None, dk=None, dv=None, grad_dtype=None, workspace=None,
-                   device=None, stream=None, parts=0):
+                   device=None, stream=None, parts=0, onepass=False):
     """cpattn_attention_host: natural-order CPU tensors (pinned for
     asynchronous copies) in and out, the whole path on the GPU in between,
     the heads in `parts` pipelined groups (0: the library's choice).
     dout None: forward only.  Returns (out, lse) or (out, lse, dq, dk, dv) as
     CPU tensors; they are complete once the stream has been synchronised."""
     dev, code, backward, res = _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype,
-                                             device, "attention_host")
+                                             device, "attention_host", onepass)
     B, S, H, D = q.shape
     Hkv = k.shape[2]
     need = attention_host_workspace_bytes(B, H, Hkv, S, D, cp, layout, code, backward)
@@ -867,13 +869,14 @@ def attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout=ZIGZAG, dtyp
 
 def attention_host_docs(q, k, v, dout, cp, cu_seqlens=None, layout=ZIGZAG, causal=True,
                         scale=None, out=None, lse=None, dq=None, dk=None, dv=None,
-                        grad_dtype=None, workspace=None, device=None, stream=None, parts=0):
+                        grad_dtype=None, workspace=None, device=None, stream=None, parts=0,
+                        onepass=False):
     """cpattn_attention_host_docs: attention_host for packed documents and any
     sequence length.  cu_seqlens: document offsets over the S tokens (a
     sequence of ints, 0 ... S), None for one document.  Returns (out, lse) or
     (out, lse, dq, dk, dv) as CPU tensors over the S real tokens."""
     dev, code, backward, res = _host_prepare(q, k, v, dout, out, lse, dq, dk, dv, grad_dtype,
-                                             device, "attention_host_docs")
+                                             device, "attention_host_docs", onepass)
     B, S, H, D = q.shape
     Hkv = k.shape[2]
     need = attention_host_docs_workspace_bytes(B, H, Hkv, S, D, cp, layout, code, backward)

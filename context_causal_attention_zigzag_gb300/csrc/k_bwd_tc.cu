@@ -1089,11 +1089,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // reproducible from run to run; the two-kernel path is).
 //
 // CTA = 512 threads: warp 0 TMA, warp 1 TMEM owner + MMA issuer (warps 0-3:
-// 88 registers), warps 4-11 the elementwise halves ([0,64) and [64,128) of
+// 104 registers), warps 4-11 the elementwise halves ([0,64) and [64,128) of
 // the query columns) and the dK / dV epilogue (152 registers), warps 12-15
-// the dQ drain (120 registers; thread = feature lane).  The split uses the
-// whole 512 x 128 registers of the launch and leaves ptxas nothing to spill.  Shared memory: K, V,
-// two Q / dO stages, dS^T (= the dQ staging), LSE / Delta rows: 226 KB.
+// the dQ drain (104 registers; thread = feature lane).  The split uses the
+// whole 512 x 128 registers of the launch and leaves ptxas nothing to
+// spill.  Shared memory: K, V, two Q / dO stages, dS^T (= the dQ staging),
+// LSE / Delta rows: 226 KB.
 namespace fz {
 
 constexpr int kThreadsF = 512;
@@ -1133,7 +1134,7 @@ constexpr int kStageRows = 32;                       // query rows per reduction
 constexpr int kStageBytes = kStageRows * kD * 4;     // 16 KB of float32
 // Registers per thread for the three roles (setmaxnreg); the launch gives
 // 512 threads x 128.
-constexpr int kRegCtl = 88, kRegEw = 152, kRegDrain = 120;
+constexpr int kRegCtl = 104, kRegEw = 152, kRegDrain = 104;
 static_assert(128 * (kRegCtl + 2 * kRegEw + kRegDrain) <= 512 * 128, "register split");
 static_assert(kSmemBytes <= 232448, "shared memory");
 
@@ -1378,20 +1379,19 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             mma_ts(tmem + kColDV, tmem + kColX + a_col(kk),
                    sdesc_sw128(sDO + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
-          // dK += dS^T Q, then dQ^T = K^T dS^T into Y (the elementwise warps
-          // have read dP^T there before signalling dS^T).
+          // dK += dS^T Q (A = the bf16 dS^T the elementwise warps packed into
+          // Y), then dQ^T = K^T dS^T (both operands in shared memory) over Y:
+          // MMAs run in order, so dK has read Y before dQ^T writes it.
           if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
             ok = false;
             break;
           }
           ds_ph ^= 1;
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + kColDK, sdesc_sw128(sDS + off, 16, 1024),
+          for (int kk = 0; kk < kT / 16; ++kk)
+            mma_ts(tmem + kColDK, tmem + kColY + a_col(kk),
                    sdesc_sw128(sQ + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
-          }
           mma_commit(bar(kBarQEmpty + st));  // Q, dO of this tile read for the last time
           for (int kk = 0; kk < kT / 16; ++kk)
             mma_ss(tmem + kColY, sdesc_sw128(sK + kk * 2048, kBoxBytes, 1024),
@@ -1525,6 +1525,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           ok = false;
           break;
         }
+        // dS^T twice: packed over the first 32 of this half's dP^T columns in
+        // TMEM (dK's A operand), and into its shared-memory box (dQ^T's B).
+        tmem_st32(tl + kColY + 64 * half, ds);
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t addr = ds_row + ((uint32_t)(c ^ (row & 7)) << 4);
@@ -1533,6 +1536,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                        : "memory");
         }
         fence_async_smem();  // generic-proxy writes -> the tensor core's reads
+        tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarDS));
         ++qi;

@@ -86,15 +86,20 @@ int main() {
   struct Case {
     int live;
     int chunk;
-  } cases[] = {{16, 65536}, {1024, 65536}, {1024, 16384}, {1024, 4096},
-               {8192, 65536}, {8192, 16384}};
+    int grid;  // 0: every SM
+  } cases[] = {{16, 65536, 0}, {1024, 65536, 0}, {1024, 16384, 0}, {1024, 4096, 0},
+               {8192, 65536, 0}, {8192, 16384, 0},
+               // fewer SMs issuing: a per-SM limit keeps the per-SM rate, an
+               // aggregate (L2) limit lets it rise
+               {1024, 65536, 8}, {1024, 65536, 38}, {1024, 65536, 76}};
   for (const Case& c : cases) {
-    reduce_kernel<<<sms, 128, kTileBytes>>>(buf, c.live, 20, c.chunk, ns);  // warm-up
+    const int grid = c.grid ? c.grid : sms;
+    reduce_kernel<<<grid, 128, kTileBytes>>>(buf, c.live, 20, c.chunk, ns);  // warm-up
     cudaEvent_t a, b;
     cudaEventCreate(&a);
     cudaEventCreate(&b);
     cudaEventRecord(a);
-    reduce_kernel<<<sms, 128, kTileBytes>>>(buf, c.live, reps, c.chunk, ns);
+    reduce_kernel<<<grid, 128, kTileBytes>>>(buf, c.live, reps, c.chunk, ns);
     cudaEventRecord(b);
     cudaError_t e = cudaEventSynchronize(b);
     if (e != cudaSuccess) {
@@ -103,9 +108,11 @@ int main() {
     }
     float ms = 0.f;
     cudaEventElapsedTime(&ms, a, b);
-    const double bytes = (double)sms * reps * kTileBytes;
-    printf("live %5d tiles (%6.1f MB) chunk %6d B: %.3f ms, %.2f TB/s reduced\n", c.live,
-           c.live * (double)kTileBytes / 1e6, c.chunk, ms, bytes / (ms * 1e-3) / 1e12);
+    const double bytes = (double)grid * reps * kTileBytes;
+    printf("%3d SMs, live %5d tiles (%6.1f MB) chunk %6d B: %.3f ms, %.2f TB/s reduced "
+           "(%.1f GB/s per SM)\n",
+           grid, c.live, c.live * (double)kTileBytes / 1e6, c.chunk, ms,
+           bytes / (ms * 1e-3) / 1e12, bytes / grid / (ms * 1e-3) / 1e9);
   }
   return 0;
 }
