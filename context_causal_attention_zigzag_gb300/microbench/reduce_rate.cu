@@ -70,6 +70,25 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// The same tile-sized reductions from registers: every thread adds float4
+// values with red.global.add.v4.f32 (the load/store path instead of the bulk
+// copy engine).
+__global__ void __launch_bounds__(512, 1)
+    red_v4_kernel(float* buf, int live, int reps, unsigned long long* ns) {
+  const float4 one = make_float4(1.f, 1.f, 1.f, 1.f);
+  const uint64_t t0 = gtimer();
+  for (int i = 0; i < reps; ++i) {
+    const int64_t slot = ((int64_t)i * gridDim.x + blockIdx.x) % live;
+    float4* dst = reinterpret_cast<float4*>(reinterpret_cast<char*>(buf) + slot * kTileBytes);
+    for (int e = threadIdx.x; e < kTileBytes / 16; e += blockDim.x)
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + e), "f"(one.x),
+                   "f"(one.y), "f"(one.z), "f"(one.w)
+                   : "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) ns[blockIdx.x] = gtimer() - t0;
+}
+
 }  // namespace
 
 int main() {
@@ -113,6 +132,29 @@ int main() {
            "(%.1f GB/s per SM)\n",
            grid, c.live, c.live * (double)kTileBytes / 1e6, c.chunk, ms,
            bytes / (ms * 1e-3) / 1e12, bytes / grid / (ms * 1e-3) / 1e9);
+  }
+  for (int grid : {sms, 8}) {
+    for (int live : {1024, 8192}) {
+      red_v4_kernel<<<grid, 512>>>(buf, live, 20, ns);  // warm-up
+      cudaEvent_t a, b;
+      cudaEventCreate(&a);
+      cudaEventCreate(&b);
+      cudaEventRecord(a);
+      red_v4_kernel<<<grid, 512>>>(buf, live, reps, ns);
+      cudaEventRecord(b);
+      cudaError_t e = cudaEventSynchronize(b);
+      if (e != cudaSuccess) {
+        printf("error %s\n", cudaGetErrorString(e));
+        return 1;
+      }
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, a, b);
+      const double bytes = (double)grid * reps * kTileBytes;
+      printf("red.v4 %3d SMs, live %5d tiles (%6.1f MB): %.3f ms, %.2f TB/s reduced "
+             "(%.1f GB/s per SM)\n",
+             grid, live, live * (double)kTileBytes / 1e6, ms, bytes / (ms * 1e-3) / 1e12,
+             bytes / grid / (ms * 1e-3) / 1e9);
+    }
   }
   return 0;
 }
