@@ -14,8 +14,8 @@
 //
 // dkdv kernel (K/V-major).  Work item: one 128-row K/V tile and one query
 // head.  The K/V tile stays in shared memory; the query tiles that see it
-// stream past (ring order), Q and dO by TMA, their LSE / Delta rows by bulk
-// copy.  Per query tile, with the tile transposed so that TMEM lanes are K/V
+// stream past (latest natural position first, see QSeq), Q and dO by TMA,
+// their LSE / Delta rows by bulk copy.  Per query tile, with the tile transposed so that TMEM lanes are K/V
 // rows:
 //   S^T  = K Q^T   -> TMEM [0,128)       dP^T = V dO^T -> TMEM [128,256)
 //   P^T  = exp2(S^T*scale*log2e - LSE*log2e)  -> bf16 over S^T
@@ -122,16 +122,20 @@ __device__ __forceinline__ TilePos tile_pos(const RingShape& sh, int knat) {
   return p;
 }
 
-// Query tiles (of one head) that see a K/V tile, in ring order: step t,
-// receiving rank (s + t) mod cp, that rank's chunks.  The tile's keys are
-// seen by the queries [lo, hi] (natural positions): under the causal rule
-// from the tile's first key on, within the documents of its keys.  In the
-// all-gather schedule (sh.kv_natural) the query chunks are taken in natural
-// order instead (t is then the chunk index); query rows stay sharded.
+// Query tiles (of one head) that see a K/V tile.  The tile's keys are seen by
+// the queries [lo, hi] (natural positions): under the causal rule from the
+// tile's first key on, within the documents of its keys.  The walk takes
+// those query tiles from the latest natural position down to the earliest,
+// whichever rank holds them, so that the CTAs in flight -- K/V tiles of one
+// head -- start on the same query tile and read the same Q / dO tiles at
+// about the same time (one fetch from HBM serves them all through L2).  The
+// ring step of each tile is reported for the census: rank r receives the
+// K/V of source rank s at step (r - s) mod cp.  Query rows stay sharded in
+// the all-gather schedule too (sh.kv_natural), where the order is the same.
 struct QSeq {
-  int cp, per, L, c, s, lo, hi, t_end;
-  int t, jq, qt, qt_end;
-  bool natural;
+  int cp, L, c, s, per;
+  int m, m_lo;  // natural query tile, current and lowest
+  int t;        // ring step of the tile last returned
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& kv, int knat) {
     cp = sh.cp;
@@ -139,39 +143,25 @@ struct QSeq {
     L = sh.L;
     c = sh.c;
     s = kv.rank;
-    natural = sh.kv_natural != 0;
-    t_end = natural ? cp * per : cp;
-    int x;
+    int lo, hi, x;
     key_window(sh, knat * kT, lo, x);
     key_window(sh, knat * kT + kT - 1, x, hi);
+    m = hi >= lo ? hi / kT : -1;
+    m_lo = lo / kT;
     t = 0;
-    jq = 0;
-    qt = 0;
-    qt_end = -1;
   }
 
   // qrow: sharded row of the query tile; qnat: natural position of its first row.
   __device__ __forceinline__ bool next(int& qrow, int& qnat) {
-    while (t < t_end) {
-      const int r = natural ? ((per == 1 || t < cp) ? t : 2 * cp - 1 - t) : (s + t) % cp;
-      while (jq < (natural ? 1 : per)) {
-        const int qc = natural ? t : ((per == 1 || jq == 0) ? r : 2 * cp - 1 - r);
-        const int slot = natural ? ((per == 1 || t < cp) ? 0 : 1) : jq;
-        if (qt_end < 0) tiles_overlapping(qc * c, c, kT, lo, hi, qt, qt_end);
-        if (qt < qt_end) {
-          qrow = r * L + slot * c + qt * kT;
-          qnat = qc * c + qt * kT;
-          ++qt;
-          return true;
-        }
-        ++jq;
-        qt = 0;
-        qt_end = -1;
-      }
-      ++t;
-      jq = 0;
-    }
-    return false;
+    if (m < m_lo) return false;
+    qnat = m * kT;
+    const int chunk = qnat / c;
+    const int r = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
+    const int slot = (per == 1 || chunk < cp) ? 0 : 1;
+    qrow = r * L + slot * c + (qnat - chunk * c);
+    t = ((r - s) % cp + cp) % cp;
+    --m;
+    return true;
   }
 };
 
@@ -1071,7 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 //
 // Work item and walk as the dkdv kernel (one 128-row K/V tile x one query
-// head, the query tiles that see it in ring order).  Per query tile j, with
+// head, the query tiles that see it, latest first).  Per query tile j, with
 // TMEM lanes = K/V rows for S^T, dP^T, dV, dK and lanes = features for dQ^T:
 //   S^T  = K Q^T  -> X             dP^T = V dO^T -> Y
 //   P^T  -> bf16 over X (TMEM)     dS^T = scale P^T (dP^T - Delta) -> bf16

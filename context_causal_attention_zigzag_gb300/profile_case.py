@@ -3,6 +3,7 @@ profiler captures (ncu) wrap.
 
     python -m context_causal_attention_zigzag_gb300.profile_case fwd_s32768
     python -m context_causal_attention_zigzag_gb300.profile_case bwd_s16384 [--onepass]
+    python -m context_causal_attention_zigzag_gb300.profile_case bwd_s131072_g1
     python -m context_causal_attention_zigzag_gb300.profile_case docs_s16384 [--onepass]
     python -m context_causal_attention_zigzag_gb300.profile_case permute_s32768
     python -m context_causal_attention_zigzag_gb300.profile_case merge_s32768
@@ -25,6 +26,10 @@ CASES = {
     # the S=131072 forward+backward workload at S=16384 (1/64 of its tile pairs)
     "bwd_s16384": inputs.Workload("bwd_s16384", 1, 32, 8, 16384, 128, 4, cpa.ZIGZAG, True,
                                   torch.bfloat16, backward=True, seed=5),
+    # one kv group of the S=131072 workload (4 query heads on 1 kv head): the
+    # same per-head Q / dO working set as the full workload, 1/8 of its heads
+    "bwd_s131072_g1": inputs.Workload("bwd_s131072_g1", 1, 4, 1, 131072, 128, 16, cpa.ZIGZAG,
+                                      True, torch.bfloat16, backward=True, seed=5),
     # the packed-document workload reduced the same way (documents of mean
     # length 1024 instead of 8192)
     "docs_s16384": inputs.Workload("docs_s16384", 1, 32, 8, 16384, 128, 4, cpa.ZIGZAG, True,
