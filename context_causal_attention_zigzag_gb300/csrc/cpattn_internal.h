@@ -7,6 +7,14 @@
 
 #include "cpattn.h"
 
+// Planted mistakes for the mutation tests: a build with -DCPATTN_MUTATION=n
+// (n > 0, into a build folder of its own) compiles mistake n into the
+// library, so that the tests can show that the GPU parity checks catch it.
+// The regular build is always 0.
+#ifndef CPATTN_MUTATION
+#define CPATTN_MUTATION 0
+#endif
+
 namespace cpattn {
 
 // Shape of one ring problem.  Positions are token indices along S.
@@ -50,7 +58,11 @@ __host__ __device__ inline int sharded_pos(const RingShape& s, int n) {
 
 // Ring step at which rank r holds the K/V of rank src.
 __host__ __device__ inline int ring_step_of(int r, int src, int cp) {
+#if CPATTN_MUTATION == 2
+  int t = (src - r) % cp;  // planted: the ring turned the other way
+#else
   int t = (r - src) % cp;
+#endif
   return t < 0 ? t + cp : t;
 }
 
@@ -109,14 +121,6 @@ __host__ __device__ inline int natural_pos(const RingShape& s, int p) {
 __host__ __device__ inline int rank_chunk(const RingShape& s, int r, int j) {
   return (s.per_rank == 1 || j == 0) ? r : 2 * s.cp - 1 - r;
 }
-
-// Planted mistakes for the mutation tests: a build with -DCPATTN_MUTATION=n
-// (n > 0, into a build folder of its own) compiles mistake n into the
-// library, so that the tests can show that the GPU parity checks catch it.
-// The regular build is always 0.
-#ifndef CPATTN_MUTATION
-#define CPATTN_MUTATION 0
-#endif
 
 // Ring source: at step t rank r holds the K/V of rank (r - t) mod cp.
 __host__ __device__ inline int ring_source(int r, int t, int cp) {

@@ -33,10 +33,10 @@
 //
 // dq kernel (query-major).  Work item: one 128-row query tile of one head.
 // Q, dO stay in shared memory, LSE / Delta in registers (TMEM lane = query
-// row); the K/V tiles of the ring stream past through a ring of five 32 KB
-// slots (K(j), V(j), K(j+1), ... in consecutive slots; V(j)'s slot is free
-// once dP(j) has read it, K(j)'s once dQ(j) has, so loads run up to two
-// tiles ahead):
+// row); the K/V tiles it sees (earliest first, see KSeq) stream past through
+// a ring of five 32 KB slots (K(j), V(j), K(j+1), ... in consecutive slots;
+// V(j)'s slot is free once dP(j) has read it, K(j)'s once dQ(j) has, so
+// loads run up to two tiles ahead):
 //   S = Q K^T -> TMEM [0,128)     dP = dO V^T -> TMEM [128,256) / [256,384)
 //   dS = scale * exp2(S*scale*log2e - LSE*log2e) (dP - Delta) -> bf16 over dP
 //   dQ += dS K  (TS, K read MN-major) -> TMEM [384,512)
@@ -159,21 +159,27 @@ struct QSeq {
     const int r = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
     const int slot = (per == 1 || chunk < cp) ? 0 : 1;
     qrow = r * L + slot * c + (qnat - chunk * c);
-    t = ((r - s) % cp + cp) % cp;
+    t = ring_step_of(r, s, cp);
     --m;
     return true;
   }
 };
 
-// K/V tiles that a query tile sees, in ring order (step t brings the shard of
-// rank (r - t) mod cp), the diagonal tile last.  The query tile sees the keys
-// [lo(first row), hi(last row)]; under the causal rule the ring walk stops
-// before the tile's own first key and the diagonal tile comes at the end.
-// All-gather schedule: natural chunk order, natural K/V rows.
+// K/V tiles that a query tile sees.  The query tile sees the keys [lo(first
+// row), hi(last row)] (natural positions; under the causal rule up to its
+// own last row, so its own tile -- the diagonal, masked element-wise -- is
+// the last one).  The walk takes them in natural order, earliest first,
+// whichever rank holds them: the CTAs in flight hold consecutive query tiles
+// of one kv head and so start on the same K/V tile and read the same K / V
+// tiles at about the same time (one fetch from HBM serves them all through
+// L2).  The ring step of each tile is reported for the census: rank r holds
+// the K/V of source rank s at step (r - s) mod cp.  All-gather schedule
+// (sh.kv_natural): the same order over the natural-order K/V rows.
 struct KSeq {
-  int cp, per, L, c, r, qrow, q0, wlo, whi, t_end;
-  int t, jj, kt, kt_end;
-  bool tail, natural;
+  int cp, L, c, r, per;
+  int m, m_hi;  // natural K/V tile, current and last
+  int t;        // ring step of the tile last returned
+  bool natural;
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& q, int knat) {
     cp = sh.cp;
@@ -181,48 +187,28 @@ struct KSeq {
     L = sh.L;
     c = sh.c;
     r = q.rank;
-    qrow = q.row;
-    q0 = knat * kT;
-    int x, hi;
-    query_window(sh, q0, wlo, x);
-    query_window(sh, q0 + kT - 1, x, hi);
-    whi = sh.causal ? q0 - 1 : hi;
     natural = sh.kv_natural != 0;
-    t_end = natural ? cp * per : cp;
+    const int q0 = knat * kT;
+    int lo, hi, x;
+    query_window(sh, q0, lo, x);
+    query_window(sh, q0 + kT - 1, x, hi);
+    m = lo / kT;
+    m_hi = hi >= lo ? hi / kT : -1;
     t = 0;
-    jj = 0;
-    kt = 0;
-    kt_end = -1;
-    tail = sh.causal;
   }
 
-  // kvrow: sharded row of the K/V tile; knat: natural position of its first key.
+  // kvrow: sharded row of the K/V tile (natural row in the all-gather
+  // schedule); knat: natural position of its first key.
   __device__ __forceinline__ bool next(int& kvrow, int& knat) {
-    while (t < t_end) {
-      const int s = natural ? 0 : ring_source(r, t, cp);
-      while (jj < (natural ? 1 : per)) {
-        const int kc = natural ? t : ((per == 1 || jj == 0) ? s : 2 * cp - 1 - s);
-        if (kt_end < 0) tiles_overlapping(kc * c, c, kT, wlo, whi, kt, kt_end);
-        if (kt < kt_end) {
-          knat = kc * c + kt * kT;
-          kvrow = natural ? knat : s * L + jj * c + kt * kT;
-          ++kt;
-          return true;
-        }
-        ++jj;
-        kt = 0;
-        kt_end = -1;
-      }
-      ++t;
-      jj = 0;
-    }
-    if (tail) {
-      kvrow = natural ? q0 : qrow;  // the diagonal tile: the query tile's own tokens
-      knat = q0;
-      tail = false;
-      return true;
-    }
-    return false;
+    if (m > m_hi) return false;
+    knat = m * kT;
+    const int chunk = knat / c;
+    const int s = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
+    const int slot = (per == 1 || chunk < cp) ? 0 : 1;
+    kvrow = natural ? knat : s * L + slot * c + (knat - chunk * c);
+    t = ring_step_of(r, s, cp);
+    ++m;
+    return true;
   }
 };
 
@@ -770,14 +756,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         KSeq seq;
         seq.init(sh, it.q, it.knat);
         int kvrow, knat;
-        // Census: K/V tiles per ring step (the diagonal tile, last in the
-        // walk, arrives at step 0), flushed at each change of step.
+        // Census: K/V tiles per ring step (the diagonal tile arrives at step
+        // 0), flushed at each change of step.
         unsigned long long* census = sh.kv_natural ? nullptr : args.tiles_q_rt;
         int c_step = -1;
         unsigned long long c_n = 0;
         while (ok && seq.next(kvrow, knat)) {
           if (census != nullptr) {
-            const int step = seq.t < seq.t_end ? seq.t : 0;
+            const int step = seq.t;
             if (step != c_step) {
               if (c_n) atomicAdd(&census[it.q.rank * sh.cp + c_step], c_n);
               c_step = step;

@@ -121,89 +121,64 @@ __device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
   return it;
 }
 
-// The K/V tiles an item visits, in ring order (step t brings the shard of
-// rank (r - t) mod cp), with the two diagonal tiles deferred to the end.
-// Query tile i sees the keys [lo[i], hi[i]] (natural positions); a tile is
-// visited when either window meets it.  Under the causal rule the ring walk
-// stops before the item's first row: keys from there on are the diagonal
-// tiles (step 0 only) or the causal future.
+// The K/V tiles an item visits.  Query tile i sees the keys [lo[i], hi[i]]
+// (natural positions); a tile is visited when either window meets it.  The
+// walk takes the tiles in natural order, earliest first, whichever rank
+// holds them: the CTAs in flight hold the query tiles of one kv head and so
+// start on the same K/V tile and read the same K / V tiles at about the same
+// time (one fetch from HBM serves them all through L2); under the causal
+// rule the two diagonal tiles, the item's own rows, come last.  `step` is
+// the ring step at which the tile's rank delivers it, (r - s) mod cp; a call
+// for a range of ring steps [t_begin, t_end) visits only those steps' tiles.
 //
-// All-gather schedule (sh.kv_natural): K/V rows are natural positions and
-// the walk takes the natural chunks in order (t is then the chunk index);
-// `step` still reports the ring step at which the chunk's owner would have
-// delivered it, so the census is the same.
+// All-gather schedule (sh.kv_natural): K/V rows are natural positions, the
+// same order, every step; `step` still reports the ring step at which the
+// chunk's owner would have delivered it, so the census is the same.
 struct KvSeq {
-  int cp, per, L, c, t_end, r, a, qrow;
-  int lo[2], hi[2], wlo, whi;
-  int t, jj, kt, kt_end, tail;
-  bool tail_on, natural;
+  int cp, per, L, c, t_begin, t_end, r, a;
+  int lo[2], hi[2];
+  int m, m_hi;
+  bool natural;
 
-  __device__ __forceinline__ void init(const RingShape& sh, int t_begin, int t_end_,
+  __device__ __forceinline__ void init(const RingShape& sh, int t_begin_, int t_end_,
                                        const Item& it) {
     cp = sh.cp;
     per = sh.per_rank;
     L = sh.L;
     c = sh.c;
+    t_begin = t_begin_;
     t_end = t_end_;
     r = it.r;
     a = it.a;
-    qrow = it.qrow;
     int x;
     for (int i = 0; i < 2; ++i) {
       query_window(sh, (a + i) * kT, lo[i], x);
       query_window(sh, (a + i) * kT + kT - 1, x, hi[i]);
     }
-    wlo = lo[0];
-    whi = sh.causal ? a * kT - 1 : hi[1];
     natural = sh.kv_natural != 0;
-    t = t_begin;
-    if (natural) t_end = cp * per;  // whole ring only
-    jj = 0;
-    kt = 0;
-    kt_end = -1;
-    tail = 0;
-    tail_on = sh.causal && t_begin == 0;
+    m = lo[0] / kT;
+    m_hi = hi[1] >= lo[0] ? hi[1] / kT : -1;
   }
 
   __device__ __forceinline__ int flags(int k0) const {
     return (tile_meets(k0, lo[0], hi[0]) ? kUse0 : 0) | (tile_meets(k0, lo[1], hi[1]) ? kUse1 : 0);
   }
 
-  // kvrow: sharded row of the tile; fl: kUse* flags; step: ring step;
-  // knat: natural position of the tile's first key.
+  // kvrow: sharded row of the tile (natural row in the all-gather schedule);
+  // fl: kUse* flags; step: ring step; knat: natural position of the tile's
+  // first key.
   __device__ __forceinline__ bool next(int& kvrow, int& fl, int& step, int& knat) {
-    while (t < t_end) {
-      // ring: source rank of step t; all-gather: owner of natural chunk t
-      const int s = natural ? ((per == 1 || t < cp) ? t : 2 * cp - 1 - t) : ring_source(r, t, cp);
-      while (jj < (natural ? 1 : per)) {
-        const int kc = natural ? t : ((per == 1 || jj == 0) ? s : 2 * cp - 1 - s);
-        if (kt_end < 0) tiles_overlapping(kc * c, c, kT, wlo, whi, kt, kt_end);
-        while (kt < kt_end) {
-          const int k0 = kc * c + kt * kT;
-          kvrow = natural ? k0 : s * L + jj * c + kt * kT;
-          ++kt;
-          fl = flags(k0);
-          if (fl == 0) continue;
-          step = natural ? ring_step_of(r, s, cp) : t;
-          knat = k0;
-          return true;
-        }
-        ++jj;
-        kt = 0;
-        kt_end = -1;
-      }
-      ++t;
-      jj = 0;
-    }
-    while (tail_on && tail < 2) {
-      // The diagonal tiles are the item's own rows; tile a + 1 is in the
-      // future of query tile 0.
-      const int k0 = (a + tail) * kT;
-      kvrow = natural ? k0 : qrow + tail * kT;
-      fl = flags(k0) & (tail == 0 ? (kUse0 | kUse1) : kUse1);
-      ++tail;
+    while (m <= m_hi) {
+      const int k0 = m * kT;
+      ++m;
+      fl = flags(k0);
       if (fl == 0) continue;
-      step = 0;
+      const int chunk = k0 / c;
+      const int s = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
+      step = ring_step_of(r, s, cp);
+      if (!natural && (step < t_begin || step >= t_end)) continue;
+      const int slot = (per == 1 || chunk < cp) ? 0 : 1;
+      kvrow = natural ? k0 : s * L + slot * c + (k0 - chunk * c);
       knat = k0;
       return true;
     }

@@ -8,7 +8,9 @@ document path), and, for some, packed documents with random lengths.  The
 bars are those of the other parity files (float32 O <= 1e-4, LSE <= 1e-5,
 gradients <= 1e-4; bf16 O <= 2e-2, LSE <= 1e-3, float32 gradients
 <= 2e-2).  The draw is fixed by the case number, so a failure names a
-reproducible problem.
+reproducible problem.  The draws with plain lengths also go through the
+hierarchical a2a+p2p schedule (when the ring splits into two levels) and the
+one-pass backward (when the tensor-core backward takes them).
 """
 import numpy as np
 import pytest
@@ -94,4 +96,54 @@ def test_random_case_matches_oracle(i):
     assert maxerr(lse, rl) <= tol["lse"], ("lse", maxerr(lse, rl))
     for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), rg):
         assert maxerr(got, ref) <= tol["grad"], (name, maxerr(got, ref))
+    assert cpa.device_status() == 0
+
+
+def hier_split(c):
+    """A two-level split [A, P] of the case's ring (A > 1, P > 1) whose head
+    slices divide the kv groups (or the reverse), or None."""
+    H, Hkv, cp = c["H"], c["Hkv"], c["cp"]
+    for A in (2, 4):
+        if cp % A or cp // A < 2 or H % A:
+            continue
+        hc, grp = H // A, H // Hkv
+        if hc % grp == 0 or grp % hc == 0:
+            return A, cp // A
+    return None
+
+
+@pytest.mark.parametrize("i", range(N_CASES), ids=case_id)
+def test_random_case_other_routes(i):
+    # The same draw through the hierarchical a2a+p2p schedule (when the ring
+    # splits in two levels) and through the one-pass backward (when the
+    # tensor-core backward takes the case), against the same oracle values.
+    c = draw(i)
+    if c["padded"] or c["cu"] is not None:
+        pytest.skip("plain sequence lengths only")
+    split = hier_split(c)
+    onepass = (c["dtype"] == torch.bfloat16 and c["D"] == 128 and
+               cpa.plan(c["B"], c["H"], c["Hkv"], c["S"], c["D"], c["cp"], c["layout"],
+                        c["causal"], c["dtype"], backward=True)[0] == cpa.PATH_TCGEN05)
+    if split is None and not onepass:
+        pytest.skip("no second route for this draw")
+    w = inputs.Workload("sweep", c["B"], c["H"], c["Hkv"], c["S"], c["D"], c["cp"], c["layout"],
+                        c["causal"], c["dtype"], seed=c["seed"])
+    q, k, v, do = inputs.generate(w, with_dout=True)
+    dev = [x.to(DEV) for x in (q, k, v, do)]
+    f = [inputs.to_f32_numpy(x) for x in (q, k, v, do)]
+    ro, rl = oracle.attn_fwd(f[0], f[1], f[2], causal=c["causal"])
+    rg = oracle.attn_bwd(*f, causal=c["causal"])
+    tol = TOL[c["dtype"]]
+    routes = []
+    if split is not None:
+        routes.append(cpa.attention_hier_fwd_bwd(*dev, split[0], split[1], c["layout"],
+                                                 c["causal"], grad_dtype=torch.float32))
+    if onepass:
+        routes.append(cpa.attention_fwd_bwd(*dev, c["cp"], c["layout"], c["causal"],
+                                            grad_dtype=torch.float32, onepass=True))
+    for out, lse, dq, dk, dv in routes:
+        assert maxerr(out, ro) <= tol["o"], ("out", maxerr(out, ro))
+        assert maxerr(lse, rl) <= tol["lse"], ("lse", maxerr(lse, rl))
+        for name, got, ref in zip(("dq", "dk", "dv"), (dq, dk, dv), rg):
+            assert maxerr(got, ref) <= tol["grad"], (name, maxerr(got, ref))
     assert cpa.device_status() == 0
