@@ -1,7 +1,8 @@
 """Builds and runs the microbenchmarks on GPU 0: the tcgen05.mma rate with one
 CTA per SM and cta_group::1 (mma_rate.cu), with CTA pairs and cta_group::2
-(mma_rate_pair.cu), and the bulk float32 reduction rate (reduce_rate.cu).
-``--pair``, ``--single`` or ``--reduce`` runs only that one."""
+(mma_rate_pair.cu), the bulk float32 reduction rate (reduce_rate.cu) and the
+rate of bulk copies from L2 into shared memory (load_rate.cu).  ``--pair``,
+``--single``, ``--reduce`` or ``--load`` runs only that one."""
 import os
 import subprocess
 import sys
@@ -24,13 +25,15 @@ def run(src):
 
 
 def main():
-    srcs = ["mma_rate.cu", "mma_rate_pair.cu", "reduce_rate.cu"]
+    srcs = ["mma_rate.cu", "mma_rate_pair.cu", "reduce_rate.cu", "load_rate.cu"]
     if "--pair" in sys.argv:
         srcs = ["mma_rate_pair.cu"]
     elif "--single" in sys.argv:
         srcs = ["mma_rate.cu"]
     elif "--reduce" in sys.argv:
         srcs = ["reduce_rate.cu"]
+    elif "--load" in sys.argv:
+        srcs = ["load_rate.cu"]
     rc = 0
     for s in srcs:
         rc |= run(s)
