@@ -34,9 +34,9 @@
 // dq kernel (query-major).  Work item: one 128-row query tile of one head.
 // Q, dO stay in shared memory, LSE / Delta in registers (TMEM lane = query
 // row); the K/V tiles it sees (earliest first, see KSeq) stream past through
-// a ring of five 32 KB slots (K(j), V(j), K(j+1), ... in consecutive slots;
-// V(j)'s slot is free once dP(j) has read it, K(j)'s once dQ(j) has, so
-// loads run up to two tiles ahead):
+// two rings of 32 KB slots, three for K and two for V (V(j)'s slot is free
+// once dP(j) has read it, K(j)'s only once dQ(j) has, a tile later; a ring
+// each keeps the copy of V(j+2) from waiting for dQ(j)):
 //   S = Q K^T -> TMEM [0,128)     dP = dO V^T -> TMEM [128,256) / [256,384)
 //   dS = scale * exp2(S*scale*log2e - LSE*log2e) (dP - Delta) -> bf16 over dP
 //   dQ += dS K  (TS, K read MN-major) -> TMEM [384,512)
@@ -638,16 +638,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ===========================================================================
 namespace qm {
 
-constexpr int kSlots = 5;  // K/V ring: K(j), V(j) take consecutive slots
+// K and V tiles in rings of their own: V(j) is free once dP(j) has read it,
+// K(j) only once dQ(j) has, which comes a tile later; with a ring each, V's
+// copies are never held up behind K's release.
+constexpr int kKSlots = 3;  // K(j) in slot j % 3
+constexpr int kVSlots = 2;  // V(j) in slot j % 2
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kOffQ + kTileBytes;
-constexpr int kOffRing = kOffDO + kTileBytes;  // [kSlots]
-constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
+constexpr int kOffRing = kOffDO + kTileBytes;  // [kKSlots] K, then [kVSlots] V
+constexpr int kOffBar = kOffRing + (kKSlots + kVSlots) * kTileBytes;
 constexpr int kBarQFull = 0;
 constexpr int kBarQEmpty = 1;
-constexpr int kBarFull = 2;                    // [kSlots]
-constexpr int kBarEmpty = kBarFull + kSlots;   // [kSlots]
-constexpr int kBarS = kBarEmpty + kSlots;
+constexpr int kBarKFull = 2;                      // [kKSlots]
+constexpr int kBarKEmpty = kBarKFull + kKSlots;   // [kKSlots]
+constexpr int kBarVFull = kBarKEmpty + kKSlots;   // [kVSlots]
+constexpr int kBarVEmpty = kBarVFull + kVSlots;   // [kVSlots]
+constexpr int kBarS = kBarVEmpty + kVSlots;
 constexpr int kBarSFree = kBarS + 1;
 constexpr int kBarDP = kBarSFree + 1;          // [2]
 constexpr int kBarDS = kBarDP + 2;
@@ -693,7 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
   const uint32_t sQ = base + kOffQ, sDO = base + kOffDO, sRing = base + kOffRing;
-  auto slot = [&](uint32_t n) { return sRing + (n % kSlots) * kTileBytes; };
+  auto kslot = [&](uint32_t j) { return sRing + (j % kKSlots) * kTileBytes; };
+  auto vslot = [&](uint32_t j) { return sRing + (kKSlots + j % kVSlots) * kTileBytes; };
   const uint32_t bars = base + kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -706,9 +713,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(bar(kBarFull + i), 1);
-      mbar_init(bar(kBarEmpty + i), 1);
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(bar(kBarKFull + i), 1);
+      mbar_init(bar(kBarKEmpty + i), 1);
+    }
+    for (int i = 0; i < kVSlots; ++i) {
+      mbar_init(bar(kBarVFull + i), 1);
+      mbar_init(bar(kBarVEmpty + i), 1);
     }
     for (int i = 0; i < 2; ++i) mbar_init(bar(kBarDP + i), 1);
     mbar_init(bar(kBarS), 1);
@@ -736,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      uint32_t seq_n = 0, q_armed = 0, armed[kSlots] = {0};
+      uint32_t tj = 0, q_armed = 0, k_armed[kKSlots] = {0}, v_armed[kVSlots] = {0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -772,53 +783,65 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++c_n;
           }
           const int krow = it.b * sh.S + kvrow;
-          for (int which = 0; which < 2; ++which) {  // K(j), then V(j)
-            const uint32_t n = seq_n++;
-            const int sl = n % kSlots;
-            if (!mbar_wait(bar(kBarEmpty + sl), ((n / kSlots) & 1) ^ 1, wc)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(bar(kBarFull + sl), kTileBytes);
-            ++armed[sl];
-            for (int half = 0; half < 2; ++half)
-              tma_load_3d(slot(n) + half * kBoxBytes, which == 0 ? &tm_k : &tm_v,
-                          bar(kBarFull + sl), half * 64, it.g, krow);
+          const uint32_t j = tj++;
+          const int ks = j % kKSlots, vs = j % kVSlots;
+          if (!mbar_wait(bar(kBarKEmpty + ks), ((j / kKSlots) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(bar(kBarKFull + ks), kTileBytes);
+          ++k_armed[ks];
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(kslot(j) + half * kBoxBytes, &tm_k, bar(kBarKFull + ks), half * 64, it.g,
+                        krow);
+          if (!mbar_wait(bar(kBarVEmpty + vs), ((j / kVSlots) & 1) ^ 1, wc)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kBarVFull + vs), kTileBytes);
+          ++v_armed[vs];
+          for (int half = 0; half < 2; ++half)
+            tma_load_3d(vslot(j) + half * kBoxBytes, &tm_v, bar(kBarVFull + vs), half * 64, it.g,
+                        krow);
         }
         if (census != nullptr && c_n) atomicAdd(&census[it.q.rank * sh.cp + c_step], c_n);
       }
       if (!ok) {
         if (q_armed) mbar_drain(bar(kBarQFull), (q_armed - 1) & 1);
-        for (int s = 0; s < kSlots; ++s)
-          if (armed[s]) mbar_drain(bar(kBarFull + s), (armed[s] - 1) & 1);
+        for (int s = 0; s < kKSlots; ++s)
+          if (k_armed[s]) mbar_drain(bar(kBarKFull + s), (k_armed[s] - 1) & 1);
+        for (int s = 0; s < kVSlots; ++s)
+          if (v_armed[s]) mbar_drain(bar(kBarVFull + s), (v_armed[s] - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
-      // Tile j's K is ring entry 2j, its V entry 2j + 1.
+      // kj counts the K/V tiles this CTA has consumed.
       uint32_t kj = 0, sf_ph = 0, ds_ph = 0;
       bool ok = true;
-      auto wait_full = [&](uint32_t n) {
-        return mbar_wait(bar(kBarFull + n % kSlots), (n / kSlots) & 1, wc);
+      auto wait_k = [&](uint32_t j) {
+        return mbar_wait(bar(kBarKFull + j % kKSlots), (j / kKSlots) & 1, wc);
       };
-      auto issue_s = [&](uint32_t kn) {
+      auto wait_v = [&](uint32_t j) {
+        return mbar_wait(bar(kBarVFull + j % kVSlots), (j / kVSlots) & 1, wc);
+      };
+      auto issue_s = [&](uint32_t j) {
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
           mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024),
-                 sdesc_sw128(slot(kn) + off, 16, 1024), kIdescKK, kk > 0);
+                 sdesc_sw128(kslot(j) + off, 16, 1024), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarS));
       };
-      auto issue_dp = [&](uint32_t vn, int buf) {
+      auto issue_dp = [&](uint32_t j, int buf) {
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
           mma_ss(tmem + col_dp(buf), sdesc_sw128(sDO + off, 16, 1024),
-                 sdesc_sw128(slot(vn) + off, 16, 1024), kIdescKK, kk > 0);
+                 sdesc_sw128(vslot(j) + off, 16, 1024), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarDP + buf));
-        mma_commit(bar(kBarEmpty + vn % kSlots));  // V is read only by dP
+        mma_commit(bar(kBarVEmpty + j % kVSlots));  // V is read only by dP
       };
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -834,25 +857,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kvrow, knat;
         bool have = seq.next(kvrow, knat);
         if (have) {
-          if (!wait_full(2 * kj)) {
+          if (!wait_k(kj)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(2 * kj);
-          if (!wait_full(2 * kj + 1)) {
+          issue_s(kj);
+          if (!wait_v(kj)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_dp(2 * kj + 1, kj & 1);
+          issue_dp(kj, kj & 1);
         }
         bool first = true;
         while (have) {
           int nkvrow, nknat;
           const bool nhave = seq.next(nkvrow, nknat);
           if (nhave) {
-            if (!wait_full(2 * kj + 2)) {
+            if (!wait_k(kj + 1)) {
               ok = false;
               break;
             }
@@ -863,15 +886,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             sf_ph ^= 1;
             tc_fence_after();
-            issue_s(2 * kj + 2);
+            issue_s(kj + 1);
             // dP into the other buffer: the dQ that read it two tiles ago was
             // issued earlier, and MMAs execute in issue order.
-            if (!wait_full(2 * kj + 3)) {
+            if (!wait_v(kj + 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            issue_dp(2 * kj + 3, (kj + 1) & 1);
+            issue_dp(kj + 1, (kj + 1) & 1);
           }
           // dQ += dS K
           if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
@@ -886,9 +909,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           for (int kk = 0; kk < kT / 16; ++kk)
             mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
-                   sdesc_sw128(slot(2 * kj) + kk * 2048, kBoxBytes, 1024), kIdescKM,
+                   sdesc_sw128(kslot(kj) + kk * 2048, kBoxBytes, 1024), kIdescKM,
                    (!first || kk > 0) ? 1u : 0u);
-          mma_commit(bar(kBarEmpty + (2 * kj) % kSlots));  // K is free after dQ
+          mma_commit(bar(kBarKEmpty + kj % kKSlots));  // K is free after dQ
           first = false;
           ++kj;
           have = nhave;
