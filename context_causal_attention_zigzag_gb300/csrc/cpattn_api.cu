@@ -61,6 +61,8 @@ int make_shape(int B, int H, int Hkv, int S, int D, int cp, int layout, int caus
   sh->scale_log2 = sh->scale * 1.4426950408889634f;
   sh->docs = nullptr;
   sh->kv_natural = 0;
+  const unsigned long long tpc = (unsigned long long)(sh->c / kTcTile);
+  sh->tile_magic = (sh->c > 0 && sh->c % kTcTile == 0) ? ((1ull << 32) + tpc - 1) / tpc : 0;
   return CPATTN_OK;
 }
 
@@ -83,12 +85,15 @@ bool device_is_sm103() {
 }
 
 // Tensor-core forward: bf16, D = 128, every chunk a whole number of 256-row
-// query pairs (two 128-row tiles share each K/V tile).
+// query pairs (two 128-row tiles share each K/V tile).  Both tensor-core
+// paths take S < 2^23 (their tile walks find a tile's chunk with a multiply
+// by RingShape::tile_magic, exact below that).
+constexpr int kTcMaxS = 1 << 23;
 bool tc_fwd_eligible(const RingShape& sh, int dtype) {
-  return dtype == CPATTN_BF16 && sh.D == 128 && sh.c % (2 * kTcTile) == 0;
+  return dtype == CPATTN_BF16 && sh.D == 128 && sh.c % (2 * kTcTile) == 0 && sh.S < kTcMaxS;
 }
 bool tc_bwd_eligible(const RingShape& sh, int dtype) {
-  return dtype == CPATTN_BF16 && sh.D == 128 && sh.c % kTcTile == 0;
+  return dtype == CPATTN_BF16 && sh.D == 128 && sh.c % kTcTile == 0 && sh.S < kTcMaxS;
 }
 
 int fwd_common(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,

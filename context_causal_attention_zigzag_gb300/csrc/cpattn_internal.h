@@ -40,6 +40,8 @@ struct RingShape {
   // dV) in natural order and walks it chunk by chunk in natural order
   // ("Context Parallelism in MegaDLMs", key-value communication patterns).
   int kv_natural;
+  // ceil(2^32 / (c / 128)) when 128 divides c (else 0), for chunk_of_tile.
+  unsigned long long tile_magic;
 };
 
 // Rank owning natural chunk kc, and the chunk's slot in that rank's shard.
@@ -56,14 +58,23 @@ __host__ __device__ inline int sharded_pos(const RingShape& s, int n) {
   return chunk_owner(s, kc) * s.L + chunk_slot(s, kc) * s.c + off;
 }
 
-// Ring step at which rank r holds the K/V of rank src.
+// Ring step at which rank r holds the K/V of rank src (r, src in [0, cp)).
 __host__ __device__ inline int ring_step_of(int r, int src, int cp) {
 #if CPATTN_MUTATION == 2
-  int t = (src - r) % cp;  // planted: the ring turned the other way
+  const int t = src - r;  // planted: the ring turned the other way
 #else
-  int t = (r - src) % cp;
+  const int t = r - src;
 #endif
   return t < 0 ? t + cp : t;
+}
+
+// Natural chunk of the tile with natural index m (tiles of 128 tokens):
+// m / (c / 128) as (m * tile_magic) >> 32 with tile_magic = ceil(2^32 / (c /
+// 128)) (RingShape::tile_magic), so that a step of a tile walk divides
+// nothing.  Exact while m * (c / 128) < 2^32 (the tensor-core paths take
+// S < 2^23, where both factors are below 2^16).
+__host__ __device__ inline int chunk_of_tile(int m, unsigned long long tile_magic) {
+  return (int)(((unsigned long long)(unsigned)m * tile_magic) >> 32);
 }
 
 // Keys visible to the query at natural position i: the natural range [lo, hi].

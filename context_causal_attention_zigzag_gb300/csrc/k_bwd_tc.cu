@@ -136,6 +136,7 @@ struct QSeq {
   int cp, L, c, s, per;
   int m, m_lo;  // natural query tile, current and lowest
   int t;        // ring step of the tile last returned
+  unsigned long long magic;  // RingShape::tile_magic, for chunk_of_tile
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& kv, int knat) {
     cp = sh.cp;
@@ -149,13 +150,14 @@ struct QSeq {
     m = hi >= lo ? hi / kT : -1;
     m_lo = lo / kT;
     t = 0;
+    magic = sh.tile_magic;
   }
 
   // qrow: sharded row of the query tile; qnat: natural position of its first row.
   __device__ __forceinline__ bool next(int& qrow, int& qnat) {
     if (m < m_lo) return false;
     qnat = m * kT;
-    const int chunk = qnat / c;
+    const int chunk = chunk_of_tile(m, magic);
     const int r = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
     const int slot = (per == 1 || chunk < cp) ? 0 : 1;
     qrow = r * L + slot * c + (qnat - chunk * c);
@@ -180,6 +182,7 @@ struct KSeq {
   int m, m_hi;  // natural K/V tile, current and last
   int t;        // ring step of the tile last returned
   bool natural;
+  unsigned long long magic;  // RingShape::tile_magic, for chunk_of_tile
 
   __device__ __forceinline__ void init(const RingShape& sh, const TilePos& q, int knat) {
     cp = sh.cp;
@@ -195,6 +198,7 @@ struct KSeq {
     m = lo / kT;
     m_hi = hi >= lo ? hi / kT : -1;
     t = 0;
+    magic = sh.tile_magic;
   }
 
   // kvrow: sharded row of the K/V tile (natural row in the all-gather
@@ -202,7 +206,7 @@ struct KSeq {
   __device__ __forceinline__ bool next(int& kvrow, int& knat) {
     if (m > m_hi) return false;
     knat = m * kT;
-    const int chunk = knat / c;
+    const int chunk = chunk_of_tile(m, magic);
     const int s = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
     const int slot = (per == 1 || chunk < cp) ? 0 : 1;
     kvrow = natural ? knat : s * L + slot * c + (knat - chunk * c);

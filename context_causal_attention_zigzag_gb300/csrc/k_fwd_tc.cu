@@ -139,6 +139,7 @@ struct KvSeq {
   int lo[2], hi[2];
   int m, m_hi;
   bool natural;
+  unsigned long long magic;  // RingShape::tile_magic, for chunk_of_tile
 
   __device__ __forceinline__ void init(const RingShape& sh, int t_begin_, int t_end_,
                                        const Item& it) {
@@ -158,6 +159,7 @@ struct KvSeq {
     natural = sh.kv_natural != 0;
     m = lo[0] / kT;
     m_hi = hi[1] >= lo[0] ? hi[1] / kT : -1;
+    magic = sh.tile_magic;
   }
 
   __device__ __forceinline__ int flags(int k0) const {
@@ -170,10 +172,10 @@ struct KvSeq {
   __device__ __forceinline__ bool next(int& kvrow, int& fl, int& step, int& knat) {
     while (m <= m_hi) {
       const int k0 = m * kT;
+      const int chunk = chunk_of_tile(m, magic);
       ++m;
       fl = flags(k0);
       if (fl == 0) continue;
-      const int chunk = k0 / c;
       const int s = (per == 1 || chunk < cp) ? chunk : 2 * cp - 1 - chunk;
       step = ring_step_of(r, s, cp);
       if (!natural && (step < t_begin || step >= t_end)) continue;

@@ -156,7 +156,11 @@ CPATTN_API int cpattn_ring_fwd_census(const void* q, const void* k, const void* 
 /*
  * Which kernel cpattn_ring_fwd / cpattn_ring_bwd would run for these
  * arguments (host only, no GPU work): *path is a cpattn_path, *tile the tile
- * edge in tokens.  Either output pointer may be NULL.
+ * edge in tokens.  Either output pointer may be NULL.  The tensor-core path
+ * takes bf16 inputs, D = 128, S < 2^23 and chunks (S / (2 cp_size) tokens
+ * zigzag, S / cp_size contiguous) of whole 128-token tiles, whole 256-token
+ * pairs of them for the forward, on an sm_103 device; everything else runs
+ * on CUDA cores.
  */
 CPATTN_API int cpattn_ring_fwd_plan(int B, int H, int Hkv, int S, int D, int cp_size, int layout,
                          int causal, int dtype, int* path, int* tile);
