@@ -389,19 +389,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t qi = 0, p_ph = 0, ds_ph = 0;
       bool ok = true;
+      // Operand descriptors, computed once and advanced by byte offsets.
+      const uint64_t d_k = sdesc_sw128(sK, 16, 1024), d_v = sdesc_sw128(sV, 16, 1024);
+      const uint64_t d_q = sdesc_sw128(sQ, 16, 1024), d_do = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t d_q_mn = sdesc_sw128(sQ, kBoxBytes, 1024);
+      const uint64_t d_do_mn = sdesc_sw128(sDO, kBoxBytes, 1024);
       auto issue_s = [&](int st) {
+        const uint64_t b0 = sdesc_advance(d_q, st * kTileBytes);
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(sK + off, 16, 1024),
-                 sdesc_sw128(sQ + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+          mma_ss(tmem + kColS, sdesc_advance(d_k, off), sdesc_advance(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarS));
       };
       auto issue_dp = [&](int st) {
+        const uint64_t b0 = sdesc_advance(d_do, st * kTileBytes);
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColDP, sdesc_sw128(sV + off, 16, 1024),
-                 sdesc_sw128(sDO + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+          mma_ss(tmem + kColDP, sdesc_advance(d_v, off), sdesc_advance(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarDP));
       };
@@ -445,10 +452,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDV, tmem + kColS + a_col(kk),
-                   sdesc_sw128(sDO + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                   (!first || kk > 0) ? 1u : 0u);
+          {
+            const uint64_t b0 = sdesc_advance(d_do_mn, st * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ts(tmem + kColDV, tmem + kColS + a_col(kk), sdesc_advance(b0, kk * 2048),
+                     kIdescKM, (!first || kk > 0) ? 1u : 0u);
+          }
           // S for the next tile (the S^T columns are free once dV has read P^T;
           // MMAs execute in issue order).
           if (nhave) {
@@ -466,10 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ds_ph ^= 1;
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDK, tmem + kColDP + a_col(kk),
-                   sdesc_sw128(sQ + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                   (!first || kk > 0) ? 1u : 0u);
+          {
+            const uint64_t b0 = sdesc_advance(d_q_mn, st * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ts(tmem + kColDK, tmem + kColDP + a_col(kk), sdesc_advance(b0, kk * 2048),
+                     kIdescKM, (!first || kk > 0) ? 1u : 0u);
+          }
           mma_commit(bar(kBarQEmpty + st));
           // dP for the next tile (the dP^T columns are free once dK has read dS^T).
           if (nhave) issue_dp(nst);
@@ -830,19 +843,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_v = [&](uint32_t j) {
         return mbar_wait(bar(kBarVFull + j % kVSlots), (j / kVSlots) & 1, wc);
       };
+      // Operand descriptors, computed once and advanced by byte offsets.
+      const uint64_t d_q = sdesc_sw128(sQ, 16, 1024), d_do = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t d_ring = sdesc_sw128(sRing, 16, 1024);
+      const uint64_t d_ring_mn = sdesc_sw128(sRing, kBoxBytes, 1024);
+      auto koff = [](uint32_t j) { return (j % kKSlots) * (uint32_t)kTileBytes; };
+      auto voff = [](uint32_t j) { return (kKSlots + j % kVSlots) * (uint32_t)kTileBytes; };
       auto issue_s = [&](uint32_t j) {
+        const uint64_t b0 = sdesc_advance(d_ring, koff(j));
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(sQ + off, 16, 1024),
-                 sdesc_sw128(kslot(j) + off, 16, 1024), kIdescKK, kk > 0);
+          mma_ss(tmem + kColS, sdesc_advance(d_q, off), sdesc_advance(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarS));
       };
       auto issue_dp = [&](uint32_t j, int buf) {
+        const uint64_t b0 = sdesc_advance(d_ring, voff(j));
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + col_dp(buf), sdesc_sw128(sDO + off, 16, 1024),
-                 sdesc_sw128(vslot(j) + off, 16, 1024), kIdescKK, kk > 0);
+          mma_ss(tmem + col_dp(buf), sdesc_advance(d_do, off), sdesc_advance(b0, off), kIdescKK,
+                 kk > 0);
         }
         mma_commit(bar(kBarDP + buf));
         mma_commit(bar(kBarVEmpty + j % kVSlots));  // V is read only by dP
@@ -911,10 +933,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
-                   sdesc_sw128(kslot(kj) + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                   (!first || kk > 0) ? 1u : 0u);
+          {
+            const uint64_t b0 = sdesc_advance(d_ring_mn, koff(kj));
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
+                     sdesc_advance(b0, kk * 2048), kIdescKM, (!first || kk > 0) ? 1u : 0u);
+          }
           mma_commit(bar(kBarKEmpty + kj % kKSlots));  // K is free after dQ
           first = false;
           ++kj;

@@ -291,6 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t kv_it = 0, p_ph[2] = {0, 0};
       bool ok = true;
+      // Operand descriptors, computed once and advanced by byte offsets: Q
+      // tile 0, ring slot 0 read K-major (K for S) and MN-major (V for P V).
+      const uint64_t d_q = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t d_k = sdesc_sw128(sRing, 16, 1024);
+      const uint64_t d_v = sdesc_sw128(sRing, kBoxBytes, 1024);
+      auto slot_off = [](uint32_t n) { return (n % kSlots) * (uint32_t)kTileBytes; };
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
@@ -319,10 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         for (int i = 0; i < 2; ++i) {
           if (!(fl & (kUse0 << i))) continue;
+          const uint64_t a0 = sdesc_advance(d_q, i * kTileBytes);
+          const uint64_t b0 = sdesc_advance(d_k, slot_off(kn));
+#pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + col_s(i), sdesc_sw128(sQ + i * kTileBytes + off, 16, 1024),
-                   sdesc_sw128(slot(kn) + off, 16, 1024), kIdescQK, kk > 0);
+            mma_ss(tmem + col_s(i), sdesc_advance(a0, off), sdesc_advance(b0, off), kIdescQK,
+                   kk > 0);
           }
           mma_commit(bar(kBarS + i));
         }
@@ -346,10 +355,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               p_ph[i] ^= 1;
               tc_fence_after();
+              const uint64_t bv = sdesc_advance(d_v, slot_off(vn));
+#pragma unroll
               for (int kk = 0; kk < kT / 16; ++kk)
-                mma_ts(tmem + col_o(i), tmem + col_s(i) + kk * 8,
-                       sdesc_sw128(slot(vn) + kk * 2048, kBoxBytes, 1024), kIdescPV,
-                       acc[i] | (kk > 0));
+                mma_ts(tmem + col_o(i), tmem + col_s(i) + kk * 8, sdesc_advance(bv, kk * 2048),
+                       kIdescPV, acc[i] | (kk > 0));
               acc[i] = 1;
             }
             if (have_next && (nfl & (kUse0 << i))) {
@@ -361,10 +371,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 k_ready = true;
               }
+              const uint64_t a0 = sdesc_advance(d_q, i * kTileBytes);
+              const uint64_t b0 = sdesc_advance(d_k, slot_off(nkn));
+#pragma unroll
               for (int kk = 0; kk < kD / 16; ++kk) {
                 const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                mma_ss(tmem + col_s(i), sdesc_sw128(sQ + i * kTileBytes + off, 16, 1024),
-                       sdesc_sw128(slot(nkn) + off, 16, 1024), kIdescQK, kk > 0);
+                mma_ss(tmem + col_s(i), sdesc_advance(a0, off), sdesc_advance(b0, off), kIdescQK,
+                       kk > 0);
               }
               mma_commit(bar(kBarS + i));
             }

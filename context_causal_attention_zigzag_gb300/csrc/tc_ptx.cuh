@@ -240,6 +240,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The descriptor of the operand `bytes` further on in shared memory (a
+// multiple of 16): the start-address field holds address / 16 in its low 14
+// bits, and shared-memory addresses stay below 2^18, so the add never
+// carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, M x N.
 // a_mn / b_mn: operand is MN-major (output dim contiguous) instead of K-major.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
