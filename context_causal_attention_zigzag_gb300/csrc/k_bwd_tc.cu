@@ -70,6 +70,7 @@ constexpr int kD = 128;
 constexpr int kBoxBytes = kT * 64 * 2;     // 16 KB
 constexpr int kTileBytes = 2 * kBoxBytes;  // 32 KB
 constexpr int kThreads = 384;
+constexpr int kPrefetchAhead = 4;  // tiles asked of L2 ahead of their loads
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kIdescKK = idesc_bf16(128, 128, false, false);  // both K-major
@@ -340,6 +341,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         QSeq seq;
         seq.init(sh, it.kv, it.knat);
+        // A second walker kPrefetchAhead tiles ahead asks L2 for the Q / dO
+        // tiles before their loads are issued.
+        QSeq pseq = seq;
+        auto prefetch_next = [&]() {
+          int prow, pnat;
+          if (!pseq.next(prow, pnat)) return;
+          const int row = it.b * sh.S + prow;
+          for (int half = 0; half < 2; ++half) {
+            tma_prefetch_l2_3d(&tm_q, half * 64, it.h, row);
+            tma_prefetch_l2_3d(&tm_do, half * 64, it.h, row);
+          }
+        };
+        for (int i = 0; i < kPrefetchAhead; ++i) prefetch_next();
         int qrow, qnat;
         // Census: query tiles per (receiving rank, ring step), flushed at
         // each change of step.
@@ -347,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c_step = -1;
         unsigned long long c_n = 0;
         while (seq.next(qrow, qnat)) {
+          prefetch_next();
           if (census != nullptr) {
             if (seq.t != c_step) {
               if (c_n) atomicAdd(&census[((it.kv.rank + c_step) % sh.cp) * sh.cp + c_step], c_n);
@@ -783,6 +798,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         KSeq seq;
         seq.init(sh, it.q, it.knat);
+        // A second walker kPrefetchAhead tiles ahead asks L2 for the K / V
+        // tiles before their loads are issued.
+        KSeq pseq = seq;
+        auto prefetch_next = [&]() {
+          int prow, pnat;
+          if (!pseq.next(prow, pnat)) return;
+          const int row = it.b * sh.S + prow;
+          for (int half = 0; half < 2; ++half) {
+            tma_prefetch_l2_3d(&tm_k, half * 64, it.g, row);
+            tma_prefetch_l2_3d(&tm_v, half * 64, it.g, row);
+          }
+        };
+        for (int i = 0; i < kPrefetchAhead; ++i) prefetch_next();
         int kvrow, knat;
         // Census: K/V tiles per ring step (the diagonal tile arrives at step
         // 0), flushed at each change of step.
@@ -790,6 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int c_step = -1;
         unsigned long long c_n = 0;
         while (ok && seq.next(kvrow, knat)) {
+          prefetch_next();
           if (census != nullptr) {
             const int step = seq.t;
             if (step != c_step) {
