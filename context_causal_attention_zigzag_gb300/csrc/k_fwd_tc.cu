@@ -21,7 +21,8 @@
 //               ring of five 32 KB slots (K(j), V(j), K(j+1), ... take
 //               consecutive slots; a slot is freed as soon as the MMAs that
 //               read it retire, so loads run up to two tiles ahead).
-//   warp 1      TMEM owner and MMA issuer (one thread):
+//   warp 1      TMEM owner and MMA issuer (the warp runs the control flow,
+//               one elected lane issues):
 //               S_i = Q_i K^T  (SS form, 128x128x128, fp32 in TMEM),
 //               O_i += P_i V   (TS form: P read from TMEM, V MN-major).
 //   warps 4-7   softmax of query tile 0, warps 8-11 of tile 1: one thread
@@ -288,7 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the control flow (its values stay warp-uniform);
+    // one elected lane issues the MMAs and commits.
+    {
+      const bool leader = elect_one();
+      // A wait that the whole warp agrees on, so its control flow stays uniform.
+      auto wwait = [&](uint32_t bar_addr, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
+      };
       uint32_t kv_it = 0, p_ph[2] = {0, 0};
       bool ok = true;
       // Operand descriptors, computed once and advanced by byte offsets: Q
@@ -301,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
         const Item it = decode_item(sh, idx);
-        if (!mbar_wait(bar(kBarQFull), k & 1, wc)) {
+        if (!wwait(bar(kBarQFull), k & 1)) {
           ok = false;
           break;
         }
@@ -311,14 +319,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         int kvrow, fl, step, knat;
         bool have = seq.next(kvrow, fl, step, knat);
         if (!have) {
-          mma_commit(bar(kBarQEmpty));
+          if (leader) mma_commit(bar(kBarQEmpty));
           continue;
         }
         unsigned long long census = 0;
         int census_step = step;
         // S for the first tile: K(j) is ring entry 2*kv_it, V(j) entry 2*kv_it + 1.
         uint32_t kn = 2 * kv_it;
-        if (!mbar_wait(bar(kBarFull + kn % kSlots), (kn / kSlots) & 1, wc)) {
+        if (!wwait(bar(kBarFull + kn % kSlots), (kn / kSlots) & 1)) {
           ok = false;
           break;
         }
@@ -327,21 +335,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(fl & (kUse0 << i))) continue;
           const uint64_t a0 = sdesc_advance(d_q, i * kTileBytes);
           const uint64_t b0 = sdesc_advance(d_k, slot_off(kn));
+          if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + col_s(i), sdesc_advance(a0, off), sdesc_advance(b0, off), kIdescQK,
-                   kk > 0);
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+              mma_ss(tmem + col_s(i), sdesc_advance(a0, off), sdesc_advance(b0, off), kIdescQK,
+                     kk > 0);
+            }
+            mma_commit(bar(kBarS + i));
           }
-          mma_commit(bar(kBarS + i));
         }
-        mma_commit(bar(kBarEmpty + kn % kSlots));
+        if (leader) mma_commit(bar(kBarEmpty + kn % kSlots));
         uint32_t acc[2] = {0, 0};
         while (true) {
           int nkvrow, nfl = 0, nstep = 0, nknat;
           const bool have_next = seq.next(nkvrow, nfl, nstep, nknat);
           const uint32_t vn = 2 * kv_it + 1, nkn = 2 * kv_it + 2;
-          if (!mbar_wait(bar(kBarFull + vn % kSlots), (vn / kSlots) & 1, wc)) {
+          if (!wwait(bar(kBarFull + vn % kSlots), (vn / kSlots) & 1)) {
             ok = false;
             break;
           }
@@ -349,22 +359,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool k_ready = false;
           for (int i = 0; i < 2; ++i) {
             if (fl & (kUse0 << i)) {
-              if (!mbar_wait(bar(kBarP + i), p_ph[i], wc)) {
+              if (!wwait(bar(kBarP + i), p_ph[i])) {
                 ok = false;
                 break;
               }
               p_ph[i] ^= 1;
               tc_fence_after();
               const uint64_t bv = sdesc_advance(d_v, slot_off(vn));
+              if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < kT / 16; ++kk)
-                mma_ts(tmem + col_o(i), tmem + col_s(i) + kk * 8, sdesc_advance(bv, kk * 2048),
-                       kIdescPV, acc[i] | (kk > 0));
+                for (int kk = 0; kk < kT / 16; ++kk)
+                  mma_ts(tmem + col_o(i), tmem + col_s(i) + kk * 8, sdesc_advance(bv, kk * 2048),
+                         kIdescPV, acc[i] | (kk > 0));
+              }
               acc[i] = 1;
             }
             if (have_next && (nfl & (kUse0 << i))) {
               if (!k_ready) {
-                if (!mbar_wait(bar(kBarFull + nkn % kSlots), (nkn / kSlots) & 1, wc)) {
+                if (!wwait(bar(kBarFull + nkn % kSlots), (nkn / kSlots) & 1)) {
                   ok = false;
                   break;
                 }
@@ -373,21 +385,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               const uint64_t a0 = sdesc_advance(d_q, i * kTileBytes);
               const uint64_t b0 = sdesc_advance(d_k, slot_off(nkn));
+              if (leader) {
 #pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                mma_ss(tmem + col_s(i), sdesc_advance(a0, off), sdesc_advance(b0, off), kIdescQK,
-                       kk > 0);
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                  const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                  mma_ss(tmem + col_s(i), sdesc_advance(a0, off), sdesc_advance(b0, off),
+                         kIdescQK, kk > 0);
+                }
+                mma_commit(bar(kBarS + i));
               }
-              mma_commit(bar(kBarS + i));
             }
           }
           if (!ok) break;
-          mma_commit(bar(kBarEmpty + vn % kSlots));
-          if (have_next) mma_commit(bar(kBarEmpty + nkn % kSlots));
+          if (leader) {
+            mma_commit(bar(kBarEmpty + vn % kSlots));
+            if (have_next) mma_commit(bar(kBarEmpty + nkn % kSlots));
+          }
           if (args.tiles_rt != nullptr) {
             if (step != census_step) {
-              atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
+              if (leader) atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
               census = 0;
               census_step = step;
             }
@@ -400,15 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           step = nstep;
         }
         if (!ok) break;
-        if (args.tiles_rt != nullptr && census)
-          atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
-        mma_commit(bar(kBarO + 0));
-        mma_commit(bar(kBarO + 1));
-        mma_commit(bar(kBarQEmpty));
+        if (leader) {
+          if (args.tiles_rt != nullptr && census)
+            atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
+          mma_commit(bar(kBarO + 0));
+          mma_commit(bar(kBarO + 1));
+          mma_commit(bar(kBarQEmpty));
+        }
       }
       if (!ok) {
         // Let every MMA already issued retire before TMEM is released.
-        mma_commit(bar(kBarDrain));
+        if (leader) mma_commit(bar(kBarDrain));
         mbar_drain(bar(kBarDrain), 0);
       }
     }
