@@ -44,7 +44,9 @@
 // the elementwise warps have read it, dP alternates between two buffers.
 //
 // Both kernels: CTA = 384 threads; warp 0 TMA, warp 1 TMEM owner + MMA
-// issuer, warps 4-7 and 8-11 the elementwise work on columns [0,64) and
+// issuer (the whole warp runs the issue loop, so its values stay
+// warp-uniform, and one elected lane issues), warps 4-7 and 8-11 the
+// elementwise work on columns [0,64) and
 // [64,128) of each tile (one thread per TMEM lane), and the epilogue.  Each
 // half writes its packed bf16 result over the first 32 of the 64 columns it
 // read itself ([0,32) and [64,96)), so the halves never wait for each other;
@@ -401,7 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the control flow (its values stay warp-uniform);
+    // one elected lane issues the MMAs and commits.
+    {
+      const bool leader = elect_one();
+      // A wait that the whole warp agrees on, so its control flow stays uniform.
+      auto wwait = [&](uint32_t bar_addr, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
+      };
       uint32_t qi = 0, p_ph = 0, ds_ph = 0;
       bool ok = true;
       // Operand descriptors, computed once and advanced by byte offsets.
@@ -410,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t d_q_mn = sdesc_sw128(sQ, kBoxBytes, 1024);
       const uint64_t d_do_mn = sdesc_sw128(sDO, kBoxBytes, 1024);
       auto issue_s = [&](int st) {
+        if (!leader) return;
         const uint64_t b0 = sdesc_advance(d_q, st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -419,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarS));
       };
       auto issue_dp = [&](int st) {
+        if (!leader) return;
         const uint64_t b0 = sdesc_advance(d_do, st * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -431,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
         const Item it = decode(sh, idx);
-        if (!mbar_wait(bar(kBarKVFull), k & 1, wc)) {
+        if (!wwait(bar(kBarKVFull), k & 1)) {
           ok = false;
           break;
         }
@@ -442,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool have = seq.next(qrow, qnat);
         if (have) {
           const int st = qi & 1;
-          if (!mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc)) {
+          if (!wwait(bar(kBarQFull + st), (qi >> 1) & 1)) {
             ok = false;
             break;
           }
@@ -457,17 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool nhave = seq.next(nqrow, nqnat);
           const int nst = (qi + 1) & 1;
           // dV += P^T dO
-          if (!mbar_wait(bar(kBarP), p_ph, wc)) {
+          if (!wwait(bar(kBarP), p_ph)) {
             ok = false;
             break;
           }
           p_ph ^= 1;
-          if (first && !mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+          if (first && !wwait(bar(kBarAccFree), (k & 1) ^ 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          {
+          if (leader) {
             const uint64_t b0 = sdesc_advance(d_do_mn, st * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S for the next tile (the S^T columns are free once dV has read P^T;
           // MMAs execute in issue order).
           if (nhave) {
-            if (!mbar_wait(bar(kBarQFull + nst), ((qi + 1) >> 1) & 1, wc)) {
+            if (!wwait(bar(kBarQFull + nst), ((qi + 1) >> 1) & 1)) {
               ok = false;
               break;
             }
@@ -485,20 +496,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_s(nst);
           }
           // dK += dS^T Q
-          if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
+          if (!wwait(bar(kBarDS), ds_ph)) {
             ok = false;
             break;
           }
           ds_ph ^= 1;
           tc_fence_after();
-          {
+          if (leader) {
             const uint64_t b0 = sdesc_advance(d_q_mn, st * kTileBytes);
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
               mma_ts(tmem + kColDK, tmem + kColDP + a_col(kk), sdesc_advance(b0, kk * 2048),
                      kIdescKM, (!first || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(kBarQEmpty + st));
+          if (leader) mma_commit(bar(kBarQEmpty + st));
           // dP for the next tile (the dP^T columns are free once dK has read dS^T).
           if (nhave) issue_dp(nst);
           first = false;
@@ -510,16 +521,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           // No query tile at all (cannot happen for well-formed windows: every
           // key sees its own query): the epilogue writes zeros once the
           // previous one has been read out.
-          if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+          if (!wwait(bar(kBarAccFree), (k & 1) ^ 1)) {
             ok = false;
             break;
           }
         }
-        mma_commit(bar(kBarAcc));
-        mma_commit(bar(kBarKVEmpty));
+        if (leader) {
+          mma_commit(bar(kBarAcc));
+          mma_commit(bar(kBarKVEmpty));
+        }
       }
       if (!ok) {
-        mma_commit(bar(kBarDrain));
+        if (leader) mma_commit(bar(kBarDrain));
         mbar_drain(bar(kBarDrain), 0);
       }
     }
@@ -862,15 +875,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the control flow (its values stay warp-uniform);
+    // one elected lane issues the MMAs and commits.
+    {
+      const bool leader = elect_one();
+      // A wait that the whole warp agrees on, so its control flow stays uniform.
+      auto wwait = [&](uint32_t bar_addr, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
+      };
       // kj counts the K/V tiles this CTA has consumed.
       uint32_t kj = 0, sf_ph = 0, ds_ph = 0;
       bool ok = true;
       auto wait_k = [&](uint32_t j) {
-        return mbar_wait(bar(kBarKFull + j % kKSlots), (j / kKSlots) & 1, wc);
+        return wwait(bar(kBarKFull + j % kKSlots), (j / kKSlots) & 1);
       };
       auto wait_v = [&](uint32_t j) {
-        return mbar_wait(bar(kBarVFull + j % kVSlots), (j / kVSlots) & 1, wc);
+        return wwait(bar(kBarVFull + j % kVSlots), (j / kVSlots) & 1);
       };
       // Operand descriptors, computed once and advanced by byte offsets.
       const uint64_t d_q = sdesc_sw128(sQ, 16, 1024), d_do = sdesc_sw128(sDO, 16, 1024);
@@ -879,6 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto koff = [](uint32_t j) { return (j % kKSlots) * (uint32_t)kTileBytes; };
       auto voff = [](uint32_t j) { return (kKSlots + j % kVSlots) * (uint32_t)kTileBytes; };
       auto issue_s = [&](uint32_t j) {
+        if (!leader) return;
         const uint64_t b0 = sdesc_advance(d_ring, koff(j));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -888,6 +909,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarS));
       };
       auto issue_dp = [&](uint32_t j, int buf) {
+        if (!leader) return;
         const uint64_t b0 = sdesc_advance(d_ring, voff(j));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -902,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
         const Item it = decode(sh, idx);
-        if (!mbar_wait(bar(kBarQFull), k & 1, wc)) {
+        if (!wwait(bar(kBarQFull), k & 1)) {
           ok = false;
           break;
         }
@@ -935,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             // S is released as soon as the elementwise warps have read it.
-            if (!mbar_wait(bar(kBarSFree), sf_ph, wc)) {
+            if (!wwait(bar(kBarSFree), sf_ph)) {
               ok = false;
               break;
             }
@@ -952,24 +974,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             issue_dp(kj + 1, (kj + 1) & 1);
           }
           // dQ += dS K
-          if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
+          if (!wwait(bar(kBarDS), ds_ph)) {
             ok = false;
             break;
           }
           ds_ph ^= 1;
-          if (first && !mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+          if (first && !wwait(bar(kBarAccFree), (k & 1) ^ 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          {
+          if (leader) {
             const uint64_t b0 = sdesc_advance(d_ring_mn, koff(kj));
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
               mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
                      sdesc_advance(b0, kk * 2048), kIdescKM, (!first || kk > 0) ? 1u : 0u);
           }
-          mma_commit(bar(kBarKEmpty + kj % kKSlots));  // K is free after dQ
+          if (leader) mma_commit(bar(kBarKEmpty + kj % kKSlots));  // K is free after dQ
           first = false;
           ++kj;
           have = nhave;
@@ -979,24 +1001,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           // No K/V tile at all (cannot happen for well-formed windows: every
           // query sees its own key): the epilogue writes zeros; it still
           // waits for the previous epilogue.
-          if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+          if (!wwait(bar(kBarAccFree), (k & 1) ^ 1)) {
             ok = false;
             break;
           }
         } else {
           // The item's last S was read but not overwritten: take its release
           // so that the next item's first S waits on a fresh phase.
-          if (!mbar_wait(bar(kBarSFree), sf_ph, wc)) {
+          if (!wwait(bar(kBarSFree), sf_ph)) {
             ok = false;
             break;
           }
           sf_ph ^= 1;
         }
-        mma_commit(bar(kBarAcc));
-        mma_commit(bar(kBarQEmpty));
+        if (leader) {
+          mma_commit(bar(kBarAcc));
+          mma_commit(bar(kBarQEmpty));
+        }
       }
       if (!ok) {
-        mma_commit(bar(kBarDrain));
+        if (leader) mma_commit(bar(kBarDrain));
         mbar_drain(bar(kBarDrain), 0);
       }
     }
