@@ -17,7 +17,8 @@
 // final normalisation uses the same stale maximum.
 //
 // CTA = 384 threads:
-//   warp 0      TMA producer: Q pair once per item, K and V tiles into a
+//   warp 0      TMA producer (the warp runs the loop, one elected lane
+//               issues): Q pair once per item, K and V tiles into a
 //               ring of five 32 KB slots (K(j), V(j), K(j+1), ... take
 //               consecutive slots; a slot is freed as soon as the MMAs that
 //               read it retire, so loads run up to two tiles ahead).
@@ -239,27 +240,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+    // The whole warp runs the loop; one elected lane issues the copies.
+    {
+      const bool leader = elect_one();
+      auto wwait = [&](uint32_t bar_addr, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
+      };
+      if (leader) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
       uint32_t seq = 0, q_armed = 0, armed[kSlots] = {0};
       bool ok = true;
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
         const Item it = decode_item(sh, idx);
-        if (!mbar_wait(bar(kBarQEmpty), (k & 1) ^ 1, wc)) {
+        if (!wwait(bar(kBarQEmpty), (k & 1) ^ 1)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
         ++q_armed;
         const int row0 = it.b * sh.S + it.qrow;
-        for (int tq = 0; tq < 2; ++tq)
-          for (int half = 0; half < 2; ++half)
-            tma_load_3d(sQ + tq * kTileBytes + half * kBoxBytes, &tm_q, bar(kBarQFull), half * 64,
-                        it.h, row0 + tq * kT);
+        if (leader) {
+          mbar_arrive_expect_tx(bar(kBarQFull), 2 * kTileBytes);
+          for (int tq = 0; tq < 2; ++tq)
+            for (int half = 0; half < 2; ++half)
+              tma_load_3d(sQ + tq * kTileBytes + half * kBoxBytes, &tm_q, bar(kBarQFull),
+                          half * 64, it.h, row0 + tq * kT);
+        }
         KvSeq kseq;
         kseq.init(sh, args.t_begin, args.t_end, it);
         int kvrow, fl, step, knat;
@@ -268,15 +278,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int which = 0; which < 2; ++which) {  // K(j), then V(j)
             const uint32_t n = seq++;
             const int sl = n % kSlots;
-            if (!mbar_wait(bar(kBarEmpty + sl), ((n / kSlots) & 1) ^ 1, wc)) {
+            if (!wwait(bar(kBarEmpty + sl), ((n / kSlots) & 1) ^ 1)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(bar(kBarFull + sl), kTileBytes);
             ++armed[sl];
-            for (int half = 0; half < 2; ++half)
-              tma_load_3d(slot(n) + half * kBoxBytes, which == 0 ? &tm_k : &tm_v,
-                          bar(kBarFull + sl), half * 64, it.g, krow);
+            if (leader) {
+              mbar_arrive_expect_tx(bar(kBarFull + sl), kTileBytes);
+              for (int half = 0; half < 2; ++half)
+                tma_load_3d(slot(n) + half * kBoxBytes, which == 0 ? &tm_k : &tm_v,
+                            bar(kBarFull + sl), half * 64, it.g, krow);
+            }
           }
         }
       }
