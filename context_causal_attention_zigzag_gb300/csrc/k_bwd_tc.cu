@@ -1391,22 +1391,40 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
+    // The whole warp runs the control flow (its values stay warp-uniform);
+    // one elected lane issues the MMAs and commits.
+    {
+      const bool leader = elect_one();
+      // A wait that the whole warp agrees on, so its control flow stays uniform.
+      auto wwait = [&](uint32_t bar_addr, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar_addr, parity, wc));
+      };
       uint32_t qi = 0, p_ph = 0, ds_ph = 0;
       bool ok = true;
+      // Operand descriptors, computed once and advanced by byte offsets.
+      const uint64_t d_k = sdesc_sw128(sK, 16, 1024), d_v = sdesc_sw128(sV, 16, 1024);
+      const uint64_t d_q = sdesc_sw128(sQ, 16, 1024), d_do = sdesc_sw128(sDO, 16, 1024);
+      const uint64_t d_q_mn = sdesc_sw128(sQ, kBoxBytes, 1024);
+      const uint64_t d_do_mn = sdesc_sw128(sDO, kBoxBytes, 1024);
+      const uint64_t d_k_mn = sdesc_sw128(sK, kBoxBytes, 1024);
+      const uint64_t d_ds_mn = sdesc_sw128(sDS, kBoxBytes, 1024);
       auto issue_s = [&](int st) {
+        if (!leader) return;
+        const uint64_t b0 = sdesc_advance(d_q, st * kTileBytes);
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColX, sdesc_sw128(sK + off, 16, 1024),
-                 sdesc_sw128(sQ + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+          mma_ss(tmem + kColX, sdesc_advance(d_k, off), sdesc_advance(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarS));
       };
       auto issue_dp = [&](int st) {
+        if (!leader) return;
+        const uint64_t b0 = sdesc_advance(d_do, st * kTileBytes);
+#pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColY, sdesc_sw128(sV + off, 16, 1024),
-                 sdesc_sw128(sDO + st * kTileBytes + off, 16, 1024), kIdescKK, kk > 0);
+          mma_ss(tmem + kColY, sdesc_advance(d_v, off), sdesc_advance(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarDP));
       };
@@ -1414,7 +1432,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
         const Item it = decode(sh, idx);
-        if (!mbar_wait(bar(kBarKVFull), k & 1, wc)) {
+        if (!wwait(bar(kBarKVFull), k & 1)) {
           ok = false;
           break;
         }
@@ -1425,14 +1443,14 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         bool have = seq.next(qrow, qnat);
         if (have) {
           const int st = qi & 1;
-          if (!mbar_wait(bar(kBarQFull + st), (qi >> 1) & 1, wc)) {
+          if (!wwait(bar(kBarQFull + st), (qi >> 1) & 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_s(st);
           // Y holds the previous tile's dQ^T until the drain has read it.
-          if (!mbar_wait(bar(kBarYFree), (qi & 1) ^ 1, wc)) {
+          if (!wwait(bar(kBarYFree), (qi & 1) ^ 1)) {
             ok = false;
             break;
           }
@@ -1446,48 +1464,55 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           const bool nhave = seq.next(nqrow, nqnat);
           const int nst = (qi + 1) & 1;
           // dV += P^T dO
-          if (!mbar_wait(bar(kBarP), p_ph, wc)) {
+          if (!wwait(bar(kBarP), p_ph)) {
             ok = false;
             break;
           }
           p_ph ^= 1;
-          if (first && !mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+          if (first && !wwait(bar(kBarAccFree), (k & 1) ^ 1)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDV, tmem + kColX + a_col(kk),
-                   sdesc_sw128(sDO + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                   (!first || kk > 0) ? 1u : 0u);
+          if (leader) {
+            const uint64_t b0 = sdesc_advance(d_do_mn, st * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ts(tmem + kColDV, tmem + kColX + a_col(kk), sdesc_advance(b0, kk * 2048),
+                     kIdescKM, (!first || kk > 0) ? 1u : 0u);
+          }
           // dK += dS^T Q (A = the bf16 dS^T the elementwise warps packed into
           // Y), then dQ^T = K^T dS^T (both operands in shared memory) over Y:
           // MMAs run in order, so dK has read Y before dQ^T writes it.
-          if (!mbar_wait(bar(kBarDS), ds_ph, wc)) {
+          if (!wwait(bar(kBarDS), ds_ph)) {
             ok = false;
             break;
           }
           ds_ph ^= 1;
           tc_fence_after();
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ts(tmem + kColDK, tmem + kColY + a_col(kk),
-                   sdesc_sw128(sQ + st * kTileBytes + kk * 2048, kBoxBytes, 1024), kIdescKM,
-                   (!first || kk > 0) ? 1u : 0u);
-          mma_commit(bar(kBarQEmpty + st));  // Q, dO of this tile read for the last time
-          for (int kk = 0; kk < kT / 16; ++kk)
-            mma_ss(tmem + kColY, sdesc_sw128(sK + kk * 2048, kBoxBytes, 1024),
-                   sdesc_sw128(sDS + kk * 2048, kBoxBytes, 1024), kIdescMM, kk > 0 ? 1u : 0u);
-          mma_commit(bar(kBarDQ));
+          if (leader) {
+            const uint64_t b0 = sdesc_advance(d_q_mn, st * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ts(tmem + kColDK, tmem + kColY + a_col(kk), sdesc_advance(b0, kk * 2048),
+                     kIdescKM, (!first || kk > 0) ? 1u : 0u);
+            mma_commit(bar(kBarQEmpty + st));  // Q, dO of this tile read for the last time
+#pragma unroll
+            for (int kk = 0; kk < kT / 16; ++kk)
+              mma_ss(tmem + kColY, sdesc_advance(d_k_mn, kk * 2048),
+                     sdesc_advance(d_ds_mn, kk * 2048), kIdescMM, kk > 0 ? 1u : 0u);
+            mma_commit(bar(kBarDQ));
+          }
           if (nhave) {
             // S of the next tile over X (dV has read P^T; MMAs run in order).
-            if (!mbar_wait(bar(kBarQFull + nst), ((qi + 1) >> 1) & 1, wc)) {
+            if (!wwait(bar(kBarQFull + nst), ((qi + 1) >> 1) & 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_s(nst);
             // dP of the next tile once the drain has read this tile's dQ^T.
-            if (!mbar_wait(bar(kBarYFree), ((qi + 1) & 1) ^ 1, wc)) {
+            if (!wwait(bar(kBarYFree), ((qi + 1) & 1) ^ 1)) {
               ok = false;
               break;
             }
@@ -1500,16 +1525,18 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         }
         if (!ok) break;
         if (first) {
-          if (!mbar_wait(bar(kBarAccFree), (k & 1) ^ 1, wc)) {
+          if (!wwait(bar(kBarAccFree), (k & 1) ^ 1)) {
             ok = false;
             break;
           }
         }
-        mma_commit(bar(kBarAcc));
-        mma_commit(bar(kBarKVEmpty));
+        if (leader) {
+          mma_commit(bar(kBarAcc));
+          mma_commit(bar(kBarKVEmpty));
+        }
       }
       if (!ok) {
-        mma_commit(bar(kBarDrain));
+        if (leader) mma_commit(bar(kBarDrain));
         mbar_drain(bar(kBarDrain), 0);
       }
     }
