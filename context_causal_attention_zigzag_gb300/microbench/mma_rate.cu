@@ -1,7 +1,10 @@
 // Microbenchmark: cycles per tcgen05.mma (kind::f16, bf16, cta_group::1) for
 // the SS and TS forms at M=128, N in {128, 256}, K=16, issued back to back by
 // one thread, optionally while eight other warps load / store TMEM the way the
-// attention kernels' softmax warps do.  Modes 4 and 5 issue N=128 MMAs that
+// attention kernels' softmax warps do.  Two issue styles: one thread
+// (`if (threadIdx.x == 0)`) building each operand descriptor per
+// instruction, or a whole warp running the loop with the descriptors built
+// once and one elected lane issuing (the style of the attention kernels).  Modes 4 and 5 issue N=128 MMAs that
 // alternate between two independent accumulators (two chains interleaved
 // instruction by instruction) instead of one accumulation chain.  One CTA of 384 threads per SM on every
 // SM; every wait is bounded.  It measures the per-instruction ceiling the
@@ -15,7 +18,7 @@
 #include "tc_ptx.cuh"
 using namespace cpattn::tc;
 
-__global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsigned long long* out, int* err, int noise) {
+__global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsigned long long* out, int* err, int noise, int wide) {
   extern __shared__ uint8_t raw_[];
   uint32_t raw = smem_u32(raw_);
   uint32_t base = (raw + 1023u) & ~1023u;
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsign
       tmem_wait_st();
     }
   }
-  if (threadIdx.x == 0) {
+  if (!wide && threadIdx.x == 0) {
     const int N = (mode == 1 || mode == 3) ? 256 : 128;
     const bool ts = mode == 2 || mode == 3 || mode == 5;
     const bool two = mode >= 4;
@@ -79,6 +82,33 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsign
     unsigned long long t1 = clock64();
     out[blockIdx.x] = ok ? (t1 - t0) : 0ull;
   }
+  if (wide && warp == 1) {
+    const bool leader = elect_one();
+    const int N = (mode == 1 || mode == 3) ? 256 : 128;
+    const bool ts = mode == 2 || mode == 3 || mode == 5;
+    const bool two = mode >= 4;
+    const uint32_t idesc = idesc_bf16(128, N, false, ts);
+    const uint64_t dA = sdesc_sw128(sA, 16, 1024), dB = sdesc_sw128(sB, 16, 1024);
+    const uint64_t dBmn = sdesc_sw128(sB, 16384, 1024);
+    unsigned long long t0 = clock64();
+    for (int r = 0; r < reps; ++r) {
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint32_t d = two ? 128u + 128u * (uint32_t)(kk & 1) : (ts ? 256u : 0u);
+          if (!ts)
+            mma_ss(tmem + d, sdesc_advance(dA, off), sdesc_advance(dB, off), idesc, 1);
+          else
+            mma_ts(tmem + d, tmem + 0 + kk * 8, sdesc_advance(dBmn, kk * 2048), idesc, 1);
+        }
+      }
+    }
+    if (leader) mma_commit(bar0);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0, 0, wc));
+    unsigned long long t1 = clock64();
+    if (leader) out[blockIdx.x] = ok ? (t1 - t0) : 0ull;
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -99,11 +129,12 @@ int main() {
   cudaFuncSetAttribute(rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   const char* names[] = {"SS N=128", "SS N=256", "TS N=128", "TS N=256",
                          "SS N=128 two chains", "TS N=128 two chains"};
+  for (int wide : {0, 1})
   for (int mode = 0; mode < 6; ++mode) {
     for (int noise : {0, 1}) {
       const int grid = sms;
       const int reps = 200;
-      rate_kernel<<<grid, 384, smem>>>(mode, reps, d, err, noise);
+      rate_kernel<<<grid, 384, smem>>>(mode, reps, d, err, noise, wide);
       cudaError_t e = cudaDeviceSynchronize();
       if (e != cudaSuccess) { printf("error %s\n", cudaGetErrorString(e)); return 1; }
       unsigned long long h[1024];
@@ -113,7 +144,8 @@ int main() {
       const int N = (mode == 1 || mode == 3) ? 256 : 128;
       double per = sum / grid / (reps * 8.0);
       double ideal = 128.0 * N * 16 * 2 / 8192.0;
-      printf("%s tmem-noise=%d: %.1f cycles per MMA (ideal at 8192 flop/clk/SM: %.1f) -> %.0f%%\n", names[mode], noise, per, ideal, 100 * ideal / per);
+      printf("%s %s tmem-noise=%d: %.1f cycles per MMA (ideal at 8192 flop/clk/SM: %.1f) -> %.0f%%\n",
+             wide ? "warp-issued" : "one-thread", names[mode], noise, per, ideal, 100 * ideal / per);
     }
   }
   int herr = 0;
