@@ -700,16 +700,18 @@ constexpr int kBarVFull = kBarKEmpty + kKSlots;   // [kVSlots]
 constexpr int kBarVEmpty = kBarVFull + kVSlots;   // [kVSlots]
 constexpr int kBarS = kBarVEmpty + kVSlots;
 constexpr int kBarSFree = kBarS + 1;
-constexpr int kBarDP = kBarSFree + 1;          // [2]
-constexpr int kBarDS = kBarDP + 2;
-constexpr int kBarAcc = kBarDS + 1;
+constexpr int kBarDP = kBarSFree + 1;
+constexpr int kBarDS = kBarDP + 1;
+constexpr int kBarQT = kBarDS + 1;             // Q and dO copied into TMEM
+constexpr int kBarAcc = kBarQT + 1;
 constexpr int kBarAccFree = kBarAcc + 1;
 constexpr int kBarDrain = kBarAccFree + 1;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-constexpr uint32_t kColS = 0, kColDQ = 384;
-__host__ __device__ constexpr uint32_t col_dp(int b) { return 128u + 128u * (uint32_t)b; }
+// TMEM: S, dP (dS packed over it), the dQ accumulator, and the item's Q and
+// dO tiles as bf16 pairs (the A operands of the S and dP products).
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColQT = 384, kColDOT = 448;
 
 struct Item {
   int b, h, g, knat;
@@ -757,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQFull), 1);
-    mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarQEmpty), 256);
     for (int i = 0; i < kKSlots; ++i) {
       mbar_init(bar(kBarKFull + i), 1);
       mbar_init(bar(kBarKEmpty + i), 1);
@@ -766,10 +768,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull + i), 1);
       mbar_init(bar(kBarVEmpty + i), 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(bar(kBarDP + i), 1);
+    mbar_init(bar(kBarDP), 1);
     mbar_init(bar(kBarS), 1);
     mbar_init(bar(kBarSFree), 256);
     mbar_init(bar(kBarDS), 256);
+    mbar_init(bar(kBarQT), 256);
     mbar_init(bar(kBarAcc), 1);
     mbar_init(bar(kBarAccFree), 256);
     mbar_init(bar(kBarDrain), 1);
@@ -893,38 +896,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         return wwait(bar(kBarVFull + j % kVSlots), (j / kVSlots) & 1);
       };
       // Operand descriptors, computed once and advanced by byte offsets.
-      const uint64_t d_q = sdesc_sw128(sQ, 16, 1024), d_do = sdesc_sw128(sDO, 16, 1024);
       const uint64_t d_ring = sdesc_sw128(sRing, 16, 1024);
       const uint64_t d_ring_mn = sdesc_sw128(sRing, kBoxBytes, 1024);
       auto koff = [](uint32_t j) { return (j % kKSlots) * (uint32_t)kTileBytes; };
       auto voff = [](uint32_t j) { return (kKSlots + j % kVSlots) * (uint32_t)kTileBytes; };
+      // S = Q K^T and dP = dO V^T take A (Q, dO) from TMEM: the TS form.
       auto issue_s = [&](uint32_t j) {
         if (!leader) return;
         const uint64_t b0 = sdesc_advance(d_ring, koff(j));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + kColS, sdesc_advance(d_q, off), sdesc_advance(b0, off), kIdescKK, kk > 0);
+          mma_ts(tmem + kColS, tmem + kColQT + kk * 8, sdesc_advance(b0, off), kIdescKK, kk > 0);
         }
         mma_commit(bar(kBarS));
       };
-      auto issue_dp = [&](uint32_t j, int buf) {
+      auto issue_dp = [&](uint32_t j) {
         if (!leader) return;
         const uint64_t b0 = sdesc_advance(d_ring, voff(j));
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          mma_ss(tmem + col_dp(buf), sdesc_advance(d_do, off), sdesc_advance(b0, off), kIdescKK,
+          mma_ts(tmem + kColDP, tmem + kColDOT + kk * 8, sdesc_advance(b0, off), kIdescKK,
                  kk > 0);
         }
-        mma_commit(bar(kBarDP + buf));
+        mma_commit(bar(kBarDP));
         mma_commit(bar(kBarVEmpty + j % kVSlots));  // V is read only by dP
       };
       for (int k = 0; ok; ++k) {
         const int idx = item_index(k, blockIdx.x, gridDim.x);
         if (idx >= n_items) break;
         const Item it = decode(sh, idx);
-        if (!wwait(bar(kBarQFull), k & 1)) {
+        // The elementwise warps have copied the item's Q and dO into TMEM.
+        if (!wwait(bar(kBarQT), k & 1)) {
           ok = false;
           break;
         }
@@ -945,7 +949,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          issue_dp(kj, kj & 1);
+          issue_dp(kj);
         }
         bool first = true;
         while (have) {
@@ -964,14 +968,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             sf_ph ^= 1;
             tc_fence_after();
             issue_s(kj + 1);
-            // dP into the other buffer: the dQ that read it two tiles ago was
-            // issued earlier, and MMAs execute in issue order.
-            if (!wait_v(kj + 1)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_dp(kj + 1, (kj + 1) & 1);
           }
           // dQ += dS K
           if (!wwait(bar(kBarDS), ds_ph)) {
@@ -988,10 +984,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t b0 = sdesc_advance(d_ring_mn, koff(kj));
 #pragma unroll
             for (int kk = 0; kk < kT / 16; ++kk)
-              mma_ts(tmem + kColDQ, tmem + col_dp(kj & 1) + a_col(kk),
-                     sdesc_advance(b0, kk * 2048), kIdescKM, (!first || kk > 0) ? 1u : 0u);
+              mma_ts(tmem + kColDQ, tmem + kColDP + a_col(kk), sdesc_advance(b0, kk * 2048),
+                     kIdescKM, (!first || kk > 0) ? 1u : 0u);
           }
           if (leader) mma_commit(bar(kBarKEmpty + kj % kKSlots));  // K is free after dQ
+          if (nhave) {
+            // dP of the next tile over the dS this dQ reads: MMAs execute in
+            // issue order, so dQ has read dS before dP overwrites it.
+            if (!wait_v(kj + 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_dp(kj + 1);
+          }
           first = false;
           ++kj;
           have = nhave;
@@ -1014,10 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sf_ph ^= 1;
         }
-        if (leader) {
-          mma_commit(bar(kBarAcc));
-          mma_commit(bar(kBarQEmpty));
-        }
+        if (leader) mma_commit(bar(kBarAcc));
       }
       if (!ok) {
         if (leader) mma_commit(bar(kBarDrain));
@@ -1031,7 +1034,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = wq * 32 + lane;    // query row of the tile (TMEM lane)
     const uint32_t tl = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = sh.scale_log2, scale = sh.scale;
-    uint32_t kj = 0, s_ph = 0, dp_ph[2] = {0, 0};
+    uint32_t s_ph = 0, dp_ph = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int idx = item_index(k, blockIdx.x, gridDim.x);
@@ -1040,6 +1043,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t li = ((int64_t)it.b * sh.H + it.h) * sh.S + it.q.row + row;
       const float nlse2 = -args.lse[li] * kLog2e;
       const float dlt = args.delta[li];  // scale * Delta
+      // Copy the item's Q (first half) or dO (second half) tile into TMEM as
+      // bf16 pairs, this thread's row: the 128-byte-swizzled TMA boxes hold
+      // 16-byte chunk c of row r at chunk c ^ (r % 8).  The previous item's
+      // products have all retired (its epilogue waited for them), and the
+      // shared-memory copy is released to the next item's loads at once.
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarQFull), k & 1, wc))) {
+        ok = false;
+        break;
+      }
+      {
+        const uint8_t* src = smem + (half ? kOffDO : kOffQ) + row * 128;
+        uint32_t w[64];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              src + (c >> 3) * kBoxBytes + (((c & 7) ^ (row & 7)) << 4));
+          w[4 * c] = v.x;
+          w[4 * c + 1] = v.y;
+          w[4 * c + 2] = v.z;
+          w[4 * c + 3] = v.w;
+        }
+        const uint32_t dst = tl + (half ? kColDOT : kColQT);
+        tmem_st32(dst, w);
+        tmem_st32(dst + 32, w + 32);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(kBarQT));
+        mbar_arrive(bar(kBarQEmpty));
+      }
       KSeq seq;
       seq.init(sh, it.q, it.knat);
       // Keys that this thread's query sees (natural positions).
@@ -1048,7 +1080,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kvrow, knat;
       int ntiles = 0;
       while (seq.next(kvrow, knat)) {
-        const int buf = kj & 1;
         const int j_lo = w_lo - knat, j_hi = w_hi - knat;  // visible key columns
         const bool cut = j_lo > 0 || j_hi < kT - 1;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarS), s_ph, wc))) {
@@ -1072,14 +1103,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 64; ++j)
             if (64 * half + j < j_lo || 64 * half + j > j_hi) p[j] = 0.f;
         }
-        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP + buf), dp_ph[buf], wc))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(kBarDP), dp_ph, wc))) {
           ok = false;
           break;
         }
-        dp_ph[buf] ^= 1;
+        dp_ph ^= 1;
         tc_fence_after();
-        tmem_ld32(tl + col_dp(buf) + 64 * half, r);
-        tmem_ld32(tl + col_dp(buf) + 64 * half + 32, r + 32);
+        tmem_ld32(tl + kColDP + 64 * half, r);
+        tmem_ld32(tl + kColDP + 64 * half + 32, r + 32);
         tmem_wait_ld_regs(r);
         reg_fence32(r + 32);
         uint32_t ds[32];
@@ -1087,11 +1118,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 32; ++j)
           ds[j] = pack_bf16(p[2 * j] * fmaf(__uint_as_float(r[2 * j]), scale, -dlt),
                             p[2 * j + 1] * fmaf(__uint_as_float(r[2 * j + 1]), scale, -dlt));
-        tmem_st32(tl + col_dp(buf) + 64 * half, ds);
+        tmem_st32(tl + kColDP + 64 * half, ds);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar(kBarDS));
-        ++kj;
         ++ntiles;
       }
       if (!ok) break;
