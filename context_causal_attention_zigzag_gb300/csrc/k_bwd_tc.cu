@@ -32,16 +32,20 @@
 // core's float32 accumulation drifts toward zero over very long chains).
 //
 // dq kernel (query-major).  Work item: one 128-row query tile of one head.
-// Q, dO stay in shared memory, LSE / Delta in registers (TMEM lane = query
-// row); the K/V tiles it sees (earliest first, see KSeq) stream past through
-// two rings of 32 KB slots, three for K and two for V (V(j)'s slot is free
-// once dP(j) has read it, K(j)'s only once dQ(j) has, a tile later; a ring
-// each keeps the copy of V(j+2) from waiting for dQ(j)):
-//   S = Q K^T -> TMEM [0,128)     dP = dO V^T -> TMEM [128,256) / [256,384)
+// Q, dO arrive in shared memory and the elementwise warps copy them into TMEM
+// as bf16 pairs at the start of the item (releasing the shared-memory copy to
+// the next item's loads), so that S and dP are TS-form products, which issue
+// faster than the SS form; LSE / Delta sit in registers (TMEM lane = query
+// row).  The K/V tiles the item sees (earliest first, see KSeq) stream past
+// through two rings of 32 KB slots, three for K and two for V (V(j)'s slot is
+// free once dP(j) has read it, K(j)'s only once dQ(j) has, a tile later):
+//   S = Q K^T -> TMEM [0,128)      dP = dO V^T -> TMEM [128,256)
 //   dS = scale * exp2(S*scale*log2e - LSE*log2e) (dP - Delta) -> bf16 over dP
-//   dQ += dS K  (TS, K read MN-major) -> TMEM [384,512)
-// MMA order per K/V tile j: S(j+1), dP(j+1), dQ(j); S is released as soon as
-// the elementwise warps have read it, dP alternates between two buffers.
+//   dQ += dS K  (TS, K read MN-major) -> TMEM [256,384)
+//   Q -> TMEM [384,448), dO -> [448,512)
+// MMA order per K/V tile j: S(j+1), dQ(j), dP(j+1); S is released as soon as
+// the elementwise warps have read it; dP(j+1) follows dQ(j), which reads the
+// dS packed over dP(j), and MMAs execute in issue order.
 //
 // Both kernels: CTA = 384 threads; warp 0 TMA, warp 1 TMEM owner + MMA
 // issuer (the whole warp runs the issue loop, so its values stay
