@@ -1,7 +1,9 @@
 // Microbenchmark: cycles per tcgen05.mma (kind::f16, bf16, fp32 accumulate)
 // issued by a CTA pair with cta_group::2, M = 256 (128 rows per SM), K = 16,
-// N in {128, 256}, SS and TS forms, back to back from one thread of the even
-// CTA of each 2-CTA cluster.  Each SM's tensor core does the same per-SM work
+// N in {128, 256}, SS and TS forms, back to back from the even CTA of each
+// 2-CTA cluster: either one thread building the operand descriptors per
+// instruction, or a whole warp with the descriptors built once and one
+// elected lane issuing (the attention kernels' style).  Each SM's tensor core does the same per-SM work
 // as a cta_group::1 M=128 instruction of the same N, so the per-SM cycles are
 // directly comparable with mma_rate.cu.  One CTA per SM (the shared-memory
 // request keeps two CTAs off one SM); every mbarrier wait is bounded.  It
@@ -75,7 +77,7 @@ __device__ __forceinline__ void commit2_both(uint32_t bar) {
 }  // namespace
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
-    pair_rate_kernel(int mode, int reps, unsigned long long* out, int* err) {
+    pair_rate_kernel(int mode, int reps, unsigned long long* out, int* err, int wide) {
   extern __shared__ uint8_t raw_[];
   uint32_t raw = smem_u32(raw_);
   uint32_t base = (raw + 1023u) & ~1023u;
@@ -108,7 +110,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
   const int N = mode == 1 ? 256 : 128;
   const bool ts = mode == 2;
   unsigned long long t0 = 0, t1 = 0;
-  if (crank == 0 && threadIdx.x == 0) {
+  if (wide && crank == 0 && warp == 1) {
+    const bool leader = elect_one();
+    const uint32_t idesc = idesc_bf16(256, N, false, ts);
+    const uint64_t dA = sdesc_sw128(sA, 16, 1024), dB = sdesc_sw128(sB, 16, 1024);
+    const uint64_t dBmn = sdesc_sw128(sB, 16384, 1024);
+    t0 = clock64();
+    for (int r = 0; r < reps; ++r) {
+      if (leader) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          if (!ts)
+            mma2_ss(tmem, sdesc_advance(dA, off), sdesc_advance(dB, off), idesc);
+          else
+            mma2_ts(tmem, tmem + 128 + kk * 8, sdesc_advance(dBmn, kk * 2048), idesc);
+        }
+      }
+    }
+    if (leader) commit2_both(bar0);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar0, 0, wc));
+    t1 = clock64();
+    if (leader) out[blockIdx.x / 2] = ok ? (t1 - t0) : 0ull;
+  }
+  if (!wide && crank == 0 && threadIdx.x == 0) {
     const uint32_t idesc = idesc_bf16(256, N, false, ts);
     t0 = clock64();
     for (int r = 0; r < reps; ++r) {
@@ -125,7 +150,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
   if (threadIdx.x == 0) {
     const bool ok = mbar_wait(bar0, 0, wc);
     t1 = clock64();
-    if (crank == 0) out[blockIdx.x / 2] = ok ? (t1 - t0) : 0ull;
+    if (crank == 0 && !wide) out[blockIdx.x / 2] = ok ? (t1 - t0) : 0ull;
   }
   tc_fence_before();
   __syncthreads();
@@ -147,10 +172,11 @@ int main() {
   cudaMemset(err, 0, 4);
   cudaFuncSetAttribute(pair_rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemReq);
   const char* names[] = {"pair SS M=256 N=128", "pair SS M=256 N=256", "pair TS M=256 N=128"};
+  for (int wide : {0, 1})
   for (int mode = 0; mode < 3; ++mode) {
     const int reps = 200;
     cudaMemset(d, 0, sizeof(unsigned long long) * grid);
-    pair_rate_kernel<<<grid, 128, kSmemReq>>>(mode, reps, d, err);
+    pair_rate_kernel<<<grid, 128, kSmemReq>>>(mode, reps, d, err, wide);
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
       printf("error %s\n", cudaGetErrorString(e));
@@ -169,8 +195,9 @@ int main() {
     const double per = n ? sum / n / (reps * 8.0) : 0.0;
     // Per SM: 128 rows x N x 16 x 2 flops per instruction.
     const double ideal = 128.0 * N * 16 * 2 / 8192.0;
-    printf("%s: %.1f cycles per MMA (per-SM ideal at 8192 flop/clk/SM: %.1f) -> %.0f%% (%d pairs)\n",
-           names[mode], per, ideal, per > 0 ? 100 * ideal / per : 0.0, n);
+    printf("%s %s: %.1f cycles per MMA (per-SM ideal at 8192 flop/clk/SM: %.1f) -> %.0f%% (%d pairs)\n",
+           wide ? "warp-issued" : "one-thread", names[mode], per, ideal,
+           per > 0 ? 100 * ideal / per : 0.0, n);
   }
   int herr = 0;
   cudaMemcpy(&herr, err, 4, cudaMemcpyDeviceToHost);
