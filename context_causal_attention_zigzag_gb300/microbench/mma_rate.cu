@@ -1,5 +1,5 @@
 // Microbenchmark: cycles per tcgen05.mma (kind::f16, bf16, cta_group::1) for
-// the SS and TS forms at M=128, N in {128, 256}, K=16, issued back to back by
+// the SS and TS forms at M=128, N in {64, 128, 256}, K=16, issued back to back by
 // one thread, optionally while eight other warps load / store TMEM the way the
 // attention kernels' softmax warps do.  Two issue styles: one thread
 // (`if (threadIdx.x == 0)`) building each operand descriptor per
@@ -60,9 +60,9 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsign
     }
   }
   if (!wide && threadIdx.x == 0) {
-    const int N = (mode == 1 || mode == 3) ? 256 : 128;
-    const bool ts = mode == 2 || mode == 3 || mode == 5;
-    const bool two = mode >= 4;
+    const int N = (mode == 1 || mode == 3) ? 256 : (mode >= 6 ? 64 : 128);
+    const bool ts = mode == 2 || mode == 3 || mode == 5 || mode == 7;
+    const bool two = mode == 4 || mode == 5;
     const uint32_t idesc = idesc_bf16(128, N, false, ts);
     unsigned long long t0 = clock64();
     for (int r = 0; r < reps; ++r) {
@@ -84,9 +84,9 @@ __global__ void __launch_bounds__(384, 1) rate_kernel(int mode, int reps, unsign
   }
   if (wide && warp == 1) {
     const bool leader = elect_one();
-    const int N = (mode == 1 || mode == 3) ? 256 : 128;
-    const bool ts = mode == 2 || mode == 3 || mode == 5;
-    const bool two = mode >= 4;
+    const int N = (mode == 1 || mode == 3) ? 256 : (mode >= 6 ? 64 : 128);
+    const bool ts = mode == 2 || mode == 3 || mode == 5 || mode == 7;
+    const bool two = mode == 4 || mode == 5;
     const uint32_t idesc = idesc_bf16(128, N, false, ts);
     const uint64_t dA = sdesc_sw128(sA, 16, 1024), dB = sdesc_sw128(sB, 16, 1024);
     const uint64_t dBmn = sdesc_sw128(sB, 16384, 1024);
@@ -128,9 +128,9 @@ int main() {
   int smem = 98304 + 1024 + 128;
   cudaFuncSetAttribute(rate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   const char* names[] = {"SS N=128", "SS N=256", "TS N=128", "TS N=256",
-                         "SS N=128 two chains", "TS N=128 two chains"};
+                         "SS N=128 two chains", "TS N=128 two chains", "SS N=64", "TS N=64"};
   for (int wide : {0, 1})
-  for (int mode = 0; mode < 6; ++mode) {
+  for (int mode = 0; mode < 8; ++mode) {
     for (int noise : {0, 1}) {
       const int grid = sms;
       const int reps = 200;
@@ -141,7 +141,7 @@ int main() {
       cudaMemcpy(h, d, sizeof(unsigned long long) * grid, cudaMemcpyDeviceToHost);
       double mx = 0, sum = 0;
       for (int i = 0; i < grid; ++i) { sum += h[i]; if (h[i] > mx) mx = h[i]; }
-      const int N = (mode == 1 || mode == 3) ? 256 : 128;
+      const int N = (mode == 1 || mode == 3) ? 256 : (mode >= 6 ? 64 : 128);
       double per = sum / grid / (reps * 8.0);
       double ideal = 128.0 * N * 16 * 2 / 8192.0;
       printf("%s %s tmem-noise=%d: %.1f cycles per MMA (ideal at 8192 flop/clk/SM: %.1f) -> %.0f%%\n",
