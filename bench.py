@@ -70,11 +70,11 @@ ALL_WORKLOADS = {**inputs.WORKLOADS, **inputs.DOC_WORKLOADS}
 REDUCED_CASE_TRAFFIC = {
     "workload": "S=16384 reduction (B1 H32 Hkv8 D128 cp4 zigzag causal, float32 gradients)",
     "bytes": {
-        "tc_fwd_kernel": 203.8e6 + 97.4e6,
+        "tc_fwd_kernel": 276.1e6 + 96.0e6,
         "bwd_prep_kernel": 268.5e6 + 4.3e6,
-        "dkdv_kernel": 394.3e6 + 487.8e6,
-        "dq_kernel": 341.0e6 + 227.0e6,
-        "grad_reduce_kernel": 536.9e6 + 117.1e6,
+        "dkdv_kernel": 484.7e6 + 485.9e6,
+        "dq_kernel": 507.4e6 + 222.5e6,
+        "grad_reduce_kernel": 536.9e6 + 117.2e6,
         "dkdvq_kernel": 889.1e6 + 907.3e6,
     },
 }

@@ -77,6 +77,49 @@ __host__ __device__ inline int chunk_of_tile(int m, unsigned long long tile_magi
   return (int)(((unsigned long long)(unsigned)m * tile_magic) >> 32);
 }
 
+// Order of the persistent kernels' work items.  An item is (group, rank,
+// sub): `group` the head (or kv head) whose tiles the item reads, `rank` its
+// place in cost order (rank 0 visits the most tiles), `sub` one of `inner`
+// items of equal cost (the query heads of a kv head).  The ranks are cut into
+// cost bands, the band outermost; inside a band the items go group by group,
+// so that the CTAs in flight share one group's tiles through L2.  CTA c takes
+// items c, 2*grid - 1 - c, 2*grid + c, ... (item_index), which over a list
+// sorted by cost gives every CTA about the same work; the bands make the
+// list sorted to within one band's cost spread.  The band count is the
+// power of two at or above 16 * grid / (items per group), at least 2 and at
+// most the number of ranks: two bands where a group holds many waves of items
+// (long sequences, whose CTAs in flight then stay within one or two groups,
+// so that L2 holds their tiles), more as a group's items shrink against the
+// grid (short sequences).  With max_groups > 0 the count is also held to the
+// largest power of two that keeps about max_groups groups in flight (a wave
+// meets grid * bands / per_group groups), for kernels whose every item
+// streams its group's tiles in full.
+__host__ __device__ inline int cost_band_count(int per_group, int nrank, int grid,
+                                               int max_groups) {
+  const int want = (16 * grid + per_group - 1) / per_group;
+  int nb = 2;
+  while (nb < want) nb *= 2;
+  if (max_groups > 0)
+    while (nb > 2 && (long long)grid * nb > (long long)max_groups * per_group) nb /= 2;
+  return nb < nrank ? nb : nrank;
+}
+
+__host__ __device__ inline void banded_item(int idx, int ngroups, int nrank, int inner, int grid,
+                                            int max_groups, int& group, int& rank, int& sub) {
+  const int nb = cost_band_count(nrank * inner, nrank, grid, max_groups);
+  const int bsz = (nrank + nb - 1) / nb;  // ranks per band; the last band may hold fewer
+  const int band_items = ngroups * bsz * inner;
+  const int band = idx / band_items;
+  int rem = idx - band * band_items;
+  const int left = nrank - band * bsz;
+  const int bw = bsz < left ? bsz : left;
+  group = rem / (bw * inner);
+  rem -= group * bw * inner;
+  const int r = rem / inner;
+  rank = band * bsz + r;
+  sub = rem - r * inner;
+}
+
 // Keys visible to the query at natural position i: the natural range [lo, hi].
 // Both ends are non-decreasing in i, so the keys that some query of a run of
 // consecutive positions i0..i1 sees form the single range [lo(i0), hi(i1)].

@@ -257,14 +257,18 @@ struct Item {
   TilePos kv;
 };
 
-// (batch, query head) outermost, then the K/V tiles earliest first (an
-// early tile is seen by the most query tiles).  Consecutive items -- the CTAs
-// running at the same time -- share one head, so the Q / dO tiles they all
-// stream stay in L2 (one head's Q and dO: 2 * S * D * 2 bytes).
+// Groups are the (batch, query head) pairs, ranks the K/V tiles earliest
+// first (an early tile is seen by the most query tiles), in cost bands
+// (banded_item).  Consecutive items -- the CTAs running at the same time --
+// share one head, so the Q / dO tiles they all stream stay in L2 (one head's
+// Q and dO: 2 * S * D * 2 bytes).  Every item streams its head's Q and dO
+// from its own tile to the end, so the bands keep at most about
+// kMaxHeadsInFlight heads in flight.
+constexpr int kMaxHeadsInFlight = 4;
 __device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
   const int ntiles = sh.S / kT;
-  const int bh = idx / ntiles;
-  const int knat = idx - bh * ntiles;
+  int bh, knat, sub;
+  banded_item(idx, sh.B * sh.H, ntiles, 1, gridDim.x, kMaxHeadsInFlight, bh, knat, sub);
   Item it;
   it.b = bh / sh.H;
   it.h = bh - it.b * sh.H;
@@ -722,20 +726,20 @@ struct Item {
   TilePos q;
 };
 
-// (batch, kv head) outermost, then the query tiles latest first (a late tile
-// sees the most K/V tiles), then the query heads of the kv head: the CTAs in
-// flight share one kv head's K/V through L2.
+// Groups are the (batch, kv head) pairs, ranks the query tiles latest first
+// (a late tile sees the most K/V tiles), each rank the query heads of the kv
+// head, in cost bands (banded_item): the CTAs in flight share one kv head's
+// K/V through L2.
 __device__ __forceinline__ Item decode(const RingShape& sh, int idx) {
   const int grp = sh.H / sh.Hkv;
   const int ntiles = sh.S / kT;
-  const int per_group = ntiles * grp;
-  const int gi = idx / per_group;
-  const int rem = idx - gi * per_group;
-  const int knat = ntiles - 1 - rem / grp;
+  int gi, rank, sub;
+  banded_item(idx, sh.B * sh.Hkv, ntiles, grp, gridDim.x, 0, gi, rank, sub);
+  const int knat = ntiles - 1 - rank;
   Item it;
   it.b = gi / sh.Hkv;
   it.g = gi - it.b * sh.Hkv;
-  it.h = it.g * grp + (rem - (rem / grp) * grp);
+  it.h = it.g * grp + sub;
   it.knat = knat;
   it.q = tile_pos(sh, knat);
   return it;

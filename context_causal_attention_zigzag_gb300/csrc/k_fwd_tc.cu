@@ -91,22 +91,21 @@ struct Item {
   int b, h, g, r, qc, a, qrow;  // qc: natural chunk, a: natural tile of query tile 0
 };
 
-// Work items: (batch, kv head) outermost, then query pairs in order of
-// decreasing cost (natural query position), then the query heads of the kv
-// head.  The CTAs running at the same time therefore share one kv head's K/V
-// (2 * S * D * 2 bytes) through L2, and every round of the snake deal holds
-// items of similar cost.
+// Work items: groups are the (batch, kv head) pairs, ranks the query pairs
+// in order of decreasing cost (natural query position), each rank the query
+// heads of the kv head, in cost bands (banded_item).  The CTAs running at the
+// same time therefore share one kv head's K/V (2 * S * D * 2 bytes) through
+// L2, and every round of the snake deal holds items of similar cost.
 __device__ __forceinline__ Item decode_item(const RingShape& sh, int idx) {
   const int grp = sh.H / sh.Hkv;
   const int npair = sh.S / (2 * kT);
-  const int per_group = npair * grp;
-  const int gi = idx / per_group;
-  const int rem = idx - gi * per_group;
-  const int pr = npair - 1 - rem / grp;
+  int gi, rank, sub;
+  banded_item(idx, sh.B * sh.Hkv, npair, grp, gridDim.x, 0, gi, rank, sub);
+  const int pr = npair - 1 - rank;
   Item it;
   it.b = gi / sh.Hkv;
   it.g = gi - it.b * sh.Hkv;
-  it.h = it.g * grp + (rem - (rem / grp) * grp);
+  it.h = it.g * grp + sub;
   const int nat0 = pr * 2 * kT;
   it.qc = nat0 / sh.c;
   const int off = nat0 - it.qc * sh.c;
