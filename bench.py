@@ -75,7 +75,7 @@ REDUCED_CASE_TRAFFIC = {
         "dkdv_kernel": 484.7e6 + 485.9e6,
         "dq_kernel": 507.4e6 + 222.5e6,
         "grad_reduce_kernel": 536.9e6 + 117.2e6,
-        "dkdvq_kernel": 889.1e6 + 907.3e6,
+        "dkdvq_kernel": 1098.1e6 + 1038.3e6,
     },
 }
 
