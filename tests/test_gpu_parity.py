@@ -112,6 +112,8 @@ FWD_CASES = [
     (2, 4, 1, 1536, 128, 3, cpa.ZIGZAG, True, torch.bfloat16),     # cp 3, GQA 4:1
     (1, 2, 2, 1024, 128, 1, cpa.ZIGZAG, True, torch.bfloat16),     # cp 1
     (1, 2, 2, 640, 128, 2, cpa.ZIGZAG, True, torch.bfloat16),      # chunk 160 (CUDA cores)
+    (1, 8, 1, 5888, 128, 1, cpa.CONTIGUOUS, True, torch.bfloat16), # 23 query pairs in cost
+                                                                   # bands of 2, the last of 1
 ]
 
 
@@ -277,6 +279,8 @@ BWD_CASES = [
     (2, 2, 2, 512, 64, 2, cpa.ZIGZAG, True, torch.bfloat16),       # D 64 (CUDA cores)
     (1, 2, 1, 768, 128, 3, cpa.ZIGZAG, True, torch.bfloat16),      # chunk 128, cp 3
     (2, 8, 4, 4096, 128, 4, cpa.ZIGZAG, True, torch.bfloat16),     # > 1 work item per CTA
+    (1, 4, 1, 5888, 128, 1, cpa.CONTIGUOUS, False, torch.bfloat16),  # dQ: 46 tiles in cost
+                                                                     # bands of 3, the last of 1
 ]
 
 
