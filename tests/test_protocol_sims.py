@@ -9,7 +9,7 @@ import random
 
 import pytest
 
-from protocol_sims import dq_kernel, onepass_kernel
+from protocol_sims import dkdv_kernel, dq_kernel, onepass_kernel
 
 CLEAN_SCHEDULES = 400
 MUTANT_SCHEDULES = 2000
@@ -22,7 +22,9 @@ def draws(n, seed, choices):
 
 MODELS = {
     # tiles per work item: K/V tiles of a query tile (dQ kernel), query tiles
-    # of a K/V tile (one-pass kernel); 0 covers an item with nothing visible.
+    # of a K/V tile (dK / dV and one-pass kernels); 0 covers an item with
+    # nothing visible.
+    "dkdv_kernel": (dkdv_kernel, [0, 1, 1, 2, 3, 5, 7]),
     "dq_kernel": (dq_kernel, [0, 1, 1, 2, 3, 5, 7]),
     "onepass_kernel": (onepass_kernel, [0, 1, 1, 2, 3, 5]),
 }
