@@ -357,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (leader) mma_commit(bar(kBarEmpty + kn % kSlots));
+        // acc[i]: query tile i has had a P V product in this item.
         uint32_t acc[2] = {0, 0};
         while (true) {
           int nkvrow, nfl = 0, nstep = 0, nknat;
@@ -430,8 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (leader) {
           if (args.tiles_rt != nullptr && census)
             atomicAdd(&args.tiles_rt[it.r * sh.cp + census_step], census);
-          mma_commit(bar(kBarO + 0));
-          mma_commit(bar(kBarO + 1));
+          // O(i) is released only to a softmax warpgroup that waits for it:
+          // the one whose query tile saw at least one K/V tile of the item.
+          if (acc[0]) mma_commit(bar(kBarO + 0));
+          if (acc[1]) mma_commit(bar(kBarO + 1));
           mma_commit(bar(kBarQEmpty));
         }
       }

@@ -9,7 +9,7 @@ import random
 
 import pytest
 
-from protocol_sims import dkdv_kernel, dq_kernel, onepass_kernel
+from protocol_sims import dkdv_kernel, dq_kernel, fwd_kernel, onepass_kernel
 
 CLEAN_SCHEDULES = 400
 MUTANT_SCHEDULES = 2000
@@ -25,6 +25,10 @@ MODELS = {
     # of a K/V tile (dK / dV and one-pass kernels); 0 covers an item with
     # nothing visible.
     "dkdv_kernel": (dkdv_kernel, [0, 1, 1, 2, 3, 5, 7]),
+    # forward: the use masks of an item's K/V tiles (1: query tile 0, 2: query
+    # tile 1, 3: both), including items where one query tile sees nothing.
+    "fwd_kernel": (fwd_kernel, [[], [3], [3, 3], [3, 3, 3, 2], [1], [2, 3], [3, 1],
+                                [3, 3, 3, 3, 3], [2], [1, 1], [3, 3, 3, 3, 3, 3, 3]]),
     "dq_kernel": (dq_kernel, [0, 1, 1, 2, 3, 5, 7]),
     "onepass_kernel": (onepass_kernel, [0, 1, 1, 2, 3, 5]),
 }
