@@ -555,9 +555,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t obase = (((int64_t)it.b * sh.S + qrow) * sh.H + it.h) * kD;
       const int64_t lidx = ((int64_t)it.b * sh.H + it.h) * sh.S + qrow;
       if (nt == 0) {
-        // Step partial with no visible key: (0, -inf).
-        float4* op = reinterpret_cast<float4*>(static_cast<float*>(args.out) + obase);
-        for (int j = 0; j < kD / 4; ++j) op[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // No visible key (a step partial): (0, -inf), in the output's format.
+        if (args.step_mode) {
+          float4* op = reinterpret_cast<float4*>(static_cast<float*>(args.out) + obase);
+          for (int j = 0; j < kD / 4; ++j) op[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + obase);
+          for (int j = 0; j < kD / 8; ++j) op[j] = make_uint4(0u, 0u, 0u, 0u);
+        }
         args.lse[lidx] = -INFINITY;
         continue;
       }
